@@ -1,0 +1,258 @@
+"""Pins for the oracle's quantizers against closed forms, exact library
+statistics, brute force and the error bounds the formats imply.
+
+Sources:
+  "Hierarchical Token Routing and Sub-2-Bit Non-Linear KV Compression",
+  Paradigm 2 (outlier isolation; 4-centroid codebook via k-means, the
+  compress_kv_head listing's linspace start and argmin assignment).
+  "The Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache
+  Quantization", section 2 (S = (max - min) / (2^b - 1); E2M1).
+  "Hierarchical Token Gating and Tiered KV-Cache Paging", section 2 (FP8 tier).
+"""
+import itertools
+import statistics
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+R_K, R_V = 0, 1
+
+
+# ------------------------------------------------------------------ outliers
+def test_outlier_rule_matches_exact_statistics():
+    """Decisions equal those from Python's exact-rational mean/stdev, except
+    where |x - mu| is within 1e-9 relative of the threshold."""
+    rng = np.random.default_rng(0)
+    checked = 0
+    for trial in range(300):
+        n = [32, 64, 128][trial % 3]
+        x = rng.standard_normal(n)
+        x[rng.integers(0, n, 3)] *= rng.uniform(2, 12)
+        mask, k = oracle.outlier_mask(x, 3.0, cap=n)
+        xs = [Fraction(float(v)) for v in x]
+        mu = statistics.mean(xs)
+        sd = statistics.stdev([float(v) for v in x])
+        for i, v in enumerate(x):
+            dev = abs(float(Fraction(float(v)) - mu))
+            if abs(dev - 3 * sd) <= 1e-9 * max(dev, 1e-300):
+                continue
+            assert mask[i] == (dev > 3 * sd)
+            checked += 1
+    assert checked > 20000
+
+
+@pytest.mark.parametrize("n", [32, 64, 128])
+def test_outlier_count_bound(n):
+    """k outliers need k*9*s^2 < (n-1)*s^2: at most ceil((n-1)/9)-1 of them."""
+    assert oracle.kmax(n) == {32: 3, 64: 6, 128: 14}[n]
+    rng = np.random.default_rng(n)
+    worst = 0
+    for _ in range(500):
+        x = rng.standard_normal(n)
+        m = rng.integers(1, n // 4)
+        x[:m] += rng.choice([-1, 1], m) * rng.uniform(5, 50, m)
+        _, k = oracle.outlier_mask(x, 3.0, cap=n)   # uncapped
+        worst = max(worst, k)
+        assert k <= oracle.kmax(n)
+    # closed form: k equal spikes over n-k zeros are all outliers iff
+    # (1 - k/n)^2 > 9 k (n-k) / (n (n-1)), i.e. (n-k)(n-1) > 9 k n
+    for k in range(1, n // 2):
+        x = np.zeros(n)
+        x[:k] = 1.0
+        mask, got = oracle.outlier_mask(x, 3.0, cap=n)
+        expect = (n - k) * (n - 1) > 9 * k * n
+        assert got == (k if expect else 0) and (mask[:k].all() == expect)
+
+
+def test_outlier_special_cases():
+    assert oracle.outlier_mask(np.full(128, 2.5))[1] == 0          # s == 0
+    assert oracle.outlier_mask(np.arange(128.0))[1] == 0           # uniform ramp: max dev 1.7 s
+    x = np.zeros(128)
+    x[5] = 100.0
+    m, k = oracle.outlier_mask(x)
+    assert k == 1 and m[5]
+
+
+# ------------------------------------------------------------------ Lloyd-Max
+def _brute_optimum(v):
+    """Minimum squared distortion over all partitions of sorted values into at
+    most 4 contiguous cells (optimal 1-D quantizer cells are intervals)."""
+    s = np.sort(v)
+    n = len(s)
+    best = np.inf
+    for k in range(1, min(4, n) + 1):
+        for cuts in itertools.combinations(range(1, n), k - 1):
+            edges = (0,) + cuts + (n,)
+            d = sum(((s[a:b] - s[a:b].mean()) ** 2).sum() for a, b in zip(edges[:-1], edges[1:]))
+            best = min(best, d)
+    return best
+
+
+def _distortion(v, c):
+    return sum(min((x - cj) ** 2 for cj in c) for x in v)
+
+
+def test_lloyd_never_beats_brute_force_and_hits_it_on_clusters():
+    rng = np.random.default_rng(1)
+    for trial in range(120):
+        n = int(rng.integers(1, 13))
+        v = rng.standard_normal(n) * rng.uniform(0.1, 5)
+        c, _, _, _ = oracle.lloyd4(v)
+        assert _distortion(v, c) >= _brute_optimum(v) - 1e-9
+    # evenly spaced, well separated clusters: the linspace start puts one
+    # centroid in each cluster's cell, so Lloyd reaches the global optimum
+    for trial in range(40):
+        centers = rng.uniform(-20, 20) + rng.uniform(5, 20) * np.arange(4)
+        v = np.concatenate([cc + rng.uniform(-0.5, 0.5, 4) for cc in centers])
+        rng.shuffle(v)
+        c, _, _, _ = oracle.lloyd4(v)
+        assert abs(_distortion(v, c) - _brute_optimum(v)) < 1e-9
+
+
+def test_lloyd_fixed_point_and_codes():
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        n = int(rng.integers(1, 17))
+        v = rng.standard_normal(n)
+        c, c16, codes, passes = oracle.lloyd4(v, iters=64)
+        # converged: each non-empty cell's centroid is the mean of its members
+        assign = np.array([int(np.argmin(np.abs(x - c))) for x in v])
+        for j in range(4):
+            if (assign == j).any():
+                assert abs(c[j] - v[assign == j].mean()) <= 1e-12 * max(1, abs(c[j]))
+        # final codes: nearest fp16 centroid, first index on ties (numpy argmin's rule)
+        cf = np.array([oracle.fp16_decode(h) for h in c16])
+        assert (codes == np.array([int(np.argmin(np.abs(x - cf))) for x in v])).all()
+        assert all(h == np.array(cj, np.float64).astype(np.float16).view(np.uint16) for h, cj in zip(c16, c))
+
+
+def test_lloyd_special_cases():
+    c, c16, codes, _ = oracle.lloyd4(np.full(16, 1.25))
+    assert (c == 1.25).all() and (codes == 0).all()
+    c, c16, codes, _ = oracle.lloyd4(np.array([]))
+    assert (c16 == 0).all()
+    # linspace start (as the listing) on 4 equally spaced points is already optimal
+    c, _, codes, passes = oracle.lloyd4(np.array([0.0, 1.0, 2.0, 3.0]))
+    assert list(c) == [0, 1, 2, 3] and list(codes) == [0, 1, 2, 3] and passes == 2
+
+
+# ------------------------------------------------------------------ per-format error bounds
+def _ulp16(x):
+    return float(np.spacing(np.float16(abs(x)))) if np.isfinite(np.float16(abs(x))) else np.inf
+
+
+def test_int4_group_bounds():
+    """Non-outliers: |x - xh| <= S/2 + |m - mn| + fp32 rounding; outliers exact fp16."""
+    rng = np.random.default_rng(3)
+    D = 64
+    for trial in range(60):
+        x = rng.standard_normal(D).astype(np.float32) * rng.uniform(0.01, 10)
+        x[rng.integers(0, D, 2)] *= 10
+        blk = np.zeros(oracle.block_stride(oracle.BLK_INT4, D), np.uint8)
+        t = int(rng.integers(0, 16))
+        oracle.quantize_token(oracle.BLK_INT4, D, x, t, blk, role=trial % 2)
+        xh = oracle.dequantize_block(oracle.BLK_INT4, D, blk, role=trial % 2)[t]
+        for g in range(D // 32):
+            seg = x[32 * g:32 * g + 32].astype(np.float64)
+            mask, _ = oracle.outlier_mask(seg, 3.0)
+            assert mask.sum() <= 3
+            norm = seg[~mask]
+            S = float(np.float16((norm.max() - norm.min()) / 15))
+            m = float(np.float16(norm.min()))
+            for i in range(32):
+                c = 32 * g + i
+                if mask[i]:
+                    assert xh[c] == np.float32(np.float16(seg[i]))
+                else:
+                    bound = S / 2 + abs(m - norm.min()) + 2 * _ulp16(S) * 15 + 1e-6 * abs(seg[i])
+                    assert abs(xh[c] - seg[i]) <= bound + 1e-7
+
+
+def test_e2m1_block_bounds():
+    rng = np.random.default_rng(4)
+    D = 128
+    for trial in range(40):
+        x = (rng.standard_t(4, D) / np.sqrt(2)).astype(np.float32) * rng.uniform(0.001, 100)
+        blk = np.zeros(oracle.block_stride(oracle.BLK_E2M1, D), np.uint8)
+        oracle.quantize_token(oracle.BLK_E2M1, D, x, 7, blk, role=trial % 2)
+        xh = oracle.dequantize_block(oracle.BLK_E2M1, D, blk, role=trial % 2)[7]
+        for s in range(D // 16):
+            seg = x[16 * s:16 * s + 16].astype(np.float64)
+            amax = np.abs(seg).max()
+            sc = oracle.e4m3_decode(oracle.e4m3_encode(float(np.float32(amax / 6))))
+            for i in range(16):
+                r = seg[i] / sc
+                # half the local grid spacing, plus the saturation loss when s rounded down
+                spacing = 0.5 if abs(r) < 2 else (1.0 if abs(r) < 4 else 2.0)
+                bound = sc * spacing / 2 + max(0.0, amax - 6 * sc) + 1e-6 * abs(seg[i])
+                assert abs(xh[16 * s + i] - seg[i]) <= bound
+
+
+def test_fp8_page_bounds():
+    rng = np.random.default_rng(5)
+    D = 128
+    for trial in range(10):
+        x = rng.standard_normal((16, D)).astype(np.float32) * rng.uniform(0.01, 50)
+        blk = oracle.quantize_page(oracle.BLK_FP8, D, x, role=trial % 2)
+        xh = oracle.dequantize_block(oracle.BLK_FP8, D, blk, role=trial % 2)
+        s = np.float32(np.abs(x).max() / np.float32(448))
+        rel = np.abs(xh - x) / np.maximum(np.abs(x), 2.0 ** -6 * s)
+        assert rel.max() <= 2.0 ** -4 + 1e-6           # 3 mantissa bits: half-ulp = 2^-4 relative
+
+
+def test_cb2_page_properties():
+    rng = np.random.default_rng(6)
+    D = 128
+    for trial in range(8):
+        x = rng.standard_normal((16, D)).astype(np.float32)
+        x[:, rng.choice(D, 4, replace=False)] *= 8
+        role = trial % 2
+        blk = oracle.quantize_page(oracle.BLK_CB2, D, x, role=role)
+        xh = oracle.dequantize_block(oracle.BLK_CB2, D, blk, role=role)
+        masks = np.array([oracle.outlier_mask(x[t].astype(np.float64))[0] for t in range(16)])
+        # outliers reproduced exactly as e4m3; counts stored per token
+        assert (blk[12 * D:12 * D + 16] == masks.sum(1)).all()
+        for t, c in zip(*np.nonzero(masks)):
+            assert xh[t, c] == oracle.e4m3_decode(oracle.e4m3_encode(float(x[t, c])))
+        # non-outliers: the stored value is the nearest of the channel's 4 fp16 centroids
+        for c in range(D):
+            vals = x[~masks[:, c], c].astype(np.float64)
+            cents, c16, _, _ = oracle.lloyd4(vals)
+            cf = np.array([oracle.fp16_decode(h) for h in c16])
+            for t in np.nonzero(~masks[:, c])[0]:
+                assert abs(float(xh[t, c]) - float(x[t, c])) <= np.abs(cf - float(x[t, c])).min()
+                assert xh[t, c] in cf
+
+
+def test_cb2_outlier_rate_near_page_claim():
+    """cb2_4k data (4 of 128 channels x8): about 2.2 outliers per token (1.7%),
+    consistent with the 'under 1.8%' volume the first page reports."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((4000, 128))
+    x[:, [3, 40, 77, 120]] *= 8
+    k = np.mean([oracle.outlier_mask(r)[1] for r in x])
+    assert 1.9 < k < 2.5 and k / 128 < 0.02
+
+
+# ------------------------------------------------------------------ layout
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("role", [R_K, R_V])
+def test_fragment_positions_are_a_bijection(D, role):
+    seen = set()
+    for t in range(16):
+        for c in range(D):
+            lane, s, k = oracle.frag_pos(role, t, c)
+            assert 0 <= lane < 32 and 0 <= k < 8 and s == c // 16
+            seen.add((lane, s, k))
+    assert len(seen) == 16 * D
+
+
+@pytest.mark.parametrize("fmt", [oracle.BLK_INT4, oracle.BLK_E2M1, oracle.BLK_CB2, oracle.BLK_FP8])
+def test_block_strides_aligned(fmt):
+    for D in (64, 128):
+        assert oracle.block_stride(fmt, D) % 128 == 0
+    assert oracle.block_stride(oracle.BLK_CB2, 128) == 2048
+    assert oracle.block_stride(oracle.BLK_E2M1, 128) == 1152
