@@ -1,0 +1,54 @@
+// kvq_internal.cuh -- argument blocks and launch entry points shared between the
+// library's translation units (not part of the public ABI).
+#pragma once
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+struct DecodeArgs {
+  const uint8_t* pool;
+  const uint8_t* tier_pool;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const float* staging;
+  const __nv_bfloat16* q;
+  float* part_o;    // [B][Hq][S][D]
+  float2* part_ml;  // [B][Hq][S] (m in log2 units, l)
+  uint32_t* status;
+  int B, Hkv, Hq, G, ppsm, num_pages, num_tier_pages;
+  int S, pps;       // splits, pages per split
+  int max_seq_len;
+  float scale_log2; // softmax_scale * log2(e)
+  int ent_prefetch; // CB2 outlier entries fetched with a block (multiple of 8, <= kEntSmem)
+};
+
+struct AppendArgs {
+  uint8_t* pool;
+  uint8_t* tier_pool;
+  const int32_t* page_table;
+  int32_t* seq_lens;
+  float* staging;
+  uint32_t* status;
+  const void* kv[2];
+  int in_dtype;
+  int t_new;
+  const int32_t* t_per_seq;
+  int B, Hkv, ppsm, num_pages, num_tier_pages, fmt, iters;
+  double sigma;
+};
+
+// Split decode + combine on `st`; out_dtype is KVQ_BF16 or KVQ_F32.
+cudaError_t decode_launch(const DecodeArgs& a, int fmt, int D, void* out, int out_dtype, cudaStream_t st);
+// Resident CTAs per SM of the split kernel for (format, head_dim, G); 0 on error.
+int decode_ctas_per_sm(int fmt, int D, int G);
+// Warps per CTA of the split decode kernel.
+constexpr int kWarpsPerCta = 4;
+// Entries of a CB2 side-list the decode kernel fetches with its block.
+constexpr int kEntPrefetchDefault = 48;
+// Quantize-on-append launches (see kvq_quantize.cu).
+cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
+// Dequantize tokens [t0, t1) of (seq, head, role) to fp32.
+cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int seq, int head, int role, int t0,
+                              int t1, float* out, cudaStream_t st);
+
+}  // namespace kvq

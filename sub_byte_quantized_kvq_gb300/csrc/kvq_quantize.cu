@@ -1,0 +1,412 @@
+// kvq_quantize.cu -- quantize-on-append into the paged cache (compiled with
+// --fmad=false: every fp64 statistic is evaluated in the order written, with no
+// fused multiply-add, so codes are bit-identical to the CPU reference).
+//
+// "The Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache
+// Quantization", section 2 ("Outlier Isolation and Block-wise Quantization"):
+// asymmetric INT4 per 32-group, S = (max - min) / (2^b - 1), and FP4 E2M1;
+// scales are computed as tokens are inserted.
+// "Hierarchical Token Routing and Sub-2-Bit Non-Linear KV Compression",
+// Paradigm 2: outliers beyond sigma standard deviations (mean / unbiased std
+// along head_dim) kept in FP8 E4M3; the rest mapped to a 4-centroid codebook
+// fitted by k-means (Lloyd-Max in one dimension) from a linspace start,
+// assignment by nearest centroid with the first index winning ties.
+// "Hierarchical Token Gating and Tiered KV-Cache Paging", section 2: FP8 pages
+// for the tier named by the page table.
+//
+// One append = up to three launches on the caller's stream:
+//   1. quantize: per-token formats write every new token into its block;
+//      page formats quantize each page the append completes (from fp32
+//      staging + the new tokens);
+//   2. (page formats) copy the new tokens of the final partial page into
+//      staging -- after 1, which may still be reading the old staging rows;
+//   3. advance seq_lens and raise status bits -- after 1 and 2, which read it.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+enum { kSeqOk = 0, kSeqNothing = 1, kSeqCapacity = 2, kSeqBadPage = 3 };
+
+// Decide, identically in every launch, whether sequence b's append proceeds.
+__device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) {
+  start = a.seq_lens[b];
+  n = a.t_per_seq ? a.t_per_seq[b] : a.t_new;
+  if (n <= 0) return kSeqNothing;
+  if (n > a.t_new || start < 0 || (long long)start + n > (long long)a.ppsm * kPage) return kSeqCapacity;
+  for (int pg = start / kPage; pg <= (start + n - 1) / kPage; ++pg) {
+    const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
+    const bool ok = (u >> 31) ? (a.fmt == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages)
+                              : phys < (uint32_t)a.num_pages;
+    if (!ok) return kSeqBadPage;
+  }
+  return kSeqOk;
+}
+
+__device__ __forceinline__ float load_in(const AppendArgs& a, int role, int b, int t, int h, int c, int D) {
+  const size_t i = (((size_t)b * a.t_new + t) * a.Hkv + h) * D + c;
+  if (a.in_dtype == KVQ_F32) return static_cast<const float*>(a.kv[role])[i];
+  if (a.in_dtype == KVQ_F16) return __half2float(static_cast<const __half*>(a.kv[role])[i]);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(a.kv[role])[i]);
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
+  return (uint8_t)(r & 0xFFu);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
+  uint32_t d;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(d) : "r"((uint32_t)v));
+  return __half2float(__ushort_as_half((unsigned short)(d & 0xFFFFu)));
+}
+__device__ __forceinline__ uint8_t f32_to_e2m1(float x) {
+  uint32_t r;
+  asm("{ .reg .b8 t; .reg .b16 w; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; mov.b16 w, {t, t}; cvt.u32.u16 %0, w; }"
+      : "=r"(r)
+      : "f"(0.f), "f"(x));
+  return (uint8_t)(r & 0xFu);
+}
+__device__ __forceinline__ uint16_t f64_to_f16_bits(double x) { return __half_as_ushort(__double2half(x)); }
+__device__ __forceinline__ double f16_bits_to_f64(uint16_t h) { return (double)__half2float(__ushort_as_half(h)); }
+
+// Outlier mask of one vector (fp64, ascending order): |x - mu| > sigma * s, at most kmax kept.
+__device__ int outlier_mask(const float* x, int n, int stride, double sigma, int kmax, uint8_t* mask, int mstride) {
+  double sum = 0.0;
+  for (int i = 0; i < n; ++i) sum += (double)x[i * stride];
+  const double mu = sum / (double)n;
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const double d = (double)x[i * stride] - mu;
+    ss += d * d;
+  }
+  const double thr = sigma * sqrt(ss / (double)(n - 1));
+  int k = 0;
+  for (int i = 0; i < n; ++i) {
+    int out = fabs((double)x[i * stride] - mu) > thr;
+    if (out && k >= kmax) out = 0;
+    mask[i * mstride] = (uint8_t)out;
+    k += out;
+  }
+  return k;
+}
+
+__device__ __forceinline__ int nearest4(double v, const double* c) {
+  int best = 0;
+  double bd = fabs(v - c[0]);
+  for (int j = 1; j < 4; ++j) {
+    const double d = fabs(v - c[j]);
+    if (d < bd) { bd = d; best = j; }
+  }
+  return best;
+}
+
+// Lloyd-Max 4-centroid fit of v[0..n) (n <= 16); fp16 centroids and codes.
+__device__ void lloyd4(const double* v, int n, int iters, uint16_t* c16, uint8_t* codes) {
+  double c[4] = {0.0, 0.0, 0.0, 0.0};
+  if (n > 0) {
+    double mn = v[0], mx = v[0];
+    for (int i = 1; i < n; ++i) { mn = v[i] < mn ? v[i] : mn; mx = v[i] > mx ? v[i] : mx; }
+    const double h = (mx - mn) / 3.0;
+    c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0 * h; c[3] = mx;
+    uint8_t a[16], prev[16];
+    bool have_prev = false;
+    for (int it = 0; it < iters; ++it) {
+      bool same = have_prev;
+      for (int i = 0; i < n; ++i) {
+        a[i] = (uint8_t)nearest4(v[i], c);
+        same = same && a[i] == prev[i];
+      }
+      if (same) break;
+      for (int j = 0; j < 4; ++j) {
+        double s = 0.0;
+        int cnt = 0;
+        for (int i = 0; i < n; ++i)
+          if (a[i] == j) { s += v[i]; ++cnt; }
+        if (cnt > 0) c[j] = s / (double)cnt;
+      }
+      for (int i = 0; i < n; ++i) prev[i] = a[i];
+      have_prev = true;
+    }
+  }
+  double cf[4];
+  for (int j = 0; j < 4; ++j) { c16[j] = f64_to_f16_bits(c[j]); cf[j] = f16_bits_to_f64(c16[j]); }
+  for (int i = 0; i < n; ++i) codes[i] = (uint8_t)nearest4(v[i], cf);
+}
+
+// Element (t, c) held by fragment (lane, step, slot) -- the inverse of frag_pos.
+__device__ __forceinline__ void frag_inverse(int role, int lane, int s, int k, int& t, int& c) {
+  if (role == 0) {
+    t = (lane >> 2) + 8 * ((k >> 1) & 1);
+    c = 16 * s + 2 * (lane & 3) + (k & 1) + 8 * (k >> 2);
+  } else {
+    c = 16 * s + (lane >> 2) + 8 * ((k >> 1) & 1);
+    t = 2 * (lane & 3) + (k & 1) + 8 * (k >> 2);
+  }
+}
+
+// ----------------------------------------------------------------------------- per-token formats
+// INT4 group-32 quantization of token slot t by one warp (lane g < D/32 owns group g).
+template <int D>
+__device__ void quantize_token_int4(const float* x, int t, uint8_t (*codes)[D], uint8_t* blk, double sigma, int lane) {
+  constexpr int NG = D / 32, CAP = int4_cap(D);
+  uint8_t mask[32];
+  int cnt = 0;
+  if (lane < NG) {
+    const float* xg = x + 32 * lane;
+    outlier_mask(xg, 32, 1, sigma, kmax_outliers(32), mask, 1);
+    bool have = false;
+    double mn = 0.0, mx = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      if (mask[i]) continue;
+      const double v = (double)xg[i];
+      if (!have || v < mn) mn = v;
+      if (!have || v > mx) mx = v;
+      have = true;
+    }
+    const uint16_t S16 = have ? f64_to_f16_bits((mx - mn) / 15.0) : 0;
+    const uint16_t m16 = have ? f64_to_f16_bits(mn) : 0;
+    const double S = f16_bits_to_f64(S16), m = f16_bits_to_f64(m16);
+    for (int i = 0; i < 32; ++i) {
+      uint8_t q = 0;
+      if (mask[i]) {
+        ++cnt;
+      } else if (S != 0.0) {
+        double r = rint(((double)xg[i] - m) / S);
+        r = r < 0.0 ? 0.0 : (r > 15.0 ? 15.0 : r);
+        q = (uint8_t)r;
+      }
+      codes[t][32 * lane + i] = q;
+    }
+    uint8_t* sz = blk + int4_sz_off(D) + 4 * (t * NG + lane);
+    *reinterpret_cast<uint16_t*>(sz) = S16;
+    *reinterpret_cast<uint16_t*>(sz + 2) = m16;
+  }
+  // entries of group g go after those of groups < g (ascending channel order)
+  int off = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, off, d);
+    if (lane >= d) off += y;
+  }
+  const int total = __shfl_sync(0xffffffffu, off, NG - 1);
+  off -= cnt;
+  uint8_t* chans = blk + int4_ch_off(D) + t * CAP;
+  uint16_t* vals = reinterpret_cast<uint16_t*>(blk + int4_val_off(D)) + t * CAP;
+  if (lane < NG) {
+    for (int i = 0; i < 32; ++i)
+      if (mask[i]) {
+        chans[off] = (uint8_t)(32 * lane + i);
+        vals[off] = __half_as_ushort(__float2half_rn(x[32 * lane + i]));
+        ++off;
+      }
+  }
+  for (int i = total + lane; i < CAP; i += 32) {
+    chans[i] = 0;
+    vals[i] = 0;
+  }
+  if (lane == 0) blk[int4_cnt_off(D) + t] = (uint8_t)total;
+}
+
+// E2M1 quantization of token slot t by one warp (lane s < D/16 owns 16 channels).
+template <int D>
+__device__ void quantize_token_e2m1(const float* x, int t, uint8_t (*codes)[D], uint8_t* blk, int lane) {
+  if (lane >= D / 16) return;
+  const float* xs = x + 16 * lane;
+  float amax = 0.f;
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+  const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+  const float sc = e4m3_to_f32(s8);
+  for (int i = 0; i < 16; ++i) codes[t][16 * lane + i] = sc != 0.f ? f32_to_e2m1(__fdiv_rn(xs[i], sc)) : 0;
+  blk[e2m1_sc_off(D) + 16 * lane + t] = s8;
+}
+
+template <int BF, int D>
+__global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
+  constexpr int kStride = block_stride(BF, D), NS = D / 16;
+  __shared__ __align__(16) uint8_t blk[kStride];
+  __shared__ uint8_t codes[16][D];
+  __shared__ float xs[16][D];
+  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, pg = start / kPage + j;
+  if (pg * kPage >= end) return;
+  const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
+  const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
+  uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
+
+  for (int i = tid; i < kStride / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(gblk)[i];
+  for (int i = tid; i < (hi - lo) * D; i += blockDim.x) {
+    const int tt = i / D, c = i - tt * D;
+    xs[(lo % kPage) + tt][c] = load_in(a, role, b, lo + tt - start, h, c, D);
+  }
+  __syncthreads();
+  for (int i = tid; i < 32 * NS * 8; i += blockDim.x) {
+    const int ln = i / (NS * 8), s = (i / 8) % NS, k = i % 8;
+    int t, c;
+    frag_inverse(role, ln, s, k, t, c);
+    codes[t][c] = (blk[4 * NS * ln + 4 * s + k / 2] >> (4 * (k & 1))) & 0xF;
+  }
+  __syncthreads();
+  for (int tt = warp; tt < hi - lo; tt += nwarps) {
+    const int t = (lo % kPage) + tt;
+    if (BF == kBlkInt4) quantize_token_int4<D>(xs[t], t, codes, blk, a.sigma, lane);
+    else quantize_token_e2m1<D>(xs[t], t, codes, blk, lane);
+  }
+  __syncthreads();
+  for (int i = tid; i < 32 * NS; i += blockDim.x) {
+    const int ln = i / NS, s = i % NS;
+    uint32_t word = 0;
+    for (int k = 0; k < 8; ++k) {
+      int t, c;
+      frag_inverse(role, ln, s, k, t, c);
+      word |= (uint32_t)codes[t][c] << (4 * k);
+    }
+    *reinterpret_cast<uint32_t*>(blk + 4 * NS * ln + 4 * s) = word;
+  }
+  __syncthreads();
+  for (int i = tid; i < kStride / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk)[i];
+}
+
+// ----------------------------------------------------------------------------- page formats
+template <int D>
+__global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
+  constexpr int NS = D / 16;
+  constexpr int kCb2 = block_stride(kBlkCb2, D), kFp8 = block_stride(kBlkFp8, D);
+  constexpr int kBlk = kCb2 > kFp8 ? kCb2 : kFp8;
+  __shared__ float xs[16][D];
+  __shared__ uint8_t mask[16][D];
+  __shared__ uint8_t codes[16][D];
+  __shared__ __align__(16) uint8_t blk[kBlk];
+  __shared__ int cnt[16];
+  __shared__ float red[4];
+  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, pg = start / kPage + j;
+  if (pg * kPage + kPage > end) return;  // only pages this append completes
+  const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
+  const bool tier = (u >> 31) != 0;
+  const int stride = tier ? kFp8 : kCb2;
+  uint8_t* gblk = (tier ? a.tier_pool : a.pool) + (((size_t)phys * a.Hkv + h) * 2 + role) * stride;
+  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
+
+  for (int i = tid; i < 16 * D; i += blockDim.x) {
+    const int t = i / D, c = i - t * D, pos = pg * kPage + t;
+    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
+  }
+  for (int i = tid; i < kBlk / 16; i += blockDim.x) reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  if (tier) {
+    float amax = 0.f;
+    for (int i = tid; i < 16 * D; i += blockDim.x) amax = fmaxf(amax, fabsf(xs[i / D][i % D]));
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    const float s = __fdiv_rn(amax, 448.0f);
+    for (int i = tid; i < 16 * D; i += blockDim.x) {
+      const int t = i / D, c = i - t * D;
+      const FragPos p = frag_pos(role, t, c);
+      blk[8 * NS * p.lane + 8 * p.step + p.slot] = s != 0.f ? f32_to_e4m3(__fdiv_rn(xs[t][c], s)) : 0;
+    }
+    if (tid == 0) *reinterpret_cast<float*>(blk + fp8_sc_off(D)) = s;
+  } else {
+    if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+    __syncthreads();
+    if (tid < D) {
+      const int c = tid;
+      double v[16];
+      uint8_t cc[16];
+      uint16_t c16[4];
+      int nv = 0;
+      for (int t = 0; t < 16; ++t)
+        if (!mask[t][c]) v[nv++] = (double)xs[t][c];
+      lloyd4(v, nv, a.iters, c16, cc);
+      nv = 0;
+      for (int t = 0; t < 16; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];
+      uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
+      for (int jj = 0; jj < 4; ++jj) {
+        cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
+        cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
+      }
+    }
+    if (tid < 16) {
+      int e = 0;
+      for (int t = 0; t < tid; ++t) e += cnt[t];
+      uint8_t* ent = blk + cb2_ent_off(D);
+      for (int c = 0; c < D; ++c)
+        if (mask[tid][c]) {
+          ent[2 * e] = (uint8_t)c;
+          ent[2 * e + 1] = f32_to_e4m3(xs[tid][c]);
+          ++e;
+        }
+      blk[cb2_cnt_off(D) + tid] = (uint8_t)cnt[tid];
+    }
+    __syncthreads();
+    for (int i = tid; i < 32 * NS; i += blockDim.x) {
+      const int ln = i / NS, s = i % NS;
+      uint32_t word = 0;
+      for (int k = 0; k < 8; ++k) {
+        int t, c;
+        frag_inverse(role, ln, s, k, t, c);
+        word |= (uint32_t)codes[t][c] << (4 * (k & 3) + 2 * (k >> 2));
+      }
+      *reinterpret_cast<uint16_t*>(blk + 2 * NS * ln + 2 * s) = (uint16_t)word;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < stride / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk)[i];
+}
+
+// New tokens of the final partial page -> fp32 staging (after the page kernel).
+__global__ void __launch_bounds__(256) append_stage_kernel(const AppendArgs a, int D) {
+  const int h = blockIdx.x >> 1, role = blockIdx.x & 1, b = blockIdx.y;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n;
+  if (end % kPage == 0) return;
+  const int lo = max(start, (end / kPage) * kPage);
+  float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
+  for (int i = threadIdx.x; i < (end - lo) * D; i += blockDim.x) {
+    const int tt = i / D, c = i - tt * D, pos = lo + tt;
+    stg[(pos % kPage) * D + c] = load_in(a, role, b, pos - start, h, c, D);
+  }
+}
+
+// Advance seq_lens and report skipped sequences (after every other launch read them).
+__global__ void append_finish_kernel(const AppendArgs a) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.B) return;
+  int start, n;
+  const int st = seq_append_state(a, b, start, n);
+  if (st == kSeqOk) a.seq_lens[b] = start + n;
+  else if (st == kSeqCapacity) atomicOr(a.status, KVQ_STATUS_CAPACITY);
+  else if (st == kSeqBadPage) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+}
+
+template <int D>
+static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
+  const int pages_max = (a.t_new + kPage - 1) / kPage + 1;
+  const dim3 grid(pages_max, a.Hkv * 2, a.B);
+  if (a.fmt == KVQ_FMT_INT4_G32) append_token_kernel<kBlkInt4, D><<<grid, 256, 0, st>>>(a);
+  else if (a.fmt == KVQ_FMT_FP4_E2M1_S16) append_token_kernel<kBlkE2m1, D><<<grid, 256, 0, st>>>(a);
+  else {
+    append_page_kernel<D><<<grid, 128, 0, st>>>(a);
+    append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
+  }
+  append_finish_kernel<<<(a.B + 127) / 128, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st) {
+  return D == 64 ? append_launch_d<64>(a, st) : append_launch_d<128>(a, st);
+}
+
+}  // namespace kvq

@@ -1,0 +1,196 @@
+"""Thin Python binding of the C ABI in include/kvq.h (argument marshalling only).
+
+Every step of the path runs in the CUDA library ``_build/libkvq.so``; torch
+supplies device memory and streams.  If the library is missing the calls raise
+``KVQError`` -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
+
+KVQ_FMT_INT4_G32, KVQ_FMT_FP4_E2M1_S16, KVQ_FMT_CB2_OUTLIER, KVQ_FMT_TIERED = 0, 1, 2, 3
+KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
+KVQ_TIER_BIT = 1 << 31
+KVQ_STATUS_BAD_PAGE, KVQ_STATUS_CAPACITY, KVQ_STATUS_SEQ_TOO_LONG, KVQ_STATUS_TIMEOUT = 1, 2, 4, 8
+KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY, KVQ_ERR_CUDA = range(6)
+
+_DTYPE = {torch.bfloat16: KVQ_BF16, torch.float16: KVQ_F16, torch.float32: KVQ_F32}
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = kvq_status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})" if what else msg)
+
+
+class kvq_config(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("pages_per_seq_max", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("num_tier_pages", ctypes.c_int32), ("format", ctypes.c_int32), ("lloyd_iters", ctypes.c_int32),
+                ("sigma", ctypes.c_double)]
+
+
+class kvq_cache(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("tier_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("staging", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
+           "kvq_decode_num_splits", "kvq_decode_attention", "kvq_dequantize", "kvq_status_string", "kvq_version")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvq.so (built by __graft_entry__.build() / sub_byte_quantized_kvq_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise KVQError(-1, f"CUDA library not built: {LIB_PATH} is missing")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            pcfg, pcache = ctypes.POINTER(kvq_config), ctypes.POINTER(kvq_cache)
+            sig = {
+                "kvq_block_bytes": (I, [pcfg, I, ctypes.POINTER(S)]),
+                "kvq_cache_bytes": (I, [pcfg, ctypes.POINTER(S), ctypes.POINTER(S), ctypes.POINTER(S)]),
+                "kvq_quantize_append": (I, [pcfg, pcache, P, P, I, I, P, P]),
+                "kvq_decode_workspace_bytes": (I, [pcfg, I, I, I, ctypes.POINTER(S)]),
+                "kvq_decode_num_splits": (I, [pcfg, I, I, ctypes.POINTER(I)]),
+                "kvq_decode_attention": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P, S, P]),
+                "kvq_dequantize": (I, [pcfg, pcache, I, I, I, I, I, P, P]),
+                "kvq_status_string": (ctypes.c_char_p, [I]),
+                "kvq_version": (ctypes.c_char_p, []),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype, f.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != KVQ_OK:
+        raise KVQError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def kvq_status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+def kvq_version() -> str:
+    return lib().kvq_version().decode()
+
+
+class QuantizedKVCache:
+    """Device buffers of one paged, quantized cache (allocated with torch)."""
+
+    def __init__(self, fmt: int, num_seqs: int, num_kv_heads: int, head_dim: int, pages_per_seq_max: int,
+                 num_pages: int, num_tier_pages: int = 0, sigma: float = 3.0, lloyd_iters: int = 16,
+                 page_table: torch.Tensor | None = None, device="cuda"):
+        self.cfg = kvq_config(num_seqs, num_kv_heads, head_dim, pages_per_seq_max, num_pages, num_tier_pages, fmt,
+                              lloyd_iters, sigma)
+        pb, tb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().kvq_cache_bytes(ctypes.byref(self.cfg), ctypes.byref(pb), ctypes.byref(tb), ctypes.byref(sb)),
+               "kvq_cache_bytes")
+        self.device = torch.device(device)
+        self.pool = torch.zeros(pb.value, dtype=torch.uint8, device=self.device)
+        self.tier_pool = torch.zeros(tb.value, dtype=torch.uint8, device=self.device) if tb.value else None
+        self.staging = torch.zeros(sb.value // 4, dtype=torch.float32, device=self.device) if sb.value else None
+        if page_table is None:
+            page_table = torch.arange(num_seqs * pages_per_seq_max, dtype=torch.int64).view(num_seqs, -1) % num_pages
+        self.page_table = torch.as_tensor(page_table).to(torch.int32).to(self.device).contiguous()
+        self.seq_lens = torch.zeros(num_seqs, dtype=torch.int32, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.c = kvq_cache(self.pool.data_ptr(), self.tier_pool.data_ptr() if self.tier_pool is not None else None,
+                           self.page_table.data_ptr(), self.seq_lens.data_ptr(),
+                           self.staging.data_ptr() if self.staging is not None else None, self.status.data_ptr())
+
+    @property
+    def head_dim(self) -> int:
+        return self.cfg.head_dim
+
+    def block_bytes(self, tier: int = 0) -> int:
+        return kvq_block_bytes(self.cfg, tier)
+
+    def status_word(self) -> int:
+        return int(self.status.item()) & 0xFFFFFFFF
+
+
+def kvq_block_bytes(cfg: kvq_config, tier: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kvq_block_bytes(ctypes.byref(cfg), tier, ctypes.byref(n)), "kvq_block_bytes")
+    return n.value
+
+
+def kvq_quantize_append(cache: QuantizedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                        t_per_seq: torch.Tensor | None = None, stream=None):
+    """k_new, v_new: [num_seqs, t_new, Hkv, D] bf16/f16/f32 on the cache's device."""
+    assert k_new.shape == v_new.shape and k_new.dtype == v_new.dtype and k_new.is_contiguous() and v_new.is_contiguous()
+    assert k_new.dim() == 4 and k_new.shape[0] == cache.cfg.num_seqs
+    if t_per_seq is not None:
+        t_per_seq = t_per_seq.to(torch.int32).contiguous()
+    _check(lib().kvq_quantize_append(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new),
+                                     _DTYPE[k_new.dtype], k_new.shape[1], _ptr(t_per_seq), _stream(stream)),
+           "kvq_quantize_append")
+
+
+def kvq_decode_num_splits(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int) -> int:
+    n = ctypes.c_int32()
+    _check(lib().kvq_decode_num_splits(ctypes.byref(cache.cfg), num_q_heads, max_seq_len, ctypes.byref(n)),
+           "kvq_decode_num_splits")
+    return n.value
+
+
+def kvq_decode_workspace_bytes(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int,
+                               num_splits: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kvq_decode_workspace_bytes(ctypes.byref(cache.cfg), num_q_heads, max_seq_len, num_splits,
+                                            ctypes.byref(n)), "kvq_decode_workspace_bytes")
+    return n.value
+
+
+def kvq_decode_attention(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale: float, max_seq_len: int,
+                         num_splits: int = 0, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q: [num_seqs, Hq, D] bf16 -> out [num_seqs, Hq, D] (bf16 or f32)."""
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if workspace is None:
+        nbytes = kvq_decode_workspace_bytes(cache, Hq, max_seq_len, num_splits)
+        workspace = torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    _check(lib().kvq_decode_attention(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(q), Hq,
+                                      float(softmax_scale), max_seq_len, num_splits, _ptr(out), _DTYPE[out.dtype],
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "kvq_decode_attention")
+    return out
+
+
+def kvq_dequantize(cache: QuantizedKVCache, seq: int, kv_head: int, which: int, tok_begin: int, tok_end: int,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Values tokens [tok_begin, tok_end) of (seq, kv_head, K=0 / V=1) stand for, fp32 [n, D]."""
+    if out is None:
+        out = torch.empty((max(tok_end - tok_begin, 0), cache.head_dim), dtype=torch.float32, device=cache.device)
+    _check(lib().kvq_dequantize(ctypes.byref(cache.cfg), ctypes.byref(cache.c), seq, kv_head, which, tok_begin,
+                                tok_end, _ptr(out), _stream(stream)), "kvq_dequantize")
+    return out

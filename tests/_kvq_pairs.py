@@ -1,0 +1,81 @@
+"""Helpers for the GPU parity tests: the same seeded inputs go through the CUDA
+path (via the C ABI binding) and through the CPU oracle."""
+import numpy as np
+import torch
+
+import oracle
+from sub_byte_quantized_kvq_gb300 import kvq, synth
+
+ORACLE_FMT = {kvq.KVQ_FMT_INT4_G32: oracle.FMT_INT4, kvq.KVQ_FMT_FP4_E2M1_S16: oracle.FMT_E2M1,
+              kvq.KVQ_FMT_CB2_OUTLIER: oracle.FMT_CB2, kvq.KVQ_FMT_TIERED: oracle.FMT_TIERED}
+
+
+def make_kv(seed, B, T, Hkv, D, dist="normal", n_out=4, factor=8.0, fixed=()):
+    w = synth.Workload("t", 0, B, Hkv, Hkv, D, T, dist, n_out, factor, fixed_channels=fixed)
+    ks, vs = zip(*[synth.workload_kv(w, seed, b, 0, T) for b in range(B)])
+    return torch.stack(ks), torch.stack(vs)
+
+
+class Pair:
+    """A GPU cache and an oracle cache built from identical inputs."""
+
+    def __init__(self, fmt, B, Hkv, D, P, seed=0, shuffled=True, tiers=None, extra_pages=0, sigma=3.0, iters=16):
+        self.fmt, self.B, self.Hkv, self.D, self.P = fmt, B, Hkv, D, P
+        pt, nm, nt = synth.page_table(seed, B, P, shuffled, tiers)
+        nm += extra_pages
+        self.pt = pt
+        self.gpu = kvq.QuantizedKVCache(fmt, B, Hkv, D, P, nm, nt, sigma=sigma, lloyd_iters=iters,
+                                        page_table=torch.from_numpy(pt), device="cuda")
+        self.ref = oracle.OracleCache(ORACLE_FMT[fmt], B, Hkv, D, P, nm, nt, sigma=sigma, lloyd_iters=iters,
+                                      page_table=pt)
+
+    def append(self, k, v, t_per_seq=None, dtype=torch.float32):
+        """k, v: float32 CPU [B, T, Hkv, D]; the GPU gets them in `dtype`, the
+        oracle gets the same values (rounded to `dtype`) as float32."""
+        kd, vd = k.to(dtype), v.to(dtype)
+        tps = None if t_per_seq is None else torch.as_tensor(t_per_seq, dtype=torch.int32)
+        kvq.kvq_quantize_append(self.gpu, kd.cuda().contiguous(), vd.cuda().contiguous(),
+                                None if tps is None else tps.cuda())
+        bad = self.ref.append(kd.float().numpy(), vd.float().numpy(), None if tps is None else tps.numpy())
+        return bad
+
+    def assert_cache_equal(self):
+        torch.cuda.synchronize()
+        assert self.gpu.status_word() == 0, hex(self.gpu.status_word())
+        np.testing.assert_array_equal(self.gpu.seq_lens.cpu().numpy(), self.ref.seq_lens)
+        gp = self.gpu.pool.cpu().numpy()
+        if not (gp == self.ref.pool).all():
+            stride = self.ref.stride
+            diff = np.nonzero(gp != self.ref.pool)[0]
+            blk = diff[0] // stride
+            raise AssertionError(f"pool differs at {len(diff)} bytes; first in block {blk} "
+                                 f"(phys {blk // (2 * self.Hkv)}, head {(blk // 2) % self.Hkv}, role {blk % 2}) "
+                                 f"offset {diff[0] % stride}: gpu {gp[diff[0]]:#x} oracle {self.ref.pool[diff[0]]:#x}")
+        if self.gpu.tier_pool is not None:
+            np.testing.assert_array_equal(self.gpu.tier_pool.cpu().numpy(), self.ref.tier_pool[:-1])
+        if self.gpu.staging is not None:
+            np.testing.assert_array_equal(self.gpu.staging.cpu().numpy(), self.ref.staging.reshape(-1))
+
+    def decode(self, Hq, seed=0, scale=None, max_seq_len=None, num_splits=0, out_dtype=torch.float32):
+        scale = self.D ** -0.5 if scale is None else scale
+        max_seq_len = int(self.ref.seq_lens.max()) if max_seq_len is None else max_seq_len
+        q = synth.queries_bf16(seed, self.B, Hq, self.D, device="cuda")
+        out = kvq.kvq_decode_attention(self.gpu, q, scale, max_seq_len, num_splits, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        exp = self.ref.decode(q.cpu().view(torch.int16).numpy().view(np.uint16), scale)
+        return out.float().cpu().numpy(), exp
+
+
+def bf16_half_ulp(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 0.5 * 2.0 ** (e - 7)
+
+
+def assert_attention_close(got, exp, out_dtype=torch.float32, tol=2e-3):
+    """max-abs <= 2e-3 in fp32 output; bf16 output adds half a bf16 ulp of the reference."""
+    err = np.abs(got - exp)
+    bound = tol + (bf16_half_ulp(exp) if out_dtype == torch.bfloat16 else 0.0)
+    bad = err > bound
+    assert not bad.any(), f"{bad.sum()} outputs outside tolerance; max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+    return float(err.max())

@@ -1,0 +1,182 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle on
+small seeded inputs that span several pages, ragged lengths and partial tails.
+
+Bar: packed caches (codes, scales, codebooks, outlier lists, tier pages,
+staging, seq_lens) and kvq_dequantize are bit-exact; decode attention is within
+max-abs 2e-3 of the fp64 oracle (fp32 output), plus half a bf16 ulp of the
+reference for bf16 output."""
+import numpy as np
+import pytest
+import torch
+
+from _kvq_pairs import Pair, assert_attention_close, make_kv
+from sub_byte_quantized_kvq_gb300 import kvq
+
+pytestmark = pytest.mark.gpu
+
+INT4, E2M1, CB2, TIERED = (kvq.KVQ_FMT_INT4_G32, kvq.KVQ_FMT_FP4_E2M1_S16, kvq.KVQ_FMT_CB2_OUTLIER,
+                           kvq.KVQ_FMT_TIERED)
+FORMATS_D = [(INT4, 64), (INT4, 128), (E2M1, 64), (E2M1, 128), (CB2, 64), (CB2, 128), (TIERED, 64), (TIERED, 128)]
+IDS = [f"{['int4', 'e2m1', 'cb2', 'tiered'][f]}-d{d}" for f, d in FORMATS_D]
+
+
+def _tiers(fmt, B, P):
+    t = np.zeros((B, P), bool)
+    if fmt == TIERED:
+        t[:, 1::3] = True
+    return t
+
+
+def _dist(fmt):
+    return ("student_t4", 0, 1.0) if fmt == E2M1 else ("normal", 4, 8.0)
+
+
+@pytest.mark.parametrize("fmt,D", FORMATS_D, ids=IDS)
+@pytest.mark.parametrize("pattern", ["prefill", "tokens", "ragged", "prefill_bf16"])
+def test_quantize_append_bit_exact(fmt, D, pattern):
+    B, Hkv, P = 3, 2, 8
+    pair = Pair(fmt, B, Hkv, D, P, seed=1, tiers=_tiers(fmt, B, P))
+    dist, n_out, factor = _dist(fmt)
+    T = 100 if pattern.startswith("prefill") else 40
+    k, v = make_kv(5, B, T if pattern != "ragged" else 120, Hkv, D, dist, n_out, factor)
+    if pattern == "prefill":
+        pair.append(k, v)
+    elif pattern == "prefill_bf16":
+        pair.append(k, v, dtype=torch.bfloat16)
+    elif pattern == "tokens":
+        for t in range(T):
+            pair.append(k[:, t:t + 1], v[:, t:t + 1])
+    else:
+        pos = np.zeros(B, int)
+        for tps in ([20, 5, 0], [3, 17, 9], [16, 16, 16], [1, 0, 31], [40, 2, 15]):
+            Tc = max(tps)
+            kc = torch.zeros((B, Tc, Hkv, D))
+            vc = torch.zeros((B, Tc, Hkv, D))
+            for b in range(B):
+                kc[b, :tps[b]] = k[b, pos[b]:pos[b] + tps[b]]
+                vc[b, :tps[b]] = v[b, pos[b]:pos[b] + tps[b]]
+                pos[b] += tps[b]
+            assert pair.append(kc, vc, t_per_seq=tps) == 0
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt,D", FORMATS_D, ids=IDS)
+def test_dequantize_bit_exact(fmt, D):
+    B, Hkv, P = 2, 2, 7
+    pair = Pair(fmt, B, Hkv, D, P, seed=2, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(6, B, 83, Hkv, D, *_dist(fmt))
+    pair.append(k, v, t_per_seq=[83, 50])
+    for b, L in enumerate([83, 50]):
+        for h in range(Hkv):
+            for role in (0, 1):
+                got = kvq.kvq_dequantize(pair.gpu, b, h, role, 0, L).cpu().numpy()
+                exp = pair.ref.dequantize(b, h, role, 0, L)
+                np.testing.assert_array_equal(got.view(np.int32), exp.view(np.int32))
+                got = kvq.kvq_dequantize(pair.gpu, b, h, role, 5, 37).cpu().numpy()
+                np.testing.assert_array_equal(got.view(np.int32), exp[5:37].view(np.int32))
+
+
+@pytest.mark.parametrize("fmt,D", FORMATS_D, ids=IDS)
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
+def test_decode_attention_parity(fmt, D, G):
+    B, Hkv, P = 3, 2, 14
+    lens = [209, 77, 1]
+    pair = Pair(fmt, B, Hkv, D, P, seed=3, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(7, B, max(lens), Hkv, D, *_dist(fmt))
+    pair.append(k, v, t_per_seq=lens)
+    for splits in (0, 1, 5):
+        for od in (torch.float32, torch.bfloat16):
+            got, exp = pair.decode(Hkv * G, seed=splits, num_splits=splits, out_dtype=od)
+            assert_attention_close(got, exp, od)
+    assert pair.gpu.status_word() == 0
+
+
+@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED])
+def test_decode_after_token_by_token_appends(fmt):
+    """Decode after every single-token append (the serving loop), crossing page boundaries."""
+    B, Hkv, D, P, G = 2, 2, 128, 4, 4
+    pair = Pair(fmt, B, Hkv, D, P, seed=4, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(8, B, 40, Hkv, D, *_dist(fmt))
+    for t in range(40):
+        pair.append(k[:, t:t + 1], v[:, t:t + 1])
+        if t in (0, 14, 15, 16, 31, 32, 39):
+            got, exp = pair.decode(Hkv * G, seed=t)
+            assert_attention_close(got, exp)
+
+
+def test_empty_and_single_token_sequences():
+    B, Hkv, D, P = 3, 1, 128, 3
+    pair = Pair(CB2, B, Hkv, D, P, seed=5)
+    k, v = make_kv(9, B, 33, Hkv, D)
+    pair.append(k, v, t_per_seq=[0, 1, 33])
+    got, exp = pair.decode(4, num_splits=2)
+    assert (got[0] == 0).all() and (exp[0] == 0).all()
+    assert_attention_close(got, exp)
+    # one cached token: the output is that token's V row (as stored: fp32 staging)
+    np.testing.assert_allclose(got[1], np.broadcast_to(v[1, 0, 0].numpy(), got[1].shape), atol=1e-6)
+
+
+@pytest.mark.parametrize("fmt", [INT4, CB2])
+def test_constant_and_extreme_values(fmt):
+    """Constant pages (zero std: no outliers, degenerate codebooks) and outliers
+    far beyond the e4m3 range (both sides saturate at 448) stay bit-exact."""
+    B, Hkv, D, P = 2, 1, 64, 3
+    pair = Pair(fmt, B, Hkv, D, P, seed=6)
+    k = torch.full((B, 48, Hkv, D), 0.75)
+    v = torch.full((B, 48, Hkv, D), -1.5)
+    k[1, :, 0, 3] = 3000.0 * torch.linspace(-1, 1, 48)
+    v[1, :, 0, 9] = 1e4
+    pair.append(k, v)
+    pair.assert_cache_equal()
+    got, exp = pair.decode(4, scale=1e-4)
+    assert_attention_close(got, exp, tol=2e-3 * max(1.0, float(np.abs(exp).max()) / 100))
+
+
+def test_bad_page_entry_is_flagged_and_skipped():
+    B, Hkv, D, P = 2, 1, 128, 4
+    pair = Pair(CB2, B, Hkv, D, P, seed=7, extra_pages=0)
+    k, v = make_kv(10, B, 40, Hkv, D)
+    pt = pair.gpu.page_table.clone()
+    pair.gpu.page_table[0, 1] = pair.gpu.cfg.num_pages + 5      # sequence 0 names a page outside the pool
+    kvq.kvq_quantize_append(pair.gpu, k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_BAD_PAGE
+    assert pair.gpu.seq_lens.cpu().tolist() == [0, 40]          # sequence 0 skipped, 1 appended
+    pair.gpu.page_table.copy_(pt)
+    pair.gpu.status.zero_()
+
+
+def test_capacity_overflow_matches_oracle():
+    B, Hkv, D, P = 2, 1, 64, 2
+    pair = Pair(E2M1, B, Hkv, D, P, seed=8)
+    k, v = make_kv(11, B, 20, Hkv, D, "student_t4", 0, 1.0)
+    pair.append(k, v)
+    bad = pair.append(k, v, t_per_seq=[20, 12])     # 40 > 32 slots for sequence 0
+    assert bad == 1
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_CAPACITY
+    pair.gpu.status.zero_()
+    pair.assert_cache_equal()
+
+
+def test_seq_longer_than_max_seq_len_is_flagged():
+    B, Hkv, D, P = 1, 1, 128, 4
+    pair = Pair(CB2, B, Hkv, D, P, seed=9)
+    k, v = make_kv(12, B, 50, Hkv, D)
+    pair.append(k, v)
+    q = torch.zeros((1, 4, D), dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_decode_attention(pair.gpu, q, 0.1, 32)
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_SEQ_TOO_LONG
+
+
+def test_workspace_and_argument_errors():
+    pair = Pair(CB2, 1, 2, 128, 2, seed=10)
+    q = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(4, dtype=torch.float32, device="cuda")
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.kvq_decode_attention(pair.gpu, q, 0.1, 32, workspace=ws)
+    assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+    with pytest.raises(kvq.KVQError) as e:   # 3 query heads do not divide over 2 kv heads
+        kvq.kvq_decode_attention(pair.gpu, torch.zeros((1, 3, 128), dtype=torch.bfloat16, device="cuda"), 0.1, 32)
+    assert e.value.status == kvq.KVQ_ERR_INVALID_ARG
