@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Quantized-KV decode attention benchmark (one JSON line on stdout).
+
+Metric: achieved HBM GB/s of one decode step = algorithmic bytes (packed cache
+blocks the step must read, fp32 staging tail, bf16 Q and output) / device time
+of the step (split kernel + combine kernel), with the cache resident in HBM and
+L2 flushed before every timed step.  ms_per_step gives the microseconds per
+decode step.  The default workload is cb2_4k (B8, Hkv8, Hq32, D128, context
+4096, 2-bit codebook + e4m3 outliers).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (plain fp64 C) on the host cores on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".  Under torchrun (N > 1) every rank runs an independent
+replica (weak scaling: the path shards by (sequence, kv head) with no exchange);
+value sums the ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sub_byte_quantized_kvq_gb300 import kvq, synth, workloads  # noqa: E402
+
+METRIC = "quantized-KV decode attention: achieved HBM GB/s vs peak; us per decode step"
+FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED"}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+KERNEL_SOURCES = ["kvq_common.cuh", "kvq_decode.cuh", "kvq_internal.cuh"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    p.add_argument("--workload", default="cb2_4k", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--splits", type=int, default=-1, help="-1: the workload's own (0 = library choice)")
+    p.add_argument("--flush-mb", type=int, default=512)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--append", action="store_true", help="also time kvq_quantize_append (1-token and prefill chunk)")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- byte accounting
+def algorithmic_bytes(built: workloads.Built) -> dict:
+    """Bytes one decode step must move: the packed contents of every block it
+    reads (codes, scales / codebooks, per-token counts and the outlier entries
+    actually present), the fp32 staging tail, Q (bf16) and the output (bf16)."""
+    w, cache = built.w, built.cache
+    D = w.D
+    L = w.N
+    full = L // 16
+    blocks = w.B * w.Hkv * 2
+    if w.fmt in (synth.FMT_CB2, synth.FMT_TIERED):
+        # CB2 block: codes + codebook (12D) + side-list header, records and values
+        pool = cache.pool.view(-1, cache.block_bytes(0))
+        nch = pool[:, 12 * D].to(torch.int64)
+        side = (4 + 4 * nch + 16 * (nch + (nch & 1))).sum().item()
+        n_tier = int(built.tiers[:, :full].sum()) * w.Hkv * 2
+        n_main = full * blocks - n_tier
+        cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
+        tail = (L % 16) * D * 4 * blocks
+    elif w.fmt == synth.FMT_INT4:
+        pool = cache.pool.view(-1, cache.block_bytes(0))
+        counts = pool[:, 10 * D:10 * D + 16].to(torch.int64).sum().item()
+        cache_bytes = ((L + 15) // 16) * blocks * (10 * D + 16) + 3 * counts
+        tail = 0
+    else:
+        cache_bytes = ((L + 15) // 16) * blocks * 9 * D
+        tail = 0
+    q_bytes = w.B * w.Hq * D * 2
+    out_bytes = w.B * w.Hq * D * 2
+    return {"cache": int(cache_bytes), "tail": int(tail), "q": q_bytes, "out": out_bytes,
+            "split_kernel": int(cache_bytes + tail + q_bytes), "step": int(cache_bytes + tail + q_bytes + out_bytes)}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "sub_byte_quantized_kvq_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[4]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r[2] >= 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_busy": len(busy)}
+
+
+# ----------------------------------------------------------------------------- GPU timing
+L2_BYTES = 129 * 1024 * 1024
+
+
+class L2Flush:
+    """Write one buffer and read another, each larger than L2, so a step starts
+    with none of its inputs cached (and no dirty lines to write back)."""
+
+    def __init__(self, mb: int, device):
+        n = max(mb, 2 * 160) * 1024 * 1024 // 2
+        self.a = torch.empty(n, dtype=torch.uint8, device=device)
+        self.b = torch.ones(n // 4, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int32, device=device)
+        self.k = 0
+
+    def __call__(self):
+        self.k += 1
+        self.a.fill_(self.k & 0xFF)
+        torch.sum(self.b, dim=0, out=self.sink)
+
+
+def time_gpu(built: workloads.Built, args, world: int, dev) -> dict:
+    w, cache = built.w, built.cache
+    S = w.splits if args.splits < 0 else args.splits
+    S_eff = S if S > 0 else kvq.kvq_decode_num_splits(cache, w.Hq, w.N)
+    q = synth.queries_bf16(args.seed, w.B, w.Hq, w.D, device=dev)
+    scale = w.D ** -0.5
+    ws = kvq.alloc_workspace(cache, w.Hq, w.N, S)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    nbytes = algorithmic_bytes(built)
+    flush = L2Flush(args.flush_mb, dev) if nbytes["step"] < 3 * L2_BYTES else None
+
+    def step(q_in, evs):
+        evs[0].record()
+        kvq.kvq_decode_split(cache, q_in, scale, w.N, ws, S)
+        evs[1].record()
+        kvq.kvq_decode_combine(cache, w.Hq, w.N, ws, out, S)
+        evs[2].record()
+
+    mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]  # noqa: E731
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        if flush:
+            flush()
+        step(q, mk(3))
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [mk(3) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush:
+            flush()
+        step(q, evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    split_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    assert cache.status_word() == 0, f"device status {cache.status_word():#x}"
+
+    # end to end through the C ABI with host buffers: pinned Q in, output back, every step
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_dev = torch.empty_like(q)
+    e2e_evs = [mk(2) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        if flush:
+            flush()
+        e = e2e_evs[i - args.warmup] if i >= args.warmup else mk(2)
+        e[0].record()
+        q_dev.copy_(q_host, non_blocking=True)
+        kvq.kvq_decode_attention(cache, q_dev, scale, w.N, S, out=out, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+        e[1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = [e[0].elapsed_time(e[1]) for e in e2e_evs]
+    return {"split_ms": float(np.mean(split_ms)), "step_ms": float(np.mean(step_ms)),
+            "step_ms_median": float(np.median(step_ms)), "e2e_ms": float(np.mean(e2e_ms)), "bytes": nbytes,
+            "splits": S_eff, "clocks": clocks, "flushed": flush is not None,
+            "h2d": q.numel() * q.element_size(), "d2h": out.numel() * out.element_size()}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+ORACLE_SAMPLE_TOKENS = 8192
+
+
+def oracle_sample(w: synth.Workload, seed: int):
+    """Oracle cache for a bounded sample: sequence 0, all kv heads, the first
+    min(N, 8192) tokens (same distributions; drawn with the CPU generator)."""
+    import oracle
+    N = min(w.N, ORACLE_SAMPLE_TOKENS)
+    pages = (N + 15) // 16
+    tiers = synth.tier_pages(seed, 1, N, w.tier_frac, w.zipf_s) if w.tier_frac > 0 else None
+    pt, nm, nt = synth.page_table(seed, 1, pages, False, tiers)
+    ref = oracle.OracleCache(w.fmt, 1, w.Hkv, w.D, pages, max(nm, 1), nt, page_table=pt)
+    for t0, T in workloads.chunks(N):
+        k, v = workloads.seq_kv(w, seed, 0, t0, T, "cpu")
+        ref.append(k[None].numpy(), v[None].numpy())
+    q = synth.queries_bf16(seed, 1, w.Hq, w.D).view(torch.int16).numpy().view(np.uint16)
+    # bytes the same step reads for this sample (same accounting as the GPU line)
+    D, full = w.D, N // 16
+    if w.fmt in (synth.FMT_CB2, synth.FMT_TIERED):
+        blocks = ref.pool.reshape(-1, ref.stride).astype(np.int64)
+        nch = blocks[:, 12 * D]
+        side = int((4 + 4 * nch + 16 * (nch + (nch & 1))).sum())
+        n_tier = (int(tiers[:, :full].sum()) if tiers is not None else 0) * w.Hkv * 2
+        cache = (full * w.Hkv * 2 - n_tier) * 12 * D + side + n_tier * (16 * D + 4)
+        cache += (N % 16) * D * 4 * w.Hkv * 2
+    elif w.fmt == synth.FMT_INT4:
+        counts = int(ref.pool.reshape(-1, ref.stride)[:, 10 * D:10 * D + 16].astype(np.int64).sum())
+        cache = pages * w.Hkv * 2 * (10 * D + 16) + 3 * counts
+    else:
+        cache = pages * w.Hkv * 2 * 9 * D
+    nbytes = cache + 2 * w.Hq * D * 2
+    return ref, q, nbytes, N
+
+
+def time_oracle(w: synth.Workload, seed: int, target_s: float, reps: int | None = None):
+    ref, q, nbytes, N = oracle_sample(w, seed)
+    cores = os.cpu_count() or 1
+    scale = w.D ** -0.5
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        ref.decode(q, scale, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+        if reps is not None and len(times) >= reps:
+            break
+        if reps is None and time.perf_counter() - t_start >= target_s:
+            break
+    mean = float(np.mean(times))
+    return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"sequence 0 of {w.name}, all {w.Hkv} kv heads x {w.G} query heads, first {N} tokens, "
+                      f"fp64 dequantize + attention, {len(times)} runs of {mean * 1e3:.1f} ms",
+            "ms_per_step": mean * 1e3, "bytes_per_step": nbytes}
+
+
+# ----------------------------------------------------------------------------- append timing (optional)
+def time_append(w: synth.Workload, dev) -> dict:
+    """kvq_quantize_append for every sequence of the workload: one token into
+    staging, one token that completes a page (page quantizer), and a 4096-token
+    prefill chunk (bf16 inputs)."""
+    res = {}
+    for label, T, start in (("1_token_staging", 1, 0), ("1_token_completes_page", 1, 15), ("prefill_4096", 4096, 0)):
+        pages = (start + T + 15) // 16
+        c = kvq.QuantizedKVCache(w.fmt, w.B, w.Hkv, w.D, pages, w.B * pages, 0, device=dev)
+        kk = torch.randn((w.B, T, w.Hkv, w.D), device=dev).to(torch.bfloat16)
+        vv = torch.randn_like(kk)
+        ts = []
+        for r in range(8):
+            c.seq_lens.fill_(start)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kvq_quantize_append(c, kk, vv)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        t = float(np.mean(ts))
+        res[label] = {"us": t * 1e6, "input_gbs": 2 * kk.numel() * kk.element_size() / t / 1e9}
+    return res
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    rank, world = dist_setup(args)
+    w = synth.WORKLOADS[args.workload]
+    config = {"workload": w.name, "format": FMT_NAME[w.fmt], "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "D": w.D,
+              "context": w.N, "page_tokens": 16}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = time_oracle(w, args.seed, 0.0, reps=args.warmup + args.steps)
+        line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": dict(config, sample=r["sample"]),
+                "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    built = workloads.build(w, seed=args.seed + rank, device=dev)
+    torch.cuda.synchronize()
+    t = time_gpu(built, args, world, dev)
+    step_ms = all_max(t["step_ms"], world)
+    split_ms = all_max(t["split_ms"], world)
+    e2e_ms = all_max(t["e2e_ms"], world)
+    nb = t["bytes"]
+    peak, peak_kind = measured_peak_gbs()
+    achieved = nb["split_kernel"] / (split_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_src_sha") == kernel_source_sha() and tr.get("workload") == w.name:
+            traffic = tr["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    line = {
+        "metric": METRIC,
+        "value": world * nb["step"] / (step_ms * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_ms, "us_per_step": step_ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 mma / f32 accumulate over 2-4 bit codes", "data": "synthetic",
+        "config": dict(config, splits=t["splits"],
+                       l2="flushed before every step (write 256 MB + read 256 MB)" if t["flushed"]
+                       else "inputs exceed L2 (no flush)",
+                       bytes_per_step=nb["step"], partial_bytes_per_step=0),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": nb["split_kernel"], "us_per_launch": split_ms * 1e3},
+        "e2e": {"value": world * nb["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": t["h2d"], "d2h_bytes_per_step": t["d2h"], "us_per_step": e2e_ms * 1e3},
+        "gpu_launches": 2 * args.steps,
+        "clocks": t["clocks"],
+    }
+    line["config"]["partial_bytes_per_step"] = 2 * w.B * w.Hq * t["splits"] * (w.D + 2) * 4
+    if args.append:
+        line["append"] = time_append(w, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_oracle(w, args.seed, args.cpu_seconds)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -71,7 +71,8 @@ typedef enum {
     /* [P1] per (page, channel) 4-centroid fp16 codebook fitted by Lloyd-Max
      * (k-means in one dimension, linspace start) over the page's non-outliers;
      * per-token outliers (sigma rule over the head vector) kept as FP8 E4M3 in
-     * a per-page side-list.  Quantized when a page fills; the partial last
+     * a per-page side-list: one (channel, token mask) record per channel
+     * holding outliers, and their values.  Quantized when a page fills; the partial last
      * page waits in fp32 staging. */
     KVQ_FMT_CB2_OUTLIER = 2,
     /* [P2] KVQ_FMT_CB2_OUTLIER pages plus FP8 E4M3 pages with one fp32 scale per
@@ -184,6 +185,19 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
                                 int32_t num_splits, void* out, kvq_dtype out_dtype, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* The two stages of kvq_decode_attention as separate calls (same arguments,
+ * same resolution of num_splits = 0): kvq_decode_split writes the fp32 split
+ * partials (m, l, o) of every (sequence, query head, split) into `workspace`;
+ * kvq_decode_combine merges them into `out`.  Calling split then combine on
+ * one stream is exactly kvq_decode_attention; the split is the HBM-bound
+ * kernel, the combine reads only the partials. */
+kvq_status kvq_decode_split(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
+                            float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* workspace,
+                            size_t workspace_bytes, void* stream);
+kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_t max_seq_len, int32_t num_splits,
+                              const void* workspace, size_t workspace_bytes, void* out, kvq_dtype out_dtype,
+                              void* stream);
+
 /* Debug: the values tokens [tok_begin, tok_end) of (seq, kv_head, which = 0 K /
  * 1 V) stand for, as fp32 [tok_end - tok_begin][D] in device memory `out`.
  * Bit-identical to the CPU reference's dequantization. */
@@ -225,10 +239,14 @@ const char* kvq_version(void);
  *             4D        codebook: 8 bytes per slot sigma(c) = {u32 L, u32 H}, L byte
  *                       i = low byte of fp16 centroid i, H byte i = its high byte;
  *                       K: sigma(c) = c;  V: sigma(c) = 16*(c/16) + 2*(c%8) + (c%16)/8
- *             12D       u8 outlier count per token [16]
- *             12D+16    outlier entries {u8 channel, u8 e4m3 value}, sorted by
- *                       (token, channel); at most 16*kmax, kmax = ceil((D-1)/9)-1
- *             stride 1024 (D=64), 2048 (D=128)
+ *             12D       outlier side-list, grouped by channel: u8 n_ch (channels
+ *                       holding an outlier), u8 total (outliers), 2 zero bytes;
+ *                       n_ch records {u8 channel, 0, u16 token mask}, channels
+ *                       ascending; then at V0 = 12D + 4 + 4*n_ch a 16 x R byte
+ *                       matrix (R = n_ch rounded up to even) of the e4m3 values,
+ *                       0 where a token is not an outlier of the channel:
+ *                       K: value(t, i) at V0 + t*R + i;  V: at V0 + 16*i + t
+ *             stride 2176 (D=64), 4224 (D=128)
  *   FP8 tier  [0, 16D)  codes: lane l at 8*NS*l, step s at +8s, slot k = byte k (e4m3)
  *             16D       fp32 scale
  *             stride 1152 (D=64), 2176 (D=128)

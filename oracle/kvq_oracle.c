@@ -291,8 +291,15 @@ EXPORT int or_lloyd4(const double* v, int n, int iters, double* c_out, uint16_t*
 /*                               byte of fp16 centroid j), u32 H (high bytes) */
 /*                               K: sigma(c) = c                              */
 /*                               V: sigma(c) = 16*(c/16) + 2*(c%8) + (c%16)/8 */
-/*            counts at 12D      u8[16] outliers per token                    */
-/*            entries at 12D+16  {u8 channel, u8 e4m3} sorted by (t, c)       */
+/*            outliers at 12D    u8 n_ch (channels holding an outlier),       */
+/*                               u8 total (outliers), 2 zero bytes; n_ch      */
+/*                               records {u8 channel, 0, u16 token mask},     */
+/*                               channels ascending; then at V0 = 4 + 4*n_ch  */
+/*                               a 16 x R byte matrix (R = n_ch rounded up to */
+/*                               even) of e4m3 values, 0 where the token is   */
+/*                               not an outlier of that channel:              */
+/*                               K: value(t, i) at V0 + t*R + i (token-major) */
+/*                               V: value(t, i) at V0 + i*16 + t              */
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
 /*            scale at 16D       fp32                                         */
@@ -310,7 +317,7 @@ EXPORT int or_block_stride(int fmt, int D)
     switch (fmt) {
     case OR_INT4: return round128(10 * D + 16 + 48 * cap);
     case OR_E2M1: return round128(9 * D);
-    case OR_CB2:  return round128(12 * D + 16 + 32 * or_kmax(D));
+    case OR_CB2:  return round128(12 * D + 4 + 4 * D + 16 * D);
     case OR_FP8:  return round128(16 * D + 16);
     }
     return -1;
@@ -509,20 +516,37 @@ static void quantize_page_cb2(const float* x, int D, double sigma, int iters, in
         for (int t = 0; t < 16; ++t)
             cb2_code_set(blk, D, role, t, c, mask[t][c] ? 0 : codes[n++]);
     }
-    uint8_t* counts = blk + 12 * D;
-    uint8_t* ent = blk + 12 * D + 16;
-    int e = 0;
-    for (int t = 0; t < 16; ++t) {
-        int cnt = 0;
-        for (int c = 0; c < D; ++c) {
-            if (!mask[t][c]) continue;
-            ent[2 * e] = (uint8_t)c;
-            ent[2 * e + 1] = or_e4m3_encode((double)x[t * D + c]);
-            ++e;
-            ++cnt;
-        }
-        counts[t] = (uint8_t)cnt;
+    /* side-list grouped by channel: a record {channel, 0, token mask} for each
+     * channel holding an outlier, then a dense 16 x R matrix of their e4m3
+     * values (0 elsewhere), token-major for K, channel-major for V */
+    uint8_t* hdr = blk + 12 * D;
+    int n_ch = 0, total = 0;
+    for (int c = 0; c < D; ++c) {
+        int any = 0;
+        for (int t = 0; t < 16; ++t) any |= mask[t][c];
+        n_ch += any;
     }
+    int R = n_ch + (n_ch & 1);
+    uint8_t* val = hdr + 4 + 4 * n_ch;
+    int i = 0;
+    for (int c = 0; c < D; ++c) {
+        unsigned tmask = 0;
+        for (int t = 0; t < 16; ++t)
+            if (mask[t][c]) tmask |= 1u << t;
+        if (!tmask) continue;
+        uint8_t* rec = hdr + 4 + 4 * i;
+        rec[0] = (uint8_t)c;
+        rec[1] = 0;
+        put_u16(rec + 2, (uint16_t)tmask);
+        for (int t = 0; t < 16; ++t)
+            if (mask[t][c]) {
+                val[role == 0 ? t * R + i : i * 16 + t] = or_e4m3_encode((double)x[t * D + c]);
+                ++total;
+            }
+        ++i;
+    }
+    hdr[0] = (uint8_t)n_ch;
+    hdr[1] = (uint8_t)total;
 }
 
 static void quantize_page_fp8(const float* x, int D, int role, uint8_t* blk)
@@ -574,12 +598,15 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
         }
     }
     if (fmt == OR_CB2) {
-        const uint8_t* ent = blk + 12 * D + 16;
-        int e = 0;
-        for (int t = 0; t < 16; ++t) {
-            int cnt = blk[12 * D + t];
-            for (int i = 0; i < cnt; ++i, ++e)
-                if (t < ntok) out[t * D + ent[2 * e]] = (float)or_e4m3_decode(ent[2 * e + 1]);
+        const uint8_t* hdr = blk + 12 * D;
+        int n_ch = hdr[0], R = n_ch + (n_ch & 1);
+        const uint8_t* val = hdr + 4 + 4 * n_ch;
+        for (int i = 0; i < n_ch; ++i) {
+            const uint8_t* rec = hdr + 4 + 4 * i;
+            unsigned tmask = get_u16(rec + 2);
+            for (int t = 0; t < 16 && t < ntok; ++t)
+                if (tmask & (1u << t))
+                    out[t * D + rec[0]] = (float)or_e4m3_decode(val[role == 0 ? t * R + i : i * 16 + t]);
         }
     }
 }

@@ -78,11 +78,15 @@ __global__ void dequantize_kernel(const DequantArgs a) {
       const uint32_t q = (w >> (4 * (p.slot & 3) + 2 * (p.slot >> 2))) & 3u;
       const uint8_t* cb = blk + cb2_cb_off(D) + 8 * cb2_slot(a.role, c);
       v = dq_f16(cb[q] | (cb[4 + q] << 8));
-      const int emax = 16 * kmax_outliers(D);  // a corrupt side-list never reads past its block
-      int e = 0;
-      for (int tt = 0; tt < t; ++tt) e += blk[cb2_cnt_off(D) + tt];
-      for (int i = 0; i < blk[cb2_cnt_off(D) + t] && e < emax; ++i, ++e)
-        if (blk[cb2_ent_off(D) + 2 * e] == c) v = dq_e4m3(blk[cb2_ent_off(D) + 2 * e + 1]);
+      const uint8_t* hdr = blk + cb2_out_off(D);
+      const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
+      const int R = n_ch + (n_ch & 1);
+      for (int i = 0; i < n_ch; ++i) {
+        const uint8_t* rec = hdr + 4 + 4 * i;
+        const uint32_t tm = rec[2] | (rec[3] << 8);
+        if (rec[0] == c && (tm >> t & 1u))
+          v = dq_e4m3(hdr[4 + 4 * n_ch + (a.role == 0 ? t * R + i : 16 * i + t)]);
+      }
     } else {
       float s;
       memcpy(&s, blk + fp8_sc_off(D), 4);
@@ -237,13 +241,16 @@ kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t num_q_heads
   return KVQ_OK;
 }
 
-kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
-                                float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* out,
-                                kvq_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!cfg_ok(cfg) || !cache_ok(cfg, cache) || !q || !out || !workspace) return KVQ_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace kvq {
+// Validate a decode request and fill the split kernel's arguments.
+static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
+                                 float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, DecodeArgs& a) {
+  if (!cfg_ok(cfg) || !cache_ok(cfg, cache) || !q || !workspace) return KVQ_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cfg->num_kv_heads || max_seq_len < 0 || num_splits < 0)
     return KVQ_ERR_INVALID_ARG;
-  if (out_dtype != KVQ_BF16 && out_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 16) return KVQ_ERR_INVALID_ARG;
   const int G = num_q_heads / cfg->num_kv_heads;
@@ -253,10 +260,10 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
   if (st != KVQ_OK) return st;
   if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
   const int S = num_splits ? num_splits : auto_splits(cfg, G, max_seq_len);
-  const int pages = (max_seq_len + kPage - 1) / kPage;
-  if ((long long)S > 65535 || (long long)cfg->num_kv_heads > 65535 || (long long)cfg->num_seqs > 65535)
-    return KVQ_ERR_CAPACITY;
-  DecodeArgs a;
+  if (S > 65535) return KVQ_ERR_CAPACITY;
+  const int cap_len = cfg->pages_per_seq_max * kPage;
+  const int len = max_seq_len < cap_len ? max_seq_len : cap_len;
+  const int pages = (len + kPage - 1) / kPage;
   a.pool = static_cast<const uint8_t*>(cache->pool);
   a.tier_pool = static_cast<const uint8_t*>(cache->tier_pool);
   a.page_table = cache->page_table;
@@ -276,12 +283,57 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
   a.num_tier_pages = cfg->num_tier_pages;
   a.S = S;
   a.pps = pages > 0 ? (pages + S - 1) / S : 1;
-  a.max_seq_len = max_seq_len < cfg->pages_per_seq_max * kPage ? max_seq_len : cfg->pages_per_seq_max * kPage;
+  a.max_seq_len = len;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  a.ent_prefetch = kEntPrefetchDefault;
-  if (decode_launch(a, cfg->format, cfg->head_dim, out, out_dtype, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  return KVQ_OK;
+}
+}  // namespace kvq
+
+extern "C" {
+
+kvq_status kvq_decode_split(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
+                            float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  DecodeArgs a;
+  kvq_status st = decode_prepare(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
+                                 workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  if (decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_t max_seq_len, int32_t num_splits,
+                              const void* workspace, size_t workspace_bytes, void* out, kvq_dtype out_dtype,
+                              void* stream) {
+  if (!cfg_ok(cfg) || !workspace || !out || num_q_heads <= 0 || num_q_heads % cfg->num_kv_heads || max_seq_len < 0 ||
+      num_splits < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (out_dtype != KVQ_BF16 && out_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16) return KVQ_ERR_INVALID_ARG;
+  if (!dim_supported(cfg) || num_q_heads / cfg->num_kv_heads > 16) return KVQ_ERR_UNSUPPORTED;
+  size_t need = 0;
+  kvq_status st = kvq_decode_workspace_bytes(cfg, num_q_heads, max_seq_len, num_splits, &need);
+  if (st != KVQ_OK) return st;
+  if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  const int S = num_splits ? num_splits : auto_splits(cfg, num_q_heads / cfg->num_kv_heads, max_seq_len);
+  const float* part_o = static_cast<const float*>(workspace);
+  const float2* part_ml = reinterpret_cast<const float2*>(part_o + (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
+  if (decode_combine_launch(part_o, part_ml, cfg->num_seqs, num_q_heads, S, cfg->head_dim, out, out_dtype,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
+                                float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* out,
+                                kvq_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out || (out_dtype != KVQ_BF16 && out_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
+  kvq_status st = kvq_decode_split(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
+                                   workspace_bytes, stream);
+  if (st != KVQ_OK) return st;
+  return kvq_decode_combine(cfg, num_q_heads, max_seq_len, num_splits, workspace, workspace_bytes, out, out_dtype,
+                            stream);
 }
 
 kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t seq, int32_t kv_head, int32_t which,

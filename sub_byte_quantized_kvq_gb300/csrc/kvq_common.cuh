@@ -29,14 +29,13 @@ __host__ __device__ constexpr int int4_ch_off(int D) { return 10 * D + 16; }
 __host__ __device__ constexpr int int4_val_off(int D) { return 10 * D + 16 + 16 * int4_cap(D); }
 __host__ __device__ constexpr int e2m1_sc_off(int D) { return 8 * D; }
 __host__ __device__ constexpr int cb2_cb_off(int D) { return 4 * D; }
-__host__ __device__ constexpr int cb2_cnt_off(int D) { return 12 * D; }
-__host__ __device__ constexpr int cb2_ent_off(int D) { return 12 * D + 16; }
+__host__ __device__ constexpr int cb2_out_off(int D) { return 12 * D; }   // outlier side-list
 __host__ __device__ constexpr int fp8_sc_off(int D) { return 16 * D; }
 
 __host__ __device__ constexpr int block_stride(int fmt, int D) {
   return fmt == kBlkInt4 ? round_up128(10 * D + 16 + 48 * int4_cap(D))
        : fmt == kBlkE2m1 ? round_up128(9 * D)
-       : fmt == kBlkCb2  ? round_up128(12 * D + 16 + 32 * kmax_outliers(D))
+       : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 4 * D + 16 * D)
                          : round_up128(16 * D + 16);
 }
 
@@ -141,12 +140,24 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// try_wait that may suspend the thread for up to `hint_ns` (woken early when
+// the phase completes), so waiting warps do not spin on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, "
+      "p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Wait for phase `parity` of `bar`, giving up after `limit_ns`.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }

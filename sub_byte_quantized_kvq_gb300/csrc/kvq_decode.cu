@@ -51,19 +51,23 @@ int decode_ctas_per_sm(int fmt, int D, int G) {
   return n;
 }
 
-cudaError_t decode_launch(const DecodeArgs& a, int fmt, int D, void* out, int out_dtype, cudaStream_t st) {
+cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_t st) {
   KernelInfo k = pick_kernel(fmt, D, a.G);
   cudaError_t err = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem);
   if (err != cudaSuccess) return err;
   void* args[] = {const_cast<DecodeArgs*>(&a)};
   err = cudaLaunchKernel(k.fn, dim3(a.S, a.Hkv, a.B), dim3(k.threads), args, k.smem, st);
   if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hq, int S, int D, void* out,
+                                  int out_dtype, cudaStream_t st) {
   if (out_dtype == KVQ_F32)
-    decode_combine_kernel<float><<<dim3(a.Hq, a.B), 128, 0, st>>>(a.part_o, a.part_ml, a.S, D, a.Hq,
-                                                                  static_cast<float*>(out));
+    decode_combine_kernel<float><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, S, D, Hq, static_cast<float*>(out));
   else
-    decode_combine_kernel<__nv_bfloat16><<<dim3(a.Hq, a.B), 128, 0, st>>>(a.part_o, a.part_ml, a.S, D, a.Hq,
-                                                                          static_cast<__nv_bfloat16*>(out));
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, S, D, Hq,
+                                                                        static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

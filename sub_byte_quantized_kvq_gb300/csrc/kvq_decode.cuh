@@ -1,5 +1,5 @@
 // kvq_decode.cuh -- split-K decode attention over the quantized paged cache with
-// dequantization fused in, and the split-combine kernel.
+// dequantization fused in.
 //
 // "Hierarchical Token Routing and Sub-2-Bit Non-Linear KV Compression",
 // "Hardware-Kernel Fusion": packed codes go from HBM to shared memory and are
@@ -15,20 +15,24 @@
 // Design (GB300, sm_103a):
 //  * grid (splits, kv heads, sequences); a CTA owns one (sequence, kv head,
 //    split) and all G query heads of that kv head; each of its W warps streams
-//    its own pages (page p0 + w, p0 + w + W, ...), with its own online-softmax
-//    state, and the warps merge in shared memory at the end.
+//    its own pages (page p0 + w, p0 + w + W, ...), PPI pages per iteration,
+//    with its own online-softmax state; the warps merge in shared memory.
 //  * each warp runs an NSTAGE-deep ring of bulk asynchronous copies
-//    (cp.async.bulk + mbarrier): one copy per block, K and V of a page per
-//    stage; no register staging, no TMA multicast.
+//    (cp.async.bulk + mbarrier): one copy per block, the K and V blocks of PPI
+//    pages per stage; no register staging, no TMA multicast.
 //  * QK^T: A = K (16 tokens x 16 channels, built in registers from the codes),
 //    B = Q^T (16 channels x 8 heads, fp16, loaded once).  PV: A = V^T (16
 //    channels x 16 tokens, built in registers), B = P^T (fp16 hi + lo split of
 //    the fp32 probabilities, so P carries ~22 bits).  mma.sync m16n8k16 with
 //    fp32 accumulation; the layouts in include/kvq.h make every A register one
-//    or two byte-permutes of shared memory words.
-//  * outliers: a code slot holding an outlier stores 0; each outlier adds
-//    q.(x - c0) to its token's scores (K) and p.(x - c0) to a per-warp fp32
-//    correction of the output (V), both through shared-memory atomics.
+//    or two byte-permutes of shared-memory words.  The PPI pages of an
+//    iteration are independent mma chains the scheduler interleaves.
+//  * CB2 outliers: a code slot holding an outlier stores 0.  Up to 16 channels
+//    with outliers are packed into one k16 tile of deltas (x - c0, split into
+//    fp16 hi + lo): one more mma against the gathered query columns corrects
+//    the scores, and one mma of the delta tile against P^T gives the output
+//    correction of those channels, accumulated in shared memory with the same
+//    online-softmax rescaling as the registers.  No atomics.
 //  * the partial last page of page formats (fp32 staging) is done on CUDA
 //    cores in fp32.
 #pragma once
@@ -36,7 +40,7 @@
 
 namespace kvq {
 
-constexpr int kEntSmem = 64;          // CB2 entries that fit in a stage
+constexpr int kOutPrefetch = 96;      // bytes of a CB2 outlier side-list fetched with its block
 constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 
 template <int FMT>
@@ -44,15 +48,15 @@ struct Fmt {
   static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED);
   static constexpr int kMain = FMT == KVQ_FMT_TIERED ? kBlkCb2 : FMT;
   static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2);
+  static constexpr int kPPI = kMain == kBlkInt4 ? 1 : 2;   // pages per warp iteration
 };
 
-// Bytes copied to shared memory per block (the kernel reads nothing else of it,
-// except CB2 outlier entries past the prefetched ones).
+// Bytes copied to shared memory per block.
 template <int D>
 __host__ __device__ constexpr int fetch_bytes(int blk) {
   return blk == kBlkInt4 ? 10 * D + 16 + 48 * int4_cap(D)
        : blk == kBlkE2m1 ? 9 * D
-       : blk == kBlkCb2  ? 12 * D + 16 + 2 * kEntSmem
+       : blk == kBlkCb2  ? 12 * D + kOutPrefetch
                          : 16 * D + 16;
 }
 template <int FMT, int D>
@@ -66,19 +70,25 @@ __host__ __device__ constexpr int half_slot_bytes() {
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
 // Shared-memory plan: [qsm: D x GS fp32] then per warp:
-// [stages: NSTAGE x 2 half-slots][mbar x NSTAGE][meta x NSTAGE][ds 16 x GS][psm 16 x GS][corr D x GS]
+// [stages: NSTAGE x PPI x 2 blocks][mbar x NSTAGE][meta x NSTAGE*PPI][ds 16 x GS][psm 16 x GS][corr D x GS]
 template <int FMT, int D, int NSTAGE>
 __host__ __device__ constexpr int warp_smem_bytes(int GS) {
-  return NSTAGE * 2 * half_slot_bytes<FMT, D>() + 8 * NSTAGE + align16(4 * NSTAGE) + 16 * GS * 4 +
-         16 * GS * 4 + (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
+  return NSTAGE * Fmt<FMT>::kPPI * 2 * half_slot_bytes<FMT, D>() + 8 * NSTAGE +
+         align16(4 * NSTAGE * Fmt<FMT>::kPPI) + 16 * GS * 4 + 16 * GS * 4 + (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
 }
 template <int FMT, int D, int W, int NSTAGE>
 __host__ __device__ constexpr int cta_smem_bytes(int GS) {
   return align16(D * GS * 4) + W * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ----------------------------------------------------------------------------- fragment builders
-// Each returns the four A registers (f16x2) of step s for this lane.
+// Each builds the four A registers (f16x2) of step s for this lane.
 
 // CB2, K role: channels x = 16s + 2q, y = x + 1 (and +8); tokens g, g + 8.
 template <int D>
@@ -120,8 +130,7 @@ __device__ __forceinline__ void fp8_frag(uint2 wd, uint32_t (&a)[4]) {
 }
 
 // E2M1 codes: slot k = nibble k of the lane's u32 for step s; register i holds
-// slots 2i, 2i+1 = byte i.  sc01 / sc23: f16x2 scales for registers 0,1 / 2,3
-// (K: {s_g, s_g} / {s_g8, s_g8} interleaved per register; see callers).
+// slots 2i, 2i+1 = byte i.
 __device__ __forceinline__ void e2m1_frag(uint32_t wd, uint32_t (&a)[4]) {
   a[0] = e2m1x2_to_f16x2(wd & 0xFFu);
   a[1] = e2m1x2_to_f16x2((wd >> 8) & 0xFFu);
@@ -132,15 +141,15 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t x, uint32_t y) {
   return h2_as_u32(__hmul2(u32_as_h2(x), u32_as_h2(y)));
 }
 
-// INT4 codes: x = q * S + m in fp32 (per token, group of 32), split into an
-// fp16 high part and an fp16 residual so the tensor-core product keeps ~22 bits.
-// Register r holds slots 2r, 2r+1 (nibbles 2r, 2r+1 of the step's u32).
+// fp32 pair -> fp16 high part and fp16 residual (together ~22 bits).
 __device__ __forceinline__ void split_hilo(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   __half2 h = __floats2half2_rn(x0, x1);
   float2 hf = __half22float2(h);
   hi = h2_as_u32(h);
   lo = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
 }
+// INT4 codes: x = q * S + m in fp32 (per token, group of 32), as fp16 hi + lo.
+// Register r holds slots 2r, 2r+1 (nibbles 2r, 2r+1 of the step's u32).
 __device__ __forceinline__ float nib(uint32_t wd, int k) { return (float)((wd >> (4 * k)) & 0xFu); }
 // K role: registers 0, 2 are token g (S0, M0); registers 1, 3 token g + 8 (S1, M1).
 __device__ __forceinline__ void int4_k_frag(uint32_t wd, float S0, float M0, float S1, float M1,
@@ -159,34 +168,6 @@ __device__ __forceinline__ void int4_v_frag(uint32_t wd, const float (&S)[4], co
   split_hilo(fmaf(nib(wd, 6), S[2], M[2]), fmaf(nib(wd, 7), S[3], M[3]), ahi[3], alo[3]);
 }
 
-// ----------------------------------------------------------------------------- outlier side-list helpers
-// Inclusive prefix sums of 16 per-token counts held in four u32 words, one byte
-// per token (sums stay below 256: at most 16 * 14 entries).
-struct CountPrefix {
-  uint32_t p[4];
-  int total;
-};
-__device__ __forceinline__ CountPrefix count_prefix(uint4 c) {
-  CountPrefix r;
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-  uint32_t carry = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    r.p[i] = (w[i] + carry) * 0x01010101u;  // byte j: carry + counts 0..j of this word
-    carry = r.p[i] >> 24;
-  }
-  r.total = (int)carry;
-  return r;
-}
-// Token holding entry e (entries are sorted by token): number of tokens whose
-// inclusive prefix is <= e.
-__device__ __forceinline__ int token_of(const CountPrefix& cp, int e) {
-  const uint32_t eb = (uint32_t)e * 0x01010101u;
-  int t = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) t += __popc(__vcmpleu4(cp.p[i], eb)) >> 3;
-  return t;
-}
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return __low2float(u32_as_h2(e4m3x2_to_f16x2(byte & 0xFFu)));
 }
@@ -194,35 +175,154 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
   return __half2float(__ushort_as_half((unsigned short)(bits & 0xFFFFu)));
 }
 
+// ----------------------------------------------------------------------------- CB2 outlier corrections
+// Side-list of a CB2 block (at 12D): {u8 n_ch, u8 total, 0, 0}, n_ch records
+// {u8 channel, 0, u16 token mask}, then a 16 x R matrix (R = n_ch rounded up
+// to even) of e4m3 values, 0 where a token is not an outlier of the channel:
+// token-major (t*R + i) in K blocks, channel-major (16*i + t) in V blocks.
+// A code slot holding an outlier stores code 0 (value c0 of its channel), so
+// the correction of a channel is sum over its outliers of (x - c0); both x
+// (e4m3) and c0 (fp16) are exact in fp16, so it is computed as two mma with
+// exact operands: + values, - c0 where flagged.
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+// -c0 of channel ch (fp16 bits) from the codebook slot `slot` of a block.
+template <int D>
+__device__ __forceinline__ uint32_t neg_c0_bits(const uint8_t* blk, int slot) {
+  const uint8_t* p = blk + cb2_cb_off(D) + 8 * slot;
+  return (p[0] | (p[4] << 8)) ^ 0x8000u;
+}
+// 0xFFFF in each half whose token bit is set: half 0 <- bit t0 of m0, half 1 <- bit t1 of m1.
+__device__ __forceinline__ uint32_t half_mask(uint32_t m0, int t0, uint32_t m1, int t1) {
+  return (0u - ((m0 >> t0) & 1u)) & 0xFFFFu | ((0u - ((m1 >> t1) & 1u)) & 0xFFFF0000u);
+}
+
+// Scores of tokens g, g+8: += sum over outlier channels c of q[h][c] * (x - c0[c]).
+// Channels go 16 at a time into one k16 tile (A = tokens x slots), B = Q^T
+// gathered at the slots' channels.  hdr may live in shared or global memory.
+template <int D, int NT>
+__device__ __forceinline__ void cb2_k_correct(const uint8_t* hdr, const uint8_t* kb, const float* qsm, int G, int GS,
+                                              int lane, float (&acc)[NT][4]) {
+  const int g = lane >> 2, q4 = lane & 3;
+  const int n_ch = min((int)hdr[0], D), R = n_ch + (n_ch & 1);
+  const uint8_t* vals = hdr + 4 + 4 * n_ch;
+  for (int base = 0; base < n_ch; base += 16) {
+    const int ia = base + 2 * q4, ib = ia + 8;  // slots ia, ia+1 (A cols of a0/a1), ib, ib+1 (a2/a3)
+    uint32_t rec[4];
+    rec[0] = ia < n_ch ? ld_u32(hdr + 4 + 4 * ia) : 0u;
+    rec[1] = ia + 1 < n_ch ? ld_u32(hdr + 8 + 4 * ia) : 0u;
+    rec[2] = ib < n_ch ? ld_u32(hdr + 4 + 4 * ib) : 0u;
+    rec[3] = ib + 1 < n_ch ? ld_u32(hdr + 8 + 4 * ib) : 0u;
+    // + outlier values (pairs of adjacent slots at one token; the pad column is 0)
+    uint32_t ax[4];
+    ax[0] = ia < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + g * R + ia)) : 0u;
+    ax[1] = ia < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + (g + 8) * R + ia)) : 0u;
+    ax[2] = ib < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + g * R + ib)) : 0u;
+    ax[3] = ib < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + (g + 8) * R + ib)) : 0u;
+    // - c0 where the token is an outlier of the slot's channel
+    const uint32_t m0 = rec[0] >> 16, m1 = rec[1] >> 16, m2 = rec[2] >> 16, m3 = rec[3] >> 16;
+    const uint32_t c01 = neg_c0_bits<D>(kb, rec[0] & (D - 1)) | (neg_c0_bits<D>(kb, rec[1] & (D - 1)) << 16);
+    const uint32_t c23 = neg_c0_bits<D>(kb, rec[2] & (D - 1)) | (neg_c0_bits<D>(kb, rec[3] & (D - 1)) << 16);
+    const uint32_t ac0 = c01 & half_mask(m0, g, m1, g), ac1 = c01 & half_mask(m0, g + 8, m1, g + 8);
+    const uint32_t ac2 = c23 & half_mask(m2, g, m3, g), ac3 = c23 & half_mask(m2, g + 8, m3, g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + g;
+      float qv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qv[k] = (h < G && rec[k]) ? qsm[(rec[k] & (D - 1)) * GS + h] : 0.f;
+      const uint32_t b0 = h2_as_u32(__floats2half2_rn(qv[0], qv[1]));
+      const uint32_t b1 = h2_as_u32(__floats2half2_rn(qv[2], qv[3]));
+      mma16816(acc[nt], ax[0], ax[1], ax[2], ax[3], b0, b1);
+      mma16816(acc[nt], ac0, ac1, ac2, ac3, b0, b1);
+    }
+  }
+}
+
+// Output correction of the outlier channels: corr[c][h] += sum_t p[t][h] * (x - c0[c]).
+// A = (slots x tokens) against the page's P^T fragments; each (channel, head)
+// is written by exactly one lane.
+template <int D, int NT>
+__device__ __forceinline__ void cb2_v_correct(const uint8_t* hdr, const uint8_t* vb, const uint32_t (&phi)[NT][2],
+                                              const uint32_t (&plo)[NT][2], float* corr, int G, int GS, int lane) {
+  const int g = lane >> 2, q4 = lane & 3;
+  const int n_ch = min((int)hdr[0], D);
+  const uint8_t* vals = hdr + 4 + 4 * n_ch;
+  const int t0 = 2 * q4;
+  for (int base = 0; base < n_ch; base += 16) {
+    const int i0 = base + g, i1 = i0 + 8;
+    const uint32_t r0 = i0 < n_ch ? ld_u32(hdr + 4 + 4 * i0) : 0u;
+    const uint32_t r1 = i1 < n_ch ? ld_u32(hdr + 4 + 4 * i1) : 0u;
+    const int ch0 = r0 & (D - 1), ch1 = r1 & (D - 1);
+    uint32_t ax[4];
+    ax[0] = r0 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i0 + t0)) : 0u;
+    ax[1] = r1 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i1 + t0)) : 0u;
+    ax[2] = r0 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i0 + t0 + 8)) : 0u;
+    ax[3] = r1 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i1 + t0 + 8)) : 0u;
+    const uint32_t m0 = r0 >> 16, m1 = r1 >> 16;
+    const uint32_t c0 = neg_c0_bits<D>(vb, cb2_slot(1, ch0)) * 0x00010001u;
+    const uint32_t c1 = neg_c0_bits<D>(vb, cb2_slot(1, ch1)) * 0x00010001u;
+    const uint32_t ac0 = c0 & half_mask(m0, t0, m0, t0 + 1), ac1 = c1 & half_mask(m1, t0, m1, t0 + 1);
+    const uint32_t ac2 = c0 & half_mask(m0, t0 + 8, m0, t0 + 9), ac3 = c1 & half_mask(m1, t0 + 8, m1, t0 + 9);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(c, ax[0], ax[1], ax[2], ax[3], phi[nt][0], phi[nt][1]);
+      mma16816(c, ax[0], ax[1], ax[2], ax[3], plo[nt][0], plo[nt][1]);
+      mma16816(c, ac0, ac1, ac2, ac3, phi[nt][0], phi[nt][1]);
+      mma16816(c, ac0, ac1, ac2, ac3, plo[nt][0], plo[nt][1]);
+      const int h0 = nt * 8 + 2 * q4;
+      if (r0) {
+        if (h0 < G) corr[ch0 * GS + h0] += c[0];
+        if (h0 + 1 < G) corr[ch0 * GS + h0 + 1] += c[1];
+      }
+      if (r1) {
+        if (h0 < G) corr[ch1 * GS + h0] += c[2];
+        if (h0 + 1 < G) corr[ch1 * GS + h0 + 1] += c[3];
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------- online softmax
-// acc[nt][r]: scores in log2 units for token g (r < 2) / g + 8 (r >= 2) and head
-// nt*8 + 2q + (r & 1).  Replaces them with p = 2^(s - m) (0 for tokens >= ntok),
-// updates the running max m (raised only when a score exceeds it by more than
-// kRescaleTh, so most pages skip the rescale) and the per-lane partial sums l.
-// Returns whether any lane changed its max; alpha holds the rescale factors.
-template <int NT>
-__device__ __forceinline__ bool online_softmax(float (&acc)[NT][4], int ntok, int g, float (&m)[NT][2],
-                                               float (&l)[NT][2], float (&alpha)[NT][2]) {
-  const bool v0 = g < ntok, v1 = g + 8 < ntok;
+// acc[p][nt][r]: scores in log2 units of page p for token g (r < 2) / g + 8
+// (r >= 2) and head nt*8 + 2q + (r & 1).  Replaces them with p = 2^(s - m) (0
+// for tokens >= ntok[p]), raises the running max m only when a score exceeds
+// it by more than kRescaleTh (so most pages skip the rescale), and updates the
+// per-lane partial sums l.  Returns whether any lane changed its max (alpha
+// holds the factors).
+template <int PPI, int NT>
+__device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const int (&ntok)[PPI], int g,
+                                               float (&m)[NT][2], float (&l)[NT][2], float (&alpha)[NT][2]) {
   bool any = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float mx = fmaxf(v0 ? acc[nt][j] : -INFINITY, v1 ? acc[nt][2 + j] : -INFINITY);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int p = 0; p < PPI; ++p) {
+        mx = fmaxf(mx, g < ntok[p] ? acc[p][nt][j] : -INFINITY);
+        mx = fmaxf(mx, g + 8 < ntok[p] ? acc[p][nt][2 + j] : -INFINITY);
+      }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const bool need = mx > m[nt][j] + kRescaleTh;
       const float mn = need ? mx : m[nt][j];
-      alpha[nt][j] = need ? exp2f(m[nt][j] - mn) : 1.f;
+      alpha[nt][j] = need ? ex2(m[nt][j] - mn) : 1.f;
       m[nt][j] = mn;
       any |= need;
-      const float p0 = v0 ? exp2f(acc[nt][j] - mn) : 0.f;
-      const float p1 = v1 ? exp2f(acc[nt][2 + j] - mn) : 0.f;
-      acc[nt][j] = p0;
-      acc[nt][2 + j] = p1;
-      l[nt][j] = l[nt][j] * alpha[nt][j] + p0 + p1;
+      float sum = 0.f;
+#pragma unroll
+      for (int p = 0; p < PPI; ++p) {
+        const float p0 = g < ntok[p] ? ex2(acc[p][nt][j] - mn) : 0.f;
+        const float p1 = g + 8 < ntok[p] ? ex2(acc[p][nt][2 + j] - mn) : 0.f;
+        acc[p][nt][j] = p0;
+        acc[p][nt][2 + j] = p1;
+        sum += p0 + p1;
+      }
+      l[nt][j] = l[nt][j] * alpha[nt][j] + sum;
     }
   }
   return __any_sync(0xffffffffu, any);
@@ -252,9 +352,9 @@ __device__ __forceinline__ void rescale_state(float (&o)[NT][D / 16][4], const f
   }
 }
 
-// P (fp32, score layout) -> B fragments of P^T for the PV mma, as an fp16 high
-// part and an fp16 residual.  Lane (g, q) needs P[token 2q, 2q+1 (+8)][head g];
-// those sit in lanes 8q + g/2 and 8q + g/2 + 4.
+// P (fp32, score layout) -> B fragments of P^T for the PV mma, as fp16 hi and
+// lo parts.  Lane (g, q) needs P[token 2q, 2q+1 (+8)][head g]; those sit in
+// lanes 8q + g/2 and 8q + g/2 + 4.
 template <int NT>
 __device__ __forceinline__ void p_frags(const float (&p)[NT][4], int g, int q4, uint32_t (&phi)[NT][2],
                                         uint32_t (&plo)[NT][2]) {
@@ -272,7 +372,7 @@ __device__ __forceinline__ void p_frags(const float (&p)[NT][4], int g, int q4, 
   }
 }
 
-// Store p into psm[t][h] (for the V outlier correction and the fp32 tail).
+// Store p into psm[t][h] (INT4 outlier corrections and the fp32 tail).
 template <int NT>
 __device__ __forceinline__ void store_p(const float (&p)[NT][4], float* psm, int G, int GS, int g, int q4) {
 #pragma unroll
@@ -287,7 +387,7 @@ __device__ __forceinline__ void store_p(const float (&p)[NT][4], float* psm, int
     }
 }
 
-// Add the K-outlier score corrections ds[t][h] to the lane's scores and clear them.
+// Add the INT4 K-outlier score corrections ds[t][h] to the lane's scores and clear them.
 template <int NT>
 __device__ __forceinline__ void apply_ds(float (&acc)[NT][4], float* ds, int G, int GS, int g, int q4) {
   __syncwarp();
@@ -305,8 +405,22 @@ __device__ __forceinline__ void apply_ds(float (&acc)[NT][4], float* ds, int G, 
     }
 }
 
-// ----------------------------------------------------------------------------- per-page processing
-// Per-warp state and the shared-memory scratch of one warp.
+// Total per-token counts of tokens < ntok (16 count bytes at p).
+__device__ __forceinline__ int masked_count_total(const uint8_t* p, int ntok) {
+  int tot = 0;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) tot += t < ntok ? p[t] : 0;
+  return tot;
+}
+
+// Zero V^T fragment halves of tokens >= ntok (stale slots of a partial page).
+__device__ __forceinline__ void mask_v_tokens(uint32_t (&a)[4], int ntok, int q4) {
+  const int t0 = 2 * q4;
+  const uint32_t m01 = (t0 < ntok ? 0xFFFFu : 0u) | (t0 + 1 < ntok ? 0xFFFF0000u : 0u);
+  const uint32_t m23 = (t0 + 8 < ntok ? 0xFFFFu : 0u) | (t0 + 9 < ntok ? 0xFFFF0000u : 0u);
+  a[0] &= m01; a[1] &= m01; a[2] &= m23; a[3] &= m23;
+}
+
 template <int D, int NT>
 struct WarpState {
   float o[NT][D / 16][4];   // O^T accumulators: rows channel 16s+g (+8), cols head nt*8+2q (+1)
@@ -315,58 +429,22 @@ struct WarpState {
 };
 struct WarpSmem {
   const float* qsm;  // [D][GS] fp32 query of the CTA's G heads
-  float* ds;         // [16][GS] K-outlier score corrections of the current page
-  float* psm;        // [16][GS] probabilities of the current page
+  float* ds;         // [16][GS] INT4 K-outlier score corrections of the current page
+  float* psm;        // [16][GS] probabilities of the current page (INT4, fp32 tail)
   float* corr;       // [D][GS] V-outlier output correction (rescaled with o)
   int G, GS;
 };
 
-template <int D, int NT, bool kCorr>
-__device__ __forceinline__ void softmax_and_frags(WarpState<D, NT>& st, float (&acc)[NT][4], int ntok, float scale,
-                                                  const WarpSmem& sm, int lane, uint32_t (&phi)[NT][2],
-                                                  uint32_t (&plo)[NT][2]) {
-  const int g = lane >> 2, q4 = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[nt][r] *= scale;
-  float alpha[NT][2];
-  if (online_softmax<NT>(acc, ntok, g, st.m, st.l, alpha))
-    rescale_state<D, NT, kCorr>(st.o, alpha, sm.corr, sm.G, sm.GS, lane);
-  p_frags<NT>(acc, g, q4, phi, plo);
-}
+// ----------------------------------------------------------------------------- per-iteration processing
+constexpr int32_t kBadEntry = 0x7FFFFFFF;  // page-table entry that failed validation
+constexpr int32_t kNoPage = 0x7FFFFFFE;    // stage slot past the warp's last page
 
-// K outliers of a CB2 block: scores[t][h] += q[h][c] * (x - c0[c]).
-template <int D>
-__device__ __forceinline__ void cb2_k_outliers(const uint8_t* kb, const uint8_t* kglob, int ent_prefetch,
-                                               const WarpSmem& sm, int lane, bool& any) {
-  CountPrefix cp = count_prefix(*reinterpret_cast<const uint4*>(kb + cb2_cnt_off(D)));
-  cp.total = min(cp.total, 16 * kmax_outliers(D));  // a corrupt side-list never reads past its block
-  any = cp.total > 0;
-  for (int e = lane; e < cp.total; e += 32) {
-    const uint32_t ent = e < ent_prefetch ? *reinterpret_cast<const uint16_t*>(kb + cb2_ent_off(D) + 2 * e)
-                                          : __ldg(reinterpret_cast<const uint16_t*>(kglob + cb2_ent_off(D) + 2 * e));
-    const int t = min(token_of(cp, e), kPage - 1), ch = ent & (D - 1);
-    const uint8_t* cbp = kb + cb2_cb_off(D) + 8 * ch;  // K codebook slot = channel
-    const float c0 = fp16_bits_to_float(cbp[0] | (cbp[4] << 8));
-    const float delta = e4m3_to_float(ent >> 8) - c0;
-    for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.ds[t * sm.GS + h], sm.qsm[ch * sm.GS + h] * delta);
-  }
-}
-
-// V outliers of a CB2 block: corr[c][h] += p[t][h] * (x - c0[c]).  psm must hold p.
-template <int D>
-__device__ __forceinline__ void cb2_v_outliers(const uint8_t* vb, const uint8_t* vglob, int ent_prefetch,
-                                               const CountPrefix& cp, const WarpSmem& sm, int lane) {
-  for (int e = lane; e < cp.total; e += 32) {
-    const uint32_t ent = e < ent_prefetch ? *reinterpret_cast<const uint16_t*>(vb + cb2_ent_off(D) + 2 * e)
-                                          : __ldg(reinterpret_cast<const uint16_t*>(vglob + cb2_ent_off(D) + 2 * e));
-    const int t = min(token_of(cp, e), kPage - 1), ch = ent & (D - 1);
-    const uint8_t* cbp = vb + cb2_cb_off(D) + 8 * cb2_slot(1, ch);
-    const float c0 = fp16_bits_to_float(cbp[0] | (cbp[4] << 8));
-    const float delta = e4m3_to_float(ent >> 8) - c0;
-    for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.corr[ch * sm.GS + h], sm.psm[t * sm.GS + h] * delta);
-  }
+template <int FMT, int D>
+__device__ __forceinline__ const uint8_t* block_src(const DecodeArgs& a, int kvh, int32_t e, int role) {
+  const uint32_t u = (uint32_t)e, phys = u & 0x7FFFFFFFu;
+  if (FMT == KVQ_FMT_TIERED && (u >> 31))
+    return a.tier_pool + (((size_t)phys * a.Hkv + kvh) * 2 + role) * block_stride(kBlkFp8, D);
+  return a.pool + (((size_t)phys * a.Hkv + kvh) * 2 + role) * block_stride(Fmt<FMT>::kMain, D);
 }
 
 template <int D>
@@ -380,156 +458,180 @@ __device__ __forceinline__ void load_codes(const uint8_t* p, uint32_t (&w)[D / 3
   }
 }
 
-// One CB2 page (K block kb, V block vb in shared memory; kglob/vglob the same
-// blocks in global memory for entries beyond the prefetched ones).
-template <int D, int NT>
-__device__ __forceinline__ void page_cb2(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
-                                         const uint8_t* vb, const uint8_t* kglob, const uint8_t* vglob,
-                                         int ent_prefetch, float scale, const WarpSmem& sm, int lane) {
+template <int D, int NT, int PPI>
+__device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)[PPI][NT][4], const int (&ntok)[PPI],
+                                              float scale, const WarpSmem& sm, int lane, bool corr,
+                                              uint32_t (&phi)[PPI][NT][2], uint32_t (&plo)[PPI][NT][2]) {
+  const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+  for (int p = 0; p < PPI; ++p)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[p][nt][r] *= scale;
+  float alpha[NT][2];
+  if (online_softmax<PPI, NT>(acc, ntok, g, st.m, st.l, alpha)) {
+    if (corr) rescale_state<D, NT, true>(st.o, alpha, sm.corr, sm.G, sm.GS, lane);
+    else rescale_state<D, NT, false>(st.o, alpha, sm.corr, sm.G, sm.GS, lane);
+  }
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
+}
+
+// CB2 pages (and, for the tiered format, FP8 tier pages), PPI at a time.
+template <int FMT, int D, int NT, int PPI>
+__device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
+                                         const uint8_t* const (&kb)[PPI], const uint8_t* const (&vb)[PPI],
+                                         const int32_t (&ent)[PPI], const int (&ntok)[PPI], const DecodeArgs& a,
+                                         int kvh, const WarpSmem& sm, int lane) {
+  constexpr int NS = D / 16;
+  constexpr bool T = FMT == KVQ_FMT_TIERED;
+  const int g = lane >> 2, q4 = lane & 3;
+  bool tier[PPI];
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) tier[p] = T && ent[p] < 0;
+
+  float acc[PPI][NT][4];
+  uint32_t kc[PPI][NS / 2];
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
+    load_codes<D>(kb[p] + 2 * NS * lane, kc[p]);
+  }
+#pragma unroll
+  for (int s = 0; s < NS; ++s)
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) {
+      uint32_t ak[4];
+      if (T && tier[p]) fp8_frag(*reinterpret_cast<const uint2*>(kb[p] + 8 * NS * lane + 8 * s), ak);
+      else cb2_k_frag<D>(kb[p], (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, q4, ak);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
+    }
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    if (T && tier[p]) {
+      const float sk = *reinterpret_cast<const float*>(kb[p] + fp8_sc_off(D));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
+    } else if (ntok[p] > 0) {
+      const uint8_t* hdr = kb[p] + cb2_out_off(D);
+      if (hdr[0] > 0) {
+        const int nc = min((int)hdr[0], D), sz = 4 + 4 * nc + 16 * (nc + (nc & 1));
+        if (sz > kOutPrefetch) hdr = block_src<FMT, D>(a, kvh, ent[p], 0) + cb2_out_off(D);
+        cb2_k_correct<D, NT>(hdr, kb[p], sm.qsm, sm.G, sm.GS, lane, acc[p]);
+      }
+    }
+  }
+
+  uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
+  softmax_frags<D, NT, PPI>(st, acc, ntok, a.scale_log2, sm, lane, true, phi, plo);
+
+  uint32_t vc[PPI][NS / 2];
+  float sv[PPI];
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    load_codes<D>(vb[p] + 2 * NS * lane, vc[p]);
+    sv[p] = (T && tier[p]) ? *reinterpret_cast<const float*>(vb[p] + fp8_sc_off(D)) : 1.f;
+  }
+#pragma unroll
+  for (int s = 0; s < NS; ++s)
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) {
+      uint32_t av[4];
+      if (T && tier[p]) {
+        fp8_frag(*reinterpret_cast<const uint2*>(vb[p] + 8 * NS * lane + 8 * s), av);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float t4[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(t4, av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
+          mma16816(t4, av[0], av[1], av[2], av[3], plo[p][nt][0], plo[p][nt][1]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) st.o[nt][s][r] = fmaf(sv[p], t4[r], st.o[nt][s][r]);
+        }
+      } else {
+        cb2_v_frag<D>(vb[p], (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, g, av);
+        if (ntok[p] < 16) mask_v_tokens(av, ntok[p], q4);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
+          mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], plo[p][nt][0], plo[p][nt][1]);
+        }
+      }
+    }
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    if (!(T && tier[p]) && ntok[p] > 0) {
+      const uint8_t* hdr = vb[p] + cb2_out_off(D);
+      if (hdr[0] > 0) {
+        const int nc = min((int)hdr[0], D), sz = 4 + 4 * nc + 16 * (nc + (nc & 1));
+        if (sz > kOutPrefetch) hdr = block_src<FMT, D>(a, kvh, ent[p], 1) + cb2_out_off(D);
+        cb2_v_correct<D, NT>(hdr, vb[p], phi[p], plo[p], sm.corr, sm.G, sm.GS, lane);
+        __syncwarp();
+      }
+    }
+  }
+}
+
+// E2M1 pages (per-token format: the last page may hold fewer than 16 tokens).
+template <int D, int NT, int PPI>
+__device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
+                                          const uint8_t* const (&kb)[PPI], const uint8_t* const (&vb)[PPI],
+                                          const int (&ntok)[PPI], float scale, const WarpSmem& sm, int lane) {
   constexpr int NS = D / 16;
   const int g = lane >> 2, q4 = lane & 3;
-  float acc[NT][4];
+  float acc[PPI][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  uint32_t kc[NS / 2];
-  load_codes<D>(kb + 2 * NS * lane, kc);
+  for (int p = 0; p < PPI; ++p)
 #pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    cb2_k_frag<D>(kb, (s & 1) ? (kc[s >> 1] >> 16) : kc[s >> 1], s, q4, a);
+    for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
-  }
-  bool any_k;
-  cb2_k_outliers<D>(kb, kglob, ent_prefetch, sm, lane, any_k);
-  if (any_k) apply_ds<NT>(acc, sm.ds, sm.G, sm.GS, g, q4);
-
-  uint32_t phi[NT][2], plo[NT][2];
-  softmax_and_frags<D, NT, true>(st, acc, 16, scale, sm, lane, phi, plo);
-
-  uint32_t vc[NS / 2];
-  load_codes<D>(vb + 2 * NS * lane, vc);
+  for (int s = 0; s < NS; ++s)
 #pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    cb2_v_frag<D>(vb, (s & 1) ? (vc[s >> 1] >> 16) : vc[s >> 1], s, g, a);
+    for (int p = 0; p < PPI; ++p) {
+      uint32_t ak[4];
+      e2m1_frag(*reinterpret_cast<const uint32_t*>(kb[p] + 4 * NS * lane + 4 * s), ak);
+      const uint8_t* sc = kb[p] + e2m1_sc_off(D) + 16 * s;
+      const uint32_t sgs = e4m3x2_to_f16x2(sc[g] | (sc[g + 8] << 8));  // {s_g, s_g+8}
+      const uint32_t s0 = prmt(sgs, sgs, 0x1010u), s1 = prmt(sgs, sgs, 0x3232u);
+      ak[0] = hmul2u(ak[0], s0); ak[1] = hmul2u(ak[1], s1); ak[2] = hmul2u(ak[2], s0); ak[3] = hmul2u(ak[3], s1);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      mma16816(st.o[nt][s], a[0], a[1], a[2], a[3], phi[nt][0], phi[nt][1]);
-      mma16816(st.o[nt][s], a[0], a[1], a[2], a[3], plo[nt][0], plo[nt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
     }
-  }
-  CountPrefix cpv = count_prefix(*reinterpret_cast<const uint4*>(vb + cb2_cnt_off(D)));
-  cpv.total = min(cpv.total, 16 * kmax_outliers(D));
-  if (cpv.total > 0) {
-    store_p<NT>(acc, sm.psm, sm.G, sm.GS, g, q4);
-    __syncwarp();
-    cb2_v_outliers<D>(vb, vglob, ent_prefetch, cpv, sm, lane);
-  }
-}
-
-// One FP8 tier page: e4m3 codes, one fp32 scale per block (scores and PV scaled in fp32).
-template <int D, int NT, bool kCorr>
-__device__ __forceinline__ void page_fp8(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
-                                         const uint8_t* vb, float scale, const WarpSmem& sm, int lane) {
-  constexpr int NS = D / 16;
-  float acc[NT][4];
+  uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
+  softmax_frags<D, NT, PPI>(st, acc, ntok, scale, sm, lane, false, phi, plo);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  for (int s = 0; s < NS; ++s)
 #pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    fp8_frag(*reinterpret_cast<const uint2*>(kb + 8 * NS * lane + 8 * s), a);
+    for (int p = 0; p < PPI; ++p) {
+      uint32_t av[4];
+      e2m1_frag(*reinterpret_cast<const uint32_t*>(vb[p] + 4 * NS * lane + 4 * s), av);
+      const uint8_t* sc = vb[p] + e2m1_sc_off(D) + 16 * s + 2 * q4;
+      const uint32_t s01 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc));
+      const uint32_t s23 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + 8));
+      av[0] = hmul2u(av[0], s01); av[1] = hmul2u(av[1], s01); av[2] = hmul2u(av[2], s23); av[3] = hmul2u(av[3], s23);
+      if (ntok[p] < 16) mask_v_tokens(av, ntok[p], q4);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
-  }
-  const float sk = *reinterpret_cast<const float*>(kb + fp8_sc_off(D));
-  const float sv = *reinterpret_cast<const float*>(vb + fp8_sc_off(D));
-  uint32_t phi[NT][2], plo[NT][2];
-  softmax_and_frags<D, NT, kCorr>(st, acc, 16, scale * sk, sm, lane, phi, plo);
-#pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    fp8_frag(*reinterpret_cast<const uint2*>(vb + 8 * NS * lane + 8 * s), a);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float t4[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(t4, a[0], a[1], a[2], a[3], phi[nt][0], phi[nt][1]);
-      mma16816(t4, a[0], a[1], a[2], a[3], plo[nt][0], plo[nt][1]);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) st.o[nt][s][r] = fmaf(sv, t4[r], st.o[nt][s][r]);
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
+        mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], plo[p][nt][0], plo[p][nt][1]);
+      }
     }
-  }
-}
-
-// Zero V^T fragment halves of tokens >= ntok (stale slots of a partial page).
-__device__ __forceinline__ void mask_v_tokens(uint32_t (&a)[4], int ntok, int q4) {
-  const int t0 = 2 * q4;
-  const uint32_t m01 = (t0 < ntok ? 0xFFFFu : 0u) | (t0 + 1 < ntok ? 0xFFFF0000u : 0u);
-  const uint32_t m23 = (t0 + 8 < ntok ? 0xFFFFu : 0u) | (t0 + 9 < ntok ? 0xFFFF0000u : 0u);
-  a[0] &= m01; a[1] &= m01; a[2] &= m23; a[3] &= m23;
-}
-
-// One E2M1 page (per-token format: the last page may hold ntok < 16 tokens).
-template <int D, int NT>
-__device__ __forceinline__ void page_e2m1(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
-                                          const uint8_t* vb, int ntok, float scale, const WarpSmem& sm, int lane) {
-  constexpr int NS = D / 16;
-  const int g = lane >> 2, q4 = lane & 3;
-  float acc[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    e2m1_frag(*reinterpret_cast<const uint32_t*>(kb + 4 * NS * lane + 4 * s), a);
-    const uint8_t* sc = kb + e2m1_sc_off(D) + 16 * s;
-    const uint32_t sgs = e4m3x2_to_f16x2(sc[g] | (sc[g + 8] << 8));   // {s_g, s_g+8}
-    const uint32_t s0 = prmt(sgs, sgs, 0x1010u), s1 = prmt(sgs, sgs, 0x3232u);
-    a[0] = hmul2u(a[0], s0); a[1] = hmul2u(a[1], s1); a[2] = hmul2u(a[2], s0); a[3] = hmul2u(a[3], s1);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
-  }
-  uint32_t phi[NT][2], plo[NT][2];
-  softmax_and_frags<D, NT, false>(st, acc, ntok, scale, sm, lane, phi, plo);
-#pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    uint32_t a[4];
-    e2m1_frag(*reinterpret_cast<const uint32_t*>(vb + 4 * NS * lane + 4 * s), a);
-    const uint8_t* sc = vb + e2m1_sc_off(D) + 16 * s + 2 * q4;
-    const uint32_t s01 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc));
-    const uint32_t s23 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + 8));
-    a[0] = hmul2u(a[0], s01); a[1] = hmul2u(a[1], s01); a[2] = hmul2u(a[2], s23); a[3] = hmul2u(a[3], s23);
-    if (ntok < 16) mask_v_tokens(a, ntok, q4);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      mma16816(st.o[nt][s], a[0], a[1], a[2], a[3], phi[nt][0], phi[nt][1]);
-      mma16816(st.o[nt][s], a[0], a[1], a[2], a[3], plo[nt][0], plo[nt][1]);
-    }
-  }
-}
-
-// Total per-token counts of tokens < ntok (16 count bytes at p).
-__device__ __forceinline__ int masked_count_total(const uint8_t* p, int ntok) {
-  uint4 c = *reinterpret_cast<const uint4*>(p);
-  uint32_t* w = reinterpret_cast<uint32_t*>(&c);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int keep = ntok - 4 * i;
-    w[i] &= keep >= 4 ? 0xFFFFFFFFu : (keep <= 0 ? 0u : ((1u << (8 * keep)) - 1u));
-  }
-  return count_prefix(c).total;
 }
 
 // One INT4 page (per-token format; fp16 outliers in per-token slots).
 template <int D, int NT>
-__device__ __forceinline__ void page_int4(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
-                                          const uint8_t* vb, int ntok, float scale, const WarpSmem& sm, int lane) {
+__device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
+                                          const uint8_t* vb, int ntok_, float scale, const WarpSmem& sm, int lane) {
   constexpr int NS = D / 16, CAP = int4_cap(D), NG = D / 32;
   const int g = lane >> 2, q4 = lane & 3;
-  float acc[NT][4];
+  const int ntok[1] = {ntok_};
+  float acc[1][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) acc[0][nt][0] = acc[0][nt][1] = acc[0][nt][2] = acc[0][nt][3] = 0.f;
 #pragma unroll
   for (int s = 0; s < NS; ++s) {
     const int grp = s >> 1;
@@ -540,25 +642,26 @@ __device__ __forceinline__ void page_int4(WarpState<D, NT>& st, const uint32_t (
                 fp16_bits_to_float(z0 >> 16), fp16_bits_to_float(z1), fp16_bits_to_float(z1 >> 16), ahi, alo);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mma16816(acc[nt], ahi[0], ahi[1], ahi[2], ahi[3], qf[nt][s][0], qf[nt][s][1]);
-      mma16816(acc[nt], alo[0], alo[1], alo[2], alo[3], qf[nt][s][0], qf[nt][s][1]);
+      mma16816(acc[0][nt], ahi[0], ahi[1], ahi[2], ahi[3], qf[nt][s][0], qf[nt][s][1]);
+      mma16816(acc[0][nt], alo[0], alo[1], alo[2], alo[3], qf[nt][s][0], qf[nt][s][1]);
     }
   }
-  // K outliers: scores[t][h] += q[h][c] * (x - m), m = value of code 0 in the group
-  if (masked_count_total(kb + int4_cnt_off(D), ntok) > 0) {
+  // K outliers: scores[t][h] += q[h][c] * (x - m), m = the group's value of code 0
+  if (ntok_ > 0 && masked_count_total(kb + int4_cnt_off(D), ntok_) > 0) {
     for (int e = lane; e < 16 * CAP; e += 32) {
       const int t = e / CAP, i = e - t * CAP;
-      if (t < ntok && i < kb[int4_cnt_off(D) + t]) {
+      if (t < ntok_ && i < kb[int4_cnt_off(D) + t]) {
         const int ch = kb[int4_ch_off(D) + e] & (D - 1);
         const float x = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(kb + int4_val_off(D) + 2 * e));
-        const float mz = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(kb + int4_sz_off(D) + 4 * (t * NG + ch / 32) + 2));
+        const float mz =
+            fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(kb + int4_sz_off(D) + 4 * (t * NG + ch / 32) + 2));
         for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.ds[t * sm.GS + h], sm.qsm[ch * sm.GS + h] * (x - mz));
       }
     }
-    apply_ds<NT>(acc, sm.ds, sm.G, sm.GS, g, q4);
+    apply_ds<NT>(acc[0], sm.ds, sm.G, sm.GS, g, q4);
   }
-  uint32_t phi[NT][2], plo[NT][2];
-  softmax_and_frags<D, NT, true>(st, acc, ntok, scale, sm, lane, phi, plo);
+  uint32_t phi[1][NT][2], plo[1][NT][2];
+  softmax_frags<D, NT, 1>(st, acc, ntok, scale, sm, lane, true, phi, plo);
 #pragma unroll
   for (int s = 0; s < NS; ++s) {
     const int grp = s >> 1;
@@ -572,29 +675,31 @@ __device__ __forceinline__ void page_int4(WarpState<D, NT>& st, const uint32_t (
     }
     uint32_t ahi[4], alo[4];
     int4_v_frag(*reinterpret_cast<const uint32_t*>(vb + 4 * NS * lane + 4 * s), S, M, ahi, alo);
-    if (ntok < 16) {
-      mask_v_tokens(ahi, ntok, q4);
-      mask_v_tokens(alo, ntok, q4);
+    if (ntok_ < 16) {
+      mask_v_tokens(ahi, ntok_, q4);
+      mask_v_tokens(alo, ntok_, q4);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mma16816(st.o[nt][s], ahi[0], ahi[1], ahi[2], ahi[3], phi[nt][0], phi[nt][1]);
-      mma16816(st.o[nt][s], ahi[0], ahi[1], ahi[2], ahi[3], plo[nt][0], plo[nt][1]);
-      mma16816(st.o[nt][s], alo[0], alo[1], alo[2], alo[3], phi[nt][0], phi[nt][1]);
+      mma16816(st.o[nt][s], ahi[0], ahi[1], ahi[2], ahi[3], phi[0][nt][0], phi[0][nt][1]);
+      mma16816(st.o[nt][s], ahi[0], ahi[1], ahi[2], ahi[3], plo[0][nt][0], plo[0][nt][1]);
+      mma16816(st.o[nt][s], alo[0], alo[1], alo[2], alo[3], phi[0][nt][0], phi[0][nt][1]);
     }
   }
-  if (masked_count_total(vb + int4_cnt_off(D), ntok) > 0) {
-    store_p<NT>(acc, sm.psm, sm.G, sm.GS, g, q4);
+  if (ntok_ > 0 && masked_count_total(vb + int4_cnt_off(D), ntok_) > 0) {
+    store_p<NT>(acc[0], sm.psm, sm.G, sm.GS, g, q4);
     __syncwarp();
     for (int e = lane; e < 16 * CAP; e += 32) {
       const int t = e / CAP, i = e - t * CAP;
-      if (t < ntok && i < vb[int4_cnt_off(D) + t]) {
+      if (t < ntok_ && i < vb[int4_cnt_off(D) + t]) {
         const int ch = vb[int4_ch_off(D) + e] & (D - 1);
         const float x = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(vb + int4_val_off(D) + 2 * e));
-        const float mz = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(vb + int4_sz_off(D) + 4 * (t * NG + ch / 32) + 2));
+        const float mz =
+            fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(vb + int4_sz_off(D) + 4 * (t * NG + ch / 32) + 2));
         for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.corr[ch * sm.GS + h], sm.psm[t * sm.GS + h] * (x - mz));
       }
     }
+    __syncwarp();
   }
 }
 
@@ -603,7 +708,7 @@ template <int D, int NT, bool kCorr>
 __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks, const float* vs, int ntail,
                                           float scale, const WarpSmem& sm, int lane) {
   const int g = lane >> 2, q4 = lane & 3;
-  float acc[NT][4];
+  float acc[1][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -612,11 +717,12 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
       float d = 0.f;
       if (t < ntail && h < sm.G)
         for (int c = 0; c < D; ++c) d = fmaf(sm.qsm[c * sm.GS + h], ks[t * D + c], d);
-      acc[nt][r] = d;
+      acc[0][nt][r] = d;
     }
-  uint32_t phi[NT][2], plo[NT][2];
-  softmax_and_frags<D, NT, kCorr>(st, acc, ntail, scale, sm, lane, phi, plo);
-  store_p<NT>(acc, sm.psm, sm.G, sm.GS, g, q4);
+  const int ntok[1] = {ntail};
+  uint32_t phi[1][NT][2], plo[1][NT][2];
+  softmax_frags<D, NT, 1>(st, acc, ntok, scale, sm, lane, kCorr, phi, plo);
+  store_p<NT>(acc[0], sm.psm, sm.G, sm.GS, g, q4);
   __syncwarp();
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -635,15 +741,11 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
 }
 
 // ----------------------------------------------------------------------------- split kernel
-constexpr int32_t kBadEntry = 0x7FFFFFFF;
-
 template <int FMT, int D, int NT, int W, int NSTAGE>
 __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a) {
   using F = Fmt<FMT>;
-  constexpr int NS = D / 16;
+  constexpr int NS = D / 16, PPI = F::kPPI;
   constexpr int HS = half_slot_bytes<FMT, D>();
-  constexpr int kMainStride = block_stride(F::kMain, D);
-  constexpr int kTierStride = block_stride(kBlkFp8, D);
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -654,17 +756,17 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
   float* qsm = reinterpret_cast<float*>(smem);
   uint8_t* wb = smem + align16(D * GS * 4) + w * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
   uint8_t* stages = wb;
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(wb + NSTAGE * 2 * HS);
-  int32_t* meta = reinterpret_cast<int32_t*>(wb + NSTAGE * 2 * HS + 8 * NSTAGE);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(wb + NSTAGE * PPI * 2 * HS);
+  int32_t* meta = reinterpret_cast<int32_t*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE);
   WarpSmem sm;
   sm.qsm = qsm;
-  sm.ds = reinterpret_cast<float*>(wb + NSTAGE * 2 * HS + 8 * NSTAGE + align16(4 * NSTAGE));
+  sm.ds = reinterpret_cast<float*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE + align16(4 * NSTAGE * PPI));
   sm.psm = sm.ds + 16 * GS;
   sm.corr = sm.psm + 16 * GS;
   sm.G = G;
   sm.GS = GS;
 
-  // query of the CTA's G heads, fp32 in shared memory ([D][GS]) and fp16 B fragments in registers
+  // query of the CTA's G heads: fp32 in shared memory ([D][GS]), fp16 B fragments in registers
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
   for (int i = threadIdx.x; i < D * GS; i += W * 32) {
     const int c = i / GS, h = i - c * GS;
@@ -701,7 +803,8 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
   const int p0 = split * a.pps;
   const int p1 = min(p0 + a.pps, n_all);
   const int pq1 = min(p1, nq);
-  const int n_local = pq1 > p0 + w ? (pq1 - p0 - w + W - 1) / W : 0;
+  const int n_local = pq1 > p0 + w ? (pq1 - p0 - w + W - 1) / W : 0;  // this warp's pages
+  const int n_iter = (n_local + PPI - 1) / PPI;
 
   WarpState<D, NT> st;
 #pragma unroll
@@ -712,85 +815,107 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
     st.l[nt][0] = st.l[nt][1] = 0.f;
   }
 
-  // page-table window: lane j holds the entry of this warp's page win_base + j
+  // page-table window: lane j holds the entry of this warp's local page win_base + j
   const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
   int win_base = 0;
   int win = lane < n_local ? pt[p0 + w + lane * W] : 0;
 
-  auto block_src = [&](int32_t e, int role) -> const uint8_t* {
-    const uint32_t u = (uint32_t)e, phys = u & 0x7FFFFFFFu;
-    if (FMT == KVQ_FMT_TIERED && (u >> 31))
-      return a.tier_pool + (((size_t)phys * a.Hkv + kvh) * 2 + role) * kTierStride;
-    return a.pool + (((size_t)phys * a.Hkv + kvh) * 2 + role) * kMainStride;
-  };
-
-  auto issue = [&](int i) {
-    if (i >= n_local) return;
-    if (i - win_base >= 32) {
-      win_base += 32;
-      const int j = win_base + lane;
-      win = j < n_local ? pt[p0 + w + j * W] : 0;
+  // Stage `it` of the ring: the K and V blocks of local pages it*PPI .. it*PPI+PPI-1.
+  auto issue = [&](int it) {
+    if (it >= n_iter) return;
+    const int slot = it % NSTAGE;
+    int32_t ent[PPI];
+#pragma unroll
+    for (int j = 0; j < PPI; ++j) {
+      const int li = it * PPI + j;
+      ent[j] = kNoPage;
+      if (li < n_local) {
+        if (li - win_base >= 32) {
+          win_base += 32;
+          const int jj = win_base + lane;
+          win = jj < n_local ? pt[p0 + w + jj * W] : 0;
+        }
+        ent[j] = __shfl_sync(0xffffffffu, win, li - win_base);
+      }
     }
-    const int32_t e = __shfl_sync(0xffffffffu, win, i - win_base);
     if (lane == 0) {
-      const int slot = i % NSTAGE;
-      const uint32_t u = (uint32_t)e, phys = u & 0x7FFFFFFFu;
-      const bool tier = (u >> 31) != 0;
-      const bool ok = tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
+      uint32_t bytes[PPI], total = 0;
+#pragma unroll
+      for (int j = 0; j < PPI; ++j) {
+        bytes[j] = 0;
+        int32_t m = kNoPage;
+        if (ent[j] != kNoPage) {
+          const uint32_t u = (uint32_t)ent[j], phys = u & 0x7FFFFFFFu;
+          const bool tier = (u >> 31) != 0;
+          const bool ok =
+              tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
+          if (ok) {
+            m = ent[j];
+            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : fetch_bytes<D>(F::kMain);
+          } else {
+            m = kBadEntry;
+            atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+          }
+        }
+        meta[slot * PPI + j] = m;
+        total += 2 * bytes[j];
+      }
       fence_proxy_async();
-      if (!ok) {
-        meta[slot] = kBadEntry;
-        atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+      if (total == 0) {
         mbar_arrive(&mbar[slot]);
       } else {
-        meta[slot] = e;
-        uint32_t bytes;
-        if (tier) bytes = fetch_bytes<D>(kBlkFp8);
-        else if (F::kMain == kBlkCb2) bytes = 12 * D + 16 + 2 * a.ent_prefetch;
-        else bytes = fetch_bytes<D>(F::kMain);
-        uint8_t* dst = stages + slot * 2 * HS;
-        mbar_arrive_expect_tx(&mbar[slot], 2 * bytes);
-        bulk_g2s(dst, block_src(e, 0), bytes, &mbar[slot]);
-        bulk_g2s(dst + HS, block_src(e, 1), bytes, &mbar[slot]);
+        mbar_arrive_expect_tx(&mbar[slot], total);
+#pragma unroll
+        for (int j = 0; j < PPI; ++j)
+          if (bytes[j]) {
+            uint8_t* dst = stages + (slot * PPI + j) * 2 * HS;
+            bulk_g2s(dst, block_src<FMT, D>(a, kvh, ent[j], 0), bytes[j], &mbar[slot]);
+            bulk_g2s(dst + HS, block_src<FMT, D>(a, kvh, ent[j], 1), bytes[j], &mbar[slot]);
+          }
       }
     }
   };
 
 #pragma unroll 1
-  for (int i = 0; i < NSTAGE; ++i) issue(i);
+  for (int it = 0; it < NSTAGE; ++it) issue(it);
 
   bool timed_out = false;
-  int i = 0;
+  int it = 0;
 #pragma unroll 1
-  for (; i < n_local; ++i) {
-    const int slot = i % NSTAGE;
-    const bool ok = mbar_wait_bounded(&mbar[slot], (i / NSTAGE) & 1, kWaitLimitNs);
+  for (; it < n_iter; ++it) {
+    const int slot = it % NSTAGE;
+    const bool ok = mbar_wait_bounded(&mbar[slot], (it / NSTAGE) & 1, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) {
       timed_out = true;
       if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
       break;
     }
-    const int32_t e = meta[slot];
-    if (e != kBadEntry) {
-      const int page = p0 + w + i * W;
-      const uint8_t* kb = stages + slot * 2 * HS;
-      const uint8_t* vb = kb + HS;
-      if (FMT == KVQ_FMT_TIERED && e < 0) {
-        page_fp8<D, NT, true>(st, qf, kb, vb, a.scale_log2, sm, lane);
-      } else if (F::kMain == kBlkCb2) {
-        page_cb2<D, NT>(st, qf, kb, vb, block_src(e, 0), block_src(e, 1), a.ent_prefetch, a.scale_log2, sm, lane);
-      } else if (F::kMain == kBlkE2m1) {
-        page_e2m1<D, NT>(st, qf, kb, vb, min(kPage, L - kPage * page), a.scale_log2, sm, lane);
-      } else {
-        page_int4<D, NT>(st, qf, kb, vb, min(kPage, L - kPage * page), a.scale_log2, sm, lane);
-      }
+    int32_t ent[PPI];
+    int ntok[PPI];
+    const uint8_t* kb[PPI];
+    const uint8_t* vb[PPI];
+#pragma unroll
+    for (int j = 0; j < PPI; ++j) {
+      ent[j] = meta[slot * PPI + j];
+      const int page = p0 + w + (it * PPI + j) * W;
+      ntok[j] = (ent[j] == kBadEntry || ent[j] == kNoPage) ? 0 : (F::kPaged ? kPage : min(kPage, L - kPage * page));
+      kb[j] = stages + (slot * PPI + j) * 2 * HS;
+      vb[j] = kb[j] + HS;
+    }
+    if constexpr (F::kMain == kBlkCb2) {
+      iter_cb2<FMT, D, NT, PPI>(st, qf, kb, vb, ent, ntok, a, kvh, sm, lane);
+    } else if constexpr (F::kMain == kBlkE2m1) {
+      iter_e2m1<D, NT, PPI>(st, qf, kb, vb, ntok, a.scale_log2, sm, lane);
+    } else {
+      iter_int4<D, NT>(st, qf, kb[0], vb[0], ntok[0], a.scale_log2, sm, lane);
     }
     __syncwarp();
-    issue(i + NSTAGE);
+    issue(it + NSTAGE);
   }
   if (timed_out) {
     // let copies still in flight land (bounded) before the CTA can exit
-    for (int j = i; j < min(i + NSTAGE, n_local); ++j) mbar_wait_bounded(&mbar[j % NSTAGE], (j / NSTAGE) & 1, kWaitLimitNs);
+    for (int j = it; j < min(it + NSTAGE, n_iter); ++j)
+      mbar_wait_bounded(&mbar[j % NSTAGE], (j / NSTAGE) & 1, kWaitLimitNs);
   }
 
   // partial last page of a page format, from fp32 staging
@@ -870,10 +995,12 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
   }
 }
 
-
 // ----------------------------------------------------------------------------- launch configuration
 constexpr int kWarps = kWarpsPerCta;
-constexpr int kStages = 3;
+template <int FMT>
+struct Stages {
+  static constexpr int kN = Fmt<FMT>::kPPI == 1 ? 3 : 2;   // ring depth (stages of PPI pages)
+};
 
 struct KernelInfo {
   void* fn;
@@ -883,10 +1010,11 @@ struct KernelInfo {
 
 template <int FMT, int D, int NT>
 static KernelInfo kernel_info(int G) {
+  constexpr int NSTAGE = Stages<FMT>::kN;
   const int GS = (G + 3) & ~3;
-  const size_t plan = cta_smem_bytes<FMT, D, kWarps, kStages>(GS);
+  const size_t plan = cta_smem_bytes<FMT, D, kWarps, NSTAGE>(GS);
   const size_t merge = align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 + 2 * (size_t)kWarps * GS * 4;
-  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps, kStages>), plan > merge ? plan : merge,
+  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps, NSTAGE>), plan > merge ? plan : merge,
           kWarps * 32};
 }
 

@@ -19,7 +19,6 @@ struct DecodeArgs {
   int S, pps;       // splits, pages per split
   int max_seq_len;
   float scale_log2; // softmax_scale * log2(e)
-  int ent_prefetch; // CB2 outlier entries fetched with a block (multiple of 8, <= kEntSmem)
 };
 
 struct AppendArgs {
@@ -37,14 +36,14 @@ struct AppendArgs {
   double sigma;
 };
 
-// Split decode + combine on `st`; out_dtype is KVQ_BF16 or KVQ_F32.
-cudaError_t decode_launch(const DecodeArgs& a, int fmt, int D, void* out, int out_dtype, cudaStream_t st);
+// The split decode kernel, and the combine kernel (out_dtype KVQ_BF16 or KVQ_F32), on `st`.
+cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_t st);
+cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hq, int S, int D, void* out,
+                                  int out_dtype, cudaStream_t st);
 // Resident CTAs per SM of the split kernel for (format, head_dim, G); 0 on error.
 int decode_ctas_per_sm(int fmt, int D, int G);
 // Warps per CTA of the split decode kernel.
 constexpr int kWarpsPerCta = 4;
-// Entries of a CB2 side-list the decode kernel fetches with its block.
-constexpr int kEntPrefetchDefault = 48;
 // Quantize-on-append launches (see kvq_quantize.cu).
 cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
 // Dequantize tokens [t0, t1) of (seq, head, role) to fp32.

@@ -336,17 +336,46 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
       }
     }
-    if (tid < 16) {
-      int e = 0;
-      for (int t = 0; t < tid; ++t) e += cnt[t];
-      uint8_t* ent = blk + cb2_ent_off(D);
-      for (int c = 0; c < D; ++c)
-        if (mask[tid][c]) {
-          ent[2 * e] = (uint8_t)c;
-          ent[2 * e + 1] = f32_to_e4m3(xs[tid][c]);
-          ++e;
-        }
-      blk[cb2_cnt_off(D) + tid] = (uint8_t)cnt[tid];
+    if (tid < 32) {
+      // side-list grouped by channel: lane l owns channels [l*CPL, (l+1)*CPL)
+      constexpr int CPL = D / 32;
+      const int lane = tid;
+      uint32_t tm[CPL];
+      int nch = 0, nval = 0;
+      for (int k = 0; k < CPL; ++k) {
+        const int c = lane * CPL + k;
+        uint32_t m = 0;
+        for (int t = 0; t < 16; ++t) m |= (uint32_t)mask[t][c] << t;
+        tm[k] = m;
+        nch += m != 0;
+        nval += __popc(m);
+      }
+      int ich = nch, ival = nval;
+      for (int d = 1; d < 32; d <<= 1) {
+        const int a1 = __shfl_up_sync(0xffffffffu, ich, d), a2 = __shfl_up_sync(0xffffffffu, ival, d);
+        if (lane >= d) { ich += a1; ival += a2; }
+      }
+      const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
+      const int R = tot_ch + (tot_ch & 1);
+      uint8_t* hdr = blk + cb2_out_off(D);
+      uint8_t* val = hdr + 4 + 4 * tot_ch;   // dense 16 x R values; zeros from the block clear
+      int ci = ich - nch;
+      for (int k = 0; k < CPL; ++k) {
+        if (!tm[k]) continue;
+        const int c = lane * CPL + k;
+        uint8_t* rec = hdr + 4 + 4 * ci;
+        rec[0] = (uint8_t)c;
+        rec[1] = 0;
+        rec[2] = (uint8_t)(tm[k] & 0xFF);
+        rec[3] = (uint8_t)(tm[k] >> 8);
+        for (int t = 0; t < 16; ++t)
+          if (tm[k] >> t & 1u) val[role == 0 ? t * R + ci : ci * 16 + t] = f32_to_e4m3(xs[t][c]);
+        ++ci;
+      }
+      if (lane == 0) {
+        hdr[0] = (uint8_t)tot_ch;
+        hdr[1] = (uint8_t)tot_val;
+      }
     }
     __syncthreads();
     for (int i = tid; i < 32 * NS; i += blockDim.x) {

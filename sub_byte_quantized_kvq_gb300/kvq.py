@@ -46,7 +46,8 @@ class kvq_cache(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
-           "kvq_decode_num_splits", "kvq_decode_attention", "kvq_dequantize", "kvq_status_string", "kvq_version")
+           "kvq_decode_num_splits", "kvq_decode_split", "kvq_decode_combine", "kvq_decode_attention",
+           "kvq_dequantize", "kvq_status_string", "kvq_version")
 
 
 def lib() -> ctypes.CDLL:
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
                 "kvq_quantize_append": (I, [pcfg, pcache, P, P, I, I, P, P]),
                 "kvq_decode_workspace_bytes": (I, [pcfg, I, I, I, ctypes.POINTER(S)]),
                 "kvq_decode_num_splits": (I, [pcfg, I, I, ctypes.POINTER(I)]),
+                "kvq_decode_split": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, S, P]),
+                "kvq_decode_combine": (I, [pcfg, I, I, I, P, S, P, I, P]),
                 "kvq_decode_attention": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P, S, P]),
                 "kvq_dequantize": (I, [pcfg, pcache, I, I, I, I, I, P, P]),
                 "kvq_status_string": (ctypes.c_char_p, [I]),
@@ -177,12 +180,34 @@ def kvq_decode_attention(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
-        nbytes = kvq_decode_workspace_bytes(cache, Hq, max_seq_len, num_splits)
-        workspace = torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+        workspace = alloc_workspace(cache, Hq, max_seq_len, num_splits)
     _check(lib().kvq_decode_attention(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(q), Hq,
                                       float(softmax_scale), max_seq_len, num_splits, _ptr(out), _DTYPE[out.dtype],
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "kvq_decode_attention")
+    return out
+
+
+def alloc_workspace(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int, num_splits: int = 0) -> torch.Tensor:
+    nbytes = kvq_decode_workspace_bytes(cache, num_q_heads, max_seq_len, num_splits)
+    return torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=cache.device)
+
+
+def kvq_decode_split(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale: float, max_seq_len: int,
+                     workspace: torch.Tensor, num_splits: int = 0, stream=None):
+    """Stage 1 of kvq_decode_attention: split partials into `workspace`."""
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3
+    _check(lib().kvq_decode_split(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(q), q.shape[1],
+                                  float(softmax_scale), max_seq_len, num_splits, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)), "kvq_decode_split")
+
+
+def kvq_decode_combine(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int, workspace: torch.Tensor,
+                       out: torch.Tensor, num_splits: int = 0, stream=None) -> torch.Tensor:
+    """Stage 2 of kvq_decode_attention: merge the split partials into `out`."""
+    _check(lib().kvq_decode_combine(ctypes.byref(cache.cfg), num_q_heads, max_seq_len, num_splits, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(out), _DTYPE[out.dtype],
+                                    _stream(stream)), "kvq_decode_combine")
     return out
 
 

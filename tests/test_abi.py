@@ -62,7 +62,7 @@ def test_cache_bytes(kvq):
     c = _cfg(kvq, 3, 128, num_tier_pages=5)
     p, t, s = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
     assert L.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(p), ctypes.byref(t), ctypes.byref(s)) == 0
-    assert p.value == 64 * 8 * 2 * 2048 and t.value == 5 * 8 * 2 * 2176 and s.value == 4 * 8 * 2 * 16 * 128 * 4
+    assert p.value == 64 * 8 * 2 * 4224 and t.value == 5 * 8 * 2 * 2176 and s.value == 4 * 8 * 2 * 16 * 128 * 4
     c = _cfg(kvq, 1, 64)
     assert L.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(p), ctypes.byref(t), ctypes.byref(s)) == 0
     assert s.value == 0 and t.value == 0

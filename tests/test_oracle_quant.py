@@ -213,8 +213,23 @@ def test_cb2_page_properties():
         blk = oracle.quantize_page(oracle.BLK_CB2, D, x, role=role)
         xh = oracle.dequantize_block(oracle.BLK_CB2, D, blk, role=role)
         masks = np.array([oracle.outlier_mask(x[t].astype(np.float64))[0] for t in range(16)])
-        # outliers reproduced exactly as e4m3; counts stored per token
-        assert (blk[12 * D:12 * D + 16] == masks.sum(1)).all()
+        # side-list grouped by channel: header {n_ch, total}, records
+        # {channel, 0, token mask} with channels ascending, then a dense 16 x R
+        # matrix of e4m3 values (token-major for K, channel-major for V)
+        chans = np.nonzero(masks.any(0))[0]
+        hdr = blk[12 * D:]
+        n = len(chans)
+        R = n + (n & 1)
+        assert hdr[0] == n and hdr[1] == masks.sum()
+        for i, c in enumerate(chans):
+            rec = hdr[4 + 4 * i:8 + 4 * i]
+            assert rec[0] == c and rec[1] == 0
+            assert int(rec[2]) | (int(rec[3]) << 8) == sum(1 << t for t in range(16) if masks[t, c])
+            for t in range(16):
+                pos = 4 + 4 * n + (t * R + i if role == 0 else i * 16 + t)
+                want = oracle.e4m3_encode(float(x[t, c])) if masks[t, c] else 0
+                assert hdr[pos] == want
+        # outliers reproduced exactly as e4m3
         for t, c in zip(*np.nonzero(masks)):
             assert xh[t, c] == oracle.e4m3_decode(oracle.e4m3_encode(float(x[t, c])))
         # non-outliers: the stored value is the nearest of the channel's 4 fp16 centroids
@@ -254,5 +269,5 @@ def test_fragment_positions_are_a_bijection(D, role):
 def test_block_strides_aligned(fmt):
     for D in (64, 128):
         assert oracle.block_stride(fmt, D) % 128 == 0
-    assert oracle.block_stride(oracle.BLK_CB2, 128) == 2048
+    assert oracle.block_stride(oracle.BLK_CB2, 128) == 4224
     assert oracle.block_stride(oracle.BLK_E2M1, 128) == 1152
