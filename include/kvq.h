@@ -198,6 +198,29 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
                               const void* workspace, size_t workspace_bytes, void* out, kvq_dtype out_dtype,
                               void* stream);
 
+/* Decode attention that allocates nothing and takes no workspace.  The pages
+ * have no counterpart to this call; it exists for callers that may not
+ * allocate device memory when they run decode -- a serving loop that reserves
+ * all of its memory at start-up and treats any later allocation as an error,
+ * code running inside an allocator or memory-pool callback (allocating there
+ * would recurse or deadlock), a plugin whose host hands it only inputs and
+ * outputs.  Same arguments and result as kvq_decode_attention without the
+ * workspace: the split partials go to one scratch array compiled into the
+ * library (KVQ_NOALLOC_SCRATCH_BYTES, a copy on every GPU that loads the
+ * library, kept until the process exits).
+ *   - Returns KVQ_ERR_WORKSPACE, before anything is enqueued, when the
+ *     partials (kvq_decode_workspace_bytes) would exceed the scratch.
+ *   - Calls no allocator.  Its first call on a device looks up the scratch's
+ *     device address once (cudaGetSymbolAddress, with that device current);
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch, which keeps the last
+ *     call's contents; calls that may overlap on the GPU (different streams)
+ *     race on it -- serialise them.  Nothing in it needs to start at zero. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q,
+                                        int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,
+                                        int32_t num_splits, void* out, kvq_dtype out_dtype, void* stream);
+
 /* Debug: the values tokens [tok_begin, tok_end) of (seq, kv_head, which = 0 K /
  * 1 V) stand for, as fp32 [tok_end - tok_begin][D] in device memory `out`.
  * Bit-identical to the CPU reference's dequantization. */

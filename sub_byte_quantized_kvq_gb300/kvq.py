@@ -47,7 +47,7 @@ _lib = None
 _lock = threading.Lock()
 EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
            "kvq_decode_num_splits", "kvq_decode_split", "kvq_decode_combine", "kvq_decode_attention",
-           "kvq_dequantize", "kvq_status_string", "kvq_version")
+           "kvq_decode_attention_noalloc", "kvq_dequantize", "kvq_status_string", "kvq_version")
 
 
 def lib() -> ctypes.CDLL:
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "kvq_decode_split": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, S, P]),
                 "kvq_decode_combine": (I, [pcfg, I, I, I, P, S, P, I, P]),
                 "kvq_decode_attention": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P, S, P]),
+                "kvq_decode_attention_noalloc": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P]),
                 "kvq_dequantize": (I, [pcfg, pcache, I, I, I, I, I, P, P]),
                 "kvq_status_string": (ctypes.c_char_p, [I]),
                 "kvq_version": (ctypes.c_char_p, []),
@@ -208,6 +209,31 @@ def kvq_decode_combine(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: i
     _check(lib().kvq_decode_combine(ctypes.byref(cache.cfg), num_q_heads, max_seq_len, num_splits, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _ptr(out), _DTYPE[out.dtype],
                                     _stream(stream)), "kvq_decode_combine")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def kvq_decode_attention_noalloc(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale: float, max_seq_len: int,
+                                 num_splits: int = 0, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                                 stream=None) -> torch.Tensor:
+    """kvq_decode_attention without a workspace, for callers that may not
+    allocate device memory while they decode (the library's own fixed scratch
+    holds the split partials).  `out` should be passed by such callers; it is
+    allocated here only as a convenience when omitted.  Concurrent calls on
+    different streams share that scratch and must be serialised."""
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    st = lib().kvq_decode_attention_noalloc(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(q), q.shape[1],
+                                            float(softmax_scale), max_seq_len, num_splits, _ptr(out),
+                                            _DTYPE[out.dtype], _stream(stream))
+    if st == KVQ_ERR_WORKSPACE:
+        need = kvq_decode_workspace_bytes(cache, q.shape[1], max_seq_len, num_splits)
+        raise KVQError(st, f"kvq_decode_attention_noalloc: split partials need {need} bytes, more than the "
+                           f"{NOALLOC_SCRATCH_BYTES}-byte built-in scratch")
+    _check(st, "kvq_decode_attention_noalloc")
     return out
 
 
