@@ -17,9 +17,11 @@
  *        Quantization", section "2. FP4/INT4 KV-Cache Quantization"
  *        (block-wise asymmetric quantization, E2M1, the scale formula).
  *
- * Arithmetic is fp64 with ascending-index reductions; compile with
- * -ffp-contract=off so no multiply-add is fused.  Where the pages leave a step
- * open, the reading taken is stated next to the code.
+ * Attention is fp64.  The quantizer takes its decisions (outlier tests,
+ * Lloyd-Max assignments, INT4 codes) in IEEE binary32, the precision the CUDA
+ * kernels use -- the pages fix none -- with ascending-index reductions; compile
+ * with -ffp-contract=off so no multiply-add is fused.  Where the pages leave a
+ * step open, the reading taken is stated next to the code.
  *
  * Every function here is pinned by tests/test_oracle_*.py against something
  * other than itself (library routines, closed forms, brute force, invariants).
@@ -155,8 +157,8 @@ static float f32_div(float a, float b) { return (float)((double)a / (double)b); 
 /* Outlier isolation ([P1] "1. Dynamic Outlier Isolation" and the             */
 /* compress_kv_head listing; [P3] outlier channels; [P4] "Channel-Outlier     */
 /* Isolation").  For one vector x[0..n) (a token's head vector, or one        */
-/* 32-value group for INT4):                                                  */
-/*   mu  = (sum x) / n                    ascending index, fp64               */
+/* 32-value group for INT4), in binary32:                                     */
+/*   mu  = (sum x) / n                    ascending index                     */
 /*   s   = sqrt( sum (x - mu)^2 / (n-1) ) unbiased, as torch's .std()         */
 /*   x_i is an outlier  iff  |x_i - mu| > sigma * s   (strict, as the listing)*/
 /* Reading: sigma = 3 (the pages print 3.5 in the text and "> 3 Sigma" in the */
@@ -172,21 +174,21 @@ EXPORT int or_kmax(int n) /* capacity at sigma = 3 */
     return k < 0 ? 0 : k;
 }
 
-EXPORT int or_outlier_mask(const double* x, int n, double sigma, int kmax, uint8_t* mask)
+EXPORT int or_outlier_mask(const float* x, int n, double sigma, int kmax, uint8_t* mask)
 {
-    double sum = 0.0;
+    float sum = 0.0f;
     for (int i = 0; i < n; ++i) sum += x[i];
-    double mu = sum / (double)n;
-    double ss = 0.0;
+    float mu = sum / (float)n;
+    float ss = 0.0f;
     for (int i = 0; i < n; ++i) {
-        double d = x[i] - mu;
+        float d = x[i] - mu;
         ss += d * d;
     }
-    double s = sqrt(ss / (double)(n - 1));
-    double thr = sigma * s;
+    float s = sqrtf(ss / (float)(n - 1));
+    float thr = (float)sigma * s;
     int k = 0;
     for (int i = 0; i < n; ++i) {
-        int out = fabs(x[i] - mu) > thr;
+        int out = fabsf(x[i] - mu) > thr;
         if (out && k >= kmax) out = 0;
         mask[i] = (uint8_t)out;
         k += out;
@@ -198,7 +200,7 @@ EXPORT int or_outlier_mask(const double* x, int n, double sigma, int kmax, uint8
 /* 2-bit non-uniform codebook ([P1] "2. Centroid Vector Quantization for      */
 /* Residuals": a 4-centroid codebook fitted by k-means; the listing starts    */
 /* the centroids at linspace(min, max, 4) and assigns by argmin distance).    */
-/* In one dimension k-means is the Lloyd-Max iteration:                       */
+/* In one dimension k-means is the Lloyd-Max iteration (binary32):            */
 /*   c = (mn, mn+h, mn+2h, mx) with h = (mx-mn)/3                             */
 /*   repeat up to `iters` times:                                              */
 /*     a = nearest-centroid assignment (ties -> lower index, argmin's rule)   */
@@ -211,32 +213,31 @@ EXPORT int or_outlier_mask(const double* x, int n, double sigma, int kmax, uint8
 /* centroids.  Returns the number of assignment passes made.                  */
 /* ------------------------------------------------------------------------- */
 
-static int nearest4(double v, const double* c)
+static int nearest4(float v, const float* c)
 {
     int best = 0;
-    double bd = fabs(v - c[0]);
+    float bd = fabsf(v - c[0]);
     for (int j = 1; j < 4; ++j) {
-        double d = fabs(v - c[j]);
+        float d = fabsf(v - c[j]);
         if (d < bd) { bd = d; best = j; }
     }
     return best;
 }
 
-EXPORT int or_lloyd4(const double* v, int n, int iters, double* c_out, uint16_t* c16_out,
-                     uint8_t* codes_out)
+EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c16_out, uint8_t* codes_out)
 {
-    double c[4] = {0.0, 0.0, 0.0, 0.0};
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int passes = 0;
     if (n > 0) {
-        double mn = v[0], mx = v[0];
+        float mn = v[0], mx = v[0];
         for (int i = 1; i < n; ++i) {
             if (v[i] < mn) mn = v[i];
             if (v[i] > mx) mx = v[i];
         }
-        double h = (mx - mn) / 3.0;
+        float h = (mx - mn) / 3.0f;
         c[0] = mn;
         c[1] = mn + h;
-        c[2] = mn + 2.0 * h;
+        c[2] = mn + 2.0f * h;
         c[3] = mx;
         uint8_t prev[64], a[64];
         int have_prev = 0;
@@ -245,21 +246,21 @@ EXPORT int or_lloyd4(const double* v, int n, int iters, double* c_out, uint16_t*
             ++passes;
             if (have_prev && memcmp(a, prev, (size_t)n) == 0) break;
             for (int j = 0; j < 4; ++j) {
-                double sum = 0.0;
+                float sum = 0.0f;
                 int cnt = 0;
                 for (int i = 0; i < n; ++i)
                     if (a[i] == j) { sum += v[i]; ++cnt; }
-                if (cnt > 0) c[j] = sum / (double)cnt;
+                if (cnt > 0) c[j] = sum / (float)cnt;
             }
             memcpy(prev, a, (size_t)n);
             have_prev = 1;
         }
     }
-    double c16[4];
+    float c16[4];
     for (int j = 0; j < 4; ++j) {
-        uint16_t h = or_fp16_encode(c[j]);
+        uint16_t h = or_fp16_encode((double)c[j]);
         if (c16_out) c16_out[j] = h;
-        c16[j] = or_fp16_decode(h);
+        c16[j] = (float)or_fp16_decode(h);
         if (c_out) c_out[j] = c[j];
     }
     if (codes_out)
@@ -412,7 +413,7 @@ static int fp8_byte(int D, int role, int t, int c)
 /*   mn, mx over the group's non-outliers; S = fp16((mx - mn) / 15),          */
 /*   m = fp16(mn) (the zero point stored as the group minimum: x = q*S + m is */
 /*   the same affine map as (q - Z)*S with Z = -mn/S);                        */
-/*   q = clamp(rint((x - m) / S), 0, 15) in fp64 from the stored S and m;     */
+/*   q = clamp(rint((x - m) / S), 0, 15) in binary32 from the stored S, m;    */
 /*   S == 0 gives q = 0; outlier slots hold q = 0 and the value as fp16.      */
 /* E2M1 reading (one e4m3 scale per 16 values, no outliers):                  */
 /*   s = e4m3(f32(amax / 6)); q = e2m1(f32(x / s)), s == 0 gives q = 0.       */
@@ -426,12 +427,11 @@ static void quantize_token_int4(const float* x, int D, double sigma, int role, i
     uint8_t* vals = blk + 10 * D + 16 + 16 * cap;
     for (int i = 0; i < cap; ++i) { chans[t * cap + i] = 0; put_u16(vals + 2 * (t * cap + i), 0); }
     for (int g = 0; g < D / 32; ++g) {
-        double v[32];
+        const float* v = x + 32 * g;
         uint8_t mask[32];
-        for (int i = 0; i < 32; ++i) v[i] = (double)x[32 * g + i];
         or_outlier_mask(v, 32, sigma, or_kmax(32), mask);
         int have = 0;
-        double mn = 0.0, mx = 0.0;
+        float mn = 0.0f, mx = 0.0f;
         for (int i = 0; i < 32; ++i) {
             if (mask[i]) continue;
             if (!have || v[i] < mn) mn = v[i];
@@ -439,19 +439,19 @@ static void quantize_token_int4(const float* x, int D, double sigma, int role, i
             have = 1;
         }
         uint16_t S16 = 0, m16 = 0;
-        if (have) { S16 = or_fp16_encode((mx - mn) / 15.0); m16 = or_fp16_encode(mn); }
-        double S = or_fp16_decode(S16), m = or_fp16_decode(m16);
+        if (have) { S16 = or_fp16_encode((double)((mx - mn) / 15.0f)); m16 = or_fp16_encode((double)mn); }
+        float S = (float)or_fp16_decode(S16), m = (float)or_fp16_decode(m16);
         for (int i = 0; i < 32; ++i) {
             int c = 32 * g + i;
             uint8_t q = 0;
             if (mask[i]) {
                 chans[t * cap + cnt] = (uint8_t)c;
-                put_u16(vals + 2 * (t * cap + cnt), or_fp16_encode(v[i]));
+                put_u16(vals + 2 * (t * cap + cnt), or_fp16_encode((double)v[i]));
                 ++cnt;
-            } else if (S != 0.0) {
-                double r = rint((v[i] - m) / S);
-                if (r < 0.0) r = 0.0;
-                if (r > 15.0) r = 15.0;
+            } else if (S != 0.0f) {
+                float r = rintf((v[i] - m) / S);
+                if (r < 0.0f) r = 0.0f;
+                if (r > 15.0f) r = 15.0f;
                 q = (uint8_t)r;
             }
             nib_set(blk, D, role, t, c, q);
@@ -497,19 +497,15 @@ static void quantize_page_cb2(const float* x, int D, double sigma, int iters, in
 {
     memset(blk, 0, (size_t)or_block_stride(OR_CB2, D));
     uint8_t mask[16][128];
-    double row[128];
     int kmax = or_kmax(D);
-    for (int t = 0; t < 16; ++t) {
-        for (int c = 0; c < D; ++c) row[c] = (double)x[t * D + c];
-        or_outlier_mask(row, D, sigma, kmax, mask[t]);
-    }
+    for (int t = 0; t < 16; ++t) or_outlier_mask(x + t * D, D, sigma, kmax, mask[t]);
     for (int c = 0; c < D; ++c) {
-        double v[16];
+        float v[16];
         uint8_t codes[16];
         uint16_t c16[4];
         int n = 0;
         for (int t = 0; t < 16; ++t)
-            if (!mask[t][c]) v[n++] = (double)x[t * D + c];
+            if (!mask[t][c]) v[n++] = x[t * D + c];
         or_lloyd4(v, n, iters, NULL, c16, codes);
         for (int j = 0; j < 4; ++j) cb2_cent_set(blk, D, role, c, j, c16[j]);
         n = 0;

@@ -1,6 +1,7 @@
-// kvq_quantize.cu -- quantize-on-append into the paged cache (compiled with
-// --fmad=false: every fp64 statistic is evaluated in the order written, with no
-// fused multiply-add, so codes are bit-identical to the CPU reference).
+// kvq_quantize.cu -- quantize-on-append into the paged cache.  The quantizer's
+// decisions (outlier tests, Lloyd-Max, INT4 codes) are taken in binary32 in a
+// fixed order; the file is compiled with --fmad=false so no multiply-add is
+// fused and codes are bit-identical to the CPU reference.
 //
 // "The Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache
 // Quantization", section 2 ("Outlier Isolation and Block-wise Quantization"):
@@ -66,23 +67,24 @@ __device__ __forceinline__ uint8_t f32_to_e2m1(float x) {
       : "f"(0.f), "f"(x));
   return (uint8_t)(r & 0xFu);
 }
-__device__ __forceinline__ uint16_t f64_to_f16_bits(double x) { return __half_as_ushort(__double2half(x)); }
-__device__ __forceinline__ double f16_bits_to_f64(uint16_t h) { return (double)__half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Outlier mask of one vector (fp64, ascending order): |x - mu| > sigma * s, at most kmax kept.
-__device__ int outlier_mask(const float* x, int n, int stride, double sigma, int kmax, uint8_t* mask, int mstride) {
-  double sum = 0.0;
-  for (int i = 0; i < n; ++i) sum += (double)x[i * stride];
-  const double mu = sum / (double)n;
-  double ss = 0.0;
+// Outlier mask of one vector (binary32, ascending order): |x - mu| > sigma * s,
+// s the unbiased standard deviation; at most kmax kept (lowest indices).
+__device__ int outlier_mask(const float* x, int n, int stride, float sigma, int kmax, uint8_t* mask, int mstride) {
+  float sum = 0.f;
+  for (int i = 0; i < n; ++i) sum += x[i * stride];
+  const float mu = __fdiv_rn(sum, (float)n);
+  float ss = 0.f;
   for (int i = 0; i < n; ++i) {
-    const double d = (double)x[i * stride] - mu;
+    const float d = x[i * stride] - mu;
     ss += d * d;
   }
-  const double thr = sigma * sqrt(ss / (double)(n - 1));
+  const float thr = sigma * __fsqrt_rn(__fdiv_rn(ss, (float)(n - 1)));
   int k = 0;
   for (int i = 0; i < n; ++i) {
-    int out = fabs((double)x[i * stride] - mu) > thr;
+    int out = fabsf(x[i * stride] - mu) > thr;
     if (out && k >= kmax) out = 0;
     mask[i * mstride] = (uint8_t)out;
     k += out;
@@ -90,24 +92,24 @@ __device__ int outlier_mask(const float* x, int n, int stride, double sigma, int
   return k;
 }
 
-__device__ __forceinline__ int nearest4(double v, const double* c) {
+__device__ __forceinline__ int nearest4(float v, const float* c) {
   int best = 0;
-  double bd = fabs(v - c[0]);
+  float bd = fabsf(v - c[0]);
   for (int j = 1; j < 4; ++j) {
-    const double d = fabs(v - c[j]);
+    const float d = fabsf(v - c[j]);
     if (d < bd) { bd = d; best = j; }
   }
   return best;
 }
 
-// Lloyd-Max 4-centroid fit of v[0..n) (n <= 16); fp16 centroids and codes.
-__device__ void lloyd4(const double* v, int n, int iters, uint16_t* c16, uint8_t* codes) {
-  double c[4] = {0.0, 0.0, 0.0, 0.0};
+// Lloyd-Max 4-centroid fit of v[0..n) (n <= 16) in binary32; fp16 centroids and codes.
+__device__ void lloyd4(const float* v, int n, int iters, uint16_t* c16, uint8_t* codes) {
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 0) {
-    double mn = v[0], mx = v[0];
+    float mn = v[0], mx = v[0];
     for (int i = 1; i < n; ++i) { mn = v[i] < mn ? v[i] : mn; mx = v[i] > mx ? v[i] : mx; }
-    const double h = (mx - mn) / 3.0;
-    c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0 * h; c[3] = mx;
+    const float h = __fdiv_rn(mx - mn, 3.0f);
+    c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0f * h; c[3] = mx;
     uint8_t a[16], prev[16];
     bool have_prev = false;
     for (int it = 0; it < iters; ++it) {
@@ -118,18 +120,18 @@ __device__ void lloyd4(const double* v, int n, int iters, uint16_t* c16, uint8_t
       }
       if (same) break;
       for (int j = 0; j < 4; ++j) {
-        double s = 0.0;
+        float s = 0.f;
         int cnt = 0;
         for (int i = 0; i < n; ++i)
           if (a[i] == j) { s += v[i]; ++cnt; }
-        if (cnt > 0) c[j] = s / (double)cnt;
+        if (cnt > 0) c[j] = __fdiv_rn(s, (float)cnt);
       }
       for (int i = 0; i < n; ++i) prev[i] = a[i];
       have_prev = true;
     }
   }
-  double cf[4];
-  for (int j = 0; j < 4; ++j) { c16[j] = f64_to_f16_bits(c[j]); cf[j] = f16_bits_to_f64(c16[j]); }
+  float cf[4];
+  for (int j = 0; j < 4; ++j) { c16[j] = f32_to_f16_bits(c[j]); cf[j] = f16_bits_to_f32(c16[j]); }
   for (int i = 0; i < n; ++i) codes[i] = (uint8_t)nearest4(v[i], cf);
 }
 
@@ -153,26 +155,26 @@ __device__ void quantize_token_int4(const float* x, int t, uint8_t (*codes)[D], 
   int cnt = 0;
   if (lane < NG) {
     const float* xg = x + 32 * lane;
-    outlier_mask(xg, 32, 1, sigma, kmax_outliers(32), mask, 1);
+    outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
     bool have = false;
-    double mn = 0.0, mx = 0.0;
+    float mn = 0.f, mx = 0.f;
     for (int i = 0; i < 32; ++i) {
       if (mask[i]) continue;
-      const double v = (double)xg[i];
+      const float v = xg[i];
       if (!have || v < mn) mn = v;
       if (!have || v > mx) mx = v;
       have = true;
     }
-    const uint16_t S16 = have ? f64_to_f16_bits((mx - mn) / 15.0) : 0;
-    const uint16_t m16 = have ? f64_to_f16_bits(mn) : 0;
-    const double S = f16_bits_to_f64(S16), m = f16_bits_to_f64(m16);
+    const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 15.0f)) : 0;
+    const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
+    const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
     for (int i = 0; i < 32; ++i) {
       uint8_t q = 0;
       if (mask[i]) {
         ++cnt;
-      } else if (S != 0.0) {
-        double r = rint(((double)xg[i] - m) / S);
-        r = r < 0.0 ? 0.0 : (r > 15.0 ? 15.0 : r);
+      } else if (S != 0.f) {
+        float r = rintf(__fdiv_rn(xg[i] - m, S));
+        r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
         q = (uint8_t)r;
       }
       codes[t][32 * lane + i] = q;
@@ -317,16 +319,16 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
     }
     if (tid == 0) *reinterpret_cast<float*>(blk + fp8_sc_off(D)) = s;
   } else {
-    if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+    if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
     __syncthreads();
     if (tid < D) {
       const int c = tid;
-      double v[16];
+      float v[16];
       uint8_t cc[16];
       uint16_t c16[4];
       int nv = 0;
       for (int t = 0; t < 16; ++t)
-        if (!mask[t][c]) v[nv++] = (double)xs[t][c];
+        if (!mask[t][c]) v[nv++] = xs[t][c];
       lloyd4(v, nv, a.iters, c16, cc);
       nv = 0;
       for (int t = 0; t < 16; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];

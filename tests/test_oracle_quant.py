@@ -23,21 +23,23 @@ R_K, R_V = 0, 1
 
 # ------------------------------------------------------------------ outliers
 def test_outlier_rule_matches_exact_statistics():
-    """Decisions equal those from Python's exact-rational mean/stdev, except
-    where |x - mu| is within 1e-9 relative of the threshold."""
+    """Decisions (taken in binary32) equal those from Python's exact-rational
+    mean/stdev of the same values, except where |x - mu| is within 1e-4
+    relative of the threshold (binary32 rounding of the statistics)."""
     rng = np.random.default_rng(0)
     checked = 0
     for trial in range(300):
         n = [32, 64, 128][trial % 3]
         x = rng.standard_normal(n)
         x[rng.integers(0, n, 3)] *= rng.uniform(2, 12)
+        x = x.astype(np.float32).astype(np.float64)
         mask, k = oracle.outlier_mask(x, 3.0, cap=n)
         xs = [Fraction(float(v)) for v in x]
         mu = statistics.mean(xs)
         sd = statistics.stdev([float(v) for v in x])
         for i, v in enumerate(x):
             dev = abs(float(Fraction(float(v)) - mu))
-            if abs(dev - 3 * sd) <= 1e-9 * max(dev, 1e-300):
+            if abs(dev - 3 * sd) <= 1e-4 * max(dev, sd):
                 continue
             assert mask[i] == (dev > 3 * sd)
             checked += 1
@@ -92,41 +94,43 @@ def _brute_optimum(v):
 
 
 def _distortion(v, c):
-    return sum(min((x - cj) ** 2 for cj in c) for x in v)
+    return sum(min((float(x) - float(cj)) ** 2 for cj in c) for x in v)
 
 
 def test_lloyd_never_beats_brute_force_and_hits_it_on_clusters():
     rng = np.random.default_rng(1)
     for trial in range(120):
         n = int(rng.integers(1, 13))
-        v = rng.standard_normal(n) * rng.uniform(0.1, 5)
+        v = (rng.standard_normal(n) * rng.uniform(0.1, 5)).astype(np.float32).astype(np.float64)
         c, _, _, _ = oracle.lloyd4(v)
-        assert _distortion(v, c) >= _brute_optimum(v) - 1e-9
+        opt = _brute_optimum(v)
+        assert _distortion(v, c) >= opt - 1e-5 * max(opt, 1e-6)
     # evenly spaced, well separated clusters: the linspace start puts one
     # centroid in each cluster's cell, so Lloyd reaches the global optimum
     for trial in range(40):
         centers = rng.uniform(-20, 20) + rng.uniform(5, 20) * np.arange(4)
-        v = np.concatenate([cc + rng.uniform(-0.5, 0.5, 4) for cc in centers])
+        v = np.concatenate([cc + rng.uniform(-0.5, 0.5, 4) for cc in centers]).astype(np.float32).astype(np.float64)
         rng.shuffle(v)
         c, _, _, _ = oracle.lloyd4(v)
-        assert abs(_distortion(v, c) - _brute_optimum(v)) < 1e-9
+        opt = _brute_optimum(v)
+        assert abs(_distortion(v, c) - opt) <= 1e-5 * max(opt, 1e-3)
 
 
 def test_lloyd_fixed_point_and_codes():
     rng = np.random.default_rng(2)
     for _ in range(200):
         n = int(rng.integers(1, 17))
-        v = rng.standard_normal(n)
+        v = rng.standard_normal(n).astype(np.float32).astype(np.float64)
         c, c16, codes, passes = oracle.lloyd4(v, iters=64)
         # converged: each non-empty cell's centroid is the mean of its members
-        assign = np.array([int(np.argmin(np.abs(x - c))) for x in v])
+        assign = np.array([int(np.argmin(np.abs(x - c.astype(np.float64)))) for x in v])
         for j in range(4):
             if (assign == j).any():
-                assert abs(c[j] - v[assign == j].mean()) <= 1e-12 * max(1, abs(c[j]))
+                assert abs(float(c[j]) - v[assign == j].mean()) <= 1e-5 * max(1, abs(float(c[j])))
         # final codes: nearest fp16 centroid, first index on ties (numpy argmin's rule)
         cf = np.array([oracle.fp16_decode(h) for h in c16])
         assert (codes == np.array([int(np.argmin(np.abs(x - cf))) for x in v])).all()
-        assert all(h == np.array(cj, np.float64).astype(np.float16).view(np.uint16) for h, cj in zip(c16, c))
+        assert all(h == np.array(float(cj), np.float64).astype(np.float16).view(np.uint16) for h, cj in zip(c16, c))
 
 
 def test_lloyd_special_cases():
