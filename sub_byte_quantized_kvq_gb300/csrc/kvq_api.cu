@@ -151,18 +151,31 @@ static int num_sms() {
   return n;
 }
 
-// Splits per (sequence, kv head): fill the resident CTA slots of the GPU once
-// (units >= slots: one split), keeping at least 2 pages per warp in each split.
+// Splits per (sequence, kv head): the smallest count whose grid fills at least
+// 90% of its last wave of resident CTA slots (so no nearly empty final wave),
+// keeping at least 2 pages per warp in each split; otherwise the count with the
+// best last-wave fill.
 static int auto_splits(const kvq_config* c, int G, int max_seq_len) {
-  const int pages = (max_seq_len + kPage - 1) / kPage;
+  const long long pages = (max_seq_len + kPage - 1) / kPage;
   const long long units = (long long)c->num_seqs * c->num_kv_heads;
   const int per_sm = decode_ctas_per_sm(c->format, c->head_dim, G);
   const long long slots = (long long)num_sms() * (per_sm > 0 ? per_sm : 1);
-  long long s = units >= slots ? 1 : slots / units;
-  const long long smax = pages / (2 * kWarpsPerCta) > 1 ? pages / (2 * kWarpsPerCta) : 1;
-  if (s > smax) s = smax;
-  if (s < 1) s = 1;
-  return (int)s;
+  long long smax = pages / (2 * kWarpsPerCta);
+  if (smax < 1) smax = 1;
+  if (smax > 256) smax = 256;
+  long long best = 1;
+  double best_fill = -1.0;
+  for (long long s = 1; s <= smax; ++s) {
+    const long long ctas = units * s;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double fill = (double)ctas / (double)(waves * slots);
+    if (fill >= 0.9) return (int)s;
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = s;
+    }
+  }
+  return (int)best;
 }
 
 }  // namespace kvq

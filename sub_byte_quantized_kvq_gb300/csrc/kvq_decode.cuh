@@ -69,16 +69,25 @@ __host__ __device__ constexpr int half_slot_bytes() {
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-// Shared-memory plan: [qsm: D x GS fp32] then per warp:
-// [stages: NSTAGE x PPI x 2 blocks][mbar x NSTAGE][meta x NSTAGE*PPI][ds 16 x GS][psm 16 x GS][corr D x GS]
+// Shared-memory plan: [qsm: D x GS fp32][zero block, page formats] then per warp:
+// [stages: NSTAGE x PPI x 2 blocks][mbar x NSTAGE][meta x NSTAGE*PPI][ds 16 x GS, INT4 only][psm 16 x GS]
+// [corr D x GS, formats with outliers]
+template <int FMT>
+__host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kMain == kBlkInt4; }
 template <int FMT, int D, int NSTAGE>
 __host__ __device__ constexpr int warp_smem_bytes(int GS) {
   return NSTAGE * Fmt<FMT>::kPPI * 2 * half_slot_bytes<FMT, D>() + 8 * NSTAGE +
-         align16(4 * NSTAGE * Fmt<FMT>::kPPI) + 16 * GS * 4 + 16 * GS * 4 + (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
+         align16(4 * NSTAGE * Fmt<FMT>::kPPI) + (has_ds<FMT>() ? 16 * GS * 4 : 0) + 16 * GS * 4 +
+         (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
+}
+// Page formats keep one zeroed block (K and V both read it) for absent pages.
+template <int FMT, int D>
+__host__ __device__ constexpr int zero_block_bytes() {
+  return Fmt<FMT>::kPaged ? align16(half_slot_bytes<FMT, D>()) : 0;
 }
 template <int FMT, int D, int W, int NSTAGE>
 __host__ __device__ constexpr int cta_smem_bytes(int GS) {
-  return align16(D * GS * 4) + W * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
+  return align16(D * GS * 4) + zero_block_bytes<FMT, D>() + W * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -86,17 +95,21 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 
 // ----------------------------------------------------------------------------- fragment builders
-// Each builds the four A registers (f16x2) of step s for this lane.
+// Each builds the four A registers (f16x2) of step s for this lane from
+// 32-bit shared-memory addresses.
 
 // CB2, K role: channels x = 16s + 2q, y = x + 1 (and +8); tokens g, g + 8.
-template <int D>
-__device__ __forceinline__ void cb2_k_frag(const uint8_t* kb, uint32_t w16, int s, int q4, uint32_t (&a)[4]) {
+// kcb = block + 4D + 16q (the lane's codebook column).
+__device__ __forceinline__ void cb2_k_frag(uint32_t kcb, uint32_t w16, int s, uint32_t (&a)[4]) {
   const uint32_t sel1 = (w16 & 0x3333u) | 0x4040u;
   const uint32_t sel2 = ((w16 >> 2) & 0x3333u) | 0x4040u;
-  const uint4 ca = *reinterpret_cast<const uint4*>(kb + cb2_cb_off(D) + 8 * (16 * s + 2 * q4));
-  const uint4 cb = *reinterpret_cast<const uint4*>(kb + cb2_cb_off(D) + 8 * (16 * s + 2 * q4 + 8));
+  const uint4 ca = lds128(kcb + 128 * s);
+  const uint4 cb = lds128(kcb + 128 * s + 64);
   uint32_t lo = prmt(ca.x, ca.z, sel1), hi = prmt(ca.y, ca.w, sel1);
   a[0] = prmt(lo, hi, 0x5140u);
   a[1] = prmt(lo, hi, 0x7362u);
@@ -107,11 +120,11 @@ __device__ __forceinline__ void cb2_k_frag(const uint8_t* kb, uint32_t w16, int 
 }
 
 // CB2, V role: channels cA = 16s + g, cB = cA + 8; tokens 2q, 2q+1 (and +8).
-template <int D>
-__device__ __forceinline__ void cb2_v_frag(const uint8_t* vb, uint32_t w16, int s, int g, uint32_t (&a)[4]) {
+// vcb = block + 4D + 16g.
+__device__ __forceinline__ void cb2_v_frag(uint32_t vcb, uint32_t w16, int s, uint32_t (&a)[4]) {
   const uint32_t sel1 = (w16 & 0x3333u) | 0x4400u;
   const uint32_t sel2 = ((w16 >> 2) & 0x3333u) | 0x4400u;
-  const uint4 c = *reinterpret_cast<const uint4*>(vb + cb2_cb_off(D) + 16 * (8 * s + g));
+  const uint4 c = lds128(vcb + 128 * s);
   uint32_t lo = prmt(c.x, c.z, sel1), hi = prmt(c.y, c.w, sel1);
   a[0] = prmt(lo, hi, 0x5140u);
   a[1] = prmt(lo, hi, 0x7362u);
@@ -168,9 +181,6 @@ __device__ __forceinline__ void int4_v_frag(uint32_t wd, const float (&S)[4], co
   split_hilo(fmaf(nib(wd, 6), S[2], M[2]), fmaf(nib(wd, 7), S[3], M[3]), ahi[3], alo[3]);
 }
 
-__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
-  return __low2float(u32_as_h2(e4m3x2_to_f16x2(byte & 0xFFu)));
-}
 __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
   return __half2float(__ushort_as_half((unsigned short)(bits & 0xFFFFu)));
 }
@@ -184,53 +194,61 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
 // the correction of a channel is sum over its outliers of (x - c0); both x
 // (e4m3) and c0 (fp16) are exact in fp16, so it is computed as two mma with
 // exact operands: + values, - c0 where flagged.
-__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
-__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
-// -c0 of channel ch (fp16 bits) from the codebook slot `slot` of a block.
+//
+// The side-list is read through a generic pointer -- shared memory when it fits
+// the bytes fetched with the block, global memory otherwise -- so one copy of
+// the correction code serves both.
+struct SideList {
+  const uint8_t* p;
+  __device__ __forceinline__ uint32_t u8(int off) const { return p[off]; }
+  __device__ __forceinline__ uint32_t u16(int off) const { return *reinterpret_cast<const uint16_t*>(p + off); }
+  __device__ __forceinline__ uint32_t u32(int off) const { return *reinterpret_cast<const uint32_t*>(p + off); }
+};
+
+// {c0, c0}: fp16 bits of centroid 0 of codebook slot `slot` (the slot's (L, H)
+// byte planes hold its low and high bytes at byte 0).
 template <int D>
-__device__ __forceinline__ uint32_t neg_c0_bits(const uint8_t* blk, int slot) {
-  const uint8_t* p = blk + cb2_cb_off(D) + 8 * slot;
-  return (p[0] | (p[4] << 8)) ^ 0x8000u;
-}
-// 0xFFFF in each half whose token bit is set: half 0 <- bit t0 of m0, half 1 <- bit t1 of m1.
-__device__ __forceinline__ uint32_t half_mask(uint32_t m0, int t0, uint32_t m1, int t1) {
-  return (0u - ((m0 >> t0) & 1u)) & 0xFFFFu | ((0u - ((m1 >> t1) & 1u)) & 0xFFFF0000u);
+__device__ __forceinline__ uint32_t c0_bits(uint32_t blk_s, int slot) {
+  const uint2 lh = lds64(blk_s + cb2_cb_off(D) + 8 * slot);
+  return prmt(lh.x, lh.y, 0x4040u);
 }
 
 // Scores of tokens g, g+8: += sum over outlier channels c of q[h][c] * (x - c0[c]).
 // Channels go 16 at a time into one k16 tile (A = tokens x slots), B = Q^T
-// gathered at the slots' channels.  hdr may live in shared or global memory.
-template <int D, int NT>
-__device__ __forceinline__ void cb2_k_correct(const uint8_t* hdr, const uint8_t* kb, const float* qsm, int G, int GS,
-                                              int lane, float (&acc)[NT][4]) {
+// gathered at the slots' channels.
+template <int D, int NT, class Mem>
+__device__ __forceinline__ void cb2_k_correct(const Mem hdr, uint32_t kb_s, uint32_t qsm_s, int G, int GS, int lane,
+                                              float (&acc)[NT][4]) {
   const int g = lane >> 2, q4 = lane & 3;
-  const int n_ch = min((int)hdr[0], D), R = n_ch + (n_ch & 1);
-  const uint8_t* vals = hdr + 4 + 4 * n_ch;
+  const int n_ch = min((int)hdr.u8(0), D), R = n_ch + (n_ch & 1), V0 = 4 + 4 * n_ch;
   for (int base = 0; base < n_ch; base += 16) {
     const int ia = base + 2 * q4, ib = ia + 8;  // slots ia, ia+1 (A cols of a0/a1), ib, ib+1 (a2/a3)
     uint32_t rec[4];
-    rec[0] = ia < n_ch ? ld_u32(hdr + 4 + 4 * ia) : 0u;
-    rec[1] = ia + 1 < n_ch ? ld_u32(hdr + 8 + 4 * ia) : 0u;
-    rec[2] = ib < n_ch ? ld_u32(hdr + 4 + 4 * ib) : 0u;
-    rec[3] = ib + 1 < n_ch ? ld_u32(hdr + 8 + 4 * ib) : 0u;
+    rec[0] = ia < n_ch ? hdr.u32(4 + 4 * ia) : 0u;
+    rec[1] = ia + 1 < n_ch ? hdr.u32(8 + 4 * ia) : 0u;
+    rec[2] = ib < n_ch ? hdr.u32(4 + 4 * ib) : 0u;
+    rec[3] = ib + 1 < n_ch ? hdr.u32(8 + 4 * ib) : 0u;
     // + outlier values (pairs of adjacent slots at one token; the pad column is 0)
     uint32_t ax[4];
-    ax[0] = ia < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + g * R + ia)) : 0u;
-    ax[1] = ia < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + (g + 8) * R + ia)) : 0u;
-    ax[2] = ib < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + g * R + ib)) : 0u;
-    ax[3] = ib < n_ch ? e4m3x2_to_f16x2(ld_u16(vals + (g + 8) * R + ib)) : 0u;
-    // - c0 where the token is an outlier of the slot's channel
-    const uint32_t m0 = rec[0] >> 16, m1 = rec[1] >> 16, m2 = rec[2] >> 16, m3 = rec[3] >> 16;
-    const uint32_t c01 = neg_c0_bits<D>(kb, rec[0] & (D - 1)) | (neg_c0_bits<D>(kb, rec[1] & (D - 1)) << 16);
-    const uint32_t c23 = neg_c0_bits<D>(kb, rec[2] & (D - 1)) | (neg_c0_bits<D>(kb, rec[3] & (D - 1)) << 16);
-    const uint32_t ac0 = c01 & half_mask(m0, g, m1, g), ac1 = c01 & half_mask(m0, g + 8, m1, g + 8);
-    const uint32_t ac2 = c23 & half_mask(m2, g, m3, g), ac3 = c23 & half_mask(m2, g + 8, m3, g + 8);
+    ax[0] = ia < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + g * R + ia)) : 0u;
+    ax[1] = ia < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + (g + 8) * R + ia)) : 0u;
+    ax[2] = ib < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + g * R + ib)) : 0u;
+    ax[3] = ib < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + (g + 8) * R + ib)) : 0u;
+    // - c0 where the token is an outlier of the slot's channel.  Token masks:
+    // shifting (m_a | m_b << 16) left by 7-g puts bit g / g+8 of m_a / m_b in the
+    // sign bits of bytes 0 / 1 / 2 / 3; prmt's sign-replicate mode widens them.
+    const uint32_t c01 = prmt(c0_bits<D>(kb_s, rec[0] & (D - 1)), c0_bits<D>(kb_s, rec[1] & (D - 1)), 0x5410u) ^ 0x80008000u;
+    const uint32_t c23 = prmt(c0_bits<D>(kb_s, rec[2] & (D - 1)), c0_bits<D>(kb_s, rec[3] & (D - 1)), 0x5410u) ^ 0x80008000u;
+    const uint32_t x01 = prmt(rec[0], rec[1], 0x7632u) << (7 - g);
+    const uint32_t x23 = prmt(rec[2], rec[3], 0x7632u) << (7 - g);
+    const uint32_t ac0 = c01 & prmt(x01, 0u, 0xAA88u), ac1 = c01 & prmt(x01, 0u, 0xBB99u);
+    const uint32_t ac2 = c23 & prmt(x23, 0u, 0xAA88u), ac3 = c23 & prmt(x23, 0u, 0xBB99u);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h = nt * 8 + g;
       float qv[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) qv[k] = (h < G && rec[k]) ? qsm[(rec[k] & (D - 1)) * GS + h] : 0.f;
+      for (int k = 0; k < 4; ++k) qv[k] = (h < G && rec[k]) ? ldsf(qsm_s + 4 * ((rec[k] & (D - 1)) * GS + h)) : 0.f;
       const uint32_t b0 = h2_as_u32(__floats2half2_rn(qv[0], qv[1]));
       const uint32_t b1 = h2_as_u32(__floats2half2_rn(qv[2], qv[3]));
       mma16816(acc[nt], ax[0], ax[1], ax[2], ax[3], b0, b1);
@@ -242,28 +260,30 @@ __device__ __forceinline__ void cb2_k_correct(const uint8_t* hdr, const uint8_t*
 // Output correction of the outlier channels: corr[c][h] += sum_t p[t][h] * (x - c0[c]).
 // A = (slots x tokens) against the page's P^T fragments; each (channel, head)
 // is written by exactly one lane.
-template <int D, int NT>
-__device__ __forceinline__ void cb2_v_correct(const uint8_t* hdr, const uint8_t* vb, const uint32_t (&phi)[NT][2],
-                                              const uint32_t (&plo)[NT][2], float* corr, int G, int GS, int lane) {
+template <int D, int NT, class Mem>
+__device__ __forceinline__ void cb2_v_correct(const Mem hdr, uint32_t vb_s, const uint32_t (&phi)[NT][2],
+                                              const uint32_t (&plo)[NT][2], uint32_t corr_s, int G, int GS, int lane) {
   const int g = lane >> 2, q4 = lane & 3;
-  const int n_ch = min((int)hdr[0], D);
-  const uint8_t* vals = hdr + 4 + 4 * n_ch;
+  const int n_ch = min((int)hdr.u8(0), D), V0 = 4 + 4 * n_ch;
   const int t0 = 2 * q4;
   for (int base = 0; base < n_ch; base += 16) {
     const int i0 = base + g, i1 = i0 + 8;
-    const uint32_t r0 = i0 < n_ch ? ld_u32(hdr + 4 + 4 * i0) : 0u;
-    const uint32_t r1 = i1 < n_ch ? ld_u32(hdr + 4 + 4 * i1) : 0u;
+    const uint32_t r0 = i0 < n_ch ? hdr.u32(4 + 4 * i0) : 0u;
+    const uint32_t r1 = i1 < n_ch ? hdr.u32(4 + 4 * i1) : 0u;
     const int ch0 = r0 & (D - 1), ch1 = r1 & (D - 1);
     uint32_t ax[4];
-    ax[0] = r0 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i0 + t0)) : 0u;
-    ax[1] = r1 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i1 + t0)) : 0u;
-    ax[2] = r0 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i0 + t0 + 8)) : 0u;
-    ax[3] = r1 ? e4m3x2_to_f16x2(ld_u16(vals + 16 * i1 + t0 + 8)) : 0u;
-    const uint32_t m0 = r0 >> 16, m1 = r1 >> 16;
-    const uint32_t c0 = neg_c0_bits<D>(vb, cb2_slot(1, ch0)) * 0x00010001u;
-    const uint32_t c1 = neg_c0_bits<D>(vb, cb2_slot(1, ch1)) * 0x00010001u;
-    const uint32_t ac0 = c0 & half_mask(m0, t0, m0, t0 + 1), ac1 = c1 & half_mask(m1, t0, m1, t0 + 1);
-    const uint32_t ac2 = c0 & half_mask(m0, t0 + 8, m0, t0 + 9), ac3 = c1 & half_mask(m1, t0 + 8, m1, t0 + 9);
+    ax[0] = r0 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i0 + t0)) : 0u;
+    ax[1] = r1 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i1 + t0)) : 0u;
+    ax[2] = r0 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i0 + t0 + 8)) : 0u;
+    ax[3] = r1 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i1 + t0 + 8)) : 0u;
+    // token masks: with w = m0 | m1 << 16, (w << 7-t0) / (w << 6-t0) hold bits
+    // t0 / t0+1 (and +8, of m0 / m1) in the sign bits of their bytes
+    const uint32_t w = prmt(r0, r1, 0x7632u);
+    const uint32_t x = w << (7 - t0), y = w << (6 - t0);
+    const uint32_t c0 = c0_bits<D>(vb_s, cb2_slot(1, ch0)) ^ 0x80008000u;
+    const uint32_t c1 = c0_bits<D>(vb_s, cb2_slot(1, ch1)) ^ 0x80008000u;
+    const uint32_t ac0 = c0 & prmt(x, y, 0xCC88u), ac2 = c0 & prmt(x, y, 0xDD99u);
+    const uint32_t ac1 = c1 & prmt(x, y, 0xEEAAu), ac3 = c1 & prmt(x, y, 0xFFBBu);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -272,13 +292,14 @@ __device__ __forceinline__ void cb2_v_correct(const uint8_t* hdr, const uint8_t*
       mma16816(c, ac0, ac1, ac2, ac3, phi[nt][0], phi[nt][1]);
       mma16816(c, ac0, ac1, ac2, ac3, plo[nt][0], plo[nt][1]);
       const int h0 = nt * 8 + 2 * q4;
+      const uint32_t a0 = corr_s + 4 * (ch0 * GS + h0), a1 = corr_s + 4 * (ch1 * GS + h0);
       if (r0) {
-        if (h0 < G) corr[ch0 * GS + h0] += c[0];
-        if (h0 + 1 < G) corr[ch0 * GS + h0 + 1] += c[1];
+        if (h0 < G) sts32(a0, __float_as_uint(ldsf(a0) + c[0]));
+        if (h0 + 1 < G) sts32(a0 + 4, __float_as_uint(ldsf(a0 + 4) + c[1]));
       }
       if (r1) {
-        if (h0 < G) corr[ch1 * GS + h0] += c[2];
-        if (h0 + 1 < G) corr[ch1 * GS + h0 + 1] += c[3];
+        if (h0 < G) sts32(a1, __float_as_uint(ldsf(a1) + c[2]));
+        if (h0 + 1 < G) sts32(a1 + 4, __float_as_uint(ldsf(a1 + 4) + c[3]));
       }
     }
   }
@@ -302,8 +323,8 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
       float mx = -INFINITY;
 #pragma unroll
       for (int p = 0; p < PPI; ++p) {
-        mx = fmaxf(mx, g < ntok[p] ? acc[p][nt][j] : -INFINITY);
-        mx = fmaxf(mx, g + 8 < ntok[p] ? acc[p][nt][2 + j] : -INFINITY);
+        mx = fmaxf(mx, (g < ntok[p]) ? acc[p][nt][j] : -INFINITY);
+        mx = fmaxf(mx, (g + 8 < ntok[p]) ? acc[p][nt][2 + j] : -INFINITY);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -316,8 +337,8 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
       float sum = 0.f;
 #pragma unroll
       for (int p = 0; p < PPI; ++p) {
-        const float p0 = g < ntok[p] ? ex2(acc[p][nt][j] - mn) : 0.f;
-        const float p1 = g + 8 < ntok[p] ? ex2(acc[p][nt][2 + j] - mn) : 0.f;
+        const float p0 = (g < ntok[p]) ? ex2(acc[p][nt][j] - mn) : 0.f;
+        const float p1 = (g + 8 < ntok[p]) ? ex2(acc[p][nt][2 + j] - mn) : 0.f;
         acc[p][nt][j] = p0;
         acc[p][nt][2 + j] = p1;
         sum += p0 + p1;
@@ -331,8 +352,8 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
 // Rescale the output accumulators (and the shared-memory outlier correction
 // corr[c][h]) by alpha after a max change.
 template <int D, int NT, bool kCorr>
-__device__ __forceinline__ void rescale_state(float (&o)[NT][D / 16][4], const float (&alpha)[NT][2], float* corr,
-                                              int G, int GS, int lane) {
+__device__ __forceinline__ void rescale_state(float (&o)[NT][D / 16][4], const float (&alpha)[NT][2],
+                                              uint32_t corr_s, int G, int GS, int lane) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -346,7 +367,10 @@ __device__ __forceinline__ void rescale_state(float (&o)[NT][D / 16][4], const f
       // alpha of head h lives in lanes with q = (h % 8) / 2, register h % 2
       const float ah = __shfl_sync(0xffffffffu, alpha[h >> 3][h & 1], (h & 7) >> 1);
       if (h < G)
-        for (int c = lane; c < D; c += 32) corr[c * GS + h] *= ah;
+        for (int c = lane; c < D; c += 32) {
+          const uint32_t a = corr_s + 4 * (c * GS + h);
+          sts32(a, __float_as_uint(ldsf(a) * ah));
+        }
     }
     __syncwarp();
   }
@@ -432,6 +456,9 @@ struct WarpSmem {
   float* ds;         // [16][GS] INT4 K-outlier score corrections of the current page
   float* psm;        // [16][GS] probabilities of the current page (INT4, fp32 tail)
   float* corr;       // [D][GS] V-outlier output correction (rescaled with o)
+  uint32_t qsm_s, corr_s;  // the same two arrays as shared-window addresses
+  const uint8_t* stages;   // the warp's stage ring (generic), and its shared-window address
+  uint32_t stages_s;
   int G, GS;
 };
 
@@ -447,13 +474,14 @@ __device__ __forceinline__ const uint8_t* block_src(const DecodeArgs& a, int kvh
   return a.pool + (((size_t)phys * a.Hkv + kvh) * 2 + role) * block_stride(Fmt<FMT>::kMain, D);
 }
 
+// The lane's 2-bit codes of a CB2 block: one u16 per step, D/32 words.
 template <int D>
-__device__ __forceinline__ void load_codes(const uint8_t* p, uint32_t (&w)[D / 32]) {
+__device__ __forceinline__ void load_codes(uint32_t blk_s, int lane, uint32_t (&w)[D / 32]) {
   if constexpr (D == 128) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint4 v = lds128(blk_s + 16 * lane);
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
   } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const uint2 v = lds64(blk_s + 8 * lane);
     w[0] = v.x; w[1] = v.y;
   }
 }
@@ -470,18 +498,36 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[p][nt][r] *= scale;
   float alpha[NT][2];
-  if (online_softmax<PPI, NT>(acc, ntok, g, st.m, st.l, alpha)) {
-    if (corr) rescale_state<D, NT, true>(st.o, alpha, sm.corr, sm.G, sm.GS, lane);
-    else rescale_state<D, NT, false>(st.o, alpha, sm.corr, sm.G, sm.GS, lane);
+  const bool rescale = online_softmax<PPI, NT>(acc, ntok, g, st.m, st.l, alpha);
+  if (rescale) {
+    if (corr) rescale_state<D, NT, true>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
+    else rescale_state<D, NT, false>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
   }
 #pragma unroll
   for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
 }
 
+// Bytes of a CB2 side-list with n_ch channels.
+__device__ __forceinline__ int cb2_side_bytes(int n_ch) { return 4 + 4 * n_ch + 16 * (n_ch + (n_ch & 1)); }
+
+// x[i] for a runtime i (selects; keeps small register arrays in registers).
+template <int N, class T>
+__device__ __forceinline__ T pick(const T (&x)[N], int i) {
+  T v = x[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) v = i == k ? x[k] : v;
+  return v;
+}
+
 // CB2 pages (and, for the tiered format, FP8 tier pages), PPI at a time.
+// kb_s / vb_s: shared addresses of the staged K / V blocks; an absent page
+// points at the CTA's zero block, so it needs no masking outside the softmax.
+// The outlier corrections run page by page through one copy of their code
+// (a rolled loop), which keeps the loop body small enough for the
+// instruction cache.
 template <int FMT, int D, int NT, int PPI>
 __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
-                                         const uint8_t* const (&kb)[PPI], const uint8_t* const (&vb)[PPI],
+                                         const uint32_t (&kb_s)[PPI], const uint32_t (&vb_s)[PPI],
                                          const int32_t (&ent)[PPI], const int (&ntok)[PPI], const DecodeArgs& a,
                                          int kvh, const WarpSmem& sm, int lane) {
   constexpr int NS = D / 16;
@@ -497,33 +543,46 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
   for (int p = 0; p < PPI; ++p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
-    load_codes<D>(kb[p] + 2 * NS * lane, kc[p]);
+    load_codes<D>(kb_s[p], lane, kc[p]);
   }
 #pragma unroll
   for (int s = 0; s < NS; ++s)
 #pragma unroll
     for (int p = 0; p < PPI; ++p) {
       uint32_t ak[4];
-      if (T && tier[p]) fp8_frag(*reinterpret_cast<const uint2*>(kb[p] + 8 * NS * lane + 8 * s), ak);
-      else cb2_k_frag<D>(kb[p], (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, q4, ak);
+      if (T && tier[p]) fp8_frag(lds64(kb_s[p] + 8 * NS * lane + 8 * s), ak);
+      else cb2_k_frag(kb_s[p] + cb2_cb_off(D) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
     }
+  if constexpr (T) {
 #pragma unroll
-  for (int p = 0; p < PPI; ++p) {
-    if (T && tier[p]) {
-      const float sk = *reinterpret_cast<const float*>(kb[p] + fp8_sc_off(D));
+    for (int p = 0; p < PPI; ++p) {
+      const float sk = tier[p] ? ldsf(kb_s[p] + fp8_sc_off(D)) : 1.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
-    } else if (ntok[p] > 0) {
-      const uint8_t* hdr = kb[p] + cb2_out_off(D);
-      if (hdr[0] > 0) {
-        const int nc = min((int)hdr[0], D), sz = 4 + 4 * nc + 16 * (nc + (nc & 1));
-        if (sz > kOutPrefetch) hdr = block_src<FMT, D>(a, kvh, ent[p], 0) + cb2_out_off(D);
-        cb2_k_correct<D, NT>(hdr, kb[p], sm.qsm, sm.G, sm.GS, lane, acc[p]);
-      }
+    }
+  }
+#pragma unroll 1
+  for (int p = 0; p < PPI; ++p) {
+    const uint32_t kbs = pick(kb_s, p);
+    const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(kbs + cb2_out_off(D));
+    if (n_ch > 0) {
+      const uint8_t* hdr = cb2_side_bytes(min(n_ch, D)) > kOutPrefetch
+                               ? block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D)
+                               : sm.stages + (kbs - sm.stages_s) + cb2_out_off(D);
+      float c[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+      cb2_k_correct<D, NT>(SideList{hdr}, kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
+#pragma unroll
+      for (int pp = 0; pp < PPI; ++pp)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[pp][nt][r] += pp == p ? c[nt][r] : 0.f;
     }
   }
 
@@ -534,8 +593,8 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
   float sv[PPI];
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
-    load_codes<D>(vb[p] + 2 * NS * lane, vc[p]);
-    sv[p] = (T && tier[p]) ? *reinterpret_cast<const float*>(vb[p] + fp8_sc_off(D)) : 1.f;
+    load_codes<D>(vb_s[p], lane, vc[p]);
+    sv[p] = (T && tier[p]) ? ldsf(vb_s[p] + fp8_sc_off(D)) : 1.f;
   }
 #pragma unroll
   for (int s = 0; s < NS; ++s)
@@ -543,7 +602,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     for (int p = 0; p < PPI; ++p) {
       uint32_t av[4];
       if (T && tier[p]) {
-        fp8_frag(*reinterpret_cast<const uint2*>(vb[p] + 8 * NS * lane + 8 * s), av);
+        fp8_frag(lds64(vb_s[p] + 8 * NS * lane + 8 * s), av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float t4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -553,8 +612,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
           for (int r = 0; r < 4; ++r) st.o[nt][s][r] = fmaf(sv[p], t4[r], st.o[nt][s][r]);
         }
       } else {
-        cb2_v_frag<D>(vb[p], (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, g, av);
-        if (ntok[p] < 16) mask_v_tokens(av, ntok[p], q4);
+        cb2_v_frag(vb_s[p] + cb2_cb_off(D) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
@@ -562,40 +620,66 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         }
       }
     }
-#pragma unroll
+#pragma unroll 1
   for (int p = 0; p < PPI; ++p) {
-    if (!(T && tier[p]) && ntok[p] > 0) {
-      const uint8_t* hdr = vb[p] + cb2_out_off(D);
-      if (hdr[0] > 0) {
-        const int nc = min((int)hdr[0], D), sz = 4 + 4 * nc + 16 * (nc + (nc & 1));
-        if (sz > kOutPrefetch) hdr = block_src<FMT, D>(a, kvh, ent[p], 1) + cb2_out_off(D);
-        cb2_v_correct<D, NT>(hdr, vb[p], phi[p], plo[p], sm.corr, sm.G, sm.GS, lane);
-        __syncwarp();
-      }
+    const uint32_t vbs = pick(vb_s, p);
+    const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(vbs + cb2_out_off(D));
+    if (n_ch > 0) {
+      const uint8_t* hdr = cb2_side_bytes(min(n_ch, D)) > kOutPrefetch
+                               ? block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D)
+                               : sm.stages + (vbs - sm.stages_s) + cb2_out_off(D);
+      uint32_t ph[NT][2], pl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          ph[nt][k] = phi[0][nt][k];
+          pl[nt][k] = plo[0][nt][k];
+#pragma unroll
+          for (int pp = 1; pp < PPI; ++pp) {
+            ph[nt][k] = pp == p ? phi[pp][nt][k] : ph[nt][k];
+            pl[nt][k] = pp == p ? plo[pp][nt][k] : pl[nt][k];
+          }
+        }
+      cb2_v_correct<D, NT>(SideList{hdr}, vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
+      __syncwarp();
     }
+  }
+}
+
+// The lane's E2M1 code words of a block: one u32 per step, NS contiguous words.
+template <int D>
+__device__ __forceinline__ void load_e2m1_words(uint32_t blk_s, int lane, uint32_t (&w)[D / 16]) {
+#pragma unroll
+  for (int i = 0; i < D / 64; ++i) {
+    const uint4 v = lds128(blk_s + 4 * (D / 16) * lane + 16 * i);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
   }
 }
 
 // E2M1 pages (per-token format: the last page may hold fewer than 16 tokens).
 template <int D, int NT, int PPI>
 __device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
-                                          const uint8_t* const (&kb)[PPI], const uint8_t* const (&vb)[PPI],
+                                          const uint32_t (&kb_s)[PPI], const uint32_t (&vb_s)[PPI],
                                           const int (&ntok)[PPI], float scale, const WarpSmem& sm, int lane) {
   constexpr int NS = D / 16;
   const int g = lane >> 2, q4 = lane & 3;
   float acc[PPI][NT][4];
+  uint32_t kw[PPI][NS];
 #pragma unroll
-  for (int p = 0; p < PPI; ++p)
+  for (int p = 0; p < PPI; ++p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
+    load_e2m1_words<D>(kb_s[p], lane, kw[p]);
+  }
 #pragma unroll
   for (int s = 0; s < NS; ++s)
 #pragma unroll
     for (int p = 0; p < PPI; ++p) {
       uint32_t ak[4];
-      e2m1_frag(*reinterpret_cast<const uint32_t*>(kb[p] + 4 * NS * lane + 4 * s), ak);
-      const uint8_t* sc = kb[p] + e2m1_sc_off(D) + 16 * s;
-      const uint32_t sgs = e4m3x2_to_f16x2(sc[g] | (sc[g + 8] << 8));  // {s_g, s_g+8}
+      e2m1_frag(kw[p][s], ak);
+      const uint32_t sc = kb_s[p] + e2m1_sc_off(D) + 16 * s;
+      const uint32_t sgs = e4m3x2_to_f16x2(lds8(sc + g) | (lds8(sc + g + 8) << 8));  // {s_g, s_g+8}
       const uint32_t s0 = prmt(sgs, sgs, 0x1010u), s1 = prmt(sgs, sgs, 0x3232u);
       ak[0] = hmul2u(ak[0], s0); ak[1] = hmul2u(ak[1], s1); ak[2] = hmul2u(ak[2], s0); ak[3] = hmul2u(ak[3], s1);
 #pragma unroll
@@ -603,23 +687,46 @@ __device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (
     }
   uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
   softmax_frags<D, NT, PPI>(st, acc, ntok, scale, sm, lane, false, phi, plo);
+  // token masks of the page's valid slots (per-token formats: the last page may be partial)
+  bool full = true;
+  uint32_t m01[PPI], m23[PPI];
+  uint32_t vw[PPI][NS];
 #pragma unroll
-  for (int s = 0; s < NS; ++s)
-#pragma unroll
-    for (int p = 0; p < PPI; ++p) {
-      uint32_t av[4];
-      e2m1_frag(*reinterpret_cast<const uint32_t*>(vb[p] + 4 * NS * lane + 4 * s), av);
-      const uint8_t* sc = vb[p] + e2m1_sc_off(D) + 16 * s + 2 * q4;
-      const uint32_t s01 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc));
-      const uint32_t s23 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + 8));
-      av[0] = hmul2u(av[0], s01); av[1] = hmul2u(av[1], s01); av[2] = hmul2u(av[2], s23); av[3] = hmul2u(av[3], s23);
-      if (ntok[p] < 16) mask_v_tokens(av, ntok[p], q4);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
-        mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], plo[p][nt][0], plo[p][nt][1]);
-      }
+  for (int p = 0; p < PPI; ++p) {
+    full = full && ntok[p] == kPage;
+    uint32_t a4[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+    mask_v_tokens(a4, ntok[p], q4);
+    m01[p] = a4[0];
+    m23[p] = a4[2];
+    load_e2m1_words<D>(vb_s[p], lane, vw[p]);
+  }
+  auto pv_step = [&](int s, int p, bool masked) {
+    uint32_t av[4];
+    e2m1_frag(vw[p][s], av);
+    const uint32_t sc = vb_s[p] + e2m1_sc_off(D) + 16 * s + 2 * q4;
+    const uint32_t s01 = e4m3x2_to_f16x2(lds16(sc));
+    const uint32_t s23 = e4m3x2_to_f16x2(lds16(sc + 8));
+    av[0] = hmul2u(av[0], s01); av[1] = hmul2u(av[1], s01); av[2] = hmul2u(av[2], s23); av[3] = hmul2u(av[3], s23);
+    if (masked) {
+      av[0] &= m01[p]; av[1] &= m01[p]; av[2] &= m23[p]; av[3] &= m23[p];
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
+      mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], plo[p][nt][0], plo[p][nt][1]);
+    }
+  };
+  if (full) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+      for (int p = 0; p < PPI; ++p) pv_step(s, p, false);
+  } else {
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+      for (int p = 0; p < PPI; ++p) pv_step(s, p, true);
+  }
 }
 
 // One INT4 page (per-token format; fp16 outliers in per-token slots).
@@ -629,17 +736,20 @@ __device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (
   constexpr int NS = D / 16, CAP = int4_cap(D), NG = D / 32;
   const int g = lane >> 2, q4 = lane & 3;
   const int ntok[1] = {ntok_};
+  const uint32_t kb_s = smem_u32(kb), vb_s = smem_u32(vb);
   float acc[1][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[0][nt][0] = acc[0][nt][1] = acc[0][nt][2] = acc[0][nt][3] = 0.f;
+  uint32_t kw[NS];
+  load_e2m1_words<D>(kb_s, lane, kw);   // same word layout as E2M1: one u32 of nibbles per step
 #pragma unroll
   for (int s = 0; s < NS; ++s) {
     const int grp = s >> 1;
-    const uint32_t z0 = *reinterpret_cast<const uint32_t*>(kb + int4_sz_off(D) + 4 * (g * NG + grp));
-    const uint32_t z1 = *reinterpret_cast<const uint32_t*>(kb + int4_sz_off(D) + 4 * ((g + 8) * NG + grp));
+    const uint32_t z0 = lds32(kb_s + int4_sz_off(D) + 4 * (g * NG + grp));
+    const uint32_t z1 = lds32(kb_s + int4_sz_off(D) + 4 * ((g + 8) * NG + grp));
     uint32_t ahi[4], alo[4];
-    int4_k_frag(*reinterpret_cast<const uint32_t*>(kb + 4 * NS * lane + 4 * s), fp16_bits_to_float(z0),
-                fp16_bits_to_float(z0 >> 16), fp16_bits_to_float(z1), fp16_bits_to_float(z1 >> 16), ahi, alo);
+    int4_k_frag(kw[s], fp16_bits_to_float(z0), fp16_bits_to_float(z0 >> 16), fp16_bits_to_float(z1),
+                fp16_bits_to_float(z1 >> 16), ahi, alo);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       mma16816(acc[0][nt], ahi[0], ahi[1], ahi[2], ahi[3], qf[nt][s][0], qf[nt][s][1]);
@@ -662,6 +772,8 @@ __device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (
   }
   uint32_t phi[1][NT][2], plo[1][NT][2];
   softmax_frags<D, NT, 1>(st, acc, ntok, scale, sm, lane, true, phi, plo);
+  uint32_t vw[NS];
+  load_e2m1_words<D>(vb_s, lane, vw);
 #pragma unroll
   for (int s = 0; s < NS; ++s) {
     const int grp = s >> 1;
@@ -669,12 +781,12 @@ __device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 2 * q4 + (i & 1) + 8 * (i >> 1);
-      const uint32_t z = *reinterpret_cast<const uint32_t*>(vb + int4_sz_off(D) + 4 * (t * NG + grp));
+      const uint32_t z = lds32(vb_s + int4_sz_off(D) + 4 * (t * NG + grp));
       S[i] = fp16_bits_to_float(z);
       M[i] = fp16_bits_to_float(z >> 16);
     }
     uint32_t ahi[4], alo[4];
-    int4_v_frag(*reinterpret_cast<const uint32_t*>(vb + 4 * NS * lane + 4 * s), S, M, ahi, alo);
+    int4_v_frag(vw[s], S, M, ahi, alo);
     if (ntok_ < 16) {
       mask_v_tokens(ahi, ntok_, q4);
       mask_v_tokens(alo, ntok_, q4);
@@ -741,8 +853,15 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
 }
 
 // ----------------------------------------------------------------------------- split kernel
+// Resident CTAs per SM the register budget is cut for (shared memory allows
+// as many for G <= 8).
+template <int FMT, int D, int NT>
+__host__ __device__ constexpr int min_ctas_per_sm() {
+  return NT == 2 ? 2 : (D == 64 && Fmt<FMT>::kMain != kBlkInt4) ? 4 : 3;
+}
+
 template <int FMT, int D, int NT, int W, int NSTAGE>
-__global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_split_kernel(const DecodeArgs a) {
   using F = Fmt<FMT>;
   constexpr int NS = D / 16, PPI = F::kPPI;
   constexpr int HS = half_slot_bytes<FMT, D>();
@@ -754,43 +873,58 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
   const int G = a.G, GS = (G + 3) & ~3;
 
   float* qsm = reinterpret_cast<float*>(smem);
-  uint8_t* wb = smem + align16(D * GS * 4) + w * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
+  uint8_t* zb = smem + align16(D * GS * 4);
+  uint8_t* wb = zb + zero_block_bytes<FMT, D>() + w * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
   uint8_t* stages = wb;
+  const uint32_t stages_s = smem_u32(stages);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(wb + NSTAGE * PPI * 2 * HS);
   int32_t* meta = reinterpret_cast<int32_t*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE);
   WarpSmem sm;
   sm.qsm = qsm;
   sm.ds = reinterpret_cast<float*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE + align16(4 * NSTAGE * PPI));
-  sm.psm = sm.ds + 16 * GS;
+  sm.psm = sm.ds + (has_ds<FMT>() ? 16 * GS : 0);
   sm.corr = sm.psm + 16 * GS;
+  sm.qsm_s = smem_u32(qsm);
+  sm.corr_s = smem_u32(sm.corr);
+  sm.stages = stages;
+  sm.stages_s = stages_s;
+  const uint32_t zb_s = smem_u32(zb);
   sm.G = G;
   sm.GS = GS;
 
-  // query of the CTA's G heads: fp32 in shared memory ([D][GS]), fp16 B fragments in registers
+  // query of the CTA's G heads: fp32 in shared memory as [D][GS] (outlier
+  // corrections gather its columns), fp16 B fragments in registers
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
-  for (int i = threadIdx.x; i < D * GS; i += W * 32) {
-    const int c = i / GS, h = i - c * GS;
-    qsm[i] = h < G ? __bfloat162float(qg[h * D + c]) : 0.f;
+  for (int i = threadIdx.x; i < GS * D; i += W * 32) {
+    const int h = i / D, c = i % D;   // D is a power of two
+    qsm[c * GS + h] = h < G ? __bfloat162float(qg[i]) : 0.f;
   }
-  for (int i = lane; i < 16 * GS; i += 32) sm.ds[i] = 0.f;
+  for (int i = threadIdx.x; i < zero_block_bytes<FMT, D>() / 16; i += W * 32)
+    reinterpret_cast<uint4*>(zb)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (has_ds<FMT>())
+    for (int i = lane; i < 16 * GS; i += 32) sm.ds[i] = 0.f;
   if (F::kOutliers)
     for (int i = lane; i < D * GS; i += 32) sm.corr[i] = 0.f;
   if (lane == 0) {
     for (int j = 0; j < NSTAGE; ++j) mbar_init(&mbar[j], 1);
     fence_mbar_init();
   }
-  __syncthreads();
 
   uint32_t qf[NT][NS][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + g;
+    const __nv_bfloat16* qh = qg + (size_t)h * D + 2 * q4;
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
-      const int h = nt * 8 + g, c = 16 * s + 2 * q4;
       const bool on = h < G;
-      qf[nt][s][0] = h2_as_u32(__floats2half2_rn(on ? qsm[c * GS + h] : 0.f, on ? qsm[(c + 1) * GS + h] : 0.f));
-      qf[nt][s][1] = h2_as_u32(__floats2half2_rn(on ? qsm[(c + 8) * GS + h] : 0.f, on ? qsm[(c + 9) * GS + h] : 0.f));
+      const float x0 = on ? __bfloat162float(qh[16 * s]) : 0.f, x1 = on ? __bfloat162float(qh[16 * s + 1]) : 0.f;
+      const float x8 = on ? __bfloat162float(qh[16 * s + 8]) : 0.f, x9 = on ? __bfloat162float(qh[16 * s + 9]) : 0.f;
+      qf[nt][s][0] = h2_as_u32(__floats2half2_rn(x0, x1));
+      qf[nt][s][1] = h2_as_u32(__floats2half2_rn(x8, x9));
     }
+  }
+  __syncthreads();
 
   int L = a.seq_lens[b];
   if (L > a.max_seq_len) {
@@ -892,22 +1026,23 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
     }
     int32_t ent[PPI];
     int ntok[PPI];
-    const uint8_t* kb[PPI];
-    const uint8_t* vb[PPI];
+    uint32_t kb_s[PPI], vb_s[PPI];
 #pragma unroll
     for (int j = 0; j < PPI; ++j) {
       ent[j] = meta[slot * PPI + j];
       const int page = p0 + w + (it * PPI + j) * W;
       ntok[j] = (ent[j] == kBadEntry || ent[j] == kNoPage) ? 0 : (F::kPaged ? kPage : min(kPage, L - kPage * page));
-      kb[j] = stages + (slot * PPI + j) * 2 * HS;
-      vb[j] = kb[j] + HS;
+      kb_s[j] = stages_s + (slot * PPI + j) * 2 * HS;
+      vb_s[j] = kb_s[j] + HS;
+      if (F::kPaged && ntok[j] == 0) kb_s[j] = vb_s[j] = zb_s;
     }
     if constexpr (F::kMain == kBlkCb2) {
-      iter_cb2<FMT, D, NT, PPI>(st, qf, kb, vb, ent, ntok, a, kvh, sm, lane);
+      iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane);
     } else if constexpr (F::kMain == kBlkE2m1) {
-      iter_e2m1<D, NT, PPI>(st, qf, kb, vb, ntok, a.scale_log2, sm, lane);
+      iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane);
     } else {
-      iter_int4<D, NT>(st, qf, kb[0], vb[0], ntok[0], a.scale_log2, sm, lane);
+      const uint8_t* kb = stages + slot * 2 * HS;
+      iter_int4<D, NT>(st, qf, kb, kb + HS, ntok[0], a.scale_log2, sm, lane);
     }
     __syncwarp();
     issue(it + NSTAGE);
@@ -949,9 +1084,13 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
         }
   }
   __syncthreads();
-  float* mo = reinterpret_cast<float*>(smem + align16(D * GS * 4));  // [W][GS][D]
-  float* mm = mo + W * GS * D;                                       // [W][GS]
-  float* ml = mm + W * GS;                                           // [W][GS]
+  // merge area (reuses the stages): mo [W][GS][D], mm / ml [W][GS] (mm turns
+  // into the warps' weights), mM / mL [GS]
+  float* mo = reinterpret_cast<float*>(smem + align16(D * GS * 4));
+  float* mm = mo + W * GS * D;
+  float* ml = mm + W * GS;
+  float* mM = ml + W * GS;
+  float* mL = mM + GS;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -974,24 +1113,31 @@ __global__ void __launch_bounds__(W * 32) decode_split_kernel(const DecodeArgs a
       }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-    const int h = idx / D, c = idx - h * D;
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < W; ++ww) M = fmaxf(M, mm[ww * GS + h]);
-    float ov = 0.f, lv = 0.f;
-    if (M != -INFINITY) {
+    float lv = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < W; ++ww) {
-        const float mw = mm[ww * GS + h];
-        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        ov = fmaf(f, mo[(ww * GS + h) * D + c], ov);
-        lv = fmaf(f, ml[ww * GS + h], lv);
-      }
+    for (int ww = 0; ww < W; ++ww) {
+      const float mw = mm[ww * GS + h];
+      const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : ex2(mw - M);
+      mm[ww * GS + h] = f;
+      lv = fmaf(f, ml[ww * GS + h], lv);
     }
+    mM[h] = M;
+    mL[h] = lv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int h = idx / D, c = idx % D;
+    float ov = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < W; ++ww) ov = fmaf(mm[ww * GS + h], mo[(ww * GS + h) * D + c], ov);
     const size_t row = ((size_t)b * a.Hq + (size_t)kvh * G + h) * a.S + split;
     a.part_o[row * D + c] = ov;
-    if (c == 0) a.part_ml[row] = make_float2(M, lv);
+    if (c == 0) a.part_ml[row] = make_float2(mM[h], mL[h]);
   }
 }
 
@@ -1013,7 +1159,8 @@ static KernelInfo kernel_info(int G) {
   constexpr int NSTAGE = Stages<FMT>::kN;
   const int GS = (G + 3) & ~3;
   const size_t plan = cta_smem_bytes<FMT, D, kWarps, NSTAGE>(GS);
-  const size_t merge = align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 + 2 * (size_t)kWarps * GS * 4;
+  const size_t merge =
+      align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 + 2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4;
   return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps, NSTAGE>), plan > merge ? plan : merge,
           kWarps * 32};
 }
