@@ -17,9 +17,10 @@
 //    split) and all G query heads of that kv head; each of its W warps streams
 //    its own pages (page p0 + w, p0 + w + W, ...), PPI pages per iteration,
 //    with its own online-softmax state; the warps merge in shared memory.
-//  * each warp runs an NSTAGE-deep ring of bulk asynchronous copies
-//    (cp.async.bulk + mbarrier): one copy per block, the K and V blocks of PPI
-//    pages per stage; no register staging, no TMA multicast.
+//  * each warp runs two rings of bulk asynchronous copies (cp.async.bulk +
+//    mbarrier), one copy per block: K blocks two iterations ahead, V blocks
+//    one (a V block is read only after the K phase and the softmax of its
+//    iteration); no register staging, no TMA multicast.
 //  * QK^T: A = K (16 tokens x 16 channels, built in registers from the codes),
 //    B = Q^T (16 channels x 8 heads, fp16, loaded once).  PV: A = V^T (16
 //    channels x 16 tokens, built in registers), B = P^T (fp16 hi + lo split of
@@ -27,12 +28,13 @@
 //    fp32 accumulation; the layouts in include/kvq.h make every A register one
 //    or two byte-permutes of shared-memory words.  The PPI pages of an
 //    iteration are independent mma chains the scheduler interleaves.
-//  * CB2 outliers: a code slot holding an outlier stores 0.  Up to 16 channels
-//    with outliers are packed into one k16 tile of deltas (x - c0, split into
-//    fp16 hi + lo): one more mma against the gathered query columns corrects
-//    the scores, and one mma of the delta tile against P^T gives the output
-//    correction of those channels, accumulated in shared memory with the same
-//    online-softmax rescaling as the registers.  No atomics.
+//  * CB2 outliers: a code slot holding an outlier stores code 0 (value c0).
+//    Up to 16 channels with outliers form one k16 tile; the correction
+//    x - c0 is applied as two mma with exact fp16 operands (+ the e4m3
+//    values, - c0 where the token mask is set) against the gathered query
+//    columns (scores) or against P^T (output of those channels, accumulated
+//    in shared memory with the same online-softmax rescaling as the
+//    registers).  No atomics.
 //  * the partial last page of page formats (fp32 staging) is done on CUDA
 //    cores in fp32.
 #pragma once
@@ -40,7 +42,7 @@
 
 namespace kvq {
 
-constexpr int kOutPrefetch = 96;      // bytes of a CB2 outlier side-list fetched with its block
+constexpr int kOutPrefetch = 128;     // bytes of a CB2 outlier side-list fetched with its block (up to 6 channels)
 constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 
 template <int FMT>
@@ -69,25 +71,40 @@ __host__ __device__ constexpr int half_slot_bytes() {
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-// Shared-memory plan: [qsm: D x GS fp32][zero block, page formats] then per warp:
-// [stages: NSTAGE x PPI x 2 blocks][mbar x NSTAGE][meta x NSTAGE*PPI][ds 16 x GS, INT4 only][psm 16 x GS]
-// [corr D x GS, formats with outliers]
+// Per-warp copy rings: K blocks run kK iterations ahead, V blocks kV (a V
+// block is needed only after the iteration's K phase and softmax, so a
+// shallower V ring still hides the fetch and leaves room for more CTAs).
 template <int FMT>
-__host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kMain == kBlkInt4; }
-template <int FMT, int D, int NSTAGE>
+struct Ring {
+  static constexpr int kK = Fmt<FMT>::kPPI == 1 ? 3 : 2;
+  static constexpr int kV = Fmt<FMT>::kPPI == 1 ? 2 : Fmt<FMT>::kPaged ? 1 : 2;
+};
+
+// Shared-memory plan: [mbarriers: W x (kK + kV)][qsm: D x GS fp32][zero block, page formats]
+// then per warp: [K slots: kK x PPI blocks][V slots: kV x PPI blocks][meta: kK x PPI]
+// [ds 16 x GS, INT4 only][psm 16 x GS][corr D x GS, formats with outliers].
+// The CTA merge reuses everything after qsm, so the mbarriers sit before it.
+template <int FMT>
+__host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kOutliers; }
+template <int FMT, int D>
 __host__ __device__ constexpr int warp_smem_bytes(int GS) {
-  return NSTAGE * Fmt<FMT>::kPPI * 2 * half_slot_bytes<FMT, D>() + 8 * NSTAGE +
-         align16(4 * NSTAGE * Fmt<FMT>::kPPI) + (has_ds<FMT>() ? 16 * GS * 4 : 0) + 16 * GS * 4 +
-         (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
+  return (Ring<FMT>::kK + Ring<FMT>::kV) * Fmt<FMT>::kPPI * half_slot_bytes<FMT, D>() +
+         align16(4 * Ring<FMT>::kK * Fmt<FMT>::kPPI) +
+         (has_ds<FMT>() ? 16 * GS * 4 : 0) + 16 * GS * 4 + (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
 }
 // Page formats keep one zeroed block (K and V both read it) for absent pages.
 template <int FMT, int D>
 __host__ __device__ constexpr int zero_block_bytes() {
   return Fmt<FMT>::kPaged ? align16(half_slot_bytes<FMT, D>()) : 0;
 }
-template <int FMT, int D, int W, int NSTAGE>
+template <int FMT, int W>
+__host__ __device__ constexpr int mbar_bytes() {
+  return align16(8 * W * (Ring<FMT>::kK + Ring<FMT>::kV));
+}
+template <int FMT, int D, int W>
 __host__ __device__ constexpr int cta_smem_bytes(int GS) {
-  return align16(D * GS * 4) + zero_block_bytes<FMT, D>() + W * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
+  return mbar_bytes<FMT, W>() + align16(D * GS * 4) + zero_block_bytes<FMT, D>() +
+         W * align16(warp_smem_bytes<FMT, D>(GS));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -195,14 +212,13 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
 // (e4m3) and c0 (fp16) are exact in fp16, so it is computed as two mma with
 // exact operands: + values, - c0 where flagged.
 //
-// The side-list is read through a generic pointer -- shared memory when it fits
-// the bytes fetched with the block, global memory otherwise -- so one copy of
-// the correction code serves both.
-struct SideList {
-  const uint8_t* p;
-  __device__ __forceinline__ uint32_t u8(int off) const { return p[off]; }
-  __device__ __forceinline__ uint32_t u16(int off) const { return *reinterpret_cast<const uint16_t*>(p + off); }
-  __device__ __forceinline__ uint32_t u32(int off) const { return *reinterpret_cast<const uint32_t*>(p + off); }
+// The side-list is read from shared memory when it fits the bytes fetched with
+// the block; a longer one (rare) goes through the scalar path further down.
+struct SmemBytes {
+  uint32_t a;
+  __device__ __forceinline__ uint32_t u8(int off) const { return lds8(a + off); }
+  __device__ __forceinline__ uint32_t u16(int off) const { return lds16(a + off); }
+  __device__ __forceinline__ uint32_t u32(int off) const { return lds32(a + off); }
 };
 
 // {c0, c0}: fp16 bits of centroid 0 of codebook slot `slot` (the slot's (L, H)
@@ -457,10 +473,46 @@ struct WarpSmem {
   float* psm;        // [16][GS] probabilities of the current page (INT4, fp32 tail)
   float* corr;       // [D][GS] V-outlier output correction (rescaled with o)
   uint32_t qsm_s, corr_s;  // the same two arrays as shared-window addresses
-  const uint8_t* stages;   // the warp's stage ring (generic), and its shared-window address
-  uint32_t stages_s;
   int G, GS;
 };
+
+// CB2 side-lists longer than the bytes fetched with their block (rare: many
+// channels with outliers) are read from global memory and applied one outlier
+// at a time through shared-memory atomics -- compact code, kept apart from the
+// tensor-core path.  K: ds[t][h] += q[h][c] * (x - c0[c]).
+template <int D>
+__device__ __forceinline__ void cb2_scalar_k(const uint8_t* hdr, uint32_t kb_s, const WarpSmem& sm, int lane) {
+  const int n_ch = min((int)hdr[0], D), R = n_ch + (n_ch & 1), V0 = 4 + 4 * n_ch;
+#pragma unroll 1
+  for (int e = lane; e < 16 * n_ch; e += 32) {
+    const int i = e >> 4, t = e & 15;
+    const uint32_t rec = *reinterpret_cast<const uint32_t*>(hdr + 4 + 4 * i);
+    if ((rec >> (16 + t)) & 1u) {
+      const int c = rec & (D - 1);
+      const float x = __half2float(u32_as_h2(e4m3x2_to_f16x2(hdr[V0 + t * R + i])).x);
+      const float d = x - fp16_bits_to_float(c0_bits<D>(kb_s, c));
+#pragma unroll 1
+      for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.ds[t * sm.GS + h], sm.qsm[c * sm.GS + h] * d);
+    }
+  }
+}
+// V: corr[c][h] += p[t][h] * (x - c0[c]), with p of the page in psm[t][h].
+template <int D>
+__device__ __forceinline__ void cb2_scalar_v(const uint8_t* hdr, uint32_t vb_s, const WarpSmem& sm, int lane) {
+  const int n_ch = min((int)hdr[0], D), V0 = 4 + 4 * n_ch;
+#pragma unroll 1
+  for (int e = lane; e < 16 * n_ch; e += 32) {
+    const int i = e >> 4, t = e & 15;
+    const uint32_t rec = *reinterpret_cast<const uint32_t*>(hdr + 4 + 4 * i);
+    if ((rec >> (16 + t)) & 1u) {
+      const int c = rec & (D - 1);
+      const float x = __half2float(u32_as_h2(e4m3x2_to_f16x2(hdr[V0 + 16 * i + t])).x);
+      const float d = x - fp16_bits_to_float(c0_bits<D>(vb_s, cb2_slot(1, c)));
+#pragma unroll 1
+      for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.corr[c * sm.GS + h], sm.psm[t * sm.GS + h] * d);
+    }
+  }
+}
 
 // ----------------------------------------------------------------------------- per-iteration processing
 constexpr int32_t kBadEntry = 0x7FFFFFFF;  // page-table entry that failed validation
@@ -525,11 +577,11 @@ __device__ __forceinline__ T pick(const T (&x)[N], int i) {
 // The outlier corrections run page by page through one copy of their code
 // (a rolled loop), which keeps the loop body small enough for the
 // instruction cache.
-template <int FMT, int D, int NT, int PPI>
+template <int FMT, int D, int NT, int PPI, class KDone, class VWait>
 __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
                                          const uint32_t (&kb_s)[PPI], const uint32_t (&vb_s)[PPI],
                                          const int32_t (&ent)[PPI], const int (&ntok)[PPI], const DecodeArgs& a,
-                                         int kvh, const WarpSmem& sm, int lane) {
+                                         int kvh, const WarpSmem& sm, int lane, KDone&& k_done, VWait&& v_wait) {
   constexpr int NS = D / 16;
   constexpr bool T = FMT == KVQ_FMT_TIERED;
   const int g = lane >> 2, q4 = lane & 3;
@@ -570,13 +622,15 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     const uint32_t kbs = pick(kb_s, p);
     const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(kbs + cb2_out_off(D));
     if (n_ch > 0) {
-      const uint8_t* hdr = cb2_side_bytes(min(n_ch, D)) > kOutPrefetch
-                               ? block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D)
-                               : sm.stages + (kbs - sm.stages_s) + cb2_out_off(D);
       float c[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-      cb2_k_correct<D, NT>(SideList{hdr}, kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
+      if (cb2_side_bytes(min(n_ch, D)) > kOutPrefetch) {
+        cb2_scalar_k<D>(block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D), kbs, sm, lane);
+        apply_ds<NT>(c, sm.ds, sm.G, sm.GS, g, q4);
+      } else {
+        cb2_k_correct<D, NT>(SmemBytes{kbs + cb2_out_off(D)}, kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
+      }
 #pragma unroll
       for (int pp = 0; pp < PPI; ++pp)
 #pragma unroll
@@ -586,8 +640,10 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     }
   }
 
+  k_done();   // the K blocks are no longer read
   uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
   softmax_frags<D, NT, PPI>(st, acc, ntok, a.scale_log2, sm, lane, true, phi, plo);
+  v_wait();
 
   uint32_t vc[PPI][NS / 2];
   float sv[PPI];
@@ -625,23 +681,35 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     const uint32_t vbs = pick(vb_s, p);
     const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(vbs + cb2_out_off(D));
     if (n_ch > 0) {
-      const uint8_t* hdr = cb2_side_bytes(min(n_ch, D)) > kOutPrefetch
-                               ? block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D)
-                               : sm.stages + (vbs - sm.stages_s) + cb2_out_off(D);
-      uint32_t ph[NT][2], pl[NT][2];
+      if (cb2_side_bytes(min(n_ch, D)) > kOutPrefetch) {
+        float pcur[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          ph[nt][k] = phi[0][nt][k];
-          pl[nt][k] = plo[0][nt][k];
+          for (int r = 0; r < 4; ++r) {
+            pcur[nt][r] = acc[0][nt][r];
 #pragma unroll
-          for (int pp = 1; pp < PPI; ++pp) {
-            ph[nt][k] = pp == p ? phi[pp][nt][k] : ph[nt][k];
-            pl[nt][k] = pp == p ? plo[pp][nt][k] : pl[nt][k];
+            for (int q = 1; q < PPI; ++q) pcur[nt][r] = q == p ? acc[q][nt][r] : pcur[nt][r];
           }
-        }
-      cb2_v_correct<D, NT>(SideList{hdr}, vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
+        store_p<NT>(pcur, sm.psm, sm.G, sm.GS, g, q4);
+        __syncwarp();
+        cb2_scalar_v<D>(block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D), vbs, sm, lane);
+      } else {
+        uint32_t ph[NT][2], pl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            ph[nt][k] = phi[0][nt][k];
+            pl[nt][k] = plo[0][nt][k];
+#pragma unroll
+            for (int q = 1; q < PPI; ++q) {
+              ph[nt][k] = q == p ? phi[q][nt][k] : ph[nt][k];
+              pl[nt][k] = q == p ? plo[q][nt][k] : pl[nt][k];
+            }
+          }
+        cb2_v_correct<D, NT>(SmemBytes{vbs + cb2_out_off(D)}, vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
+      }
       __syncwarp();
     }
   }
@@ -658,10 +726,11 @@ __device__ __forceinline__ void load_e2m1_words(uint32_t blk_s, int lane, uint32
 }
 
 // E2M1 pages (per-token format: the last page may hold fewer than 16 tokens).
-template <int D, int NT, int PPI>
+template <int D, int NT, int PPI, class KDone, class VWait>
 __device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
                                           const uint32_t (&kb_s)[PPI], const uint32_t (&vb_s)[PPI],
-                                          const int (&ntok)[PPI], float scale, const WarpSmem& sm, int lane) {
+                                          const int (&ntok)[PPI], float scale, const WarpSmem& sm, int lane,
+                                          KDone&& k_done, VWait&& v_wait) {
   constexpr int NS = D / 16;
   const int g = lane >> 2, q4 = lane & 3;
   float acc[PPI][NT][4];
@@ -685,8 +754,10 @@ __device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
     }
+  k_done();
   uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
   softmax_frags<D, NT, PPI>(st, acc, ntok, scale, sm, lane, false, phi, plo);
+  v_wait();
   // token masks of the page's valid slots (per-token formats: the last page may be partial)
   bool full = true;
   uint32_t m01[PPI], m23[PPI];
@@ -730,9 +801,10 @@ __device__ __forceinline__ void iter_e2m1(WarpState<D, NT>& st, const uint32_t (
 }
 
 // One INT4 page (per-token format; fp16 outliers in per-token slots).
-template <int D, int NT>
+template <int D, int NT, class KDone, class VWait>
 __device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2], const uint8_t* kb,
-                                          const uint8_t* vb, int ntok_, float scale, const WarpSmem& sm, int lane) {
+                                          const uint8_t* vb, int ntok_, float scale, const WarpSmem& sm, int lane,
+                                          KDone&& k_done, VWait&& v_wait) {
   constexpr int NS = D / 16, CAP = int4_cap(D), NG = D / 32;
   const int g = lane >> 2, q4 = lane & 3;
   const int ntok[1] = {ntok_};
@@ -770,8 +842,10 @@ __device__ __forceinline__ void iter_int4(WarpState<D, NT>& st, const uint32_t (
     }
     apply_ds<NT>(acc[0], sm.ds, sm.G, sm.GS, g, q4);
   }
+  k_done();
   uint32_t phi[1][NT][2], plo[1][NT][2];
   softmax_frags<D, NT, 1>(st, acc, ntok, scale, sm, lane, true, phi, plo);
+  v_wait();
   uint32_t vw[NS];
   load_e2m1_words<D>(vb_s, lane, vw);
 #pragma unroll
@@ -857,13 +931,13 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
 // as many for G <= 8).
 template <int FMT, int D, int NT>
 __host__ __device__ constexpr int min_ctas_per_sm() {
-  return NT == 2 ? 2 : (D == 64 && Fmt<FMT>::kMain != kBlkInt4) ? 4 : 3;
+  return NT == 2 ? 2 : Fmt<FMT>::kMain == kBlkInt4 ? 3 : 4;
 }
 
-template <int FMT, int D, int NT, int W, int NSTAGE>
+template <int FMT, int D, int NT, int W>
 __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_split_kernel(const DecodeArgs a) {
   using F = Fmt<FMT>;
-  constexpr int NS = D / 16, PPI = F::kPPI;
+  constexpr int NS = D / 16, PPI = F::kPPI, NK = Ring<FMT>::kK, NV = Ring<FMT>::kV;
   constexpr int HS = half_slot_bytes<FMT, D>();
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -872,25 +946,26 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = a.G, GS = (G + 3) & ~3;
 
-  float* qsm = reinterpret_cast<float*>(smem);
-  uint8_t* zb = smem + align16(D * GS * 4);
-  uint8_t* wb = zb + zero_block_bytes<FMT, D>() + w * align16(warp_smem_bytes<FMT, D, NSTAGE>(GS));
-  uint8_t* stages = wb;
-  const uint32_t stages_s = smem_u32(stages);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(wb + NSTAGE * PPI * 2 * HS);
-  int32_t* meta = reinterpret_cast<int32_t*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem) + w * (NK + NV);
+  uint64_t* vbar = kbar + NK;
+  uint8_t* const base = smem + mbar_bytes<FMT, W>();   // everything from here on is reused by the merge
+  float* qsm = reinterpret_cast<float*>(base);
+  uint8_t* zb = base + align16(D * GS * 4);
+  uint8_t* wb = zb + zero_block_bytes<FMT, D>() + w * align16(warp_smem_bytes<FMT, D>(GS));
+  uint8_t* kslots = wb;                    // NK x PPI K blocks
+  uint8_t* vslots = wb + NK * PPI * HS;    // NV x PPI V blocks
+  const uint32_t kslots_s = smem_u32(kslots), vslots_s = smem_u32(vslots);
+  int32_t* meta = reinterpret_cast<int32_t*>(wb + (NK + NV) * PPI * HS);
   WarpSmem sm;
   sm.qsm = qsm;
-  sm.ds = reinterpret_cast<float*>(wb + NSTAGE * PPI * 2 * HS + 8 * NSTAGE + align16(4 * NSTAGE * PPI));
+  sm.ds = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(meta) + align16(4 * NK * PPI));
   sm.psm = sm.ds + (has_ds<FMT>() ? 16 * GS : 0);
   sm.corr = sm.psm + 16 * GS;
   sm.qsm_s = smem_u32(qsm);
   sm.corr_s = smem_u32(sm.corr);
-  sm.stages = stages;
-  sm.stages_s = stages_s;
-  const uint32_t zb_s = smem_u32(zb);
   sm.G = G;
   sm.GS = GS;
+  const uint32_t zb_s = smem_u32(zb);
 
   // query of the CTA's G heads: fp32 in shared memory as [D][GS] (outlier
   // corrections gather its columns), fp16 B fragments in registers
@@ -906,7 +981,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   if (F::kOutliers)
     for (int i = lane; i < D * GS; i += 32) sm.corr[i] = 0.f;
   if (lane == 0) {
-    for (int j = 0; j < NSTAGE; ++j) mbar_init(&mbar[j], 1);
+    for (int j = 0; j < NK + NV; ++j) mbar_init(&kbar[j], 1);
     fence_mbar_init();
   }
 
@@ -954,10 +1029,13 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   int win_base = 0;
   int win = lane < n_local ? pt[p0 + w + lane * W] : 0;
 
-  // Stage `it` of the ring: the K and V blocks of local pages it*PPI .. it*PPI+PPI-1.
-  auto issue = [&](int it) {
+  // K copies of iteration `it` (local pages it*PPI .. it*PPI+PPI-1): validates
+  // the page-table entries and records them in meta for the V copies and the
+  // iteration itself.
+  int k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
+  auto issue_k = [&](int it) {
     if (it >= n_iter) return;
-    const int slot = it % NSTAGE;
+    const int slot = it % NK;
     int32_t ent[PPI];
 #pragma unroll
     for (int j = 0; j < PPI; ++j) {
@@ -992,66 +1070,114 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
           }
         }
         meta[slot * PPI + j] = m;
-        total += 2 * bytes[j];
+        total += bytes[j];
       }
       fence_proxy_async();
       if (total == 0) {
-        mbar_arrive(&mbar[slot]);
+        mbar_arrive(&kbar[slot]);
       } else {
-        mbar_arrive_expect_tx(&mbar[slot], total);
+        mbar_arrive_expect_tx(&kbar[slot], total);
 #pragma unroll
         for (int j = 0; j < PPI; ++j)
-          if (bytes[j]) {
-            uint8_t* dst = stages + (slot * PPI + j) * 2 * HS;
-            bulk_g2s(dst, block_src<FMT, D>(a, kvh, ent[j], 0), bytes[j], &mbar[slot]);
-            bulk_g2s(dst + HS, block_src<FMT, D>(a, kvh, ent[j], 1), bytes[j], &mbar[slot]);
-          }
+          if (bytes[j]) bulk_g2s(kslots + (slot * PPI + j) * HS, block_src<FMT, D>(a, kvh, ent[j], 0), bytes[j],
+                                 &kbar[slot]);
       }
     }
+    __syncwarp();
+    ++k_issued;
+  };
+  // V copies of iteration `it`; its entries were recorded by issue_k(it),
+  // which ran earlier and whose meta slot is rewritten only by issue_k(it + NK).
+  auto issue_v = [&](int it) {
+    if (it >= n_iter) return;
+    const int slot = it % NV, kslot = it % NK;
+    if (lane == 0) {
+      uint32_t bytes[PPI], total = 0;
+      int32_t ent[PPI];
+#pragma unroll
+      for (int j = 0; j < PPI; ++j) {
+        ent[j] = meta[kslot * PPI + j];
+        bytes[j] = (ent[j] == kNoPage || ent[j] == kBadEntry) ? 0u
+                   : (FMT == KVQ_FMT_TIERED && ent[j] < 0) ? (uint32_t)fetch_bytes<D>(kBlkFp8)
+                                                           : (uint32_t)fetch_bytes<D>(F::kMain);
+        total += bytes[j];
+      }
+      fence_proxy_async();
+      if (total == 0) {
+        mbar_arrive(&vbar[slot]);
+      } else {
+        mbar_arrive_expect_tx(&vbar[slot], total);
+#pragma unroll
+        for (int j = 0; j < PPI; ++j)
+          if (bytes[j]) bulk_g2s(vslots + (slot * PPI + j) * HS, block_src<FMT, D>(a, kvh, ent[j], 1), bytes[j],
+                                 &vbar[slot]);
+      }
+    }
+    __syncwarp();
+    ++v_issued;
   };
 
 #pragma unroll 1
-  for (int it = 0; it < NSTAGE; ++it) issue(it);
+  for (int it = 0; it < NK; ++it) issue_k(it);
+#pragma unroll 1
+  for (int it = 0; it < NV; ++it) issue_v(it);
 
   bool timed_out = false;
-  int it = 0;
 #pragma unroll 1
-  for (; it < n_iter; ++it) {
-    const int slot = it % NSTAGE;
-    const bool ok = mbar_wait_bounded(&mbar[slot], (it / NSTAGE) & 1, kWaitLimitNs);
+  for (int it = 0; it < n_iter; ++it) {
+    const int ks = it % NK, vs = it % NV;
+    const bool ok = mbar_wait_bounded(&kbar[ks], (it / NK) & 1, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) {
       timed_out = true;
-      if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
       break;
     }
+    ++k_waited;
     int32_t ent[PPI];
     int ntok[PPI];
     uint32_t kb_s[PPI], vb_s[PPI];
 #pragma unroll
     for (int j = 0; j < PPI; ++j) {
-      ent[j] = meta[slot * PPI + j];
+      ent[j] = meta[ks * PPI + j];
       const int page = p0 + w + (it * PPI + j) * W;
       ntok[j] = (ent[j] == kBadEntry || ent[j] == kNoPage) ? 0 : (F::kPaged ? kPage : min(kPage, L - kPage * page));
-      kb_s[j] = stages_s + (slot * PPI + j) * 2 * HS;
-      vb_s[j] = kb_s[j] + HS;
+      kb_s[j] = kslots_s + (ks * PPI + j) * HS;
+      vb_s[j] = vslots_s + (vs * PPI + j) * HS;
       if (F::kPaged && ntok[j] == 0) kb_s[j] = vb_s[j] = zb_s;
     }
+    // k_done: the K slot is free, refill it; v_wait: the V blocks must have landed
+    auto k_done = [&]() {
+      __syncwarp();
+      issue_k(it + NK);
+    };
+    bool v_ok = true;
+    auto v_wait = [&]() {
+      v_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[vs], (it / NV) & 1, kWaitLimitNs));
+      v_waited += v_ok;
+    };
     if constexpr (F::kMain == kBlkCb2) {
-      iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane);
+      iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
     } else if constexpr (F::kMain == kBlkE2m1) {
-      iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane);
+      iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane, k_done, v_wait);
     } else {
-      const uint8_t* kb = stages + slot * 2 * HS;
-      iter_int4<D, NT>(st, qf, kb, kb + HS, ntok[0], a.scale_log2, sm, lane);
+      iter_int4<D, NT>(st, qf, kslots + ks * HS, vslots + vs * HS, ntok[0], a.scale_log2, sm, lane, k_done,
+                       v_wait);
+    }
+    if (!v_ok) {
+      timed_out = true;
+      break;
     }
     __syncwarp();
-    issue(it + NSTAGE);
+    issue_v(it + NV);
   }
   if (timed_out) {
+    if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
     // let copies still in flight land (bounded) before the CTA can exit
-    for (int j = it; j < min(it + NSTAGE, n_iter); ++j)
-      mbar_wait_bounded(&mbar[j % NSTAGE], (j / NSTAGE) & 1, kWaitLimitNs);
+    for (int j = k_waited; j < k_issued; ++j) mbar_wait_bounded(&kbar[j % NK], (j / NK) & 1, kWaitLimitNs);
+    for (int j = v_waited; j < v_issued; ++j) mbar_wait_bounded(&vbar[j % NV], (j / NV) & 1, kWaitLimitNs);
   }
+  __syncwarp();
+  if (!timed_out && lane == 0)
+    for (int j = 0; j < NK + NV; ++j) mbar_inval(&kbar[j]);
 
   // partial last page of a page format, from fp32 staging
   if (F::kPaged && (L % kPage) != 0 && !timed_out) {
@@ -1086,7 +1212,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   __syncthreads();
   // merge area (reuses the stages): mo [W][GS][D], mm / ml [W][GS] (mm turns
   // into the warps' weights), mM / mL [GS]
-  float* mo = reinterpret_cast<float*>(smem + align16(D * GS * 4));
+  float* mo = reinterpret_cast<float*>(base + align16(D * GS * 4));
   float* mm = mo + W * GS * D;
   float* ml = mm + W * GS;
   float* mM = ml + W * GS;
@@ -1143,11 +1269,6 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
 
 // ----------------------------------------------------------------------------- launch configuration
 constexpr int kWarps = kWarpsPerCta;
-template <int FMT>
-struct Stages {
-  static constexpr int kN = Fmt<FMT>::kPPI == 1 ? 3 : 2;   // ring depth (stages of PPI pages)
-};
-
 struct KernelInfo {
   void* fn;
   size_t smem;
@@ -1156,12 +1277,11 @@ struct KernelInfo {
 
 template <int FMT, int D, int NT>
 static KernelInfo kernel_info(int G) {
-  constexpr int NSTAGE = Stages<FMT>::kN;
   const int GS = (G + 3) & ~3;
-  const size_t plan = cta_smem_bytes<FMT, D, kWarps, NSTAGE>(GS);
-  const size_t merge =
-      align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 + 2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4;
-  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps, NSTAGE>), plan > merge ? plan : merge,
+  const size_t plan = cta_smem_bytes<FMT, D, kWarps>(GS);
+  const size_t merge = mbar_bytes<FMT, kWarps>() + align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 +
+                       2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4;
+  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps>), plan > merge ? plan : merge,
           kWarps * 32};
 }
 

@@ -91,6 +91,29 @@ def test_decode_attention_parity(fmt, D, G):
     assert pair.gpu.status_word() == 0
 
 
+@pytest.mark.parametrize("fmt", [CB2, TIERED])
+@pytest.mark.parametrize("D,dist", [(64, "student_t4"), (128, "student_t4"), (128, "normal")])
+def test_decode_side_lists_longer_than_prefetch(fmt, D, dist):
+    """Outlier side-lists longer than the 128 bytes the decode kernel fetches
+    with each block are read from global memory by its scalar correction path.
+    Heavy tails, or no dominant outlier channels, spread the outliers over many
+    channels and make such blocks common."""
+    B, Hkv, P, G = 2, 2, 10, 8
+    lens = [150, 97]
+    pair = Pair(fmt, B, Hkv, D, P, seed=12, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(13, B, max(lens), Hkv, D, dist, 0, 1.0)
+    pair.append(k, v, t_per_seq=lens)
+    blocks = pair.ref.pool.reshape(-1, pair.ref.stride)
+    nch = blocks[:, 12 * D].astype(np.int64)
+    side = 4 + 4 * nch + 16 * (nch + (nch & 1))
+    assert (side > 128).sum() >= 2
+    for splits in (0, 3):
+        for od in (torch.float32, torch.bfloat16):
+            got, exp = pair.decode(Hkv * G, seed=splits, num_splits=splits, out_dtype=od)
+            assert_attention_close(got, exp, od)
+    assert pair.gpu.status_word() == 0
+
+
 @pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED])
 def test_decode_after_token_by_token_appends(fmt):
     """Decode after every single-token append (the serving loop), crossing page boundaries."""
