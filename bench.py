@@ -102,7 +102,7 @@ def algorithmic_bytes(built: workloads.Built) -> dict:
         # CB2 block: codes + codebook (12D) + side-list header, records and values
         pool = cache.pool.view(-1, cache.block_bytes(0))
         nch = pool[:, 12 * D].to(torch.int64)
-        side = (4 + 4 * nch + 16 * (nch + (nch & 1))).sum().item()
+        side = (4 + 20 * nch).sum().item()
         n_tier = int(built.tiers[:, :full].sum()) * w.Hkv * 2
         n_main = full * blocks - n_tier
         cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
@@ -288,7 +288,7 @@ def oracle_sample(w: synth.Workload, seed: int):
     if w.fmt in (synth.FMT_CB2, synth.FMT_TIERED):
         blocks = ref.pool.reshape(-1, ref.stride).astype(np.int64)
         nch = blocks[:, 12 * D]
-        side = int((4 + 4 * nch + 16 * (nch + (nch & 1))).sum())
+        side = int((4 + 20 * nch).sum())
         n_tier = (int(tiers[:, :full].sum()) if tiers is not None else 0) * w.Hkv * 2
         cache = (full * w.Hkv * 2 - n_tier) * 12 * D + side + n_tier * (16 * D + 4)
         cache += (N % 16) * D * 4 * w.Hkv * 2

@@ -71,8 +71,8 @@ typedef enum {
     /* [P1] per (page, channel) 4-centroid fp16 codebook fitted by Lloyd-Max
      * (k-means in one dimension, linspace start) over the page's non-outliers;
      * per-token outliers (sigma rule over the head vector) kept as FP8 E4M3 in
-     * a per-page side-list: one (channel, token mask) record per channel
-     * holding outliers, and their values.  Quantized when a page fills; the partial last
+     * a per-page side-list: one (channel, token mask, 16 values) record per
+     * channel holding outliers.  Quantized when a page fills; the partial last
      * page waits in fp32 staging. */
     KVQ_FMT_CB2_OUTLIER = 2,
     /* [P2] KVQ_FMT_CB2_OUTLIER pages plus FP8 E4M3 pages with one fp32 scale per
@@ -264,11 +264,12 @@ const char* kvq_version(void);
  *                       K: sigma(c) = c;  V: sigma(c) = 16*(c/16) + 2*(c%8) + (c%16)/8
  *             12D       outlier side-list, grouped by channel: u8 n_ch (channels
  *                       holding an outlier), u8 total (outliers), 2 zero bytes;
- *                       n_ch records {u8 channel, 0, u16 token mask}, channels
- *                       ascending; then at V0 = 12D + 4 + 4*n_ch a 16 x R byte
- *                       matrix (R = n_ch rounded up to even) of the e4m3 values,
- *                       0 where a token is not an outlier of the channel:
- *                       K: value(t, i) at V0 + t*R + i;  V: at V0 + 16*i + t
+ *                       then n_ch 20-byte records at 12D + 4 + 20*i, channels
+ *                       ascending: {u8 channel, 0, u16 token mask, u8 value[16]},
+ *                       value[t] = e4m3 of the outlier at token t, 0 where t is
+ *                       not an outlier of the channel (K and V alike).  The first
+ *                       six records travel with the block's codes; decode reads
+ *                       further ones six at a time.
  *             stride 2176 (D=64), 4224 (D=128)
  *   FP8 tier  [0, 16D)  codes: lane l at 8*NS*l, step s at +8s, slot k = byte k (e4m3)
  *             16D       fp32 scale

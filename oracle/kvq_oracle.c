@@ -293,14 +293,12 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /*                               K: sigma(c) = c                              */
 /*                               V: sigma(c) = 16*(c/16) + 2*(c%8) + (c%16)/8 */
 /*            outliers at 12D    u8 n_ch (channels holding an outlier),       */
-/*                               u8 total (outliers), 2 zero bytes; n_ch      */
-/*                               records {u8 channel, 0, u16 token mask},     */
-/*                               channels ascending; then at V0 = 4 + 4*n_ch  */
-/*                               a 16 x R byte matrix (R = n_ch rounded up to */
-/*                               even) of e4m3 values, 0 where the token is   */
-/*                               not an outlier of that channel:              */
-/*                               K: value(t, i) at V0 + t*R + i (token-major) */
-/*                               V: value(t, i) at V0 + i*16 + t              */
+/*                               u8 total (outliers), 2 zero bytes; then n_ch */
+/*                               20-byte records, channels ascending:         */
+/*                               {u8 channel, 0, u16 token mask, u8 value[16]}*/
+/*                               value[t] = e4m3 of the outlier at token t,   */
+/*                               0 where t is not an outlier of the channel   */
+/*                               (record i at 4 + 20*i; K and V alike)        */
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
 /*            scale at 16D       fp32                                         */
@@ -318,7 +316,7 @@ EXPORT int or_block_stride(int fmt, int D)
     switch (fmt) {
     case OR_INT4: return round128(10 * D + 16 + 48 * cap);
     case OR_E2M1: return round128(9 * D);
-    case OR_CB2:  return round128(12 * D + 4 + 4 * D + 16 * D);
+    case OR_CB2:  return round128(12 * D + 4 + 20 * D);
     case OR_FP8:  return round128(16 * D + 16);
     }
     return -1;
@@ -512,34 +510,26 @@ static void quantize_page_cb2(const float* x, int D, double sigma, int iters, in
         for (int t = 0; t < 16; ++t)
             cb2_code_set(blk, D, role, t, c, mask[t][c] ? 0 : codes[n++]);
     }
-    /* side-list grouped by channel: a record {channel, 0, token mask} for each
-     * channel holding an outlier, then a dense 16 x R matrix of their e4m3
-     * values (0 elsewhere), token-major for K, channel-major for V */
+    /* side-list grouped by channel: one 20-byte record {channel, 0, token
+     * mask, 16 e4m3 values (0 where the token is not an outlier)} for each
+     * channel holding an outlier, channels ascending */
     uint8_t* hdr = blk + 12 * D;
     int n_ch = 0, total = 0;
-    for (int c = 0; c < D; ++c) {
-        int any = 0;
-        for (int t = 0; t < 16; ++t) any |= mask[t][c];
-        n_ch += any;
-    }
-    int R = n_ch + (n_ch & 1);
-    uint8_t* val = hdr + 4 + 4 * n_ch;
-    int i = 0;
     for (int c = 0; c < D; ++c) {
         unsigned tmask = 0;
         for (int t = 0; t < 16; ++t)
             if (mask[t][c]) tmask |= 1u << t;
         if (!tmask) continue;
-        uint8_t* rec = hdr + 4 + 4 * i;
+        uint8_t* rec = hdr + 4 + 20 * n_ch;
         rec[0] = (uint8_t)c;
         rec[1] = 0;
         put_u16(rec + 2, (uint16_t)tmask);
         for (int t = 0; t < 16; ++t)
             if (mask[t][c]) {
-                val[role == 0 ? t * R + i : i * 16 + t] = or_e4m3_encode((double)x[t * D + c]);
+                rec[4 + t] = or_e4m3_encode((double)x[t * D + c]);
                 ++total;
             }
-        ++i;
+        ++n_ch;
     }
     hdr[0] = (uint8_t)n_ch;
     hdr[1] = (uint8_t)total;
@@ -595,14 +585,13 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
     }
     if (fmt == OR_CB2) {
         const uint8_t* hdr = blk + 12 * D;
-        int n_ch = hdr[0], R = n_ch + (n_ch & 1);
-        const uint8_t* val = hdr + 4 + 4 * n_ch;
+        int n_ch = hdr[0];
         for (int i = 0; i < n_ch; ++i) {
-            const uint8_t* rec = hdr + 4 + 4 * i;
+            const uint8_t* rec = hdr + 4 + 20 * i;
             unsigned tmask = get_u16(rec + 2);
             for (int t = 0; t < 16 && t < ntok; ++t)
                 if (tmask & (1u << t))
-                    out[t * D + rec[0]] = (float)or_e4m3_decode(val[role == 0 ? t * R + i : i * 16 + t]);
+                    out[t * D + rec[0]] = (float)or_e4m3_decode(rec[4 + t]);
         }
     }
 }

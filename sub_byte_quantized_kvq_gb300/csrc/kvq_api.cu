@@ -80,12 +80,10 @@ __global__ void dequantize_kernel(const DequantArgs a) {
       v = dq_f16(cb[q] | (cb[4 + q] << 8));
       const uint8_t* hdr = blk + cb2_out_off(D);
       const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
-      const int R = n_ch + (n_ch & 1);
       for (int i = 0; i < n_ch; ++i) {
-        const uint8_t* rec = hdr + 4 + 4 * i;
+        const uint8_t* rec = hdr + 4 + 20 * i;
         const uint32_t tm = rec[2] | (rec[3] << 8);
-        if (rec[0] == c && (tm >> t & 1u))
-          v = dq_e4m3(hdr[4 + 4 * n_ch + (a.role == 0 ? t * R + i : 16 * i + t)]);
+        if (rec[0] == c && (tm >> t & 1u)) v = dq_e4m3(rec[4 + t]);
       }
     } else {
       float s;

@@ -35,7 +35,7 @@ __host__ __device__ constexpr int fp8_sc_off(int D) { return 16 * D; }
 __host__ __device__ constexpr int block_stride(int fmt, int D) {
   return fmt == kBlkInt4 ? round_up128(10 * D + 16 + 48 * int4_cap(D))
        : fmt == kBlkE2m1 ? round_up128(9 * D)
-       : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 4 * D + 16 * D)
+       : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 20 * D)
                          : round_up128(16 * D + 16);
 }
 
@@ -98,6 +98,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
+}
+
+// m16n8k8 fp16 x fp16 -> fp32, D += A * B.
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(b0));
 }
 
 // m16n8k16 fp16 x fp16 -> fp32, D += A * B.

@@ -42,7 +42,7 @@
 
 namespace kvq {
 
-constexpr int kOutPrefetch = 128;     // bytes of a CB2 outlier side-list fetched with its block (up to 6 channels)
+constexpr int kOutPrefetch = 128;     // bytes of a CB2 outlier side-list fetched with its block
 constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 
 template <int FMT>
@@ -85,7 +85,7 @@ struct Ring {
 // [ds 16 x GS, INT4 only][psm 16 x GS][corr D x GS, formats with outliers].
 // The CTA merge reuses everything after qsm, so the mbarriers sit before it.
 template <int FMT>
-__host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kOutliers; }
+__host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kMain == kBlkInt4; }
 template <int FMT, int D>
 __host__ __device__ constexpr int warp_smem_bytes(int GS) {
   return (Ring<FMT>::kK + Ring<FMT>::kV) * Fmt<FMT>::kPPI * half_slot_bytes<FMT, D>() +
@@ -203,23 +203,20 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
 }
 
 // ----------------------------------------------------------------------------- CB2 outlier corrections
-// Side-list of a CB2 block (at 12D): {u8 n_ch, u8 total, 0, 0}, n_ch records
-// {u8 channel, 0, u16 token mask}, then a 16 x R matrix (R = n_ch rounded up
-// to even) of e4m3 values, 0 where a token is not an outlier of the channel:
-// token-major (t*R + i) in K blocks, channel-major (16*i + t) in V blocks.
+// Side-list of a CB2 block (at 12D): {u8 n_ch, u8 total, 0, 0}, then n_ch
+// 20-byte records {u8 channel, 0, u16 token mask, u8 value[16]} (e4m3 values,
+// 0 where the token is not an outlier of the channel), channels ascending.
 // A code slot holding an outlier stores code 0 (value c0 of its channel), so
-// the correction of a channel is sum over its outliers of (x - c0); both x
-// (e4m3) and c0 (fp16) are exact in fp16, so it is computed as two mma with
-// exact operands: + values, - c0 where flagged.
+// the correction of a channel is the sum over its outliers of (x - c0).  Both
+// x (e4m3) and c0 (fp16) are exact in fp16, so it is applied as mma with exact
+// operands: + the values, - c0 where the token mask is set.
 //
-// The side-list is read from shared memory when it fits the bytes fetched with
-// the block; a longer one (rare) goes through the scalar path further down.
-struct SmemBytes {
-  uint32_t a;
-  __device__ __forceinline__ uint32_t u8(int off) const { return lds8(a + off); }
-  __device__ __forceinline__ uint32_t u16(int off) const { return lds16(a + off); }
-  __device__ __forceinline__ uint32_t u32(int off) const { return lds32(a + off); }
-};
+// Records go kChunk at a time: the first chunk arrives with the block's codes
+// (the prefetched bytes), later ones (rare: many channels with outliers) are
+// copied from global memory into a per-warp bounce buffer, and the same code
+// runs on every chunk.
+constexpr int kChunk = 6;   // records per chunk
+static_assert(4 + 20 * kChunk <= kOutPrefetch, "the first chunk must arrive with its block");
 
 // {c0, c0}: fp16 bits of centroid 0 of codebook slot `slot` (the slot's (L, H)
 // byte planes hold its low and high bytes at byte 0).
@@ -229,96 +226,80 @@ __device__ __forceinline__ uint32_t c0_bits(uint32_t blk_s, int slot) {
   return prmt(lh.x, lh.y, 0x4040u);
 }
 
-// Scores of tokens g, g+8: += sum over outlier channels c of q[h][c] * (x - c0[c]).
-// Channels go 16 at a time into one k16 tile (A = tokens x slots), B = Q^T
-// gathered at the slots' channels.
-template <int D, int NT, class Mem>
-__device__ __forceinline__ void cb2_k_correct(const Mem hdr, uint32_t kb_s, uint32_t qsm_s, int G, int GS, int lane,
-                                              float (&acc)[NT][4]) {
+// Scores of tokens g, g + 8 += sum over the chunk's channels c of
+// q[h][c] * (x - c0[c]): one m16n8k8 tile, A = tokens x slots (slot i = the
+// chunk's record i; slots >= nc are zero), B = Q^T gathered at the slots'
+// channels.  recs: shared address of the chunk's first record.
+template <int D, int NT>
+__device__ __forceinline__ void cb2_k_correct(uint32_t recs, int nc, uint32_t kb_s, uint32_t qsm_s, int G, int GS,
+                                              int lane, float (&acc)[NT][4]) {
   const int g = lane >> 2, q4 = lane & 3;
-  const int n_ch = min((int)hdr.u8(0), D), R = n_ch + (n_ch & 1), V0 = 4 + 4 * n_ch;
-  for (int base = 0; base < n_ch; base += 16) {
-    const int ia = base + 2 * q4, ib = ia + 8;  // slots ia, ia+1 (A cols of a0/a1), ib, ib+1 (a2/a3)
-    uint32_t rec[4];
-    rec[0] = ia < n_ch ? hdr.u32(4 + 4 * ia) : 0u;
-    rec[1] = ia + 1 < n_ch ? hdr.u32(8 + 4 * ia) : 0u;
-    rec[2] = ib < n_ch ? hdr.u32(4 + 4 * ib) : 0u;
-    rec[3] = ib + 1 < n_ch ? hdr.u32(8 + 4 * ib) : 0u;
-    // + outlier values (pairs of adjacent slots at one token; the pad column is 0)
-    uint32_t ax[4];
-    ax[0] = ia < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + g * R + ia)) : 0u;
-    ax[1] = ia < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + (g + 8) * R + ia)) : 0u;
-    ax[2] = ib < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + g * R + ib)) : 0u;
-    ax[3] = ib < n_ch ? e4m3x2_to_f16x2(hdr.u16(V0 + (g + 8) * R + ib)) : 0u;
-    // - c0 where the token is an outlier of the slot's channel.  Token masks:
-    // shifting (m_a | m_b << 16) left by 7-g puts bit g / g+8 of m_a / m_b in the
-    // sign bits of bytes 0 / 1 / 2 / 3; prmt's sign-replicate mode widens them.
-    const uint32_t c01 = prmt(c0_bits<D>(kb_s, rec[0] & (D - 1)), c0_bits<D>(kb_s, rec[1] & (D - 1)), 0x5410u) ^ 0x80008000u;
-    const uint32_t c23 = prmt(c0_bits<D>(kb_s, rec[2] & (D - 1)), c0_bits<D>(kb_s, rec[3] & (D - 1)), 0x5410u) ^ 0x80008000u;
-    const uint32_t x01 = prmt(rec[0], rec[1], 0x7632u) << (7 - g);
-    const uint32_t x23 = prmt(rec[2], rec[3], 0x7632u) << (7 - g);
-    const uint32_t ac0 = c01 & prmt(x01, 0u, 0xAA88u), ac1 = c01 & prmt(x01, 0u, 0xBB99u);
-    const uint32_t ac2 = c23 & prmt(x23, 0u, 0xAA88u), ac3 = c23 & prmt(x23, 0u, 0xBB99u);
+  const int ia = 2 * q4;   // this lane's slots ia, ia + 1
+  const bool va = ia < nc, vb = ia + 1 < nc;
+  const uint32_t ra = recs + 20 * ia, rb = ra + 20;
+  const uint32_t hA = va ? lds32(ra) : 0u, hB = vb ? lds32(rb) : 0u;   // {channel, 0, token mask}
+  // + outlier values: a0 = tokens g, a1 = tokens g + 8 (slot ia low, ia + 1 high)
+  const uint32_t x0 = (va ? lds8(ra + 4 + g) : 0u) | ((vb ? lds8(rb + 4 + g) : 0u) << 8);
+  const uint32_t x1 = (va ? lds8(ra + 12 + g) : 0u) | ((vb ? lds8(rb + 12 + g) : 0u) << 8);
+  const uint32_t a0 = e4m3x2_to_f16x2(x0), a1 = e4m3x2_to_f16x2(x1);
+  // - c0 where flagged: shifting (mask_A | mask_B << 16) left by 7 - g puts
+  // bits g / g + 8 of each mask in the sign bits of bytes 0 / 1 (A) and 2 / 3
+  // (B); prmt's sign-replicate mode widens them into half masks.
+  const uint32_t c01 =
+      prmt(c0_bits<D>(kb_s, hA & (D - 1)), c0_bits<D>(kb_s, hB & (D - 1)), 0x5410u) ^ 0x80008000u;
+  const uint32_t xm = prmt(hA, hB, 0x7632u) << (7 - g);
+  const uint32_t n0 = c01 & prmt(xm, 0u, 0xAA88u), n1 = c01 & prmt(xm, 0u, 0xBB99u);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h = nt * 8 + g;
-      float qv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) qv[k] = (h < G && rec[k]) ? ldsf(qsm_s + 4 * ((rec[k] & (D - 1)) * GS + h)) : 0.f;
-      const uint32_t b0 = h2_as_u32(__floats2half2_rn(qv[0], qv[1]));
-      const uint32_t b1 = h2_as_u32(__floats2half2_rn(qv[2], qv[3]));
-      mma16816(acc[nt], ax[0], ax[1], ax[2], ax[3], b0, b1);
-      mma16816(acc[nt], ac0, ac1, ac2, ac3, b0, b1);
-    }
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + g;
+    const float qa = (h < G && va) ? ldsf(qsm_s + 4 * ((hA & (D - 1)) * GS + h)) : 0.f;
+    const float qb = (h < G && vb) ? ldsf(qsm_s + 4 * ((hB & (D - 1)) * GS + h)) : 0.f;
+    const uint32_t b0 = h2_as_u32(__floats2half2_rn(qa, qb));
+    mma1688(acc[nt], a0, a1, b0);
+    mma1688(acc[nt], n0, n1, b0);
   }
 }
 
-// Output correction of the outlier channels: corr[c][h] += sum_t p[t][h] * (x - c0[c]).
-// A = (slots x tokens) against the page's P^T fragments; each (channel, head)
-// is written by exactly one lane.
-template <int D, int NT, class Mem>
-__device__ __forceinline__ void cb2_v_correct(const Mem hdr, uint32_t vb_s, const uint32_t (&phi)[NT][2],
-                                              const uint32_t (&plo)[NT][2], uint32_t corr_s, int G, int GS, int lane) {
+// Output correction of the chunk's channels: corr[c][h] += sum_t p[t][h] *
+// (x - c0[c]).  A = slots x tokens (row g = slot g; rows 8..15 are empty)
+// against the page's P^T fragments; each (channel, head) is written by one lane.
+template <int D, int NT>
+__device__ __forceinline__ void cb2_v_correct(uint32_t recs, int nc, uint32_t vb_s, const uint32_t (&phi)[NT][2],
+                                              const uint32_t (&plo)[NT][2], uint32_t corr_s, int G, int GS,
+                                              int lane) {
   const int g = lane >> 2, q4 = lane & 3;
-  const int n_ch = min((int)hdr.u8(0), D), V0 = 4 + 4 * n_ch;
   const int t0 = 2 * q4;
-  for (int base = 0; base < n_ch; base += 16) {
-    const int i0 = base + g, i1 = i0 + 8;
-    const uint32_t r0 = i0 < n_ch ? hdr.u32(4 + 4 * i0) : 0u;
-    const uint32_t r1 = i1 < n_ch ? hdr.u32(4 + 4 * i1) : 0u;
-    const int ch0 = r0 & (D - 1), ch1 = r1 & (D - 1);
-    uint32_t ax[4];
-    ax[0] = r0 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i0 + t0)) : 0u;
-    ax[1] = r1 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i1 + t0)) : 0u;
-    ax[2] = r0 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i0 + t0 + 8)) : 0u;
-    ax[3] = r1 ? e4m3x2_to_f16x2(hdr.u16(V0 + 16 * i1 + t0 + 8)) : 0u;
-    // token masks: with w = m0 | m1 << 16, (w << 7-t0) / (w << 6-t0) hold bits
-    // t0 / t0+1 (and +8, of m0 / m1) in the sign bits of their bytes
-    const uint32_t w = prmt(r0, r1, 0x7632u);
-    const uint32_t x = w << (7 - t0), y = w << (6 - t0);
-    const uint32_t c0 = c0_bits<D>(vb_s, cb2_slot(1, ch0)) ^ 0x80008000u;
-    const uint32_t c1 = c0_bits<D>(vb_s, cb2_slot(1, ch1)) ^ 0x80008000u;
-    const uint32_t ac0 = c0 & prmt(x, y, 0xCC88u), ac2 = c0 & prmt(x, y, 0xDD99u);
-    const uint32_t ac1 = c1 & prmt(x, y, 0xEEAAu), ac3 = c1 & prmt(x, y, 0xFFBBu);
+  const bool on = g < nc;   // every lane takes part in the mma; rows >= nc are zero
+  const uint32_t r = recs + 20 * g;
+  const uint32_t hr = on ? lds32(r) : 0u;
+  const int ch = hr & (D - 1);
+  const uint32_t a0 = on ? e4m3x2_to_f16x2(lds16(r + 4 + t0)) : 0u;
+  const uint32_t a2 = on ? e4m3x2_to_f16x2(lds16(r + 12 + t0)) : 0u;
+  // token masks: (mask << 7 - t0) / (mask << 6 - t0) hold bits t0 / t0 + 1 (and
+  // + 8) in the sign bits of bytes 0 (and 1)
+  const uint32_t m = hr >> 16, x = m << (7 - t0), y = m << (6 - t0);
+  const uint32_t c0 = c0_bits<D>(vb_s, cb2_slot(1, ch)) ^ 0x80008000u;
+  const uint32_t n0 = c0 & prmt(x, y, 0xCC88u), n2 = c0 & prmt(x, y, 0xDD99u);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(c, ax[0], ax[1], ax[2], ax[3], phi[nt][0], phi[nt][1]);
-      mma16816(c, ax[0], ax[1], ax[2], ax[3], plo[nt][0], plo[nt][1]);
-      mma16816(c, ac0, ac1, ac2, ac3, phi[nt][0], phi[nt][1]);
-      mma16816(c, ac0, ac1, ac2, ac3, plo[nt][0], plo[nt][1]);
-      const int h0 = nt * 8 + 2 * q4;
-      const uint32_t a0 = corr_s + 4 * (ch0 * GS + h0), a1 = corr_s + 4 * (ch1 * GS + h0);
-      if (r0) {
-        if (h0 < G) sts32(a0, __float_as_uint(ldsf(a0) + c[0]));
-        if (h0 + 1 < G) sts32(a0 + 4, __float_as_uint(ldsf(a0 + 4) + c[1]));
-      }
-      if (r1) {
-        if (h0 < G) sts32(a1, __float_as_uint(ldsf(a1) + c[2]));
-        if (h0 + 1 < G) sts32(a1 + 4, __float_as_uint(ldsf(a1 + 4) + c[3]));
-      }
-    }
+  for (int nt = 0; nt < NT; ++nt) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16816(c, a0, 0u, a2, 0u, phi[nt][0], phi[nt][1]);
+    mma16816(c, a0, 0u, a2, 0u, plo[nt][0], plo[nt][1]);
+    mma16816(c, n0, 0u, n2, 0u, phi[nt][0], phi[nt][1]);
+    mma16816(c, n0, 0u, n2, 0u, plo[nt][0], plo[nt][1]);
+    const int h0 = nt * 8 + t0;
+    const uint32_t ad = corr_s + 4 * (ch * GS + h0);
+    if (on && h0 < G) sts32(ad, __float_as_uint(ldsf(ad) + c[0]));
+    if (on && h0 + 1 < G) sts32(ad + 4, __float_as_uint(ldsf(ad + 4) + c[1]));
   }
+}
+
+// Copy records [base, base + nc) of a side-list from global memory into the
+// warp's bounce buffer (nc <= kChunk; 5 * nc u32 words).
+__device__ __forceinline__ void cb2_bounce(const uint8_t* side, int base, int nc, uint32_t bounce_s, int lane) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(side + 4 + 20 * base);
+  if (lane < 5 * nc) sts32(bounce_s + 4 * lane, src[lane]);
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------------------- online softmax
@@ -473,46 +454,9 @@ struct WarpSmem {
   float* psm;        // [16][GS] probabilities of the current page (INT4, fp32 tail)
   float* corr;       // [D][GS] V-outlier output correction (rescaled with o)
   uint32_t qsm_s, corr_s;  // the same two arrays as shared-window addresses
+  uint32_t bounce_s;       // CB2 side-list records beyond the prefetch (the psm area)
   int G, GS;
 };
-
-// CB2 side-lists longer than the bytes fetched with their block (rare: many
-// channels with outliers) are read from global memory and applied one outlier
-// at a time through shared-memory atomics -- compact code, kept apart from the
-// tensor-core path.  K: ds[t][h] += q[h][c] * (x - c0[c]).
-template <int D>
-__device__ __forceinline__ void cb2_scalar_k(const uint8_t* hdr, uint32_t kb_s, const WarpSmem& sm, int lane) {
-  const int n_ch = min((int)hdr[0], D), R = n_ch + (n_ch & 1), V0 = 4 + 4 * n_ch;
-#pragma unroll 1
-  for (int e = lane; e < 16 * n_ch; e += 32) {
-    const int i = e >> 4, t = e & 15;
-    const uint32_t rec = *reinterpret_cast<const uint32_t*>(hdr + 4 + 4 * i);
-    if ((rec >> (16 + t)) & 1u) {
-      const int c = rec & (D - 1);
-      const float x = __half2float(u32_as_h2(e4m3x2_to_f16x2(hdr[V0 + t * R + i])).x);
-      const float d = x - fp16_bits_to_float(c0_bits<D>(kb_s, c));
-#pragma unroll 1
-      for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.ds[t * sm.GS + h], sm.qsm[c * sm.GS + h] * d);
-    }
-  }
-}
-// V: corr[c][h] += p[t][h] * (x - c0[c]), with p of the page in psm[t][h].
-template <int D>
-__device__ __forceinline__ void cb2_scalar_v(const uint8_t* hdr, uint32_t vb_s, const WarpSmem& sm, int lane) {
-  const int n_ch = min((int)hdr[0], D), V0 = 4 + 4 * n_ch;
-#pragma unroll 1
-  for (int e = lane; e < 16 * n_ch; e += 32) {
-    const int i = e >> 4, t = e & 15;
-    const uint32_t rec = *reinterpret_cast<const uint32_t*>(hdr + 4 + 4 * i);
-    if ((rec >> (16 + t)) & 1u) {
-      const int c = rec & (D - 1);
-      const float x = __half2float(u32_as_h2(e4m3x2_to_f16x2(hdr[V0 + 16 * i + t])).x);
-      const float d = x - fp16_bits_to_float(c0_bits<D>(vb_s, cb2_slot(1, c)));
-#pragma unroll 1
-      for (int h = 0; h < sm.G; ++h) atomicAdd(&sm.corr[c * sm.GS + h], sm.psm[t * sm.GS + h] * d);
-    }
-  }
-}
 
 // ----------------------------------------------------------------------------- per-iteration processing
 constexpr int32_t kBadEntry = 0x7FFFFFFF;  // page-table entry that failed validation
@@ -558,9 +502,6 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
 #pragma unroll
   for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
 }
-
-// Bytes of a CB2 side-list with n_ch channels.
-__device__ __forceinline__ int cb2_side_bytes(int n_ch) { return 4 + 4 * n_ch + 16 * (n_ch + (n_ch & 1)); }
 
 // x[i] for a runtime i (selects; keeps small register arrays in registers).
 template <int N, class T>
@@ -620,16 +561,21 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll 1
   for (int p = 0; p < PPI; ++p) {
     const uint32_t kbs = pick(kb_s, p);
-    const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(kbs + cb2_out_off(D));
+    const int n_ch = (T && pick(tier, p)) ? 0 : min((int)lds8(kbs + cb2_out_off(D)), D);
     if (n_ch > 0) {
       float c[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-      if (cb2_side_bytes(min(n_ch, D)) > kOutPrefetch) {
-        cb2_scalar_k<D>(block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D), kbs, sm, lane);
-        apply_ds<NT>(c, sm.ds, sm.G, sm.GS, g, q4);
-      } else {
-        cb2_k_correct<D, NT>(SmemBytes{kbs + cb2_out_off(D)}, kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
+#pragma unroll 1
+      for (int base = 0; base < n_ch; base += kChunk) {
+        uint32_t recs = kbs + cb2_out_off(D) + 4;
+        if (base > 0) {
+          cb2_bounce(block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D), base, min(kChunk, n_ch - base),
+                     sm.bounce_s, lane);
+          recs = sm.bounce_s;
+        }
+        cb2_k_correct<D, NT>(recs, min(kChunk, n_ch - base), kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
+        __syncwarp();
       }
 #pragma unroll
       for (int pp = 0; pp < PPI; ++pp)
@@ -679,38 +625,32 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll 1
   for (int p = 0; p < PPI; ++p) {
     const uint32_t vbs = pick(vb_s, p);
-    const int n_ch = (T && pick(tier, p)) ? 0 : (int)lds8(vbs + cb2_out_off(D));
+    const int n_ch = (T && pick(tier, p)) ? 0 : min((int)lds8(vbs + cb2_out_off(D)), D);
     if (n_ch > 0) {
-      if (cb2_side_bytes(min(n_ch, D)) > kOutPrefetch) {
-        float pcur[NT][4];
+      uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            pcur[nt][r] = acc[0][nt][r];
+        for (int k = 0; k < 2; ++k) {
+          ph[nt][k] = phi[0][nt][k];
+          pl[nt][k] = plo[0][nt][k];
 #pragma unroll
-            for (int q = 1; q < PPI; ++q) pcur[nt][r] = q == p ? acc[q][nt][r] : pcur[nt][r];
+          for (int q = 1; q < PPI; ++q) {
+            ph[nt][k] = q == p ? phi[q][nt][k] : ph[nt][k];
+            pl[nt][k] = q == p ? plo[q][nt][k] : pl[nt][k];
           }
-        store_p<NT>(pcur, sm.psm, sm.G, sm.GS, g, q4);
+        }
+#pragma unroll 1
+      for (int base = 0; base < n_ch; base += kChunk) {
+        uint32_t recs = vbs + cb2_out_off(D) + 4;
+        if (base > 0) {
+          cb2_bounce(block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D), base, min(kChunk, n_ch - base),
+                     sm.bounce_s, lane);
+          recs = sm.bounce_s;
+        }
+        cb2_v_correct<D, NT>(recs, min(kChunk, n_ch - base), vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
         __syncwarp();
-        cb2_scalar_v<D>(block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D), vbs, sm, lane);
-      } else {
-        uint32_t ph[NT][2], pl[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            ph[nt][k] = phi[0][nt][k];
-            pl[nt][k] = plo[0][nt][k];
-#pragma unroll
-            for (int q = 1; q < PPI; ++q) {
-              ph[nt][k] = q == p ? phi[q][nt][k] : ph[nt][k];
-              pl[nt][k] = q == p ? plo[q][nt][k] : pl[nt][k];
-            }
-          }
-        cb2_v_correct<D, NT>(SmemBytes{vbs + cb2_out_off(D)}, vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
       }
-      __syncwarp();
     }
   }
 }
@@ -963,6 +903,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   sm.corr = sm.psm + 16 * GS;
   sm.qsm_s = smem_u32(qsm);
   sm.corr_s = smem_u32(sm.corr);
+  sm.bounce_s = smem_u32(sm.psm);
   sm.G = G;
   sm.GS = GS;
   const uint32_t zb_s = smem_u32(zb);

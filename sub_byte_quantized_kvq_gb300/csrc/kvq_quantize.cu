@@ -358,20 +358,19 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         if (lane >= d) { ich += a1; ival += a2; }
       }
       const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
-      const int R = tot_ch + (tot_ch & 1);
       uint8_t* hdr = blk + cb2_out_off(D);
-      uint8_t* val = hdr + 4 + 4 * tot_ch;   // dense 16 x R values; zeros from the block clear
       int ci = ich - nch;
       for (int k = 0; k < CPL; ++k) {
         if (!tm[k]) continue;
         const int c = lane * CPL + k;
-        uint8_t* rec = hdr + 4 + 4 * ci;
+        // 20-byte record {channel, 0, token mask, 16 values}; zeros from the block clear
+        uint8_t* rec = hdr + 4 + 20 * ci;
         rec[0] = (uint8_t)c;
         rec[1] = 0;
         rec[2] = (uint8_t)(tm[k] & 0xFF);
         rec[3] = (uint8_t)(tm[k] >> 8);
         for (int t = 0; t < 16; ++t)
-          if (tm[k] >> t & 1u) val[role == 0 ? t * R + ci : ci * 16 + t] = f32_to_e4m3(xs[t][c]);
+          if (tm[k] >> t & 1u) rec[4 + t] = f32_to_e4m3(xs[t][c]);
         ++ci;
       }
       if (lane == 0) {

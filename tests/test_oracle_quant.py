@@ -217,22 +217,21 @@ def test_cb2_page_properties():
         blk = oracle.quantize_page(oracle.BLK_CB2, D, x, role=role)
         xh = oracle.dequantize_block(oracle.BLK_CB2, D, blk, role=role)
         masks = np.array([oracle.outlier_mask(x[t].astype(np.float64))[0] for t in range(16)])
-        # side-list grouped by channel: header {n_ch, total}, records
-        # {channel, 0, token mask} with channels ascending, then a dense 16 x R
-        # matrix of e4m3 values (token-major for K, channel-major for V)
+        # side-list grouped by channel: header {n_ch, total}, then one 20-byte
+        # record {channel, 0, token mask, 16 e4m3 values} per channel holding
+        # an outlier, channels ascending; values 0 where the token is not one
         chans = np.nonzero(masks.any(0))[0]
         hdr = blk[12 * D:]
         n = len(chans)
-        R = n + (n & 1)
         assert hdr[0] == n and hdr[1] == masks.sum()
         for i, c in enumerate(chans):
-            rec = hdr[4 + 4 * i:8 + 4 * i]
+            rec = hdr[4 + 20 * i:24 + 20 * i]
             assert rec[0] == c and rec[1] == 0
             assert int(rec[2]) | (int(rec[3]) << 8) == sum(1 << t for t in range(16) if masks[t, c])
             for t in range(16):
-                pos = 4 + 4 * n + (t * R + i if role == 0 else i * 16 + t)
                 want = oracle.e4m3_encode(float(x[t, c])) if masks[t, c] else 0
-                assert hdr[pos] == want
+                assert rec[4 + t] == want
+        assert not hdr[4 + 20 * n:].any()
         # outliers reproduced exactly as e4m3
         for t, c in zip(*np.nonzero(masks)):
             assert xh[t, c] == oracle.e4m3_decode(oracle.e4m3_encode(float(x[t, c])))
