@@ -173,24 +173,31 @@ kvq_status kvq_decode_num_splits(const kvq_config* cfg, int32_t num_q_heads, int
  *           (0 for an empty sequence).
  *   max_seq_len  host bound on seq_lens (sizes the split grid); tokens beyond it
  *           are ignored and flagged KVQ_STATUS_SEQ_TOO_LONG.
- *   num_splits   context splits per (sequence, kv head); 0 = library choice.
- *   workspace    device, >= kvq_decode_workspace_bytes(), 16-byte aligned,
- *           holds fp32 split partials; its contents need no initialisation.
- * A split kernel streams each page's packed blocks into shared memory with bulk
- * asynchronous copies, expands codes straight into tensor-core fragments,
- * corrects outliers, runs an online softmax and writes (m, l, o) partials; a
- * combine kernel merges the splits. */
+ *   num_splits   context splits per (sequence, kv head), at most 256
+ *           (KVQ_ERR_CAPACITY beyond); 0 = library choice.
+ *   workspace    device, >= kvq_decode_workspace_bytes(), 16-byte aligned:
+ *           fp32 split partials, then 4 * num_seqs * Hkv bytes of arrival
+ *           counters.  The counters must be zero before a workspace's first
+ *           use (zero the whole workspace once); every call leaves them zero
+ *           again, except one that sets KVQ_STATUS_TIMEOUT, after which the
+ *           workspace must be zeroed before its next use.  The partials need
+ *           no initialisation.
+ * One kernel launch: split CTAs stream each page's packed blocks into shared
+ * memory with bulk asynchronous copies, expand codes straight into
+ * tensor-core fragments, correct outliers, run an online softmax and write
+ * (m, l, o) partials; the last CTA of each (sequence, kv head) to finish
+ * (counted on its arrival counter) merges the splits into `out`. */
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q,
                                 int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,
                                 int32_t num_splits, void* out, kvq_dtype out_dtype, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* The two stages of kvq_decode_attention as separate calls (same arguments,
- * same resolution of num_splits = 0): kvq_decode_split writes the fp32 split
- * partials (m, l, o) of every (sequence, query head, split) into `workspace`;
- * kvq_decode_combine merges them into `out`.  Calling split then combine on
- * one stream is exactly kvq_decode_attention; the split is the HBM-bound
- * kernel, the combine reads only the partials. */
+/* The two stages of kvq_decode_attention as separate launches (same
+ * arguments, same resolution of num_splits = 0): kvq_decode_split writes the
+ * fp32 split partials (m, l, o) of every (sequence, query head, split) into
+ * `workspace` and leaves its arrival counters alone; kvq_decode_combine
+ * merges them into `out` with the same arithmetic as the fused merge, so
+ * split then combine on one stream gives kvq_decode_attention's result. */
 kvq_status kvq_decode_split(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
                             float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* workspace,
                             size_t workspace_bytes, void* stream);
@@ -215,7 +222,10 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
  *     make that first call before any stream capture.
  *   - Every call on a device shares the one scratch, which keeps the last
  *     call's contents; calls that may overlap on the GPU (different streams)
- *     race on it -- serialise them.  Nothing in it needs to start at zero. */
+ *     race on it -- serialise them.  The scratch starts zeroed, and its
+ *     arrival counters return to zero after every call (a call that sets
+ *     KVQ_STATUS_TIMEOUT may leave them set; this entry point offers no way
+ *     to clear them, so treat that status as fatal for it). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q,
                                         int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,

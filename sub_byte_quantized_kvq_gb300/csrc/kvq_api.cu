@@ -153,6 +153,13 @@ static int num_sms() {
 // 90% of its last wave of resident CTA slots (so no nearly empty final wave),
 // keeping at least 2 pages per warp in each split; otherwise the count with the
 // best last-wave fill.
+// Workspace layout: part_o fp32 [B][Hq][S][D], part_ml float2 [B][Hq][S],
+// then (16-byte aligned) the fused combine's arrival counters u32 [B][Hkv].
+static size_t arrivals_offset(const kvq_config* c, int num_q_heads, int S) {
+  const size_t rows = (size_t)c->num_seqs * num_q_heads * S;
+  return (rows * c->head_dim * sizeof(float) + rows * sizeof(float2) + 15) / 16 * 16;
+}
+
 static int auto_splits(const kvq_config* c, int G, int max_seq_len) {
   const long long pages = (max_seq_len + kPage - 1) / kPage;
   const long long units = (long long)c->num_seqs * c->num_kv_heads;
@@ -247,15 +254,15 @@ kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t num_q_heads
   if (!dim_supported(cfg) || num_q_heads / cfg->num_kv_heads > 16) return KVQ_ERR_UNSUPPORTED;
   int S = num_splits;
   if (S == 0) S = auto_splits(cfg, num_q_heads / cfg->num_kv_heads, max_seq_len);
-  const size_t rows = (size_t)cfg->num_seqs * num_q_heads * S;
-  *bytes = rows * cfg->head_dim * sizeof(float) + rows * sizeof(float2);
+  *bytes = arrivals_offset(cfg, num_q_heads, S) + (size_t)cfg->num_seqs * cfg->num_kv_heads * sizeof(uint32_t);
   return KVQ_OK;
 }
 
 }  // extern "C"
 
 namespace kvq {
-// Validate a decode request and fill the split kernel's arguments.
+// Validate a decode request and fill the split kernel's arguments (partials
+// only: out == nullptr).
 static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
                                  float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* workspace,
                                  size_t workspace_bytes, DecodeArgs& a) {
@@ -271,7 +278,7 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   if (st != KVQ_OK) return st;
   if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
   const int S = num_splits ? num_splits : auto_splits(cfg, G, max_seq_len);
-  if (S > 65535) return KVQ_ERR_CAPACITY;
+  if (S > kMaxSplits) return KVQ_ERR_CAPACITY;
   const int cap_len = cfg->pages_per_seq_max * kPage;
   const int len = max_seq_len < cap_len ? max_seq_len : cap_len;
   const int pages = (len + kPage - 1) / kPage;
@@ -296,6 +303,9 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.pps = pages > 0 ? (pages + S - 1) / S : 1;
   a.max_seq_len = len;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.out = nullptr;
+  a.out_dtype = KVQ_F32;
+  a.arrivals = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + arrivals_offset(cfg, num_q_heads, S));
   return KVQ_OK;
 }
 }  // namespace kvq
@@ -330,8 +340,9 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
   const int S = num_splits ? num_splits : auto_splits(cfg, num_q_heads / cfg->num_kv_heads, max_seq_len);
   const float* part_o = static_cast<const float*>(workspace);
   const float2* part_ml = reinterpret_cast<const float2*>(part_o + (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
-  if (decode_combine_launch(part_o, part_ml, cfg->num_seqs, num_q_heads, S, cfg->head_dim, out, out_dtype,
-                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (S > kMaxSplits) return KVQ_ERR_CAPACITY;
+  if (decode_combine_launch(part_o, part_ml, cfg->num_seqs, cfg->num_kv_heads, num_q_heads, S, cfg->head_dim, out,
+                            out_dtype, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -340,11 +351,15 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
                                 float softmax_scale, int32_t max_seq_len, int32_t num_splits, void* out,
                                 kvq_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
   if (!out || (out_dtype != KVQ_BF16 && out_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
-  kvq_status st = kvq_decode_split(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
-                                   workspace_bytes, stream);
+  DecodeArgs a;
+  kvq_status st = decode_prepare(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
+                                 workspace_bytes, a);
   if (st != KVQ_OK) return st;
-  return kvq_decode_combine(cfg, num_q_heads, max_seq_len, num_splits, workspace, workspace_bytes, out, out_dtype,
-                            stream);
+  a.out = out;   // one launch: the split kernel's last CTA per (sequence, kv head) merges the splits
+  a.out_dtype = out_dtype;
+  if (decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
 }
 
 kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t seq, int32_t kv_head, int32_t which,

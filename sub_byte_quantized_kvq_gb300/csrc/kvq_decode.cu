@@ -6,30 +6,12 @@
 namespace kvq {
 
 // ----------------------------------------------------------------------------- combine kernel
-// out[b][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max_s m_s (0 if no tokens).
-template <typename OutT>
+// One CTA per (kv head, sequence): the split merge of its G query heads.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __restrict__ part_o,
                                                              const float2* __restrict__ part_ml, int S, int D,
-                                                             int Hq, OutT* __restrict__ out) {
-  const size_t row = (size_t)blockIdx.y * Hq + blockIdx.x;
-  const float2* ml = part_ml + row * S;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[s].x);
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float acc = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float2 v = ml[s];
-        if (v.x == -INFINITY) continue;
-        const float f = exp2f(v.x - M);
-        L = fmaf(f, v.y, L);
-        acc = fmaf(f, part_o[(row * S + s) * D + c], acc);
-      }
-    }
-    const float r = L > 0.f ? acc / L : 0.f;
-    if constexpr (sizeof(OutT) == 2) out[row * D + c] = __float2bfloat16_rn(r);
-    else out[row * D + c] = r;
-  }
+                                                             int Hq, int G, void* out, int out_dtype) {
+  extern __shared__ float wts[];
+  merge_group(part_o, part_ml, (size_t)blockIdx.y * Hq + (size_t)blockIdx.x * G, G, S, D, out, out_dtype, wts);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -61,13 +43,11 @@ cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hq, int S, int D, void* out,
+cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hkv, int Hq, int S, int D, void* out,
                                   int out_dtype, cudaStream_t st) {
-  if (out_dtype == KVQ_F32)
-    decode_combine_kernel<float><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, S, D, Hq, static_cast<float*>(out));
-  else
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, S, D, Hq,
-                                                                        static_cast<__nv_bfloat16*>(out));
+  const int G = Hq / Hkv;
+  decode_combine_kernel<<<dim3(Hkv, B), 128, (size_t)(G * S + G) * sizeof(float), st>>>(part_o, part_ml, S, D, Hq, G,
+                                                                                       out, out_dtype);
   return cudaGetLastError();
 }
 

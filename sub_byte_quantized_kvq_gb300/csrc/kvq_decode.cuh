@@ -866,6 +866,71 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
   __syncwarp();
 }
 
+// ----------------------------------------------------------------------------- split merge
+// out[r] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the S split
+// partials of the G rows r0 .. r0 + G - 1 (M = max_s m_s; 0 if no split saw a
+// token).  Called by every thread of a CTA (blockDim.x a multiple of 32);
+// `wts` is shared scratch of G * S + G floats.  One warp per row reduces the
+// split maxima and sums in a fixed order, then every thread forms its outputs
+// with the split loads of a column in flight together.  Shared by the combine
+// kernel and the split kernel's fused merge, so both give the same bits.
+__device__ __forceinline__ void merge_group(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                                            size_t r0, int G, int S, int D, void* out, int out_dtype, float* wts) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  float* lsum = wts + G * S;
+  for (int i = tid; i < G * S; i += nthreads) wts[i] = part_ml[r0 * S + i].x;
+  __syncthreads();
+  for (int h = warp; h < G; h += nthreads >> 5) {
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, wts[h * S + s]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float m = wts[h * S + s];
+      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      wts[h * S + s] = wgt;
+      L = fmaf(wgt, part_ml[(r0 + h) * S + s].y, L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) lsum[h] = L;
+  }
+  __syncthreads();
+  // outputs: a thread takes 4 adjacent columns of one row and keeps 8 splits' loads in flight
+  const int D4 = D / 4;
+  for (int idx = tid; idx < G * D4; idx += nthreads) {
+    const int h = idx / D4, c4 = idx % D4;
+    const float4* po = reinterpret_cast<const float4*>(part_o + (r0 + h) * (size_t)S * D) + c4;
+    const float* wh = wts + h * S;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float wgt, const float4& v) {
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
+    };
+    int s = 0;
+    for (; s + 8 <= S; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = po[(size_t)(s + k) * D4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) add(wh[s + k], v[k]);
+    }
+    for (; s < S; ++s) add(wh[s], po[(size_t)s * D4]);
+    const float L = lsum[h];
+    const float r[4] = {L > 0.f ? acc.x / L : 0.f, L > 0.f ? acc.y / L : 0.f, L > 0.f ? acc.z / L : 0.f,
+                        L > 0.f ? acc.w / L : 0.f};
+    const size_t o = (r0 + h) * D + 4 * c4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[o + k] = __float2bfloat16_rn(r[k]);
+      else static_cast<float*>(out)[o + k] = r[k];
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------- split kernel
 // Resident CTAs per SM the register budget is cut for (shared memory allows
 // as many for G <= 8).
@@ -1206,6 +1271,18 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     a.part_o[row * D + c] = ov;
     if (c == 0) a.part_ml[row] = make_float2(mM[h], mL[h]);
   }
+
+  // ---- fused combine: the last CTA of this (sequence, kv head) to arrive merges the S partials
+  if (a.out == nullptr) return;
+  int* last = reinterpret_cast<int*>(mL + GS);
+  __threadfence();   // this CTA's partials are visible device-wide before it arrives
+  __syncthreads();
+  if (threadIdx.x == 0) *last = atomicAdd(&a.arrivals[(size_t)b * a.Hkv + kvh], 1u) == (uint32_t)(a.S - 1);
+  __syncthreads();
+  if (!*last) return;
+  __threadfence();
+  merge_group(a.part_o, a.part_ml, (size_t)b * a.Hq + (size_t)kvh * G, G, a.S, D, a.out, a.out_dtype, mo);
+  if (threadIdx.x == 0) a.arrivals[(size_t)b * a.Hkv + kvh] = 0u;   // ready for the next call
 }
 
 // ----------------------------------------------------------------------------- launch configuration
@@ -1221,7 +1298,7 @@ static KernelInfo kernel_info(int G) {
   const int GS = (G + 3) & ~3;
   const size_t plan = cta_smem_bytes<FMT, D, kWarps>(GS);
   const size_t merge = mbar_bytes<FMT, kWarps>() + align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 +
-                       2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4;
+                       2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4 + 16;
   return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps>), plan > merge ? plan : merge,
           kWarps * 32};
 }

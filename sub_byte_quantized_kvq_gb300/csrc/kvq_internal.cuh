@@ -5,6 +5,10 @@
 
 namespace kvq {
 
+// Largest split count: the split merge keeps G x S weights in the split
+// kernel's shared merge area (at least 4 D + 8 floats per query head).
+constexpr int kMaxSplits = 256;
+
 struct DecodeArgs {
   const uint8_t* pool;
   const uint8_t* tier_pool;
@@ -19,6 +23,12 @@ struct DecodeArgs {
   int S, pps;       // splits, pages per split
   int max_seq_len;
   float scale_log2; // softmax_scale * log2(e)
+  // Fused combine (kvq_decode_attention): the last split CTA of a (sequence,
+  // kv head) to finish merges the partials into `out`.  out == nullptr: the
+  // split kernel only writes partials (kvq_decode_split).
+  void* out;        // [B][Hq][D] in out_dtype
+  int out_dtype;    // KVQ_BF16 or KVQ_F32
+  uint32_t* arrivals;  // [B][Hkv] arrival counters, zero between calls
 };
 
 struct AppendArgs {
@@ -38,7 +48,7 @@ struct AppendArgs {
 
 // The split decode kernel, and the combine kernel (out_dtype KVQ_BF16 or KVQ_F32), on `st`.
 cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_t st);
-cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hq, int S, int D, void* out,
+cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hkv, int Hq, int S, int D, void* out,
                                   int out_dtype, cudaStream_t st);
 // Resident CTAs per SM of the split kernel for (format, head_dim, G); 0 on error.
 int decode_ctas_per_sm(int fmt, int D, int G);

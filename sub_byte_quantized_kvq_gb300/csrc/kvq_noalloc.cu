@@ -50,8 +50,8 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // before anything is enqueued
   void* scratch = scratch_on_current_device();
   if (!scratch) return KVQ_ERR_CUDA;
-  // Nothing in the scratch has to start at zero: the split kernel writes every
-  // partial (m, l, o) row before the combine kernel reads it.
+  // The scratch starts zeroed (static storage), so its arrival counters do;
+  // every call leaves them zero again.  The partials need no initialisation.
   return kvq_decode_attention(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, out, out_dtype,
                               scratch, (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -191,7 +191,8 @@ def kvq_decode_attention(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale
 
 def alloc_workspace(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int, num_splits: int = 0) -> torch.Tensor:
     nbytes = kvq_decode_workspace_bytes(cache, num_q_heads, max_seq_len, num_splits)
-    return torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=cache.device)
+    # zeroed once: its tail holds the fused split merge's arrival counters
+    return torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.float32, device=cache.device)
 
 
 def kvq_decode_split(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale: float, max_seq_len: int,

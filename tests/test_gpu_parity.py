@@ -91,6 +91,35 @@ def test_decode_attention_parity(fmt, D, G):
     assert pair.gpu.status_word() == 0
 
 
+@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED])
+def test_fused_merge_matches_split_then_combine(fmt):
+    """kvq_decode_attention merges the splits inside its one launch (the last
+    CTA of each (sequence, kv head) to arrive); kvq_decode_split followed by
+    kvq_decode_combine does it in a second kernel with the same arithmetic.
+    The results are identical, and repeated calls on one workspace work (the
+    arrival counters return to zero)."""
+    B, Hkv, D, P, G = 3, 2, 128, 14, 4
+    lens = [209, 77, 1]
+    pair = Pair(fmt, B, Hkv, D, P, seed=9, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(10, B, max(lens), Hkv, D, *_dist(fmt))
+    pair.append(k, v, t_per_seq=lens)
+    cache, Hq, L = pair.gpu, Hkv * G, max(lens)
+    from sub_byte_quantized_kvq_gb300 import synth
+    q = synth.queries_bf16(4, B, Hq, D, device="cuda")
+    for S in (1, 2, 5, 14):
+        ws = kvq.alloc_workspace(cache, Hq, L, S)
+        two = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        kvq.kvq_decode_split(cache, q, D ** -0.5, L, ws, S)
+        kvq.kvq_decode_combine(cache, Hq, L, ws, two, S)
+        for _ in range(3):
+            one = kvq.kvq_decode_attention(cache, q, D ** -0.5, L, S, out_dtype=torch.float32, workspace=ws)
+            torch.cuda.synchronize()
+            assert torch.equal(one, two), f"S={S}"
+        off = kvq.kvq_decode_workspace_bytes(cache, Hq, L, S) - 4 * B * Hkv   # the arrival counters
+        assert (ws.view(torch.int32)[off // 4:off // 4 + B * Hkv] == 0).all()
+    assert cache.status_word() == 0
+
+
 @pytest.mark.parametrize("fmt", [CB2, TIERED])
 @pytest.mark.parametrize("D,dist", [(64, "student_t4"), (128, "student_t4"), (128, "normal")])
 def test_decode_side_lists_longer_than_prefetch(fmt, D, dist):
