@@ -503,21 +503,11 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
   for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
 }
 
-// x[i] for a runtime i (selects; keeps small register arrays in registers).
-template <int N, class T>
-__device__ __forceinline__ T pick(const T (&x)[N], int i) {
-  T v = x[0];
-#pragma unroll
-  for (int k = 1; k < N; ++k) v = i == k ? x[k] : v;
-  return v;
-}
-
 // CB2 pages (and, for the tiered format, FP8 tier pages), PPI at a time.
 // kb_s / vb_s: shared addresses of the staged K / V blocks; an absent page
 // points at the CTA's zero block, so it needs no masking outside the softmax.
-// The outlier corrections run page by page through one copy of their code
-// (a rolled loop), which keeps the loop body small enough for the
-// instruction cache.
+// Each page's outlier corrections run over its side-list records in chunks of
+// kChunk (a rolled loop; one chunk in the common case).
 template <int FMT, int D, int NT, int PPI, class KDone, class VWait>
 __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&qf)[NT][D / 16][2],
                                          const uint32_t (&kb_s)[PPI], const uint32_t (&vb_s)[PPI],
@@ -558,31 +548,20 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
     }
   }
-#pragma unroll 1
+  // outlier corrections (the chunk loop is rolled; the pages are unrolled)
+#pragma unroll
   for (int p = 0; p < PPI; ++p) {
-    const uint32_t kbs = pick(kb_s, p);
-    const int n_ch = (T && pick(tier, p)) ? 0 : min((int)lds8(kbs + cb2_out_off(D)), D);
-    if (n_ch > 0) {
-      float c[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(kb_s[p] + cb2_out_off(D)), D);
 #pragma unroll 1
-      for (int base = 0; base < n_ch; base += kChunk) {
-        uint32_t recs = kbs + cb2_out_off(D) + 4;
-        if (base > 0) {
-          cb2_bounce(block_src<FMT, D>(a, kvh, pick(ent, p), 0) + cb2_out_off(D), base, min(kChunk, n_ch - base),
-                     sm.bounce_s, lane);
-          recs = sm.bounce_s;
-        }
-        cb2_k_correct<D, NT>(recs, min(kChunk, n_ch - base), kbs, sm.qsm_s, sm.G, sm.GS, lane, c);
-        __syncwarp();
+    for (int base = 0; base < n_ch; base += kChunk) {
+      uint32_t recs = kb_s[p] + cb2_out_off(D) + 4;
+      if (base > 0) {
+        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + cb2_out_off(D), base, min(kChunk, n_ch - base),
+                   sm.bounce_s, lane);
+        recs = sm.bounce_s;
       }
-#pragma unroll
-      for (int pp = 0; pp < PPI; ++pp)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) acc[pp][nt][r] += pp == p ? c[nt][r] : 0.f;
+      cb2_k_correct<D, NT>(recs, min(kChunk, n_ch - base), kb_s[p], sm.qsm_s, sm.G, sm.GS, lane, acc[p]);
+      __syncwarp();
     }
   }
 
@@ -622,35 +601,19 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         }
       }
     }
-#pragma unroll 1
+#pragma unroll
   for (int p = 0; p < PPI; ++p) {
-    const uint32_t vbs = pick(vb_s, p);
-    const int n_ch = (T && pick(tier, p)) ? 0 : min((int)lds8(vbs + cb2_out_off(D)), D);
-    if (n_ch > 0) {
-      uint32_t ph[NT][2], pl[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          ph[nt][k] = phi[0][nt][k];
-          pl[nt][k] = plo[0][nt][k];
-#pragma unroll
-          for (int q = 1; q < PPI; ++q) {
-            ph[nt][k] = q == p ? phi[q][nt][k] : ph[nt][k];
-            pl[nt][k] = q == p ? plo[q][nt][k] : pl[nt][k];
-          }
-        }
+    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + cb2_out_off(D)), D);
 #pragma unroll 1
-      for (int base = 0; base < n_ch; base += kChunk) {
-        uint32_t recs = vbs + cb2_out_off(D) + 4;
-        if (base > 0) {
-          cb2_bounce(block_src<FMT, D>(a, kvh, pick(ent, p), 1) + cb2_out_off(D), base, min(kChunk, n_ch - base),
-                     sm.bounce_s, lane);
-          recs = sm.bounce_s;
-        }
-        cb2_v_correct<D, NT>(recs, min(kChunk, n_ch - base), vbs, ph, pl, sm.corr_s, sm.G, sm.GS, lane);
-        __syncwarp();
+    for (int base = 0; base < n_ch; base += kChunk) {
+      uint32_t recs = vb_s[p] + cb2_out_off(D) + 4;
+      if (base > 0) {
+        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + cb2_out_off(D), base, min(kChunk, n_ch - base),
+                   sm.bounce_s, lane);
+        recs = sm.bounce_s;
       }
+      cb2_v_correct<D, NT>(recs, min(kChunk, n_ch - base), vb_s[p], phi[p], plo[p], sm.corr_s, sm.G, sm.GS, lane);
+      __syncwarp();
     }
   }
 }
