@@ -24,8 +24,8 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED = 0, 1, 2, 3
-BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8 = 0, 1, 2, 3
+FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S = 0, 1, 2, 3, 4
+BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8, BLK_CB2S = 0, 1, 2, 3, 4
 TIER_BIT = 1 << 31
 
 
@@ -44,7 +44,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("D", ctypes.c_int32), ("pages_per_seq_max", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("num_tier_pages", ctypes.c_int32),
-                ("iters", ctypes.c_int32), ("sigma", ctypes.c_double)]
+                ("iters", ctypes.c_int32), ("sigma", ctypes.c_double),
+                ("n_static", ctypes.c_int32), ("static_ch", ctypes.c_void_p)]
 
 
 def lib():
@@ -65,6 +66,8 @@ def lib():
                 "or_frag_pos": (None, [I, I, I, P, P, P]),
                 "or_quantize_token": (None, [I, I, D_, I, I, P, P]),
                 "or_quantize_page": (None, [I, I, D_, I, I, P, P]),
+                "or_quantize_page_static": (None, [I, I, I, P, P, I, P]),
+                "or_select_static": (None, [P, I, I, I, I, P]),
                 "or_dequantize_block": (None, [I, I, P, I, I, P]),
                 "or_append": (I, [P, P, P, P, P, P, P, P, I, P]),
                 "or_dequantize_range": (None, [P, P, P, P, P, P, I, I, I, I, I, P]),
@@ -134,6 +137,24 @@ def quantize_page(blk_fmt: int, D: int, x, role: int = 0, sigma: float = 3.0, it
     return blk
 
 
+def quantize_page_static(D: int, x, channels, role: int = 0, iters: int = 16) -> np.ndarray:
+    """CB2 page with static fp16 channels `channels` (ascending, at most 8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(16, D)
+    ch = np.ascontiguousarray(channels, dtype=np.uint8)
+    blk = np.zeros(block_stride(BLK_CB2S, D), np.uint8)
+    lib().or_quantize_page_static(D, iters, role, _p(x), _p(ch), len(ch), _p(blk))
+    return blk
+
+
+def select_static(x, n_s: int) -> np.ndarray:
+    """x: float [t, Hkv, D] calibration values -> uint8 [Hkv, n_s] static channels."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    t, Hkv, D = x.shape
+    out = np.zeros((Hkv, n_s), np.uint8)
+    lib().or_select_static(_p(x), t, Hkv, D, n_s, _p(out))
+    return out
+
+
 def dequantize_block(blk_fmt: int, D: int, blk: np.ndarray, role: int = 0, ntok: int = 16) -> np.ndarray:
     out = np.zeros((16, D), np.float32)
     lib().or_dequantize_block(blk_fmt, D, _p(np.ascontiguousarray(blk)), role, ntok, _p(out))
@@ -157,11 +178,14 @@ class OracleCache:
 
     def __init__(self, fmt: int, num_seqs: int, num_kv_heads: int, head_dim: int, pages_per_seq_max: int,
                  num_pages: int, num_tier_pages: int = 0, sigma: float = 3.0, lloyd_iters: int = 16,
-                 page_table: np.ndarray | None = None):
+                 page_table: np.ndarray | None = None, static_channels: np.ndarray | None = None):
+        # static_channels (format 4): uint8 [Hkv, 2, n_s], ascending per (head, role)
+        self.static_ch = (np.zeros((num_kv_heads, 2, 1), np.uint8) if static_channels is None
+                          else np.ascontiguousarray(static_channels, dtype=np.uint8))
         self.cfg = _Cfg(fmt, num_seqs, num_kv_heads, head_dim, pages_per_seq_max, num_pages,
-                        num_tier_pages, lloyd_iters, sigma)
+                        num_tier_pages, lloyd_iters, sigma, self.static_ch.shape[-1], _p(self.static_ch))
         self.fmt, self.B, self.Hkv, self.D = fmt, num_seqs, num_kv_heads, head_dim
-        main = BLK_CB2 if fmt == FMT_TIERED else fmt
+        main = BLK_CB2 if fmt == FMT_TIERED else fmt   # FMT_CB2S blocks are BLK_CB2S
         self.stride = block_stride(main, head_dim)
         self.tier_stride = block_stride(BLK_FP8, head_dim)
         self.pool = np.zeros(num_pages * num_kv_heads * 2 * self.stride, np.uint8)

@@ -299,6 +299,12 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /*                               value[t] = e4m3 of the outlier at token t,   */
 /*                               0 where t is not an outlier of the channel   */
 /*                               (record i at 4 + 20*i; K and V alike)        */
+/*  CB2 static codes, codebook   as CB2; the static channels have code 0 and  */
+/*  (f4)                         an all-zero codebook                         */
+/*            at 12D             u8 n_s, u8 channel[n_s] (ascending), zeros  */
+/*                               to 12D + 16                                  */
+/*            at 12D + 16        fp16 value(i, t) at 12D + 16 + 32*i + 2*t of */
+/*                               static channel i (K and V alike)             */
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
 /*            scale at 16D       fp32                                         */
@@ -306,7 +312,8 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /* Page Sizes with Memory Bus Lines").                                        */
 /* ------------------------------------------------------------------------- */
 
-enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3 };
+enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3, OR_CB2S = 4 };
+enum { OR_MAX_STATIC = 8 };
 
 static int round128(int x) { return (x + 127) / 128 * 128; }
 
@@ -318,6 +325,7 @@ EXPORT int or_block_stride(int fmt, int D)
     case OR_E2M1: return round128(9 * D);
     case OR_CB2:  return round128(12 * D + 4 + 20 * D);
     case OR_FP8:  return round128(16 * D + 16);
+    case OR_CB2S: return round128(12 * D + 16 + 32 * OR_MAX_STATIC);
     }
     return -1;
 }
@@ -553,6 +561,63 @@ static void quantize_page_fp8(const float* x, int D, int role, uint8_t* blk)
     put_f32(blk + 16 * D, s);
 }
 
+/* CB2 with a static FP16 channel mask ([P4] "Key Production Engineering     */
+/* Takeaways", item 2: the top 1% channels by absolute magnitude stay in      */
+/* FP16).  No per-token outlier detection: every other channel gets the CB2   */
+/* codebook fitted over all 16 of its values; the n_s static channels keep    */
+/* fp16(x) for every token (code 0, all-zero centroids).                      */
+static void quantize_page_cb2s(const float* x, int D, int iters, int role, const uint8_t* ch, int n_s, uint8_t* blk)
+{
+    memset(blk, 0, (size_t)or_block_stride(OR_CB2S, D));
+    uint8_t is_static[128] = {0};
+    for (int i = 0; i < n_s; ++i) is_static[ch[i] & (D - 1)] = 1;
+    for (int c = 0; c < D; ++c) {
+        if (is_static[c]) continue;   /* codes 0 and zero centroids from the clear */
+        float v[16];
+        uint8_t codes[16];
+        uint16_t c16[4];
+        for (int t = 0; t < 16; ++t) v[t] = x[t * D + c];
+        or_lloyd4(v, 16, iters, NULL, c16, codes);
+        for (int j = 0; j < 4; ++j) cb2_cent_set(blk, D, role, c, j, c16[j]);
+        for (int t = 0; t < 16; ++t) cb2_code_set(blk, D, role, t, c, codes[t]);
+    }
+    uint8_t* hdr = blk + 12 * D;
+    hdr[0] = (uint8_t)n_s;
+    for (int i = 0; i < n_s; ++i) {
+        int c = ch[i] & (D - 1);
+        hdr[1 + i] = (uint8_t)c;
+        for (int t = 0; t < 16; ++t) put_u16(hdr + 16 + 32 * i + 2 * t, or_fp16_encode((double)x[t * D + c]));
+    }
+}
+
+/* The n_s static channels of one (head, role): the channels with the largest */
+/* max_t |x[t][c]| over the calibration tokens, ties to the lower channel,    */
+/* written in ascending channel order.  x is float [t][Hkv][D].               */
+EXPORT void or_select_static(const float* x, int t, int Hkv, int D, int n_s, uint8_t* out /* [Hkv][n_s] */)
+{
+    for (int h = 0; h < Hkv; ++h) {
+        float score[128];
+        uint8_t taken[128] = {0};
+        for (int c = 0; c < D; ++c) {
+            float m = 0.0f;
+            for (int i = 0; i < t; ++i) {
+                float a = fabsf(x[((size_t)i * Hkv + h) * D + c]);
+                if (a > m) m = a;
+            }
+            score[c] = m;
+        }
+        for (int k = 0; k < n_s; ++k) {
+            int best = -1;
+            for (int c = 0; c < D; ++c)
+                if (!taken[c] && (best < 0 || score[c] > score[best])) best = c;
+            taken[best] = 1;
+        }
+        int k = 0;
+        for (int c = 0; c < D; ++c)
+            if (taken[c]) out[(size_t)h * n_s + k++] = (uint8_t)c;
+    }
+}
+
 /* Dequantize tokens [0, ntok) of a block to fp32 (values the codes stand for;
  * every one is exactly representable in fp32 as computed here). */
 EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, int ntok, float* out)
@@ -567,7 +632,7 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
             } else if (fmt == OR_E2M1) {
                 double sc = or_e4m3_decode(blk[8 * D + 16 * (c / 16) + t]);
                 xv = or_e2m1_decode(nib_get(blk, D, role, t, c)) * sc;
-            } else if (fmt == OR_CB2) {
+            } else if (fmt == OR_CB2 || fmt == OR_CB2S) {
                 xv = or_fp16_decode(cb2_cent_get(blk, D, role, c, cb2_code_get(blk, D, role, t, c)));
             } else {
                 xv = or_e4m3_decode(blk[fp8_byte(D, role, t, c)]) * (double)get_f32(blk + 16 * D);
@@ -582,6 +647,13 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
                 out[t * D + c] = (float)or_fp16_decode(get_u16(blk + 10 * D + 16 + 16 * cap + 2 * (t * cap + i)));
             }
         }
+    }
+    if (fmt == OR_CB2S) {   /* the static channels hold their fp16 values */
+        const uint8_t* hdr = blk + 12 * D;
+        int n_s = hdr[0] < OR_MAX_STATIC ? hdr[0] : OR_MAX_STATIC;
+        for (int i = 0; i < n_s; ++i)
+            for (int t = 0; t < ntok; ++t)
+                out[t * D + (hdr[1 + i] & (D - 1))] = (float)or_fp16_decode(get_u16(hdr + 16 + 32 * i + 2 * t));
     }
     if (fmt == OR_CB2) {
         const uint8_t* hdr = blk + 12 * D;
@@ -601,6 +673,11 @@ EXPORT void or_quantize_token(int fmt, int D, double sigma, int role, int t, con
 {
     if (fmt == OR_INT4) quantize_token_int4(x, D, sigma, role, t, blk);
     else quantize_token_e2m1(x, D, role, t, blk);
+}
+EXPORT void or_quantize_page_static(int D, int iters, int role, const float* x, const uint8_t* ch, int n_s,
+                                    uint8_t* blk)
+{
+    quantize_page_cb2s(x, D, iters, role, ch, n_s, blk);
 }
 EXPORT void or_quantize_page(int fmt, int D, double sigma, int iters, int role, const float* x, uint8_t* blk)
 {
@@ -622,13 +699,16 @@ EXPORT void or_quantize_page(int fmt, int D, double sigma, int iters, int role, 
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier) */
+    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier), 4 CB2 static */
     int32_t B, Hkv, D, pages_per_seq_max, num_pages, num_tier_pages;
     int32_t iters;
     double sigma;
+    int32_t n_static;              /* format 4: static channels per (head, role) */
+    const uint8_t* static_ch;      /* format 4: [Hkv][2][n_static] */
 } or_cfg;
 
 static int page_fmt(const or_cfg* c) { return c->fmt == 3 ? OR_CB2 : c->fmt; }
+static int is_paged(const or_cfg* c) { return c->fmt == OR_CB2 || c->fmt == 3 || c->fmt == OR_CB2S; }
 
 static int entry_ok(const or_cfg* c, int32_t e)
 {
@@ -692,7 +772,11 @@ EXPORT int or_append(const or_cfg* c, uint8_t* pool, uint8_t* tier_pool, const i
                             memcpy(x + t * D, r, sizeof(float) * D);
                         }
                         int tier = ((uint32_t)e >> 31) & 1;
-                        or_quantize_page(tier ? OR_FP8 : OR_CB2, D, c->sigma, c->iters, role, x, blk);
+                        if (c->fmt == OR_CB2S)
+                            quantize_page_cb2s(x, D, c->iters, role, c->static_ch + ((size_t)h * 2 + role) * c->n_static,
+                                               c->n_static, blk);
+                        else
+                            or_quantize_page(tier ? OR_FP8 : OR_CB2, D, c->sigma, c->iters, role, x, blk);
                         free(x);
                     } else {
                         for (int pos = lo; pos < hi; ++pos)
@@ -712,7 +796,7 @@ EXPORT void or_dequantize_range(const or_cfg* c, uint8_t* pool, uint8_t* tier_po
                                 float* out)
 {
     int D = c->D, len = seq_lens[b];
-    int paged = (c->fmt == OR_CB2 || c->fmt == 3);
+    int paged = is_paged(c);
     float* tmp = (float*)malloc(sizeof(float) * 16 * D);
     for (int pg = t0 / 16; t1 > t0 && pg <= (t1 - 1) / 16; ++pg) {
         int full = (pg + 1) * 16 <= len;

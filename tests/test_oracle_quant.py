@@ -274,3 +274,81 @@ def test_block_strides_aligned(fmt):
         assert oracle.block_stride(fmt, D) % 128 == 0
     assert oracle.block_stride(oracle.BLK_CB2, 128) == 4224
     assert oracle.block_stride(oracle.BLK_E2M1, 128) == 1152
+
+
+# ----------------------------------------------------------------------------- CB2 with a static fp16 channel mask
+def test_select_static_matches_brute_force():
+    """Top-n_s channels by max |x| over the calibration tokens, ties to the lower
+    channel, ascending ("The Sub-10ms Barrier", Key Production Engineering
+    Takeaways, item 2: top 1% channels by absolute magnitude stay in FP16)."""
+    rng = np.random.default_rng(11)
+    for trial in range(6):
+        t, Hkv, D, n_s = int(rng.integers(1, 40)), 3, (64, 128)[trial % 2], int(rng.integers(1, 9))
+        x = rng.standard_normal((t, Hkv, D)).astype(np.float32)
+        if trial >= 3:   # ties: quantize magnitudes coarsely
+            x = np.round(x * 2) / 2
+        got = oracle.select_static(x, n_s)
+        score = np.abs(x).max(0)                     # [Hkv, D]
+        for h in range(Hkv):
+            order = sorted(range(D), key=lambda c: (-score[h, c], c))
+            assert list(got[h]) == sorted(order[:n_s])
+
+
+def test_cb2_static_page_properties():
+    rng = np.random.default_rng(12)
+    for trial in range(6):
+        D = (64, 128)[trial % 2]
+        role = (trial // 2) % 2
+        x = rng.standard_normal((16, D)).astype(np.float32)
+        n_s = 1 + trial % 3
+        ch = np.sort(rng.choice(D, n_s, replace=False))
+        x[:, ch] *= 20
+        x[3, (ch[0] + 1) % D] = 40.0      # a large value outside the mask gets no special treatment
+        blk = oracle.quantize_page_static(D, x, ch, role=role)
+        xh = oracle.dequantize_block(oracle.BLK_CB2S, D, blk, role=role)
+        hdr = blk[12 * D:]
+        assert hdr[0] == n_s and list(hdr[1:1 + n_s]) == list(ch) and not hdr[1 + n_s:16].any()
+        for i, c in enumerate(ch):
+            for t in range(16):
+                h16 = int(hdr[16 + 32 * i + 2 * t]) | (int(hdr[17 + 32 * i + 2 * t]) << 8)
+                assert h16 == oracle.fp16_encode(float(x[t, c]))
+                assert xh[t, c] == oracle.fp16_decode(h16)
+        assert not hdr[16 + 32 * n_s:].any()
+        # the same codes and codebook as a CB2 page of the other channels, fitted over all 16 values
+        for c in range(D):
+            if c in ch:
+                continue
+            _, c16, codes, _ = oracle.lloyd4(x[:, c].astype(np.float64))
+            cf = np.array([oracle.fp16_decode(h) for h in c16])
+            for t in range(16):
+                assert abs(float(xh[t, c]) - float(x[t, c])) <= np.abs(cf - float(x[t, c])).min()
+                assert xh[t, c] in cf
+        # static channels carry code 0 and an all-zero codebook in the 2-bit planes
+        plain = blk.copy()
+        plain[12 * D:] = 0
+        plain[12 * D] = 0
+        xz = oracle.dequantize_block(oracle.BLK_CB2, D, plain, role=role)
+        assert (xz[:, ch] == 0).all()
+
+
+def test_cb2_static_cache_round_trip():
+    """Appends in ragged chunks give the same cache as one prefill (pages are
+    quantized once complete, from fp32 staging); dequantize returns fp16 values
+    on the static channels."""
+    rng = np.random.default_rng(13)
+    B, Hkv, D, P = 2, 2, 64, 4
+    x = rng.standard_normal((2, B, 50, Hkv, D)).astype(np.float32)
+    st = np.zeros((Hkv, 2, 2), np.uint8)
+    st[:, :, 0], st[:, :, 1] = 3, 40
+    x[..., 3] *= 15
+    a = oracle.OracleCache(oracle.FMT_CB2S, B, Hkv, D, P, B * P, static_channels=st)
+    b = oracle.OracleCache(oracle.FMT_CB2S, B, Hkv, D, P, B * P, static_channels=st)
+    a.append(x[0], x[1])
+    for t0, t1 in ((0, 7), (7, 16), (16, 33), (33, 50)):
+        b.append(x[0][:, t0:t1], x[1][:, t0:t1])
+    # staging rows past the partial page's 2 tokens are stale in the chunked cache and never read
+    assert (a.pool == b.pool).all() and (a.staging[:, :, :, :2] == b.staging[:, :, :, :2]).all()
+    for role in (0, 1):
+        got = a.dequantize(1, 1, role, 0, 48)
+        want = np.array([[oracle.fp16_decode(oracle.fp16_encode(float(v))) for v in row] for row in x[role][1, :48, 1][:, [3, 40]]])
+        assert (got[:, [3, 40]] == want).all()
