@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 from sub_byte_quantized_kvq_gb300 import kvq, synth, workloads  # noqa: E402
 
 METRIC = "quantized-KV decode attention: achieved HBM GB/s vs peak; us per decode step"
-FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED"}
+FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 KERNEL_SOURCES = ["kvq_common.cuh", "kvq_decode.cuh", "kvq_internal.cuh"]
 
@@ -106,6 +106,10 @@ def algorithmic_bytes(built: workloads.Built) -> dict:
         n_tier = int(built.tiers[:, :full].sum()) * w.Hkv * 2
         n_main = full * blocks - n_tier
         cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
+        tail = (L % 16) * D * 4 * blocks
+    elif w.fmt == synth.FMT_CB2S:
+        # codes + codebook (12D) + {n_s, channels} (16) + the static channels' fp16 values
+        cache_bytes = full * blocks * (12 * D + 16 + 32 * w.static_channels)
         tail = (L % 16) * D * 4 * blocks
     elif w.fmt == synth.FMT_INT4:
         pool = cache.pool.view(-1, cache.block_bytes(0))
@@ -276,7 +280,12 @@ def oracle_sample(w: synth.Workload, seed: int):
     pages = (N + 15) // 16
     tiers = synth.tier_pages(seed, 1, N, w.tier_frac, w.zipf_s) if w.tier_frac > 0 else None
     pt, nm, nt = synth.page_table(seed, 1, pages, False, tiers)
-    ref = oracle.OracleCache(w.fmt, 1, w.Hkv, w.D, pages, max(nm, 1), nt, page_table=pt)
+    st = None
+    if w.fmt == synth.FMT_CB2S:   # the oracle's own static channels, from the same calibration values
+        kc, vc = workloads.calibration_kv(w, seed, "cpu")
+        st = np.stack([oracle.select_static(kc.numpy(), w.static_channels),
+                       oracle.select_static(vc.numpy(), w.static_channels)], 1)
+    ref = oracle.OracleCache(w.fmt, 1, w.Hkv, w.D, pages, max(nm, 1), nt, page_table=pt, static_channels=st)
     for t0, T in workloads.chunks(N):
         k, v = workloads.seq_kv(w, seed, 0, t0, T, "cpu")
         ref.append(k[None].numpy(), v[None].numpy())
@@ -290,6 +299,8 @@ def oracle_sample(w: synth.Workload, seed: int):
         n_tier = (int(tiers[:, :full].sum()) if tiers is not None else 0) * w.Hkv * 2
         cache = (full * w.Hkv * 2 - n_tier) * 12 * D + side + n_tier * (16 * D + 4)
         cache += (N % 16) * D * 4 * w.Hkv * 2
+    elif w.fmt == synth.FMT_CB2S:
+        cache = full * w.Hkv * 2 * (12 * D + 16 + 32 * w.static_channels) + (N % 16) * D * 4 * w.Hkv * 2
     elif w.fmt == synth.FMT_INT4:
         counts = int(ref.pool.reshape(-1, ref.stride)[:, 10 * D:10 * D + 16].astype(np.int64).sum())
         cache = pages * w.Hkv * 2 * (10 * D + 16) + 3 * counts

@@ -78,7 +78,16 @@ typedef enum {
     /* [P2] KVQ_FMT_CB2_OUTLIER pages plus FP8 E4M3 pages with one fp32 scale per
      * (page, head, K|V) (s = amax/448).  A page-table entry with bit 31 set
      * lives in the FP8 tier pool. */
-    KVQ_FMT_TIERED = 3
+    KVQ_FMT_TIERED = 3,
+    /* [P4] "Key Production Engineering Takeaways" item 2: a static
+     * high-precision channel mask -- the cfg->static_channels channels of each
+     * (kv head, K|V) named by cache->static_mask keep fp16 values for every
+     * token; every other channel gets the KVQ_FMT_CB2_OUTLIER codebook fitted
+     * over all 16 of its page values (no per-token outlier detection, no
+     * side-list).  kvq_select_static_channels picks the mask (top channels by
+     * absolute magnitude) from calibration values.  Quantized when a page
+     * fills; the partial last page waits in fp32 staging. */
+    KVQ_FMT_CB2_STATIC = 4
 } kvq_format;
 
 typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
@@ -102,6 +111,8 @@ typedef struct {
     int32_t format;             /* kvq_format */
     int32_t lloyd_iters;        /* CB2: maximum Lloyd-Max assignment passes (16) */
     double sigma;               /* outlier threshold in standard deviations, >= 3 (3.0) */
+    int32_t static_channels;    /* CB2_STATIC: fp16 channels per (kv head, K|V), 1..8
+                                   (ceil(D / 100) for the pages' 1%); ignored otherwise */
 } kvq_config;
 
 /* The cache.  All pointers are device memory owned by the caller.
@@ -116,6 +127,10 @@ typedef struct {
  *   staging     fp32 [num_seqs][Hkv][2][16][D]: partial last page of the CB2 and
  *               TIERED formats (NULL for INT4 / E2M1).
  *   status      one uint32 word, OR-ed with KVQ_STATUS_* bits; the caller clears it.
+ *   static_mask uint8 [Hkv][2][static_channels] (CB2_STATIC only, else NULL):
+ *               the static channels of each (kv head, K|V), ascending, distinct,
+ *               below D.  Fixed for the cache's lifetime (set before the first
+ *               append, e.g. by kvq_select_static_channels).
  * The byte layout of a block (a definition of this library, chosen so the decode
  * kernel loads tensor-core fragments directly) is given at the end of this
  * header. */
@@ -126,6 +141,7 @@ typedef struct {
     int32_t* seq_lens;
     float* staging;
     uint32_t* status;
+    const uint8_t* static_mask;
 } kvq_cache;
 
 /* Bytes of one block: tier = 0 for the pool's own format, 1 for an FP8 tier
@@ -231,6 +247,15 @@ kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* 
                                         int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,
                                         int32_t num_splits, void* out, kvq_dtype out_dtype, void* stream);
 
+/* The static channel mask of KVQ_FMT_CB2_STATIC ([P4] "Key Production
+ * Engineering Takeaways" item 2: the top 1% channels by absolute magnitude stay
+ * in FP16): for each (kv head, K|V), the cfg->static_channels channels with the
+ * largest max |x| over `t` calibration tokens, ties to the lower channel,
+ * written ascending to mask (device uint8 [Hkv][2][static_channels]).
+ * k, v: device [t][Hkv][D] in in_dtype (bf16, f16 or f32), t >= 1. */
+kvq_status kvq_select_static_channels(const kvq_config* cfg, const void* k, const void* v, kvq_dtype in_dtype,
+                                      int32_t t, uint8_t* mask, void* stream);
+
 /* Debug: the values tokens [tok_begin, tok_end) of (seq, kv_head, which = 0 K /
  * 1 V) stand for, as fp32 [tok_end - tok_begin][D] in device memory `out`.
  * Bit-identical to the CPU reference's dequantization. */
@@ -281,6 +306,11 @@ const char* kvq_version(void);
  *                       six records travel with the block's codes; decode reads
  *                       further ones six at a time.
  *             stride 2176 (D=64), 4224 (D=128)
+ *   CB2_STATIC [0, 12D) codes and codebook as CB2; the static channels have code 0
+ *                       and an all-zero codebook
+ *             12D       u8 n_s, u8 channel[n_s] (ascending), zeros to 12D + 16
+ *             12D + 16  fp16 value of static channel i, token t at 12D + 16 + 32*i + 2*t
+ *             stride 1152 (D=64), 1920 (D=128)
  *   FP8 tier  [0, 16D)  codes: lane l at 8*NS*l, step s at +8s, slot k = byte k (e4m3)
  *             16D       fp32 scale
  *             stride 1152 (D=64), 2176 (D=128)

@@ -41,7 +41,7 @@ __global__ void dequantize_kernel(const DequantArgs a) {
   const int pos = a.t0 + (int)(idx / D), c = (int)(idx % D);
   const int t = pos % kPage, pg = pos / kPage;
   const int L = a.seq_lens[a.seq];
-  const bool paged = a.fmt == KVQ_FMT_CB2_OUTLIER || a.fmt == KVQ_FMT_TIERED;
+  const bool paged = a.fmt == KVQ_FMT_CB2_OUTLIER || a.fmt == KVQ_FMT_TIERED || a.fmt == KVQ_FMT_CB2_STATIC;
   float v = 0.f;
   if (pos >= L || pg >= a.ppsm) {
     v = 0.f;
@@ -73,17 +73,27 @@ __global__ void dequantize_kernel(const DequantArgs a) {
     } else if (bf == kBlkE2m1) {
       const uint32_t q = (blk[4 * NS * p.lane + 4 * p.step + p.slot / 2] >> (4 * (p.slot & 1))) & 0xFu;
       v = dq_e2m1(q) * dq_e4m3(blk[e2m1_sc_off(D) + 16 * (c / 16) + t]);
-    } else if (bf == kBlkCb2) {
+    } else if (bf == kBlkCb2 || bf == kBlkCb2s) {
       const uint32_t w = blk[2 * NS * p.lane + 2 * p.step] | (blk[2 * NS * p.lane + 2 * p.step + 1] << 8);
       const uint32_t q = (w >> (4 * (p.slot & 3) + 2 * (p.slot >> 2))) & 3u;
       const uint8_t* cb = blk + cb2_cb_off(D) + 8 * cb2_slot(a.role, c);
       v = dq_f16(cb[q] | (cb[4 + q] << 8));
-      const uint8_t* hdr = blk + cb2_out_off(D);
-      const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
-      for (int i = 0; i < n_ch; ++i) {
-        const uint8_t* rec = hdr + 4 + 20 * i;
-        const uint32_t tm = rec[2] | (rec[3] << 8);
-        if (rec[0] == c && (tm >> t & 1u)) v = dq_e4m3(rec[4 + t]);
+      if (bf == kBlkCb2s) {   // static fp16 channels
+        const uint8_t* hdr = blk + cb2s_hdr_off(D);
+        const int n_s = min((int)hdr[0], kMaxStatic);
+        for (int i = 0; i < n_s; ++i)
+          if (hdr[1 + i] == c) {
+            const uint8_t* vp = blk + cb2s_val_off(D) + 32 * i + 2 * t;
+            v = dq_f16(vp[0] | (vp[1] << 8));
+          }
+      } else {                // outlier side-list
+        const uint8_t* hdr = blk + cb2_out_off(D);
+        const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
+        for (int i = 0; i < n_ch; ++i) {
+          const uint8_t* rec = hdr + 4 + 20 * i;
+          const uint32_t tm = rec[2] | (rec[3] << 8);
+          if (rec[0] == c && (tm >> t & 1u)) v = dq_e4m3(rec[4 + t]);
+        }
       }
     } else {
       float s;
@@ -125,7 +135,8 @@ cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int
 static bool cfg_ok(const kvq_config* c) {
   if (!c) return false;
   if (c->num_seqs <= 0 || c->num_kv_heads <= 0 || c->pages_per_seq_max <= 0 || c->num_pages <= 0) return false;
-  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_TIERED) return false;
+  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_CB2_STATIC) return false;
+  if (c->format == KVQ_FMT_CB2_STATIC && (c->static_channels < 1 || c->static_channels > kMaxStatic)) return false;
   if (c->num_tier_pages < 0 || (c->format != KVQ_FMT_TIERED && c->num_tier_pages != 0)) return false;
   if (!(c->sigma >= 3.0) || !std::isfinite(c->sigma)) return false;
   if (c->lloyd_iters < 1 || c->lloyd_iters > 64) return false;
@@ -133,10 +144,13 @@ static bool cfg_ok(const kvq_config* c) {
   return true;
 }
 static bool dim_supported(const kvq_config* c) { return c->head_dim == 64 || c->head_dim == 128; }
+static bool paged_format(int f) {
+  return f == KVQ_FMT_CB2_OUTLIER || f == KVQ_FMT_TIERED || f == KVQ_FMT_CB2_STATIC;
+}
 static bool cache_ok(const kvq_config* c, const kvq_cache* k) {
   if (!k || !k->pool || !k->page_table || !k->seq_lens || !k->status) return false;
-  const bool paged = c->format == KVQ_FMT_CB2_OUTLIER || c->format == KVQ_FMT_TIERED;
-  if (paged && !k->staging) return false;
+  if (paged_format(c->format) && !k->staging) return false;
+  if (c->format == KVQ_FMT_CB2_STATIC && !k->static_mask) return false;
   if (c->format == KVQ_FMT_TIERED && c->num_tier_pages > 0 && !k->tier_pool) return false;
   return true;
 }
@@ -202,8 +216,7 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* ti
   const size_t per_page = (size_t)cfg->num_kv_heads * 2;
   *pool_bytes = (size_t)cfg->num_pages * per_page * block_stride(main_blk(cfg), cfg->head_dim);
   *tier_pool_bytes = (size_t)cfg->num_tier_pages * per_page * block_stride(kBlkFp8, cfg->head_dim);
-  const bool paged = cfg->format == KVQ_FMT_CB2_OUTLIER || cfg->format == KVQ_FMT_TIERED;
-  *staging_bytes = paged ? (size_t)cfg->num_seqs * cfg->num_kv_heads * 2 * kPage * cfg->head_dim * sizeof(float) : 0;
+  *staging_bytes = paged_format(cfg->format) ? (size_t)cfg->num_seqs * cfg->num_kv_heads * 2 * kPage * cfg->head_dim * sizeof(float) : 0;
   return KVQ_OK;
 }
 
@@ -234,6 +247,8 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
   a.fmt = cfg->format;
   a.iters = cfg->lloyd_iters;
   a.sigma = cfg->sigma;
+  a.static_mask = cache->static_mask;
+  a.n_static = cfg->format == KVQ_FMT_CB2_STATIC ? cfg->static_channels : 0;
   if (append_launch(a, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -306,6 +321,8 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.out = nullptr;
   a.out_dtype = KVQ_F32;
   a.arrivals = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + arrivals_offset(cfg, num_q_heads, S));
+  a.static_mask = cache->static_mask;
+  a.n_static = cfg->format == KVQ_FMT_CB2_STATIC ? cfg->static_channels : 0;
   return KVQ_OK;
 }
 }  // namespace kvq
@@ -358,6 +375,17 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
   a.out = out;   // one launch: the split kernel's last CTA per (sequence, kv head) merges the splits
   a.out_dtype = out_dtype;
   if (decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_select_static_channels(const kvq_config* cfg, const void* k, const void* v, kvq_dtype in_dtype,
+                                      int32_t t, uint8_t* mask, void* stream) {
+  if (!cfg_ok(cfg) || cfg->format != KVQ_FMT_CB2_STATIC || !k || !v || !mask || t < 1) return KVQ_ERR_INVALID_ARG;
+  if (in_dtype != KVQ_BF16 && in_dtype != KVQ_F16 && in_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
+  if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
+  if (select_static_launch(k, v, in_dtype, t, cfg->num_kv_heads, cfg->head_dim, cfg->static_channels, mask,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

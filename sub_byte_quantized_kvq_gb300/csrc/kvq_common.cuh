@@ -14,7 +14,8 @@ namespace kvq {
 constexpr int kPage = KVQ_PAGE_TOKENS;
 
 // Block formats (the pool format of a cache; FP8 is the tier-1 page format).
-enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3 };
+enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3, kBlkCb2s = 4 };
+constexpr int kMaxStatic = 8;   // CB2_STATIC: static fp16 channels per (kv head, K|V)
 
 // Largest number of values of an n-vector that can lie more than 3 standard
 // deviations (unbiased) from its mean: k * 9 * s^2 < (n - 1) * s^2.
@@ -31,11 +32,14 @@ __host__ __device__ constexpr int e2m1_sc_off(int D) { return 8 * D; }
 __host__ __device__ constexpr int cb2_cb_off(int D) { return 4 * D; }
 __host__ __device__ constexpr int cb2_out_off(int D) { return 12 * D; }   // outlier side-list
 __host__ __device__ constexpr int fp8_sc_off(int D) { return 16 * D; }
+__host__ __device__ constexpr int cb2s_hdr_off(int D) { return 12 * D; }      // u8 n_s, u8 channel[n_s]
+__host__ __device__ constexpr int cb2s_val_off(int D) { return 12 * D + 16; } // fp16 [n_s][16]
 
 __host__ __device__ constexpr int block_stride(int fmt, int D) {
   return fmt == kBlkInt4 ? round_up128(10 * D + 16 + 48 * int4_cap(D))
        : fmt == kBlkE2m1 ? round_up128(9 * D)
        : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 20 * D)
+       : fmt == kBlkCb2s ? round_up128(12 * D + 16 + 32 * kMaxStatic)
                          : round_up128(16 * D + 16);
 }
 

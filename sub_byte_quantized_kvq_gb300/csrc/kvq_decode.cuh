@@ -47,7 +47,7 @@ constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 
 template <int FMT>
 struct Fmt {
-  static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED);
+  static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED || FMT == KVQ_FMT_CB2_STATIC);
   static constexpr int kMain = FMT == KVQ_FMT_TIERED ? kBlkCb2 : FMT;
   static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2);
   static constexpr int kPPI = kMain == kBlkInt4 ? 1 : 2;   // pages per warp iteration
@@ -59,6 +59,7 @@ __host__ __device__ constexpr int fetch_bytes(int blk) {
   return blk == kBlkInt4 ? 10 * D + 16 + 48 * int4_cap(D)
        : blk == kBlkE2m1 ? 9 * D
        : blk == kBlkCb2  ? 12 * D + kOutPrefetch
+       : blk == kBlkCb2s ? 12 * D + 16 + 32 * kMaxStatic   // the copy itself takes 32 n_s
                          : 16 * D + 16;
 }
 template <int FMT, int D>
@@ -447,6 +448,10 @@ struct WarpState {
   float o[NT][D / 16][4];   // O^T accumulators: rows channel 16s+g (+8), cols head nt*8+2q (+1)
   float m[NT][2];           // running max (log2 units) of heads nt*8+2q, +1
   float l[NT][2];           // per-lane partial softmax sums
+  // CB2_STATIC: the CTA's query at the K static channels (B fragment of the
+  // m16n8k8 correction) and the output of the V static channels (rows = slots)
+  uint32_t qs[NT];
+  float sv[NT][4];
 };
 struct WarpSmem {
   const float* qsm;  // [D][GS] fp32 query of the CTA's G heads
@@ -498,9 +503,45 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
   if (rescale) {
     if (corr) rescale_state<D, NT, true>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
     else rescale_state<D, NT, false>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) st.sv[nt][r] *= alpha[nt][r & 1];
   }
 #pragma unroll
   for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
+}
+
+// CB2_STATIC, K side: scores[t][h] += sum_i q[h][ch_i] * x[t][ch_i] over the
+// static fp16 channels -- one m16n8k8 tile, A = tokens x slots from the block,
+// B = st.qs (the query at the static channels, gathered once per CTA).
+template <int D, int NT>
+__device__ __forceinline__ void cb2s_k_correct(uint32_t kb_s, int n_s, const uint32_t (&qs)[NT], int lane,
+                                               float (&acc)[NT][4]) {
+  const int g = lane >> 2, ia = 2 * (lane & 3);
+  const uint32_t base = kb_s + cb2s_val_off(D) + 32 * ia + 2 * g;
+  const bool va = ia < n_s, vb = ia + 1 < n_s;
+  const uint32_t a0 = (va ? lds16(base) : 0u) | ((vb ? lds16(base + 32) : 0u) << 16);        // token g
+  const uint32_t a1 = (va ? lds16(base + 16) : 0u) | ((vb ? lds16(base + 48) : 0u) << 16);   // token g + 8
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) mma1688(acc[nt], a0, a1, qs[nt]);
+}
+
+// CB2_STATIC, V side: sv[slot][h] += sum_t p[t][h] * x[t][ch_slot] (A = slots x
+// tokens, rows 8..15 empty), accumulated across pages in registers and
+// rescaled with the output.
+template <int D, int NT>
+__device__ __forceinline__ void cb2s_v_accum(uint32_t vb_s, int n_s, const uint32_t (&phi)[NT][2],
+                                             const uint32_t (&plo)[NT][2], int lane, float (&sv)[NT][4]) {
+  const int g = lane >> 2, t0 = 2 * (lane & 3);
+  const bool on = g < n_s;
+  const uint32_t base = vb_s + cb2s_val_off(D) + 32 * g + 2 * t0;
+  const uint32_t a0 = on ? lds32(base) : 0u, a2 = on ? lds32(base + 16) : 0u;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    mma16816(sv[nt], a0, 0u, a2, 0u, phi[nt][0], phi[nt][1]);
+    mma16816(sv[nt], a0, 0u, a2, 0u, plo[nt][0], plo[nt][1]);
+  }
 }
 
 // CB2 pages (and, for the tiered format, FP8 tier pages), PPI at a time.
@@ -548,9 +589,14 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
     }
   }
+  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) cb2s_k_correct<D, NT>(kb_s[p], a.n_static, st.qs, lane, acc[p]);
+  }
   // outlier corrections (the chunk loop is rolled; the pages are unrolled)
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
+    if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
     const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(kb_s[p] + cb2_out_off(D)), D);
 #pragma unroll 1
     for (int base = 0; base < n_ch; base += kChunk) {
@@ -567,7 +613,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 
   k_done();   // the K blocks are no longer read
   uint32_t phi[PPI][NT][2], plo[PPI][NT][2];
-  softmax_frags<D, NT, PPI>(st, acc, ntok, a.scale_log2, sm, lane, true, phi, plo);
+  softmax_frags<D, NT, PPI>(st, acc, ntok, a.scale_log2, sm, lane, Fmt<FMT>::kOutliers, phi, plo);
   v_wait();
 
   uint32_t vc[PPI][NS / 2];
@@ -601,8 +647,13 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         }
       }
     }
+  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) cb2s_v_accum<D, NT>(vb_s[p], a.n_static, phi[p], plo[p], lane, st.sv);
+  }
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
+    if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
     const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + cb2_out_off(D)), D);
 #pragma unroll 1
     for (int base = 0; base < n_ch; base += kChunk) {
@@ -991,7 +1042,27 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     for (int s = 0; s < NS; ++s) st.o[nt][s][0] = st.o[nt][s][1] = st.o[nt][s][2] = st.o[nt][s][3] = 0.f;
     st.m[nt][0] = st.m[nt][1] = -INFINITY;
     st.l[nt][0] = st.l[nt][1] = 0.f;
+    st.sv[nt][0] = st.sv[nt][1] = st.sv[nt][2] = st.sv[nt][3] = 0.f;
+    st.qs[nt] = 0u;
   }
+  int vch = 0;   // CB2_STATIC: the V static channel of slot g (lanes g < n_s)
+  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
+    const uint8_t* mk = a.static_mask + (size_t)kvh * 2 * a.n_static;   // K channels, then V channels
+    const int ia = 2 * q4;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + g;
+      const bool on = h < G;
+      const float qa = (on && ia < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia] & (D - 1))]) : 0.f;
+      const float qb =
+          (on && ia + 1 < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia + 1] & (D - 1))]) : 0.f;
+      st.qs[nt] = h2_as_u32(__floats2half2_rn(qa, qb));
+    }
+    vch = g < a.n_static ? (mk[a.n_static + g] & (D - 1)) : 0;
+  }
+
+  // bytes copied per main-pool block (CB2_STATIC: only its n_s static channels' values)
+  const int main_fetch = F::kMain == kBlkCb2s ? 12 * D + 16 + 32 * a.n_static : fetch_bytes<D>(F::kMain);
 
   // page-table window: lane j holds the entry of this warp's local page win_base + j
   const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
@@ -1032,7 +1103,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
               tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
           if (ok) {
             m = ent[j];
-            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : fetch_bytes<D>(F::kMain);
+            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : main_fetch;
           } else {
             m = kBadEntry;
             atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
@@ -1068,7 +1139,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         ent[j] = meta[kslot * PPI + j];
         bytes[j] = (ent[j] == kNoPage || ent[j] == kBadEntry) ? 0u
                    : (FMT == KVQ_FMT_TIERED && ent[j] < 0) ? (uint32_t)fetch_bytes<D>(kBlkFp8)
-                                                           : (uint32_t)fetch_bytes<D>(F::kMain);
+                                                           : (uint32_t)main_fetch;
         total += bytes[j];
       }
       fence_proxy_async();
@@ -1123,7 +1194,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
       v_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[vs], (it / NV) & 1, kWaitLimitNs));
       v_waited += v_ok;
     };
-    if constexpr (F::kMain == kBlkCb2) {
+    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s) {
       iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
     } else if constexpr (F::kMain == kBlkE2m1) {
       iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane, k_done, v_wait);
@@ -1207,6 +1278,19 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         }
       }
   }
+  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
+    // the static V channels: slot g's output goes to channel vch (distinct per slot)
+    __syncwarp();
+    if (g < a.n_static) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int h = nt * 8 + 2 * q4 + j;
+          if (h < G) mo[(w * GS + h) * D + vch] += st.sv[nt][j];
+        }
+    }
+  }
   __syncthreads();
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
@@ -1277,5 +1361,6 @@ KernelInfo decode_kernel_int4(int D, int G);
 KernelInfo decode_kernel_e2m1(int D, int G);
 KernelInfo decode_kernel_cb2(int D, int G);
 KernelInfo decode_kernel_tiered(int D, int G);
+KernelInfo decode_kernel_cb2s(int D, int G);
 
 }  // namespace kvq

@@ -29,6 +29,8 @@ struct DecodeArgs {
   void* out;        // [B][Hq][D] in out_dtype
   int out_dtype;    // KVQ_BF16 or KVQ_F32
   uint32_t* arrivals;  // [B][Hkv] arrival counters, zero between calls
+  const uint8_t* static_mask;  // CB2_STATIC: [Hkv][2][n_static] channels
+  int n_static;
 };
 
 struct AppendArgs {
@@ -44,6 +46,8 @@ struct AppendArgs {
   const int32_t* t_per_seq;
   int B, Hkv, ppsm, num_pages, num_tier_pages, fmt, iters;
   double sigma;
+  const uint8_t* static_mask;  // CB2_STATIC: [Hkv][2][n_static] channels
+  int n_static;
 };
 
 // The split decode kernel, and the combine kernel (out_dtype KVQ_BF16 or KVQ_F32), on `st`.
@@ -56,6 +60,8 @@ int decode_ctas_per_sm(int fmt, int D, int G);
 constexpr int kWarpsPerCta = 4;
 // Quantize-on-append launches (see kvq_quantize.cu).
 cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
+cudaError_t select_static_launch(const void* k, const void* v, int in_dtype, int t, int Hkv, int D, int n_s,
+                                 uint8_t* mask, cudaStream_t st);
 // Dequantize tokens [t0, t1) of (seq, head, role) to fp32.
 cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int seq, int head, int role, int t0,
                               int t1, float* out, cudaStream_t st);

@@ -274,6 +274,22 @@ __global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
 }
 
 // ----------------------------------------------------------------------------- page formats
+// 2-bit codes [16][D] -> the block's lane-major code words (CB2 layout).
+template <int D>
+__device__ __forceinline__ void pack_cb2_codes(const uint8_t (&codes)[16][D], uint8_t* blk, int role, int tid) {
+  constexpr int NS = D / 16;
+  for (int i = tid; i < 32 * NS; i += blockDim.x) {
+    const int ln = i / NS, s = i % NS;
+    uint32_t word = 0;
+    for (int k = 0; k < 8; ++k) {
+      int t, c;
+      frag_inverse(role, ln, s, k, t, c);
+      word |= (uint32_t)codes[t][c] << (4 * (k & 3) + 2 * (k >> 2));
+    }
+    *reinterpret_cast<uint16_t*>(blk + 2 * NS * ln + 2 * s) = (uint16_t)word;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
   constexpr int NS = D / 16;
@@ -293,7 +309,8 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
   if (pg * kPage + kPage > end) return;  // only pages this append completes
   const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
   const bool tier = (u >> 31) != 0;
-  const int stride = tier ? kFp8 : kCb2;
+  const bool stat = a.fmt == KVQ_FMT_CB2_STATIC;
+  const int stride = tier ? kFp8 : stat ? block_stride(kBlkCb2s, D) : kCb2;
   uint8_t* gblk = (tier ? a.tier_pool : a.pool) + (((size_t)phys * a.Hkv + h) * 2 + role) * stride;
   const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
 
@@ -318,6 +335,40 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
       blk[8 * NS * p.lane + 8 * p.step + p.slot] = s != 0.f ? f32_to_e4m3(__fdiv_rn(xs[t][c], s)) : 0;
     }
     if (tid == 0) *reinterpret_cast<float*>(blk + fp8_sc_off(D)) = s;
+  } else if (stat) {
+    // static fp16 channels (all tokens); every other channel: codebook over all 16 values
+    const uint8_t* chs = a.static_mask + ((size_t)h * 2 + role) * a.n_static;
+    if (tid < D) mask[0][tid] = 0;
+    __syncthreads();
+    if (tid < a.n_static) mask[0][chs[tid] & (D - 1)] = 1;
+    __syncthreads();
+    if (tid < D) {
+      const int c = tid;
+      if (mask[0][c]) {
+        for (int t = 0; t < 16; ++t) codes[t][c] = 0;   // all-zero centroids from the block clear
+      } else {
+        float v[16];
+        uint8_t cc[16];
+        uint16_t c16[4];
+        for (int t = 0; t < 16; ++t) v[t] = xs[t][c];
+        lloyd4(v, 16, a.iters, c16, cc);
+        for (int t = 0; t < 16; ++t) codes[t][c] = cc[t];
+        uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
+        for (int jj = 0; jj < 4; ++jj) {
+          cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
+          cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
+        }
+      }
+    }
+    if (tid < a.n_static) {
+      const int c = chs[tid] & (D - 1);
+      blk[cb2s_hdr_off(D) + 1 + tid] = (uint8_t)c;
+      for (int t = 0; t < 16; ++t)
+        *reinterpret_cast<uint16_t*>(blk + cb2s_val_off(D) + 32 * tid + 2 * t) = f32_to_f16_bits(xs[t][c]);
+    }
+    if (tid == 0) blk[cb2s_hdr_off(D)] = (uint8_t)a.n_static;
+    __syncthreads();
+    pack_cb2_codes<D>(codes, blk, role, tid);
   } else {
     if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
     __syncthreads();
@@ -379,16 +430,7 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
       }
     }
     __syncthreads();
-    for (int i = tid; i < 32 * NS; i += blockDim.x) {
-      const int ln = i / NS, s = i % NS;
-      uint32_t word = 0;
-      for (int k = 0; k < 8; ++k) {
-        int t, c;
-        frag_inverse(role, ln, s, k, t, c);
-        word |= (uint32_t)codes[t][c] << (4 * (k & 3) + 2 * (k >> 2));
-      }
-      *reinterpret_cast<uint16_t*>(blk + 2 * NS * ln + 2 * s) = (uint16_t)word;
-    }
+    pack_cb2_codes<D>(codes, blk, role, tid);
   }
   __syncthreads();
   for (int i = tid; i < stride / 16; i += blockDim.x)
@@ -419,6 +461,48 @@ __global__ void append_finish_kernel(const AppendArgs a) {
   if (st == kSeqOk) a.seq_lens[b] = start + n;
   else if (st == kSeqCapacity) atomicOr(a.status, KVQ_STATUS_CAPACITY);
   else if (st == kSeqBadPage) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+}
+
+// Static channel mask of CB2_STATIC: one CTA per (kv head, K|V); thread c
+// takes max_t |x[t][h][c]|, then n_s argmax passes (ties to the lower channel)
+// and an ascending write-out.
+__global__ void __launch_bounds__(128) select_static_kernel(const void* k, const void* v, int in_dtype, int t, int Hkv,
+                                                            int D, int n_s, uint8_t* mask) {
+  __shared__ float score[128];
+  __shared__ uint8_t taken[128];
+  const int h = blockIdx.x >> 1, role = blockIdx.x & 1, c = threadIdx.x;
+  const void* x = role ? v : k;
+  if (c < D) {
+    float m = 0.f;
+    for (int i = 0; i < t; ++i) {
+      const size_t idx = ((size_t)i * Hkv + h) * D + c;
+      const float val = in_dtype == KVQ_F32   ? static_cast<const float*>(x)[idx]
+                        : in_dtype == KVQ_F16 ? __half2float(static_cast<const __half*>(x)[idx])
+                                              : __bfloat162float(static_cast<const __nv_bfloat16*>(x)[idx]);
+      m = fmaxf(m, fabsf(val));
+    }
+    score[c] = m;
+    taken[c] = 0;
+  }
+  __syncthreads();
+  if (c == 0) {
+    for (int k2 = 0; k2 < n_s; ++k2) {
+      int best = -1;
+      for (int j = 0; j < D; ++j)
+        if (!taken[j] && (best < 0 || score[j] > score[best])) best = j;
+      taken[best] = 1;
+    }
+    uint8_t* out = mask + ((size_t)h * 2 + role) * n_s;
+    int n = 0;
+    for (int j = 0; j < D; ++j)
+      if (taken[j]) out[n++] = (uint8_t)j;
+  }
+}
+
+cudaError_t select_static_launch(const void* k, const void* v, int in_dtype, int t, int Hkv, int D, int n_s,
+                                 uint8_t* mask, cudaStream_t st) {
+  select_static_kernel<<<Hkv * 2, 128, 0, st>>>(k, v, in_dtype, t, Hkv, D, n_s, mask);
+  return cudaGetLastError();
 }
 
 template <int D>

@@ -15,7 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
-KVQ_FMT_INT4_G32, KVQ_FMT_FP4_E2M1_S16, KVQ_FMT_CB2_OUTLIER, KVQ_FMT_TIERED = 0, 1, 2, 3
+KVQ_FMT_INT4_G32, KVQ_FMT_FP4_E2M1_S16, KVQ_FMT_CB2_OUTLIER, KVQ_FMT_TIERED, KVQ_FMT_CB2_STATIC = 0, 1, 2, 3, 4
 KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 KVQ_TIER_BIT = 1 << 31
 KVQ_STATUS_BAD_PAGE, KVQ_STATUS_CAPACITY, KVQ_STATUS_SEQ_TOO_LONG, KVQ_STATUS_TIMEOUT = 1, 2, 4, 8
@@ -35,19 +35,21 @@ class kvq_config(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("pages_per_seq_max", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("num_tier_pages", ctypes.c_int32), ("format", ctypes.c_int32), ("lloyd_iters", ctypes.c_int32),
-                ("sigma", ctypes.c_double)]
+                ("sigma", ctypes.c_double), ("static_channels", ctypes.c_int32)]
 
 
 class kvq_cache(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("tier_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
-                ("seq_lens", ctypes.c_void_p), ("staging", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+                ("seq_lens", ctypes.c_void_p), ("staging", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("static_mask", ctypes.c_void_p)]
 
 
 _lib = None
 _lock = threading.Lock()
 EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
            "kvq_decode_num_splits", "kvq_decode_split", "kvq_decode_combine", "kvq_decode_attention",
-           "kvq_decode_attention_noalloc", "kvq_dequantize", "kvq_status_string", "kvq_version")
+           "kvq_decode_attention_noalloc", "kvq_select_static_channels", "kvq_dequantize", "kvq_status_string",
+           "kvq_version")
 
 
 def lib() -> ctypes.CDLL:
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
                 "kvq_decode_combine": (I, [pcfg, I, I, I, P, S, P, I, P]),
                 "kvq_decode_attention": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P, S, P]),
                 "kvq_decode_attention_noalloc": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, I, P]),
+                "kvq_select_static_channels": (I, [pcfg, P, P, I, I, P, P]),
                 "kvq_dequantize": (I, [pcfg, pcache, I, I, I, I, I, P, P]),
                 "kvq_status_string": (ctypes.c_char_p, [I]),
                 "kvq_version": (ctypes.c_char_p, []),
@@ -109,9 +112,12 @@ class QuantizedKVCache:
 
     def __init__(self, fmt: int, num_seqs: int, num_kv_heads: int, head_dim: int, pages_per_seq_max: int,
                  num_pages: int, num_tier_pages: int = 0, sigma: float = 3.0, lloyd_iters: int = 16,
-                 page_table: torch.Tensor | None = None, device="cuda"):
+                 page_table: torch.Tensor | None = None, device="cuda", static_channels: int = 0):
+        """static_channels (KVQ_FMT_CB2_STATIC): fp16 channels per (kv head, K|V);
+        fill `static_mask` ([Hkv, 2, n]) before the first append, e.g. with
+        kvq_select_static_channels."""
         self.cfg = kvq_config(num_seqs, num_kv_heads, head_dim, pages_per_seq_max, num_pages, num_tier_pages, fmt,
-                              lloyd_iters, sigma)
+                              lloyd_iters, sigma, static_channels)
         pb, tb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
         _check(lib().kvq_cache_bytes(ctypes.byref(self.cfg), ctypes.byref(pb), ctypes.byref(tb), ctypes.byref(sb)),
                "kvq_cache_bytes")
@@ -124,9 +130,12 @@ class QuantizedKVCache:
         self.page_table = torch.as_tensor(page_table).to(torch.int32).to(self.device).contiguous()
         self.seq_lens = torch.zeros(num_seqs, dtype=torch.int32, device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.static_mask = (torch.zeros((num_kv_heads, 2, static_channels), dtype=torch.uint8, device=self.device)
+                            if fmt == KVQ_FMT_CB2_STATIC else None)
         self.c = kvq_cache(self.pool.data_ptr(), self.tier_pool.data_ptr() if self.tier_pool is not None else None,
                            self.page_table.data_ptr(), self.seq_lens.data_ptr(),
-                           self.staging.data_ptr() if self.staging is not None else None, self.status.data_ptr())
+                           self.staging.data_ptr() if self.staging is not None else None, self.status.data_ptr(),
+                           self.static_mask.data_ptr() if self.static_mask is not None else None)
 
     @property
     def head_dim(self) -> int:
@@ -187,6 +196,14 @@ def kvq_decode_attention(cache: QuantizedKVCache, q: torch.Tensor, softmax_scale
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "kvq_decode_attention")
     return out
+
+
+def kvq_select_static_channels(cache: QuantizedKVCache, k: torch.Tensor, v: torch.Tensor, stream=None):
+    """Fill cache.static_mask from calibration values k, v [t, Hkv, D] (device)."""
+    assert k.shape == v.shape and k.dim() == 3 and k.dtype == v.dtype and k.is_contiguous() and v.is_contiguous()
+    _check(lib().kvq_select_static_channels(ctypes.byref(cache.cfg), _ptr(k), _ptr(v), _DTYPE[k.dtype], k.shape[0],
+                                            _ptr(cache.static_mask), _stream(stream)), "kvq_select_static_channels")
+    return cache.static_mask
 
 
 def alloc_workspace(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int, num_splits: int = 0) -> torch.Tensor:

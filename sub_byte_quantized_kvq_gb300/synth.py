@@ -17,6 +17,9 @@ on; no public dataset is involved, these stand in for real KV caches):
                  as cb2_4k
   longctx_128k   B4  Hkv8 Hq32 D128 N131072  2-bit codebook, 1% (=1) outlier
                  channel x10, 64 splits
+  static_4k      B8  Hkv8 Hq32 D128 N4096    2-bit codebook with a static fp16
+                 channel mask (2 = ceil(1% of 128) channels per K|V and head,
+                 chosen from sequence 0's first 256 tokens), 1 channel x10
 
 Every generator takes an explicit seed; per-sequence data is drawn from a
 generator seeded by (seed, sequence) so one sequence of a large workload can be
@@ -30,7 +33,8 @@ import math
 import numpy as np
 import torch
 
-FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED = 0, 1, 2, 3
+FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S = 0, 1, 2, 3, 4
+CALIBRATION_TOKENS = 256   # static channel mask: chosen from sequence 0's first tokens
 TIER_BIT = 1 << 31
 
 
@@ -51,6 +55,7 @@ class Workload:
     tier_frac: float = 0.0
     zipf_s: float = 1.1
     splits: int = 0              # 0 = library heuristic
+    static_channels: int = 0     # FMT_CB2S: fp16 channels per (K|V, head)
 
     @property
     def G(self) -> int:
@@ -68,6 +73,7 @@ WORKLOADS = {
     "tiered_32k": Workload("tiered_32k", FMT_TIERED, 64, 8, 64, 128, 32768, "normal", 4, 8.0, shuffled=True,
                            tier_frac=0.10),
     "longctx_128k": Workload("longctx_128k", FMT_CB2, 4, 8, 32, 128, 131072, "normal", 1, 10.0, splits=64),
+    "static_4k": Workload("static_4k", FMT_CB2S, 8, 8, 32, 128, 4096, "normal", 1, 10.0, static_channels=2),
 }
 
 

@@ -38,12 +38,20 @@ def seq_kv(w: synth.Workload, seed: int, b: int, t0: int, T: int, device) -> tup
     return synth.workload_kv(w, seed, b, t0, T, device=device)
 
 
+def calibration_kv(w: synth.Workload, seed: int, device) -> tuple[torch.Tensor, torch.Tensor]:
+    """K, V [t, Hkv, D] the static channel mask is chosen from: sequence 0's first tokens."""
+    return seq_kv(w, seed, 0, 0, min(w.N, synth.CALIBRATION_TOKENS), device)
+
+
 def build(w: synth.Workload, seed: int = 0, device="cuda", in_dtype=torch.float32) -> Built:
     pages = w.pages
     tiers = synth.tier_pages(seed, w.B, w.N, w.tier_frac, w.zipf_s) if w.tier_frac > 0 else np.zeros((w.B, pages), bool)
     pt, n_main, n_tier = synth.page_table(seed, w.B, pages, w.shuffled, tiers)
     cache = kvq.QuantizedKVCache(w.fmt, w.B, w.Hkv, w.D, pages, max(n_main, 1), n_tier,
-                                 page_table=torch.from_numpy(pt), device=device)
+                                 page_table=torch.from_numpy(pt), device=device, static_channels=w.static_channels)
+    if w.fmt == synth.FMT_CB2S:   # the static channel mask, from calibration tokens
+        kc, vc = calibration_kv(w, seed, device)
+        kvq.kvq_select_static_channels(cache, kc.to(in_dtype).contiguous(), vc.to(in_dtype).contiguous())
     for t0, T in chunks(w.N):
         k = torch.empty((w.B, T, w.Hkv, w.D), dtype=in_dtype, device=device)
         v = torch.empty_like(k)

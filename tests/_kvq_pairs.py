@@ -6,7 +6,8 @@ import torch
 import oracle
 from sub_byte_quantized_kvq_gb300 import kvq, synth
 
-ORACLE_FMT = {kvq.KVQ_FMT_INT4_G32: oracle.FMT_INT4, kvq.KVQ_FMT_FP4_E2M1_S16: oracle.FMT_E2M1,
+ORACLE_FMT = {kvq.KVQ_FMT_CB2_STATIC: oracle.FMT_CB2S,
+              kvq.KVQ_FMT_INT4_G32: oracle.FMT_INT4, kvq.KVQ_FMT_FP4_E2M1_S16: oracle.FMT_E2M1,
               kvq.KVQ_FMT_CB2_OUTLIER: oracle.FMT_CB2, kvq.KVQ_FMT_TIERED: oracle.FMT_TIERED}
 
 
@@ -19,20 +20,42 @@ def make_kv(seed, B, T, Hkv, D, dist="normal", n_out=4, factor=8.0, fixed=()):
 class Pair:
     """A GPU cache and an oracle cache built from identical inputs."""
 
-    def __init__(self, fmt, B, Hkv, D, P, seed=0, shuffled=True, tiers=None, extra_pages=0, sigma=3.0, iters=16):
+    def __init__(self, fmt, B, Hkv, D, P, seed=0, shuffled=True, tiers=None, extra_pages=0, sigma=3.0, iters=16,
+                 static_channels=0):
         self.fmt, self.B, self.Hkv, self.D, self.P = fmt, B, Hkv, D, P
+        if fmt == kvq.KVQ_FMT_CB2_STATIC and static_channels == 0:
+            static_channels = -(-D // 100)   # ceil(1% of D)
+        self.calibrated = fmt != kvq.KVQ_FMT_CB2_STATIC
         pt, nm, nt = synth.page_table(seed, B, P, shuffled, tiers)
         nm += extra_pages
         self.pt = pt
         self.gpu = kvq.QuantizedKVCache(fmt, B, Hkv, D, P, nm, nt, sigma=sigma, lloyd_iters=iters,
-                                        page_table=torch.from_numpy(pt), device="cuda")
+                                        page_table=torch.from_numpy(pt), device="cuda",
+                                        static_channels=static_channels)
+        st = np.zeros((Hkv, 2, max(static_channels, 1)), np.uint8)
         self.ref = oracle.OracleCache(ORACLE_FMT[fmt], B, Hkv, D, P, nm, nt, sigma=sigma, lloyd_iters=iters,
-                                      page_table=pt)
+                                      page_table=pt, static_channels=st)
+
+    def calibrate(self, k, v, dtype=torch.float32):
+        """Static channel mask from calibration values k, v (CPU float32 [t, Hkv, D]):
+        the GPU selects it, the oracle selects it independently; they must agree."""
+        kd, vd = k.to(dtype), v.to(dtype)
+        got = kvq.kvq_select_static_channels(self.gpu, kd.cuda().contiguous(), vd.cuda().contiguous())
+        torch.cuda.synchronize()
+        n = self.gpu.cfg.static_channels
+        exp = np.stack([oracle.select_static(kd.float().numpy(), n), oracle.select_static(vd.float().numpy(), n)], 1)
+        np.testing.assert_array_equal(got.cpu().numpy(), exp)
+        self.ref.static_ch[...] = exp      # the oracle's config points at this array
+        self.calibrated = True
+        return exp
 
     def append(self, k, v, t_per_seq=None, dtype=torch.float32):
         """k, v: float32 CPU [B, T, Hkv, D]; the GPU gets them in `dtype`, the
         oracle gets the same values (rounded to `dtype`) as float32."""
         kd, vd = k.to(dtype), v.to(dtype)
+        if not self.calibrated:   # static mask from the first append's first tokens of sequence 0
+            n = min(k.shape[1], 64)
+            self.calibrate(k[0, :n], v[0, :n], dtype)
         tps = None if t_per_seq is None else torch.as_tensor(t_per_seq, dtype=torch.int32)
         kvq.kvq_quantize_append(self.gpu, kd.cuda().contiguous(), vd.cuda().contiguous(),
                                 None if tps is None else tps.cuda())

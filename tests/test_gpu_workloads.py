@@ -19,11 +19,21 @@ pytestmark = pytest.mark.gpu
 SEED = 0
 
 
+def _static_mask(built, dev):
+    """The oracle's own choice of the static channels from the same calibration values."""
+    w = built.w
+    kc, vc = workloads.calibration_kv(w, built.seed, dev)
+    n = w.static_channels
+    return np.stack([oracle.select_static(kc.cpu().numpy(), n), oracle.select_static(vc.cpu().numpy(), n)], 1)
+
+
 def _oracle_unit(built, b, h, dev):
     w = built.w
     tiers = built.tiers[b:b + 1]
     pt, nm, nt = synth.page_table(SEED, 1, w.pages, False, tiers)
-    ref = oracle.OracleCache(ORACLE_FMT[w.fmt], 1, 1, w.D, w.pages, max(nm, 1), nt, page_table=pt)
+    st = _static_mask(built, dev)[h:h + 1] if w.fmt == synth.FMT_CB2S else None
+    ref = oracle.OracleCache(ORACLE_FMT[w.fmt], 1, 1, w.D, w.pages, max(nm, 1), nt, page_table=pt,
+                             static_channels=st)
     for t0, T in workloads.chunks(w.N):
         k, v = workloads.seq_kv(w, built.seed, b, t0, T, dev)
         ref.append(k[:, h:h + 1].cpu().numpy()[None], v[:, h:h + 1].cpu().numpy()[None])
@@ -47,7 +57,7 @@ def _ref_block(ref, entry, role):
     return pool[off:off + stride]
 
 
-@pytest.mark.parametrize("name", ["cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k"])
+@pytest.mark.parametrize("name", ["cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k", "static_4k"])
 def test_full_size_workload_sampled(name):
     w = synth.WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -59,6 +69,8 @@ def test_full_size_workload_sampled(name):
     torch.cuda.synchronize()
     assert built.cache.status_word() == 0
     assert built.cache.seq_lens.cpu().tolist() == [w.N] * w.B
+    if w.fmt == synth.FMT_CB2S:
+        np.testing.assert_array_equal(built.cache.static_mask.cpu().numpy(), _static_mask(built, dev))
     qbits = q.cpu().view(torch.int16).numpy().view(np.uint16)
     rng = np.random.default_rng(1)
     units = [(0, 0), (w.B - 1, w.Hkv - 1)]
