@@ -24,8 +24,8 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S = 0, 1, 2, 3, 4
-BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8, BLK_CB2S = 0, 1, 2, 3, 4
+FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S, FMT_A3 = 0, 1, 2, 3, 4, 5
+BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8, BLK_CB2S, BLK_A3 = 0, 1, 2, 3, 4, 5
 TIER_BIT = 1 << 31
 
 

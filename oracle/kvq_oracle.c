@@ -305,6 +305,15 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /*                               to 12D + 16                                  */
 /*            at 12D + 16        fp16 value(i, t) at 12D + 16 + 32*i + 2*t of */
 /*                               static channel i (K and V alike)             */
+/*  ASYM3     codes  [0, 6D)     3-bit codes at the fragment positions, in    */
+/*  (f3)                         two planes: low 2 bits in u32 words X, lane  */
+/*                               l's word j (steps 2j, 2j+1) at 4*(l*NS/2+j), */
+/*                               slot k of step s at bit 8*(s%2) + 16*(k%2) + */
+/*                               2*(k/2); high bit in u32 words Y at 4D +      */
+/*                               4*(l*NS/4 + s/4), bit 4*(s%4) + 16*(k%2) +   */
+/*                               k/2                                          */
+/*            S at 6D, m at 8D   fp16 per channel c at +2c: x = fp16(q*S + m) */
+/*            outliers at 10D    as CB2's side-list (records at 10D + 4 + 20i)*/
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
 /*            scale at 16D       fp32                                         */
@@ -312,7 +321,7 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /* Page Sizes with Memory Bus Lines").                                        */
 /* ------------------------------------------------------------------------- */
 
-enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3, OR_CB2S = 4 };
+enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3, OR_CB2S = 4, OR_A3 = 5 };
 enum { OR_MAX_STATIC = 8 };
 
 static int round128(int x) { return (x + 127) / 128 * 128; }
@@ -326,6 +335,7 @@ EXPORT int or_block_stride(int fmt, int D)
     case OR_CB2:  return round128(12 * D + 4 + 20 * D);
     case OR_FP8:  return round128(16 * D + 16);
     case OR_CB2S: return round128(12 * D + 16 + 32 * OR_MAX_STATIC);
+    case OR_A3:   return round128(10 * D + 4 + 20 * D);
     }
     return -1;
 }
@@ -382,6 +392,33 @@ static uint8_t cb2_code_get(const uint8_t* blk, int D, int role, int t, int c)
     or_frag_pos(role, t, c, &lane, &s, &k);
     uint16_t v = get_u16(blk + 2 * (D / 16) * lane + 2 * s);
     return (uint8_t)((v >> (4 * (k % 4) + 2 * (k / 4))) & 3u);
+}
+
+/* ASYM3 3-bit codes (layout above). */
+static void a3_code_set(uint8_t* blk, int D, int role, int t, int c, uint8_t q)
+{
+    int lane, s, k, NS = D / 16;
+    or_frag_pos(role, t, c, &lane, &s, &k);
+    uint8_t* x = blk + 4 * (lane * (NS / 2) + s / 2);
+    uint8_t* y = blk + 4 * D + 4 * (lane * (NS / 4) + s / 4);
+    int bx = 8 * (s % 2) + 16 * (k % 2) + 2 * (k / 2), by = 4 * (s % 4) + 16 * (k % 2) + k / 2;
+    uint32_t vx, vy;
+    memcpy(&vx, x, 4);
+    memcpy(&vy, y, 4);
+    vx = (vx & ~(3u << bx)) | ((uint32_t)(q & 3) << bx);
+    vy = (vy & ~(1u << by)) | ((uint32_t)((q >> 2) & 1) << by);
+    memcpy(x, &vx, 4);
+    memcpy(y, &vy, 4);
+}
+static uint8_t a3_code_get(const uint8_t* blk, int D, int role, int t, int c)
+{
+    int lane, s, k, NS = D / 16;
+    or_frag_pos(role, t, c, &lane, &s, &k);
+    uint32_t vx, vy;
+    memcpy(&vx, blk + 4 * (lane * (NS / 2) + s / 2), 4);
+    memcpy(&vy, blk + 4 * D + 4 * (lane * (NS / 4) + s / 4), 4);
+    int bx = 8 * (s % 2) + 16 * (k % 2) + 2 * (k / 2), by = 4 * (s % 4) + 16 * (k % 2) + k / 2;
+    return (uint8_t)(((vx >> bx) & 3u) | (((vy >> by) & 1u) << 2));
 }
 
 static int cb2_slot(int role, int c)
@@ -499,6 +536,8 @@ static void quantize_token_e2m1(const float* x, int D, int role, int t, uint8_t*
 /* s = f32(amax / 448); q = e4m3(f32(x / s)); s == 0 gives q = 0.             */
 /* ------------------------------------------------------------------------- */
 
+static void write_side_list(const float* x, int D, uint8_t mask[16][128], uint8_t* hdr);
+
 static void quantize_page_cb2(const float* x, int D, double sigma, int iters, int role, uint8_t* blk)
 {
     memset(blk, 0, (size_t)or_block_stride(OR_CB2, D));
@@ -518,10 +557,14 @@ static void quantize_page_cb2(const float* x, int D, double sigma, int iters, in
         for (int t = 0; t < 16; ++t)
             cb2_code_set(blk, D, role, t, c, mask[t][c] ? 0 : codes[n++]);
     }
-    /* side-list grouped by channel: one 20-byte record {channel, 0, token
-     * mask, 16 e4m3 values (0 where the token is not an outlier)} for each
-     * channel holding an outlier, channels ascending */
-    uint8_t* hdr = blk + 12 * D;
+    write_side_list(x, D, mask, blk + 12 * D);
+}
+
+/* The outlier side-list of a page (CB2, ASYM3): one 20-byte record {channel,
+ * 0, token mask, 16 e4m3 values (0 where the token is not an outlier)} for
+ * each channel holding an outlier, channels ascending, after {n_ch, total}. */
+static void write_side_list(const float* x, int D, uint8_t mask[16][128], uint8_t* hdr)
+{
     int n_ch = 0, total = 0;
     for (int c = 0; c < D; ++c) {
         unsigned tmask = 0;
@@ -541,6 +584,48 @@ static void quantize_page_cb2(const float* x, int D, double sigma, int iters, in
     }
     hdr[0] = (uint8_t)n_ch;
     hdr[1] = (uint8_t)total;
+}
+
+/* ASYM3 ([P3] "Sub-Byte KV-Cache Quantization": asymmetric 3-bit packing with
+ * dynamic outlier preservation).  Outliers as CB2 (sigma rule per token over
+ * the head vector, e4m3 side-list).  Per channel, over its non-outliers in
+ * binary32 (the INT4 recipe with 8 levels): S = fp16((max - min) / 7),
+ * m = fp16(min), q = clamp(rint((x - m) / S), 0, 7) (q = 0 when S == 0 or the
+ * channel has no non-outlier); outlier slots hold q = 0.  The value a code
+ * stands for is fp16(q * S + m), one rounding of the exact value. */
+static void quantize_page_a3(const float* x, int D, double sigma, int role, uint8_t* blk)
+{
+    memset(blk, 0, (size_t)or_block_stride(OR_A3, D));
+    uint8_t mask[16][128];
+    int kmax = or_kmax(D);
+    for (int t = 0; t < 16; ++t) or_outlier_mask(x + t * D, D, sigma, kmax, mask[t]);
+    for (int c = 0; c < D; ++c) {
+        int have = 0;
+        float mn = 0.0f, mx = 0.0f;
+        for (int t = 0; t < 16; ++t) {
+            if (mask[t][c]) continue;
+            float v = x[t * D + c];
+            if (!have || v < mn) mn = v;
+            if (!have || v > mx) mx = v;
+            have = 1;
+        }
+        uint16_t S16 = 0, m16 = 0;
+        if (have) { S16 = or_fp16_encode((double)((mx - mn) / 7.0f)); m16 = or_fp16_encode((double)mn); }
+        float S = (float)or_fp16_decode(S16), m = (float)or_fp16_decode(m16);
+        put_u16(blk + 6 * D + 2 * c, S16);
+        put_u16(blk + 8 * D + 2 * c, m16);
+        for (int t = 0; t < 16; ++t) {
+            uint8_t q = 0;
+            if (!mask[t][c] && S != 0.0f) {
+                float r = rintf((x[t * D + c] - m) / S);
+                if (r < 0.0f) r = 0.0f;
+                if (r > 7.0f) r = 7.0f;
+                q = (uint8_t)r;
+            }
+            a3_code_set(blk, D, role, t, c, q);
+        }
+    }
+    write_side_list(x, D, mask, blk + 10 * D);
 }
 
 static void quantize_page_fp8(const float* x, int D, int role, uint8_t* blk)
@@ -634,6 +719,9 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
                 xv = or_e2m1_decode(nib_get(blk, D, role, t, c)) * sc;
             } else if (fmt == OR_CB2 || fmt == OR_CB2S) {
                 xv = or_fp16_decode(cb2_cent_get(blk, D, role, c, cb2_code_get(blk, D, role, t, c)));
+            } else if (fmt == OR_A3) {
+                double S = or_fp16_decode(get_u16(blk + 6 * D + 2 * c)), m = or_fp16_decode(get_u16(blk + 8 * D + 2 * c));
+                xv = or_fp16_decode(or_fp16_encode((double)a3_code_get(blk, D, role, t, c) * S + m));   /* exact, then fp16 */
             } else {
                 xv = or_e4m3_decode(blk[fp8_byte(D, role, t, c)]) * (double)get_f32(blk + 16 * D);
             }
@@ -655,8 +743,8 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
             for (int t = 0; t < ntok; ++t)
                 out[t * D + (hdr[1 + i] & (D - 1))] = (float)or_fp16_decode(get_u16(hdr + 16 + 32 * i + 2 * t));
     }
-    if (fmt == OR_CB2) {
-        const uint8_t* hdr = blk + 12 * D;
+    if (fmt == OR_CB2 || fmt == OR_A3) {
+        const uint8_t* hdr = blk + (fmt == OR_CB2 ? 12 : 10) * D;
         int n_ch = hdr[0];
         for (int i = 0; i < n_ch; ++i) {
             const uint8_t* rec = hdr + 4 + 20 * i;
@@ -682,6 +770,7 @@ EXPORT void or_quantize_page_static(int D, int iters, int role, const float* x, 
 EXPORT void or_quantize_page(int fmt, int D, double sigma, int iters, int role, const float* x, uint8_t* blk)
 {
     if (fmt == OR_CB2) quantize_page_cb2(x, D, sigma, iters, role, blk);
+    else if (fmt == OR_A3) quantize_page_a3(x, D, sigma, role, blk);
     else quantize_page_fp8(x, D, role, blk);
 }
 
@@ -699,7 +788,7 @@ EXPORT void or_quantize_page(int fmt, int D, double sigma, int iters, int role, 
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier), 4 CB2 static */
+    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier), 4 CB2 static, 5 ASYM3 */
     int32_t B, Hkv, D, pages_per_seq_max, num_pages, num_tier_pages;
     int32_t iters;
     double sigma;
@@ -708,7 +797,7 @@ typedef struct {
 } or_cfg;
 
 static int page_fmt(const or_cfg* c) { return c->fmt == 3 ? OR_CB2 : c->fmt; }
-static int is_paged(const or_cfg* c) { return c->fmt == OR_CB2 || c->fmt == 3 || c->fmt == OR_CB2S; }
+static int is_paged(const or_cfg* c) { return c->fmt == OR_CB2 || c->fmt == 3 || c->fmt == OR_CB2S || c->fmt == OR_A3; }
 
 static int entry_ok(const or_cfg* c, int32_t e)
 {
@@ -776,7 +865,7 @@ EXPORT int or_append(const or_cfg* c, uint8_t* pool, uint8_t* tier_pool, const i
                             quantize_page_cb2s(x, D, c->iters, role, c->static_ch + ((size_t)h * 2 + role) * c->n_static,
                                                c->n_static, blk);
                         else
-                            or_quantize_page(tier ? OR_FP8 : OR_CB2, D, c->sigma, c->iters, role, x, blk);
+                            or_quantize_page(tier ? OR_FP8 : page_fmt(c), D, c->sigma, c->iters, role, x, blk);
                         free(x);
                     } else {
                         for (int pos = lo; pos < hi; ++pos)

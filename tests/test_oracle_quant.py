@@ -352,3 +352,70 @@ def test_cb2_static_cache_round_trip():
         got = a.dequantize(1, 1, role, 0, 48)
         want = np.array([[oracle.fp16_decode(oracle.fp16_encode(float(v))) for v in row] for row in x[role][1, :48, 1][:, [3, 40]]])
         assert (got[:, [3, 40]] == want).all()
+
+
+# ----------------------------------------------------------------------------- ASYM3 (3-bit asymmetric + outliers)
+def _a3_code(blk, D, role, t, c):
+    """3-bit code of (t, c), unpacked from the documented bit positions."""
+    lane, s, k = oracle.frag_pos(role, t, c)
+    NS = D // 16
+    x = int.from_bytes(bytes(blk[4 * (lane * (NS // 2) + s // 2):][:4]), "little")
+    y = int.from_bytes(bytes(blk[4 * D + 4 * (lane * (NS // 4) + s // 4):][:4]), "little")
+    bx = 8 * (s % 2) + 16 * (k % 2) + 2 * (k // 2)
+    by = 4 * (s % 4) + 16 * (k % 2) + k // 2
+    return ((x >> bx) & 3) | (((y >> by) & 1) << 2)
+
+
+def test_a3_page_matches_the_recipe():
+    """Per channel over its non-outliers, in binary32: S = fp16((max-min)/7),
+    m = fp16(min), q = clamp(rint((x-m)/S), 0, 7); outlier slots hold 0; the
+    side-list is CB2's for the same page; a code stands for fp16(q*S + m)
+    ("Sub-5ms MoE Inference", Sub-Byte KV-Cache Quantization: asymmetric 3-bit
+    packing with dynamic outlier preservation)."""
+    rng = np.random.default_rng(21)
+    for trial in range(6):
+        D = (64, 128)[trial % 2]
+        role = (trial // 2) % 2
+        x = rng.standard_normal((16, D)).astype(np.float32)
+        x[:, rng.choice(D, 3, replace=False)] *= 8
+        if trial == 5:
+            x[:, 7] = 0.25          # a constant channel: S = 0, every code 0
+        blk = oracle.quantize_page(oracle.BLK_A3, D, x, role=role)
+        cb2 = oracle.quantize_page(oracle.BLK_CB2, D, x, role=role)
+        assert (blk[10 * D:10 * D + 4 + 20 * D] == cb2[12 * D:12 * D + 4 + 20 * D]).all()
+        masks = np.array([oracle.outlier_mask(x[t])[0] for t in range(16)])
+        xh = oracle.dequantize_block(oracle.BLK_A3, D, blk, role=role)
+        for c in range(D):
+            keep = ~masks[:, c]
+            vals = x[keep, c]
+            S16 = oracle.fp16_encode(float(np.float32(vals.max() - vals.min()) / np.float32(7))) if keep.any() else 0
+            m16 = oracle.fp16_encode(float(vals.min())) if keep.any() else 0
+            assert int(blk[6 * D + 2 * c]) | (int(blk[6 * D + 2 * c + 1]) << 8) == S16
+            assert int(blk[8 * D + 2 * c]) | (int(blk[8 * D + 2 * c + 1]) << 8) == m16
+            S, m = np.float32(oracle.fp16_decode(S16)), np.float32(oracle.fp16_decode(m16))
+            for t in range(16):
+                q = _a3_code(blk, D, role, t, c)
+                if masks[t, c] or S == 0:
+                    assert q == 0
+                else:
+                    assert q == int(np.clip(np.rint((x[t, c] - m) / S), 0, 7))
+                want = oracle.fp16_decode(oracle.fp16_encode(q * float(S) + float(m)))
+                if masks[t, c]:
+                    want = oracle.e4m3_decode(oracle.e4m3_encode(float(x[t, c])))
+                assert xh[t, c] == np.float32(want)
+                if not masks[t, c]:   # half a step plus the fp16 rounding of the level
+                    assert abs(float(xh[t, c]) - float(x[t, c])) <= float(S) / 2 + abs(want) * 2.0 ** -11 + 1e-7
+
+
+def test_a3_cache_chunking_independent():
+    rng = np.random.default_rng(22)
+    B, Hkv, D, P = 2, 2, 128, 4
+    x = rng.standard_normal((2, B, 50, Hkv, D)).astype(np.float32)
+    x[..., 9] *= 10
+    a = oracle.OracleCache(oracle.FMT_A3, B, Hkv, D, P, B * P)
+    b = oracle.OracleCache(oracle.FMT_A3, B, Hkv, D, P, B * P)
+    a.append(x[0], x[1])
+    for t0, t1 in ((0, 5), (5, 16), (16, 40), (40, 50)):
+        b.append(x[0][:, t0:t1], x[1][:, t0:t1])
+    assert (a.pool == b.pool).all() and (a.staging[:, :, :, :2] == b.staging[:, :, :, :2]).all()
+    assert (a.dequantize(0, 1, 1, 0, 50) == b.dequantize(0, 1, 1, 0, 50)).all()
