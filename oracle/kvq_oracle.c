@@ -312,7 +312,10 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /*                               2*(k/2); high bit in u32 words Y at 4D +      */
 /*                               4*(l*NS/4 + s/4), bit 4*(s%4) + 16*(k%2) +   */
 /*                               k/2                                          */
-/*            S at 6D, m at 8D   fp16 per channel c at +2c: x = fp16(q*S + m) */
+/*            S at 6D, m at 8D   fp16 per channel c at +2*rho(c):             */
+/*                               x = fp16(q*S + m); K: rho(c) = 16*(c/16) +   */
+/*                               4*((c%8)/2) + 2*((c%16)/8) + c%2, V: rho(c)  */
+/*                               = 16*(c/16) + 2*(c%8) + (c%16)/8             */
 /*            outliers at 10D    as CB2's side-list (records at 10D + 4 + 20i)*/
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
@@ -392,6 +395,13 @@ static uint8_t cb2_code_get(const uint8_t* blk, int D, int role, int t, int c)
     or_frag_pos(role, t, c, &lane, &s, &k);
     uint16_t v = get_u16(blk + 2 * (D / 16) * lane + 2 * s);
     return (uint8_t)((v >> (4 * (k % 4) + 2 * (k / 4))) & 3u);
+}
+
+/* ASYM3 per-channel S / m position (layout above). */
+static int a3_rho(int role, int c)
+{
+    if (role == 0) return 16 * (c / 16) + 4 * ((c % 8) / 2) + 2 * ((c % 16) / 8) + c % 2;
+    return 16 * (c / 16) + 2 * (c % 8) + (c % 16) / 8;
 }
 
 /* ASYM3 3-bit codes (layout above). */
@@ -612,8 +622,8 @@ static void quantize_page_a3(const float* x, int D, double sigma, int role, uint
         uint16_t S16 = 0, m16 = 0;
         if (have) { S16 = or_fp16_encode((double)((mx - mn) / 7.0f)); m16 = or_fp16_encode((double)mn); }
         float S = (float)or_fp16_decode(S16), m = (float)or_fp16_decode(m16);
-        put_u16(blk + 6 * D + 2 * c, S16);
-        put_u16(blk + 8 * D + 2 * c, m16);
+        put_u16(blk + 6 * D + 2 * a3_rho(role, c), S16);
+        put_u16(blk + 8 * D + 2 * a3_rho(role, c), m16);
         for (int t = 0; t < 16; ++t) {
             uint8_t q = 0;
             if (!mask[t][c] && S != 0.0f) {
@@ -720,7 +730,8 @@ EXPORT void or_dequantize_block(int fmt, int D, const uint8_t* blk, int role, in
             } else if (fmt == OR_CB2 || fmt == OR_CB2S) {
                 xv = or_fp16_decode(cb2_cent_get(blk, D, role, c, cb2_code_get(blk, D, role, t, c)));
             } else if (fmt == OR_A3) {
-                double S = or_fp16_decode(get_u16(blk + 6 * D + 2 * c)), m = or_fp16_decode(get_u16(blk + 8 * D + 2 * c));
+                double S = or_fp16_decode(get_u16(blk + 6 * D + 2 * a3_rho(role, c)));
+                double m = or_fp16_decode(get_u16(blk + 8 * D + 2 * a3_rho(role, c)));
                 xv = or_fp16_decode(or_fp16_encode((double)a3_code_get(blk, D, role, t, c) * S + m));   /* exact, then fp16 */
             } else {
                 xv = or_e4m3_decode(blk[fp8_byte(D, role, t, c)]) * (double)get_f32(blk + 16 * D);

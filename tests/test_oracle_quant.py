@@ -390,8 +390,10 @@ def test_a3_page_matches_the_recipe():
             vals = x[keep, c]
             S16 = oracle.fp16_encode(float(np.float32(vals.max() - vals.min()) / np.float32(7))) if keep.any() else 0
             m16 = oracle.fp16_encode(float(vals.min())) if keep.any() else 0
-            assert int(blk[6 * D + 2 * c]) | (int(blk[6 * D + 2 * c + 1]) << 8) == S16
-            assert int(blk[8 * D + 2 * c]) | (int(blk[8 * D + 2 * c + 1]) << 8) == m16
+            rho = (16 * (c // 16) + 4 * ((c % 8) // 2) + 2 * ((c % 16) // 8) + c % 2 if role == 0
+                   else 16 * (c // 16) + 2 * (c % 8) + (c % 16) // 8)
+            assert int(blk[6 * D + 2 * rho]) | (int(blk[6 * D + 2 * rho + 1]) << 8) == S16
+            assert int(blk[8 * D + 2 * rho]) | (int(blk[8 * D + 2 * rho + 1]) << 8) == m16
             S, m = np.float32(oracle.fp16_decode(S16)), np.float32(oracle.fp16_decode(m16))
             for t in range(16):
                 q = _a3_code(blk, D, role, t, c)
