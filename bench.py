@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 from sub_byte_quantized_kvq_gb300 import kvq, synth, workloads  # noqa: E402
 
 METRIC = "quantized-KV decode attention: achieved HBM GB/s vs peak; us per decode step"
-FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC"}
+FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC", 5: "ASYM3_OUTLIER"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 KERNEL_SOURCES = ["kvq_common.cuh", "kvq_decode.cuh", "kvq_internal.cuh"]
 
@@ -106,6 +106,12 @@ def algorithmic_bytes(built: workloads.Built) -> dict:
         n_tier = int(built.tiers[:, :full].sum()) * w.Hkv * 2
         n_main = full * blocks - n_tier
         cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
+        tail = (L % 16) * D * 4 * blocks
+    elif w.fmt == synth.FMT_A3:
+        # codes (6D) + S and m (4D) + side-list header and records
+        pool = cache.pool.view(-1, cache.block_bytes(0))
+        nch = pool[:, 10 * D].to(torch.int64)
+        cache_bytes = full * blocks * 10 * D + (4 + 20 * nch).sum().item()
         tail = (L % 16) * D * 4 * blocks
     elif w.fmt == synth.FMT_CB2S:
         # codes + codebook (12D) + {n_s, channels} (16) + the static channels' fp16 values
@@ -301,6 +307,9 @@ def oracle_sample(w: synth.Workload, seed: int):
         cache += (N % 16) * D * 4 * w.Hkv * 2
     elif w.fmt == synth.FMT_CB2S:
         cache = full * w.Hkv * 2 * (12 * D + 16 + 32 * w.static_channels) + (N % 16) * D * 4 * w.Hkv * 2
+    elif w.fmt == synth.FMT_A3:
+        nch = ref.pool.reshape(-1, ref.stride)[:, 10 * D].astype(np.int64)
+        cache = full * w.Hkv * 2 * 10 * D + int((4 + 20 * nch).sum()) + (N % 16) * D * 4 * w.Hkv * 2
     elif w.fmt == synth.FMT_INT4:
         counts = int(ref.pool.reshape(-1, ref.stride)[:, 10 * D:10 * D + 16].astype(np.int64).sum())
         cache = pages * w.Hkv * 2 * (10 * D + 16) + 3 * counts

@@ -87,7 +87,15 @@ typedef enum {
      * side-list).  kvq_select_static_channels picks the mask (top channels by
      * absolute magnitude) from calibration values.  Quantized when a page
      * fills; the partial last page waits in fp32 staging. */
-    KVQ_FMT_CB2_STATIC = 4
+    KVQ_FMT_CB2_STATIC = 4,
+    /* [P3] "Sub-Byte KV-Cache Quantization": asymmetric 3-bit codes with
+     * dynamic outlier preservation.  Per (page, channel) over its
+     * non-outliers: S = fp16((max - min)/7), m = fp16(min), q =
+     * clamp(rint((x - m)/S), 0, 7) (binary32); a code stands for
+     * fp16(q*S + m).  Outliers as KVQ_FMT_CB2_OUTLIER (sigma rule per token,
+     * e4m3 side-list).  Quantized when a page fills; the partial last page
+     * waits in fp32 staging. */
+    KVQ_FMT_ASYM3_OUTLIER = 5
 } kvq_format;
 
 typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
@@ -311,6 +319,15 @@ const char* kvq_version(void);
  *             12D       u8 n_s, u8 channel[n_s] (ascending), zeros to 12D + 16
  *             12D + 16  fp16 value of static channel i, token t at 12D + 16 + 32*i + 2*t
  *             stride 1152 (D=64), 1920 (D=128)
+ *   ASYM3     [0, 4D)   low 2 code bits: u32 word j of lane l (steps 2j, 2j+1) at
+ *                       4*(l*NS/2 + j), slot k of step s at bit 8*(s%2) + 16*(k%2) + 2*(k/2)
+ *             4D        high code bit: u32 word at 4D + 4*(l*NS/4 + s/4), bit
+ *                       4*(s%4) + 16*(k%2) + k/2
+ *             6D, 8D    fp16 S and m of channel c at +2*rho(c); K: rho(c) = 16*(c/16) +
+ *                       4*((c%8)/2) + 2*((c%16)/8) + c%2, V: rho(c) = 16*(c/16) +
+ *                       2*(c%8) + (c%16)/8
+ *             10D       outlier side-list as CB2's (records at 10D + 4 + 20*i)
+ *             stride 2048 (D=64), 3968 (D=128)
  *   FP8 tier  [0, 16D)  codes: lane l at 8*NS*l, step s at +8s, slot k = byte k (e4m3)
  *             16D       fp32 scale
  *             stride 1152 (D=64), 2176 (D=128)

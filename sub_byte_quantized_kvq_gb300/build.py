@@ -21,7 +21,8 @@ COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relax
 # multiply-add), so that they match the CPU oracle bit for bit.
 PER_TU = {"kvq_quantize.cu": ["--fmad=false"]}
 TUS = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu", "kvq_decode_int4.cu", "kvq_decode_e2m1.cu",
-       "kvq_decode_cb2.cu", "kvq_decode_tiered.cu", "kvq_decode_cb2s.cu", "kvq_noalloc.cu"]
+       "kvq_decode_cb2.cu", "kvq_decode_tiered.cu", "kvq_decode_cb2s.cu",
+       "kvq_decode_a3.cu", "kvq_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -34,6 +34,17 @@ struct DequantArgs {
   int Hkv, D, ppsm, num_pages, num_tier_pages, fmt, seq, head, role, t0, t1;
 };
 
+// The value an outlier side-list (CB2, ASYM3) gives (t, c), else v.
+__device__ __forceinline__ float side_list_value(const uint8_t* hdr, int D, int t, int c, float v) {
+  const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
+  for (int i = 0; i < n_ch; ++i) {
+    const uint8_t* rec = hdr + 4 + 20 * i;
+    const uint32_t tm = rec[2] | (rec[3] << 8);
+    if (rec[0] == c && (tm >> t & 1u)) v = dq_e4m3(rec[4 + t]);
+  }
+  return v;
+}
+
 __global__ void dequantize_kernel(const DequantArgs a) {
   const int D = a.D, NS = D / 16;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -41,7 +52,8 @@ __global__ void dequantize_kernel(const DequantArgs a) {
   const int pos = a.t0 + (int)(idx / D), c = (int)(idx % D);
   const int t = pos % kPage, pg = pos / kPage;
   const int L = a.seq_lens[a.seq];
-  const bool paged = a.fmt == KVQ_FMT_CB2_OUTLIER || a.fmt == KVQ_FMT_TIERED || a.fmt == KVQ_FMT_CB2_STATIC;
+  const bool paged = a.fmt == KVQ_FMT_CB2_OUTLIER || a.fmt == KVQ_FMT_TIERED || a.fmt == KVQ_FMT_CB2_STATIC ||
+                     a.fmt == KVQ_FMT_ASYM3_OUTLIER;
   float v = 0.f;
   if (pos >= L || pg >= a.ppsm) {
     v = 0.f;
@@ -86,15 +98,23 @@ __global__ void dequantize_kernel(const DequantArgs a) {
             const uint8_t* vp = blk + cb2s_val_off(D) + 32 * i + 2 * t;
             v = dq_f16(vp[0] | (vp[1] << 8));
           }
-      } else {                // outlier side-list
-        const uint8_t* hdr = blk + cb2_out_off(D);
-        const int n_ch = min((int)hdr[0], D);  // a corrupt side-list never reads past its block
-        for (int i = 0; i < n_ch; ++i) {
-          const uint8_t* rec = hdr + 4 + 20 * i;
-          const uint32_t tm = rec[2] | (rec[3] << 8);
-          if (rec[0] == c && (tm >> t & 1u)) v = dq_e4m3(rec[4 + t]);
-        }
+      } else {
+        v = side_list_value(blk + cb2_out_off(D), D, t, c, v);
       }
+    } else if (bf == kBlkA3) {
+      uint32_t vx, vy;
+      memcpy(&vx, blk + 4 * (p.lane * (NS / 2) + p.step / 2), 4);
+      memcpy(&vy, blk + a3_hi_off(D) + 4 * (p.lane * (NS / 4) + p.step / 4), 4);
+      const int bx = 8 * (p.step % 2) + 16 * (p.slot % 2) + 2 * (p.slot / 2);
+      const int by = 4 * (p.step % 4) + 16 * (p.slot % 2) + p.slot / 2;
+      const uint32_t q = ((vx >> bx) & 3u) | (((vy >> by) & 1u) << 2);
+      const int r = a3_rho(a.role, c);
+      const uint8_t* sp = blk + a3_s_off(D) + 2 * r;
+      const uint8_t* mp = blk + a3_m_off(D) + 2 * r;
+      // fp16(q * S + m): one rounding of the exact value (fp16 fused multiply-add)
+      v = __half2float(__hfma(__float2half_rn((float)q), __ushort_as_half((unsigned short)(sp[0] | (sp[1] << 8))),
+                              __ushort_as_half((unsigned short)(mp[0] | (mp[1] << 8)))));
+      v = side_list_value(blk + a3_out_off(D), D, t, c, v);
     } else {
       float s;
       memcpy(&s, blk + fp8_sc_off(D), 4);
@@ -135,7 +155,7 @@ cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int
 static bool cfg_ok(const kvq_config* c) {
   if (!c) return false;
   if (c->num_seqs <= 0 || c->num_kv_heads <= 0 || c->pages_per_seq_max <= 0 || c->num_pages <= 0) return false;
-  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_CB2_STATIC) return false;
+  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_ASYM3_OUTLIER) return false;
   if (c->format == KVQ_FMT_CB2_STATIC && (c->static_channels < 1 || c->static_channels > kMaxStatic)) return false;
   if (c->num_tier_pages < 0 || (c->format != KVQ_FMT_TIERED && c->num_tier_pages != 0)) return false;
   if (!(c->sigma >= 3.0) || !std::isfinite(c->sigma)) return false;
@@ -145,7 +165,7 @@ static bool cfg_ok(const kvq_config* c) {
 }
 static bool dim_supported(const kvq_config* c) { return c->head_dim == 64 || c->head_dim == 128; }
 static bool paged_format(int f) {
-  return f == KVQ_FMT_CB2_OUTLIER || f == KVQ_FMT_TIERED || f == KVQ_FMT_CB2_STATIC;
+  return f == KVQ_FMT_CB2_OUTLIER || f == KVQ_FMT_TIERED || f == KVQ_FMT_CB2_STATIC || f == KVQ_FMT_ASYM3_OUTLIER;
 }
 static bool cache_ok(const kvq_config* c, const kvq_cache* k) {
   if (!k || !k->pool || !k->page_table || !k->seq_lens || !k->status) return false;

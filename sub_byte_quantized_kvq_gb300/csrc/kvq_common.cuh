@@ -14,7 +14,7 @@ namespace kvq {
 constexpr int kPage = KVQ_PAGE_TOKENS;
 
 // Block formats (the pool format of a cache; FP8 is the tier-1 page format).
-enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3, kBlkCb2s = 4 };
+enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3, kBlkCb2s = 4, kBlkA3 = 5 };
 constexpr int kMaxStatic = 8;   // CB2_STATIC: static fp16 channels per (kv head, K|V)
 
 // Largest number of values of an n-vector that can lie more than 3 standard
@@ -34,12 +34,22 @@ __host__ __device__ constexpr int cb2_out_off(int D) { return 12 * D; }   // out
 __host__ __device__ constexpr int fp8_sc_off(int D) { return 16 * D; }
 __host__ __device__ constexpr int cb2s_hdr_off(int D) { return 12 * D; }      // u8 n_s, u8 channel[n_s]
 __host__ __device__ constexpr int cb2s_val_off(int D) { return 12 * D + 16; } // fp16 [n_s][16]
+__host__ __device__ constexpr int a3_hi_off(int D) { return 4 * D; }          // high code bits
+__host__ __device__ constexpr int a3_s_off(int D) { return 6 * D; }           // fp16 S by rho(c)
+__host__ __device__ constexpr int a3_m_off(int D) { return 8 * D; }           // fp16 m by rho(c)
+__host__ __device__ constexpr int a3_out_off(int D) { return 10 * D; }        // outlier side-list
+// ASYM3 position of channel c's S / m (K: 4 channels of a lane-step adjacent; V: 2).
+__host__ __device__ inline int a3_rho(int role, int c) {
+  return role == 0 ? 16 * (c / 16) + 4 * ((c % 8) / 2) + 2 * ((c % 16) / 8) + c % 2
+                   : 16 * (c / 16) + 2 * (c % 8) + (c % 16) / 8;
+}
 
 __host__ __device__ constexpr int block_stride(int fmt, int D) {
   return fmt == kBlkInt4 ? round_up128(10 * D + 16 + 48 * int4_cap(D))
        : fmt == kBlkE2m1 ? round_up128(9 * D)
        : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 20 * D)
        : fmt == kBlkCb2s ? round_up128(12 * D + 16 + 32 * kMaxStatic)
+       : fmt == kBlkA3   ? round_up128(10 * D + 4 + 20 * D)
                          : round_up128(16 * D + 16);
 }
 

@@ -21,6 +21,7 @@ static KernelInfo pick_kernel(int fmt, int D, int G) {
     case KVQ_FMT_FP4_E2M1_S16: return decode_kernel_e2m1(D, G);
     case KVQ_FMT_CB2_OUTLIER: return decode_kernel_cb2(D, G);
     case KVQ_FMT_CB2_STATIC: return decode_kernel_cb2s(D, G);
+    case KVQ_FMT_ASYM3_OUTLIER: return decode_kernel_a3(D, G);
     default: return decode_kernel_tiered(D, G);
   }
 }

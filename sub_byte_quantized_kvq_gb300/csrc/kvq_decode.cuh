@@ -47,9 +47,11 @@ constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 
 template <int FMT>
 struct Fmt {
-  static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED || FMT == KVQ_FMT_CB2_STATIC);
+  static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED || FMT == KVQ_FMT_CB2_STATIC ||
+                                  FMT == KVQ_FMT_ASYM3_OUTLIER);
   static constexpr int kMain = FMT == KVQ_FMT_TIERED ? kBlkCb2 : FMT;
-  static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2);
+  static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2 || kMain == kBlkA3);
+  static constexpr bool kSideList = (kMain == kBlkCb2 || kMain == kBlkA3);   // 20-byte outlier records
   static constexpr int kPPI = kMain == kBlkInt4 ? 1 : 2;   // pages per warp iteration
 };
 
@@ -60,6 +62,7 @@ __host__ __device__ constexpr int fetch_bytes(int blk) {
        : blk == kBlkE2m1 ? 9 * D
        : blk == kBlkCb2  ? 12 * D + kOutPrefetch
        : blk == kBlkCb2s ? 12 * D + 16 + 32 * kMaxStatic   // the copy itself takes 32 n_s
+       : blk == kBlkA3   ? 10 * D + kOutPrefetch
                          : 16 * D + 16;
 }
 template <int FMT, int D>
@@ -203,6 +206,66 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
   return __half2float(__ushort_as_half((unsigned short)(bits & 0xFFFFu)));
 }
 
+// ASYM3: a code q stands for fp16(q * S + m).  The low 2 bits come from
+// words X (two steps each), the high bit from words Y (four steps each);
+// register r of step s holds slots 2r (low half) and 2r + 1 (high half).
+template <int D>
+__device__ __forceinline__ void load_a3_words(uint32_t blk_s, int lane, uint32_t (&xw)[D / 32],
+                                              uint32_t (&yw)[D / 64]) {
+  if constexpr (D == 128) {
+    const uint4 x = lds128(blk_s + 16 * lane);
+    const uint2 y = lds64(blk_s + a3_hi_off(D) + 8 * lane);
+    xw[0] = x.x; xw[1] = x.y; xw[2] = x.z; xw[3] = x.w;
+    yw[0] = y.x; yw[1] = y.y;
+  } else {
+    const uint2 x = lds64(blk_s + 8 * lane);
+    xw[0] = x.x; xw[1] = x.y;
+    yw[0] = lds32(blk_s + a3_hi_off(D) + 4 * lane);
+  }
+}
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// fp16x2 {q(2r), q(2r+1)} of step s, then fp16(q * S + m) with one rounding.
+// (s and r are loop indices of fully unrolled loops: the shifts fold to constants.)
+__device__ __forceinline__ uint32_t a3_value(uint32_t xw, uint32_t yw, int S_, int R, uint32_t sc, uint32_t zp) {
+  const int SH = 4 * (S_ & 3) + R;   // the high bits sit at SH and SH + 16
+  const uint32_t lo = (xw >> (8 * (S_ & 1) + 2 * R)) & 0x00030003u;
+  const uint32_t hi = (SH >= 2 ? (yw >> (SH - 2)) : (yw << (2 - SH))) & 0x00040004u;
+  const uint32_t q1024 = lo | hi | 0x64006400u;   // fp16 1024 + q, exact
+  const uint32_t q = h2_as_u32(__hsub2(u32_as_h2(q1024), u32_as_h2(0x64006400u)));
+  return hfma2_rn(q, sc, zp);
+}
+// K role: channels x = 16s + 2q, x + 1 (registers 0, 1: tokens g, g + 8) and
+// x + 8, x + 9 (registers 2, 3); their S and m are 4 adjacent fp16.
+template <int D>
+__device__ __forceinline__ void a3_k_frag(uint32_t kb_s, const uint32_t (&xw)[D / 32], const uint32_t (&yw)[D / 64],
+                                          int S_, int q4, uint32_t (&a)[4]) {
+  const uint2 sc = lds64(kb_s + a3_s_off(D) + 2 * (16 * S_ + 4 * q4));
+  const uint2 zp = lds64(kb_s + a3_m_off(D) + 2 * (16 * S_ + 4 * q4));
+  const uint32_t x = xw[S_ >> 1], y = yw[S_ >> 2];
+  a[0] = a3_value(x, y, S_, 0, sc.x, zp.x);
+  a[1] = a3_value(x, y, S_, 1, sc.x, zp.x);
+  a[2] = a3_value(x, y, S_, 2, sc.y, zp.y);
+  a[3] = a3_value(x, y, S_, 3, sc.y, zp.y);
+}
+// V role: channels c = 16s + g (registers 0, 2) and c + 8 (registers 1, 3).
+template <int D>
+__device__ __forceinline__ void a3_v_frag(uint32_t vb_s, const uint32_t (&xw)[D / 32], const uint32_t (&yw)[D / 64],
+                                          int S_, int g, uint32_t (&a)[4]) {
+  const uint32_t sc = lds32(vb_s + a3_s_off(D) + 2 * (16 * S_ + 2 * g));
+  const uint32_t zp = lds32(vb_s + a3_m_off(D) + 2 * (16 * S_ + 2 * g));
+  const uint32_t sA = prmt(sc, sc, 0x1010u), sB = prmt(sc, sc, 0x3232u);
+  const uint32_t mA = prmt(zp, zp, 0x1010u), mB = prmt(zp, zp, 0x3232u);
+  const uint32_t x = xw[S_ >> 1], y = yw[S_ >> 2];
+  a[0] = a3_value(x, y, S_, 0, sA, mA);
+  a[1] = a3_value(x, y, S_, 1, sB, mB);
+  a[2] = a3_value(x, y, S_, 2, sA, mA);
+  a[3] = a3_value(x, y, S_, 3, sB, mB);
+}
+
 // ----------------------------------------------------------------------------- CB2 outlier corrections
 // Side-list of a CB2 block (at 12D): {u8 n_ch, u8 total, 0, 0}, then n_ch
 // 20-byte records {u8 channel, 0, u16 token mask, u8 value[16]} (e4m3 values,
@@ -227,11 +290,25 @@ __device__ __forceinline__ uint32_t c0_bits(uint32_t blk_s, int slot) {
   return prmt(lh.x, lh.y, 0x4040u);
 }
 
+// {c0, c0}: the value code 0 of channel c stands for -- CB2: centroid 0;
+// ASYM3: m (q = 0 gives fp16(0 * S + m) = m).
+template <int D, int BLK>
+__device__ __forceinline__ uint32_t code0_bits(uint32_t blk_s, int role, int c) {
+  if constexpr (BLK == kBlkA3) {
+    const uint32_t m = lds16(blk_s + a3_m_off(D) + 2 * a3_rho(role, c));
+    return prmt(m, m, 0x1010u);
+  } else {
+    return c0_bits<D>(blk_s, cb2_slot(role, c));
+  }
+}
+template <int D, int BLK>
+__host__ __device__ constexpr int side_off() { return BLK == kBlkA3 ? a3_out_off(D) : cb2_out_off(D); }
+
 // Scores of tokens g, g + 8 += sum over the chunk's channels c of
 // q[h][c] * (x - c0[c]): one m16n8k8 tile, A = tokens x slots (slot i = the
 // chunk's record i; slots >= nc are zero), B = Q^T gathered at the slots'
 // channels.  recs: shared address of the chunk's first record.
-template <int D, int NT>
+template <int D, int NT, int BLK>
 __device__ __forceinline__ void cb2_k_correct(uint32_t recs, int nc, uint32_t kb_s, uint32_t qsm_s, int G, int GS,
                                               int lane, float (&acc)[NT][4]) {
   const int g = lane >> 2, q4 = lane & 3;
@@ -247,7 +324,7 @@ __device__ __forceinline__ void cb2_k_correct(uint32_t recs, int nc, uint32_t kb
   // bits g / g + 8 of each mask in the sign bits of bytes 0 / 1 (A) and 2 / 3
   // (B); prmt's sign-replicate mode widens them into half masks.
   const uint32_t c01 =
-      prmt(c0_bits<D>(kb_s, hA & (D - 1)), c0_bits<D>(kb_s, hB & (D - 1)), 0x5410u) ^ 0x80008000u;
+      prmt(code0_bits<D, BLK>(kb_s, 0, hA & (D - 1)), code0_bits<D, BLK>(kb_s, 0, hB & (D - 1)), 0x5410u) ^ 0x80008000u;
   const uint32_t xm = prmt(hA, hB, 0x7632u) << (7 - g);
   const uint32_t n0 = c01 & prmt(xm, 0u, 0xAA88u), n1 = c01 & prmt(xm, 0u, 0xBB99u);
 #pragma unroll
@@ -264,7 +341,7 @@ __device__ __forceinline__ void cb2_k_correct(uint32_t recs, int nc, uint32_t kb
 // Output correction of the chunk's channels: corr[c][h] += sum_t p[t][h] *
 // (x - c0[c]).  A = slots x tokens (row g = slot g; rows 8..15 are empty)
 // against the page's P^T fragments; each (channel, head) is written by one lane.
-template <int D, int NT>
+template <int D, int NT, int BLK>
 __device__ __forceinline__ void cb2_v_correct(uint32_t recs, int nc, uint32_t vb_s, const uint32_t (&phi)[NT][2],
                                               const uint32_t (&plo)[NT][2], uint32_t corr_s, int G, int GS,
                                               int lane) {
@@ -279,7 +356,7 @@ __device__ __forceinline__ void cb2_v_correct(uint32_t recs, int nc, uint32_t vb
   // token masks: (mask << 7 - t0) / (mask << 6 - t0) hold bits t0 / t0 + 1 (and
   // + 8) in the sign bits of bytes 0 (and 1)
   const uint32_t m = hr >> 16, x = m << (7 - t0), y = m << (6 - t0);
-  const uint32_t c0 = c0_bits<D>(vb_s, cb2_slot(1, ch)) ^ 0x80008000u;
+  const uint32_t c0 = code0_bits<D, BLK>(vb_s, 1, ch) ^ 0x80008000u;
   const uint32_t n0 = c0 & prmt(x, y, 0xCC88u), n2 = c0 & prmt(x, y, 0xDD99u);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -561,13 +638,16 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
   for (int p = 0; p < PPI; ++p) tier[p] = T && ent[p] < 0;
 
+  constexpr bool A3 = Fmt<FMT>::kMain == kBlkA3;
+  constexpr int SIDE = side_off<D, Fmt<FMT>::kMain>();
   float acc[PPI][NT][4];
-  uint32_t kc[PPI][NS / 2];
+  uint32_t kc[PPI][NS / 2], ky[PPI][A3 ? NS / 4 : 1];   // codes (ASYM3: low-bit and high-bit words)
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
-    load_codes<D>(kb_s[p], lane, kc[p]);
+    if constexpr (A3) load_a3_words<D>(kb_s[p], lane, kc[p], ky[p]);
+    else load_codes<D>(kb_s[p], lane, kc[p]);
   }
 #pragma unroll
   for (int s = 0; s < NS; ++s)
@@ -575,6 +655,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     for (int p = 0; p < PPI; ++p) {
       uint32_t ak[4];
       if (T && tier[p]) fp8_frag(lds64(kb_s[p] + 8 * NS * lane + 8 * s), ak);
+      else if constexpr (A3) a3_k_frag<D>(kb_s[p], kc[p], ky[p], s, q4, ak);
       else cb2_k_frag(kb_s[p] + cb2_cb_off(D) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
@@ -597,16 +678,15 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
     if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
-    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(kb_s[p] + cb2_out_off(D)), D);
+    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(kb_s[p] + SIDE), D);
 #pragma unroll 1
     for (int base = 0; base < n_ch; base += kChunk) {
-      uint32_t recs = kb_s[p] + cb2_out_off(D) + 4;
+      uint32_t recs = kb_s[p] + SIDE + 4;
       if (base > 0) {
-        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + cb2_out_off(D), base, min(kChunk, n_ch - base),
-                   sm.bounce_s, lane);
+        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
         recs = sm.bounce_s;
       }
-      cb2_k_correct<D, NT>(recs, min(kChunk, n_ch - base), kb_s[p], sm.qsm_s, sm.G, sm.GS, lane, acc[p]);
+      cb2_k_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), kb_s[p], sm.qsm_s, sm.G, sm.GS, lane, acc[p]);
       __syncwarp();
     }
   }
@@ -616,11 +696,12 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
   softmax_frags<D, NT, PPI>(st, acc, ntok, a.scale_log2, sm, lane, Fmt<FMT>::kOutliers, phi, plo);
   v_wait();
 
-  uint32_t vc[PPI][NS / 2];
+  uint32_t vc[PPI][NS / 2], vy[PPI][A3 ? NS / 4 : 1];
   float sv[PPI];
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
-    load_codes<D>(vb_s[p], lane, vc[p]);
+    if constexpr (A3) load_a3_words<D>(vb_s[p], lane, vc[p], vy[p]);
+    else load_codes<D>(vb_s[p], lane, vc[p]);
     sv[p] = (T && tier[p]) ? ldsf(vb_s[p] + fp8_sc_off(D)) : 1.f;
   }
 #pragma unroll
@@ -639,7 +720,8 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
           for (int r = 0; r < 4; ++r) st.o[nt][s][r] = fmaf(sv[p], t4[r], st.o[nt][s][r]);
         }
       } else {
-        cb2_v_frag(vb_s[p] + cb2_cb_off(D) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
+        if constexpr (A3) a3_v_frag<D>(vb_s[p], vc[p], vy[p], s, g, av);
+        else cb2_v_frag(vb_s[p] + cb2_cb_off(D) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
@@ -654,16 +736,15 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
     if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
-    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + cb2_out_off(D)), D);
+    const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + SIDE), D);
 #pragma unroll 1
     for (int base = 0; base < n_ch; base += kChunk) {
-      uint32_t recs = vb_s[p] + cb2_out_off(D) + 4;
+      uint32_t recs = vb_s[p] + SIDE + 4;
       if (base > 0) {
-        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + cb2_out_off(D), base, min(kChunk, n_ch - base),
-                   sm.bounce_s, lane);
+        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
         recs = sm.bounce_s;
       }
-      cb2_v_correct<D, NT>(recs, min(kChunk, n_ch - base), vb_s[p], phi[p], plo[p], sm.corr_s, sm.G, sm.GS, lane);
+      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), vb_s[p], phi[p], plo[p], sm.corr_s, sm.G, sm.GS, lane);
       __syncwarp();
     }
   }
@@ -1194,7 +1275,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
       v_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[vs], (it / NV) & 1, kWaitLimitNs));
       v_waited += v_ok;
     };
-    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s) {
+    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s || F::kMain == kBlkA3) {
       iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
     } else if constexpr (F::kMain == kBlkE2m1) {
       iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane, k_done, v_wait);
@@ -1362,5 +1443,6 @@ KernelInfo decode_kernel_e2m1(int D, int G);
 KernelInfo decode_kernel_cb2(int D, int G);
 KernelInfo decode_kernel_tiered(int D, int G);
 KernelInfo decode_kernel_cb2s(int D, int G);
+KernelInfo decode_kernel_a3(int D, int G);
 
 }  // namespace kvq

@@ -290,6 +290,32 @@ __device__ __forceinline__ void pack_cb2_codes(const uint8_t (&codes)[16][D], ui
   }
 }
 
+// 3-bit codes [16][D] -> the block's two ASYM3 code planes (include/kvq.h):
+// one thread per (lane, 4-step group) builds one high-bit word and two
+// low-bit words.
+template <int D>
+__device__ __forceinline__ void pack_a3_codes(const uint8_t (&codes)[16][D], uint8_t* blk, int role, int tid) {
+  constexpr int NS = D / 16, NG = NS / 4;
+  for (int i = tid; i < 32 * NG; i += blockDim.x) {
+    const int ln = i / NG, grp = i % NG;
+    uint32_t lo[2] = {0u, 0u}, hi = 0u;
+    for (int ss = 0; ss < 4; ++ss) {
+      const int s = 4 * grp + ss;
+      for (int k = 0; k < 8; ++k) {
+        int t, c;
+        frag_inverse(role, ln, s, k, t, c);
+        const uint32_t q = codes[t][c];
+        lo[ss >> 1] |= (q & 3u) << (8 * (s % 2) + 16 * (k % 2) + 2 * (k / 2));
+        hi |= ((q >> 2) & 1u) << (4 * (s % 4) + 16 * (k % 2) + k / 2);
+      }
+    }
+    uint32_t* xw = reinterpret_cast<uint32_t*>(blk) + ln * (NS / 2) + 2 * grp;
+    xw[0] = lo[0];
+    xw[1] = lo[1];
+    reinterpret_cast<uint32_t*>(blk + a3_hi_off(D))[ln * NG + grp] = hi;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
   constexpr int NS = D / 16;
@@ -310,7 +336,9 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
   const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
   const bool tier = (u >> 31) != 0;
   const bool stat = a.fmt == KVQ_FMT_CB2_STATIC;
-  const int stride = tier ? kFp8 : stat ? block_stride(kBlkCb2s, D) : kCb2;
+  const int stride = tier ? kFp8
+                   : stat ? block_stride(kBlkCb2s, D)
+                   : a.fmt == KVQ_FMT_ASYM3_OUTLIER ? block_stride(kBlkA3, D) : kCb2;
   uint8_t* gblk = (tier ? a.tier_pool : a.pool) + (((size_t)phys * a.Hkv + h) * 2 + role) * stride;
   const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
 
@@ -370,9 +398,38 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
     __syncthreads();
     pack_cb2_codes<D>(codes, blk, role, tid);
   } else {
+    // CB2 or ASYM3: per-token outliers, then per channel a codebook (CB2) or an
+    // 8-level affine grid (ASYM3) over the non-outliers
+    const bool a3 = a.fmt == KVQ_FMT_ASYM3_OUTLIER;
     if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
     __syncthreads();
-    if (tid < D) {
+    if (tid < D && a3) {
+      const int c = tid;
+      bool have = false;
+      float mn = 0.f, mx = 0.f;
+      for (int t = 0; t < 16; ++t) {
+        if (mask[t][c]) continue;
+        const float v = xs[t][c];
+        if (!have || v < mn) mn = v;
+        if (!have || v > mx) mx = v;
+        have = true;
+      }
+      const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 7.0f)) : 0;
+      const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
+      const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
+      for (int t = 0; t < 16; ++t) {
+        uint8_t q = 0;
+        if (!mask[t][c] && S != 0.f) {
+          float r = rintf(__fdiv_rn(xs[t][c] - m, S));
+          r = fminf(fmaxf(r, 0.f), 7.f);
+          q = (uint8_t)r;
+        }
+        codes[t][c] = q;
+      }
+      const int r = a3_rho(role, c);
+      *reinterpret_cast<uint16_t*>(blk + a3_s_off(D) + 2 * r) = S16;
+      *reinterpret_cast<uint16_t*>(blk + a3_m_off(D) + 2 * r) = m16;
+    } else if (tid < D) {
       const int c = tid;
       float v[16];
       uint8_t cc[16];
@@ -409,7 +466,7 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         if (lane >= d) { ich += a1; ival += a2; }
       }
       const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
-      uint8_t* hdr = blk + cb2_out_off(D);
+      uint8_t* hdr = blk + (a3 ? a3_out_off(D) : cb2_out_off(D));
       int ci = ich - nch;
       for (int k = 0; k < CPL; ++k) {
         if (!tm[k]) continue;
@@ -430,7 +487,8 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
       }
     }
     __syncthreads();
-    pack_cb2_codes<D>(codes, blk, role, tid);
+    if (a3) pack_a3_codes<D>(codes, blk, role, tid);
+    else pack_cb2_codes<D>(codes, blk, role, tid);
   }
   __syncthreads();
   for (int i = tid; i < stride / 16; i += blockDim.x)
