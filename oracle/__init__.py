@@ -24,8 +24,9 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S, FMT_A3 = 0, 1, 2, 3, 4, 5
-BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8, BLK_CB2S, BLK_A3 = 0, 1, 2, 3, 4, 5
+FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S, FMT_A3, FMT_CB2G = 0, 1, 2, 3, 4, 5, 6
+BLK_INT4, BLK_E2M1, BLK_CB2, BLK_FP8, BLK_CB2S, BLK_A3, BLK_CB2G = 0, 1, 2, 3, 4, 5, 6
+GROUP_PAGES = 4   # pages per CB2 group codebook
 TIER_BIT = 1 << 31
 
 
@@ -68,6 +69,8 @@ def lib():
                 "or_quantize_page": (None, [I, I, D_, I, I, P, P]),
                 "or_quantize_page_static": (None, [I, I, I, P, P, I, P]),
                 "or_select_static": (None, [P, I, I, I, I, P]),
+                "or_quantize_group": (None, [I, D_, I, I, P, P]),
+                "or_dequantize_group_page": (None, [I, P, P, I, I, P]),
                 "or_dequantize_block": (None, [I, I, P, I, I, P]),
                 "or_append": (I, [P, P, P, P, P, P, P, P, I, P]),
                 "or_dequantize_range": (None, [P, P, P, P, P, P, I, I, I, I, I, P]),
@@ -155,6 +158,22 @@ def select_static(x, n_s: int) -> np.ndarray:
     return out
 
 
+def quantize_group(D: int, x, role: int = 0, sigma: float = 3.0, iters: int = 16) -> np.ndarray:
+    """CB2 group of 4 pages from x [64, D] -> uint8 [4, stride] (codebook in block 0)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(64, D)
+    blks = np.zeros((4, block_stride(BLK_CB2G, D)), np.uint8)
+    lib().or_quantize_group(D, sigma, iters, role, _p(x), _p(blks))
+    return blks
+
+
+def dequantize_group_page(D: int, codes_blk: np.ndarray, codebook_blk: np.ndarray, role: int = 0,
+                          ntok: int = 16) -> np.ndarray:
+    out = np.zeros((16, D), np.float32)
+    lib().or_dequantize_group_page(D, _p(np.ascontiguousarray(codes_blk)), _p(np.ascontiguousarray(codebook_blk)),
+                                   role, ntok, _p(out))
+    return out[:ntok]
+
+
 def dequantize_block(blk_fmt: int, D: int, blk: np.ndarray, role: int = 0, ntok: int = 16) -> np.ndarray:
     out = np.zeros((16, D), np.float32)
     lib().or_dequantize_block(blk_fmt, D, _p(np.ascontiguousarray(blk)), role, ntok, _p(out))
@@ -194,7 +213,8 @@ class OracleCache:
             page_table = np.arange(num_seqs * pages_per_seq_max, dtype=np.int64).reshape(num_seqs, -1) % max(num_pages, 1)
         self.page_table = np.ascontiguousarray(page_table.astype(np.uint32).view(np.int32))
         self.seq_lens = np.zeros(num_seqs, np.int32)
-        self.staging = np.zeros((num_seqs, num_kv_heads, 2, 16, head_dim), np.float32)
+        rows = 16 * GROUP_PAGES if fmt == FMT_CB2G else 16
+        self.staging = np.zeros((num_seqs, num_kv_heads, 2, rows, head_dim), np.float32)
 
     def _args(self):
         return (ctypes.byref(self.cfg), _p(self.pool), _p(self.tier_pool), _p(self.page_table))

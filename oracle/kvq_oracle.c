@@ -317,6 +317,11 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /*                               4*((c%8)/2) + 2*((c%16)/8) + c%2, V: rho(c)  */
 /*                               = 16*(c/16) + 2*(c%8) + (c%16)/8             */
 /*            outliers at 10D    as CB2's side-list (records at 10D + 4 + 20i)*/
+/*  CB2 group codebook [0, 8D)   as CB2's codebook, fitted over a group of 4  */
+/*  (f1)                         pages (64 tokens); only the group's first    */
+/*                               page holds it (zeros in the other three)     */
+/*            codes  [8D, 12D)   as CB2's codes                               */
+/*            outliers at 12D    as CB2's side-list (per page)                */
 /*  FP8 tier  codes  [0, 16D)    lane-major, 8*NS B/lane, step s at 8s,       */
 /*                               slot k = byte k (e4m3)                       */
 /*            scale at 16D       fp32                                         */
@@ -324,7 +329,8 @@ EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c
 /* Page Sizes with Memory Bus Lines").                                        */
 /* ------------------------------------------------------------------------- */
 
-enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3, OR_CB2S = 4, OR_A3 = 5 };
+enum { OR_INT4 = 0, OR_E2M1 = 1, OR_CB2 = 2, OR_FP8 = 3, OR_CB2S = 4, OR_A3 = 5, OR_CB2G = 6 };
+enum { OR_GROUP = 4 };   /* pages per CB2 group codebook */
 enum { OR_MAX_STATIC = 8 };
 
 static int round128(int x) { return (x + 127) / 128 * 128; }
@@ -339,6 +345,7 @@ EXPORT int or_block_stride(int fmt, int D)
     case OR_FP8:  return round128(16 * D + 16);
     case OR_CB2S: return round128(12 * D + 16 + 32 * OR_MAX_STATIC);
     case OR_A3:   return round128(10 * D + 4 + 20 * D);
+    case OR_CB2G: return round128(12 * D + 4 + 20 * D);
     }
     return -1;
 }
@@ -429,6 +436,37 @@ static uint8_t a3_code_get(const uint8_t* blk, int D, int role, int t, int c)
     memcpy(&vy, blk + 4 * D + 4 * (lane * (NS / 4) + s / 4), 4);
     int bx = 8 * (s % 2) + 16 * (k % 2) + 2 * (k / 2), by = 4 * (s % 4) + 16 * (k % 2) + k / 2;
     return (uint8_t)(((vx >> bx) & 3u) | (((vy >> by) & 1u) << 2));
+}
+
+static int cb2_slot(int role, int c);
+/* CB2 codes / centroids relative to explicit section bases (CB2 group pages). */
+static void code2_set(uint8_t* codes, int D, int role, int t, int c, uint8_t code)
+{
+    int lane, s, k;
+    or_frag_pos(role, t, c, &lane, &s, &k);
+    uint8_t* w = codes + 2 * (D / 16) * lane + 2 * s;
+    uint16_t v = get_u16(w);
+    int bit = 4 * (k % 4) + 2 * (k / 4);
+    v = (uint16_t)((v & ~(3u << bit)) | ((unsigned)(code & 3) << bit));
+    put_u16(w, v);
+}
+static uint8_t code2_get(const uint8_t* codes, int D, int role, int t, int c)
+{
+    int lane, s, k;
+    or_frag_pos(role, t, c, &lane, &s, &k);
+    uint16_t v = get_u16(codes + 2 * (D / 16) * lane + 2 * s);
+    return (uint8_t)((v >> (4 * (k % 4) + 2 * (k / 4))) & 3u);
+}
+static void cent_set(uint8_t* cb, int role, int c, int j, uint16_t h)
+{
+    uint8_t* p = cb + 8 * cb2_slot(role, c);
+    p[j] = (uint8_t)(h & 0xFF);
+    p[4 + j] = (uint8_t)(h >> 8);
+}
+static uint16_t cent_get(const uint8_t* cb, int role, int c, int j)
+{
+    const uint8_t* p = cb + 8 * cb2_slot(role, c);
+    return (uint16_t)(p[j] | (p[4 + j] << 8));
 }
 
 static int cb2_slot(int role, int c)
@@ -638,6 +676,60 @@ static void quantize_page_a3(const float* x, int D, double sigma, int role, uint
     write_side_list(x, D, mask, blk + 10 * D);
 }
 
+/* CB2 with a codebook per group of 4 pages ([P1] "2. Centroid Vector          */
+/* Quantization for Residuals": k-means "per head-group block").  Outliers as */
+/* CB2, per token; per channel, Lloyd-Max (as CB2) over the non-outliers of   */
+/* all 64 tokens of the group, in token order; codes of every page from that  */
+/* one codebook (0 at outliers); the side-list per page.  x: float [64][D];   */
+/* blk[p] receives page p of the group.                                       */
+static void quantize_group_cb2g(const float* x, int D, double sigma, int iters, int role, uint8_t* const blk[4])
+{
+    int n_tok = 16 * OR_GROUP;
+    for (int p = 0; p < OR_GROUP; ++p) memset(blk[p], 0, (size_t)or_block_stride(OR_CB2G, D));
+    uint8_t mask[64][128];
+    int kmax = or_kmax(D);
+    for (int t = 0; t < n_tok; ++t) or_outlier_mask(x + t * D, D, sigma, kmax, mask[t]);
+    for (int c = 0; c < D; ++c) {
+        float v[64];
+        uint8_t codes[64];
+        uint16_t c16[4];
+        int n = 0;
+        for (int t = 0; t < n_tok; ++t)
+            if (!mask[t][c]) v[n++] = x[t * D + c];
+        or_lloyd4(v, n, iters, NULL, c16, codes);
+        for (int j = 0; j < 4; ++j) cent_set(blk[0], role, c, j, c16[j]);
+        n = 0;
+        for (int t = 0; t < n_tok; ++t)
+            code2_set(blk[t / 16] + 8 * D, D, role, t % 16, c, mask[t][c] ? 0 : codes[n++]);
+    }
+    for (int p = 0; p < OR_GROUP; ++p) write_side_list(x + (size_t)16 * p * D, D, &mask[16 * p], blk[p] + 12 * D);
+}
+
+/* Dequantize page `codes_blk` of a CB2 group whose codebook lives in `cb_blk`. */
+EXPORT void or_dequantize_group_page(int D, const uint8_t* codes_blk, const uint8_t* cb_blk, int role, int ntok,
+                                     float* out)
+{
+    for (int t = 0; t < ntok; ++t)
+        for (int c = 0; c < D; ++c)
+            out[t * D + c] = (float)or_fp16_decode(cent_get(cb_blk, role, c, code2_get(codes_blk + 8 * D, D, role, t, c)));
+    const uint8_t* hdr = codes_blk + 12 * D;
+    int n_ch = hdr[0];
+    for (int i = 0; i < n_ch; ++i) {
+        const uint8_t* rec = hdr + 4 + 20 * i;
+        unsigned tmask = get_u16(rec + 2);
+        for (int t = 0; t < 16 && t < ntok; ++t)
+            if (tmask & (1u << t)) out[t * D + rec[0]] = (float)or_e4m3_decode(rec[4 + t]);
+    }
+}
+
+/* Single-group entry point for the pins: x float [64][D] -> 4 blocks. */
+EXPORT void or_quantize_group(int D, double sigma, int iters, int role, const float* x, uint8_t* blocks)
+{
+    size_t stride = (size_t)or_block_stride(OR_CB2G, D);
+    uint8_t* const blk[4] = {blocks, blocks + stride, blocks + 2 * stride, blocks + 3 * stride};
+    quantize_group_cb2g(x, D, sigma, iters, role, blk);
+}
+
 static void quantize_page_fp8(const float* x, int D, int role, uint8_t* blk)
 {
     memset(blk, 0, (size_t)or_block_stride(OR_FP8, D));
@@ -792,14 +884,17 @@ EXPORT void or_quantize_page(int fmt, int D, double sigma, int iters, int role, 
 /* the page lives in the FP8 tier pool ([P2] "Dual-Tier Paged Compression    */
 /* Protocol").  Pool layout: block (phys, head, role) at                      */
 /* ((phys * Hkv + head) * 2 + role) * stride.                                 */
-/* Per-token formats quantize every token when it arrives.  Page formats keep */
+/* Per-token formats quantize every token when it arrives.  The CB2 group    */
+/* format keeps the partial last group in staging [B][Hkv][2][64][D] and      */
+/* quantizes a group when its 64th token arrives.  Page formats keep          */
 /* the partial last page in fp32 staging [B][Hkv][2][16][D] and quantize a    */
 /* page when its 16th token arrives (reading: the pages never discuss partial */
 /* pages; page statistics stay fixed once written).                           */
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier), 4 CB2 static, 5 ASYM3 */
+    int32_t fmt;            /* 0 INT4, 1 E2M1, 2 CB2, 3 TIERED (CB2 + FP8 tier), 4 CB2 static, 5 ASYM3,
+                               6 CB2 group (codebook per 4 pages) */
     int32_t B, Hkv, D, pages_per_seq_max, num_pages, num_tier_pages;
     int32_t iters;
     double sigma;
@@ -808,7 +903,13 @@ typedef struct {
 } or_cfg;
 
 static int page_fmt(const or_cfg* c) { return c->fmt == 3 ? OR_CB2 : c->fmt; }
-static int is_paged(const or_cfg* c) { return c->fmt == OR_CB2 || c->fmt == 3 || c->fmt == OR_CB2S || c->fmt == OR_A3; }
+static int is_paged(const or_cfg* c)
+{
+    return c->fmt == OR_CB2 || c->fmt == 3 || c->fmt == OR_CB2S || c->fmt == OR_A3 || c->fmt == OR_CB2G;
+}
+/* fp32 staging rows per (sequence, head, role): the partial page, or for the
+ * group format the partial group. */
+static int stg_rows(const or_cfg* c) { return c->fmt == OR_CB2G ? 16 * OR_GROUP : 16; }
 
 static int entry_ok(const or_cfg* c, int32_t e)
 {
@@ -830,7 +931,7 @@ static uint8_t* block_ptr(const or_cfg* c, uint8_t* pool, uint8_t* tier_pool, in
 
 static float* staging_row(const or_cfg* c, float* staging, int b, int h, int role, int t)
 {
-    return staging + ((((size_t)b * c->Hkv + h) * 2 + role) * 16 + t) * c->D;
+    return staging + ((((size_t)b * c->Hkv + h) * 2 + role) * stg_rows(c) + t) * c->D;
 }
 
 /* Append t_new tokens (or t_per_seq[b] <= t_new of them) to every sequence.
@@ -849,13 +950,38 @@ EXPORT int or_append(const or_cfg* c, uint8_t* pool, uint8_t* tier_pool, const i
         if (n <= 0) continue;
         if (end > c->pages_per_seq_max * 16 || n > t_new) { ++bad; continue; }
         int ok = 1;
-        for (int pg = start / 16; pg <= (end - 1) / 16; ++pg)
+        int first_pg = c->fmt == OR_CB2G ? (start / 64) * OR_GROUP : start / 16;   /* a group writes all its pages */
+        for (int pg = first_pg; pg <= (end - 1) / 16; ++pg)
             if (!entry_ok(c, page_table[(size_t)b * c->pages_per_seq_max + pg])) ok = 0;
         if (!ok) { ++bad; continue; }
         for (int h = 0; h < c->Hkv; ++h)
             for (int role = 0; role < 2; ++role) {
                 const float* in = src[role];
 #define IN_ROW(pos) (in + (((size_t)b * t_new + (size_t)((pos) - start)) * c->Hkv + h) * D)
+                if (c->fmt == OR_CB2G) {
+                    for (int gr = start / 64; gr <= (end - 1) / 64; ++gr) {
+                        int lo = start > gr * 64 ? start : gr * 64;
+                        int hi = end < gr * 64 + 64 ? end : gr * 64 + 64;
+                        if (hi == gr * 64 + 64) {   /* the group completes: quantize its 4 pages */
+                            float* x = (float*)malloc(sizeof(float) * 64 * D);
+                            for (int t = 0; t < 64; ++t) {
+                                int pos = gr * 64 + t;
+                                const float* r = pos < start ? staging_row(c, staging, b, h, role, t) : IN_ROW(pos);
+                                memcpy(x + t * D, r, sizeof(float) * D);
+                            }
+                            uint8_t* blks[4];
+                            for (int q = 0; q < OR_GROUP; ++q)
+                                blks[q] = block_ptr(c, pool, tier_pool,
+                                                    page_table[(size_t)b * c->pages_per_seq_max + gr * OR_GROUP + q], h, role);
+                            quantize_group_cb2g(x, D, c->sigma, c->iters, role, blks);
+                            free(x);
+                        } else {
+                            for (int pos = lo; pos < hi; ++pos)
+                                memcpy(staging_row(c, staging, b, h, role, pos % 64), IN_ROW(pos), sizeof(float) * D);
+                        }
+                    }
+                    continue;
+                }
                 for (int pg = start / 16; pg <= (end - 1) / 16; ++pg) {
                     int32_t e = page_table[(size_t)b * c->pages_per_seq_max + pg];
                     uint8_t* blk = block_ptr(c, pool, tier_pool, e, h, role);
@@ -900,7 +1026,17 @@ EXPORT void or_dequantize_range(const or_cfg* c, uint8_t* pool, uint8_t* tier_po
     float* tmp = (float*)malloc(sizeof(float) * 16 * D);
     for (int pg = t0 / 16; t1 > t0 && pg <= (t1 - 1) / 16; ++pg) {
         int full = (pg + 1) * 16 <= len;
-        if (paged && !full) {
+        if (c->fmt == OR_CB2G) {
+            int gr = pg / OR_GROUP;
+            if ((gr + 1) * 64 <= len) {   /* quantized group: the codebook lives in its first page */
+                const int32_t* row = page_table + (size_t)b * c->pages_per_seq_max;
+                or_dequantize_group_page(D, block_ptr(c, pool, tier_pool, row[pg], h, role),
+                                         block_ptr(c, pool, tier_pool, row[gr * OR_GROUP], h, role), role, 16, tmp);
+            } else {
+                for (int t = 0; t < 16; ++t)
+                    memcpy(tmp + t * D, staging_row(c, staging, b, h, role, (pg % OR_GROUP) * 16 + t), sizeof(float) * D);
+            }
+        } else if (paged && !full) {
             for (int t = 0; t < 16; ++t) memcpy(tmp + t * D, staging_row(c, staging, b, h, role, t), sizeof(float) * D);
         } else {
             int32_t e = page_table[(size_t)b * c->pages_per_seq_max + pg];

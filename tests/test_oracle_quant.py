@@ -421,3 +421,60 @@ def test_a3_cache_chunking_independent():
         b.append(x[0][:, t0:t1], x[1][:, t0:t1])
     assert (a.pool == b.pool).all() and (a.staging[:, :, :, :2] == b.staging[:, :, :, :2]).all()
     assert (a.dequantize(0, 1, 1, 0, 50) == b.dequantize(0, 1, 1, 0, 50)).all()
+
+
+# ----------------------------------------------------------------------------- CB2 with a codebook per group of 4 pages
+def test_cb2_group_matches_the_recipe():
+    """One codebook per (group of 4 pages, channel), fitted like CB2's over the
+    non-outliers of all 64 tokens ("Hierarchical Token Routing and Sub-2-Bit
+    Non-Linear KV Compression", 2. Centroid Vector Quantization for Residuals:
+    k-means per head-group block).  It lives in the group's first page; every
+    page's side-list is the CB2 side-list of its own 16 tokens."""
+    rng = np.random.default_rng(31)
+    for trial in range(4):
+        D = (64, 128)[trial % 2]
+        role = trial // 2
+        x = rng.standard_normal((64, D)).astype(np.float32)
+        x[:, rng.choice(D, 4, replace=False)] *= 8
+        blks = oracle.quantize_group(D, x, role=role)
+        masks = np.array([oracle.outlier_mask(x[t])[0] for t in range(64)])
+        assert not blks[1:, :8 * D].any()
+        for p in range(4):
+            page = oracle.quantize_page(oracle.BLK_CB2, D, x[16 * p:16 * p + 16], role=role)
+            assert (blks[p, 12 * D:] == page[12 * D:]).all()
+        xh = np.concatenate([oracle.dequantize_group_page(D, blks[p], blks[0], role=role) for p in range(4)])
+        for c in range(D):
+            keep = ~masks[:, c]
+            _, c16, _, _ = oracle.lloyd4(x[keep, c].astype(np.float64))
+            cf = np.array([oracle.fp16_decode(h) for h in c16])
+            for t in range(64):
+                if masks[t, c]:
+                    assert xh[t, c] == oracle.e4m3_decode(oracle.e4m3_encode(float(x[t, c])))
+                else:
+                    assert xh[t, c] in cf
+                    assert abs(float(xh[t, c]) - float(x[t, c])) <= np.abs(cf - float(x[t, c])).min()
+
+
+def test_cb2_group_cache_chunking_and_staging():
+    """A group is quantized when its 64th token arrives, from fp32 staging;
+    before that dequantize returns the staged values exactly."""
+    rng = np.random.default_rng(32)
+    B, Hkv, D, P = 2, 2, 64, 12
+    x = rng.standard_normal((2, B, 150, Hkv, D)).astype(np.float32)
+    x[..., 5] *= 8
+    a = oracle.OracleCache(oracle.FMT_CB2G, B, Hkv, D, P, B * P)
+    b = oracle.OracleCache(oracle.FMT_CB2G, B, Hkv, D, P, B * P)
+    a.append(x[0], x[1])
+    for t0, t1 in ((0, 30), (30, 64), (64, 65), (65, 140), (140, 150)):
+        b.append(x[0][:, t0:t1], x[1][:, t0:t1])
+    assert (a.pool == b.pool).all()
+    assert (a.staging[:, :, :, :150 - 128] == b.staging[:, :, :, :150 - 128]).all()
+    for role in (0, 1):
+        got = a.dequantize(1, 0, role, 0, 150)
+        assert (got[128:] == x[role][1, 128:150, 0]).all()          # the partial group, from staging
+        blk = a.pool.reshape(-1, a.stride)
+        pt = a.page_table.view(np.uint32)
+        cb = blk[(pt[1, 4] * Hkv + 0) * 2 + role]
+        for p in range(4, 8):                                        # the second group, from blocks
+            page = blk[(pt[1, p] * Hkv + 0) * 2 + role]
+            assert (got[16 * p:16 * p + 16] == oracle.dequantize_group_page(D, page, cb, role=role)).all()
