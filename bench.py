@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 from sub_byte_quantized_kvq_gb300 import kvq, synth, workloads  # noqa: E402
 
 METRIC = "quantized-KV decode attention: achieved HBM GB/s vs peak; us per decode step"
-FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC", 5: "ASYM3_OUTLIER"}
+FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC", 5: "ASYM3_OUTLIER",
+            6: "CB2_GROUP4"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 KERNEL_SOURCES = ["kvq_common.cuh", "kvq_decode.cuh", "kvq_internal.cuh"]
 
@@ -107,6 +108,14 @@ def algorithmic_bytes(built: workloads.Built) -> dict:
         n_main = full * blocks - n_tier
         cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
         tail = (L % 16) * D * 4 * blocks
+    elif w.fmt == synth.FMT_CB2G:
+        # per group: one codebook (8D); per page: codes (4D) + side-list; the partial group in fp32
+        pool = cache.pool.view(-1, cache.block_bytes(0))
+        nch = pool[:, 12 * D].to(torch.int64)
+        groups = L // 64
+        unq = pool.shape[0] - groups * 4 * w.B * w.Hkv * 2     # blocks no complete group wrote
+        cache_bytes = groups * blocks * (8 * D + 4 * 4 * D) + (4 + 20 * nch).sum().item() - 4 * unq
+        tail = (L - 64 * groups) * D * 4 * blocks
     elif w.fmt == synth.FMT_A3:
         # codes (6D) + S and m (4D) + side-list header and records
         pool = cache.pool.view(-1, cache.block_bytes(0))
@@ -307,6 +316,12 @@ def oracle_sample(w: synth.Workload, seed: int):
         cache += (N % 16) * D * 4 * w.Hkv * 2
     elif w.fmt == synth.FMT_CB2S:
         cache = full * w.Hkv * 2 * (12 * D + 16 + 32 * w.static_channels) + (N % 16) * D * 4 * w.Hkv * 2
+    elif w.fmt == synth.FMT_CB2G:
+        nch = ref.pool.reshape(-1, ref.stride)[:, 12 * D].astype(np.int64)
+        groups = N // 64
+        unq = nch.shape[0] - groups * 4 * w.Hkv * 2
+        cache = groups * w.Hkv * 2 * (8 * D + 16 * D) + int((4 + 20 * nch).sum()) - 4 * unq
+        cache += (N - 64 * groups) * D * 4 * w.Hkv * 2
     elif w.fmt == synth.FMT_A3:
         nch = ref.pool.reshape(-1, ref.stride)[:, 10 * D].astype(np.int64)
         cache = full * w.Hkv * 2 * 10 * D + int((4 + 20 * nch).sum()) + (N % 16) * D * 4 * w.Hkv * 2

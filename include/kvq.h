@@ -95,7 +95,15 @@ typedef enum {
      * fp16(q*S + m).  Outliers as KVQ_FMT_CB2_OUTLIER (sigma rule per token,
      * e4m3 side-list).  Quantized when a page fills; the partial last page
      * waits in fp32 staging. */
-    KVQ_FMT_ASYM3_OUTLIER = 5
+    KVQ_FMT_ASYM3_OUTLIER = 5,
+    /* [P1] "2. Centroid Vector Quantization for Residuals" (k-means "per
+     * head-group block"): as KVQ_FMT_CB2_OUTLIER, but each channel's
+     * 4-centroid codebook is fitted over a group of 4 consecutive pages (64
+     * tokens) of one (sequence, kv head, K|V) and stored once, in the group's
+     * first page; outliers and side-lists stay per page.  Quantized when a
+     * group fills; the partial last group (up to 63 tokens) waits in fp32
+     * staging [num_seqs][Hkv][2][64][D]. */
+    KVQ_FMT_CB2_GROUP4 = 6
 } kvq_format;
 
 typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
@@ -132,8 +140,9 @@ typedef struct {
  *               logical page; bit 31 selects the tier pool (TIERED only).
  *               Entries are read only for pages a call touches.
  *   seq_lens    int32 [num_seqs]: tokens cached per sequence; appends advance it.
- *   staging     fp32 [num_seqs][Hkv][2][16][D]: partial last page of the CB2 and
- *               TIERED formats (NULL for INT4 / E2M1).
+ *   staging     fp32 [num_seqs][Hkv][2][16][D]: partial last page of the page
+ *               formats (CB2, TIERED, CB2_STATIC, ASYM3); [num_seqs][Hkv][2][64][D]
+ *               (partial last group) for CB2_GROUP4; NULL for INT4 / E2M1.
  *   status      one uint32 word, OR-ed with KVQ_STATUS_* bits; the caller clears it.
  *   static_mask uint8 [Hkv][2][static_channels] (CB2_STATIC only, else NULL):
  *               the static channels of each (kv head, K|V), ascending, distinct,
@@ -328,6 +337,11 @@ const char* kvq_version(void);
  *                       2*(c%8) + (c%16)/8
  *             10D       outlier side-list as CB2's (records at 10D + 4 + 20*i)
  *             stride 2048 (D=64), 3968 (D=128)
+ *   CB2_GROUP4 [0, 8D)  the group's codebook, as CB2's (first page of a group; zeros
+ *                       in the other three)
+ *             8D        codes as CB2's
+ *             12D       outlier side-list as CB2's (per page)
+ *             stride 2176 (D=64), 4224 (D=128)
  *   FP8 tier  [0, 16D)  codes: lane l at 8*NS*l, step s at +8s, slot k = byte k (e4m3)
  *             16D       fp32 scale
  *             stride 1152 (D=64), 2176 (D=128)

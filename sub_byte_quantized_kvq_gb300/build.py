@@ -22,7 +22,7 @@ COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relax
 PER_TU = {"kvq_quantize.cu": ["--fmad=false"]}
 TUS = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu", "kvq_decode_int4.cu", "kvq_decode_e2m1.cu",
        "kvq_decode_cb2.cu", "kvq_decode_tiered.cu", "kvq_decode_cb2s.cu",
-       "kvq_decode_a3.cu", "kvq_noalloc.cu"]
+       "kvq_decode_a3.cu", "kvq_decode_cb2g.cu", "kvq_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -52,13 +52,34 @@ __global__ void dequantize_kernel(const DequantArgs a) {
   const int pos = a.t0 + (int)(idx / D), c = (int)(idx % D);
   const int t = pos % kPage, pg = pos / kPage;
   const int L = a.seq_lens[a.seq];
+  const bool group = a.fmt == KVQ_FMT_CB2_GROUP4;
   const bool paged = a.fmt == KVQ_FMT_CB2_OUTLIER || a.fmt == KVQ_FMT_TIERED || a.fmt == KVQ_FMT_CB2_STATIC ||
-                     a.fmt == KVQ_FMT_ASYM3_OUTLIER;
+                     a.fmt == KVQ_FMT_ASYM3_OUTLIER || group;
+  // tokens not yet in a block: the partial last page, or for the group format the partial last group
+  const int unit = group ? kPage * kGroupPages : kPage;
   float v = 0.f;
   if (pos >= L || pg >= a.ppsm) {
     v = 0.f;
-  } else if (paged && (pg + 1) * kPage > L) {
-    v = a.staging[((((size_t)a.seq * a.Hkv + a.head) * 2 + a.role) * kPage + t) * D + c];
+  } else if (paged && (pos / unit + 1) * unit > L) {
+    v = a.staging[((((size_t)a.seq * a.Hkv + a.head) * 2 + a.role) * unit + pos % unit) * D + c];
+  } else if (group) {
+    // codes of this page, codebook of the group's first page
+    const int32_t* row = a.page_table + (size_t)a.seq * a.ppsm;
+    const uint32_t u = (uint32_t)row[pg], u0 = (uint32_t)row[(pg / kGroupPages) * kGroupPages];
+    if ((u >> 31) || (u0 >> 31) || u >= (uint32_t)a.num_pages || u0 >= (uint32_t)a.num_pages) {
+      atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+      a.out[idx] = 0.f;
+      return;
+    }
+    const size_t stride = (size_t)block_stride(kBlkCb2g, D);
+    const uint8_t* blk = a.pool + (((size_t)u * a.Hkv + a.head) * 2 + a.role) * stride;
+    const uint8_t* cbk = a.pool + (((size_t)u0 * a.Hkv + a.head) * 2 + a.role) * stride;
+    const FragPos p = frag_pos(a.role, t, c);
+    const uint8_t* cw = blk + cb2g_code_off(D) + 2 * NS * p.lane + 2 * p.step;
+    const uint32_t q = ((cw[0] | (cw[1] << 8)) >> (4 * (p.slot & 3) + 2 * (p.slot >> 2))) & 3u;
+    const uint8_t* cb = cbk + 8 * cb2_slot(a.role, c);
+    v = dq_f16(cb[q] | (cb[4 + q] << 8));
+    v = side_list_value(blk + cb2_out_off(D), D, t, c, v);
   } else {
     const uint32_t u = (uint32_t)a.page_table[(size_t)a.seq * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
     const bool tier = (u >> 31) != 0;
@@ -155,7 +176,7 @@ cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int
 static bool cfg_ok(const kvq_config* c) {
   if (!c) return false;
   if (c->num_seqs <= 0 || c->num_kv_heads <= 0 || c->pages_per_seq_max <= 0 || c->num_pages <= 0) return false;
-  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_ASYM3_OUTLIER) return false;
+  if (c->format < KVQ_FMT_INT4_G32 || c->format > KVQ_FMT_CB2_GROUP4) return false;
   if (c->format == KVQ_FMT_CB2_STATIC && (c->static_channels < 1 || c->static_channels > kMaxStatic)) return false;
   if (c->num_tier_pages < 0 || (c->format != KVQ_FMT_TIERED && c->num_tier_pages != 0)) return false;
   if (!(c->sigma >= 3.0) || !std::isfinite(c->sigma)) return false;
@@ -165,7 +186,8 @@ static bool cfg_ok(const kvq_config* c) {
 }
 static bool dim_supported(const kvq_config* c) { return c->head_dim == 64 || c->head_dim == 128; }
 static bool paged_format(int f) {
-  return f == KVQ_FMT_CB2_OUTLIER || f == KVQ_FMT_TIERED || f == KVQ_FMT_CB2_STATIC || f == KVQ_FMT_ASYM3_OUTLIER;
+  return f == KVQ_FMT_CB2_OUTLIER || f == KVQ_FMT_TIERED || f == KVQ_FMT_CB2_STATIC || f == KVQ_FMT_ASYM3_OUTLIER ||
+         f == KVQ_FMT_CB2_GROUP4;
 }
 static bool cache_ok(const kvq_config* c, const kvq_cache* k) {
   if (!k || !k->pool || !k->page_table || !k->seq_lens || !k->status) return false;
@@ -236,7 +258,8 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* ti
   const size_t per_page = (size_t)cfg->num_kv_heads * 2;
   *pool_bytes = (size_t)cfg->num_pages * per_page * block_stride(main_blk(cfg), cfg->head_dim);
   *tier_pool_bytes = (size_t)cfg->num_tier_pages * per_page * block_stride(kBlkFp8, cfg->head_dim);
-  *staging_bytes = paged_format(cfg->format) ? (size_t)cfg->num_seqs * cfg->num_kv_heads * 2 * kPage * cfg->head_dim * sizeof(float) : 0;
+  const int rows = cfg->format == KVQ_FMT_CB2_GROUP4 ? kPage * kGroupPages : kPage;
+  *staging_bytes = paged_format(cfg->format) ? (size_t)cfg->num_seqs * cfg->num_kv_heads * 2 * rows * cfg->head_dim * sizeof(float) : 0;
   return KVQ_OK;
 }
 
@@ -336,6 +359,7 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.num_tier_pages = cfg->num_tier_pages;
   a.S = S;
   a.pps = pages > 0 ? (pages + S - 1) / S : 1;
+  if (cfg->format == KVQ_FMT_CB2_GROUP4) a.pps = (a.pps + kGroupPages - 1) / kGroupPages * kGroupPages;   // whole groups
   a.max_seq_len = len;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = nullptr;

@@ -14,7 +14,8 @@ namespace kvq {
 constexpr int kPage = KVQ_PAGE_TOKENS;
 
 // Block formats (the pool format of a cache; FP8 is the tier-1 page format).
-enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3, kBlkCb2s = 4, kBlkA3 = 5 };
+enum BlkFmt : int { kBlkInt4 = 0, kBlkE2m1 = 1, kBlkCb2 = 2, kBlkFp8 = 3, kBlkCb2s = 4, kBlkA3 = 5, kBlkCb2g = 6 };
+constexpr int kGroupPages = 4;  // CB2_GROUP4: pages sharing one codebook
 constexpr int kMaxStatic = 8;   // CB2_STATIC: static fp16 channels per (kv head, K|V)
 
 // Largest number of values of an n-vector that can lie more than 3 standard
@@ -38,6 +39,7 @@ __host__ __device__ constexpr int a3_hi_off(int D) { return 4 * D; }          //
 __host__ __device__ constexpr int a3_s_off(int D) { return 6 * D; }           // fp16 S by rho(c)
 __host__ __device__ constexpr int a3_m_off(int D) { return 8 * D; }           // fp16 m by rho(c)
 __host__ __device__ constexpr int a3_out_off(int D) { return 10 * D; }        // outlier side-list
+__host__ __device__ constexpr int cb2g_code_off(int D) { return 8 * D; }      // codes (codebook at 0)
 // ASYM3 position of channel c's S / m (K: 4 channels of a lane-step adjacent; V: 2).
 __host__ __device__ inline int a3_rho(int role, int c) {
   return role == 0 ? 16 * (c / 16) + 4 * ((c % 8) / 2) + 2 * ((c % 16) / 8) + c % 2
@@ -50,6 +52,7 @@ __host__ __device__ constexpr int block_stride(int fmt, int D) {
        : fmt == kBlkCb2  ? round_up128(12 * D + 4 + 20 * D)
        : fmt == kBlkCb2s ? round_up128(12 * D + 16 + 32 * kMaxStatic)
        : fmt == kBlkA3   ? round_up128(10 * D + 4 + 20 * D)
+       : fmt == kBlkCb2g ? round_up128(12 * D + 4 + 20 * D)
                          : round_up128(16 * D + 16);
 }
 

@@ -22,6 +22,7 @@ static KernelInfo pick_kernel(int fmt, int D, int G) {
     case KVQ_FMT_CB2_OUTLIER: return decode_kernel_cb2(D, G);
     case KVQ_FMT_CB2_STATIC: return decode_kernel_cb2s(D, G);
     case KVQ_FMT_ASYM3_OUTLIER: return decode_kernel_a3(D, G);
+    case KVQ_FMT_CB2_GROUP4: return decode_kernel_cb2g(D, G);
     default: return decode_kernel_tiered(D, G);
   }
 }

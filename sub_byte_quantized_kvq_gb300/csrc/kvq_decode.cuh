@@ -48,11 +48,14 @@ constexpr float kRescaleTh = 8.0f;    // lazy rescale: p stays <= 2^8
 template <int FMT>
 struct Fmt {
   static constexpr bool kPaged = (FMT == KVQ_FMT_CB2_OUTLIER || FMT == KVQ_FMT_TIERED || FMT == KVQ_FMT_CB2_STATIC ||
-                                  FMT == KVQ_FMT_ASYM3_OUTLIER);
+                                  FMT == KVQ_FMT_ASYM3_OUTLIER || FMT == KVQ_FMT_CB2_GROUP4);
   static constexpr int kMain = FMT == KVQ_FMT_TIERED ? kBlkCb2 : FMT;
-  static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2 || kMain == kBlkA3);
-  static constexpr bool kSideList = (kMain == kBlkCb2 || kMain == kBlkA3);   // 20-byte outlier records
-  static constexpr int kPPI = kMain == kBlkInt4 ? 1 : 2;   // pages per warp iteration
+  static constexpr bool kGroup = kMain == kBlkCb2g;   // 4 pages share the first page's codebook
+  static constexpr bool kOutliers = (kMain == kBlkInt4 || kMain == kBlkCb2 || kMain == kBlkA3 || kGroup);
+  static constexpr bool kSideList = (kMain == kBlkCb2 || kMain == kBlkA3 || kGroup);   // 20-byte outlier records
+  // pages per warp iteration (a whole group for the group format)
+  static constexpr int kPPI = kMain == kBlkInt4 ? 1 : kGroup ? kGroupPages : 2;
+  static constexpr int kUnit = kGroup ? kGroupPages : 1;   // pages per unit of the page-to-warp assignment
 };
 
 // Bytes copied to shared memory per block.
@@ -80,9 +83,31 @@ __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 // shallower V ring still hides the fetch and leaves room for more CTAs).
 template <int FMT>
 struct Ring {
-  static constexpr int kK = Fmt<FMT>::kPPI == 1 ? 3 : 2;
-  static constexpr int kV = Fmt<FMT>::kPPI == 1 ? 2 : Fmt<FMT>::kPaged ? 1 : 2;
+  static constexpr int kK = Fmt<FMT>::kGroup ? 1 : Fmt<FMT>::kPPI == 1 ? 3 : 2;
+  static constexpr int kV = Fmt<FMT>::kGroup ? 1 : Fmt<FMT>::kPPI == 1 ? 2 : Fmt<FMT>::kPaged ? 1 : 2;
 };
+
+// Bytes of one ring stage (the blocks of one iteration, one role).  The group
+// format stages [codebook 8D][page 0 codes + side-list prefix]...[page 3 ...],
+// page j at 8D + j * (4D + kOutPrefetch).
+template <int FMT, int D>
+__host__ __device__ constexpr int group_page_bytes() { return 4 * D + kOutPrefetch; }
+// Offsets of page j within a stage (its virtual block base), of its copy's
+// destination, and of the copied bytes within its block.  The group format
+// copies page 0 whole (codebook, codes, side-list prefix) and pages 1..3
+// from their codes on; a page's virtual base puts its codes at 8D and its
+// side-list at 12D, as in its block.
+template <int FMT, int D>
+__host__ __device__ constexpr int page_base(int j);
+template <int FMT, int D>
+__host__ __device__ constexpr int copy_dst(int j);
+template <int FMT, int D>
+__host__ __device__ constexpr int copy_src(int j) { return Fmt<FMT>::kGroup && j > 0 ? 8 * D : 0; }
+template <int FMT, int D>
+__host__ __device__ constexpr int stage_bytes() {
+  return Fmt<FMT>::kGroup ? 8 * D + kGroupPages * group_page_bytes<FMT, D>()
+                          : Fmt<FMT>::kPPI * half_slot_bytes<FMT, D>();
+}
 
 // Shared-memory plan: [mbarriers: W x (kK + kV)][qsm: D x GS fp32][zero block, page formats]
 // then per warp: [K slots: kK x PPI blocks][V slots: kV x PPI blocks][meta: kK x PPI]
@@ -91,15 +116,23 @@ struct Ring {
 template <int FMT>
 __host__ __device__ constexpr bool has_ds() { return Fmt<FMT>::kMain == kBlkInt4; }
 template <int FMT, int D>
+__host__ __device__ constexpr int page_base(int j) {
+  return Fmt<FMT>::kGroup ? j * group_page_bytes<FMT, D>() : j * half_slot_bytes<FMT, D>();
+}
+template <int FMT, int D>
+__host__ __device__ constexpr int copy_dst(int j) {
+  return Fmt<FMT>::kGroup ? page_base<FMT, D>(j) + copy_src<FMT, D>(j) : page_base<FMT, D>(j);
+}
+template <int FMT, int D>
 __host__ __device__ constexpr int warp_smem_bytes(int GS) {
-  return (Ring<FMT>::kK + Ring<FMT>::kV) * Fmt<FMT>::kPPI * half_slot_bytes<FMT, D>() +
+  return (Ring<FMT>::kK + Ring<FMT>::kV) * stage_bytes<FMT, D>() +
          align16(4 * Ring<FMT>::kK * Fmt<FMT>::kPPI) +
          (has_ds<FMT>() ? 16 * GS * 4 : 0) + 16 * GS * 4 + (Fmt<FMT>::kOutliers ? D * GS * 4 : 0);
 }
 // Page formats keep one zeroed block (K and V both read it) for absent pages.
 template <int FMT, int D>
 __host__ __device__ constexpr int zero_block_bytes() {
-  return Fmt<FMT>::kPaged ? align16(half_slot_bytes<FMT, D>()) : 0;
+  return !Fmt<FMT>::kPaged ? 0 : Fmt<FMT>::kGroup ? align16(stage_bytes<FMT, D>()) : align16(half_slot_bytes<FMT, D>());
 }
 template <int FMT, int W>
 __host__ __device__ constexpr int mbar_bytes() {
@@ -297,6 +330,9 @@ __device__ __forceinline__ uint32_t code0_bits(uint32_t blk_s, int role, int c) 
   if constexpr (BLK == kBlkA3) {
     const uint32_t m = lds16(blk_s + a3_m_off(D) + 2 * a3_rho(role, c));
     return prmt(m, m, 0x1010u);
+  } else if constexpr (BLK == kBlkCb2g) {   // blk_s: the group's codebook (its first page)
+    const uint2 lh = lds64(blk_s + 8 * cb2_slot(role, c));
+    return prmt(lh.x, lh.y, 0x4040u);
   } else {
     return c0_bits<D>(blk_s, cb2_slot(role, c));
   }
@@ -638,8 +674,12 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
   for (int p = 0; p < PPI; ++p) tier[p] = T && ent[p] < 0;
 
-  constexpr bool A3 = Fmt<FMT>::kMain == kBlkA3;
+  constexpr bool A3 = Fmt<FMT>::kMain == kBlkA3, GRP = Fmt<FMT>::kGroup;
   constexpr int SIDE = side_off<D, Fmt<FMT>::kMain>();
+  constexpr int CODES = GRP ? cb2g_code_off(D) : 0;   // codes within a page's (virtual) block
+  // codebook of page p: its own block, or (group format) the group's first page
+  auto kcb = [&](int p) { return GRP ? kb_s[0] : kb_s[p] + cb2_cb_off(D); };
+  auto vcb = [&](int p) { return GRP ? vb_s[0] : vb_s[p] + cb2_cb_off(D); };
   float acc[PPI][NT][4];
   uint32_t kc[PPI][NS / 2], ky[PPI][A3 ? NS / 4 : 1];   // codes (ASYM3: low-bit and high-bit words)
 #pragma unroll
@@ -647,7 +687,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
     if constexpr (A3) load_a3_words<D>(kb_s[p], lane, kc[p], ky[p]);
-    else load_codes<D>(kb_s[p], lane, kc[p]);
+    else load_codes<D>(kb_s[p] + CODES, lane, kc[p]);
   }
 #pragma unroll
   for (int s = 0; s < NS; ++s)
@@ -656,7 +696,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
       uint32_t ak[4];
       if (T && tier[p]) fp8_frag(lds64(kb_s[p] + 8 * NS * lane + 8 * s), ak);
       else if constexpr (A3) a3_k_frag<D>(kb_s[p], kc[p], ky[p], s, q4, ak);
-      else cb2_k_frag(kb_s[p] + cb2_cb_off(D) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
+      else cb2_k_frag(kcb(p) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
     }
@@ -686,7 +726,8 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
         recs = sm.bounce_s;
       }
-      cb2_k_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), kb_s[p], sm.qsm_s, sm.G, sm.GS, lane, acc[p]);
+      cb2_k_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), GRP ? kb_s[0] : kb_s[p], sm.qsm_s, sm.G,
+                                            sm.GS, lane, acc[p]);
       __syncwarp();
     }
   }
@@ -701,7 +742,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
     if constexpr (A3) load_a3_words<D>(vb_s[p], lane, vc[p], vy[p]);
-    else load_codes<D>(vb_s[p], lane, vc[p]);
+    else load_codes<D>(vb_s[p] + CODES, lane, vc[p]);
     sv[p] = (T && tier[p]) ? ldsf(vb_s[p] + fp8_sc_off(D)) : 1.f;
   }
 #pragma unroll
@@ -721,7 +762,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         }
       } else {
         if constexpr (A3) a3_v_frag<D>(vb_s[p], vc[p], vy[p], s, g, av);
-        else cb2_v_frag(vb_s[p] + cb2_cb_off(D) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
+        else cb2_v_frag(vcb(p) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
@@ -744,7 +785,8 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
         recs = sm.bounce_s;
       }
-      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), vb_s[p], phi[p], plo[p], sm.corr_s, sm.G, sm.GS, lane);
+      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), GRP ? vb_s[0] : vb_s[p], phi[p], plo[p],
+                                            sm.corr_s, sm.G, sm.GS, lane);
       __syncwarp();
     }
   }
@@ -1052,10 +1094,11 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   float* qsm = reinterpret_cast<float*>(base);
   uint8_t* zb = base + align16(D * GS * 4);
   uint8_t* wb = zb + zero_block_bytes<FMT, D>() + w * align16(warp_smem_bytes<FMT, D>(GS));
-  uint8_t* kslots = wb;                    // NK x PPI K blocks
-  uint8_t* vslots = wb + NK * PPI * HS;    // NV x PPI V blocks
+  constexpr int STG = stage_bytes<FMT, D>(), GPB = group_page_bytes<FMT, D>();
+  uint8_t* kslots = wb;                    // NK K stages
+  uint8_t* vslots = wb + NK * STG;         // NV V stages
   const uint32_t kslots_s = smem_u32(kslots), vslots_s = smem_u32(vslots);
-  int32_t* meta = reinterpret_cast<int32_t*>(wb + (NK + NV) * PPI * HS);
+  int32_t* meta = reinterpret_cast<int32_t*>(wb + (NK + NV) * STG);
   WarpSmem sm;
   sm.qsm = qsm;
   sm.ds = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(meta) + align16(4 * NK * PPI));
@@ -1109,11 +1152,22 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   }
   L = max(L, 0);
   const int n_all = (L + kPage - 1) / kPage;
-  const int nq = F::kPaged ? L / kPage : n_all;  // pages stored as blocks
+  // pages stored as blocks (the group format quantizes whole groups)
+  const int nq = F::kPaged ? (L / (kPage * F::kUnit)) * F::kUnit : n_all;
   const int p0 = split * a.pps;
   const int p1 = min(p0 + a.pps, n_all);
   const int pq1 = min(p1, nq);
-  const int n_local = pq1 > p0 + w ? (pq1 - p0 - w + W - 1) / W : 0;  // this warp's pages
+  // this warp's pages: every W-th page, or for the group format every W-th group
+  int n_local;
+  if constexpr (F::kGroup) {
+    const int ng = max(pq1 - p0, 0) / kGroupPages;
+    n_local = ng > w ? kGroupPages * ((ng - w + W - 1) / W) : 0;
+  } else {
+    n_local = pq1 > p0 + w ? (pq1 - p0 - w + W - 1) / W : 0;
+  }
+  auto page_of = [&](int li) {   // the sequence page of this warp's local page li
+    return F::kGroup ? p0 + kGroupPages * (w + (li / kGroupPages) * W) + li % kGroupPages : p0 + w + li * W;
+  };
   const int n_iter = (n_local + PPI - 1) / PPI;
 
   WarpState<D, NT> st;
@@ -1148,7 +1202,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   // page-table window: lane j holds the entry of this warp's local page win_base + j
   const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
   int win_base = 0;
-  int win = lane < n_local ? pt[p0 + w + lane * W] : 0;
+  int win = lane < n_local ? pt[page_of(lane)] : 0;
 
   // K copies of iteration `it` (local pages it*PPI .. it*PPI+PPI-1): validates
   // the page-table entries and records them in meta for the V copies and the
@@ -1166,7 +1220,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         if (li - win_base >= 32) {
           win_base += 32;
           const int jj = win_base + lane;
-          win = jj < n_local ? pt[p0 + w + jj * W] : 0;
+          win = jj < n_local ? pt[page_of(jj)] : 0;
         }
         ent[j] = __shfl_sync(0xffffffffu, win, li - win_base);
       }
@@ -1184,7 +1238,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
               tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
           if (ok) {
             m = ent[j];
-            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : main_fetch;
+            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : F::kGroup ? (j == 0 ? 8 * D + GPB : GPB) : main_fetch;
           } else {
             m = kBadEntry;
             atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
@@ -1200,8 +1254,9 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         mbar_arrive_expect_tx(&kbar[slot], total);
 #pragma unroll
         for (int j = 0; j < PPI; ++j)
-          if (bytes[j]) bulk_g2s(kslots + (slot * PPI + j) * HS, block_src<FMT, D>(a, kvh, ent[j], 0), bytes[j],
-                                 &kbar[slot]);
+          if (bytes[j])
+            bulk_g2s(kslots + slot * STG + copy_dst<FMT, D>(j), block_src<FMT, D>(a, kvh, ent[j], 0) + copy_src<FMT, D>(j),
+                     bytes[j], &kbar[slot]);
       }
     }
     __syncwarp();
@@ -1220,6 +1275,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         ent[j] = meta[kslot * PPI + j];
         bytes[j] = (ent[j] == kNoPage || ent[j] == kBadEntry) ? 0u
                    : (FMT == KVQ_FMT_TIERED && ent[j] < 0) ? (uint32_t)fetch_bytes<D>(kBlkFp8)
+                   : F::kGroup                             ? (uint32_t)(j == 0 ? 8 * D + GPB : GPB)
                                                            : (uint32_t)main_fetch;
         total += bytes[j];
       }
@@ -1230,8 +1286,9 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         mbar_arrive_expect_tx(&vbar[slot], total);
 #pragma unroll
         for (int j = 0; j < PPI; ++j)
-          if (bytes[j]) bulk_g2s(vslots + (slot * PPI + j) * HS, block_src<FMT, D>(a, kvh, ent[j], 1), bytes[j],
-                                 &vbar[slot]);
+          if (bytes[j])
+            bulk_g2s(vslots + slot * STG + copy_dst<FMT, D>(j), block_src<FMT, D>(a, kvh, ent[j], 1) + copy_src<FMT, D>(j),
+                     bytes[j], &vbar[slot]);
       }
     }
     __syncwarp();
@@ -1256,14 +1313,23 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     int32_t ent[PPI];
     int ntok[PPI];
     uint32_t kb_s[PPI], vb_s[PPI];
+    bool group_ok = true;
 #pragma unroll
     for (int j = 0; j < PPI; ++j) {
       ent[j] = meta[ks * PPI + j];
-      const int page = p0 + w + (it * PPI + j) * W;
+      const int page = page_of(it * PPI + j);
       ntok[j] = (ent[j] == kBadEntry || ent[j] == kNoPage) ? 0 : (F::kPaged ? kPage : min(kPage, L - kPage * page));
-      kb_s[j] = kslots_s + (ks * PPI + j) * HS;
-      vb_s[j] = vslots_s + (vs * PPI + j) * HS;
-      if (F::kPaged && ntok[j] == 0) kb_s[j] = vb_s[j] = zb_s;
+      group_ok = group_ok && ntok[j] > 0;
+      kb_s[j] = kslots_s + ks * STG + page_base<FMT, D>(j);
+      vb_s[j] = vslots_s + vs * STG + page_base<FMT, D>(j);
+      if (F::kPaged && !F::kGroup && ntok[j] == 0) kb_s[j] = vb_s[j] = zb_s;
+    }
+    if (F::kGroup && !group_ok) {   // a group with a bad page is left out whole
+#pragma unroll
+      for (int j = 0; j < PPI; ++j) {
+        ntok[j] = 0;
+        kb_s[j] = vb_s[j] = zb_s + page_base<FMT, D>(j);
+      }
     }
     // k_done: the K slot is free, refill it; v_wait: the V blocks must have landed
     auto k_done = [&]() {
@@ -1275,12 +1341,12 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
       v_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[vs], (it / NV) & 1, kWaitLimitNs));
       v_waited += v_ok;
     };
-    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s || F::kMain == kBlkA3) {
+    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s || F::kMain == kBlkA3 || F::kGroup) {
       iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
     } else if constexpr (F::kMain == kBlkE2m1) {
       iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane, k_done, v_wait);
     } else {
-      iter_int4<D, NT>(st, qf, kslots + ks * HS, vslots + vs * HS, ntok[0], a.scale_log2, sm, lane, k_done,
+      iter_int4<D, NT>(st, qf, kslots + ks * STG, vslots + vs * STG, ntok[0], a.scale_log2, sm, lane, k_done,
                        v_wait);
     }
     if (!v_ok) {
@@ -1301,12 +1367,16 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     for (int j = 0; j < NK + NV; ++j) mbar_inval(&kbar[j]);
 
   // partial last page of a page format, from fp32 staging
-  if (F::kPaged && (L % kPage) != 0 && !timed_out) {
-    const int tp = nq;
-    if (tp >= p0 && tp < p1 && (tp - p0) % W == w) {
-      const float* ks = a.staging + (((size_t)b * a.Hkv + kvh) * 2) * kPage * D;
-      page_tail<D, NT, F::kOutliers>(st, ks, ks + kPage * D, L % kPage, a.scale_log2, sm, lane);
-    }
+  // (the group format: up to kGroupPages staged pages of the partial last group)
+  if (F::kPaged && !timed_out) {
+    constexpr int ROWS = kPage * F::kUnit;   // staging rows per (sequence, kv head, K|V)
+    const float* ks = a.staging + (((size_t)b * a.Hkv + kvh) * 2) * ROWS * D;
+    for (int tp = max(nq, p0); tp < p1; ++tp)
+      if ((tp - p0) % W == w) {
+        const int off = (tp % F::kUnit) * kPage * D;
+        page_tail<D, NT, F::kOutliers>(st, ks + off, ks + ROWS * D + off, min(kPage, L - kPage * tp), a.scale_log2, sm,
+                                       lane);
+      }
   }
 
   // ---- merge the W warps of the CTA and write the split's partial state
@@ -1444,5 +1514,6 @@ KernelInfo decode_kernel_cb2(int D, int G);
 KernelInfo decode_kernel_tiered(int D, int G);
 KernelInfo decode_kernel_cb2s(int D, int G);
 KernelInfo decode_kernel_a3(int D, int G);
+KernelInfo decode_kernel_cb2g(int D, int G);
 
 }  // namespace kvq

@@ -34,7 +34,9 @@ __device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) 
   n = a.t_per_seq ? a.t_per_seq[b] : a.t_new;
   if (n <= 0) return kSeqNothing;
   if (n > a.t_new || start < 0 || (long long)start + n > (long long)a.ppsm * kPage) return kSeqCapacity;
-  for (int pg = start / kPage; pg <= (start + n - 1) / kPage; ++pg) {
+  // a completed CB2 group rewrites all of its pages, including earlier ones
+  const int first = a.fmt == KVQ_FMT_CB2_GROUP4 ? (start / (kPage * kGroupPages)) * kGroupPages : start / kPage;
+  for (int pg = first; pg <= (start + n - 1) / kPage; ++pg) {
     const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
     const bool ok = (u >> 31) ? (a.fmt == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages)
                               : phys < (uint32_t)a.num_pages;
@@ -102,7 +104,8 @@ __device__ __forceinline__ int nearest4(float v, const float* c) {
   return best;
 }
 
-// Lloyd-Max 4-centroid fit of v[0..n) (n <= 16) in binary32; fp16 centroids and codes.
+// Lloyd-Max 4-centroid fit of v[0..n) (n <= NMAX) in binary32; fp16 centroids and codes.
+template <int NMAX>
 __device__ void lloyd4(const float* v, int n, int iters, uint16_t* c16, uint8_t* codes) {
   float c[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 0) {
@@ -110,7 +113,7 @@ __device__ void lloyd4(const float* v, int n, int iters, uint16_t* c16, uint8_t*
     for (int i = 1; i < n; ++i) { mn = v[i] < mn ? v[i] : mn; mx = v[i] > mx ? v[i] : mx; }
     const float h = __fdiv_rn(mx - mn, 3.0f);
     c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0f * h; c[3] = mx;
-    uint8_t a[16], prev[16];
+    uint8_t a[NMAX], prev[NMAX];
     bool have_prev = false;
     for (int it = 0; it < iters; ++it) {
       bool same = have_prev;
@@ -274,6 +277,49 @@ __global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
 }
 
 // ----------------------------------------------------------------------------- page formats
+// Outlier side-list of one page (CB2, ASYM3, CB2 group) from its mask and
+// values [16][D], built by one warp: lane l owns channels [l*D/32, (l+1)*D/32);
+// one 20-byte record {channel, 0, token mask, 16 e4m3 values} per channel
+// with an outlier, channels ascending, after {n_ch, total}.  Zeros come from
+// the block clear.
+template <int D>
+__device__ void build_side_list(const uint8_t (*mask)[D], const float (*xs)[D], uint8_t* hdr, int lane) {
+  constexpr int CPL = D / 32;
+  uint32_t tm[CPL];
+  int nch = 0, nval = 0;
+  for (int k = 0; k < CPL; ++k) {
+    const int c = lane * CPL + k;
+    uint32_t m = 0;
+    for (int t = 0; t < 16; ++t) m |= (uint32_t)mask[t][c] << t;
+    tm[k] = m;
+    nch += m != 0;
+    nval += __popc(m);
+  }
+  int ich = nch, ival = nval;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int a1 = __shfl_up_sync(0xffffffffu, ich, d), a2 = __shfl_up_sync(0xffffffffu, ival, d);
+    if (lane >= d) { ich += a1; ival += a2; }
+  }
+  const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
+  int ci = ich - nch;
+  for (int k = 0; k < CPL; ++k) {
+    if (!tm[k]) continue;
+    const int c = lane * CPL + k;
+    uint8_t* rec = hdr + 4 + 20 * ci;
+    rec[0] = (uint8_t)c;
+    rec[1] = 0;
+    rec[2] = (uint8_t)(tm[k] & 0xFF);
+    rec[3] = (uint8_t)(tm[k] >> 8);
+    for (int t = 0; t < 16; ++t)
+      if (tm[k] >> t & 1u) rec[4 + t] = f32_to_e4m3(xs[t][c]);
+    ++ci;
+  }
+  if (lane == 0) {
+    hdr[0] = (uint8_t)tot_ch;
+    hdr[1] = (uint8_t)tot_val;
+  }
+}
+
 // 2-bit codes [16][D] -> the block's lane-major code words (CB2 layout).
 template <int D>
 __device__ __forceinline__ void pack_cb2_codes(const uint8_t (&codes)[16][D], uint8_t* blk, int role, int tid) {
@@ -379,7 +425,7 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         uint8_t cc[16];
         uint16_t c16[4];
         for (int t = 0; t < 16; ++t) v[t] = xs[t][c];
-        lloyd4(v, 16, a.iters, c16, cc);
+        lloyd4<16>(v, 16, a.iters, c16, cc);
         for (int t = 0; t < 16; ++t) codes[t][c] = cc[t];
         uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
         for (int jj = 0; jj < 4; ++jj) {
@@ -437,7 +483,7 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
       int nv = 0;
       for (int t = 0; t < 16; ++t)
         if (!mask[t][c]) v[nv++] = xs[t][c];
-      lloyd4(v, nv, a.iters, c16, cc);
+      lloyd4<16>(v, nv, a.iters, c16, cc);
       nv = 0;
       for (int t = 0; t < 16; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];
       uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
@@ -446,46 +492,7 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
       }
     }
-    if (tid < 32) {
-      // side-list grouped by channel: lane l owns channels [l*CPL, (l+1)*CPL)
-      constexpr int CPL = D / 32;
-      const int lane = tid;
-      uint32_t tm[CPL];
-      int nch = 0, nval = 0;
-      for (int k = 0; k < CPL; ++k) {
-        const int c = lane * CPL + k;
-        uint32_t m = 0;
-        for (int t = 0; t < 16; ++t) m |= (uint32_t)mask[t][c] << t;
-        tm[k] = m;
-        nch += m != 0;
-        nval += __popc(m);
-      }
-      int ich = nch, ival = nval;
-      for (int d = 1; d < 32; d <<= 1) {
-        const int a1 = __shfl_up_sync(0xffffffffu, ich, d), a2 = __shfl_up_sync(0xffffffffu, ival, d);
-        if (lane >= d) { ich += a1; ival += a2; }
-      }
-      const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
-      uint8_t* hdr = blk + (a3 ? a3_out_off(D) : cb2_out_off(D));
-      int ci = ich - nch;
-      for (int k = 0; k < CPL; ++k) {
-        if (!tm[k]) continue;
-        const int c = lane * CPL + k;
-        // 20-byte record {channel, 0, token mask, 16 values}; zeros from the block clear
-        uint8_t* rec = hdr + 4 + 20 * ci;
-        rec[0] = (uint8_t)c;
-        rec[1] = 0;
-        rec[2] = (uint8_t)(tm[k] & 0xFF);
-        rec[3] = (uint8_t)(tm[k] >> 8);
-        for (int t = 0; t < 16; ++t)
-          if (tm[k] >> t & 1u) rec[4 + t] = f32_to_e4m3(xs[t][c]);
-        ++ci;
-      }
-      if (lane == 0) {
-        hdr[0] = (uint8_t)tot_ch;
-        hdr[1] = (uint8_t)tot_val;
-      }
-    }
+    if (tid < 32) build_side_list<D>(mask, xs, blk + (a3 ? a3_out_off(D) : cb2_out_off(D)), tid);
     __syncthreads();
     if (a3) pack_a3_codes<D>(codes, blk, role, tid);
     else pack_cb2_codes<D>(codes, blk, role, tid);
@@ -495,18 +502,90 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
     reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk)[i];
 }
 
-// New tokens of the final partial page -> fp32 staging (after the page kernel).
+// CB2 group format: each group of 4 pages (64 tokens) this append completes,
+// from fp32 staging + the new tokens: outliers per token, one codebook per
+// channel over the group's non-outliers in token order (in the group's first
+// page), codes and side-list per page.  One CTA per (group, kv head x role,
+// sequence); dynamic shared memory holds the values, masks, codes and the
+// four blocks.
+template <int D>
+__global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
+  constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D);
+  extern __shared__ __align__(16) uint8_t gsm[];
+  float(*xs)[D] = reinterpret_cast<float(*)[D]>(gsm);
+  uint8_t(*mask)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 4);
+  uint8_t(*codes)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 5);
+  uint8_t* blk = gsm + GT * D * 6;   // 4 blocks of kStride bytes
+  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, gr = start / GT + j;
+  if (gr * GT + GT > end) return;  // only groups this append completes
+  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
+  for (int i = tid; i < GT * D; i += blockDim.x) {
+    const int t = i / D, c = i - t * D, pos = gr * GT + t;
+    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
+  }
+  for (int i = tid; i < kGroupPages * kStride / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid < GT) outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+  __syncthreads();
+  if (tid < D) {
+    const int c = tid;
+    float v[GT];
+    uint8_t cc[GT];
+    uint16_t c16[4];
+    int nv = 0;
+    for (int t = 0; t < GT; ++t)
+      if (!mask[t][c]) v[nv++] = xs[t][c];
+    lloyd4<GT>(v, nv, a.iters, c16, cc);
+    nv = 0;
+    for (int t = 0; t < GT; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];
+    uint8_t* cbp = blk + 8 * cb2_slot(role, c);   // the codebook sits at the start of the group's first block
+    for (int jj = 0; jj < 4; ++jj) {
+      cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
+      cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
+    }
+  }
+  // one warp per page builds its side-list
+  {
+    const int w = tid >> 5;
+    build_side_list<D>(mask + 16 * w, xs + 16 * w, blk + w * kStride + cb2_out_off(D), tid & 31);
+  }
+  __syncthreads();
+  for (int p = 0; p < kGroupPages; ++p)
+    pack_cb2_codes<D>(*reinterpret_cast<const uint8_t(*)[16][D]>(&codes[16 * p][0]), blk + p * kStride + cb2g_code_off(D),
+                      role, tid);
+  __syncthreads();
+  for (int p = 0; p < kGroupPages; ++p) {
+    const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + gr * kGroupPages + p];
+    uint8_t* gblk = a.pool + (((size_t)(u & 0x7FFFFFFFu) * a.Hkv + h) * 2 + role) * kStride;
+    for (int i = tid; i < kStride / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk + p * kStride)[i];
+  }
+}
+
+template <int D>
+constexpr size_t group_smem_bytes() {
+  return (size_t)kPage * kGroupPages * D * 6 + (size_t)kGroupPages * block_stride(kBlkCb2g, D);
+}
+
+// New tokens of the final partial page (the final partial group for the CB2
+// group format) -> fp32 staging (after the page / group kernel).
 __global__ void __launch_bounds__(256) append_stage_kernel(const AppendArgs a, int D) {
   const int h = blockIdx.x >> 1, role = blockIdx.x & 1, b = blockIdx.y;
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int rows = a.fmt == KVQ_FMT_CB2_GROUP4 ? kPage * kGroupPages : kPage;
   const int end = start + n;
-  if (end % kPage == 0) return;
-  const int lo = max(start, (end / kPage) * kPage);
-  float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
+  if (end % rows == 0) return;
+  const int lo = max(start, (end / rows) * rows);
+  float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * rows * D;
   for (int i = threadIdx.x; i < (end - lo) * D; i += blockDim.x) {
     const int tt = i / D, c = i - tt * D, pos = lo + tt;
-    stg[(pos % kPage) * D + c] = load_in(a, role, b, pos - start, h, c, D);
+    stg[(pos % rows) * D + c] = load_in(a, role, b, pos - start, h, c, D);
   }
 }
 
@@ -569,7 +648,17 @@ static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
   const dim3 grid(pages_max, a.Hkv * 2, a.B);
   if (a.fmt == KVQ_FMT_INT4_G32) append_token_kernel<kBlkInt4, D><<<grid, 256, 0, st>>>(a);
   else if (a.fmt == KVQ_FMT_FP4_E2M1_S16) append_token_kernel<kBlkE2m1, D><<<grid, 256, 0, st>>>(a);
-  else {
+  else if (a.fmt == KVQ_FMT_CB2_GROUP4) {
+    constexpr size_t smem = group_smem_bytes<D>();
+    if (smem > 48 * 1024) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(append_group_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    const int groups_max = a.t_new / (kPage * kGroupPages) + 2;
+    append_group_kernel<D><<<dim3(groups_max, a.Hkv * 2, a.B), 128, smem, st>>>(a);
+    append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
+  } else {
     append_page_kernel<D><<<grid, 128, 0, st>>>(a);
     append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
   }

@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
 KVQ_FMT_INT4_G32, KVQ_FMT_FP4_E2M1_S16, KVQ_FMT_CB2_OUTLIER, KVQ_FMT_TIERED, KVQ_FMT_CB2_STATIC = 0, 1, 2, 3, 4
-KVQ_FMT_ASYM3_OUTLIER = 5
+KVQ_FMT_ASYM3_OUTLIER, KVQ_FMT_CB2_GROUP4 = 5, 6
 KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 KVQ_TIER_BIT = 1 << 31
 KVQ_STATUS_BAD_PAGE, KVQ_STATUS_CAPACITY, KVQ_STATUS_SEQ_TOO_LONG, KVQ_STATUS_TIMEOUT = 1, 2, 4, 8

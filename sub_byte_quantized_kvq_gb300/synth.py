@@ -22,6 +22,8 @@ on; no public dataset is involved, these stand in for real KV caches):
                  chosen from sequence 0's first 256 tokens), 1 channel x10
   a3_4k          B8  Hkv8 Hq32 D128 N4096    3-bit asymmetric codes + e4m3
                  outliers, data as cb2_4k
+  group_4k       B8  Hkv8 Hq32 D128 N4096    2-bit codebook per group of 4
+                 pages + e4m3 outliers, data as cb2_4k
 
 Every generator takes an explicit seed; per-sequence data is drawn from a
 generator seeded by (seed, sequence) so one sequence of a large workload can be
@@ -35,7 +37,7 @@ import math
 import numpy as np
 import torch
 
-FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S, FMT_A3 = 0, 1, 2, 3, 4, 5
+FMT_INT4, FMT_E2M1, FMT_CB2, FMT_TIERED, FMT_CB2S, FMT_A3, FMT_CB2G = 0, 1, 2, 3, 4, 5, 6
 CALIBRATION_TOKENS = 256   # static channel mask: chosen from sequence 0's first tokens
 TIER_BIT = 1 << 31
 
@@ -77,6 +79,7 @@ WORKLOADS = {
     "longctx_128k": Workload("longctx_128k", FMT_CB2, 4, 8, 32, 128, 131072, "normal", 1, 10.0, splits=64),
     "static_4k": Workload("static_4k", FMT_CB2S, 8, 8, 32, 128, 4096, "normal", 1, 10.0, static_channels=2),
     "a3_4k": Workload("a3_4k", FMT_A3, 8, 8, 32, 128, 4096, "normal", 4, 8.0),
+    "group_4k": Workload("group_4k", FMT_CB2G, 8, 8, 32, 128, 4096, "normal", 4, 8.0),
 }
 
 

@@ -7,6 +7,7 @@ import oracle
 from sub_byte_quantized_kvq_gb300 import kvq, synth
 
 ORACLE_FMT = {kvq.KVQ_FMT_CB2_STATIC: oracle.FMT_CB2S, kvq.KVQ_FMT_ASYM3_OUTLIER: oracle.FMT_A3,
+              kvq.KVQ_FMT_CB2_GROUP4: oracle.FMT_CB2G,
               kvq.KVQ_FMT_INT4_G32: oracle.FMT_INT4, kvq.KVQ_FMT_FP4_E2M1_S16: oracle.FMT_E2M1,
               kvq.KVQ_FMT_CB2_OUTLIER: oracle.FMT_CB2, kvq.KVQ_FMT_TIERED: oracle.FMT_TIERED}
 

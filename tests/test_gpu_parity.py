@@ -14,12 +14,12 @@ from sub_byte_quantized_kvq_gb300 import kvq
 
 pytestmark = pytest.mark.gpu
 
-CB2S, A3 = kvq.KVQ_FMT_CB2_STATIC, kvq.KVQ_FMT_ASYM3_OUTLIER
+CB2S, A3, CB2G = kvq.KVQ_FMT_CB2_STATIC, kvq.KVQ_FMT_ASYM3_OUTLIER, kvq.KVQ_FMT_CB2_GROUP4
 INT4, E2M1, CB2, TIERED = (kvq.KVQ_FMT_INT4_G32, kvq.KVQ_FMT_FP4_E2M1_S16, kvq.KVQ_FMT_CB2_OUTLIER,
                            kvq.KVQ_FMT_TIERED)
 FORMATS_D = [(INT4, 64), (INT4, 128), (E2M1, 64), (E2M1, 128), (CB2, 64), (CB2, 128), (TIERED, 64), (TIERED, 128),
-             (CB2S, 64), (CB2S, 128), (A3, 64), (A3, 128)]
-IDS = [f"{['int4', 'e2m1', 'cb2', 'tiered', 'cb2s', 'a3'][f]}-d{d}" for f, d in FORMATS_D]
+             (CB2S, 64), (CB2S, 128), (A3, 64), (A3, 128), (CB2G, 64), (CB2G, 128)]
+IDS = [f"{['int4', 'e2m1', 'cb2', 'tiered', 'cb2s', 'a3', 'cb2g'][f]}-d{d}" for f, d in FORMATS_D]
 
 
 def _tiers(fmt, B, P):
@@ -93,7 +93,7 @@ def test_decode_attention_parity(fmt, D, G):
     assert pair.gpu.status_word() == 0
 
 
-@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED, CB2S, A3])
+@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED, CB2S, A3, CB2G])
 def test_fused_merge_matches_split_then_combine(fmt):
     """kvq_decode_attention merges the splits inside its one launch (the last
     CTA of each (sequence, kv head) to arrive); kvq_decode_split followed by
@@ -122,7 +122,7 @@ def test_fused_merge_matches_split_then_combine(fmt):
     assert cache.status_word() == 0
 
 
-@pytest.mark.parametrize("fmt", [CB2, TIERED, A3])
+@pytest.mark.parametrize("fmt", [CB2, TIERED, A3, CB2G])
 @pytest.mark.parametrize("D,dist", [(64, "student_t4"), (128, "student_t4"), (128, "normal")])
 def test_decode_side_lists_longer_than_prefetch(fmt, D, dist):
     """The decode kernel gets the first six side-list records (channels) with
@@ -144,7 +144,7 @@ def test_decode_side_lists_longer_than_prefetch(fmt, D, dist):
     assert pair.gpu.status_word() == 0
 
 
-@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED, CB2S, A3])
+@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED, CB2S, A3, CB2G])
 def test_decode_after_token_by_token_appends(fmt):
     """Decode after every single-token append (the serving loop), crossing page boundaries."""
     B, Hkv, D, P, G = 2, 2, 128, 4, 4

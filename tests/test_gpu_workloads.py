@@ -57,7 +57,8 @@ def _ref_block(ref, entry, role):
     return pool[off:off + stride]
 
 
-@pytest.mark.parametrize("name", ["cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k", "static_4k", "a3_4k"])
+@pytest.mark.parametrize("name", ["cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k", "static_4k", "a3_4k",
+                                  "group_4k"])
 def test_full_size_workload_sampled(name):
     w = synth.WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
