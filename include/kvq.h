@@ -186,6 +186,30 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
                                const void* v_new, kvq_dtype in_dtype, int32_t t_new,
                                const int32_t* t_per_seq, void* stream);
 
+/* K/V projection fused with quantize-on-append ([P3] "Engineering Real-Time
+ * Autonomous Workflows", item 1: the attention projection and the KV-cache
+ * write in one kernel).  For appended token i of sequence b and kv head h,
+ *   k = x[b][i] . W_k[h*D + j][:],  v = x[b][i] . W_v[h*D + j][:]   (j < D)
+ * with bf16 operands and fp32 accumulation on the tensor cores; k and v are
+ * then quantized into the cache exactly as kvq_quantize_append quantizes fp32
+ * inputs (same blocks, staging, seq_lens and status behaviour), without being
+ * written to global memory.  Every format.
+ *   x         device bf16 [num_seqs][t_new][hidden], 16-byte aligned.
+ *   hidden    a positive multiple of 32.
+ *   w_k, w_v  device bf16 [num_kv_heads * head_dim][hidden] (a linear layer's
+ *             weight, output-major), 16-byte aligned.
+ *   t_per_seq as for kvq_quantize_append.
+ *   kv_out    NULL, or device fp32 [2][num_seqs][t_new][num_kv_heads][head_dim],
+ *             16-byte aligned: receives the projected K (index 0) and V of the
+ *             tokens appended; other rows are not written.
+ * Errors: KVQ_ERR_INVALID_ARG for a null or misaligned pointer or a bad size,
+ * KVQ_ERR_UNSUPPORTED for head_dim other than 64 / 128, KVQ_ERR_CAPACITY as
+ * for kvq_quantize_append.  A tensor-core wait that gives up sets
+ * KVQ_STATUS_TIMEOUT and leaves that tile's blocks unwritten. */
+kvq_status kvq_project_append(const kvq_config* cfg, const kvq_cache* cache, const void* x, int32_t hidden,
+                              const void* w_k, const void* w_v, int32_t t_new, const int32_t* t_per_seq,
+                              float* kv_out, void* stream);
+
 /* Workspace bytes kvq_decode_attention needs for (num_q_heads, max_seq_len,
  * num_splits); num_splits = 0 asks for the library's choice. */
 kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t num_q_heads, int32_t max_seq_len,

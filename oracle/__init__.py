@@ -192,6 +192,22 @@ def attention(q, k, v, scale: float) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- paged cache model
+def project_kv(x, w_k, w_v, Hkv: int, D: int):
+    """The appended tokens' K and V as the attention projection of the layer
+    input ("Sub-5ms MoE Inference: Sub-Byte KV Quantization and Expert
+    Pipelining at Scale", Engineering Real-Time Autonomous Workflows, item 1,
+    which fuses this projection with the KV-cache write):
+        k[b, i, h, j] = sum_e x[b, i, e] * w_k[h * D + j, e]   (likewise v)
+    in fp64.  x [B, T, hidden], w_k / w_v [Hkv * D, hidden] (a linear layer's
+    output-major weight).  Returns (k, v) float64 [B, T, Hkv, D]."""
+    x = np.asarray(x, np.float64)
+    out = []
+    for w in (w_k, w_v):
+        w = np.asarray(w, np.float64)
+        out.append(np.matmul(x, w.T).reshape(x.shape[0], x.shape[1], Hkv, D))
+    return out[0], out[1]
+
+
 class OracleCache:
     """numpy model of the paged, quantized cache (same layout as the library's)."""
 

@@ -263,23 +263,16 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* ti
   return KVQ_OK;
 }
 
-kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, const void* k_new, const void* v_new,
-                               kvq_dtype in_dtype, int32_t t_new, const int32_t* t_per_seq, void* stream) {
-  if (!cfg_ok(cfg) || !cache_ok(cfg, cache) || !k_new || !v_new || t_new < 0) return KVQ_ERR_INVALID_ARG;
-  if (in_dtype != KVQ_BF16 && in_dtype != KVQ_F16 && in_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
-  if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
-  if (t_new == 0) return KVQ_OK;
-  if ((long long)t_new > (long long)cfg->pages_per_seq_max * kPage) return KVQ_ERR_CAPACITY;
-  AppendArgs a;
+static void fill_append_args(const kvq_config* cfg, const kvq_cache* cache, int32_t t_new, const int32_t* t_per_seq,
+                             AppendArgs& a) {
   a.pool = static_cast<uint8_t*>(cache->pool);
   a.tier_pool = static_cast<uint8_t*>(cache->tier_pool);
   a.page_table = cache->page_table;
   a.seq_lens = cache->seq_lens;
   a.staging = cache->staging;
   a.status = cache->status;
-  a.kv[0] = k_new;
-  a.kv[1] = v_new;
-  a.in_dtype = in_dtype;
+  a.kv[0] = a.kv[1] = nullptr;
+  a.in_dtype = KVQ_F32;
   a.t_new = t_new;
   a.t_per_seq = t_per_seq;
   a.B = cfg->num_seqs;
@@ -292,7 +285,43 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
   a.sigma = cfg->sigma;
   a.static_mask = cache->static_mask;
   a.n_static = cfg->format == KVQ_FMT_CB2_STATIC ? cfg->static_channels : 0;
+}
+
+kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, const void* k_new, const void* v_new,
+                               kvq_dtype in_dtype, int32_t t_new, const int32_t* t_per_seq, void* stream) {
+  if (!cfg_ok(cfg) || !cache_ok(cfg, cache) || !k_new || !v_new || t_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (in_dtype != KVQ_BF16 && in_dtype != KVQ_F16 && in_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
+  if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
+  if (t_new == 0) return KVQ_OK;
+  if ((long long)t_new > (long long)cfg->pages_per_seq_max * kPage) return KVQ_ERR_CAPACITY;
+  AppendArgs a;
+  fill_append_args(cfg, cache, t_new, t_per_seq, a);
+  a.kv[0] = k_new;
+  a.kv[1] = v_new;
+  a.in_dtype = in_dtype;
   if (append_launch(a, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status kvq_project_append(const kvq_config* cfg, const kvq_cache* cache, const void* x, int32_t hidden,
+                              const void* w_k, const void* w_v, int32_t t_new, const int32_t* t_per_seq,
+                              float* kv_out, void* stream) {
+  if (!cfg_ok(cfg) || !cache_ok(cfg, cache) || !x || !w_k || !w_v || t_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (hidden <= 0 || hidden % 32 || !aligned16(x) || !aligned16(w_k) || !aligned16(w_v) || !aligned16(kv_out))
+    return KVQ_ERR_INVALID_ARG;
+  if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
+  if (t_new == 0) return KVQ_OK;
+  if ((long long)t_new > (long long)cfg->pages_per_seq_max * kPage) return KVQ_ERR_CAPACITY;
+  ProjArgs p;
+  fill_append_args(cfg, cache, t_new, t_per_seq, p.a);
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w[0] = static_cast<const __nv_bfloat16*>(w_k);
+  p.w[1] = static_cast<const __nv_bfloat16*>(w_v);
+  p.hidden = hidden;
+  p.kv_out = kv_out;
+  if (project_append_launch(p, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 

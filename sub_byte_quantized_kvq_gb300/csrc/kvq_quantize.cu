@@ -225,43 +225,40 @@ __device__ void quantize_token_e2m1(const float* x, int t, uint8_t (*codes)[D], 
   blk[e2m1_sc_off(D) + 16 * lane + t] = s8;
 }
 
-template <int BF, int D>
-__global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
-  constexpr int kStride = block_stride(BF, D), NS = D / 16;
-  __shared__ __align__(16) uint8_t blk[kStride];
-  __shared__ uint8_t codes[16][D];
-  __shared__ float xs[16][D];
-  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  int start, n;
-  if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int end = start + n, pg = start / kPage + j;
-  if (pg * kPage >= end) return;
-  const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
-  const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
-  uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
+// Threads [0, n) of a group of a CTA (tid is the index within the group, n a
+// multiple of 32) that synchronise on named barrier `bar`; bar 0 with
+// n = blockDim.x is the whole CTA.
+struct Grp {
+  int tid, n, bar;
+  __device__ __forceinline__ void sync() const { asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(n) : "memory"); }
+};
+__device__ __forceinline__ Grp whole_cta() { return Grp{(int)threadIdx.x, (int)blockDim.x, 0}; }
 
-  for (int i = tid; i < kStride / 16; i += blockDim.x)
+// Per-token formats: re-quantize token slots [lo, hi) of one block from rows
+// xs[slot] (row stride XS floats); the other slots keep their codes and
+// metadata.  blk (the block's bytes) and codes[16][D] are the group's scratch;
+// the caller's writes of xs come before the call.
+template <int BF, int D, int XS>
+__device__ void token_block_update(const AppendArgs& a, int role, const float (*xs)[XS], int lo, int hi, uint8_t* gblk,
+                                   uint8_t* blk, uint8_t (*codes)[D], const Grp& g) {
+  constexpr int kStride = block_stride(BF, D), NS = D / 16;
+  const int lane = g.tid & 31, warp = g.tid >> 5, nw = g.n >> 5;
+  for (int i = g.tid; i < kStride / 16; i += g.n)
     reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(gblk)[i];
-  for (int i = tid; i < (hi - lo) * D; i += blockDim.x) {
-    const int tt = i / D, c = i - tt * D;
-    xs[(lo % kPage) + tt][c] = load_in(a, role, b, lo + tt - start, h, c, D);
-  }
-  __syncthreads();
-  for (int i = tid; i < 32 * NS * 8; i += blockDim.x) {
+  g.sync();
+  for (int i = g.tid; i < 32 * NS * 8; i += g.n) {
     const int ln = i / (NS * 8), s = (i / 8) % NS, k = i % 8;
     int t, c;
     frag_inverse(role, ln, s, k, t, c);
     codes[t][c] = (blk[4 * NS * ln + 4 * s + k / 2] >> (4 * (k & 1))) & 0xF;
   }
-  __syncthreads();
-  for (int tt = warp; tt < hi - lo; tt += nwarps) {
-    const int t = (lo % kPage) + tt;
+  g.sync();
+  for (int t = lo + warp; t < hi; t += nw) {
     if (BF == kBlkInt4) quantize_token_int4<D>(xs[t], t, codes, blk, a.sigma, lane);
     else quantize_token_e2m1<D>(xs[t], t, codes, blk, lane);
   }
-  __syncthreads();
-  for (int i = tid; i < 32 * NS; i += blockDim.x) {
+  g.sync();
+  for (int i = g.tid; i < 32 * NS; i += g.n) {
     const int ln = i / NS, s = i % NS;
     uint32_t word = 0;
     for (int k = 0; k < 8; ++k) {
@@ -271,19 +268,42 @@ __global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
     }
     *reinterpret_cast<uint32_t*>(blk + 4 * NS * ln + 4 * s) = word;
   }
-  __syncthreads();
-  for (int i = tid; i < kStride / 16; i += blockDim.x)
+  g.sync();
+  for (int i = g.tid; i < kStride / 16; i += g.n)
     reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk)[i];
+  g.sync();   // the scratch may be reused by the next call
+}
+
+template <int BF, int D>
+__global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
+  constexpr int kStride = block_stride(BF, D);
+  __shared__ __align__(16) uint8_t blk[kStride];
+  __shared__ uint8_t codes[16][D];
+  __shared__ float xs[16][D];
+  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, pg = start / kPage + j;
+  if (pg * kPage >= end) return;
+  const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
+  const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
+  uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
+  for (int i = tid; i < (hi - lo) * D; i += blockDim.x) {
+    const int tt = i / D, c = i - tt * D;
+    xs[(lo % kPage) + tt][c] = load_in(a, role, b, lo + tt - start, h, c, D);
+  }
+  token_block_update<BF, D, D>(a, role, xs, lo % kPage, lo % kPage + (hi - lo), gblk, blk, codes, whole_cta());
 }
 
 // ----------------------------------------------------------------------------- page formats
 // Outlier side-list of one page (CB2, ASYM3, CB2 group) from its mask and
-// values [16][D], built by one warp: lane l owns channels [l*D/32, (l+1)*D/32);
-// one 20-byte record {channel, 0, token mask, 16 e4m3 values} per channel
-// with an outlier, channels ascending, after {n_ch, total}.  Zeros come from
-// the block clear.
-template <int D>
-__device__ void build_side_list(const uint8_t (*mask)[D], const float (*xs)[D], uint8_t* hdr, int lane) {
+// values [16][D] (row stride XS), built by one warp: lane l owns channels
+// [l*D/32, (l+1)*D/32); one 20-byte record {channel, 0, token mask, 16 e4m3
+// values} per channel with an outlier, channels ascending, after {n_ch,
+// total}.  Zeros come from the block clear.
+template <int D, int XS>
+__device__ void build_side_list(const uint8_t (*mask)[D], const float (*xs)[XS], uint8_t* hdr, int lane) {
   constexpr int CPL = D / 32;
   uint32_t tm[CPL];
   int nch = 0, nval = 0;
@@ -322,9 +342,9 @@ __device__ void build_side_list(const uint8_t (*mask)[D], const float (*xs)[D], 
 
 // 2-bit codes [16][D] -> the block's lane-major code words (CB2 layout).
 template <int D>
-__device__ __forceinline__ void pack_cb2_codes(const uint8_t (&codes)[16][D], uint8_t* blk, int role, int tid) {
+__device__ __forceinline__ void pack_cb2_codes(const uint8_t (*codes)[D], uint8_t* blk, int role, const Grp& g) {
   constexpr int NS = D / 16;
-  for (int i = tid; i < 32 * NS; i += blockDim.x) {
+  for (int i = g.tid; i < 32 * NS; i += g.n) {
     const int ln = i / NS, s = i % NS;
     uint32_t word = 0;
     for (int k = 0; k < 8; ++k) {
@@ -340,9 +360,9 @@ __device__ __forceinline__ void pack_cb2_codes(const uint8_t (&codes)[16][D], ui
 // one thread per (lane, 4-step group) builds one high-bit word and two
 // low-bit words.
 template <int D>
-__device__ __forceinline__ void pack_a3_codes(const uint8_t (&codes)[16][D], uint8_t* blk, int role, int tid) {
+__device__ __forceinline__ void pack_a3_codes(const uint8_t (*codes)[D], uint8_t* blk, int role, const Grp& g) {
   constexpr int NS = D / 16, NG = NS / 4;
-  for (int i = tid; i < 32 * NG; i += blockDim.x) {
+  for (int i = g.tid; i < 32 * NG; i += g.n) {
     const int ln = i / NG, grp = i % NG;
     uint32_t lo[2] = {0u, 0u}, hi = 0u;
     for (int ss = 0; ss < 4; ++ss) {
@@ -362,48 +382,54 @@ __device__ __forceinline__ void pack_a3_codes(const uint8_t (&codes)[16][D], uin
   }
 }
 
+// Bytes of the block buffer a page quantization needs (CB2, CB2_STATIC, ASYM3 or an FP8 tier block).
 template <int D>
-__global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
-  constexpr int NS = D / 16;
+__host__ __device__ constexpr int page_blk_bytes() {
+  return block_stride(kBlkCb2, D) > block_stride(kBlkFp8, D) ? block_stride(kBlkCb2, D) : block_stride(kBlkFp8, D);
+}
+
+// Shared scratch of one page quantization.
+template <int D>
+struct PageWs {
+  uint8_t (*mask)[D];   // [16][D]
+  uint8_t (*codes)[D];  // [16][D]
+  uint8_t* blk;         // page_blk_bytes<D>(), 16-byte aligned
+  float* red;           // one float per warp of the group
+};
+
+// Page formats: quantize the 16 tokens xs[16] (row stride XS) of one page into
+// the block named by page-table entry u (tier bit, physical page) and store it.
+// The caller's writes of xs come before the call.
+template <int D, int XS>
+__device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, const float (*xs)[XS],
+                              const PageWs<D>& ws, const Grp& g) {
+  constexpr int NS = D / 16, kBlk = page_blk_bytes<D>();
   constexpr int kCb2 = block_stride(kBlkCb2, D), kFp8 = block_stride(kBlkFp8, D);
-  constexpr int kBlk = kCb2 > kFp8 ? kCb2 : kFp8;
-  __shared__ float xs[16][D];
-  __shared__ uint8_t mask[16][D];
-  __shared__ uint8_t codes[16][D];
-  __shared__ __align__(16) uint8_t blk[kBlk];
-  __shared__ int cnt[16];
-  __shared__ float red[4];
-  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
-  const int tid = threadIdx.x;
-  int start, n;
-  if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int end = start + n, pg = start / kPage + j;
-  if (pg * kPage + kPage > end) return;  // only pages this append completes
-  const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
+  uint8_t(*mask)[D] = ws.mask;
+  uint8_t(*codes)[D] = ws.codes;
+  uint8_t* blk = ws.blk;
+  const int tid = g.tid;
+  const uint32_t phys = u & 0x7FFFFFFFu;
   const bool tier = (u >> 31) != 0;
   const bool stat = a.fmt == KVQ_FMT_CB2_STATIC;
   const int stride = tier ? kFp8
                    : stat ? block_stride(kBlkCb2s, D)
                    : a.fmt == KVQ_FMT_ASYM3_OUTLIER ? block_stride(kBlkA3, D) : kCb2;
   uint8_t* gblk = (tier ? a.tier_pool : a.pool) + (((size_t)phys * a.Hkv + h) * 2 + role) * stride;
-  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
 
-  for (int i = tid; i < 16 * D; i += blockDim.x) {
-    const int t = i / D, c = i - t * D, pos = pg * kPage + t;
-    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
-  }
-  for (int i = tid; i < kBlk / 16; i += blockDim.x) reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
+  for (int i = tid; i < kBlk / 16; i += g.n) reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
+  g.sync();
 
   if (tier) {
     float amax = 0.f;
-    for (int i = tid; i < 16 * D; i += blockDim.x) amax = fmaxf(amax, fabsf(xs[i / D][i % D]));
+    for (int i = tid; i < 16 * D; i += g.n) amax = fmaxf(amax, fabsf(xs[i / D][i % D]));
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    if ((tid & 31) == 0) red[tid >> 5] = amax;
-    __syncthreads();
-    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    if ((tid & 31) == 0) ws.red[tid >> 5] = amax;
+    g.sync();
+    amax = 0.f;
+    for (int w = 0; w < g.n / 32; ++w) amax = fmaxf(amax, ws.red[w]);
     const float s = __fdiv_rn(amax, 448.0f);
-    for (int i = tid; i < 16 * D; i += blockDim.x) {
+    for (int i = tid; i < 16 * D; i += g.n) {
       const int t = i / D, c = i - t * D;
       const FragPos p = frag_pos(role, t, c);
       blk[8 * NS * p.lane + 8 * p.step + p.slot] = s != 0.f ? f32_to_e4m3(__fdiv_rn(xs[t][c], s)) : 0;
@@ -413,9 +439,9 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
     // static fp16 channels (all tokens); every other channel: codebook over all 16 values
     const uint8_t* chs = a.static_mask + ((size_t)h * 2 + role) * a.n_static;
     if (tid < D) mask[0][tid] = 0;
-    __syncthreads();
+    g.sync();
     if (tid < a.n_static) mask[0][chs[tid] & (D - 1)] = 1;
-    __syncthreads();
+    g.sync();
     if (tid < D) {
       const int c = tid;
       if (mask[0][c]) {
@@ -441,14 +467,14 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         *reinterpret_cast<uint16_t*>(blk + cb2s_val_off(D) + 32 * tid + 2 * t) = f32_to_f16_bits(xs[t][c]);
     }
     if (tid == 0) blk[cb2s_hdr_off(D)] = (uint8_t)a.n_static;
-    __syncthreads();
-    pack_cb2_codes<D>(codes, blk, role, tid);
+    g.sync();
+    pack_cb2_codes<D>(codes, blk, role, g);
   } else {
     // CB2 or ASYM3: per-token outliers, then per channel a codebook (CB2) or an
     // 8-level affine grid (ASYM3) over the non-outliers
     const bool a3 = a.fmt == KVQ_FMT_ASYM3_OUTLIER;
-    if (tid < 16) cnt[tid] = outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
-    __syncthreads();
+    if (tid < 16) outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+    g.sync();
     if (tid < D && a3) {
       const int c = tid;
       bool have = false;
@@ -492,46 +518,64 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
         cbp[4 + jj] = (uint8_t)(c16[jj] >> 8);
       }
     }
-    if (tid < 32) build_side_list<D>(mask, xs, blk + (a3 ? a3_out_off(D) : cb2_out_off(D)), tid);
-    __syncthreads();
-    if (a3) pack_a3_codes<D>(codes, blk, role, tid);
-    else pack_cb2_codes<D>(codes, blk, role, tid);
+    if (tid < 32) build_side_list<D, XS>(mask, xs, blk + (a3 ? a3_out_off(D) : cb2_out_off(D)), tid);
+    g.sync();
+    if (a3) pack_a3_codes<D>(codes, blk, role, g);
+    else pack_cb2_codes<D>(codes, blk, role, g);
   }
-  __syncthreads();
-  for (int i = tid; i < stride / 16; i += blockDim.x)
+  g.sync();
+  for (int i = tid; i < stride / 16; i += g.n)
     reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk)[i];
+  g.sync();   // the scratch may be reused by the next call
 }
 
-// CB2 group format: each group of 4 pages (64 tokens) this append completes,
-// from fp32 staging + the new tokens: outliers per token, one codebook per
-// channel over the group's non-outliers in token order (in the group's first
-// page), codes and side-list per page.  One CTA per (group, kv head x role,
-// sequence); dynamic shared memory holds the values, masks, codes and the
-// four blocks.
 template <int D>
-__global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
-  constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D);
-  extern __shared__ __align__(16) uint8_t gsm[];
-  float(*xs)[D] = reinterpret_cast<float(*)[D]>(gsm);
-  uint8_t(*mask)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 4);
-  uint8_t(*codes)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 5);
-  uint8_t* blk = gsm + GT * D * 6;   // 4 blocks of kStride bytes
+__global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
+  __shared__ float xs[16][D];
+  __shared__ uint8_t mask[16][D];
+  __shared__ uint8_t codes[16][D];
+  __shared__ __align__(16) uint8_t blk[page_blk_bytes<D>()];
+  __shared__ float red[4];
   const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
   const int tid = threadIdx.x;
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int end = start + n, gr = start / GT + j;
-  if (gr * GT + GT > end) return;  // only groups this append completes
-  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
-  for (int i = tid; i < GT * D; i += blockDim.x) {
-    const int t = i / D, c = i - t * D, pos = gr * GT + t;
+  const int end = start + n, pg = start / kPage + j;
+  if (pg * kPage + kPage > end) return;  // only pages this append completes
+  const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg];
+  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
+  for (int i = tid; i < 16 * D; i += blockDim.x) {
+    const int t = i / D, c = i - t * D, pos = pg * kPage + t;
     xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
   }
-  for (int i = tid; i < kGroupPages * kStride / 16; i += blockDim.x)
+  page_quantize<D, D>(a, h, role, u, xs, PageWs<D>{mask, codes, blk, red}, whole_cta());
+}
+
+// Shared scratch of one CB2 group quantization.
+template <int D>
+struct GroupWs {
+  uint8_t (*mask)[D];   // [64][D]
+  uint8_t (*codes)[D];  // [64][D]
+  uint8_t* blk;         // kGroupPages blocks
+};
+
+// CB2 group format: quantize the 64 tokens xs[64] (row stride XS) of group gr
+// of the sequence whose page-table row is pt: outliers per token, one codebook
+// per channel over the group's non-outliers in token order (in the group's
+// first page), codes and side-list per page.
+template <int D, int XS>
+__device__ void group_quantize(const AppendArgs& a, int h, int role, const int32_t* pt, int gr, const float (*xs)[XS],
+                               const GroupWs<D>& ws, const Grp& g) {
+  constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D);
+  uint8_t(*mask)[D] = ws.mask;
+  uint8_t(*codes)[D] = ws.codes;
+  uint8_t* blk = ws.blk;
+  const int tid = g.tid;
+  for (int i = tid; i < kGroupPages * kStride / 16; i += g.n)
     reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
+  g.sync();
   if (tid < GT) outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
-  __syncthreads();
+  g.sync();
   if (tid < D) {
     const int c = tid;
     float v[GT];
@@ -550,21 +594,45 @@ __global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
     }
   }
   // one warp per page builds its side-list
-  {
-    const int w = tid >> 5;
-    build_side_list<D>(mask + 16 * w, xs + 16 * w, blk + w * kStride + cb2_out_off(D), tid & 31);
-  }
-  __syncthreads();
-  for (int p = 0; p < kGroupPages; ++p)
-    pack_cb2_codes<D>(*reinterpret_cast<const uint8_t(*)[16][D]>(&codes[16 * p][0]), blk + p * kStride + cb2g_code_off(D),
-                      role, tid);
-  __syncthreads();
+  for (int w = tid >> 5; w < kGroupPages; w += g.n >> 5)
+    build_side_list<D, XS>(mask + 16 * w, xs + 16 * w, blk + w * kStride + cb2_out_off(D), tid & 31);
+  g.sync();
+  for (int p = 0; p < kGroupPages; ++p) pack_cb2_codes<D>(codes + 16 * p, blk + p * kStride + cb2g_code_off(D), role, g);
+  g.sync();
   for (int p = 0; p < kGroupPages; ++p) {
-    const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + gr * kGroupPages + p];
+    const uint32_t u = (uint32_t)pt[gr * kGroupPages + p];
     uint8_t* gblk = a.pool + (((size_t)(u & 0x7FFFFFFFu) * a.Hkv + h) * 2 + role) * kStride;
-    for (int i = tid; i < kStride / 16; i += blockDim.x)
+    for (int i = tid; i < kStride / 16; i += g.n)
       reinterpret_cast<uint4*>(gblk)[i] = reinterpret_cast<const uint4*>(blk + p * kStride)[i];
   }
+  g.sync();   // the scratch may be reused by the next call
+}
+
+// CB2 group format: each group of 4 pages (64 tokens) this append completes,
+// from fp32 staging + the new tokens.  One CTA per (group, kv head x role,
+// sequence); dynamic shared memory holds the values, masks, codes and the
+// four blocks.
+template <int D>
+__global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
+  constexpr int GT = kPage * kGroupPages;
+  extern __shared__ __align__(16) uint8_t gsm[];
+  float(*xs)[D] = reinterpret_cast<float(*)[D]>(gsm);
+  uint8_t(*mask)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 4);
+  uint8_t(*codes)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 5);
+  uint8_t* blk = gsm + GT * D * 6;   // 4 blocks
+  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, gr = start / GT + j;
+  if (gr * GT + GT > end) return;  // only groups this append completes
+  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
+  for (int i = tid; i < GT * D; i += blockDim.x) {
+    const int t = i / D, c = i - t * D, pos = gr * GT + t;
+    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
+  }
+  group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{mask, codes, blk},
+                       whole_cta());
 }
 
 template <int D>
@@ -668,6 +736,307 @@ static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
 
 cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st) {
   return D == 64 ? append_launch_d<64>(a, st) : append_launch_d<128>(a, st);
+}
+
+// ----------------------------------------------------------------------------- fused projection + append
+// K = x W_k^T and V = x W_v^T for the appended tokens, computed on the 5th
+// generation tensor cores (tcgen05.mma, fp32 accumulators in tensor memory)
+// and handed straight to the quantizer of the cache's format: the projected
+// K/V never reach global memory ("Sub-5ms MoE Inference: Sub-Byte KV
+// Quantization and Expert Pipelining at Scale", Engineering Real-Time
+// Autonomous Workflows, item 1: the attention projection and the KV-cache
+// write in one kernel).
+//
+// One CTA (512 threads) per (tile of 128 sequence positions, kv head,
+// sequence) computes K and V together (N = 2 D accumulator columns).  Tile
+// rows are whole pages (4-page groups for the CB2 group format), so each block
+// is written by one CTA.  Operands are staged with cp.async into the K-major,
+// no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix), three
+// stages of 32 columns of the hidden dimension; one thread issues the MMAs and
+// commits each stage to an mbarrier.  The epilogue reads the accumulators
+// with tcgen05.ld into an fp32 tile in shared memory and runs the same
+// per-token / per-page / per-group quantizers as kvq_quantize_append.
+namespace tc {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);   // SWIZZLE_NONE, version 1
+}
+// kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 accumulator, M x N
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accumulate) {
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem),
+               "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 fp32 columns of the calling warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+// 16-byte global -> shared copy; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+}  // namespace tc
+
+// Fused projection plan: a tile is kPM rows (sequence positions, whole units
+// of U rows: pages, or 4-page groups for the CB2 group format) x N = 2 D
+// columns (K then V of one kv head) in TMEM; the hidden dimension streams
+// through kPStages shared-memory stages of kPK columns.
+enum { kProjInt4 = 0, kProjE2m1 = 1, kProjPage = 2, kProjGroup = 3 };
+constexpr int kPM = 128, kPK = 32, kPStages = 3, kPThreads = 512;
+static_assert(kPK == 32, "the operand staging maps 4 core matrices per row group");
+
+template <int KIND, int D>
+struct ProjPlan {
+  static constexpr int U = KIND == kProjGroup ? kPage * kGroupPages : kPage;  // rows of one unit
+  static constexpr int SPT = kPM / U;                                         // units per tile
+  static constexpr int NB = KIND == kProjGroup ? 2 : 4;                       // unit groups working at once
+  static constexpr int GS = kPThreads / NB;                                   // threads per unit group
+  static constexpr int N = 2 * D;                                             // TMEM columns: K | V
+  static constexpr int XS = D + 4;  // row stride of the fp32 tile: rows start 4 banks apart
+  static constexpr int A_BYTES = kPM * kPK * 2, B_BYTES = N * kPK * 2, STAGE = A_BYTES + B_BYTES;
+  static constexpr int R0 = kPStages * STAGE > kPM * XS * 4 ? kPStages * STAGE : kPM * XS * 4;
+  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
+                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
+                          : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
+                                                : kGroupPages * block_stride(kBlkCb2g, D) + 128 * D;
+  static constexpr int WSR = (WS + 127) / 128 * 128;
+  static constexpr int SMEM = R0 + NB * WSR + kPM * 4 + kPStages * 8 + 16;
+};
+
+#define KVQ_PLAN_FITS(K, D_)                                                                          \
+  static_assert(ProjPlan<K, D_>::SMEM <= 227 * 1024 && ProjPlan<K, D_>::N <= 256 &&                     \
+                    ProjPlan<K, D_>::R0 >= kPM * ProjPlan<K, D_>::XS * 4 &&                           \
+                    ProjPlan<K, D_>::R0 >= kPStages * ProjPlan<K, D_>::STAGE,                          \
+                "fused projection plan does not fit")
+KVQ_PLAN_FITS(kProjInt4, 64);
+KVQ_PLAN_FITS(kProjInt4, 128);
+KVQ_PLAN_FITS(kProjE2m1, 64);
+KVQ_PLAN_FITS(kProjE2m1, 128);
+KVQ_PLAN_FITS(kProjPage, 64);
+KVQ_PLAN_FITS(kProjPage, 128);
+KVQ_PLAN_FITS(kProjGroup, 64);
+KVQ_PLAN_FITS(kProjGroup, 128);
+#undef KVQ_PLAN_FITS
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const ProjArgs p) {
+  using P = ProjPlan<KIND, D>;
+  constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS;
+  extern __shared__ __align__(1024) uint8_t psm[];
+  const AppendArgs& a = p.a;
+  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int start, n;
+  if (seq_append_state(a, b, start, n) != kSeqOk) return;
+  const int end = start + n, first = start / U, last = (end - 1) / U, nu = last - first + 1;
+  const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
+  // Unit in slot s of this tile, or -1.  Tile 0 holds both the first unit
+  // (which reads the staged rows) and the last (which writes them), so no
+  // other CTA touches this sequence's staging.
+  auto unit_of = [&](int s) -> int {
+    if (nu <= SPT) return tile == 0 && s < nu ? first + s : -1;
+    if (tile == 0) return s < SPT - 1 ? first + s : last;
+    const int u = first + (SPT - 1) + SPT * (tile - 1) + s;
+    return u < last ? u : -1;
+  };
+  if (unit_of(0) < 0) return;
+
+  float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(psm);   // the fp32 tile, once the stages are done
+  uint8_t* ws = psm + P::R0;
+  int* rowtok = reinterpret_cast<int*>(ws + NB * P::WSR);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(rowtok + kPM);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + kPStages);
+
+  for (int r = tid; r < kPM; r += kPThreads) {
+    const int u = unit_of(r / U), pos = u * U + r % U;
+    rowtok[r] = u >= 0 && pos >= start && pos < end ? pos - start : -1;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kPStages; ++s) mbar_init(&mbar[s], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(N)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+
+  // Stage kc: x rows (zeros for rows without a token) and the K|V weight rows
+  // of head h, columns [kPK kc, kPK kc + kPK).  16-byte chunk i sits at 16 i:
+  // row group i / 32, core matrix (i / 8) % 4 along K, row i % 8.
+  const __nv_bfloat16* xb = p.x + (size_t)b * a.t_new * p.hidden;
+  const int nk = p.hidden / kPK;
+  auto issue = [&](int kc) {
+    const uint32_t sa = smem_u32(psm + (kc % kPStages) * P::STAGE), sb = sa + P::A_BYTES;
+    const int k0 = kc * kPK;
+    for (int i = tid; i < kPM * kPK / 8; i += kPThreads) {
+      const int r = (i >> 5) * 8 + (i & 7), kcr = (i >> 3) & 3, tt = rowtok[r];
+      const __nv_bfloat16* src = tt >= 0 ? xb + (size_t)tt * p.hidden + k0 + 8 * kcr : p.x;
+      tc::cp16(sa + 16 * i, src, tt >= 0 ? 16u : 0u);
+    }
+    for (int i = tid; i < N * kPK / 8; i += kPThreads) {
+      const int r = (i >> 5) * 8 + (i & 7), kcr = (i >> 3) & 3, role = r >= D;
+      tc::cp16(sb + 16 * i, p.w[role] + ((size_t)h * D + (r - role * D)) * p.hidden + k0 + 8 * kcr, 16u);
+    }
+  };
+  // K-major, no swizzle: core matrices 128 B apart along K (LBO), 8-row groups
+  // 512 B apart (SBO); one MMA covers K = 16, i.e. two core matrices.
+  const uint32_t idesc = tc::idesc_bf16(kPM, N);
+  bool ok = true;
+  for (int s = 0; s < kPStages - 1; ++s) {
+    if (s < nk) issue(s);
+    tc::cp_commit();
+  }
+  for (int kc = 0; kc < nk; ++kc) {
+    const int nxt = kc + kPStages - 1;
+    if (nxt < nk) {
+      // stage nxt % kPStages was last read by the MMAs of slice kc - 1
+      if (kc >= 1 && ok && !mbar_wait_bounded(&mbar[(kc - 1) % kPStages], ((kc - 1) / kPStages) & 1, kWaitLimitNs))
+        ok = false;
+      issue(nxt);
+    }
+    tc::cp_commit();
+    tc::cp_wait<kPStages - 1>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // cp.async data -> the tensor core's view
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t sa = smem_u32(psm + (kc % kPStages) * P::STAGE), sb = sa + P::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < kPK / 16; ++kk)
+        tc::mma(tmem, tc::smem_desc(sa + 256 * kk, 128, 512), tc::smem_desc(sb + 256 * kk, 128, 512), idesc,
+                (kc | kk) != 0);
+      tc::commit(&mbar[kc % kPStages]);
+    }
+  }
+  const bool done =
+      ok && mbar_wait_bounded(&mbar[(nk - 1) % kPStages], ((nk - 1) / kPStages) & 1, kWaitLimitNs);
+  tc::cp_wait<0>();
+  const bool all_ok = __syncthreads_and(done) != 0;
+  tc::fence_after();
+  if (all_ok) {
+    const int grp = warp / (GS / 32);
+    const Grp g{tid % GS, GS, 1 + grp};
+    uint8_t* gws = ws + grp * P::WSR;
+    for (int role = 0; role < 2; ++role) {
+      // accumulators of this role -> xs: warp w reads TMEM lanes (tile rows)
+      // 32 (w % 4) .. and 32 columns from 32 (w / 4)
+      const int q = warp & 3, cc = warp >> 2, r = 32 * q + lane;
+      if (32 * cc < D) {
+        float v[32];
+        tc::ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(role * D + 32 * cc), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(&xs[r][32 * cc + 4 * j]) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        const int tt = rowtok[r];
+        if (p.kv_out && tt >= 0) {
+          float4* o = reinterpret_cast<float4*>(p.kv_out + ((((size_t)role * a.B + b) * a.t_new + tt) * a.Hkv + h) * D +
+                                                32 * cc);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      }
+      __syncthreads();
+      if (KIND >= kProjPage && tile == 0) {   // the first unit's earlier tokens come from staging
+        const int pre = start - first * U;
+        const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
+        for (int i = tid; i < pre * D; i += kPThreads) xs[i / D][i % D] = stg[i];
+        __syncthreads();
+      }
+      for (int s = grp; s < SPT; s += NB) {
+        const int u = unit_of(s);
+        if (u < 0) continue;
+        const int lo = max(start, u * U) - u * U, hi = min(end, u * U + U) - u * U;   // new rows of the unit
+        const float(*xu)[XS] = xs + s * U;
+        if constexpr (KIND == kProjInt4 || KIND == kProjE2m1) {
+          constexpr int BF = KIND == kProjInt4 ? kBlkInt4 : kBlkE2m1, kStride = block_stride(BF, D);
+          const uint32_t phys = (uint32_t)pt[u] & 0x7FFFFFFFu;
+          token_block_update<BF, D, XS>(a, role, xu, lo, hi, a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride,
+                                        gws, reinterpret_cast<uint8_t(*)[D]>(gws + kStride), g);
+        } else if (u * U + U <= end) {   // the append completes the unit
+          if constexpr (KIND == kProjPage) {
+            constexpr int kB = page_blk_bytes<D>();
+            const PageWs<D> pw{reinterpret_cast<uint8_t(*)[D]>(gws + kB), reinterpret_cast<uint8_t(*)[D]>(gws + kB + 16 * D),
+                               gws, reinterpret_cast<float*>(gws + kB + 32 * D)};
+            page_quantize<D, XS>(a, h, role, (uint32_t)pt[u], xu, pw, g);
+          } else {
+            constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
+            const GroupWs<D> gw{reinterpret_cast<uint8_t(*)[D]>(gws + kB), reinterpret_cast<uint8_t(*)[D]>(gws + kB + 64 * D),
+                                gws};
+            group_quantize<D, XS>(a, h, role, pt, u, xu, gw, g);
+          }
+        } else {   // the final partial unit: its new rows wait in staging
+          float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
+          for (int i = g.tid; i < (hi - lo) * D; i += g.n) {
+            const int t = lo + i / D, c = i % D;
+            stg[t * D + c] = xu[t][c];
+          }
+        }
+      }
+      __syncthreads();
+    }
+  } else if (tid == 0) {
+    atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
+  if (tid == 0)
+    for (int s = 0; s < kPStages; ++s) mbar_inval(&mbar[s]);
+}
+
+template <int KIND, int D>
+static cudaError_t project_launch_k(const ProjArgs& p, cudaStream_t st) {
+  using P = ProjPlan<KIND, D>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(project_append_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+  if (e != cudaSuccess) return e;
+  const int units_max = (p.a.t_new + 2 * P::U - 2) / P::U;   // units a span of t_new positions can touch
+  const dim3 grid((units_max + P::SPT - 1) / P::SPT, p.a.Hkv, p.a.B);
+  project_append_kernel<KIND, D><<<grid, kPThreads, P::SMEM, st>>>(p);
+  append_finish_kernel<<<(p.a.B + 127) / 128, 128, 0, st>>>(p.a);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t project_launch_d(const ProjArgs& p, cudaStream_t st) {
+  switch (p.a.fmt) {
+    case KVQ_FMT_INT4_G32: return project_launch_k<kProjInt4, D>(p, st);
+    case KVQ_FMT_FP4_E2M1_S16: return project_launch_k<kProjE2m1, D>(p, st);
+    case KVQ_FMT_CB2_GROUP4: return project_launch_k<kProjGroup, D>(p, st);
+    default: return project_launch_k<kProjPage, D>(p, st);
+  }
+}
+
+cudaError_t project_append_launch(const ProjArgs& p, int D, cudaStream_t st) {
+  return D == 64 ? project_launch_d<64>(p, st) : project_launch_d<128>(p, st);
 }
 
 }  // namespace kvq

@@ -47,7 +47,8 @@ class kvq_cache(ctypes.Structure):
 
 _lib = None
 _lock = threading.Lock()
-EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
+EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_project_append",
+           "kvq_decode_workspace_bytes",
            "kvq_decode_num_splits", "kvq_decode_split", "kvq_decode_combine", "kvq_decode_attention",
            "kvq_decode_attention_noalloc", "kvq_select_static_channels", "kvq_dequantize", "kvq_status_string",
            "kvq_version")
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
                 "kvq_block_bytes": (I, [pcfg, I, ctypes.POINTER(S)]),
                 "kvq_cache_bytes": (I, [pcfg, ctypes.POINTER(S), ctypes.POINTER(S), ctypes.POINTER(S)]),
                 "kvq_quantize_append": (I, [pcfg, pcache, P, P, I, I, P, P]),
+                "kvq_project_append": (I, [pcfg, pcache, P, I, P, P, I, P, P, P]),
                 "kvq_decode_workspace_bytes": (I, [pcfg, I, I, I, ctypes.POINTER(S)]),
                 "kvq_decode_num_splits": (I, [pcfg, I, I, ctypes.POINTER(I)]),
                 "kvq_decode_split": (I, [pcfg, pcache, P, I, ctypes.c_float, I, I, P, S, P]),
@@ -165,6 +167,27 @@ def kvq_quantize_append(cache: QuantizedKVCache, k_new: torch.Tensor, v_new: tor
     _check(lib().kvq_quantize_append(ctypes.byref(cache.cfg), ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new),
                                      _DTYPE[k_new.dtype], k_new.shape[1], _ptr(t_per_seq), _stream(stream)),
            "kvq_quantize_append")
+
+
+def kvq_project_append(cache: QuantizedKVCache, x: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor,
+                       t_per_seq: torch.Tensor | None = None, kv_out: torch.Tensor | None = None, stream=None):
+    """x: bf16 [num_seqs, t_new, hidden]; w_k, w_v: bf16 [Hkv * D, hidden].  K = x w_k^T and
+    V = x w_v^T are projected on the tensor cores and quantized into the cache in one kernel.
+    kv_out: optional fp32 [2, num_seqs, t_new, Hkv, D] that receives the projected K and V."""
+    cfg = cache.cfg
+    assert x.dtype == torch.bfloat16 and w_k.dtype == torch.bfloat16 and w_v.dtype == torch.bfloat16
+    assert x.is_contiguous() and w_k.is_contiguous() and w_v.is_contiguous()
+    assert x.dim() == 3 and x.shape[0] == cfg.num_seqs
+    hidden = x.shape[2]
+    assert w_k.shape == (cfg.num_kv_heads * cfg.head_dim, hidden) and w_v.shape == w_k.shape
+    if kv_out is not None:
+        assert kv_out.dtype == torch.float32 and kv_out.is_contiguous()
+        assert kv_out.shape == (2, cfg.num_seqs, x.shape[1], cfg.num_kv_heads, cfg.head_dim)
+    if t_per_seq is not None:
+        t_per_seq = t_per_seq.to(torch.int32).contiguous()
+    _check(lib().kvq_project_append(ctypes.byref(cfg), ctypes.byref(cache.c), _ptr(x), hidden, _ptr(w_k), _ptr(w_v),
+                                    x.shape[1], _ptr(t_per_seq), _ptr(kv_out), _stream(stream)),
+           "kvq_project_append")
 
 
 def kvq_decode_num_splits(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int) -> int:

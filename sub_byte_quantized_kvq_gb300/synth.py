@@ -122,6 +122,25 @@ def workload_kv(w: Workload, seed: int, b: int, t0: int, T: int, device="cpu"):
     return kv_tokens(seed, b, t0, T, w.Hkv, w.D, w.dist, ch, w.factor, device)
 
 
+def projection_inputs(seed: int, B: int, T: int, hidden: int, Hkv: int, D: int, n_out: int = 4,
+                      factor: float = 8.0, device="cpu"):
+    """Layer input x bf16 [B, T, hidden] ~ N(0, 1) and K / V projection weights
+    bf16 [Hkv * D, hidden] ~ N(0, 1 / hidden) (so projected values are about
+    unit variance), the weight rows of n_out channels per (K|V, head) scaled by
+    `factor` so the projected K / V carry outlier channels like the workloads'."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) * 131 + 7)
+    x = torch.randn((B, T, hidden), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    ch = outlier_channels(seed, Hkv, D, n_out)
+    ws = []
+    for r in range(2):
+        w = torch.randn((Hkv, D, hidden), generator=g, dtype=torch.float32) * hidden ** -0.5
+        for h in range(Hkv):
+            w[h, torch.as_tensor(ch[r, h])] *= factor
+        ws.append(w.reshape(Hkv * D, hidden).to(torch.bfloat16))
+    return x.to(device), ws[0].to(device), ws[1].to(device)
+
+
 def queries_bf16(seed: int, B: int, Hq: int, D: int, device="cpu") -> torch.Tensor:
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed) * 31 + 17)

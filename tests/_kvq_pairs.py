@@ -63,6 +63,26 @@ class Pair:
         bad = self.ref.append(kd.float().numpy(), vd.float().numpy(), None if tps is None else tps.numpy())
         return bad
 
+    def project(self, x, w_k, w_v, t_per_seq=None):
+        """x: bf16 CPU [B, T, hidden], w_k / w_v: bf16 CPU [Hkv * D, hidden].  The GPU
+        projects and appends in one kernel and hands back the fp32 K / V it
+        quantized; the oracle appends those same values.  Returns the GPU's
+        (k, v) float32 [B, T, Hkv, D] (rows past t_per_seq[b] zero)."""
+        B, T = x.shape[0], x.shape[1]
+        if not self.calibrated:   # static mask from the oracle's projection of sequence 0's first tokens
+            n = min(T, 64)
+            kc, vc = oracle.project_kv(x[:1, :n].float().numpy(), w_k.float().numpy(), w_v.float().numpy(),
+                                       self.Hkv, self.D)
+            self.calibrate(torch.from_numpy(kc[0]).float(), torch.from_numpy(vc[0]).float())
+        tps = None if t_per_seq is None else torch.as_tensor(t_per_seq, dtype=torch.int32)
+        kv_out = torch.zeros((2, B, T, self.Hkv, self.D), dtype=torch.float32, device="cuda")
+        kvq.kvq_project_append(self.gpu, x.cuda().contiguous(), w_k.cuda().contiguous(), w_v.cuda().contiguous(),
+                               None if tps is None else tps.cuda(), kv_out)
+        torch.cuda.synchronize()
+        kv = kv_out.cpu().numpy()
+        self.ref.append(kv[0], kv[1], None if tps is None else tps.numpy())
+        return kv[0], kv[1]
+
     def assert_cache_equal(self):
         torch.cuda.synchronize()
         assert self.gpu.status_word() == 0, hex(self.gpu.status_word())

@@ -80,6 +80,8 @@ def test_invalid_arguments_rejected_before_launch(kvq):
     c = _cfg(kvq)
     assert L.kvq_quantize_append(ctypes.byref(c), ctypes.byref(cache), None, None, 0, 1, None, None) == \
         kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_project_append(ctypes.byref(c), ctypes.byref(cache), None, 64, None, None, 1, None, None, None) == \
+        kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_decode_attention(ctypes.byref(c), ctypes.byref(cache), None, 32, ctypes.c_float(0.1), 16, 0, None, 0,
                                   None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_dequantize(ctypes.byref(c), ctypes.byref(cache), 0, 0, 0, 0, 1, None, None) == kvq.KVQ_ERR_INVALID_ARG

@@ -1,0 +1,98 @@
+"""K/V projection fused with quantize-on-append (kvq_project_append): the
+projected values it hands back agree with the oracle's fp64 projection within
+the fp32-accumulation bound, and the cache it writes is bit-identical to the
+oracle appending those same values -- every format, both head dims, ragged
+appends that span several 128-row tiles, a staged tail from an earlier
+append, and an append that starts mid-group."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sub_byte_quantized_kvq_gb300 import kvq, synth
+
+from _kvq_pairs import Pair
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [kvq.KVQ_FMT_INT4_G32, kvq.KVQ_FMT_FP4_E2M1_S16, kvq.KVQ_FMT_CB2_OUTLIER, kvq.KVQ_FMT_TIERED,
+           kvq.KVQ_FMT_CB2_STATIC, kvq.KVQ_FMT_ASYM3_OUTLIER, kvq.KVQ_FMT_CB2_GROUP4]
+
+
+def assert_projection_close(got, x, w, which, Hkv, D, t_per_seq):
+    """|got - exact| <= hidden * 2^-23 * sum_e |x_e w_e|: bf16 products are exact in
+    fp32, so the only error is the fp32 accumulation over `hidden` terms."""
+    xf, wf = x.float().numpy().astype(np.float64), w.float().numpy().astype(np.float64)
+    exact = oracle.project_kv(xf, wf, wf, Hkv, D)[0]
+    mag = np.matmul(np.abs(xf), np.abs(wf).T).reshape(exact.shape)
+    bound = x.shape[2] * 2.0 ** -23 * mag + 1e-30
+    for b in range(x.shape[0]):
+        n = x.shape[1] if t_per_seq is None else t_per_seq[b]
+        err = np.abs(got[b, :n] - exact[b, :n])
+        assert (err <= bound[b, :n]).all(), f"{which} seq {b}: max err {err.max():.3e}"
+        assert (got[b, n:] == 0).all(), f"{which} seq {b}: rows past the append were written"
+
+
+def tiers_for(fmt, B, P):
+    if fmt != kvq.KVQ_FMT_TIERED:
+        return None
+    t = np.zeros((B, P), bool)
+    t[:, 1::3] = True
+    return t
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_project_append_matches_oracle(fmt, D):
+    B, Hkv, P, hidden = 2, 2, 24, 256
+    pair = Pair(fmt, B, Hkv, D, P, seed=3, tiers=tiers_for(fmt, B, P))
+    x, wk, wv = synth.projection_inputs(3, B, 200, hidden, Hkv, D)
+    # a ragged first append, then one that spans two tiles (more than 8 pages / 2 groups)
+    for sl, tps in [(slice(0, 37), [37, 21]), (slice(37, 200), [163, 150])]:
+        xs = x[:, sl].contiguous()
+        k, v = pair.project(xs, wk, wv, tps)
+        assert_projection_close(k, xs, wk, "K", Hkv, D, tps)
+        assert_projection_close(v, xs, wv, "V", Hkv, D, tps)
+        pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_CB2_OUTLIER, kvq.KVQ_FMT_CB2_GROUP4, kvq.KVQ_FMT_INT4_G32])
+def test_project_after_plain_append_uses_the_staged_tail(fmt):
+    B, Hkv, D, P, hidden = 2, 2, 128, 16, 128
+    pair = Pair(fmt, B, Hkv, D, P, seed=4)
+    k0, v0 = synth.kv_tokens(4, 0, 0, 27, Hkv, D, "normal", np.zeros((2, Hkv, 0), np.int64), 1.0)
+    pair.append(torch.stack([k0, k0 * 0.5]), torch.stack([v0, v0 * 0.5]), t_per_seq=[27, 9])
+    pair.assert_cache_equal()
+    x, wk, wv = synth.projection_inputs(4, B, 120, hidden, Hkv, D)
+    pair.project(x, wk, wv, [120, 101])
+    pair.assert_cache_equal()
+    # and a plain append after the projected one
+    k1, v1 = synth.kv_tokens(5, 0, 0, 30, Hkv, D, "normal", np.zeros((2, Hkv, 0), np.int64), 1.0)
+    pair.append(torch.stack([k1, k1]), torch.stack([v1, v1]), t_per_seq=[30, 11])
+    pair.assert_cache_equal()
+
+
+def test_project_single_token_decode_appends():
+    B, Hkv, D, P, hidden = 3, 2, 128, 4, 64
+    pair = Pair(kvq.KVQ_FMT_CB2_OUTLIER, B, Hkv, D, P, seed=6)
+    x, wk, wv = synth.projection_inputs(6, B, 40, hidden, Hkv, D)
+    for t in range(40):
+        pair.project(x[:, t:t + 1].contiguous(), wk, wv, [1, 1 if t % 3 else 0, 1])
+    pair.assert_cache_equal()
+
+
+def test_project_rejects_bad_arguments():
+    pair = Pair(kvq.KVQ_FMT_INT4_G32, 1, 1, 64, 4, seed=0)
+    x, wk, wv = synth.projection_inputs(0, 1, 4, 64, 1, 64)
+    L = kvq.lib()
+    import ctypes
+    c, cc = ctypes.byref(pair.gpu.cfg), ctypes.byref(pair.gpu.c)
+    xp, kp, vp = x.cuda(), wk.cuda(), wv.cuda()
+    assert L.kvq_project_append(c, cc, xp.data_ptr(), 48, kp.data_ptr(), vp.data_ptr(), 4, None, None, None) == \
+        kvq.KVQ_ERR_INVALID_ARG   # hidden not a multiple of 32
+    assert L.kvq_project_append(c, cc, xp.data_ptr() + 2, 64, kp.data_ptr(), vp.data_ptr(), 4, None, None, None) == \
+        kvq.KVQ_ERR_INVALID_ARG   # misaligned x
+    assert L.kvq_project_append(c, cc, xp.data_ptr(), 64, kp.data_ptr(), vp.data_ptr(), 4 * 16 + 1, None, None,
+                                None) == kvq.KVQ_ERR_CAPACITY
+    assert L.kvq_project_append(c, cc, xp.data_ptr(), 64, kp.data_ptr(), vp.data_ptr(), 0, None, None, None) == \
+        kvq.KVQ_OK
