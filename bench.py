@@ -19,6 +19,7 @@ value sums the ranks' bytes over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -55,6 +56,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--append", action="store_true", help="also time kvq_quantize_append (1-token and prefill chunk)")
+    p.add_argument("--project", action="store_true",
+                   help="also time kvq_project_append against a cuBLAS projection + kvq_quantize_append")
+    p.add_argument("--project-only", action="store_true",
+                   help="time only the projection + append comparison (no decode cache, no decode timing)")
+    p.add_argument("--project-b", type=int, default=0, help="sequences for the projection timing (0: the workload's)")
     return p.parse_args()
 
 
@@ -381,6 +387,67 @@ def time_append(w: synth.Workload, dev) -> dict:
     return res
 
 
+# ----------------------------------------------------------------------------- fused projection timing (optional)
+def time_project(w: synth.Workload, dev, flush_mb: int, reps: int = 10, warmup: int = 3, B: int = 0) -> dict:
+    """K/V projection + quantize-on-append for every sequence of the workload,
+    hidden = Hq * D: the fused kvq_project_append against the unfused pair
+    (two cuBLAS bf16 GEMMs writing K and V in bf16, then kvq_quantize_append),
+    for a 4096-token prefill chunk and a 1-token append.  L2 flushed before
+    every timed call; CUDA events on the current stream."""
+    hidden = w.Hq * w.D
+    if B:
+        w = dataclasses.replace(w, B=B)
+    flush = L2Flush(flush_mb, dev)
+    res = {"hidden": hidden, "B": w.B, "l2": "flushed before every timed call"}
+
+    def timed(fn, c):
+        ts = []
+        for r in range(warmup + reps):
+            c.seq_lens.zero_()
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= warmup:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        return float(np.mean(ts))
+
+    for label, T in (("prefill_4096", 4096), ("1_token", 1)):
+        pages = -(-((T + 15) // 16) // 4) * 4
+        c = kvq.QuantizedKVCache(w.fmt, w.B, w.Hkv, w.D, pages, w.B * pages, 0, device=dev,
+                                 static_channels=w.static_channels)
+        x, wk, wv = synth.projection_inputs(0, w.B, T, hidden, w.Hkv, w.D, device=dev)
+        if w.fmt == synth.FMT_CB2S:
+            n = min(T, synth.CALIBRATION_TOKENS)
+            kc = torch.matmul(x[0, :n].float(), wk.float().t()).view(n, w.Hkv, w.D).contiguous()
+            vc = torch.matmul(x[0, :n].float(), wv.float().t()).view(n, w.Hkv, w.D).contiguous()
+            kvq.kvq_select_static_channels(c, kc, vc)
+
+        def unfused():
+            k = torch.matmul(x, wk.t()).view(w.B, T, w.Hkv, w.D)
+            v = torch.matmul(x, wv.t()).view(w.B, T, w.Hkv, w.D)
+            kvq.kvq_quantize_append(c, k, v)
+
+        def gemm_only():
+            torch.matmul(x, wk.t())
+            torch.matmul(x, wv.t())
+
+        k_pre = torch.matmul(x, wk.t()).view(w.B, T, w.Hkv, w.D)
+        v_pre = torch.matmul(x, wv.t()).view(w.B, T, w.Hkv, w.D)
+        t_f = timed(lambda: kvq.kvq_project_append(c, x, wk, wv), c)
+        t_u = timed(unfused, c)
+        t_g = timed(gemm_only, c)
+        t_a = timed(lambda: kvq.kvq_quantize_append(c, k_pre, v_pre), c)
+        flops = 2.0 * w.B * T * hidden * 2 * w.Hkv * w.D
+        res[label] = {"fused_us": t_f * 1e6, "unfused_us": t_u * 1e6, "cublas_gemms_us": t_g * 1e6,
+                      "append_bf16_us": t_a * 1e6, "fused_tflops": flops / t_f / 1e12,
+                      "speedup_vs_unfused": t_u / t_f}
+        del c, x, wk, wv, k_pre, v_pre
+    return res
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -404,6 +471,11 @@ def main():
         return
 
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.project_only:
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "format": FMT_NAME[w.fmt],
+                              "project": time_project(w, dev, args.flush_mb, B=args.project_b)}), flush=True)
+        return
     built = workloads.build(w, seed=args.seed + rank, device=dev)
     torch.cuda.synchronize()
     t = time_gpu(built, args, world, dev)
@@ -444,6 +516,8 @@ def main():
     line["config"]["partial_bytes_per_step"] = 2 * w.B * w.Hq * t["splits"] * (w.D + 2) * 4
     if args.append:
         line["append"] = time_append(w, dev)
+    if args.project:
+        line["project"] = time_project(w, dev, args.flush_mb, B=args.project_b)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = time_oracle(w, args.seed, args.cpu_seconds)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}

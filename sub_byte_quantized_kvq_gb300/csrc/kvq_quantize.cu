@@ -29,6 +29,8 @@ namespace kvq {
 enum { kSeqOk = 0, kSeqNothing = 1, kSeqCapacity = 2, kSeqBadPage = 3 };
 
 // Decide, identically in every launch, whether sequence b's append proceeds.
+// Every thread of the CTA calls it together: they share the page-table checks
+// (one strided pass) and agree on the answer.
 __device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) {
   start = a.seq_lens[b];
   n = a.t_per_seq ? a.t_per_seq[b] : a.t_new;
@@ -36,13 +38,15 @@ __device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) 
   if (n > a.t_new || start < 0 || (long long)start + n > (long long)a.ppsm * kPage) return kSeqCapacity;
   // a completed CB2 group rewrites all of its pages, including earlier ones
   const int first = a.fmt == KVQ_FMT_CB2_GROUP4 ? (start / (kPage * kGroupPages)) * kGroupPages : start / kPage;
-  for (int pg = first; pg <= (start + n - 1) / kPage; ++pg) {
+  const int last = (start + n - 1) / kPage;
+  int bad = 0;
+  for (int pg = first + (int)threadIdx.x; pg <= last; pg += (int)blockDim.x) {
     const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
     const bool ok = (u >> 31) ? (a.fmt == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages)
                               : phys < (uint32_t)a.num_pages;
-    if (!ok) return kSeqBadPage;
+    bad |= !ok;
   }
-  return kSeqOk;
+  return __syncthreads_or(bad) ? kSeqBadPage : kSeqOk;
 }
 
 __device__ __forceinline__ float load_in(const AppendArgs& a, int role, int b, int t, int h, int c, int D) {
@@ -658,11 +662,11 @@ __global__ void __launch_bounds__(256) append_stage_kernel(const AppendArgs a, i
 }
 
 // Advance seq_lens and report skipped sequences (after every other launch read them).
-__global__ void append_finish_kernel(const AppendArgs a) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= a.B) return;
+__global__ void __launch_bounds__(128) append_finish_kernel(const AppendArgs a) {
+  const int b = blockIdx.x;   // one CTA per sequence
   int start, n;
   const int st = seq_append_state(a, b, start, n);
+  if (threadIdx.x != 0) return;
   if (st == kSeqOk) a.seq_lens[b] = start + n;
   else if (st == kSeqCapacity) atomicOr(a.status, KVQ_STATUS_CAPACITY);
   else if (st == kSeqBadPage) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
@@ -730,7 +734,7 @@ static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
     append_page_kernel<D><<<grid, 128, 0, st>>>(a);
     append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
   }
-  append_finish_kernel<<<(a.B + 127) / 128, 128, 0, st>>>(a);
+  append_finish_kernel<<<a.B, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -1021,7 +1025,7 @@ static cudaError_t project_launch_k(const ProjArgs& p, cudaStream_t st) {
   const int units_max = (p.a.t_new + 2 * P::U - 2) / P::U;   // units a span of t_new positions can touch
   const dim3 grid((units_max + P::SPT - 1) / P::SPT, p.a.Hkv, p.a.B);
   project_append_kernel<KIND, D><<<grid, kPThreads, P::SMEM, st>>>(p);
-  append_finish_kernel<<<(p.a.B + 127) / 128, 128, 0, st>>>(p.a);
+  append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
   return cudaGetLastError();
 }
 
