@@ -49,11 +49,34 @@ __device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) 
   return __syncthreads_or(bad) ? kSeqBadPage : kSeqOk;
 }
 
-__device__ __forceinline__ float load_in(const AppendArgs& a, int role, int b, int t, int h, int c, int D) {
+// Channels [c, c + 8) of new token t (c a multiple of 8) as fp32 into dst[0..8):
+// one or two 16-byte loads when the input is 16-byte aligned (then every such
+// run is, D being a multiple of 8), else element loads.
+__device__ __forceinline__ void load_in8(const AppendArgs& a, int role, int b, int t, int h, int c, int D, float* dst) {
   const size_t i = (((size_t)b * a.t_new + t) * a.Hkv + h) * D + c;
-  if (a.in_dtype == KVQ_F32) return static_cast<const float*>(a.kv[role])[i];
-  if (a.in_dtype == KVQ_F16) return __half2float(static_cast<const __half*>(a.kv[role])[i]);
-  return __bfloat162float(static_cast<const __nv_bfloat16*>(a.kv[role])[i]);
+  const bool vec = (reinterpret_cast<uintptr_t>(a.kv[role]) & 15u) == 0;
+  if (a.in_dtype == KVQ_F32) {
+    const float* p = static_cast<const float*>(a.kv[role]) + i;
+    if (vec) {
+      const float4 u = reinterpret_cast<const float4*>(p)[0], w = reinterpret_cast<const float4*>(p)[1];
+      dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
+      dst[4] = w.x; dst[5] = w.y; dst[6] = w.z; dst[7] = w.w;
+    } else {
+      for (int j = 0; j < 8; ++j) dst[j] = p[j];
+    }
+    return;
+  }
+  const uint16_t* p = static_cast<const uint16_t*>(a.kv[role]) + i;
+  uint16_t hv[8];
+  if (vec) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    for (int j = 0; j < 4; ++j) { hv[2 * j] = (uint16_t)(w4[j] & 0xFFFFu); hv[2 * j + 1] = (uint16_t)(w4[j] >> 16); }
+  } else {
+    for (int j = 0; j < 8; ++j) hv[j] = p[j];
+  }
+  for (int j = 0; j < 8; ++j)
+    dst[j] = a.in_dtype == KVQ_F16 ? __half2float(__ushort_as_half(hv[j])) : __uint_as_float((uint32_t)hv[j] << 16);
 }
 
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
@@ -108,38 +131,60 @@ __device__ __forceinline__ int nearest4(float v, const float* c) {
   return best;
 }
 
-// Lloyd-Max 4-centroid fit of v[0..n) (n <= NMAX) in binary32; fp16 centroids and codes.
-template <int NMAX>
-__device__ void lloyd4(const float* v, int n, int iters, uint16_t* c16, uint8_t* codes) {
+// Lloyd-Max 4-centroid fit, in binary32, of the values x[r * xs] of the rows
+// r < NROWS set in `keep`, taken in row order: linspace(min, max, 4) start,
+// nearest centroid (lowest index on ties), at most `iters` assignment passes,
+// stop when an assignment repeats, centroid = mean of its values.  Returns the
+// fp16 centroids and, 2 bits per row, the code of each kept row (0 elsewhere).
+// Values are read from shared memory on every pass; assignments are packed 16
+// to a word, so the fit holds few registers.
+template <int NROWS>
+__device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
+                            uint32_t (&code)[(NROWS + 15) / 16]) {
+  constexpr int NW = (NROWS + 15) / 16;
   float c[4] = {0.f, 0.f, 0.f, 0.f};
-  if (n > 0) {
-    float mn = v[0], mx = v[0];
-    for (int i = 1; i < n; ++i) { mn = v[i] < mn ? v[i] : mn; mx = v[i] > mx ? v[i] : mx; }
+#pragma unroll
+  for (int w = 0; w < NW; ++w) code[w] = 0u;
+  if (keep) {
+    bool have = false;
+    float mn = 0.f, mx = 0.f;
+    for (int r = 0; r < NROWS; ++r) {
+      if (!(keep >> r & 1u)) continue;
+      const float v = x[r * xs];
+      if (!have) { mn = v; mx = v; have = true; }
+      mn = v < mn ? v : mn;
+      mx = v > mx ? v : mx;
+    }
     const float h = __fdiv_rn(mx - mn, 3.0f);
     c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0f * h; c[3] = mx;
-    uint8_t a[NMAX], prev[NMAX];
+    uint32_t prev[NW];
     bool have_prev = false;
     for (int it = 0; it < iters; ++it) {
+      uint32_t a[NW];
+#pragma unroll
+      for (int w = 0; w < NW; ++w) a[w] = 0u;
+      for (int r = 0; r < NROWS; ++r)
+        if (keep >> r & 1u) a[r >> 4] |= (uint32_t)nearest4(x[r * xs], c) << (2 * (r & 15));
       bool same = have_prev;
-      for (int i = 0; i < n; ++i) {
-        a[i] = (uint8_t)nearest4(v[i], c);
-        same = same && a[i] == prev[i];
-      }
+#pragma unroll
+      for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
       if (same) break;
-      for (int j = 0; j < 4; ++j) {
-        float s = 0.f;
+      for (int jj = 0; jj < 4; ++jj) {
+        float sum = 0.f;
         int cnt = 0;
-        for (int i = 0; i < n; ++i)
-          if (a[i] == j) { s += v[i]; ++cnt; }
-        if (cnt > 0) c[j] = __fdiv_rn(s, (float)cnt);
+        for (int r = 0; r < NROWS; ++r)
+          if ((keep >> r & 1u) && ((a[r >> 4] >> (2 * (r & 15))) & 3u) == (uint32_t)jj) { sum += x[r * xs]; ++cnt; }
+        if (cnt > 0) c[jj] = __fdiv_rn(sum, (float)cnt);
       }
-      for (int i = 0; i < n; ++i) prev[i] = a[i];
+#pragma unroll
+      for (int w = 0; w < NW; ++w) prev[w] = a[w];
       have_prev = true;
     }
   }
   float cf[4];
-  for (int j = 0; j < 4; ++j) { c16[j] = f32_to_f16_bits(c[j]); cf[j] = f16_bits_to_f32(c16[j]); }
-  for (int i = 0; i < n; ++i) codes[i] = (uint8_t)nearest4(v[i], cf);
+  for (int jj = 0; jj < 4; ++jj) { c16[jj] = f32_to_f16_bits(c[jj]); cf[jj] = f16_bits_to_f32(c16[jj]); }
+  for (int r = 0; r < NROWS; ++r)
+    if (keep >> r & 1u) code[r >> 4] |= (uint32_t)nearest4(x[r * xs], cf) << (2 * (r & 15));
 }
 
 // Element (t, c) held by fragment (lane, step, slot) -- the inverse of frag_pos.
@@ -154,79 +199,86 @@ __device__ __forceinline__ void frag_inverse(int role, int lane, int s, int k, i
 }
 
 // ----------------------------------------------------------------------------- per-token formats
-// INT4 group-32 quantization of token slot t by one warp (lane g < D/32 owns group g).
-template <int D>
-__device__ void quantize_token_int4(const float* x, int t, uint8_t (*codes)[D], uint8_t* blk, double sigma, int lane) {
+// INT4 group-32 quantization of token slots [t0, min(t0 + 32 / NG, hi)) by one
+// warp (NG = D / 32 groups): lane s * NG + g owns group g of slot t0 + s.
+// Lanes past hi compute on slot t0 but store nothing; t0 < hi.
+template <int D, int XS>
+__device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
+                                     double sigma, int lane) {
   constexpr int NG = D / 32, CAP = int4_cap(D);
+  const int g = lane % NG, t = t0 + lane / NG;
+  const bool act = t < hi;
+  const float* xg = xs[act ? t : t0] + 32 * g;
   uint8_t mask[32];
-  int cnt = 0;
-  if (lane < NG) {
-    const float* xg = x + 32 * lane;
-    outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
-    bool have = false;
-    float mn = 0.f, mx = 0.f;
-    for (int i = 0; i < 32; ++i) {
-      if (mask[i]) continue;
-      const float v = xg[i];
-      if (!have || v < mn) mn = v;
-      if (!have || v > mx) mx = v;
-      have = true;
-    }
-    const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 15.0f)) : 0;
-    const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
-    const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
-    for (int i = 0; i < 32; ++i) {
-      uint8_t q = 0;
-      if (mask[i]) {
-        ++cnt;
-      } else if (S != 0.f) {
-        float r = rintf(__fdiv_rn(xg[i] - m, S));
-        r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
-        q = (uint8_t)r;
-      }
-      codes[t][32 * lane + i] = q;
-    }
-    uint8_t* sz = blk + int4_sz_off(D) + 4 * (t * NG + lane);
-    *reinterpret_cast<uint16_t*>(sz) = S16;
-    *reinterpret_cast<uint16_t*>(sz + 2) = m16;
+  outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
+  bool have = false;
+  float mn = 0.f, mx = 0.f;
+  for (int i = 0; i < 32; ++i) {
+    if (mask[i]) continue;
+    const float v = xg[i];
+    if (!have || v < mn) mn = v;
+    if (!have || v > mx) mx = v;
+    have = true;
   }
-  // entries of group g go after those of groups < g (ascending channel order)
+  const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 15.0f)) : 0;
+  const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
+  const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
+  int cnt = 0;
+  for (int i = 0; i < 32; ++i) {
+    uint8_t q = 0;
+    if (mask[i]) {
+      ++cnt;
+    } else if (S != 0.f) {
+      float r = rintf(__fdiv_rn(xg[i] - m, S));
+      r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
+      q = (uint8_t)r;
+    }
+    if (act) codes[t][32 * g + i] = q;
+  }
+  // entries of group g go after those of groups < g of the same token (ascending channel order)
   int off = cnt;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, off, d);
-    if (lane >= d) off += y;
+  for (int d = 1; d < NG; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, off, d, NG);
+    if (g >= d) off += y;
   }
-  const int total = __shfl_sync(0xffffffffu, off, NG - 1);
+  const int total = __shfl_sync(0xffffffffu, off, NG - 1, NG);
   off -= cnt;
+  if (!act) return;
+  uint8_t* sz = blk + int4_sz_off(D) + 4 * (t * NG + g);
+  *reinterpret_cast<uint16_t*>(sz) = S16;
+  *reinterpret_cast<uint16_t*>(sz + 2) = m16;
   uint8_t* chans = blk + int4_ch_off(D) + t * CAP;
   uint16_t* vals = reinterpret_cast<uint16_t*>(blk + int4_val_off(D)) + t * CAP;
-  if (lane < NG) {
-    for (int i = 0; i < 32; ++i)
-      if (mask[i]) {
-        chans[off] = (uint8_t)(32 * lane + i);
-        vals[off] = __half_as_ushort(__float2half_rn(x[32 * lane + i]));
-        ++off;
-      }
-  }
-  for (int i = total + lane; i < CAP; i += 32) {
+  for (int i = 0; i < 32; ++i)
+    if (mask[i]) {
+      chans[off] = (uint8_t)(32 * g + i);
+      vals[off] = __half_as_ushort(__float2half_rn(xg[i]));
+      ++off;
+    }
+  for (int i = total + g; i < CAP; i += NG) {
     chans[i] = 0;
     vals[i] = 0;
   }
-  if (lane == 0) blk[int4_cnt_off(D) + t] = (uint8_t)total;
+  if (g == 0) blk[int4_cnt_off(D) + t] = (uint8_t)total;
 }
 
-// E2M1 quantization of token slot t by one warp (lane s < D/16 owns 16 channels).
-template <int D>
-__device__ void quantize_token_e2m1(const float* x, int t, uint8_t (*codes)[D], uint8_t* blk, int lane) {
-  if (lane >= D / 16) return;
-  const float* xs = x + 16 * lane;
+// E2M1 quantization of token slots [t0, min(t0 + 32 / NS, hi)) by one warp
+// (NS = D / 16 scale groups): lane s * NS + g owns channels [16 g, 16 g + 16)
+// of slot t0 + s.
+template <int D, int XS>
+__device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
+                                     int lane) {
+  constexpr int NS = D / 16;
+  const int g = lane % NS, t = t0 + lane / NS;
+  if (t >= hi) return;
+  const float* x = xs[t] + 16 * g;
   float amax = 0.f;
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
   const float sc = e4m3_to_f32(s8);
-  for (int i = 0; i < 16; ++i) codes[t][16 * lane + i] = sc != 0.f ? f32_to_e2m1(__fdiv_rn(xs[i], sc)) : 0;
-  blk[e2m1_sc_off(D) + 16 * lane + t] = s8;
+  for (int i = 0; i < 16; ++i) codes[t][16 * g + i] = sc != 0.f ? f32_to_e2m1(__fdiv_rn(x[i], sc)) : 0;
+  blk[e2m1_sc_off(D) + 16 * g + t] = s8;
 }
 
 // Threads [0, n) of a group of a CTA (tid is the index within the group, n a
@@ -247,19 +299,26 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
                                    uint8_t* blk, uint8_t (*codes)[D], const Grp& g) {
   constexpr int kStride = block_stride(BF, D), NS = D / 16;
   const int lane = g.tid & 31, warp = g.tid >> 5, nw = g.n >> 5;
-  for (int i = g.tid; i < kStride / 16; i += g.n)
-    reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(gblk)[i];
-  g.sync();
-  for (int i = g.tid; i < 32 * NS * 8; i += g.n) {
-    const int ln = i / (NS * 8), s = (i / 8) % NS, k = i % 8;
-    int t, c;
-    frag_inverse(role, ln, s, k, t, c);
-    codes[t][c] = (blk[4 * NS * ln + 4 * s + k / 2] >> (4 * (k & 1))) & 0xF;
+  // a block whose 16 slots are all rewritten keeps nothing of its old
+  // contents: start it from zeros (its padding included) instead of unpacking
+  if (lo > 0 || hi < kPage) {
+    for (int i = g.tid; i < kStride / 16; i += g.n)
+      reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(gblk)[i];
+    g.sync();
+    for (int i = g.tid; i < 32 * NS * 8; i += g.n) {
+      const int ln = i / (NS * 8), s = (i / 8) % NS, k = i % 8;
+      int t, c;
+      frag_inverse(role, ln, s, k, t, c);
+      codes[t][c] = (blk[4 * NS * ln + 4 * s + k / 2] >> (4 * (k & 1))) & 0xF;
+    }
+  } else {
+    for (int i = g.tid; i < kStride / 16; i += g.n) reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
   }
   g.sync();
-  for (int t = lo + warp; t < hi; t += nw) {
-    if (BF == kBlkInt4) quantize_token_int4<D>(xs[t], t, codes, blk, a.sigma, lane);
-    else quantize_token_e2m1<D>(xs[t], t, codes, blk, lane);
+  constexpr int TPW = 32 / (BF == kBlkInt4 ? D / 32 : D / 16);   // token slots per warp pass
+  for (int t0 = lo + warp * TPW; t0 < hi; t0 += nw * TPW) {
+    if (BF == kBlkInt4) quantize_tokens_int4<D, XS>(xs, t0, hi, codes, blk, a.sigma, lane);
+    else quantize_tokens_e2m1<D, XS>(xs, t0, hi, codes, blk, lane);
   }
   g.sync();
   for (int i = g.tid; i < 32 * NS; i += g.n) {
@@ -279,11 +338,11 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
 }
 
 template <int BF, int D>
-__global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(256, 4) append_token_kernel(const AppendArgs a) {
   constexpr int kStride = block_stride(BF, D);
   __shared__ __align__(16) uint8_t blk[kStride];
   __shared__ uint8_t codes[16][D];
-  __shared__ float xs[16][D];
+  __shared__ __align__(16) float xs[16][D];
   const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
   const int tid = threadIdx.x;
   int start, n;
@@ -293,9 +352,9 @@ __global__ void __launch_bounds__(256) append_token_kernel(const AppendArgs a) {
   const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
   const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
   uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
-  for (int i = tid; i < (hi - lo) * D; i += blockDim.x) {
-    const int tt = i / D, c = i - tt * D;
-    xs[(lo % kPage) + tt][c] = load_in(a, role, b, lo + tt - start, h, c, D);
+  for (int i = tid; i < (hi - lo) * (D / 8); i += blockDim.x) {
+    const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8));
+    load_in8(a, role, b, lo + tt - start, h, c, D, &xs[(lo % kPage) + tt][c]);
   }
   token_block_update<BF, D, D>(a, role, xs, lo % kPage, lo % kPage + (hi - lo), gblk, blk, codes, whole_cta());
 }
@@ -451,12 +510,10 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
       if (mask[0][c]) {
         for (int t = 0; t < 16; ++t) codes[t][c] = 0;   // all-zero centroids from the block clear
       } else {
-        float v[16];
-        uint8_t cc[16];
+        uint32_t cc[1];
         uint16_t c16[4];
-        for (int t = 0; t < 16; ++t) v[t] = xs[t][c];
-        lloyd4<16>(v, 16, a.iters, c16, cc);
-        for (int t = 0; t < 16; ++t) codes[t][c] = cc[t];
+        lloyd4_rows<16>(&xs[0][c], XS, 0xFFFFull, a.iters, c16, cc);
+        for (int t = 0; t < 16; ++t) codes[t][c] = (cc[0] >> (2 * t)) & 3u;
         uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
         for (int jj = 0; jj < 4; ++jj) {
           cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
@@ -507,15 +564,12 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
       *reinterpret_cast<uint16_t*>(blk + a3_m_off(D) + 2 * r) = m16;
     } else if (tid < D) {
       const int c = tid;
-      float v[16];
-      uint8_t cc[16];
+      uint32_t cc[1];
       uint16_t c16[4];
-      int nv = 0;
-      for (int t = 0; t < 16; ++t)
-        if (!mask[t][c]) v[nv++] = xs[t][c];
-      lloyd4<16>(v, nv, a.iters, c16, cc);
-      nv = 0;
-      for (int t = 0; t < 16; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];
+      uint64_t keep = 0;
+      for (int t = 0; t < 16; ++t) keep |= (uint64_t)(mask[t][c] == 0) << t;
+      lloyd4_rows<16>(&xs[0][c], XS, keep, a.iters, c16, cc);
+      for (int t = 0; t < 16; ++t) codes[t][c] = (cc[0] >> (2 * t)) & 3u;
       uint8_t* cbp = blk + cb2_cb_off(D) + 8 * cb2_slot(role, c);
       for (int jj = 0; jj < 4; ++jj) {
         cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
@@ -534,8 +588,8 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
-  __shared__ float xs[16][D];
+__global__ void __launch_bounds__(128, 8) append_page_kernel(const AppendArgs a) {
+  __shared__ __align__(16) float xs[16][D];
   __shared__ uint8_t mask[16][D];
   __shared__ uint8_t codes[16][D];
   __shared__ __align__(16) uint8_t blk[page_blk_bytes<D>()];
@@ -548,9 +602,13 @@ __global__ void __launch_bounds__(128) append_page_kernel(const AppendArgs a) {
   if (pg * kPage + kPage > end) return;  // only pages this append completes
   const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg];
   const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
-  for (int i = tid; i < 16 * D; i += blockDim.x) {
-    const int t = i / D, c = i - t * D, pos = pg * kPage + t;
-    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
+  for (int i = tid; i < 16 * (D / 8); i += blockDim.x) {
+    const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = pg * kPage + t;
+    if (pos < start) {
+      for (int j = 0; j < 8; ++j) xs[t][c + j] = stg[t * D + c + j];
+    } else {
+      load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+    }
   }
   page_quantize<D, D>(a, h, role, u, xs, PageWs<D>{mask, codes, blk, red}, whole_cta());
 }
@@ -582,15 +640,12 @@ __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32
   g.sync();
   if (tid < D) {
     const int c = tid;
-    float v[GT];
-    uint8_t cc[GT];
+    uint32_t cc[GT / 16];
     uint16_t c16[4];
-    int nv = 0;
-    for (int t = 0; t < GT; ++t)
-      if (!mask[t][c]) v[nv++] = xs[t][c];
-    lloyd4<GT>(v, nv, a.iters, c16, cc);
-    nv = 0;
-    for (int t = 0; t < GT; ++t) codes[t][c] = mask[t][c] ? 0 : cc[nv++];
+    uint64_t keep = 0;
+    for (int t = 0; t < GT; ++t) keep |= (uint64_t)(mask[t][c] == 0) << t;
+    lloyd4_rows<GT>(&xs[0][c], XS, keep, a.iters, c16, cc);
+    for (int t = 0; t < GT; ++t) codes[t][c] = (cc[t >> 4] >> (2 * (t & 15))) & 3u;
     uint8_t* cbp = blk + 8 * cb2_slot(role, c);   // the codebook sits at the start of the group's first block
     for (int jj = 0; jj < 4; ++jj) {
       cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
@@ -631,9 +686,13 @@ __global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
   const int end = start + n, gr = start / GT + j;
   if (gr * GT + GT > end) return;  // only groups this append completes
   const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
-  for (int i = tid; i < GT * D; i += blockDim.x) {
-    const int t = i / D, c = i - t * D, pos = gr * GT + t;
-    xs[t][c] = pos < start ? stg[t * D + c] : load_in(a, role, b, pos - start, h, c, D);
+  for (int i = tid; i < GT * (D / 8); i += blockDim.x) {
+    const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = gr * GT + t;
+    if (pos < start) {
+      for (int j = 0; j < 8; ++j) xs[t][c + j] = stg[t * D + c + j];
+    } else {
+      load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+    }
   }
   group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{mask, codes, blk},
                        whole_cta());
@@ -655,9 +714,11 @@ __global__ void __launch_bounds__(256) append_stage_kernel(const AppendArgs a, i
   if (end % rows == 0) return;
   const int lo = max(start, (end / rows) * rows);
   float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * rows * D;
-  for (int i = threadIdx.x; i < (end - lo) * D; i += blockDim.x) {
-    const int tt = i / D, c = i - tt * D, pos = lo + tt;
-    stg[(pos % rows) * D + c] = load_in(a, role, b, pos - start, h, c, D);
+  for (int i = threadIdx.x; i < (end - lo) * (D / 8); i += blockDim.x) {
+    const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8)), pos = lo + tt;
+    float v[8];
+    load_in8(a, role, b, pos - start, h, c, D, v);
+    for (int j = 0; j < 8; ++j) stg[(pos % rows) * D + c + j] = v[j];
   }
 }
 
@@ -754,16 +815,20 @@ cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st) {
 // One CTA (512 threads) per (tile of 128 sequence positions, kv head,
 // sequence) computes K and V together (N = 2 D accumulator columns).  Tile
 // rows are whole pages (4-page groups for the CB2 group format), so each block
-// is written by one CTA.  Operands are staged with cp.async into the K-major,
-// no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix), three
-// stages of 32 columns of the hidden dimension; one thread issues the MMAs and
-// commits each stage to an mbarrier.  The epilogue reads the accumulators
+// is written by one CTA.  Warp 0 streams the operands with TMA (one 2-D box
+// per unit of x rows, one per weight matrix; 128-byte swizzle, 64 hidden
+// columns per stage) into a ring of shared-memory stages; warp 1 issues the
+// MMAs of each stage and commits it back to the producer; the other warps
+// sleep on the accumulator's mbarrier.  The epilogue reads the accumulators
 // with tcgen05.ld into an fp32 tile in shared memory and runs the same
 // per-token / per-page / per-group quantizers as kvq_quantize_append.
 namespace tc {
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);   // SWIZZLE_NONE, version 1
+// Shared-memory matrix descriptor, K-major with 128-byte swizzle: rows of
+// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), leading byte
+// offset unused (1), descriptor version 1, layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
 }
 // kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 accumulator, M x N
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
@@ -794,22 +859,23 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
-// 16-byte global -> shared copy; src_bytes = 0 fills zeros.
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+// 2-D TMA load of one box (x = column in elements, y = row; rows outside the
+// tensor read as zeros) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 }  // namespace tc
 
 // Fused projection plan: a tile is kPM rows (sequence positions, whole units
 // of U rows: pages, or 4-page groups for the CB2 group format) x N = 2 D
 // columns (K then V of one kv head) in TMEM; the hidden dimension streams
-// through kPStages shared-memory stages of kPK columns.
+// through S stages of kPK columns (A: kPM rows, B: N rows, 128 bytes each).
 enum { kProjInt4 = 0, kProjE2m1 = 1, kProjPage = 2, kProjGroup = 3 };
-constexpr int kPM = 128, kPK = 32, kPStages = 3, kPThreads = 512;
-static_assert(kPK == 32, "the operand staging maps 4 core matrices per row group");
+constexpr int kPM = 128, kPK = 64, kPThreads = 512;
 
 template <int KIND, int D>
 struct ProjPlan {
@@ -819,20 +885,21 @@ struct ProjPlan {
   static constexpr int GS = kPThreads / NB;                                   // threads per unit group
   static constexpr int N = 2 * D;                                             // TMEM columns: K | V
   static constexpr int XS = D + 4;  // row stride of the fp32 tile: rows start 4 banks apart
+  static constexpr int S = D == 128 ? 2 : 3;                                  // operand stages
   static constexpr int A_BYTES = kPM * kPK * 2, B_BYTES = N * kPK * 2, STAGE = A_BYTES + B_BYTES;
-  static constexpr int R0 = kPStages * STAGE > kPM * XS * 4 ? kPStages * STAGE : kPM * XS * 4;
   static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
                           : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
                           : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
                                                 : kGroupPages * block_stride(kBlkCb2g, D) + 128 * D;
   static constexpr int WSR = (WS + 127) / 128 * 128;
-  static constexpr int SMEM = R0 + NB * WSR + kPM * 4 + kPStages * 8 + 16;
+  static constexpr int EPI = kPM * XS * 4 + NB * WSR;   // the epilogue's fp32 tile and scratch
+  static constexpr int R0 = S * STAGE > EPI ? S * STAGE : EPI;
+  static constexpr int SMEM = 1024 + R0 + kPM * 4 + (2 * S + 1) * 8 + 16;   // 1024: alignment slack
 };
 
 #define KVQ_PLAN_FITS(K, D_)                                                                          \
   static_assert(ProjPlan<K, D_>::SMEM <= 227 * 1024 && ProjPlan<K, D_>::N <= 256 &&                     \
-                    ProjPlan<K, D_>::R0 >= kPM * ProjPlan<K, D_>::XS * 4 &&                           \
-                    ProjPlan<K, D_>::R0 >= kPStages * ProjPlan<K, D_>::STAGE,                          \
+                    ProjPlan<K, D_>::STAGE % 1024 == 0 && ProjPlan<K, D_>::A_BYTES % 1024 == 0,        \
                 "fused projection plan does not fit")
 KVQ_PLAN_FITS(kProjInt4, 64);
 KVQ_PLAN_FITS(kProjInt4, 128);
@@ -845,10 +912,10 @@ KVQ_PLAN_FITS(kProjGroup, 128);
 #undef KVQ_PLAN_FITS
 
 template <int KIND, int D>
-__global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const ProjArgs p) {
+__global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __grid_constant__ ProjArgs p) {
   using P = ProjPlan<KIND, D>;
-  constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS;
-  extern __shared__ __align__(1024) uint8_t psm[];
+  constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS, S = P::S;
+  extern __shared__ __align__(1024) uint8_t psm_raw[];
   const AppendArgs& a = p.a;
   const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -867,18 +934,26 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const Proj
   };
   if (unit_of(0) < 0) return;
 
+  // 1024-byte aligned base: the swizzled stages need it
+  uint8_t* psm = psm_raw + (((smem_u32(psm_raw) + 1023u) & ~1023u) - smem_u32(psm_raw));
   float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(psm);   // the fp32 tile, once the stages are done
-  uint8_t* ws = psm + P::R0;
-  int* rowtok = reinterpret_cast<int*>(ws + NB * P::WSR);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(rowtok + kPM);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + kPStages);
+  uint8_t* ws = psm + kPM * XS * 4;
+  int* rowtok = reinterpret_cast<int*>(psm + P::R0);
+  uint64_t* full = reinterpret_cast<uint64_t*>(rowtok + kPM);   // [S]: a stage's bytes have landed
+  uint64_t* empty = full + S;                                    // [S]: a stage's MMAs are done
+  uint64_t* done = empty + S;                                    // every MMA is done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
 
   for (int r = tid; r < kPM; r += kPThreads) {
     const int u = unit_of(r / U), pos = u * U + r % U;
     rowtok[r] = u >= 0 && pos >= start && pos < end ? pos - start : -1;
   }
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) mbar_init(&mbar[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -890,59 +965,53 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const Proj
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
-
-  // Stage kc: x rows (zeros for rows without a token) and the K|V weight rows
-  // of head h, columns [kPK kc, kPK kc + kPK).  16-byte chunk i sits at 16 i:
-  // row group i / 32, core matrix (i / 8) % 4 along K, row i % 8.
-  const __nv_bfloat16* xb = p.x + (size_t)b * a.t_new * p.hidden;
-  const int nk = p.hidden / kPK;
-  auto issue = [&](int kc) {
-    const uint32_t sa = smem_u32(psm + (kc % kPStages) * P::STAGE), sb = sa + P::A_BYTES;
-    const int k0 = kc * kPK;
-    for (int i = tid; i < kPM * kPK / 8; i += kPThreads) {
-      const int r = (i >> 5) * 8 + (i & 7), kcr = (i >> 3) & 3, tt = rowtok[r];
-      const __nv_bfloat16* src = tt >= 0 ? xb + (size_t)tt * p.hidden + k0 + 8 * kcr : p.x;
-      tc::cp16(sa + 16 * i, src, tt >= 0 ? 16u : 0u);
-    }
-    for (int i = tid; i < N * kPK / 8; i += kPThreads) {
-      const int r = (i >> 5) * 8 + (i & 7), kcr = (i >> 3) & 3, role = r >= D;
-      tc::cp16(sb + 16 * i, p.w[role] + ((size_t)h * D + (r - role * D)) * p.hidden + k0 + 8 * kcr, 16u);
-    }
-  };
-  // K-major, no swizzle: core matrices 128 B apart along K (LBO), 8-row groups
-  // 512 B apart (SBO); one MMA covers K = 16, i.e. two core matrices.
-  const uint32_t idesc = tc::idesc_bf16(kPM, N);
+  const int nk = (p.hidden + kPK - 1) / kPK;
   bool ok = true;
-  for (int s = 0; s < kPStages - 1; ++s) {
-    if (s < nk) issue(s);
-    tc::cp_commit();
-  }
-  for (int kc = 0; kc < nk; ++kc) {
-    const int nxt = kc + kPStages - 1;
-    if (nxt < nk) {
-      // stage nxt % kPStages was last read by the MMAs of slice kc - 1
-      if (kc >= 1 && ok && !mbar_wait_bounded(&mbar[(kc - 1) % kPStages], ((kc - 1) / kPStages) & 1, kWaitLimitNs))
-        ok = false;
-      issue(nxt);
+
+  if (tid == 0) {
+    // producer: stage kc = the x rows of every unit of the tile (one box per
+    // unit; rows of other sequences or past the end are never used) and the
+    // K | V weight rows of head h, hidden columns [kPK kc, kPK kc + kPK)
+    int nvalid = 0;
+    for (int s = 0; s < SPT; ++s) nvalid += unit_of(s) >= 0;
+    const uint32_t bytes = (uint32_t)(nvalid * U * kPK * 2 + P::B_BYTES);
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      const int s = kc % S;
+      if (kc >= S && !mbar_wait_bounded(&empty[s], (kc / S - 1) & 1, kWaitLimitNs)) ok = false;
+      if (!ok) break;
+      uint8_t* st = psm + s * P::STAGE;
+      mbar_arrive_expect_tx(&full[s], bytes);
+      for (int sl = 0; sl < SPT; ++sl) {
+        const int u = unit_of(sl);
+        if (u >= 0) tc::tma2d(st + sl * U * kPK * 2, &p.tm_x, kPK * kc, b * a.t_new + (u * U - start), &full[s]);
+      }
+      tc::tma2d(st + P::A_BYTES, &p.tm_w[0], kPK * kc, h * D, &full[s]);
+      tc::tma2d(st + P::A_BYTES + D * kPK * 2, &p.tm_w[1], kPK * kc, h * D, &full[s]);
     }
-    tc::cp_commit();
-    tc::cp_wait<kPStages - 1>();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // cp.async data -> the tensor core's view
-    __syncthreads();
-    if (tid == 0) {
+  } else if (tid == 32) {
+    // MMA issuer: kPK / 16 MMAs per stage, the stage handed back on completion
+    const uint32_t idesc = tc::idesc_bf16(kPM, N);
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      const int s = kc % S;
+      if (!mbar_wait_bounded(&full[s], (kc / S) & 1, kWaitLimitNs)) { ok = false; break; }
       tc::fence_after();
-      const uint32_t sa = smem_u32(psm + (kc % kPStages) * P::STAGE), sb = sa + P::A_BYTES;
+      const uint32_t sa = smem_u32(psm + s * P::STAGE), sb = sa + P::A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < kPK / 16; ++kk)
-        tc::mma(tmem, tc::smem_desc(sa + 256 * kk, 128, 512), tc::smem_desc(sb + 256 * kk, 128, 512), idesc,
-                (kc | kk) != 0);
-      tc::commit(&mbar[kc % kPStages]);
+        tc::mma(tmem, tc::desc_sw128(sa + 32 * kk), tc::desc_sw128(sb + 32 * kk), idesc, (kc | kk) != 0);
+      tc::commit(&empty[s]);
     }
+    tc::commit(done);
   }
-  const bool done =
-      ok && mbar_wait_bounded(&mbar[(nk - 1) % kPStages], ((nk - 1) / kPStages) & 1, kWaitLimitNs);
-  tc::cp_wait<0>();
-  const bool all_ok = __syncthreads_and(done) != 0;
+  // everyone: sleep until the accumulators are complete
+  {
+    bool got = false;
+    const uint64_t t0 = global_timer_ns();
+    while (!(got = mbar_try_wait_sleep(done, 0, 1000000u)))
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    ok = ok && got;
+  }
+  const bool all_ok = __syncthreads_and(ok) != 0;
   tc::fence_after();
   if (all_ok) {
     const int grp = warp / (GS / 32);
@@ -1012,13 +1081,50 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const Proj
   tc::fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
-  if (tid == 0)
-    for (int s = 0; s < kPStages; ++s) mbar_inval(&mbar[s]);
+  if (tid == 0 && all_ok) {   // after a timeout a late arrival may still be pending: leave them
+    for (int s = 0; s < S; ++s) {
+      mbar_inval(&full[s]);
+      mbar_inval(&empty[s]);
+    }
+    mbar_inval(done);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Row-major bf16 [rows][cols] matrix, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+static bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows}, strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kPK, box_rows}, es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int KIND, int D>
-static cudaError_t project_launch_k(const ProjArgs& p, cudaStream_t st) {
+static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
   using P = ProjPlan<KIND, D>;
+  if (!encode_rows(&p.tm_x, p.x, (uint64_t)p.a.B * p.a.t_new, (uint64_t)p.hidden, (uint32_t)P::U) ||
+      !encode_rows(&p.tm_w[0], p.w[0], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D) ||
+      !encode_rows(&p.tm_w[1], p.w[1], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D))
+    return cudaErrorInvalidValue;
   const cudaError_t e =
       cudaFuncSetAttribute(project_append_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
   if (e != cudaSuccess) return e;
@@ -1030,7 +1136,7 @@ static cudaError_t project_launch_k(const ProjArgs& p, cudaStream_t st) {
 }
 
 template <int D>
-static cudaError_t project_launch_d(const ProjArgs& p, cudaStream_t st) {
+static cudaError_t project_launch_d(ProjArgs& p, cudaStream_t st) {
   switch (p.a.fmt) {
     case KVQ_FMT_INT4_G32: return project_launch_k<kProjInt4, D>(p, st);
     case KVQ_FMT_FP4_E2M1_S16: return project_launch_k<kProjE2m1, D>(p, st);
@@ -1039,7 +1145,7 @@ static cudaError_t project_launch_d(const ProjArgs& p, cudaStream_t st) {
   }
 }
 
-cudaError_t project_append_launch(const ProjArgs& p, int D, cudaStream_t st) {
+cudaError_t project_append_launch(ProjArgs& p, int D, cudaStream_t st) {
   return D == 64 ? project_launch_d<64>(p, st) : project_launch_d<128>(p, st);
 }
 
