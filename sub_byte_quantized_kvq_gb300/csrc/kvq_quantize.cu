@@ -99,18 +99,24 @@ __device__ __forceinline__ uint8_t f32_to_e2m1(float x) {
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Outlier mask of one vector (binary32, ascending order): |x - mu| > sigma * s,
-// s the unbiased standard deviation; at most kmax kept (lowest indices).
-__device__ int outlier_mask(const float* x, int n, int stride, float sigma, int kmax, uint8_t* mask, int mstride) {
+// Outlier statistics of one vector (binary32, ascending order): mean mu and
+// threshold sigma * s, s the unbiased standard deviation.
+__device__ __forceinline__ void outlier_stats(const float* x, int n, int stride, float sigma, float& mu, float& thr) {
   float sum = 0.f;
   for (int i = 0; i < n; ++i) sum += x[i * stride];
-  const float mu = __fdiv_rn(sum, (float)n);
+  mu = __fdiv_rn(sum, (float)n);
   float ss = 0.f;
   for (int i = 0; i < n; ++i) {
     const float d = x[i * stride] - mu;
     ss += d * d;
   }
-  const float thr = sigma * __fsqrt_rn(__fdiv_rn(ss, (float)(n - 1)));
+  thr = sigma * __fsqrt_rn(__fdiv_rn(ss, (float)(n - 1)));
+}
+
+// Outlier mask of one vector: |x - mu| > sigma * s; at most kmax kept (lowest indices).
+__device__ int outlier_mask(const float* x, int n, int stride, float sigma, int kmax, uint8_t* mask, int mstride) {
+  float mu, thr;
+  outlier_stats(x, n, stride, sigma, mu, thr);
   int k = 0;
   for (int i = 0; i < n; ++i) {
     int out = fabsf(x[i * stride] - mu) > thr;
@@ -119,6 +125,25 @@ __device__ int outlier_mask(const float* x, int n, int stride, float sigma, int 
     k += out;
   }
   return k;
+}
+
+// The same decisions for one row of D values as bits: bit c % 32 of
+// bits[c / 32] is set for an outlier channel c.
+template <int D>
+__device__ void outlier_bits(const float* x, float sigma, int kmax, uint32_t* bits) {
+  float mu, thr;
+  outlier_stats(x, D, 1, sigma, mu, thr);
+  int k = 0;
+  for (int w = 0; w < D / 32; ++w) {
+    uint32_t m = 0;
+    for (int j = 0; j < 32; ++j) {
+      int out = fabsf(x[32 * w + j] - mu) > thr;
+      if (out && k >= kmax) out = 0;
+      m |= (uint32_t)out << j;
+      k += out;
+    }
+    bits[w] = m;
+  }
 }
 
 __device__ __forceinline__ int nearest4(float v, const float* c) {
@@ -465,7 +490,7 @@ struct PageWs {
 // The caller's writes of xs come before the call.
 template <int D, int XS>
 __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, const float (*xs)[XS],
-                              const PageWs<D>& ws, const Grp& g) {
+                              const PageWs<D>& ws, const Grp& g, const uint32_t* rbits = nullptr) {
   constexpr int NS = D / 16, kBlk = page_blk_bytes<D>();
   constexpr int kCb2 = block_stride(kBlkCb2, D), kFp8 = block_stride(kBlkFp8, D);
   uint8_t(*mask)[D] = ws.mask;
@@ -534,7 +559,12 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
     // CB2 or ASYM3: per-token outliers, then per channel a codebook (CB2) or an
     // 8-level affine grid (ASYM3) over the non-outliers
     const bool a3 = a.fmt == KVQ_FMT_ASYM3_OUTLIER;
-    if (tid < 16) outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+    if (rbits) {   // decisions taken beforehand (outlier_bits), one row of D / 32 words per token
+      for (int i = tid; i < 16 * D; i += g.n)
+        mask[i / D][i % D] = (uint8_t)((rbits[(i / D) * (D / 32) + (i % D) / 32] >> (i % 32)) & 1u);
+    } else if (tid < 16) {
+      outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+    }
     g.sync();
     if (tid < D && a3) {
       const int c = tid;
@@ -627,7 +657,7 @@ struct GroupWs {
 // first page), codes and side-list per page.
 template <int D, int XS>
 __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32_t* pt, int gr, const float (*xs)[XS],
-                               const GroupWs<D>& ws, const Grp& g) {
+                               const GroupWs<D>& ws, const Grp& g, const uint32_t* rbits = nullptr) {
   constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D);
   uint8_t(*mask)[D] = ws.mask;
   uint8_t(*codes)[D] = ws.codes;
@@ -636,7 +666,12 @@ __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32
   for (int i = tid; i < kGroupPages * kStride / 16; i += g.n)
     reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
   g.sync();
-  if (tid < GT) outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+  if (rbits) {
+    for (int i = tid; i < GT * D; i += g.n)
+      mask[i / D][i % D] = (uint8_t)((rbits[(i / D) * (D / 32) + (i % D) / 32] >> (i % 32)) & 1u);
+  } else if (tid < GT) {
+    outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+  }
   g.sync();
   if (tid < D) {
     const int c = tid;
@@ -894,7 +929,7 @@ struct ProjPlan {
   static constexpr int WSR = (WS + 127) / 128 * 128;
   static constexpr int EPI = kPM * XS * 4 + NB * WSR;   // the epilogue's fp32 tile and scratch
   static constexpr int R0 = S * STAGE > EPI ? S * STAGE : EPI;
-  static constexpr int SMEM = 1024 + R0 + kPM * 4 + (2 * S + 1) * 8 + 16;   // 1024: alignment slack
+  static constexpr int SMEM = 1024 + R0 + kPM * 4 + kPM * D / 8 + (2 * S + 1) * 8 + 16;   // 1024: alignment slack
 };
 
 #define KVQ_PLAN_FITS(K, D_)                                                                          \
@@ -939,7 +974,8 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
   float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(psm);   // the fp32 tile, once the stages are done
   uint8_t* ws = psm + kPM * XS * 4;
   int* rowtok = reinterpret_cast<int*>(psm + P::R0);
-  uint64_t* full = reinterpret_cast<uint64_t*>(rowtok + kPM);   // [S]: a stage's bytes have landed
+  uint32_t* rbits = reinterpret_cast<uint32_t*>(rowtok + kPM);   // [kPM][D / 32] outlier decisions of the tile's rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(rbits + kPM * D / 32);   // [S]: a stage's bytes have landed
   uint64_t* empty = full + S;                                    // [S]: a stage's MMAs are done
   uint64_t* done = empty + S;                                    // every MMA is done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
@@ -1043,6 +1079,12 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
         for (int i = tid; i < pre * D; i += kPThreads) xs[i / D][i % D] = stg[i];
         __syncthreads();
       }
+      // per-token outlier decisions of every row at once (one thread per row)
+      const bool pre_bits = KIND >= kProjPage && a.fmt != KVQ_FMT_CB2_STATIC;
+      if (pre_bits) {
+        for (int r = tid; r < kPM; r += kPThreads) outlier_bits<D>(xs[r], (float)a.sigma, kmax_outliers(D), rbits + r * (D / 32));
+        __syncthreads();
+      }
       for (int s = grp; s < SPT; s += NB) {
         const int u = unit_of(s);
         if (u < 0) continue;
@@ -1058,12 +1100,12 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
             constexpr int kB = page_blk_bytes<D>();
             const PageWs<D> pw{reinterpret_cast<uint8_t(*)[D]>(gws + kB), reinterpret_cast<uint8_t(*)[D]>(gws + kB + 16 * D),
                                gws, reinterpret_cast<float*>(gws + kB + 32 * D)};
-            page_quantize<D, XS>(a, h, role, (uint32_t)pt[u], xu, pw, g);
+            page_quantize<D, XS>(a, h, role, (uint32_t)pt[u], xu, pw, g, pre_bits ? rbits + s * U * (D / 32) : nullptr);
           } else {
             constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
             const GroupWs<D> gw{reinterpret_cast<uint8_t(*)[D]>(gws + kB), reinterpret_cast<uint8_t(*)[D]>(gws + kB + 64 * D),
                                 gws};
-            group_quantize<D, XS>(a, h, role, pt, u, xu, gw, g);
+            group_quantize<D, XS>(a, h, role, pt, u, xu, gw, g, rbits + s * U * (D / 32));
           }
         } else {   // the final partial unit: its new rows wait in staging
           float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
