@@ -1111,6 +1111,17 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   sm.GS = GS;
   const uint32_t zb_s = smem_u32(zb);
 
+  // sequence length and this warp's first page-table entries are loaded
+  // first, so their latency overlaps the query loads below
+  int L = a.seq_lens[b];
+  const int p0 = split * a.pps;
+  auto page_of = [&](int li) {   // the sequence page of this warp's local page li
+    return F::kGroup ? p0 + kGroupPages * (w + (li / kGroupPages) * W) + li % kGroupPages : p0 + w + li * W;
+  };
+  const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
+  const int spec_page = page_of(lane);
+  const int win_spec = spec_page < min(p0 + a.pps, a.ppsm) ? pt[spec_page] : 0;
+
   // query of the CTA's G heads: fp32 in shared memory as [D][GS] (outlier
   // corrections gather its columns), fp16 B fragments in registers
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
@@ -1129,23 +1140,6 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     fence_mbar_init();
   }
 
-  uint32_t qf[NT][NS][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int h = nt * 8 + g;
-    const __nv_bfloat16* qh = qg + (size_t)h * D + 2 * q4;
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      const bool on = h < G;
-      const float x0 = on ? __bfloat162float(qh[16 * s]) : 0.f, x1 = on ? __bfloat162float(qh[16 * s + 1]) : 0.f;
-      const float x8 = on ? __bfloat162float(qh[16 * s + 8]) : 0.f, x9 = on ? __bfloat162float(qh[16 * s + 9]) : 0.f;
-      qf[nt][s][0] = h2_as_u32(__floats2half2_rn(x0, x1));
-      qf[nt][s][1] = h2_as_u32(__floats2half2_rn(x8, x9));
-    }
-  }
-  __syncthreads();
-
-  int L = a.seq_lens[b];
   if (L > a.max_seq_len) {
     if (split == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(a.status, KVQ_STATUS_SEQ_TOO_LONG);
     L = a.max_seq_len;
@@ -1154,7 +1148,6 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   const int n_all = (L + kPage - 1) / kPage;
   // pages stored as blocks (the group format quantizes whole groups)
   const int nq = F::kPaged ? (L / (kPage * F::kUnit)) * F::kUnit : n_all;
-  const int p0 = split * a.pps;
   const int p1 = min(p0 + a.pps, n_all);
   const int pq1 = min(p1, nq);
   // this warp's pages: every W-th page, or for the group format every W-th group
@@ -1165,44 +1158,14 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   } else {
     n_local = pq1 > p0 + w ? (pq1 - p0 - w + W - 1) / W : 0;
   }
-  auto page_of = [&](int li) {   // the sequence page of this warp's local page li
-    return F::kGroup ? p0 + kGroupPages * (w + (li / kGroupPages) * W) + li % kGroupPages : p0 + w + li * W;
-  };
   const int n_iter = (n_local + PPI - 1) / PPI;
-
-  WarpState<D, NT> st;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int s = 0; s < NS; ++s) st.o[nt][s][0] = st.o[nt][s][1] = st.o[nt][s][2] = st.o[nt][s][3] = 0.f;
-    st.m[nt][0] = st.m[nt][1] = -INFINITY;
-    st.l[nt][0] = st.l[nt][1] = 0.f;
-    st.sv[nt][0] = st.sv[nt][1] = st.sv[nt][2] = st.sv[nt][3] = 0.f;
-    st.qs[nt] = 0u;
-  }
-  int vch = 0;   // CB2_STATIC: the V static channel of slot g (lanes g < n_s)
-  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
-    const uint8_t* mk = a.static_mask + (size_t)kvh * 2 * a.n_static;   // K channels, then V channels
-    const int ia = 2 * q4;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h = nt * 8 + g;
-      const bool on = h < G;
-      const float qa = (on && ia < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia] & (D - 1))]) : 0.f;
-      const float qb =
-          (on && ia + 1 < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia + 1] & (D - 1))]) : 0.f;
-      st.qs[nt] = h2_as_u32(__floats2half2_rn(qa, qb));
-    }
-    vch = g < a.n_static ? (mk[a.n_static + g] & (D - 1)) : 0;
-  }
 
   // bytes copied per main-pool block (CB2_STATIC: only its n_s static channels' values)
   const int main_fetch = F::kMain == kBlkCb2s ? 12 * D + 16 + 32 * a.n_static : fetch_bytes<D>(F::kMain);
 
   // page-table window: lane j holds the entry of this warp's local page win_base + j
-  const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
   int win_base = 0;
-  int win = lane < n_local ? pt[page_of(lane)] : 0;
+  int win = lane < n_local ? win_spec : 0;   // lane < n_local: a page of [p0, p1)
 
   // K copies of iteration `it` (local pages it*PPI .. it*PPI+PPI-1): validates
   // the page-table entries and records them in meta for the V copies and the
@@ -1295,10 +1258,53 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     ++v_issued;
   };
 
+  __syncwarp();   // lane 0 initialised this warp's mbarriers
 #pragma unroll 1
   for (int it = 0; it < NK; ++it) issue_k(it);
 #pragma unroll 1
   for (int it = 0; it < NV; ++it) issue_v(it);
+
+  uint32_t qf[NT][NS][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + g;
+    const __nv_bfloat16* qh = qg + (size_t)h * D + 2 * q4;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      const bool on = h < G;
+      const float x0 = on ? __bfloat162float(qh[16 * s]) : 0.f, x1 = on ? __bfloat162float(qh[16 * s + 1]) : 0.f;
+      const float x8 = on ? __bfloat162float(qh[16 * s + 8]) : 0.f, x9 = on ? __bfloat162float(qh[16 * s + 9]) : 0.f;
+      qf[nt][s][0] = h2_as_u32(__floats2half2_rn(x0, x1));
+      qf[nt][s][1] = h2_as_u32(__floats2half2_rn(x8, x9));
+    }
+  }
+  __syncthreads();
+
+  WarpState<D, NT> st;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) st.o[nt][s][0] = st.o[nt][s][1] = st.o[nt][s][2] = st.o[nt][s][3] = 0.f;
+    st.m[nt][0] = st.m[nt][1] = -INFINITY;
+    st.l[nt][0] = st.l[nt][1] = 0.f;
+    st.sv[nt][0] = st.sv[nt][1] = st.sv[nt][2] = st.sv[nt][3] = 0.f;
+    st.qs[nt] = 0u;
+  }
+  int vch = 0;   // CB2_STATIC: the V static channel of slot g (lanes g < n_s)
+  if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
+    const uint8_t* mk = a.static_mask + (size_t)kvh * 2 * a.n_static;   // K channels, then V channels
+    const int ia = 2 * q4;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + g;
+      const bool on = h < G;
+      const float qa = (on && ia < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia] & (D - 1))]) : 0.f;
+      const float qb =
+          (on && ia + 1 < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia + 1] & (D - 1))]) : 0.f;
+      st.qs[nt] = h2_as_u32(__floats2half2_rn(qa, qb));
+    }
+    vch = g < a.n_static ? (mk[a.n_static + g] & (D - 1)) : 0;
+  }
 
   bool timed_out = false;
 #pragma unroll 1
