@@ -3,10 +3,13 @@
 
 Metric: achieved HBM GB/s of one decode step = algorithmic bytes (packed cache
 blocks the step must read, fp32 staging tail, bf16 Q and output) / device time
-of the step (split kernel + combine kernel), with the cache resident in HBM and
-L2 flushed before every timed step.  ms_per_step gives the microseconds per
-decode step.  The default workload is cb2_4k (B8, Hkv8, Hq32, D128, context
-4096, 2-bit codebook + e4m3 outliers).
+of the step (one launch of the split kernel, whose last CTA per (sequence, kv
+head) merges the splits), with the cache resident in HBM and L2 flushed before
+every timed step.  ms_per_step gives the microseconds per decode step.  The
+default workload is cb2_4k (B8, Hkv8, Hq32, D128, context 4096, 2-bit codebook
++ e4m3 outliers).  The line also carries "append": kvq_quantize_append timed on
+1-token appends and a 4096-token prefill chunk of the same shape (--no-append
+skips it); --project adds the fused projection + append comparison.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -55,7 +58,8 @@ def parse_args():
     p.add_argument("--flush-mb", type=int, default=512)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--append", action="store_true", help="also time kvq_quantize_append (1-token and prefill chunk)")
+    p.add_argument("--no-append", action="store_true",
+                   help="skip timing kvq_quantize_append (1-token appends and a 4096-token prefill chunk)")
     p.add_argument("--project", action="store_true",
                    help="also time kvq_project_append against a cuBLAS projection + kvq_quantize_append")
     p.add_argument("--project-only", action="store_true",
@@ -362,19 +366,25 @@ def time_oracle(w: synth.Workload, seed: int, target_s: float, reps: int | None 
 
 
 # ----------------------------------------------------------------------------- append timing (optional)
-def time_append(w: synth.Workload, dev) -> dict:
+def time_append(w: synth.Workload, dev, flush_mb: int) -> dict:
     """kvq_quantize_append for every sequence of the workload: one token into
     staging, one token that completes a page (page quantizer), and a 4096-token
-    prefill chunk (bf16 inputs)."""
-    res = {}
+    prefill chunk (bf16 inputs, N(0,1)).  L2 flushed before every timed call;
+    CUDA events on the current stream; mean of 5 calls after 3 warm-up calls."""
+    flush = L2Flush(flush_mb, dev)
+    res = {"l2": "flushed before every timed call"}
     for label, T, start in (("1_token_staging", 1, 0), ("1_token_completes_page", 1, 15), ("prefill_4096", 4096, 0)):
-        pages = (start + T + 15) // 16
-        c = kvq.QuantizedKVCache(w.fmt, w.B, w.Hkv, w.D, pages, w.B * pages, 0, device=dev)
+        pages = -(-((start + T + 15) // 16) // 4) * 4   # whole groups for the CB2 group format
+        c = kvq.QuantizedKVCache(w.fmt, w.B, w.Hkv, w.D, pages, w.B * pages, 0, device=dev,
+                                 static_channels=w.static_channels)
         kk = torch.randn((w.B, T, w.Hkv, w.D), device=dev).to(torch.bfloat16)
         vv = torch.randn_like(kk)
+        if w.fmt == synth.FMT_CB2S:
+            kvq.kvq_select_static_channels(c, kk[0].contiguous(), vv[0].contiguous())
         ts = []
         for r in range(8):
             c.seq_lens.fill_(start)
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             kvq.kvq_quantize_append(c, kk, vv)
@@ -383,7 +393,8 @@ def time_append(w: synth.Workload, dev) -> dict:
             if r >= 3:
                 ts.append(e0.elapsed_time(e1) * 1e-3)
         t = float(np.mean(ts))
-        res[label] = {"us": t * 1e6, "input_gbs": 2 * kk.numel() * kk.element_size() / t / 1e9}
+        res[label] = {"us": t * 1e6, "tokens": w.B * T, "input_gbs": 2 * kk.numel() * kk.element_size() / t / 1e9}
+        del c, kk, vv
     return res
 
 
@@ -514,8 +525,8 @@ def main():
         "clocks": t["clocks"],
     }
     line["config"]["partial_bytes_per_step"] = 2 * w.B * w.Hq * t["splits"] * (w.D + 2) * 4
-    if args.append:
-        line["append"] = time_append(w, dev)
+    if not args.no_append:
+        line["append"] = time_append(w, dev, args.flush_mb)
     if args.project:
         line["project"] = time_project(w, dev, args.flush_mb, B=args.project_b)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
