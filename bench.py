@@ -518,7 +518,8 @@ def main():
                        bytes_per_step=nb["step"], partial_bytes_per_step=0),
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nb["step"], "us_per_launch": split_ms * 1e3},
+                     "algorithmic_bytes_per_launch": nb["step"], "us_per_launch": split_ms * 1e3,
+                     "frac_of_nominal_8000_gbs": achieved / 8000.0},
         "e2e": {"value": world * nb["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": t["h2d"], "d2h_bytes_per_step": t["d2h"], "us_per_step": e2e_ms * 1e3},
         "gpu_launches": args.steps,
