@@ -363,7 +363,7 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
 }
 
 template <int BF, int D>
-__global__ void __launch_bounds__(256, 4) append_token_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 6) append_token_kernel(const AppendArgs a) {
   constexpr int kStride = block_stride(BF, D);
   __shared__ __align__(16) uint8_t blk[kStride];
   __shared__ uint8_t codes[16][D];
