@@ -2,7 +2,7 @@
 // the split heuristic, and the debug dequantization kernel.
 #include <cmath>
 
-#include "kvq_internal.cuh"
+#include "kvq_project.cuh"
 
 namespace kvq {
 

@@ -1,8 +1,6 @@
 // kvq_internal.cuh -- argument blocks and launch entry points shared between the
 // library's translation units (not part of the public ABI).
 #pragma once
-#include <cuda.h>
-
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -63,19 +61,6 @@ constexpr int kWarpsPerCta = 4;
 // Quantize-on-append launches (see kvq_quantize.cu).
 cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
 
-// K/V projection fused with quantize-on-append: the new tokens' K and V are
-// x W_k^T and x W_v^T (bf16 operands, fp32 accumulation) instead of inputs.
-struct ProjArgs {
-  CUtensorMap tm_x;            // x as [B * t_new][hidden], boxes of one unit of rows
-  CUtensorMap tm_w[2];         // W_k, W_v as [Hkv * D][hidden], boxes of one head's rows
-  AppendArgs a;                // kv[] unused
-  const __nv_bfloat16* x;      // [B][t_new][hidden]
-  const __nv_bfloat16* w[2];   // W_k, W_v: [Hkv * D][hidden]
-  int hidden;                  // a multiple of 32
-  float* kv_out;               // NULL or [2][B][t_new][Hkv][D]: the projected values
-};
-// Encodes p's tensor maps, then launches.
-cudaError_t project_append_launch(ProjArgs& p, int D, cudaStream_t st);
 cudaError_t select_static_launch(const void* k, const void* v, int in_dtype, int t, int Hkv, int D, int n_s,
                                  uint8_t* mask, cudaStream_t st);
 // Dequantize tokens [t0, t1) of (seq, head, role) to fp32.

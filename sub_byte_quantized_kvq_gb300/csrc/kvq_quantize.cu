@@ -22,7 +22,7 @@
 //   2. (page formats) copy the new tokens of the final partial page into
 //      staging -- after 1, which may still be reading the old staging rows;
 //   3. advance seq_lens and raise status bits -- after 1 and 2, which read it.
-#include "kvq_internal.cuh"
+#include "kvq_project.cuh"
 
 namespace kvq {
 
