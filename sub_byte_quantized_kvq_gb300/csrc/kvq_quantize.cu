@@ -194,13 +194,24 @@ __device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, ui
 #pragma unroll
       for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
       if (same) break;
-      for (int jj = 0; jj < 4; ++jj) {
-        float sum = 0.f;
-        int cnt = 0;
-        for (int r = 0; r < NROWS; ++r)
-          if ((keep >> r & 1u) && ((a[r >> 4] >> (2 * (r & 15))) & 3u) == (uint32_t)jj) { sum += x[r * xs]; ++cnt; }
-        if (cnt > 0) c[jj] = __fdiv_rn(sum, (float)cnt);
+      // centroid j = the mean of its values, each summed in row order; one pass
+      // keeps four independent sums (adding +0.0 to the others changes none of
+      // them: a sum that starts at +0.0 never becomes -0.0)
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      int cnt[4] = {0, 0, 0, 0};
+      for (int r = 0; r < NROWS; ++r) {
+        if (!(keep >> r & 1u)) continue;
+        const uint32_t j = (a[r >> 4] >> (2 * (r & 15))) & 3u;
+        const float v = x[r * xs];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          sum[jj] += j == (uint32_t)jj ? v : 0.f;
+          cnt[jj] += j == (uint32_t)jj;
+        }
       }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+        if (cnt[jj] > 0) c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
 #pragma unroll
       for (int w = 0; w < NW; ++w) prev[w] = a[w];
       have_prev = true;
