@@ -96,3 +96,35 @@ def test_project_rejects_bad_arguments():
                                 None) == kvq.KVQ_ERR_CAPACITY
     assert L.kvq_project_append(c, cc, xp.data_ptr(), 64, kp.data_ptr(), vp.data_ptr(), 0, None, None, None) == \
         kvq.KVQ_OK
+
+
+def test_project_full_size_prefill_sampled():
+    """The long-context shape's prefill chunk (4 sequences x 4096 tokens, 8 kv
+    heads, head_dim 128, hidden 4096 = 32 query heads x 128) through the fused
+    path: sampled projected rows against the oracle's fp64 projection, and
+    sampled blocks bit-exact against the oracle quantizing the returned rows."""
+    B, Hkv, D, T, hidden = 4, 8, 128, 4096, 4096
+    P = T // 16
+    c = kvq.QuantizedKVCache(kvq.KVQ_FMT_CB2_OUTLIER, B, Hkv, D, P, B * P, 0, device="cuda")
+    x, wk, wv = synth.projection_inputs(12, B, T, hidden, Hkv, D, device="cuda")
+    kv_out = torch.empty((2, B, T, Hkv, D), dtype=torch.float32, device="cuda")
+    kvq.kvq_project_append(c, x, wk, wv, None, kv_out)
+    torch.cuda.synchronize()
+    assert c.status_word() == 0
+    assert (c.seq_lens.cpu().numpy() == T).all()
+    rng = np.random.default_rng(0)
+    wk_c, wv_c = wk.cpu(), wv.cpu()
+    for b, t in zip(rng.integers(0, B, 24), rng.integers(0, T, 24)):
+        xr = x[b:b + 1, t:t + 1].cpu()
+        for role, w in ((0, wk_c), (1, wv_c)):
+            assert_projection_close(kv_out[role, b:b + 1, t:t + 1].cpu().numpy(), xr, w, "KV"[role], Hkv, D, None)
+    pool = c.pool.cpu().numpy()
+    pt = c.page_table.cpu().numpy()
+    stride = oracle.block_stride(oracle.BLK_CB2, D)
+    for b, pg, h, role in zip(rng.integers(0, B, 12), rng.integers(0, P, 12), rng.integers(0, Hkv, 12),
+                              rng.integers(0, 2, 12)):
+        rows = kv_out[role, b, 16 * pg:16 * pg + 16, h].cpu().numpy()
+        exp = oracle.quantize_page(oracle.BLK_CB2, D, rows, role=int(role))
+        phys = int(pt[b, pg]) & 0x7FFFFFFF
+        off = ((phys * Hkv + h) * 2 + role) * stride
+        np.testing.assert_array_equal(pool[off:off + stride], exp[:stride])
