@@ -1034,7 +1034,8 @@ __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, co
     if (lane == 0) lsum[h] = L;
   }
   __syncthreads();
-  // outputs: a thread takes 4 adjacent columns of one row and keeps 8 splits' loads in flight
+  // outputs: a thread takes 4 adjacent columns of one row and keeps up to 16
+  // splits' loads in flight (one round trip for S <= 16); sums in split order
   const int D4 = D / 4;
   for (int idx = tid; idx < G * D4; idx += nthreads) {
     const int h = idx / D4, c4 = idx % D4;
@@ -1047,15 +1048,15 @@ __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, co
       acc.z = fmaf(wgt, v.z, acc.z);
       acc.w = fmaf(wgt, v.w, acc.w);
     };
-    int s = 0;
-    for (; s + 8 <= S; s += 8) {
-      float4 v[8];
+    for (int s = 0; s < S; s += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = po[(size_t)(s + k) * D4];
+      for (int k = 0; k < 16; ++k)
+        if (s + k < S) v[k] = po[(size_t)(s + k) * D4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) add(wh[s + k], v[k]);
+      for (int k = 0; k < 16; ++k)
+        if (s + k < S) add(wh[s + k], v[k]);
     }
-    for (; s < S; ++s) add(wh[s], po[(size_t)s * D4]);
     const float L = lsum[h];
     const float r[4] = {L > 0.f ? acc.x / L : 0.f, L > 0.f ? acc.y / L : 0.f, L > 0.f ? acc.z / L : 0.f,
                         L > 0.f ? acc.w / L : 0.f};
