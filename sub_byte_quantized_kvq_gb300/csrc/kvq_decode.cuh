@@ -1007,57 +1007,60 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
 // out[r] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the S split
 // partials of the G rows r0 .. r0 + G - 1 (M = max_s m_s; 0 if no split saw a
 // token).  Called by every thread of a CTA (blockDim.x a multiple of 32);
-// `wts` is shared scratch of G * S + G floats.  One warp per row reduces the
-// split maxima and sums in a fixed order, then every thread forms its outputs
-// with the split loads of a column in flight together.  Shared by the combine
-// kernel and the split kernel's fused merge, so both give the same bits.
+// `wts` is shared scratch of G * S floats.  One warp per row reduces the split
+// maxima and turns them into weights, then every thread forms its outputs and
+// the weighted sum of l, in split order, with the split loads of a column in
+// flight together.  Shared by the combine kernel and the split kernel's fused
+// merge, so both give the same bits.
 __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                             size_t r0, int G, int S, int D, void* out, int out_dtype, float* wts) {
   const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  float* lsum = wts + G * S;
   for (int i = tid; i < G * S; i += nthreads) wts[i] = part_ml[r0 * S + i].x;
   __syncthreads();
+  // split weights 2^(m_s - M), one warp per head
   for (int h = warp; h < G; h += nthreads >> 5) {
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, wts[h * S + s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
+    __syncwarp();
     for (int s = lane; s < S; s += 32) {
       const float m = wts[h * S + s];
-      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      wts[h * S + s] = wgt;
-      L = fmaf(wgt, part_ml[(r0 + h) * S + s].y, L);
+      wts[h * S + s] = (m == -INFINITY) ? 0.f : exp2f(m - M);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) lsum[h] = L;
   }
   __syncthreads();
-  // outputs: a thread takes 4 adjacent columns of one row and keeps up to 16
-  // splits' loads in flight (one round trip for S <= 16); sums in split order
+  // outputs: a thread takes 4 adjacent columns of one row; each round keeps up
+  // to 16 splits' o and l loads in flight (one round trip for S <= 16); the
+  // weighted sums of o and of l run in split order
   const int D4 = D / 4;
   for (int idx = tid; idx < G * D4; idx += nthreads) {
     const int h = idx / D4, c4 = idx % D4;
     const float4* po = reinterpret_cast<const float4*>(part_o + (r0 + h) * (size_t)S * D) + c4;
+    const float2* pml = part_ml + (r0 + h) * S;
     const float* wh = wts + h * S;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](float wgt, const float4& v) {
-      acc.x = fmaf(wgt, v.x, acc.x);
-      acc.y = fmaf(wgt, v.y, acc.y);
-      acc.z = fmaf(wgt, v.z, acc.z);
-      acc.w = fmaf(wgt, v.w, acc.w);
-    };
+    float L = 0.f;
     for (int s = 0; s < S; s += 16) {
       float4 v[16];
+      float l[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        if (s + k < S) v[k] = po[(size_t)(s + k) * D4];
+        if (s + k < S) {
+          v[k] = po[(size_t)(s + k) * D4];
+          l[k] = pml[s + k].y;
+        }
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        if (s + k < S) add(wh[s + k], v[k]);
+        if (s + k < S) {
+          const float wgt = wh[s + k];
+          acc.x = fmaf(wgt, v[k].x, acc.x);
+          acc.y = fmaf(wgt, v[k].y, acc.y);
+          acc.z = fmaf(wgt, v[k].z, acc.z);
+          acc.w = fmaf(wgt, v[k].w, acc.w);
+          L = fmaf(wgt, l[k], L);
+        }
     }
-    const float L = lsum[h];
     const float r[4] = {L > 0.f ? acc.x / L : 0.f, L > 0.f ? acc.y / L : 0.f, L > 0.f ? acc.z / L : 0.f,
                         L > 0.f ? acc.w / L : 0.f};
     const size_t o = (r0 + h) * D + 4 * c4;
@@ -1480,12 +1483,19 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   // ---- fused combine: the last CTA of this (sequence, kv head) to arrive merges the S partials
   if (a.out == nullptr) return;
   int* last = reinterpret_cast<int*>(mL + GS);
-  __threadfence();   // this CTA's partials are visible device-wide before it arrives
+  // arrive with release semantics (the barrier orders every thread's partial
+  // stores before thread 0's release); the last to arrive acquires the others'
   __syncthreads();
-  if (threadIdx.x == 0) *last = atomicAdd(&a.arrivals[(size_t)b * a.Hkv + kvh], 1u) == (uint32_t)(a.S - 1);
+  if (threadIdx.x == 0) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(&a.arrivals[(size_t)b * a.Hkv + kvh])
+                 : "memory");
+    *last = old == (uint32_t)(a.S - 1);
+  }
   __syncthreads();
   if (!*last) return;
-  __threadfence();
   merge_group(a.part_o, a.part_ml, (size_t)b * a.Hq + (size_t)kvh * G, G, a.S, D, a.out, a.out_dtype, mo);
   if (threadIdx.x == 0) a.arrivals[(size_t)b * a.Hkv + kvh] = 0u;   // ready for the next call
 }
