@@ -1007,14 +1007,60 @@ __device__ __forceinline__ void page_tail(WarpState<D, NT>& st, const float* ks,
 // out[r] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the S split
 // partials of the G rows r0 .. r0 + G - 1 (M = max_s m_s; 0 if no split saw a
 // token).  Called by every thread of a CTA (blockDim.x a multiple of 32);
-// `wts` is shared scratch of G * S floats.  One warp per row reduces the split
-// maxima and turns them into weights, then every thread forms its outputs and
-// the weighted sum of l, in split order, with the split loads of a column in
-// flight together.  Shared by the combine kernel and the split kernel's fused
-// merge, so both give the same bits.
+// `wts` is shared scratch of G * S floats.  For S <= 16 every thread loads its
+// row's (m, l) pairs with its o columns and forms the weights itself (one
+// round trip); otherwise one warp per row reduces the split maxima into
+// weights first.  Either way the weighted sums of o and l run in split order.
+// Shared by the combine kernel and the split kernel's fused merge, so both
+// give the same bits.
 __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                             size_t r0, int G, int S, int D, void* out, int out_dtype, float* wts) {
   const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int D4 = D / 4;
+  auto store = [&](size_t o, const float (&r)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[o + k] = __float2bfloat16_rn(r[k]);
+      else static_cast<float*>(out)[o + k] = r[k];
+    }
+  };
+  if (S <= 16) {
+    // one round trip: each thread loads its row's S (m, l) pairs with its o
+    // columns and forms the weights itself (the same values and order as below)
+    for (int idx = tid; idx < G * D4; idx += nthreads) {
+      const int h = idx / D4, c4 = idx % D4;
+      const float4* po = reinterpret_cast<const float4*>(part_o + (r0 + h) * (size_t)S * D) + c4;
+      const float2* pml = part_ml + (r0 + h) * S;
+      float2 ml[16];
+      float4 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (k < S) {
+          ml[k] = pml[k];
+          v[k] = po[(size_t)k * D4];
+        }
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (k < S) M = fmaxf(M, ml[k].x);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (k < S) {
+          const float wgt = (ml[k].x == -INFINITY) ? 0.f : exp2f(ml[k].x - M);
+          acc.x = fmaf(wgt, v[k].x, acc.x);
+          acc.y = fmaf(wgt, v[k].y, acc.y);
+          acc.z = fmaf(wgt, v[k].z, acc.z);
+          acc.w = fmaf(wgt, v[k].w, acc.w);
+          L = fmaf(wgt, ml[k].y, L);
+        }
+      const float r[4] = {L > 0.f ? acc.x / L : 0.f, L > 0.f ? acc.y / L : 0.f, L > 0.f ? acc.z / L : 0.f,
+                          L > 0.f ? acc.w / L : 0.f};
+      store((r0 + h) * D + 4 * c4, r);
+    }
+    return;
+  }
   for (int i = tid; i < G * S; i += nthreads) wts[i] = part_ml[r0 * S + i].x;
   __syncthreads();
   // split weights 2^(m_s - M), one warp per head
@@ -1030,10 +1076,9 @@ __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, co
     }
   }
   __syncthreads();
-  // outputs: a thread takes 4 adjacent columns of one row; each round keeps up
-  // to 16 splits' o and l loads in flight (one round trip for S <= 16); the
-  // weighted sums of o and of l run in split order
-  const int D4 = D / 4;
+  // outputs: a thread takes 4 adjacent columns of one row; each round keeps
+  // 16 splits' o and l loads in flight; the weighted sums of o and of l run
+  // in split order
   for (int idx = tid; idx < G * D4; idx += nthreads) {
     const int h = idx / D4, c4 = idx % D4;
     const float4* po = reinterpret_cast<const float4*>(part_o + (r0 + h) * (size_t)S * D) + c4;
@@ -1063,12 +1108,7 @@ __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, co
     }
     const float r[4] = {L > 0.f ? acc.x / L : 0.f, L > 0.f ? acc.y / L : 0.f, L > 0.f ? acc.z / L : 0.f,
                         L > 0.f ? acc.w / L : 0.f};
-    const size_t o = (r0 + h) * D + 4 * c4;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[o + k] = __float2bfloat16_rn(r[k]);
-      else static_cast<float*>(out)[o + k] = r[k];
-    }
+    store((r0 + h) * D + 4 * c4, r);
   }
 }
 
