@@ -15,13 +15,13 @@
 // "Hierarchical Token Gating and Tiered KV-Cache Paging", section 2: FP8 pages
 // for the tier named by the page table.
 //
-// One append = up to three launches on the caller's stream:
+// One append = two launches on the caller's stream:
 //   1. quantize: per-token formats write every new token into its block;
-//      page formats quantize each page the append completes (from fp32
-//      staging + the new tokens);
-//   2. (page formats) copy the new tokens of the final partial page into
-//      staging -- after 1, which may still be reading the old staging rows;
-//   3. advance seq_lens and raise status bits -- after 1 and 2, which read it.
+//      page formats quantize each page (group) the append completes, from
+//      fp32 staging + the new tokens, and the CTA of the append's first page
+//      (the only one that reads staged rows) then stages the new tokens of
+//      the final partial page;
+//   2. advance seq_lens and raise status bits -- after 1, which reads them.
 #include "kvq_project.cuh"
 
 namespace kvq {
@@ -628,6 +628,22 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
   g.sync();   // the scratch may be reused by the next call
 }
 
+// New tokens of the final partial page (the final partial group for the CB2
+// group format) -> fp32 staging.  Run by the CTA of the append's first page
+// (first group) after it has read the staged rows: no other CTA reads them.
+__device__ void stage_tail(const AppendArgs& a, int b, int h, int role, int start, int n, int rows, int D) {
+  const int end = start + n;
+  if (end % rows == 0) return;
+  const int lo = max(start, (end / rows) * rows);
+  float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * rows * D;
+  for (int i = threadIdx.x; i < (end - lo) * (D / 8); i += blockDim.x) {
+    const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8)), pos = lo + tt;
+    float v[8];
+    load_in8(a, role, b, pos - start, h, c, D, v);
+    for (int j = 0; j < 8; ++j) stg[(pos % rows) * D + c + j] = v[j];
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(128, 8) append_page_kernel(const AppendArgs a) {
   __shared__ __align__(16) float xs[16][D];
@@ -640,18 +656,22 @@ __global__ void __launch_bounds__(128, 8) append_page_kernel(const AppendArgs a)
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
   const int end = start + n, pg = start / kPage + j;
-  if (pg * kPage + kPage > end) return;  // only pages this append completes
-  const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg];
-  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
-  for (int i = tid; i < 16 * (D / 8); i += blockDim.x) {
-    const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = pg * kPage + t;
-    if (pos < start) {
-      for (int j = 0; j < 8; ++j) xs[t][c + j] = stg[t * D + c + j];
-    } else {
-      load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+  const bool full = pg * kPage + kPage <= end;   // quantize only the pages this append completes
+  if (!full && j != 0) return;
+  if (full) {
+    const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg];
+    const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * kPage * D;
+    for (int i = tid; i < 16 * (D / 8); i += blockDim.x) {
+      const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = pg * kPage + t;
+      if (pos < start) {
+        for (int jj = 0; jj < 8; ++jj) xs[t][c + jj] = stg[t * D + c + jj];
+      } else {
+        load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+      }
     }
+    page_quantize<D, D>(a, h, role, u, xs, PageWs<D>{mask, codes, blk, red}, whole_cta());   // ends with a barrier
   }
-  page_quantize<D, D>(a, h, role, u, xs, PageWs<D>{mask, codes, blk, red}, whole_cta());
+  if (j == 0) stage_tail(a, b, h, role, start, n, kPage, D);
 }
 
 // Shared scratch of one CB2 group quantization.
@@ -730,42 +750,27 @@ __global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
   const int end = start + n, gr = start / GT + j;
-  if (gr * GT + GT > end) return;  // only groups this append completes
-  const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
-  for (int i = tid; i < GT * (D / 8); i += blockDim.x) {
-    const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = gr * GT + t;
-    if (pos < start) {
-      for (int j = 0; j < 8; ++j) xs[t][c + j] = stg[t * D + c + j];
-    } else {
-      load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+  const bool full = gr * GT + GT <= end;   // quantize only the groups this append completes
+  if (!full && j != 0) return;
+  if (full) {
+    const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * GT * D;
+    for (int i = tid; i < GT * (D / 8); i += blockDim.x) {
+      const int t = i / (D / 8), c = 8 * (i - t * (D / 8)), pos = gr * GT + t;
+      if (pos < start) {
+        for (int jj = 0; jj < 8; ++jj) xs[t][c + jj] = stg[t * D + c + jj];
+      } else {
+        load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
+      }
     }
+    group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{mask, codes, blk},
+                         whole_cta());   // ends with a barrier
   }
-  group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{mask, codes, blk},
-                       whole_cta());
+  if (j == 0) stage_tail(a, b, h, role, start, n, GT, D);
 }
 
 template <int D>
 constexpr size_t group_smem_bytes() {
   return (size_t)kPage * kGroupPages * D * 6 + (size_t)kGroupPages * block_stride(kBlkCb2g, D);
-}
-
-// New tokens of the final partial page (the final partial group for the CB2
-// group format) -> fp32 staging (after the page / group kernel).
-__global__ void __launch_bounds__(256) append_stage_kernel(const AppendArgs a, int D) {
-  const int h = blockIdx.x >> 1, role = blockIdx.x & 1, b = blockIdx.y;
-  int start, n;
-  if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int rows = a.fmt == KVQ_FMT_CB2_GROUP4 ? kPage * kGroupPages : kPage;
-  const int end = start + n;
-  if (end % rows == 0) return;
-  const int lo = max(start, (end / rows) * rows);
-  float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * rows * D;
-  for (int i = threadIdx.x; i < (end - lo) * (D / 8); i += blockDim.x) {
-    const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8)), pos = lo + tt;
-    float v[8];
-    load_in8(a, role, b, pos - start, h, c, D, v);
-    for (int j = 0; j < 8; ++j) stg[(pos % rows) * D + c + j] = v[j];
-  }
 }
 
 // Advance seq_lens and report skipped sequences (after every other launch read them).
@@ -836,10 +841,8 @@ static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
     }
     const int groups_max = a.t_new / (kPage * kGroupPages) + 2;
     append_group_kernel<D><<<dim3(groups_max, a.Hkv * 2, a.B), 128, smem, st>>>(a);
-    append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
   } else {
     append_page_kernel<D><<<grid, 128, 0, st>>>(a);
-    append_stage_kernel<<<dim3(a.Hkv * 2, a.B), 256, 0, st>>>(a, D);
   }
   append_finish_kernel<<<a.B, 128, 0, st>>>(a);
   return cudaGetLastError();
