@@ -128,3 +128,16 @@ def test_project_full_size_prefill_sampled():
         phys = int(pt[b, pg]) & 0x7FFFFFFF
         off = ((phys * Hkv + h) * 2 + role) * stride
         np.testing.assert_array_equal(pool[off:off + stride], exp[:stride])
+
+
+@pytest.mark.parametrize("hidden", [32, 96, 160])
+def test_project_hidden_not_a_multiple_of_the_stage_width(hidden):
+    """hidden a multiple of 32 but not of the 64-column stage: the last stage's
+    boxes run past the matrices and read zeros."""
+    B, Hkv, D, P = 2, 2, 128, 8
+    pair = Pair(kvq.KVQ_FMT_FP4_E2M1_S16, B, Hkv, D, P, seed=8)
+    x, wk, wv = synth.projection_inputs(8, B, 50, hidden, Hkv, D)
+    k, v = pair.project(x, wk, wv, [50, 33])
+    assert_projection_close(k, x, wk, "K", Hkv, D, [50, 33])
+    assert_projection_close(v, x, wv, "V", Hkv, D, [50, 33])
+    pair.assert_cache_equal()
