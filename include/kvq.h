@@ -13,7 +13,8 @@
  *        ("2. Entropy-Guided Tiered KV-Cache Quantization").
  *   [P3] "Sub-5ms MoE Inference: Sub-Byte KV Quantization and Expert Pipelining
  *        at Scale": FP16 outlier tensor beside sub-byte codes ("Sub-Byte
- *        KV-Cache Quantization").
+ *        KV-Cache Quantization"); the attention projection fused with the
+ *        KV-cache write ("Engineering Real-Time Autonomous Workflows", item 1).
  *   [P4] "The Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache
  *        Quantization": block-wise asymmetric INT4 and FP4 E2M1 with per-group
  *        scales, dequantized during the flash-decoding reduction
@@ -34,8 +35,9 @@
  *     device word `cache->status` (KVQ_STATUS_*); the affected sequence is
  *     skipped, nothing outside the caller's buffers is touched, and the host
  *     reads the word whenever it chooses.  No call ever traps or spins forever:
- *     the one wait in device code (for the asynchronous copies of a page) gives
- *     up after 100 ms and sets KVQ_STATUS_TIMEOUT.
+ *     every wait in device code (for the asynchronous copies of a page, for a
+ *     tensor-memory copy or MMA to complete) gives up after 100 ms and sets
+ *     KVQ_STATUS_TIMEOUT.
  *   - No C++ exception crosses this interface.
  */
 #ifndef KVQ_H_
