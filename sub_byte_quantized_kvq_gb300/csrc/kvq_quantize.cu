@@ -185,30 +185,30 @@ __device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, ui
     uint32_t prev[NW];
     bool have_prev = false;
     for (int it = 0; it < iters; ++it) {
+      // one pass assigns every value and sums each centroid's members in row
+      // order (four independent sums: adding +0.0 to the others changes none
+      // of them, a sum that starts at +0.0 never being -0.0)
       uint32_t a[NW];
 #pragma unroll
       for (int w = 0; w < NW; ++w) a[w] = 0u;
-      for (int r = 0; r < NROWS; ++r)
-        if (keep >> r & 1u) a[r >> 4] |= (uint32_t)nearest4(x[r * xs], c) << (2 * (r & 15));
-      bool same = have_prev;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
-      if (same) break;
-      // centroid j = the mean of its values, each summed in row order; one pass
-      // keeps four independent sums (adding +0.0 to the others changes none of
-      // them: a sum that starts at +0.0 never becomes -0.0)
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
       int cnt[4] = {0, 0, 0, 0};
       for (int r = 0; r < NROWS; ++r) {
         if (!(keep >> r & 1u)) continue;
-        const uint32_t j = (a[r >> 4] >> (2 * (r & 15))) & 3u;
         const float v = x[r * xs];
+        const uint32_t j = (uint32_t)nearest4(v, c);
+        a[r >> 4] |= j << (2 * (r & 15));
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           sum[jj] += j == (uint32_t)jj ? v : 0.f;
           cnt[jj] += j == (uint32_t)jj;
         }
       }
+      bool same = have_prev;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
+      if (same) break;
+      // centroid j = the mean of its values
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
         if (cnt[jj] > 0) c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
