@@ -677,41 +677,96 @@ __global__ void __launch_bounds__(128, 8) append_page_kernel(const AppendArgs a)
 // Shared scratch of one CB2 group quantization.
 template <int D>
 struct GroupWs {
-  uint8_t (*mask)[D];   // [64][D]
-  uint8_t (*codes)[D];  // [64][D]
+  uint32_t* rbits;      // [64][D / 32] outlier decisions of the group's tokens (bit c % 32 of word c / 32)
+  uint32_t (*cc)[4];    // [D][4] the 64 tokens' 2-bit codes of each channel, token t at bits 2 (t % 16) of word t / 16
   uint8_t* blk;         // kGroupPages blocks
 };
+
+// Outlier side-list of page p of a group (CB2 record layout, see
+// build_side_list) from the group's outlier bits: lane l owns channels
+// [l*D/32, (l+1)*D/32).
+template <int D, int XS>
+__device__ void build_side_list_bits(const uint32_t* rbits, const float (*xs)[XS], uint8_t* hdr, int lane) {
+  constexpr int CPL = D / 32;
+  uint32_t tm[CPL];
+  int nch = 0, nval = 0;
+  for (int k = 0; k < CPL; ++k) {
+    const int c = lane * CPL + k;
+    uint32_t m = 0;
+    for (int t = 0; t < 16; ++t) m |= ((rbits[t * (D / 32) + c / 32] >> (c % 32)) & 1u) << t;
+    tm[k] = m;
+    nch += m != 0;
+    nval += __popc(m);
+  }
+  int ich = nch, ival = nval;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int a1 = __shfl_up_sync(0xffffffffu, ich, d), a2 = __shfl_up_sync(0xffffffffu, ival, d);
+    if (lane >= d) { ich += a1; ival += a2; }
+  }
+  const int tot_ch = __shfl_sync(0xffffffffu, ich, 31), tot_val = __shfl_sync(0xffffffffu, ival, 31);
+  int ci = ich - nch;
+  for (int k = 0; k < CPL; ++k) {
+    if (!tm[k]) continue;
+    const int c = lane * CPL + k;
+    uint8_t* rec = hdr + 4 + 20 * ci;
+    rec[0] = (uint8_t)c;
+    rec[1] = 0;
+    rec[2] = (uint8_t)(tm[k] & 0xFF);
+    rec[3] = (uint8_t)(tm[k] >> 8);
+    for (int t = 0; t < 16; ++t)
+      if (tm[k] >> t & 1u) rec[4 + t] = f32_to_e4m3(xs[t][c]);
+    ++ci;
+  }
+  if (lane == 0) {
+    hdr[0] = (uint8_t)tot_ch;
+    hdr[1] = (uint8_t)tot_val;
+  }
+}
+
+// Page p's 2-bit codes (word p of every channel's packed codes) -> the block's
+// lane-major code words (CB2 layout).
+template <int D>
+__device__ __forceinline__ void pack_cb2_codes_packed(const uint32_t (*cc)[4], int p, uint8_t* blk, int role,
+                                                      const Grp& g) {
+  constexpr int NS = D / 16;
+  for (int i = g.tid; i < 32 * NS; i += g.n) {
+    const int ln = i / NS, s = i % NS;
+    uint32_t word = 0;
+    for (int k = 0; k < 8; ++k) {
+      int t, c;
+      frag_inverse(role, ln, s, k, t, c);
+      word |= ((cc[c][p] >> (2 * t)) & 3u) << (4 * (k & 3) + 2 * (k >> 2));
+    }
+    *reinterpret_cast<uint16_t*>(blk + 2 * NS * ln + 2 * s) = (uint16_t)word;
+  }
+}
 
 // CB2 group format: quantize the 64 tokens xs[64] (row stride XS) of group gr
 // of the sequence whose page-table row is pt: outliers per token, one codebook
 // per channel over the group's non-outliers in token order (in the group's
-// first page), codes and side-list per page.
+// first page), codes and side-list per page.  have_bits: ws.rbits already
+// holds the tokens' outlier decisions (else they are taken here).
 template <int D, int XS>
 __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32_t* pt, int gr, const float (*xs)[XS],
-                               const GroupWs<D>& ws, const Grp& g, const uint32_t* rbits = nullptr) {
-  constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D);
-  uint8_t(*mask)[D] = ws.mask;
-  uint8_t(*codes)[D] = ws.codes;
+                               const GroupWs<D>& ws, const Grp& g, bool have_bits) {
+  constexpr int GT = kPage * kGroupPages, kStride = block_stride(kBlkCb2g, D), NWD = D / 32;
   uint8_t* blk = ws.blk;
   const int tid = g.tid;
   for (int i = tid; i < kGroupPages * kStride / 16; i += g.n)
     reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
-  g.sync();
-  if (rbits) {
-    for (int i = tid; i < GT * D; i += g.n)
-      mask[i / D][i % D] = (uint8_t)((rbits[(i / D) * (D / 32) + (i % D) / 32] >> (i % 32)) & 1u);
-  } else if (tid < GT) {
-    outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+  g.sync();   // also orders the caller's writes of xs before the reads below
+  if (!have_bits) {
+    if (tid < GT) outlier_bits<D>(&xs[tid][0], (float)a.sigma, kmax_outliers(D), ws.rbits + tid * NWD);
+    g.sync();
   }
-  g.sync();
   if (tid < D) {
     const int c = tid;
     uint32_t cc[GT / 16];
     uint16_t c16[4];
     uint64_t keep = 0;
-    for (int t = 0; t < GT; ++t) keep |= (uint64_t)(mask[t][c] == 0) << t;
+    for (int t = 0; t < GT; ++t) keep |= (uint64_t)(((ws.rbits[t * NWD + c / 32] >> (c % 32)) & 1u) ^ 1u) << t;
     lloyd4_rows<GT>(&xs[0][c], XS, keep, a.iters, c16, cc);
-    for (int t = 0; t < GT; ++t) codes[t][c] = (cc[t >> 4] >> (2 * (t & 15))) & 3u;
+    for (int w = 0; w < GT / 16; ++w) ws.cc[c][w] = cc[w];
     uint8_t* cbp = blk + 8 * cb2_slot(role, c);   // the codebook sits at the start of the group's first block
     for (int jj = 0; jj < 4; ++jj) {
       cbp[jj] = (uint8_t)(c16[jj] & 0xFF);
@@ -720,9 +775,9 @@ __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32
   }
   // one warp per page builds its side-list
   for (int w = tid >> 5; w < kGroupPages; w += g.n >> 5)
-    build_side_list<D, XS>(mask + 16 * w, xs + 16 * w, blk + w * kStride + cb2_out_off(D), tid & 31);
+    build_side_list_bits<D, XS>(ws.rbits + 16 * w * NWD, xs + 16 * w, blk + w * kStride + cb2_out_off(D), tid & 31);
   g.sync();
-  for (int p = 0; p < kGroupPages; ++p) pack_cb2_codes<D>(codes + 16 * p, blk + p * kStride + cb2g_code_off(D), role, g);
+  for (int p = 0; p < kGroupPages; ++p) pack_cb2_codes_packed<D>(ws.cc, p, blk + p * kStride + cb2g_code_off(D), role, g);
   g.sync();
   for (int p = 0; p < kGroupPages; ++p) {
     const uint32_t u = (uint32_t)pt[gr * kGroupPages + p];
@@ -733,18 +788,25 @@ __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32
   g.sync();   // the scratch may be reused by the next call
 }
 
+// Shared memory of the standalone group kernel: the group's values, their
+// outlier bits, the packed codes and the four blocks.
+template <int D>
+constexpr size_t group_smem_bytes() {
+  return (size_t)kPage * kGroupPages * D * 4 + (size_t)kPage * kGroupPages * (D / 32) * 4 + (size_t)D * 16 +
+         (size_t)kGroupPages * block_stride(kBlkCb2g, D);
+}
+
 // CB2 group format: each group of 4 pages (64 tokens) this append completes,
 // from fp32 staging + the new tokens.  One CTA per (group, kv head x role,
-// sequence); dynamic shared memory holds the values, masks, codes and the
-// four blocks.
+// sequence).
 template <int D>
-__global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(128, 4) append_group_kernel(const AppendArgs a) {
   constexpr int GT = kPage * kGroupPages;
   extern __shared__ __align__(16) uint8_t gsm[];
   float(*xs)[D] = reinterpret_cast<float(*)[D]>(gsm);
-  uint8_t(*mask)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 4);
-  uint8_t(*codes)[D] = reinterpret_cast<uint8_t(*)[D]>(gsm + GT * D * 5);
-  uint8_t* blk = gsm + GT * D * 6;   // 4 blocks
+  uint32_t* rbits = reinterpret_cast<uint32_t*>(gsm + GT * D * 4);
+  uint32_t(*cc)[4] = reinterpret_cast<uint32_t(*)[4]>(gsm + GT * D * 4 + GT * (D / 32) * 4);
+  uint8_t* blk = gsm + GT * D * 4 + GT * (D / 32) * 4 + D * 16;   // 4 blocks
   const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
   const int tid = threadIdx.x;
   int start, n;
@@ -762,15 +824,10 @@ __global__ void __launch_bounds__(128) append_group_kernel(const AppendArgs a) {
         load_in8(a, role, b, pos - start, h, c, D, &xs[t][c]);
       }
     }
-    group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{mask, codes, blk},
-                         whole_cta());   // ends with a barrier
+    group_quantize<D, D>(a, h, role, a.page_table + (size_t)b * a.ppsm, gr, xs, GroupWs<D>{rbits, cc, blk},
+                         whole_cta(), false);   // ends with a barrier
   }
   if (j == 0) stage_tail(a, b, h, role, start, n, GT, D);
-}
-
-template <int D>
-constexpr size_t group_smem_bytes() {
-  return (size_t)kPage * kGroupPages * D * 6 + (size_t)kGroupPages * block_stride(kBlkCb2g, D);
 }
 
 // Advance seq_lens and report skipped sequences (after every other launch read them).
@@ -939,7 +996,7 @@ struct ProjPlan {
   static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
                           : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
                           : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
-                                                : kGroupPages * block_stride(kBlkCb2g, D) + 128 * D;
+                                                : kGroupPages * block_stride(kBlkCb2g, D) + 16 * D;
   static constexpr int WSR = (WS + 127) / 128 * 128;
   static constexpr int EPI = kPM * XS * 4 + NB * WSR;   // the epilogue's fp32 tile and scratch
   static constexpr int R0 = S * STAGE > EPI ? S * STAGE : EPI;
@@ -1117,9 +1174,8 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
             page_quantize<D, XS>(a, h, role, (uint32_t)pt[u], xu, pw, g, pre_bits ? rbits + s * U * (D / 32) : nullptr);
           } else {
             constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
-            const GroupWs<D> gw{reinterpret_cast<uint8_t(*)[D]>(gws + kB), reinterpret_cast<uint8_t(*)[D]>(gws + kB + 64 * D),
-                                gws};
-            group_quantize<D, XS>(a, h, role, pt, u, xu, gw, g, rbits + s * U * (D / 32));
+            const GroupWs<D> gw{rbits + s * U * (D / 32), reinterpret_cast<uint32_t(*)[4]>(gws + kB), gws};
+            group_quantize<D, XS>(a, h, role, pt, u, xu, gw, g, true);
           }
         } else {   // the final partial unit: its new rows wait in staging
           float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
