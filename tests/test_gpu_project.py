@@ -141,3 +141,39 @@ def test_project_hidden_not_a_multiple_of_the_stage_width(hidden):
     assert_projection_close(k, x, wk, "K", Hkv, D, [50, 33])
     assert_projection_close(v, x, wv, "V", Hkv, D, [50, 33])
     pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_CB2_OUTLIER, kvq.KVQ_FMT_INT4_G32])
+def test_project_bad_page_entry_is_flagged_and_skipped(fmt):
+    """A page-table entry outside the pool: the fused path skips that sequence
+    (seq_lens unchanged, nothing written for it), flags KVQ_STATUS_BAD_PAGE,
+    and appends the other sequences exactly as the oracle does."""
+    B, Hkv, D, P, hidden = 2, 2, 128, 4, 128
+    pair = Pair(fmt, B, Hkv, D, P, seed=9)
+    x, wk, wv = synth.projection_inputs(9, B, 40, hidden, Hkv, D)
+    pt = pair.gpu.page_table.clone()
+    pair.gpu.page_table[0, 1] = pair.gpu.cfg.num_pages + 5      # sequence 0 names a page outside the pool
+    kv_out = torch.zeros((2, B, 40, Hkv, D), dtype=torch.float32, device="cuda")
+    kvq.kvq_project_append(pair.gpu, x.cuda(), wk.cuda(), wv.cuda(), None, kv_out)
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_BAD_PAGE
+    assert pair.gpu.seq_lens.cpu().tolist() == [0, 40]
+    assert (kv_out[:, 0] == 0).all()                                 # the skipped sequence produced nothing
+    pair.gpu.page_table.copy_(pt)
+    pair.gpu.status.zero_()
+    kv = kv_out.cpu().numpy()
+    pair.ref.append(kv[0], kv[1], np.array([0, 40], np.int32))      # the oracle appends sequence 1 only
+    pair.assert_cache_equal()
+
+
+def test_project_capacity_overflow_is_flagged():
+    B, Hkv, D, P, hidden = 2, 1, 64, 2, 64
+    pair = Pair(kvq.KVQ_FMT_FP4_E2M1_S16, B, Hkv, D, P, seed=10)
+    x, wk, wv = synth.projection_inputs(10, B, 20, hidden, Hkv, D)
+    pair.project(x, wk, wv)
+    pair.assert_cache_equal()
+    kvq.kvq_project_append(pair.gpu, x.cuda(), wk.cuda(), wv.cuda(), torch.tensor([20, 12], dtype=torch.int32,
+                                                                                     device="cuda"))
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_CAPACITY          # 40 tokens > 32 slots for sequence 0
+    assert pair.gpu.seq_lens.cpu().tolist() == [20, 32]
