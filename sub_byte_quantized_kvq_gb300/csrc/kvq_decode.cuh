@@ -10,7 +10,8 @@
 // Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache Quantization",
 // section 2 and its flash-decoding flowchart: values are dequantized only
 // during the attention reduction, and the sequence is split across CTAs whose
-// partial softmax states a second kernel merges.
+// partial softmax states are then merged (here by the last CTA of each
+// sequence and kv head to finish, or by a second kernel in the two-stage calls).
 //
 // Design (GB300, sm_103a):
 //  * grid (splits, kv heads, sequences); a CTA owns one (sequence, kv head,
@@ -18,9 +19,11 @@
 //    its own pages (page p0 + w, p0 + w + W, ...), PPI pages per iteration,
 //    with its own online-softmax state; the warps merge in shared memory.
 //  * each warp runs two rings of bulk asynchronous copies (cp.async.bulk +
-//    mbarrier), one copy per block: K blocks two iterations ahead, V blocks
-//    one (a V block is read only after the K phase and the softmax of its
-//    iteration); no register staging, no TMA multicast.
+//    mbarrier), one copy per block: for the page formats one K stage (refilled
+//    as soon as the iteration's scores are done) and one V stage (a V block is
+//    read only after the K phase and the softmax of its iteration); E2M1 two
+//    and two, INT4 three and two single pages; no register staging, no TMA
+//    multicast.
 //  * QK^T: A = K (16 tokens x 16 channels, built in registers from the codes),
 //    B = Q^T (16 channels x 8 heads, fp16, loaded once).  PV: A = V^T (16
 //    channels x 16 tokens, built in registers), B = P^T (fp16 hi + lo split of
@@ -29,12 +32,12 @@
 //    or two byte-permutes of shared-memory words.  The PPI pages of an
 //    iteration are independent mma chains the scheduler interleaves.
 //  * CB2 outliers: a code slot holding an outlier stores code 0 (value c0).
-//    Up to 16 channels with outliers form one k16 tile; the correction
-//    x - c0 is applied as two mma with exact fp16 operands (+ the e4m3
-//    values, - c0 where the token mask is set) against the gathered query
-//    columns (scores) or against P^T (output of those channels, accumulated
-//    in shared memory with the same online-softmax rescaling as the
-//    registers).  No atomics.
+//    The side-list's channel records go six at a time into one mma tile; the
+//    correction x - c0 is applied as two mma with exact fp16 operands (+ the
+//    e4m3 values, - c0 where the token mask is set) against the gathered
+//    query columns (scores) or against P^T (output of those channels,
+//    accumulated in shared memory with the same online-softmax rescaling as
+//    the registers).  No atomics.
 //  * the partial last page of page formats (fp32 staging) is done on CUDA
 //    cores in fp32.
 #pragma once
