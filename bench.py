@@ -406,6 +406,11 @@ def time_project(w: synth.Workload, dev, flush_mb: int, reps: int = 10, warmup: 
     for a 4096-token prefill chunk and a 1-token append.  L2 flushed before
     every timed call; CUDA events on the current stream."""
     hidden = w.Hq * w.D
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])   # burst: the call is timed alone
+    except Exception:
+        bf16_peak = 1900.0   # fallback
     if B:
         w = dataclasses.replace(w, B=B)
     flush = L2Flush(flush_mb, dev)
@@ -454,6 +459,7 @@ def time_project(w: synth.Workload, dev, flush_mb: int, reps: int = 10, warmup: 
         flops = 2.0 * w.B * T * hidden * 2 * w.Hkv * w.D
         res[label] = {"fused_us": t_f * 1e6, "unfused_us": t_u * 1e6, "cublas_gemms_us": t_g * 1e6,
                       "append_bf16_us": t_a * 1e6, "fused_tflops": flops / t_f / 1e12,
+                      "fused_frac_of_bf16_peak": flops / t_f / 1e12 / bf16_peak,
                       "speedup_vs_unfused": t_u / t_f}
         del c, x, wk, wv, k_pre, v_pre
     return res
