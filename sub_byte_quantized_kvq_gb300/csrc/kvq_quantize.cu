@@ -237,14 +237,15 @@ __device__ __forceinline__ void frag_inverse(int role, int lane, int s, int k, i
 // ----------------------------------------------------------------------------- per-token formats
 // INT4 group-32 quantization of token slots [t0, min(t0 + 32 / NG, hi)) by one
 // warp (NG = D / 32 groups): lane s * NG + g owns group g of slot t0 + s.
-// Lanes past hi compute on slot t0 but store nothing; t0 < hi.
-template <int D, int XS>
+// Lanes past hi compute on slot t0 but store nothing; t0 < hi.  Channel c of a
+// row sits at xs[t][c + GP * (c / 32)].
+template <int D, int XS, int GP>
 __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
                                      double sigma, int lane) {
   constexpr int NG = D / 32, CAP = int4_cap(D);
   const int g = lane % NG, t = t0 + lane / NG;
   const bool act = t < hi;
-  const float* xg = xs[act ? t : t0] + 32 * g;
+  const float* xg = xs[act ? t : t0] + (32 + GP) * g;
   uint8_t mask[32];
   outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
   bool have = false;
@@ -301,14 +302,14 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint
 
 // E2M1 quantization of token slots [t0, min(t0 + 32 / NS, hi)) by one warp
 // (NS = D / 16 scale groups): lane s * NS + g owns channels [16 g, 16 g + 16)
-// of slot t0 + s.
-template <int D, int XS>
+// of slot t0 + s.  Channel c of a row sits at xs[t][c + GP * (c / 32)].
+template <int D, int XS, int GP>
 __device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
                                      int lane) {
   constexpr int NS = D / 16;
   const int g = lane % NS, t = t0 + lane / NS;
   if (t >= hi) return;
-  const float* x = xs[t] + 16 * g;
+  const float* x = xs[t] + 16 * g + GP * (g >> 1);
   float amax = 0.f;
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
@@ -329,8 +330,10 @@ __device__ __forceinline__ Grp whole_cta() { return Grp{(int)threadIdx.x, (int)b
 // Per-token formats: re-quantize token slots [lo, hi) of one block from rows
 // xs[slot] (row stride XS floats); the other slots keep their codes and
 // metadata.  blk (the block's bytes) and codes[16][D] are the group's scratch;
-// the caller's writes of xs come before the call.
-template <int BF, int D, int XS>
+// the caller's writes of xs come before the call.  Channel c of a row sits at
+// xs[slot][c + GP * (c / 32)]: GP = 1 pads each 32-channel group so that the
+// lanes of a warp, one group each, read distinct banks.
+template <int BF, int D, int XS, int GP = 0>
 __device__ void token_block_update(const AppendArgs& a, int role, const float (*xs)[XS], int lo, int hi, uint8_t* gblk,
                                    uint8_t* blk, uint8_t (*codes)[D], const Grp& g) {
   constexpr int kStride = block_stride(BF, D), NS = D / 16;
@@ -353,8 +356,8 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
   g.sync();
   constexpr int TPW = 32 / (BF == kBlkInt4 ? D / 32 : D / 16);   // token slots per warp pass
   for (int t0 = lo + warp * TPW; t0 < hi; t0 += nw * TPW) {
-    if (BF == kBlkInt4) quantize_tokens_int4<D, XS>(xs, t0, hi, codes, blk, a.sigma, lane);
-    else quantize_tokens_e2m1<D, XS>(xs, t0, hi, codes, blk, lane);
+    if (BF == kBlkInt4) quantize_tokens_int4<D, XS, GP>(xs, t0, hi, codes, blk, a.sigma, lane);
+    else quantize_tokens_e2m1<D, XS, GP>(xs, t0, hi, codes, blk, lane);
   }
   g.sync();
   for (int i = g.tid; i < 32 * NS; i += g.n) {
@@ -373,26 +376,46 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
   g.sync();   // the scratch may be reused by the next call
 }
 
+// Pages one CTA of the per-token append handles: enough that every warp has
+// tokens (a warp quantizes 32 / (D / 32) INT4 or 32 / (D / 16) E2M1 tokens per
+// pass, and a page holds 16).
+template <int BF>
+__host__ __device__ constexpr int token_ppc() { return BF == kBlkInt4 ? 4 : 2; }
+
+// Dynamic shared memory of append_token_kernel<BF, D>: per page, 16 staged rows
+// of D + D / 32 floats, the block's bytes and 16 x D codes.
 template <int BF, int D>
-__global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 6) append_token_kernel(const AppendArgs a) {
-  constexpr int kStride = block_stride(BF, D);
-  __shared__ __align__(16) uint8_t blk[kStride];
-  __shared__ uint8_t codes[16][D];
-  __shared__ __align__(16) float xs[16][D];
-  const int j = blockIdx.x, h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
-  const int tid = threadIdx.x;
+constexpr size_t token_smem_bytes() {
+  return (size_t)token_ppc<BF>() * (16 * (D + D / 32) * 4 + block_stride(BF, D) + 16 * D);
+}
+
+template <int BF, int D>
+__global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 5) append_token_kernel(const AppendArgs a) {
+  // rows padded by one float per 32 channels: with D + D / 32 floats a row, the
+  // lanes of a quantizing warp (each on its own token and channel group) read
+  // 32 distinct banks
+  constexpr int kStride = block_stride(BF, D), PPC = token_ppc<BF>(), GT = 256 / PPC, XS = D + D / 32;
+  static_assert(kStride % 16 == 0, "per-page blocks must stay 16-byte aligned");
+  extern __shared__ __align__(16) uint8_t tsm[];
+  auto xs = reinterpret_cast<float (*)[16][XS]>(tsm);
+  auto blk = reinterpret_cast<uint8_t (*)[kStride]>(tsm + PPC * 16 * XS * 4);
+  auto codes = reinterpret_cast<uint8_t (*)[16][D]>(tsm + PPC * (16 * XS * 4 + kStride));
+  const int h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
+  const int grp = (int)threadIdx.x / GT;           // one thread group (its own named barrier) per page
+  const Grp g{(int)threadIdx.x % GT, GT, 1 + grp};
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int end = start + n, pg = start / kPage + j;
-  if (pg * kPage >= end) return;
+  const int end = start + n, pg = start / kPage + (int)blockIdx.x * PPC + grp;
+  if (pg * kPage >= end) return;   // no token of this append lands in the group's page
   const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
   const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
   uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
-  for (int i = tid; i < (hi - lo) * (D / 8); i += blockDim.x) {
+  for (int i = g.tid; i < (hi - lo) * (D / 8); i += g.n) {
     const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8));
-    load_in8(a, role, b, lo + tt - start, h, c, D, &xs[(lo % kPage) + tt][c]);
+    load_in8(a, role, b, lo + tt - start, h, c, D, &xs[grp][(lo % kPage) + tt][c + c / 32]);
   }
-  token_block_update<BF, D, D>(a, role, xs, lo % kPage, lo % kPage + (hi - lo), gblk, blk, codes, whole_cta());
+  token_block_update<BF, D, XS, 1>(a, role, xs[grp], lo % kPage, lo % kPage + (hi - lo), gblk, blk[grp], codes[grp],
+                                   g);
 }
 
 // ----------------------------------------------------------------------------- page formats
@@ -887,8 +910,17 @@ template <int D>
 static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
   const int pages_max = (a.t_new + kPage - 1) / kPage + 1;
   const dim3 grid(pages_max, a.Hkv * 2, a.B);
-  if (a.fmt == KVQ_FMT_INT4_G32) append_token_kernel<kBlkInt4, D><<<grid, 256, 0, st>>>(a);
-  else if (a.fmt == KVQ_FMT_FP4_E2M1_S16) append_token_kernel<kBlkE2m1, D><<<grid, 256, 0, st>>>(a);
+  if (a.fmt == KVQ_FMT_INT4_G32 || a.fmt == KVQ_FMT_FP4_E2M1_S16) {
+    const bool i4 = a.fmt == KVQ_FMT_INT4_G32;
+    const auto kern = i4 ? append_token_kernel<kBlkInt4, D> : append_token_kernel<kBlkE2m1, D>;
+    const size_t smem = i4 ? token_smem_bytes<kBlkInt4, D>() : token_smem_bytes<kBlkE2m1, D>();
+    const int ppc = i4 ? token_ppc<kBlkInt4>() : token_ppc<kBlkE2m1>();
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    kern<<<dim3((pages_max + ppc - 1) / ppc, a.Hkv * 2, a.B), 256, smem, st>>>(a);
+  }
   else if (a.fmt == KVQ_FMT_CB2_GROUP4) {
     constexpr size_t smem = group_smem_bytes<D>();
     if (smem > 48 * 1024) {
