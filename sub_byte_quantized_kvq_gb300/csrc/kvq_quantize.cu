@@ -28,25 +28,42 @@ namespace kvq {
 
 enum { kSeqOk = 0, kSeqNothing = 1, kSeqCapacity = 2, kSeqBadPage = 3 };
 
-// Decide, identically in every launch, whether sequence b's append proceeds.
-// Every thread of the CTA calls it together: they share the page-table checks
-// (one strided pass) and agree on the answer.
-__device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) {
+// The part of the append decision that needs no page-table check: kSeqOk
+// means pages [first, last] must still be checked.
+__device__ __forceinline__ int seq_append_head(const AppendArgs& a, int b, int& start, int& n, int& first, int& last) {
   start = a.seq_lens[b];
   n = a.t_per_seq ? a.t_per_seq[b] : a.t_new;
   if (n <= 0) return kSeqNothing;
   if (n > a.t_new || start < 0 || (long long)start + n > (long long)a.ppsm * kPage) return kSeqCapacity;
   // a completed CB2 group rewrites all of its pages, including earlier ones
-  const int first = a.fmt == KVQ_FMT_CB2_GROUP4 ? (start / (kPage * kGroupPages)) * kGroupPages : start / kPage;
-  const int last = (start + n - 1) / kPage;
+  first = a.fmt == KVQ_FMT_CB2_GROUP4 ? (start / (kPage * kGroupPages)) * kGroupPages : start / kPage;
+  last = (start + n - 1) / kPage;
+  return kSeqOk;
+}
+__device__ __forceinline__ bool page_entry_ok(const AppendArgs& a, int b, int pg) {
+  const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
+  return (u >> 31) ? (a.fmt == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
+}
+
+// Decide, identically in every launch, whether sequence b's append proceeds.
+// Every thread of the CTA calls it together: they share the page-table checks
+// (one strided pass) and agree on the answer.
+__device__ int seq_append_state(const AppendArgs& a, int b, int& start, int& n) {
+  int first = 0, last = -1;
+  const int st = seq_append_head(a, b, start, n, first, last);
   int bad = 0;
-  for (int pg = first + (int)threadIdx.x; pg <= last; pg += (int)blockDim.x) {
-    const uint32_t u = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg], phys = u & 0x7FFFFFFFu;
-    const bool ok = (u >> 31) ? (a.fmt == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages)
-                              : phys < (uint32_t)a.num_pages;
-    bad |= !ok;
-  }
+  for (int pg = first + (int)threadIdx.x; pg <= last; pg += (int)blockDim.x) bad |= !page_entry_ok(a, b, pg);
+  if (st != kSeqOk) return st;
   return __syncthreads_or(bad) ? kSeqBadPage : kSeqOk;
+}
+// The same decision taken by one thread alone.
+__device__ int seq_append_state_1(const AppendArgs& a, int b, int& start, int& n) {
+  int first = 0, last = -1;
+  const int st = seq_append_head(a, b, start, n, first, last);
+  if (st != kSeqOk) return st;
+  for (int pg = first; pg <= last; ++pg)
+    if (!page_entry_ok(a, b, pg)) return kSeqBadPage;
+  return kSeqOk;
 }
 
 // Channels [c, c + 8) of new token t (c a multiple of 8) as fp32 into dst[0..8):
@@ -1234,6 +1251,303 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
   }
 }
 
+// ----------------------------------------------------------------------------- one-token fused projection
+// A one-token append (decode time) has one row per sequence: as a 128-row
+// tcgen05 tile it would stream a head's whole weight for each sequence.  Here
+// the rows of up to 16 sequences share one pass over the weights, the hidden
+// dimension is split across the CTAs of a thread-block cluster (each streams
+// its slice of the head's K | V weight rows straight from HBM into mma.sync
+// fragments), the partial sums meet in distributed shared memory in rank
+// order, and each (sequence, K|V) row is then quantized by one thread group of
+// the cluster exactly as in the tile kernel's epilogue.
+namespace small {
+constexpr int kRows = 16;      // sequences per cluster (two n8 tiles)
+constexpr int kThreads = 256;  // 8 warps; two 128-thread groups in the epilogue
+constexpr int kMaxSlice = 1024;   // hidden columns one CTA stages (16 rows of bf16: 32 KB)
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// fp32 at shared address `a` of cluster CTA `rank`
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Rows of one quantization unit and the epilogue scratch of one thread group.
+template <int KIND, int D>
+struct Plan {
+  static constexpr int U = KIND == kProjGroup ? kPage * kGroupPages : kPage;
+  static constexpr int XS = D + 4;
+  static constexpr int XB = U * XS * 4;   // the unit's fp32 rows
+  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
+                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
+                          : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
+                                                : kGroupPages * block_stride(kBlkCb2g, D) + U * (D / 32) * 4 + D * 16;
+  static constexpr int EW = (XB + WS + 127) / 128 * 128;
+  static constexpr int PART = kRows * 2 * D * 4;   // fp32 partial sums [row][K | V channel]
+  // weight ring: a stage is RK hidden columns of the CTA's 2D weight rows; a
+  // thread copies its own 16-byte pieces and reads back only those
+  static constexpr int MPW = 2 * D / 16 / 8, RK = 64, NSTG = D == 128 ? 4 : 6;
+  static constexpr int WSTG = (RK / 32) * MPW * 2 * 512, STAGE = 8 * WSTG, RING = NSTG * STAGE;
+  static constexpr int smem(int slice) {
+    return PART + (kRows * slice * 2 + RING > 2 * EW ? kRows * slice * 2 + RING : 2 * EW) + 64;
+  }
+};
+
+static_assert(Plan<kProjGroup, 128>::smem(kMaxSlice) <= 227 * 1024 && Plan<kProjPage, 128>::smem(kMaxSlice) <= 227 * 1024 &&
+                  Plan<kProjInt4, 128>::smem(kMaxSlice) <= 227 * 1024 && Plan<kProjGroup, 64>::smem(kMaxSlice) <= 227 * 1024,
+              "one-token projection plan does not fit");
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs p, int slice) {
+  using P = Plan<KIND, D>;
+  constexpr int U = P::U, XS = P::XS, N = 2 * D;
+  extern __shared__ __align__(128) uint8_t osm[];
+  const AppendArgs& a = p.a;
+  float(*part)[N] = reinterpret_cast<float(*)[N]>(osm);
+  uint8_t* region = osm + P::PART;   // x slice and weight ring, then the epilogue scratch
+  int* rstart = reinterpret_cast<int*>(region + Plan<KIND, D>::smem(slice) - P::PART - 64);   // [kRows], -1 = skip
+  const uint32_t rank = cluster_rank();
+  const int h = blockIdx.y, b0 = blockIdx.z * kRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
+
+  // partial[row][oc] = sum over this slice of x[row][k] * W[oc][k].  The
+  // A fragment (16 output channels x 16 k) and the B fragment (16 k x 8
+  // rows) of lane (g, q) take the same 8 consecutive k of a 32-column step
+  // from one 16-byte piece each: k order inside a step is permuted alike on
+  // both sides, so the products pair up.  The weights stream through a ring
+  // of cp.async stages (nothing held in registers while in flight).
+  constexpr int MPW = P::MPW, RK = P::RK, NSTG = P::NSTG;
+  const size_t k0 = (size_t)rank * slice;
+  const __nv_bfloat16* wrow[MPW][2];
+#pragma unroll
+  for (int m = 0; m < MPW; ++m) {
+    const int oc = 16 * (warp * MPW + m), role = oc / D, c = oc % D;
+    wrow[m][0] = p.w[role] + (size_t)(h * D + c + g) * p.hidden + k0 + 8 * q4;
+    wrow[m][1] = wrow[m][0] + (size_t)8 * p.hidden;
+  }
+  __nv_bfloat16* xsl = reinterpret_cast<__nv_bfloat16*>(region);
+  const uint32_t ring_s = smem_u32(region + kRows * slice * 2) + warp * P::WSTG + 16 * lane;
+  const int nst = slice / RK;
+  auto issue = [&](int st) {
+    if (st < nst) {
+      const uint32_t d = ring_s + (st % NSTG) * P::STAGE;
+#pragma unroll
+      for (int u = 0; u < RK / 32; ++u)
+#pragma unroll
+        for (int m = 0; m < MPW; ++m)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) cp_async16(d + ((u * MPW + m) * 2 + hf) * 512, wrow[m][hf] + st * RK + 32 * u);
+    }
+    cp_async_commit();
+  };
+#pragma unroll 1
+  for (int st = 0; st < NSTG - 1; ++st) issue(st);
+
+  // which rows append a token (one thread per row; every CTA of the cluster
+  // decides the same), and x[b][0][rank * slice ...] of the tile's rows
+  if (tid < kRows) {
+    int start = -1, n = 0;
+    const bool ok = b0 + tid < a.B && seq_append_state_1(a, b0 + tid, start, n) == kSeqOk;
+    rstart[tid] = ok ? start : -1;
+  }
+  for (int i = tid; i < kRows * slice / 8; i += kThreads) {
+    const int r = i / (slice / 8), c = 8 * (i - r * (slice / 8));
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (b0 + r < a.B) v = *reinterpret_cast<const uint4*>(p.x + (size_t)(b0 + r) * a.t_new * p.hidden + k0 + c);
+    *reinterpret_cast<uint4*>(xsl + r * slice + c) = v;
+  }
+  __syncthreads();
+
+  const bool two = a.B - b0 > 8;   // rows 8..15 exist
+  float acc[MPW][2][4];
+#pragma unroll
+  for (int m = 0; m < MPW; ++m)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
+  const uint32_t xa = smem_u32(xsl) + 2 * (g * slice + 8 * q4), xb = xa + 2 * 8 * slice;
+  auto step = [&](int kk, const uint4 (&wa)[MPW], const uint4 (&wb)[MPW]) {
+    const uint4 x0 = lds128(xa + 2 * kk);
+    const uint4 x1 = two ? lds128(xb + 2 * kk) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int m = 0; m < MPW; ++m) {
+      mma_bf16(acc[m][0], wa[m].x, wb[m].x, wa[m].y, wb[m].y, x0.x, x0.y);
+      mma_bf16(acc[m][0], wa[m].z, wb[m].z, wa[m].w, wb[m].w, x0.z, x0.w);
+      if (two) {
+        mma_bf16(acc[m][1], wa[m].x, wb[m].x, wa[m].y, wb[m].y, x1.x, x1.y);
+        mma_bf16(acc[m][1], wa[m].z, wb[m].z, wa[m].w, wb[m].w, x1.z, x1.w);
+      }
+    }
+  };
+#pragma unroll 1
+  for (int st = 0; st < nst; ++st) {
+    issue(st + NSTG - 1);
+    cp_async_wait<NSTG - 1>();   // stage st has landed (groups complete in order)
+    const uint32_t d = ring_s + (st % NSTG) * P::STAGE;
+#pragma unroll
+    for (int u = 0; u < RK / 32; ++u) {
+      uint4 wa[MPW], wb[MPW];
+#pragma unroll
+      for (int m = 0; m < MPW; ++m) {
+        wa[m] = lds128(d + ((u * MPW + m) * 2) * 512);
+        wb[m] = lds128(d + ((u * MPW + m) * 2 + 1) * 512);
+      }
+      step(st * RK + 32 * u, wa, wb);
+    }
+  }
+  cp_async_wait<0>();
+  if (slice % RK) {   // a last 32-column step
+    const int kk = nst * RK;
+    uint4 wa[MPW], wb[MPW];
+#pragma unroll
+    for (int m = 0; m < MPW; ++m) {
+      wa[m] = ldg_stream(wrow[m][0] + kk);
+      wb[m] = ldg_stream(wrow[m][1] + kk);
+    }
+    step(kk, wa, wb);
+  }
+  // accumulator (channel g | g + 8 of the m tile, row 2q | 2q + 1 of the n tile)
+#pragma unroll
+  for (int m = 0; m < MPW; ++m) {
+    const int oc = 16 * (warp * MPW + m) + g;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int r = 8 * nt + 2 * q4;
+      part[r][oc] = acc[m][nt][0];
+      part[r + 1][oc] = acc[m][nt][1];
+      part[r][oc + 8] = acc[m][nt][2];
+      part[r + 1][oc + 8] = acc[m][nt][3];
+    }
+  }
+  cluster_sync();   // every partial is visible cluster-wide; the x slices are dead
+
+  // units (row, K|V): unit 2 rank + grp, then + 2 * cluster size ...
+  const int grp = tid >> 7;
+  const Grp gp{tid & 127, 128, 1 + grp};
+  uint8_t* ew = region + grp * P::EW;
+  float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(ew);
+  uint8_t* ws = ew + P::XB;
+  const int nrank = (int)gridDim.x;
+  for (int unit = 2 * (int)rank + grp; unit < 2 * kRows; unit += 2 * nrank) {
+    const int r = unit >> 1, role = unit & 1, b = b0 + r, pos = rstart[r];
+    if (pos < 0) continue;   // uniform within the group
+    const int32_t* ptb = a.page_table + (size_t)b * a.ppsm;
+    const int slot = pos % U;
+    // the row's sum over the cluster's slices, in rank order
+    float v = 0.f;
+    if (gp.tid < D) {
+      const uint32_t ad = smem_u32(&part[r][role * D + gp.tid]);
+      float pv[16];   // all remote loads in flight at once, then the sum in rank order
+#pragma unroll
+      for (int q = 0; q < 16; ++q) pv[q] = q < nrank ? ld_cluster_f32(ad, (uint32_t)q) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q < nrank) v += pv[q];
+      if (p.kv_out) p.kv_out[((((size_t)role * a.B + b) * a.t_new) * a.Hkv + h) * D + gp.tid] = v;
+    }
+    if constexpr (KIND == kProjInt4 || KIND == kProjE2m1) {
+      constexpr int BF = KIND == kProjInt4 ? kBlkInt4 : kBlkE2m1, kStride = block_stride(BF, D);
+      if (gp.tid < D) xs[slot][gp.tid] = v;
+      const uint32_t phys = (uint32_t)ptb[pos / U] & 0x7FFFFFFFu;
+      token_block_update<BF, D, XS>(a, role, xs, slot, slot + 1, a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride,
+                                    ws, reinterpret_cast<uint8_t(*)[D]>(ws + kStride), gp);
+    } else {
+      float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
+      if (slot < U - 1) {   // the unit is not complete: the row waits in staging
+        if (gp.tid < D) stg[slot * D + gp.tid] = v;
+      } else {
+        for (int i = gp.tid; i < (U - 1) * D; i += gp.n) xs[i / D][i % D] = stg[i];
+        if (gp.tid < D) xs[U - 1][gp.tid] = v;
+        if constexpr (KIND == kProjPage) {
+          constexpr int kB = page_blk_bytes<D>();
+          const PageWs<D> pw{reinterpret_cast<uint8_t(*)[D]>(ws + kB), reinterpret_cast<uint8_t(*)[D]>(ws + kB + 16 * D), ws,
+                             reinterpret_cast<float*>(ws + kB + 32 * D)};
+          page_quantize<D, XS>(a, h, role, (uint32_t)ptb[pos / U], xs, pw, gp);
+        } else {
+          constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
+          const GroupWs<D> gw{reinterpret_cast<uint32_t*>(ws + kB), reinterpret_cast<uint32_t(*)[4]>(ws + kB + U * (D / 32) * 4),
+                              ws};
+          group_quantize<D, XS>(a, h, role, ptb, pos / U, xs, gw, gp, false);
+        }
+      }
+    }
+    gp.sync();   // the scratch is reused by the group's next unit
+  }
+  cluster_sync();   // no CTA leaves while another may still read its partials
+}
+
+// Cluster size for a one-token projection of `hidden` columns: the largest of
+// 16, 8, 4, 2, 1 that splits hidden into 32-column multiples of at most
+// kMaxSlice columns; 0 when none does.
+inline int cluster_for(int hidden) {
+  for (int cs = 16; cs >= 1; cs >>= 1)
+    if (hidden % (32 * cs) == 0 && hidden / cs <= kMaxSlice) return cs;
+  return 0;
+}
+
+template <int KIND, int D>
+cudaError_t launch(ProjArgs& p, int cs, cudaStream_t st) {
+  const int slice = p.hidden / cs;
+  const size_t smem = (size_t)Plan<KIND, D>::smem(slice);
+  auto kern = project_one_kernel<KIND, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)cs, (unsigned)p.a.Hkv, (unsigned)((p.a.B + kRows - 1) / kRows));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nclusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (nclusters < 1) return cudaErrorLaunchOutOfResources;
+  e = cudaLaunchKernelEx(&cfg, kern, p, slice);
+  if (e != cudaSuccess) return e;
+  append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
+  return cudaGetLastError();
+}
+}  // namespace small
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1265,6 +1579,14 @@ static bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint6
 template <int KIND, int D>
 static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
   using P = ProjPlan<KIND, D>;
+  if (p.a.t_new == 1) {   // one token per sequence: the cluster split-K kernel
+    for (int cs = small::cluster_for(p.hidden); cs >= 1; cs >>= 1) {
+      if (p.hidden % (32 * cs) || p.hidden / cs > small::kMaxSlice) break;
+      const cudaError_t e = small::launch<KIND, D>(p, cs, st);
+      if (e == cudaSuccess) return e;
+      (void)cudaGetLastError();   // the configuration was refused: a smaller cluster, else the tile kernel
+    }
+  }
   if (!encode_rows(&p.tm_x, p.x, (uint64_t)p.a.B * p.a.t_new, (uint64_t)p.hidden, (uint32_t)P::U) ||
       !encode_rows(&p.tm_w[0], p.w[0], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D) ||
       !encode_rows(&p.tm_w[1], p.w[1], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D))

@@ -11,7 +11,7 @@ import torch
 import oracle
 from sub_byte_quantized_kvq_gb300 import kvq, synth
 
-from _kvq_pairs import Pair
+from _kvq_pairs import Pair, make_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -78,6 +78,63 @@ def test_project_single_token_decode_appends():
     x, wk, wv = synth.projection_inputs(6, B, 40, hidden, Hkv, D)
     for t in range(40):
         pair.project(x[:, t:t + 1].contiguous(), wk, wv, [1, 1 if t % 3 else 0, 1])
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_project_one_token_appends_every_format(fmt, D):
+    """One-token appends (the decode-time shape: one row per sequence, a
+    cluster of CTAs splitting the hidden dimension): 19 sequences (a 16-row
+    tile and a 3-row one), positions ragged so that pages and the first
+    64-token group complete on different steps, sequences that skip a step,
+    hidden 4096 (16 slices of 256 columns)."""
+    B, Hkv, P, hidden = 19, 2, 5, 4096
+    pair = Pair(fmt, B, Hkv, D, P, seed=13, tiers=tiers_for(fmt, B, P))
+    k0, v0 = make_kv(13, B, 62, Hkv, D)
+    pair.append(k0, v0, t_per_seq=[57 + b % 6 for b in range(B)])
+    pair.assert_cache_equal()
+    x, wk, wv = synth.projection_inputs(13, B, 9, hidden, Hkv, D)
+    for t in range(9):
+        tps = [0 if (b + t) % 5 == 0 else 1 for b in range(B)]
+        xt = x[:, t:t + 1].contiguous()
+        k, v = pair.project(xt, wk, wv, tps)
+        assert_projection_close(k, xt, wk, "K", Hkv, D, tps)
+        assert_projection_close(v, xt, wv, "V", Hkv, D, tps)
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("hidden", [32, 96, 992, 8192, 32768])
+def test_project_one_token_cluster_sizes(hidden):
+    """hidden 32 / 96 (one CTA: a 32-column step past the 64-column stages),
+    992 (one CTA: fifteen stages and a 32-column step), 8192 (16 CTAs of 512
+    columns), 32768 (too wide for a cluster's slices: the tile kernel)."""
+    B, Hkv, D, P = 9, 2, 128, 2
+    pair = Pair(kvq.KVQ_FMT_CB2_OUTLIER, B, Hkv, D, P, seed=15)
+    x, wk, wv = synth.projection_inputs(15, B, 17, hidden, Hkv, D)
+    for t in range(17):
+        xt = x[:, t:t + 1].contiguous()
+        k, v = pair.project(xt, wk, wv)
+        assert_projection_close(k, xt, wk, "K", Hkv, D, None)
+        assert_projection_close(v, xt, wv, "V", Hkv, D, None)
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_FP4_E2M1_S16, kvq.KVQ_FMT_CB2_OUTLIER])
+def test_project_one_token_full_size(fmt):
+    """The decode shapes' per-step append: 16 sequences, 8 kv heads, head_dim
+    128, hidden 8192 (E2M1) or 4096 (CB2), 17 steps so that every sequence
+    completes a page on the 16th."""
+    B, Hkv, D, P = 16, 8, 128, 2
+    hidden = 8192 if fmt == kvq.KVQ_FMT_FP4_E2M1_S16 else 4096
+    pair = Pair(fmt, B, Hkv, D, P, seed=14)
+    x, wk, wv = synth.projection_inputs(14, B, 17, hidden, Hkv, D)
+    for t in range(17):
+        xt = x[:, t:t + 1].contiguous()
+        k, v = pair.project(xt, wk, wv)
+        if t in (0, 15, 16):
+            assert_projection_close(k, xt, wk, "K", Hkv, D, None)
+            assert_projection_close(v, xt, wv, "V", Hkv, D, None)
     pair.assert_cache_equal()
 
 
