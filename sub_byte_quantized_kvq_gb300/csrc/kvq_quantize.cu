@@ -1261,7 +1261,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
 // order, and each (sequence, K|V) row is then quantized by one thread group of
 // the cluster exactly as in the tile kernel's epilogue.
 namespace small {
-constexpr int kRows = 16;      // sequences per cluster (two n8 tiles)
+constexpr int kMaxRows = 32;   // sequences per cluster: 16 (two n8 tiles) or 32 (four)
 constexpr int kThreads = 256;  // 8 warps; two 128-thread groups in the epilogue
 constexpr int kMaxSlice = 1024;   // hidden columns one CTA stages (16 rows of bf16: 32 KB)
 
@@ -1305,8 +1305,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Rows of one quantization unit and the epilogue scratch of one thread group.
-template <int KIND, int D>
+// Rows of one quantization unit and the epilogue scratch of one thread group;
+// R sequences per cluster.
+template <int KIND, int D, int R>
 struct Plan {
   static constexpr int U = KIND == kProjGroup ? kPage * kGroupPages : kPage;
   static constexpr int XS = D + 4;
@@ -1316,31 +1317,33 @@ struct Plan {
                           : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
                                                 : kGroupPages * block_stride(kBlkCb2g, D) + U * (D / 32) * 4 + D * 16;
   static constexpr int EW = (XB + WS + 127) / 128 * 128;
-  static constexpr int PART = kRows * 2 * D * 4;   // fp32 partial sums [row][K | V channel]
+  static constexpr int PART = R * 2 * D * 4;   // fp32 partial sums [row][K | V channel]
   // weight ring: a stage is RK hidden columns of the CTA's 2D weight rows; a
   // thread copies its own 16-byte pieces and reads back only those
   static constexpr int MPW = 2 * D / 16 / 8, RK = 64, NSTG = D == 128 ? 4 : 6;
   static constexpr int WSTG = (RK / 32) * MPW * 2 * 512, STAGE = 8 * WSTG, RING = NSTG * STAGE;
   static constexpr int smem(int slice) {
-    return PART + (kRows * slice * 2 + RING > 2 * EW ? kRows * slice * 2 + RING : 2 * EW) + 64;
+    return PART + (R * slice * 2 + RING > 2 * EW ? R * slice * 2 + RING : 2 * EW) + 4 * R;
   }
 };
 
-static_assert(Plan<kProjGroup, 128>::smem(kMaxSlice) <= 227 * 1024 && Plan<kProjPage, 128>::smem(kMaxSlice) <= 227 * 1024 &&
-                  Plan<kProjInt4, 128>::smem(kMaxSlice) <= 227 * 1024 && Plan<kProjGroup, 64>::smem(kMaxSlice) <= 227 * 1024,
+static_assert(Plan<kProjGroup, 128, kMaxRows>::smem(kMaxSlice) <= 227 * 1024 &&
+                  Plan<kProjPage, 128, kMaxRows>::smem(kMaxSlice) <= 227 * 1024 &&
+                  Plan<kProjInt4, 128, kMaxRows>::smem(kMaxSlice) <= 227 * 1024 &&
+                  Plan<kProjGroup, 64, kMaxRows>::smem(kMaxSlice) <= 227 * 1024,
               "one-token projection plan does not fit");
 
-template <int KIND, int D>
+template <int KIND, int D, int R>
 __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs p, int slice) {
-  using P = Plan<KIND, D>;
+  using P = Plan<KIND, D, R>;
   constexpr int U = P::U, XS = P::XS, N = 2 * D;
   extern __shared__ __align__(128) uint8_t osm[];
   const AppendArgs& a = p.a;
   float(*part)[N] = reinterpret_cast<float(*)[N]>(osm);
   uint8_t* region = osm + P::PART;   // x slice and weight ring, then the epilogue scratch
-  int* rstart = reinterpret_cast<int*>(region + Plan<KIND, D>::smem(slice) - P::PART - 64);   // [kRows], -1 = skip
+  int* rstart = reinterpret_cast<int*>(osm + P::smem(slice) - 4 * R);   // [R], -1 = skip
   const uint32_t rank = cluster_rank();
-  const int h = blockIdx.y, b0 = blockIdx.z * kRows;
+  const int h = blockIdx.y, b0 = blockIdx.z * R;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
 
   // partial[row][oc] = sum over this slice of x[row][k] * W[oc][k].  The
@@ -1359,7 +1362,7 @@ __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs
     wrow[m][1] = wrow[m][0] + (size_t)8 * p.hidden;
   }
   __nv_bfloat16* xsl = reinterpret_cast<__nv_bfloat16*>(region);
-  const uint32_t ring_s = smem_u32(region + kRows * slice * 2) + warp * P::WSTG + 16 * lane;
+  const uint32_t ring_s = smem_u32(region + R * slice * 2) + warp * P::WSTG + 16 * lane;
   const int nst = slice / RK;
   auto issue = [&](int st) {
     if (st < nst) {
@@ -1376,38 +1379,40 @@ __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs
 #pragma unroll 1
   for (int st = 0; st < NSTG - 1; ++st) issue(st);
 
-  // which rows append a token (one thread per row; every CTA of the cluster
-  // decides the same), and x[b][0][rank * slice ...] of the tile's rows
-  if (tid < kRows) {
-    int start = -1, n = 0;
-    const bool ok = b0 + tid < a.B && seq_append_state_1(a, b0 + tid, start, n) == kSeqOk;
-    rstart[tid] = ok ? start : -1;
-  }
-  for (int i = tid; i < kRows * slice / 8; i += kThreads) {
+  // x[b][0][rank * slice ...] of the tile's rows
+  for (int i = tid; i < R * slice / 8; i += kThreads) {
     const int r = i / (slice / 8), c = 8 * (i - r * (slice / 8));
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (b0 + r < a.B) v = *reinterpret_cast<const uint4*>(p.x + (size_t)(b0 + r) * a.t_new * p.hidden + k0 + c);
     *reinterpret_cast<uint4*>(xsl + r * slice + c) = v;
   }
   __syncthreads();
+  // which rows append a token (one thread per row; every CTA of the cluster
+  // decides the same; read only after the cluster barrier below): the first
+  // warp takes these dependent loads while its copies are in flight
+  if (tid < R) {
+    int start = -1, n = 0;
+    const bool ok = b0 + tid < a.B && seq_append_state_1(a, b0 + tid, start, n) == kSeqOk;
+    rstart[tid] = ok ? start : -1;
+  }
 
-  const bool two = a.B - b0 > 8;   // rows 8..15 exist
-  float acc[MPW][2][4];
+  constexpr int NT = R / 8;   // n8 tiles of rows
+  const int ntl = min(NT, (a.B - b0 + 7) / 8);   // the ones holding a sequence
+  float acc[MPW][NT][4];
 #pragma unroll
   for (int m = 0; m < MPW; ++m)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
-  const uint32_t xa = smem_u32(xsl) + 2 * (g * slice + 8 * q4), xb = xa + 2 * 8 * slice;
+    for (int nt = 0; nt < NT; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
+  const uint32_t xa = smem_u32(xsl) + 2 * (g * slice + 8 * q4);
   auto step = [&](int kk, const uint4 (&wa)[MPW], const uint4 (&wb)[MPW]) {
-    const uint4 x0 = lds128(xa + 2 * kk);
-    const uint4 x1 = two ? lds128(xb + 2 * kk) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int m = 0; m < MPW; ++m) {
-      mma_bf16(acc[m][0], wa[m].x, wb[m].x, wa[m].y, wb[m].y, x0.x, x0.y);
-      mma_bf16(acc[m][0], wa[m].z, wb[m].z, wa[m].w, wb[m].w, x0.z, x0.w);
-      if (two) {
-        mma_bf16(acc[m][1], wa[m].x, wb[m].x, wa[m].y, wb[m].y, x1.x, x1.y);
-        mma_bf16(acc[m][1], wa[m].z, wb[m].z, wa[m].w, wb[m].w, x1.z, x1.w);
+    for (int nt = 0; nt < NT; ++nt) {
+      if (nt > 0 && nt >= ntl) break;   // uniform
+      const uint4 x = lds128(xa + 2 * (8 * nt * slice + kk));
+#pragma unroll
+      for (int m = 0; m < MPW; ++m) {
+        mma_bf16(acc[m][nt], wa[m].x, wb[m].x, wa[m].y, wb[m].y, x.x, x.y);
+        mma_bf16(acc[m][nt], wa[m].z, wb[m].z, wa[m].w, wb[m].w, x.z, x.w);
       }
     }
   };
@@ -1443,7 +1448,7 @@ __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs
   for (int m = 0; m < MPW; ++m) {
     const int oc = 16 * (warp * MPW + m) + g;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
       const int r = 8 * nt + 2 * q4;
       part[r][oc] = acc[m][nt][0];
       part[r + 1][oc] = acc[m][nt][1];
@@ -1460,47 +1465,58 @@ __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs
   float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(ew);
   uint8_t* ws = ew + P::XB;
   const int nrank = (int)gridDim.x;
-  for (int unit = 2 * (int)rank + grp; unit < 2 * kRows; unit += 2 * nrank) {
+  // channel c of row r, role: the sum over the cluster's slices in rank order
+  // (all remote loads in flight at once), also written to kv_out
+  auto row_sum = [&](int r, int role, int c) {
+    const uint32_t ad = smem_u32(&part[r][role * D + c]);
+    float pv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) pv[q] = q < nrank ? ld_cluster_f32(ad, (uint32_t)q) : 0.f;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (q < nrank) v += pv[q];
+    if (p.kv_out) p.kv_out[((((size_t)role * a.B + b0 + r) * a.t_new) * a.Hkv + h) * D + c] = v;
+    return v;
+  };
+  if constexpr (KIND == kProjPage || KIND == kProjGroup) {
+    // rows that only wait in staging (their unit is not complete): the whole
+    // CTA at once, rows rank, rank + cluster size, ...
+    const int nr = (R - (int)rank + nrank - 1) / nrank;
+    for (int i = tid; i < nr * 2 * D; i += kThreads) {
+      const int c = i % D, role = (i / D) & 1, r = (int)rank + nrank * (i / (2 * D)), pos = rstart[r];
+      if (pos < 0 || pos % U == U - 1) continue;
+      const float v = row_sum(r, role, c);
+      a.staging[((((size_t)(b0 + r) * a.Hkv + h) * 2 + role) * U + pos % U) * D + c] = v;
+    }
+  }
+  for (int unit = 2 * (int)rank + grp; unit < 2 * R; unit += 2 * nrank) {
     const int r = unit >> 1, role = unit & 1, b = b0 + r, pos = rstart[r];
     if (pos < 0) continue;   // uniform within the group
     const int32_t* ptb = a.page_table + (size_t)b * a.ppsm;
     const int slot = pos % U;
-    // the row's sum over the cluster's slices, in rank order
-    float v = 0.f;
-    if (gp.tid < D) {
-      const uint32_t ad = smem_u32(&part[r][role * D + gp.tid]);
-      float pv[16];   // all remote loads in flight at once, then the sum in rank order
-#pragma unroll
-      for (int q = 0; q < 16; ++q) pv[q] = q < nrank ? ld_cluster_f32(ad, (uint32_t)q) : 0.f;
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        if (q < nrank) v += pv[q];
-      if (p.kv_out) p.kv_out[((((size_t)role * a.B + b) * a.t_new) * a.Hkv + h) * D + gp.tid] = v;
-    }
+    if ((KIND == kProjPage || KIND == kProjGroup) && slot < U - 1) continue;   // staged above
+    const float v = gp.tid < D ? row_sum(r, role, gp.tid) : 0.f;
     if constexpr (KIND == kProjInt4 || KIND == kProjE2m1) {
       constexpr int BF = KIND == kProjInt4 ? kBlkInt4 : kBlkE2m1, kStride = block_stride(BF, D);
       if (gp.tid < D) xs[slot][gp.tid] = v;
       const uint32_t phys = (uint32_t)ptb[pos / U] & 0x7FFFFFFFu;
       token_block_update<BF, D, XS>(a, role, xs, slot, slot + 1, a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride,
                                     ws, reinterpret_cast<uint8_t(*)[D]>(ws + kStride), gp);
-    } else {
-      float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
-      if (slot < U - 1) {   // the unit is not complete: the row waits in staging
-        if (gp.tid < D) stg[slot * D + gp.tid] = v;
+    } else {   // the row completes its unit
+      const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
+      for (int i = gp.tid; i < (U - 1) * D; i += gp.n) xs[i / D][i % D] = stg[i];
+      if (gp.tid < D) xs[U - 1][gp.tid] = v;
+      if constexpr (KIND == kProjPage) {
+        constexpr int kB = page_blk_bytes<D>();
+        const PageWs<D> pw{reinterpret_cast<uint8_t(*)[D]>(ws + kB), reinterpret_cast<uint8_t(*)[D]>(ws + kB + 16 * D), ws,
+                           reinterpret_cast<float*>(ws + kB + 32 * D)};
+        page_quantize<D, XS>(a, h, role, (uint32_t)ptb[pos / U], xs, pw, gp);
       } else {
-        for (int i = gp.tid; i < (U - 1) * D; i += gp.n) xs[i / D][i % D] = stg[i];
-        if (gp.tid < D) xs[U - 1][gp.tid] = v;
-        if constexpr (KIND == kProjPage) {
-          constexpr int kB = page_blk_bytes<D>();
-          const PageWs<D> pw{reinterpret_cast<uint8_t(*)[D]>(ws + kB), reinterpret_cast<uint8_t(*)[D]>(ws + kB + 16 * D), ws,
-                             reinterpret_cast<float*>(ws + kB + 32 * D)};
-          page_quantize<D, XS>(a, h, role, (uint32_t)ptb[pos / U], xs, pw, gp);
-        } else {
-          constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
-          const GroupWs<D> gw{reinterpret_cast<uint32_t*>(ws + kB), reinterpret_cast<uint32_t(*)[4]>(ws + kB + U * (D / 32) * 4),
-                              ws};
-          group_quantize<D, XS>(a, h, role, ptb, pos / U, xs, gw, gp, false);
-        }
+        constexpr int kB = kGroupPages * block_stride(kBlkCb2g, D);
+        const GroupWs<D> gw{reinterpret_cast<uint32_t*>(ws + kB), reinterpret_cast<uint32_t(*)[4]>(ws + kB + U * (D / 32) * 4),
+                            ws};
+        group_quantize<D, XS>(a, h, role, ptb, pos / U, xs, gw, gp, false);
       }
     }
     gp.sync();   // the scratch is reused by the group's next unit
@@ -1517,11 +1533,13 @@ inline int cluster_for(int hidden) {
   return 0;
 }
 
-template <int KIND, int D>
-cudaError_t launch(ProjArgs& p, int cs, cudaStream_t st) {
+// Launches with clusters of cs CTAs; with one_wave, only when every cluster
+// can be resident at once (else cudaErrorLaunchOutOfResources, nothing launched).
+template <int KIND, int D, int R>
+cudaError_t launch_r(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
   const int slice = p.hidden / cs;
-  const size_t smem = (size_t)Plan<KIND, D>::smem(slice);
-  auto kern = project_one_kernel<KIND, D>;
+  const size_t smem = (size_t)Plan<KIND, D, R>::smem(slice);
+  auto kern = project_one_kernel<KIND, D, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -1531,7 +1549,7 @@ cudaError_t launch(ProjArgs& p, int cs, cudaStream_t st) {
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)cs, (unsigned)p.a.Hkv, (unsigned)((p.a.B + kRows - 1) / kRows));
+  cfg.gridDim = dim3((unsigned)cs, (unsigned)p.a.Hkv, (unsigned)((p.a.B + R - 1) / R));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1540,11 +1558,19 @@ cudaError_t launch(ProjArgs& p, int cs, cudaStream_t st) {
   int nclusters = 0;
   e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
   if (e != cudaSuccess) return e;
-  if (nclusters < 1) return cudaErrorLaunchOutOfResources;
+  if (nclusters < 1 || (one_wave && (long long)nclusters < (long long)cfg.gridDim.y * cfg.gridDim.z))
+    return cudaErrorLaunchOutOfResources;
   e = cudaLaunchKernelEx(&cfg, kern, p, slice);
   if (e != cudaSuccess) return e;
   append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
   return cudaGetLastError();
+}
+
+// 16 sequences per cluster, or 32 (the weights streamed half as often) when
+// there are more than 16.
+template <int KIND, int D>
+cudaError_t launch(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
+  return p.a.B > 16 ? launch_r<KIND, D, 32>(p, cs, one_wave, st) : launch_r<KIND, D, 16>(p, cs, one_wave, st);
 }
 }  // namespace small
 
@@ -1580,12 +1606,15 @@ template <int KIND, int D>
 static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
   using P = ProjPlan<KIND, D>;
   if (p.a.t_new == 1) {   // one token per sequence: the cluster split-K kernel
-    for (int cs = small::cluster_for(p.hidden); cs >= 1; cs >>= 1) {
-      if (p.hidden % (32 * cs) || p.hidden / cs > small::kMaxSlice) break;
-      const cudaError_t e = small::launch<KIND, D>(p, cs, st);
-      if (e == cudaSuccess) return e;
-      (void)cudaGetLastError();   // the configuration was refused: a smaller cluster, else the tile kernel
-    }
+    // the widest split (within the slice limit) whose clusters are all
+    // resident at once; failing that, the widest that launches at all
+    for (int pass = 0; pass < 2; ++pass)
+      for (int cs = small::cluster_for(p.hidden); cs >= 1; cs >>= 1) {
+        if (p.hidden % (32 * cs) || p.hidden / cs > small::kMaxSlice) break;
+        const cudaError_t e = small::launch<KIND, D>(p, cs, pass == 0, st);
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();   // refused: a narrower cluster, else the tile kernel
+      }
   }
   if (!encode_rows(&p.tm_x, p.x, (uint64_t)p.a.B * p.a.t_new, (uint64_t)p.hidden, (uint32_t)P::U) ||
       !encode_rows(&p.tm_w[0], p.w[0], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D) ||

@@ -85,10 +85,10 @@ def test_project_single_token_decode_appends():
 @pytest.mark.parametrize("fmt", FORMATS)
 def test_project_one_token_appends_every_format(fmt, D):
     """One-token appends (the decode-time shape: one row per sequence, a
-    cluster of CTAs splitting the hidden dimension): 19 sequences (a 16-row
-    tile and a 3-row one), positions ragged so that pages and the first
-    64-token group complete on different steps, sequences that skip a step,
-    hidden 4096 (16 slices of 256 columns)."""
+    cluster of CTAs splitting the hidden dimension): 19 sequences (one
+    32-row cluster, three of its four row tiles used), positions ragged so
+    that pages and the first 64-token group complete on different steps,
+    sequences that skip a step, hidden 4096 (16 slices of 256 columns)."""
     B, Hkv, P, hidden = 19, 2, 5, 4096
     pair = Pair(fmt, B, Hkv, D, P, seed=13, tiers=tiers_for(fmt, B, P))
     k0, v0 = make_kv(13, B, 62, Hkv, D)
@@ -117,6 +117,21 @@ def test_project_one_token_cluster_sizes(hidden):
         k, v = pair.project(xt, wk, wv)
         assert_projection_close(k, xt, wk, "K", Hkv, D, None)
         assert_projection_close(v, xt, wv, "V", Hkv, D, None)
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_INT4_G32, kvq.KVQ_FMT_TIERED])
+def test_project_one_token_many_sequences(fmt):
+    """40 sequences: clusters of 32 rows (a full one and one holding 8)."""
+    B, Hkv, D, P, hidden = 40, 2, 128, 2, 1024
+    pair = Pair(fmt, B, Hkv, D, P, seed=16, tiers=tiers_for(fmt, B, P))
+    x, wk, wv = synth.projection_inputs(16, B, 17, hidden, Hkv, D)
+    for t in range(17):
+        tps = [0 if (b * 7 + t) % 9 == 0 else 1 for b in range(B)]
+        xt = x[:, t:t + 1].contiguous()
+        k, v = pair.project(xt, wk, wv, tps)
+        assert_projection_close(k, xt, wk, "K", Hkv, D, tps)
+        assert_projection_close(v, xt, wv, "V", Hkv, D, tps)
     pair.assert_cache_equal()
 
 
