@@ -195,7 +195,9 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
  * with bf16 operands and fp32 accumulation on the tensor cores; k and v are
  * then quantized into the cache exactly as kvq_quantize_append quantizes fp32
  * inputs (same blocks, staging, seq_lens and status behaviour), without being
- * written to global memory.  Every format.
+ * written to global memory.  Every format.  A one-token append (t_new == 1,
+ * the decode-time case) splits hidden across the CTAs of a thread-block
+ * cluster and adds their fp32 partial sums in cluster order.
  *   x         device bf16 [num_seqs][t_new][hidden], 16-byte aligned.
  *   hidden    a positive multiple of 32.
  *   w_k, w_v  device bf16 [num_kv_heads * head_dim][hidden] (a linear layer's
