@@ -252,16 +252,61 @@ __device__ __forceinline__ void frag_inverse(int role, int lane, int s, int k, i
 }
 
 // ----------------------------------------------------------------------------- per-token formats
-// INT4 group-32 quantization of token slots [t0, min(t0 + 32 / NG, hi)) by one
-// warp (NG = D / 32 groups): lane s * NG + g owns group g of slot t0 + s.
-// Lanes past hi compute on slot t0 but store nothing; t0 < hi.  Channel c of a
+// Byte of a block's code words (fragment order, see frag_inverse) that holds
+// the 4-bit codes of K channels c, c + 1 (c even) of token t -- low, high
+// nibble -- and the byte that holds tokens t, t + 1 (t even) of V channel c.
+__device__ __forceinline__ int code_byte_k(int NS, int t, int c) {
+  const int cc = c & 15;
+  return 4 * NS * (4 * (t & 7) + ((cc & 7) >> 1)) + 4 * (c >> 4) + (t >> 3) + 2 * (cc >> 3);
+}
+__device__ __forceinline__ int code_byte_v(int NS, int t, int c) {
+  const int cc = c & 15;
+  return 4 * NS * (4 * (cc & 7) + ((t & 7) >> 1)) + 4 * (c >> 4) + 2 * (t >> 3) + (cc >> 3);
+}
+
+// Store the NC codes of one lane -- token t, channels c0 .. c0 + NC, code i at
+// bits 4 (i % 8) of nb[i / 8] -- into the block's code words.  Tokens outside
+// [lo, hi) keep their codes.  K bytes belong to one token.  A V byte holds an
+// even token and the next one: the even token's lane (always in the same
+// pass, whose first token is even) writes it, with its partner's codes (the
+// lane pd above, fetched by shuffle) or the kept nibble for a token outside
+// [lo, hi).  Every lane of the warp calls this (the shuffle).
+template <int NC>
+__device__ __forceinline__ void store_codes(uint8_t* blk, int role, int NS, int t, int c0, int lo, int hi,
+                                            const uint32_t (&nb)[NC / 8], int pd) {
+  const bool act = t >= lo && t < hi;
+  if (role == 0) {
+    if (act)
+#pragma unroll
+      for (int i = 0; i < NC; i += 2) blk[code_byte_k(NS, t, c0 + i)] = (uint8_t)(nb[i >> 3] >> (4 * (i & 7)));
+    return;
+  }
+  uint32_t pn[NC / 8];
+#pragma unroll
+  for (int w = 0; w < NC / 8; ++w) pn[w] = __shfl_down_sync(0xffffffffu, nb[w], pd);
+  if (!(t & 1)) {
+    const bool pact = t + 1 >= lo && t + 1 < hi;
+    if (!act && !pact) return;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      uint8_t* p = blk + code_byte_v(NS, t, c0 + i);
+      const uint32_t lo4 = act ? (nb[i >> 3] >> (4 * (i & 7))) & 0xFu : *p & 0xFu;
+      const uint32_t hi4 = pact ? (pn[i >> 3] >> (4 * (i & 7))) & 0xFu : *p >> 4;
+      *p = (uint8_t)(lo4 | (hi4 << 4));
+    }
+  }
+}
+
+// INT4 group-32 quantization of token slots [t0, t0 + 32 / NG) by one warp (NG
+// = D / 32 groups): lane s * NG + g owns group g of slot t0 + s; slots outside
+// [lo, hi) compute on slot t0 and store nothing.  t0 < hi.  Channel c of a
 // row sits at xs[t][c + GP * (c / 32)].
 template <int D, int XS, int GP>
-__device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
+__device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int hi, uint8_t* blk, int role,
                                      double sigma, int lane) {
   constexpr int NG = D / 32, CAP = int4_cap(D);
   const int g = lane % NG, t = t0 + lane / NG;
-  const bool act = t < hi;
+  const bool act = t >= lo && t < hi;
   const float* xg = xs[act ? t : t0] + (32 + GP) * g;
   uint8_t mask[32];
   outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
@@ -278,17 +323,20 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint
   const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
   const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
   int cnt = 0;
+  uint32_t nb[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
   for (int i = 0; i < 32; ++i) {
-    uint8_t q = 0;
+    uint32_t q = 0;
     if (mask[i]) {
       ++cnt;
     } else if (S != 0.f) {
       float r = rintf(__fdiv_rn(xg[i] - m, S));
       r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
-      q = (uint8_t)r;
+      q = (uint32_t)r;
     }
-    if (act) codes[t][32 * g + i] = q;
+    nb[i >> 3] |= q << (4 * (i & 7));
   }
+  store_codes<32>(blk, role, D / 16, t, 32 * g, lo, hi, nb, NG);
   // entries of group g go after those of groups < g of the same token (ascending channel order)
   int off = cnt;
 #pragma unroll
@@ -317,22 +365,27 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int hi, uint
   if (g == 0) blk[int4_cnt_off(D) + t] = (uint8_t)total;
 }
 
-// E2M1 quantization of token slots [t0, min(t0 + 32 / NS, hi)) by one warp
-// (NS = D / 16 scale groups): lane s * NS + g owns channels [16 g, 16 g + 16)
-// of slot t0 + s.  Channel c of a row sits at xs[t][c + GP * (c / 32)].
+// E2M1 quantization of token slots [t0, t0 + 32 / NS) by one warp (NS = D / 16
+// scale groups): lane s * NS + g owns channels [16 g, 16 g + 16) of slot
+// t0 + s; slots outside [lo, hi) compute on slot t0 and store nothing.
+// Channel c of a row sits at xs[t][c + GP * (c / 32)].
 template <int D, int XS, int GP>
-__device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int hi, uint8_t (*codes)[D], uint8_t* blk,
+__device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int lo, int hi, uint8_t* blk, int role,
                                      int lane) {
   constexpr int NS = D / 16;
   const int g = lane % NS, t = t0 + lane / NS;
-  if (t >= hi) return;
-  const float* x = xs[t] + 16 * g + GP * (g >> 1);
+  const bool act = t >= lo && t < hi;
+  const float* x = xs[act ? t : t0] + 16 * g + GP * (g >> 1);
   float amax = 0.f;
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
   const float sc = e4m3_to_f32(s8);
-  for (int i = 0; i < 16; ++i) codes[t][16 * g + i] = sc != 0.f ? f32_to_e2m1(__fdiv_rn(x[i], sc)) : 0;
-  blk[e2m1_sc_off(D) + 16 * g + t] = s8;
+  uint32_t nb[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    nb[i >> 3] |= (uint32_t)(sc != 0.f ? f32_to_e2m1(__fdiv_rn(x[i], sc)) : 0) << (4 * (i & 7));
+  store_codes<16>(blk, role, NS, t, 16 * g, lo, hi, nb, NS);
+  if (act) blk[e2m1_sc_off(D) + 16 * g + t] = s8;
 }
 
 // Threads [0, n) of a group of a CTA (tid is the index within the group, n a
@@ -345,47 +398,30 @@ struct Grp {
 __device__ __forceinline__ Grp whole_cta() { return Grp{(int)threadIdx.x, (int)blockDim.x, 0}; }
 
 // Per-token formats: re-quantize token slots [lo, hi) of one block from rows
-// xs[slot] (row stride XS floats); the other slots keep their codes and
-// metadata.  blk (the block's bytes) and codes[16][D] are the group's scratch;
-// the caller's writes of xs come before the call.  Channel c of a row sits at
-// xs[slot][c + GP * (c / 32)]: GP = 1 pads each 32-channel group so that the
-// lanes of a warp, one group each, read distinct banks.
+// xs[slot] (row stride XS); the other slots keep their codes and metadata.
+// blk (the block's bytes) is the group's scratch; the caller's writes of xs
+// come before the call.  Channel c of a row sits at xs[slot][c + GP * (c /
+// 32)]: GP = 1 pads each 32-channel group so that the lanes of a warp, one
+// group each, read distinct banks.
 template <int BF, int D, int XS, int GP = 0>
 __device__ void token_block_update(const AppendArgs& a, int role, const float (*xs)[XS], int lo, int hi, uint8_t* gblk,
-                                   uint8_t* blk, uint8_t (*codes)[D], const Grp& g) {
-  constexpr int kStride = block_stride(BF, D), NS = D / 16;
+                                   uint8_t* blk, const Grp& g) {
+  constexpr int kStride = block_stride(BF, D);
   const int lane = g.tid & 31, warp = g.tid >> 5, nw = g.n >> 5;
   // a block whose 16 slots are all rewritten keeps nothing of its old
-  // contents: start it from zeros (its padding included) instead of unpacking
+  // contents: start it from zeros (its padding included) instead of a copy
   if (lo > 0 || hi < kPage) {
     for (int i = g.tid; i < kStride / 16; i += g.n)
       reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(gblk)[i];
-    g.sync();
-    for (int i = g.tid; i < 32 * NS * 8; i += g.n) {
-      const int ln = i / (NS * 8), s = (i / 8) % NS, k = i % 8;
-      int t, c;
-      frag_inverse(role, ln, s, k, t, c);
-      codes[t][c] = (blk[4 * NS * ln + 4 * s + k / 2] >> (4 * (k & 1))) & 0xF;
-    }
   } else {
     for (int i = g.tid; i < kStride / 16; i += g.n) reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
   }
   g.sync();
-  constexpr int TPW = 32 / (BF == kBlkInt4 ? D / 32 : D / 16);   // token slots per warp pass
-  for (int t0 = lo + warp * TPW; t0 < hi; t0 += nw * TPW) {
-    if (BF == kBlkInt4) quantize_tokens_int4<D, XS, GP>(xs, t0, hi, codes, blk, a.sigma, lane);
-    else quantize_tokens_e2m1<D, XS, GP>(xs, t0, hi, codes, blk, lane);
-  }
-  g.sync();
-  for (int i = g.tid; i < 32 * NS; i += g.n) {
-    const int ln = i / NS, s = i % NS;
-    uint32_t word = 0;
-    for (int k = 0; k < 8; ++k) {
-      int t, c;
-      frag_inverse(role, ln, s, k, t, c);
-      word |= (uint32_t)codes[t][c] << (4 * k);
-    }
-    *reinterpret_cast<uint32_t*>(blk + 4 * NS * ln + 4 * s) = word;
+  // passes start at an even slot, so the two tokens of a V code byte share a warp
+  constexpr int TPW = 32 / (BF == kBlkInt4 ? D / 32 : D / 16);   // token slots per warp pass (even)
+  for (int t0 = (lo & ~1) + warp * TPW; t0 < hi; t0 += nw * TPW) {
+    if (BF == kBlkInt4) quantize_tokens_int4<D, XS, GP>(xs, t0, lo, hi, blk, role, a.sigma, lane);
+    else quantize_tokens_e2m1<D, XS, GP>(xs, t0, lo, hi, blk, role, lane);
   }
   g.sync();
   for (int i = g.tid; i < kStride / 16; i += g.n)
@@ -400,10 +436,10 @@ template <int BF>
 __host__ __device__ constexpr int token_ppc() { return BF == kBlkInt4 ? 4 : 2; }
 
 // Dynamic shared memory of append_token_kernel<BF, D>: per page, 16 staged rows
-// of D + D / 32 floats, the block's bytes and 16 x D codes.
+// of D + D / 32 floats and the block's bytes.
 template <int BF, int D>
 constexpr size_t token_smem_bytes() {
-  return (size_t)token_ppc<BF>() * (16 * (D + D / 32) * 4 + block_stride(BF, D) + 16 * D);
+  return (size_t)token_ppc<BF>() * (16 * (D + D / 32) * 4 + block_stride(BF, D));
 }
 
 template <int BF, int D>
@@ -416,7 +452,6 @@ __global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 5) append_token_kern
   extern __shared__ __align__(16) uint8_t tsm[];
   auto xs = reinterpret_cast<float (*)[16][XS]>(tsm);
   auto blk = reinterpret_cast<uint8_t (*)[kStride]>(tsm + PPC * 16 * XS * 4);
-  auto codes = reinterpret_cast<uint8_t (*)[16][D]>(tsm + PPC * (16 * XS * 4 + kStride));
   const int h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
   const int grp = (int)threadIdx.x / GT;           // one thread group (its own named barrier) per page
   const Grp g{(int)threadIdx.x % GT, GT, 1 + grp};
@@ -431,8 +466,7 @@ __global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 5) append_token_kern
     const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8));
     load_in8(a, role, b, lo + tt - start, h, c, D, &xs[grp][(lo % kPage) + tt][c + c / 32]);
   }
-  token_block_update<BF, D, XS, 1>(a, role, xs[grp], lo % kPage, lo % kPage + (hi - lo), gblk, blk[grp], codes[grp],
-                                   g);
+  token_block_update<BF, D, XS, 1>(a, role, xs[grp], lo % kPage, lo % kPage + (hi - lo), gblk, blk[grp], g);
 }
 
 // ----------------------------------------------------------------------------- page formats
@@ -1214,7 +1248,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
           constexpr int BF = KIND == kProjInt4 ? kBlkInt4 : kBlkE2m1, kStride = block_stride(BF, D);
           const uint32_t phys = (uint32_t)pt[u] & 0x7FFFFFFFu;
           token_block_update<BF, D, XS>(a, role, xu, lo, hi, a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride,
-                                        gws, reinterpret_cast<uint8_t(*)[D]>(gws + kStride), g);
+                                        gws, g);
         } else if (u * U + U <= end) {   // the append completes the unit
           if constexpr (KIND == kProjPage) {
             constexpr int kB = page_blk_bytes<D>();
@@ -1502,7 +1536,7 @@ __global__ void __launch_bounds__(kThreads, 1) project_one_kernel(const ProjArgs
       if (gp.tid < D) xs[slot][gp.tid] = v;
       const uint32_t phys = (uint32_t)ptb[pos / U] & 0x7FFFFFFFu;
       token_block_update<BF, D, XS>(a, role, xs, slot, slot + 1, a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride,
-                                    ws, reinterpret_cast<uint8_t(*)[D]>(ws + kStride), gp);
+                                    ws, gp);
     } else {   // the row completes its unit
       const float* stg = a.staging + (((size_t)b * a.Hkv + h) * 2 + role) * U * D;
       for (int i = gp.tid; i < (U - 1) * D; i += gp.n) xs[i / D][i % D] = stg[i];
