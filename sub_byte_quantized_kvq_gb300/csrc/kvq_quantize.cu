@@ -96,6 +96,16 @@ __device__ __forceinline__ void load_in8(const AppendArgs& a, int role, int b, i
     dst[j] = a.in_dtype == KVQ_F16 ? __half2float(__ushort_as_half(hv[j])) : __uint_as_float((uint32_t)hv[j] << 16);
 }
 
+// 16-byte asynchronous global -> shared copies, committed and waited for per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
@@ -299,15 +309,15 @@ __device__ __forceinline__ void store_codes(uint8_t* blk, int role, int NS, int 
 
 // INT4 group-32 quantization of token slots [t0, t0 + 32 / NG) by one warp (NG
 // = D / 32 groups): lane s * NG + g owns group g of slot t0 + s; slots outside
-// [lo, hi) compute on slot t0 and store nothing.  t0 < hi.  Channel c of a
-// row sits at xs[t][c + GP * (c / 32)].
+// [lo, hi) compute on slot lo (a row the caller wrote) and store nothing.
+// t0 < hi.  Channel c of a row sits at xs[t][c + GP * (c / 32)].
 template <int D, int XS, int GP>
 __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int hi, uint8_t* blk, int role,
                                      double sigma, int lane) {
   constexpr int NG = D / 32, CAP = int4_cap(D);
   const int g = lane % NG, t = t0 + lane / NG;
   const bool act = t >= lo && t < hi;
-  const float* xg = xs[act ? t : t0] + (32 + GP) * g;
+  const float* xg = xs[act ? t : lo] + (32 + GP) * g;
   uint8_t mask[32];
   outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
   bool have = false;
@@ -367,15 +377,15 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int 
 
 // E2M1 quantization of token slots [t0, t0 + 32 / NS) by one warp (NS = D / 16
 // scale groups): lane s * NS + g owns channels [16 g, 16 g + 16) of slot
-// t0 + s; slots outside [lo, hi) compute on slot t0 and store nothing.
-// Channel c of a row sits at xs[t][c + GP * (c / 32)].
+// t0 + s; slots outside [lo, hi) compute on slot lo (a row the caller wrote)
+// and store nothing.  Channel c of a row sits at xs[t][c + GP * (c / 32)].
 template <int D, int XS, int GP>
 __device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int lo, int hi, uint8_t* blk, int role,
                                      int lane) {
   constexpr int NS = D / 16;
   const int g = lane % NS, t = t0 + lane / NS;
   const bool act = t >= lo && t < hi;
-  const float* x = xs[act ? t : t0] + 16 * g + GP * (g >> 1);
+  const float* x = xs[act ? t : lo] + 16 * g + GP * (g >> 1);
   float amax = 0.f;
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
@@ -435,13 +445,42 @@ __device__ void token_block_update(const AppendArgs& a, int role, const float (*
 template <int BF>
 __host__ __device__ constexpr int token_ppc() { return BF == kBlkInt4 ? 4 : 2; }
 
-// Dynamic shared memory of append_token_kernel<BF, D>: per page, 16 staged rows
-// of D + D / 32 floats and the block's bytes.
+// Whether the per-token append prefetches its next pages (E2M1: measured 8%
+// faster; INT4, whose CTAs already keep every warp busy, lost a resident CTA
+// per SM to the buffer and ran 25% slower), and the page groups (of token_ppc
+// pages) one CTA then takes in turn.
+template <int BF>
+__host__ __device__ constexpr bool token_pipe() { return BF == kBlkE2m1; }
+constexpr int kTokenIters = 4;
+// Dynamic shared memory of append_token_kernel<BF, D> for input elements of
+// es bytes: per page, 16 staged rows of D + D / 32 floats, the block's bytes
+// and (prefetching) the next page's raw input rows.
 template <int BF, int D>
-constexpr size_t token_smem_bytes() {
-  return (size_t)token_ppc<BF>() * (16 * (D + D / 32) * 4 + block_stride(BF, D));
+constexpr size_t token_smem_bytes(int es) {
+  return (size_t)token_ppc<BF>() * (16 * (D + D / 32) * 4 + block_stride(BF, D) + (token_pipe<BF>() ? 16 * D * es : 0));
 }
 
+// Eight input elements (es bytes each, in_dtype) at p as fp32.
+__device__ __forceinline__ void raw8_to_f32(const uint8_t* p, int in_dtype, float* dst) {
+  if (in_dtype == KVQ_F32) {
+    const float4 u = reinterpret_cast<const float4*>(p)[0], w = reinterpret_cast<const float4*>(p)[1];
+    dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
+    dst[4] = w.x; dst[5] = w.y; dst[6] = w.z; dst[7] = w.w;
+    return;
+  }
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < 4; ++j)
+    for (int k = 0; k < 2; ++k) {
+      const uint16_t hv = (uint16_t)(w4[j] >> (16 * k));
+      dst[2 * j + k] = in_dtype == KVQ_F16 ? __half2float(__ushort_as_half(hv)) : __uint_as_float((uint32_t)hv << 16);
+    }
+}
+
+// A CTA's thread groups each take one page of a group of PPC pages, for
+// page groups blockIdx.x, + gridDim.x, ... of the append; when prefetching,
+// the next group's input rows are copied (cp.async) into shared memory while
+// the current one is quantized.
 template <int BF, int D>
 __global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 5) append_token_kernel(const AppendArgs a) {
   // rows padded by one float per 32 channels: with D + D / 32 floats a row, the
@@ -450,23 +489,54 @@ __global__ void __launch_bounds__(256, BF == kBlkInt4 ? 4 : 5) append_token_kern
   constexpr int kStride = block_stride(BF, D), PPC = token_ppc<BF>(), GT = 256 / PPC, XS = D + D / 32;
   static_assert(kStride % 16 == 0, "per-page blocks must stay 16-byte aligned");
   extern __shared__ __align__(16) uint8_t tsm[];
-  auto xs = reinterpret_cast<float (*)[16][XS]>(tsm);
-  auto blk = reinterpret_cast<uint8_t (*)[kStride]>(tsm + PPC * 16 * XS * 4);
   const int h = blockIdx.y >> 1, role = blockIdx.y & 1, b = blockIdx.z;
   const int grp = (int)threadIdx.x / GT;           // one thread group (its own named barrier) per page
   const Grp g{(int)threadIdx.x % GT, GT, 1 + grp};
+  const int es = a.in_dtype == KVQ_F32 ? 4 : 2;
+  float(*xs)[XS] = reinterpret_cast<float(*)[XS]>(tsm) + grp * 16;
+  uint8_t* blk = tsm + PPC * 16 * XS * 4 + grp * kStride;
+  uint8_t* raw = tsm + PPC * (16 * XS * 4 + kStride) + grp * 16 * D * es;
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
-  const int end = start + n, pg = start / kPage + (int)blockIdx.x * PPC + grp;
-  if (pg * kPage >= end) return;   // no token of this append lands in the group's page
-  const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
-  const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
-  uint8_t* gblk = a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride;
-  for (int i = g.tid; i < (hi - lo) * (D / 8); i += g.n) {
-    const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8));
-    load_in8(a, role, b, lo + tt - start, h, c, D, &xs[grp][(lo % kPage) + tt][c + c / 32]);
+  const int end = start + n, p0 = start / kPage, np = (end - 1) / kPage - p0 + 1;   // the append's pages
+  const int ngr = (np + PPC - 1) / PPC;
+  const bool vec = token_pipe<BF>() && (reinterpret_cast<uintptr_t>(a.kv[role]) & 15u) == 0;   // 16-byte copies
+  const uint8_t* src = static_cast<const uint8_t*>(a.kv[role]);
+  auto issue = [&](int gi) {   // the group's page of page group gi -> raw
+    const int pg = p0 + gi * PPC + grp;
+    if (vec && gi < ngr && pg - p0 < np) {
+      const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
+      for (int i = g.tid; i < (hi - lo) * (D / 8); i += g.n) {
+        const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8));
+        const uint8_t* sp = src + ((((size_t)b * a.t_new + (lo + tt - start)) * a.Hkv + h) * D + c) * es;
+        const uint32_t d = smem_u32(raw + ((lo % kPage + tt) * D + c) * es);
+        cp_async16(d, sp);
+        if (es == 4) cp_async16(d + 16, sp + 16);
+      }
+    }
+    cp_async_commit();
+  };
+  issue((int)blockIdx.x);
+  for (int gi = (int)blockIdx.x; gi < ngr; gi += (int)gridDim.x) {
+    const int pg = p0 + gi * PPC + grp;
+    const bool mine = pg - p0 < np;   // uniform within the group
+    const int lo = max(start, pg * kPage), hi = min(end, pg * kPage + kPage);
+    cp_async_wait<0>();
+    g.sync();   // the group's copies of this page have landed
+    if (mine)
+      for (int i = g.tid; i < (hi - lo) * (D / 8); i += g.n) {
+        const int tt = i / (D / 8), c = 8 * (i - tt * (D / 8)), slot = lo % kPage + tt;
+        if (vec) raw8_to_f32(raw + (slot * D + c) * es, a.in_dtype, &xs[slot][c + c / 32]);
+        else load_in8(a, role, b, lo + tt - start, h, c, D, &xs[slot][c + c / 32]);
+      }
+    g.sync();   // raw is free for the next page's copies
+    issue(gi + (int)gridDim.x);
+    if (!mine) continue;
+    const uint32_t phys = (uint32_t)a.page_table[(size_t)b * a.ppsm + pg] & 0x7FFFFFFFu;
+    token_block_update<BF, D, XS, 1>(a, role, xs, lo % kPage, lo % kPage + (hi - lo),
+                                     a.pool + (((size_t)phys * a.Hkv + h) * 2 + role) * kStride, blk, g);
   }
-  token_block_update<BF, D, XS, 1>(a, role, xs[grp], lo % kPage, lo % kPage + (hi - lo), gblk, blk[grp], g);
+  cp_async_wait<0>();
 }
 
 // ----------------------------------------------------------------------------- page formats
@@ -963,14 +1033,16 @@ static cudaError_t append_launch_d(const AppendArgs& a, cudaStream_t st) {
   const dim3 grid(pages_max, a.Hkv * 2, a.B);
   if (a.fmt == KVQ_FMT_INT4_G32 || a.fmt == KVQ_FMT_FP4_E2M1_S16) {
     const bool i4 = a.fmt == KVQ_FMT_INT4_G32;
+    const int es = a.in_dtype == KVQ_F32 ? 4 : 2;
     const auto kern = i4 ? append_token_kernel<kBlkInt4, D> : append_token_kernel<kBlkE2m1, D>;
-    const size_t smem = i4 ? token_smem_bytes<kBlkInt4, D>() : token_smem_bytes<kBlkE2m1, D>();
+    const size_t smem = i4 ? token_smem_bytes<kBlkInt4, D>(es) : token_smem_bytes<kBlkE2m1, D>(es);
     const int ppc = i4 ? token_ppc<kBlkInt4>() : token_ppc<kBlkE2m1>();
+    const int groups_max = (pages_max + ppc - 1) / ppc, iters = i4 ? 1 : kTokenIters;
     if (smem > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    kern<<<dim3((pages_max + ppc - 1) / ppc, a.Hkv * 2, a.B), 256, smem, st>>>(a);
+    kern<<<dim3((groups_max + iters - 1) / iters, a.Hkv * 2, a.B), 256, smem, st>>>(a);
   }
   else if (a.fmt == KVQ_FMT_CB2_GROUP4) {
     constexpr size_t smem = group_smem_bytes<D>();
@@ -1314,14 +1386,6 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
   return v;
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
