@@ -34,7 +34,7 @@ def _dist(fmt):
 
 
 @pytest.mark.parametrize("fmt,D", FORMATS_D, ids=IDS)
-@pytest.mark.parametrize("pattern", ["prefill", "tokens", "ragged", "prefill_bf16"])
+@pytest.mark.parametrize("pattern", ["prefill", "tokens", "ragged", "prefill_bf16", "prefill_f16"])
 def test_quantize_append_bit_exact(fmt, D, pattern):
     B, Hkv, P = 3, 2, 8
     pair = Pair(fmt, B, Hkv, D, P, seed=1, tiers=_tiers(fmt, B, P))
@@ -45,6 +45,8 @@ def test_quantize_append_bit_exact(fmt, D, pattern):
         pair.append(k, v)
     elif pattern == "prefill_bf16":
         pair.append(k, v, dtype=torch.bfloat16)
+    elif pattern == "prefill_f16":
+        pair.append(k, v, dtype=torch.float16)
     elif pattern == "tokens":
         for t in range(T):
             pair.append(k[:, t:t + 1], v[:, t:t + 1])
@@ -59,6 +61,28 @@ def test_quantize_append_bit_exact(fmt, D, pattern):
                 vc[b, :tps[b]] = v[b, pos[b]:pos[b] + tps[b]]
                 pos[b] += tps[b]
             assert pair.append(kc, vc, t_per_seq=tps) == 0
+    pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [INT4, E2M1, CB2])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_append_unaligned_inputs(fmt, dtype):
+    """K / V that start one element past a 16-byte boundary: the quantizers
+    fall back to element loads and still match the oracle bit for bit."""
+    B, Hkv, D, P, T = 2, 2, 128, 8, 70
+    pair = Pair(fmt, B, Hkv, D, P, seed=21)
+    dist, n_out, factor = _dist(fmt)
+    k, v = make_kv(21, B, T, Hkv, D, dist, n_out, factor)
+    kd, vd = k.to(dtype), v.to(dtype)
+    n = kd.numel()
+    kb = torch.zeros(n + 1, dtype=dtype, device="cuda")
+    vb = torch.zeros(n + 1, dtype=dtype, device="cuda")
+    kb[1:] = kd.reshape(-1).cuda()
+    vb[1:] = vd.reshape(-1).cuda()
+    ku, vu = kb[1:].view(kd.shape), vb[1:].view(vd.shape)
+    assert ku.data_ptr() % 16 != 0 and vu.data_ptr() % 16 != 0
+    kvq.kvq_quantize_append(pair.gpu, ku, vu, torch.tensor([T, 37], dtype=torch.int32, device="cuda"))
+    pair.ref.append(kd.float().numpy(), vd.float().numpy(), np.array([T, 37], np.int32))
     pair.assert_cache_equal()
 
 
