@@ -1148,8 +1148,10 @@ struct ProjPlan {
   static constexpr int XS = D + 4;  // row stride of the fp32 tile: rows start 4 banks apart
   static constexpr int S = D == 128 ? 2 : 3;                                  // operand stages
   static constexpr int A_BYTES = kPM * kPK * 2, B_BYTES = N * kPK * 2, STAGE = A_BYTES + B_BYTES;
-  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
-                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
+  // a unit group's scratch: the block (per-token formats); the block, mask and
+  // codes, and per-warp partials (pages); the 4 blocks and 2-bit codes (groups)
+  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D)
+                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D)
                           : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
                                                 : kGroupPages * block_stride(kBlkCb2g, D) + 16 * D;
   static constexpr int WSR = (WS + 127) / 128 * 128;
@@ -1410,8 +1412,8 @@ struct Plan {
   static constexpr int U = KIND == kProjGroup ? kPage * kGroupPages : kPage;
   static constexpr int XS = D + 4;
   static constexpr int XB = U * XS * 4;   // the unit's fp32 rows
-  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D) + 16 * D
-                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D) + 16 * D
+  static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D)
+                          : KIND == kProjE2m1   ? block_stride(kBlkE2m1, D)
                           : KIND == kProjPage   ? page_blk_bytes<D>() + 32 * D + 64
                                                 : kGroupPages * block_stride(kBlkCb2g, D) + U * (D / 32) * 4 + D * 16;
   static constexpr int EW = (XB + WS + 127) / 128 * 128;
