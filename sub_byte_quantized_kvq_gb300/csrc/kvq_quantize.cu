@@ -1371,7 +1371,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
 namespace small {
 constexpr int kMaxRows = 32;   // sequences per cluster: 16 (two n8 tiles) or 32 (four)
 constexpr int kThreads = 256;  // 8 warps; two 128-thread groups in the epilogue
-constexpr int kMaxSlice = 1024;   // hidden columns one CTA stages (16 rows of bf16: 32 KB)
+constexpr int kMaxSlice = 1024;   // hidden columns one CTA stages (R rows of bf16: 32 or 64 KB)
 
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
