@@ -22,6 +22,11 @@
 //      (the only one that reads staged rows) then stages the new tokens of
 //      the final partial page;
 //   2. advance seq_lens and raise status bits -- after 1, which reads them.
+//
+// The K/V projection fused with the append (kvq_project_append) is here too:
+// a tcgen05 tile kernel for prefill chunks and a thread-block-cluster split-K
+// kernel for one-token appends, both ending in the same per-unit quantizers
+// (token_block_update, page_quantize, group_quantize) as the append kernels.
 #include "kvq_project.cuh"
 
 namespace kvq {
