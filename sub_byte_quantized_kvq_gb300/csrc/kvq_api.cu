@@ -453,6 +453,28 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
   return KVQ_OK;
 }
 
+}  // extern "C"
+
+namespace kvq {
+kvq_status decode_attention_zeroing_counters(const kvq_config* cfg, const kvq_cache* cache, const void* q,
+                                             int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,
+                                             int32_t num_splits, void* out, kvq_dtype out_dtype, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t st) {
+  if (!out || (out_dtype != KVQ_BF16 && out_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
+  DecodeArgs a;
+  kvq_status s = decode_prepare(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
+                                workspace_bytes, a);
+  if (s != KVQ_OK) return s;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  if (cudaMemsetAsync(a.arrivals, 0, (size_t)a.B * a.Hkv * sizeof(uint32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (decode_split_launch(a, cfg->format, cfg->head_dim, st) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+}  // namespace kvq
+
+extern "C" {
+
 kvq_status kvq_select_static_channels(const kvq_config* cfg, const void* k, const void* v, kvq_dtype in_dtype,
                                       int32_t t, uint8_t* mask, void* stream) {
   if (!cfg_ok(cfg) || cfg->format != KVQ_FMT_CB2_STATIC || !k || !v || !mask || t < 1) return KVQ_ERR_INVALID_ARG;

@@ -63,6 +63,12 @@ cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
 
 cudaError_t select_static_launch(const void* k, const void* v, int in_dtype, int t, int Hkv, int D, int n_s,
                                  uint8_t* mask, cudaStream_t st);
+// kvq_decode_attention after clearing the call's arrival counters with a
+// memset on `st` (validation first: an argument error enqueues nothing).
+kvq_status decode_attention_zeroing_counters(const kvq_config* cfg, const kvq_cache* cache, const void* q,
+                                             int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,
+                                             int32_t num_splits, void* out, kvq_dtype out_dtype, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t st);
 // Dequantize tokens [t0, t1) of (seq, head, role) to fp32.
 cudaError_t dequantize_launch(const kvq_config& cfg, const kvq_cache& cache, int seq, int head, int role, int t0,
                               int t1, float* out, cudaStream_t st);

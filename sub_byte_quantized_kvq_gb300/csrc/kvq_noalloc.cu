@@ -26,7 +26,9 @@ std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device ordinal
 
 // Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached; nullptr if the lookup fails.
+// device ordinal (with that device current) and cached for the life of the
+// process; nullptr if the lookup fails.  The cache is keyed by ordinal, so the
+// entry point must not be used on a device after cudaDeviceReset on it.
 void* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -50,8 +52,11 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // before anything is enqueued
   void* scratch = scratch_on_current_device();
   if (!scratch) return KVQ_ERR_CUDA;
-  // The scratch starts zeroed (static storage), so its arrival counters do;
-  // every call leaves them zero again.  The partials need no initialisation.
-  return kvq_decode_attention(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, out, out_dtype,
-                              scratch, (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);
+  // The arrival counters sit where the call's shape (sequences, query heads,
+  // splits, head_dim) puts them, so after a call of another shape they would
+  // lie on that call's partials: this call clears its own counters on the
+  // stream before the launch (a memset, which allocates nothing).
+  return kvq::decode_attention_zeroing_counters(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, out,
+                                                out_dtype, scratch, (size_t)KVQ_NOALLOC_SCRATCH_BYTES,
+                                                static_cast<cudaStream_t>(stream));
 }

@@ -4,8 +4,9 @@ scratch array built into the library instead of a caller workspace).
 
 Checked through the C ABI against kvq_decode_attention, the entry point that
 takes a workspace, on two calls in a row (the second call reuses a scratch
-that still holds the first call's partials), within the tolerance the parity
-tests use (max-abs 2e-3, fp32 output).  This file is collected last so that a
+that still holds the first call's partials), and on a run of calls whose
+shapes differ, within the tolerance the parity tests use (max-abs 2e-3, fp32
+output).  This file is collected last so that a
 run stopping at its first failure has already run every other test; it builds
 its own cache, so it also passes alone in a fresh process.
 """
@@ -67,3 +68,22 @@ def test_noalloc_rejects_partials_larger_than_its_scratch():
     assert e.value.status == kvq.KVQ_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (out == 0).all()   # nothing was launched
+
+
+def test_noalloc_shape_changes_between_calls():
+    """The arrival counters sit where each call's shape puts them.  Run
+    splits 5, then 1 (whose counters fall on the first call's partials), then
+    a cache with other sequence and head counts, then the first again: every
+    call must still merge its splits and match the workspace entry point."""
+    a, qa, La = _cache(kvq.KVQ_FMT_CB2_OUTLIER)
+    b, qb, Lb = _cache(kvq.KVQ_FMT_CB2_OUTLIER, B=5, Hkv=3, G=2, lens=(33, 160, 16, 95, 200), P=16)
+    scale = qa.shape[-1] ** -0.5
+    for cache, q, L, splits in ((a, qa, La, 5), (a, qa, La, 1), (b, qb, Lb, 7), (b, qb, Lb, 2), (a, qa, La, 5),
+                                (a, qa, La, 0)):
+        ref = kvq.kvq_decode_attention(cache, q, scale, L, splits, out_dtype=torch.float32)
+        out = torch.full_like(ref, float("nan"))
+        kvq.kvq_decode_attention_noalloc(cache, q, scale, L, splits, out=out)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all(), f"splits {splits}: output not written"
+        assert (out - ref).abs().max().item() <= TOL
+    assert a.status_word() == 0 and b.status_word() == 0
