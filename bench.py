@@ -4,12 +4,16 @@
 Metric: achieved HBM GB/s of one decode step = algorithmic bytes (packed cache
 blocks the step must read, fp32 staging tail, bf16 Q and output) / device time
 of the step (one launch of the split kernel, whose last CTA per (sequence, kv
-head) merges the splits), with the cache resident in HBM and L2 flushed before
-every timed step.  ms_per_step gives the microseconds per decode step.  The
-default workload is cb2_4k (B8, Hkv8, Hq32, D128, context 4096, 2-bit codebook
-+ e4m3 outliers).  The line also carries "append": kvq_quantize_append timed on
-1-token appends and a 4096-token prefill chunk of the same shape (--no-append
-skips it); --project adds the fused projection + append comparison.
+head) merges the splits), with the cache resident in HBM; L2 is flushed before
+every timed step where the step's bytes do not already exceed three times the
+L2 size.  ms_per_step gives the time per decode step.  The default workload is
+tiered_32k (B64, Hkv8, Hq64, D128, context 32768, FP8 pages for the 10% of
+pages with the largest synthetic attention mass, 2-bit codebook + e4m3 outliers
+elsewhere), the largest of the five workloads; the same line carries the other
+measured workloads (cb2_4k, fp4_32k, longctx_128k) under "configs", each with
+its own roofline, and "append": kvq_quantize_append timed on 1-token appends and
+a 4096-token prefill chunk of the longctx_128k shape (--no-append skips it);
+--project adds the fused projection + append comparison.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -53,7 +57,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    p.add_argument("--workload", default="cb2_4k", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--workload", default="tiered_32k", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--batch", type=int, default=0, help="override the workload's sequence count (profiling)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="time only --workload (skip the other workloads carried under \"configs\")")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--splits", type=int, default=-1, help="-1: the workload's own (0 = library choice)")
     p.add_argument("--flush-mb", type=int, default=512)
@@ -61,6 +68,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-append", action="store_true",
                    help="skip timing kvq_quantize_append (1-token appends and a 4096-token prefill chunk)")
+    p.add_argument("--append-workload", default="longctx_128k", choices=sorted(synth.WORKLOADS),
+                   help="shape of the kvq_quantize_append timing")
     p.add_argument("--project", action="store_true",
                    help="also time kvq_project_append against a cuBLAS projection + kvq_quantize_append")
     p.add_argument("--project-only", action="store_true",
@@ -101,54 +110,68 @@ def all_max(x: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------------------- byte accounting
-def algorithmic_bytes(built: workloads.Built) -> dict:
-    """Bytes one decode step must move: the packed contents of every block it
-    reads (codes, scales / codebooks, per-token counts and the outlier entries
-    actually present), the fp32 staging tail, Q (bf16) and the output (bf16)."""
-    w, cache = built.w, built.cache
-    D = w.D
-    L = w.N
-    full = L // 16
-    blocks = w.B * w.Hkv * 2
-    if w.fmt in (synth.FMT_CB2, synth.FMT_TIERED):
-        # CB2 block: codes + codebook (12D) + side-list header, records and values
-        pool = cache.pool.view(-1, cache.block_bytes(0))
-        nch = pool[:, 12 * D].to(torch.int64)
-        side = (4 + 20 * nch).sum().item()
-        n_tier = int(built.tiers[:, :full].sum()) * w.Hkv * 2
-        n_main = full * blocks - n_tier
-        cache_bytes = n_main * 12 * D + side + n_tier * (16 * D + 4)
-        tail = (L % 16) * D * 4 * blocks
-    elif w.fmt == synth.FMT_CB2G:
-        # per group: one codebook (8D); per page: codes (4D) + side-list; the partial group in fp32
-        pool = cache.pool.view(-1, cache.block_bytes(0))
-        nch = pool[:, 12 * D].to(torch.int64)
-        groups = L // 64
-        unq = pool.shape[0] - groups * 4 * w.B * w.Hkv * 2     # blocks no complete group wrote
-        cache_bytes = groups * blocks * (8 * D + 4 * 4 * D) + (4 + 20 * nch).sum().item() - 4 * unq
-        tail = (L - 64 * groups) * D * 4 * blocks
-    elif w.fmt == synth.FMT_A3:
-        # codes (6D) + S and m (4D) + side-list header and records
-        pool = cache.pool.view(-1, cache.block_bytes(0))
-        nch = pool[:, 10 * D].to(torch.int64)
-        cache_bytes = full * blocks * 10 * D + (4 + 20 * nch).sum().item()
-        tail = (L % 16) * D * 4 * blocks
-    elif w.fmt == synth.FMT_CB2S:
-        # codes + codebook (12D) + {n_s, channels} (16) + the static channels' fp16 values
-        cache_bytes = full * blocks * (12 * D + 16 + 32 * w.static_channels)
-        tail = (L % 16) * D * 4 * blocks
-    elif w.fmt == synth.FMT_INT4:
-        pool = cache.pool.view(-1, cache.block_bytes(0))
-        counts = pool[:, 10 * D:10 * D + 16].to(torch.int64).sum().item()
-        cache_bytes = ((L + 15) // 16) * blocks * (10 * D + 16) + 3 * counts
-        tail = 0
+def block_meta(fmt: int, D: int, blocks):
+    """The bytes of each main-pool block that the algorithmic count needs, as
+    numpy (blocks: [n_blocks, stride] uint8, a torch tensor on any device or a
+    numpy array): the side-list's channel-record count (CB2, TIERED, ASYM3,
+    CB2_GROUP4) or the outlier count of each block (INT4); None otherwise."""
+    if fmt in (synth.FMT_CB2, synth.FMT_TIERED, synth.FMT_CB2G):
+        col = blocks[:, 12 * D]
+    elif fmt == synth.FMT_A3:
+        col = blocks[:, 10 * D]
+    elif fmt == synth.FMT_INT4:
+        col = blocks[:, 10 * D:10 * D + 16]
+        col = col.to(torch.int64).sum(1) if isinstance(col, torch.Tensor) else col.astype(np.int64).sum(1)
     else:
-        cache_bytes = ((L + 15) // 16) * blocks * 9 * D
-        tail = 0
-    q_bytes = w.B * w.Hq * D * 2
-    out_bytes = w.B * w.Hq * D * 2
-    return {"cache": int(cache_bytes), "tail": int(tail), "q": q_bytes, "out": out_bytes,
-            "split_kernel": int(cache_bytes + tail + q_bytes), "step": int(cache_bytes + tail + q_bytes + out_bytes)}
+        return None
+    return (col.cpu().numpy() if isinstance(col, torch.Tensor) else np.asarray(col)).astype(np.int64)
+
+
+def step_bytes(fmt: int, D: int, Hkv: int, Hq: int, B: int, N: int, page_table: np.ndarray, meta,
+               static_channels: int = 0) -> dict:
+    """Bytes one decode step must move when every one of the B sequences holds
+    N tokens: the packed contents of every block it reads (codes, scales or
+    codebooks, and the outlier side-list or per-token outliers actually
+    present), the fp32 staging tail of the page formats, Q (bf16) and the
+    output (bf16).
+
+    page_table: int32 [B, pages] (bit 31 = FP8 tier page); meta: block_meta()
+    of the main pool, indexed by block (phys * Hkv + head) * 2 + role."""
+    pt = np.asarray(page_table).astype(np.int64) & 0xFFFFFFFF
+    paged = fmt in (synth.FMT_CB2, synth.FMT_TIERED, synth.FMT_CB2S, synth.FMT_A3, synth.FMT_CB2G)
+    unit = 64 if fmt == synth.FMT_CB2G else 16                 # tokens quantized together
+    full = (N // unit) * (unit // 16) if paged else (N + 15) // 16   # pages stored as blocks
+    ent = pt[:, :full].reshape(-1)
+    tier = (ent >> 31) != 0
+    phys = ent[~tier] & 0x7FFFFFFF
+    blk = ((phys[:, None] * Hkv + np.arange(Hkv)[None, :])[:, :, None] * 2 + np.arange(2)[None, None, :]).reshape(-1)
+    n_main = blk.size
+    n_tier = int(tier.sum()) * Hkv * 2
+    if fmt in (synth.FMT_CB2, synth.FMT_TIERED):
+        cache = n_main * 12 * D + int((4 + 20 * meta[blk]).sum()) + n_tier * (16 * D + 4)
+    elif fmt == synth.FMT_CB2G:
+        groups = full // 4 * B                                  # one 8D codebook per (group, head, role)
+        cache = n_main * 4 * D + int((4 + 20 * meta[blk]).sum()) + groups * Hkv * 2 * 8 * D
+    elif fmt == synth.FMT_A3:
+        cache = n_main * 10 * D + int((4 + 20 * meta[blk]).sum())
+    elif fmt == synth.FMT_CB2S:
+        cache = n_main * (12 * D + 16 + 32 * static_channels)
+    elif fmt == synth.FMT_INT4:
+        cache = n_main * (10 * D + 16) + 3 * int(meta[blk].sum())   # 1-byte channel + fp16 value per outlier
+    else:
+        cache = n_main * 9 * D
+    tail = (N - (N // unit) * unit) * D * 4 * 2 * B * Hkv if paged else 0
+    q_bytes = B * Hq * D * 2
+    out_bytes = B * Hq * D * 2
+    return {"cache": int(cache), "tail": int(tail), "q": q_bytes, "out": out_bytes,
+            "split_kernel": int(cache + tail + q_bytes), "step": int(cache + tail + q_bytes + out_bytes)}
+
+
+def algorithmic_bytes(built: workloads.Built) -> dict:
+    """step_bytes() of a workload built on the device."""
+    w, cache = built.w, built.cache
+    meta = block_meta(w.fmt, w.D, cache.pool.view(-1, cache.block_bytes(0)))
+    return step_bytes(w.fmt, w.D, w.Hkv, w.Hq, w.B, w.N, built.page_table, meta, w.static_channels)
 
 
 def kernel_source_sha() -> str:
@@ -287,7 +310,7 @@ def time_gpu(built: workloads.Built, args, world: int, dev) -> dict:
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = [e[0].elapsed_time(e[1]) for e in e2e_evs]
-    return {"split_ms": float(np.mean(step_ms)), "step_ms": float(np.mean(step_ms)),
+    return {"step_ms": float(np.mean(step_ms)),
             "step_ms_median": float(np.median(step_ms)), "e2e_ms": float(np.mean(e2e_ms)), "bytes": nbytes,
             "splits": S_eff, "clocks": clocks, "flushed": flush is not None,
             "h2d": q.numel() * q.element_size(), "d2h": out.numel() * out.element_size()}
@@ -315,32 +338,9 @@ def oracle_sample(w: synth.Workload, seed: int):
         k, v = workloads.seq_kv(w, seed, 0, t0, T, "cpu")
         ref.append(k[None].numpy(), v[None].numpy())
     q = synth.queries_bf16(seed, 1, w.Hq, w.D).view(torch.int16).numpy().view(np.uint16)
-    # bytes the same step reads for this sample (same accounting as the GPU line)
-    D, full = w.D, N // 16
-    if w.fmt in (synth.FMT_CB2, synth.FMT_TIERED):
-        blocks = ref.pool.reshape(-1, ref.stride).astype(np.int64)
-        nch = blocks[:, 12 * D]
-        side = int((4 + 20 * nch).sum())
-        n_tier = (int(tiers[:, :full].sum()) if tiers is not None else 0) * w.Hkv * 2
-        cache = (full * w.Hkv * 2 - n_tier) * 12 * D + side + n_tier * (16 * D + 4)
-        cache += (N % 16) * D * 4 * w.Hkv * 2
-    elif w.fmt == synth.FMT_CB2S:
-        cache = full * w.Hkv * 2 * (12 * D + 16 + 32 * w.static_channels) + (N % 16) * D * 4 * w.Hkv * 2
-    elif w.fmt == synth.FMT_CB2G:
-        nch = ref.pool.reshape(-1, ref.stride)[:, 12 * D].astype(np.int64)
-        groups = N // 64
-        unq = nch.shape[0] - groups * 4 * w.Hkv * 2
-        cache = groups * w.Hkv * 2 * (8 * D + 16 * D) + int((4 + 20 * nch).sum()) - 4 * unq
-        cache += (N - 64 * groups) * D * 4 * w.Hkv * 2
-    elif w.fmt == synth.FMT_A3:
-        nch = ref.pool.reshape(-1, ref.stride)[:, 10 * D].astype(np.int64)
-        cache = full * w.Hkv * 2 * 10 * D + int((4 + 20 * nch).sum()) + (N % 16) * D * 4 * w.Hkv * 2
-    elif w.fmt == synth.FMT_INT4:
-        counts = int(ref.pool.reshape(-1, ref.stride)[:, 10 * D:10 * D + 16].astype(np.int64).sum())
-        cache = pages * w.Hkv * 2 * (10 * D + 16) + 3 * counts
-    else:
-        cache = pages * w.Hkv * 2 * 9 * D
-    nbytes = cache + 2 * w.Hq * D * 2
+    # bytes the same step reads for this sample (same accounting as the GPU line; one sequence)
+    meta = block_meta(w.fmt, w.D, ref.pool.reshape(-1, ref.stride))
+    nbytes = step_bytes(w.fmt, w.D, w.Hkv, w.Hq, 1, N, pt, meta, w.static_channels)["step"]
     return ref, q, nbytes, N
 
 
@@ -466,10 +466,55 @@ def time_project(w: synth.Workload, dev, flush_mb: int, reps: int = 10, warmup: 
 
 
 # ----------------------------------------------------------------------------- main
+CONFIG_WORKLOADS = ("cb2_4k", "fp4_32k", "longctx_128k")   # carried beside the headline workload
+
+
+def traffic_record(workload: str, batch: int):
+    """DRAM bytes per launch of decode_split_kernel for `workload` from the
+    committed ncu record, or None when the record is for other kernel sources
+    (the kernel changed since the counters were taken) or another shape."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+    except Exception:
+        return None
+    if tr.get("kernel_src_sha") != kernel_source_sha():
+        return None
+    rec = tr.get("workloads", {}).get(workload)
+    if rec is None or batch:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def measure_workload(w: synth.Workload, args, world: int, rank: int, dev, peak: float, peak_kind: str) -> dict:
+    """Build the workload's cache on the device, time its decode step, and
+    return the timing with its roofline (the split kernel is the whole step)."""
+    built = workloads.build(w, seed=args.seed + rank, device=dev)
+    torch.cuda.synchronize()
+    t = time_gpu(built, args, world, dev)
+    del built
+    torch.cuda.empty_cache()
+    t["step_ms"] = all_max(t["step_ms"], world)
+    t["e2e_ms"] = all_max(t["e2e_ms"], world)
+    t["step_ms_median"] = all_max(t["step_ms_median"], world)
+    nb = t["bytes"]
+    achieved = nb["step"] / (t["step_ms"] * 1e-3) / 1e9
+    t["roofline"] = {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic_record(w.name, args.batch),
+                     "algorithmic_bytes_per_launch": nb["step"], "us_per_launch": t["step_ms"] * 1e3,
+                     "frac_of_nominal_8000_gbs": achieved / 8000.0}
+    t["l2"] = ("flushed before every step (write 256 MB + read 256 MB)" if t["flushed"]
+               else f"inputs exceed L2 ({nb['step'] / L2_BYTES:.1f} x its 129 MB; no flush)")
+    return t
+
+
 def main():
     args = parse_args()
     rank, world = dist_setup(args)
     w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
     config = {"workload": w.name, "format": FMT_NAME[w.fmt], "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "D": w.D,
               "context": w.N, "page_tokens": 16}
 
@@ -493,48 +538,45 @@ def main():
             print(json.dumps({"workload": w.name, "format": FMT_NAME[w.fmt],
                               "project": time_project(w, dev, args.flush_mb, B=args.project_b)}), flush=True)
         return
-    built = workloads.build(w, seed=args.seed + rank, device=dev)
-    torch.cuda.synchronize()
-    t = time_gpu(built, args, world, dev)
-    step_ms = all_max(t["step_ms"], world)
-    split_ms = all_max(t["split_ms"], world)
-    e2e_ms = all_max(t["e2e_ms"], world)
-    nb = t["bytes"]
     peak, peak_kind = measured_peak_gbs()
-    achieved = nb["step"] / (split_ms * 1e-3) / 1e9   # the fused kernel is the whole step
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_src_sha") == kernel_source_sha() and tr.get("workload") == w.name:
-            traffic = tr["dram_bytes_per_launch"]
-    except Exception:
-        pass
+    t = measure_workload(w, args, world, rank, dev, peak, peak_kind)
+    nb = t["bytes"]
+    step_ms, e2e_ms = t["step_ms"], t["e2e_ms"]
     line = {
         "metric": METRIC,
         "value": world * nb["step"] / (step_ms * 1e-3) / 1e9,
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_ms, "us_per_step": step_ms * 1e3,
-        "us_per_step_median": all_max(t["step_ms_median"], world) * 1e3,   # event timestamps tick in ~2 us steps
+        "us_per_step_median": t["step_ms_median"] * 1e3,   # event timestamps tick in ~2 us steps
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 mma / f32 accumulate over 2-4 bit codes", "data": "synthetic",
-        "config": dict(config, splits=t["splits"],
-                       l2="flushed before every step (write 256 MB + read 256 MB)" if t["flushed"]
-                       else "inputs exceed L2 (no flush)",
-                       bytes_per_step=nb["step"], partial_bytes_per_step=0),
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nb["step"], "us_per_launch": split_ms * 1e3,
-                     "frac_of_nominal_8000_gbs": achieved / 8000.0},
+        "config": dict(config, splits=t["splits"], l2=t["l2"], bytes_per_step=nb["step"],
+                       partial_bytes_per_step=2 * w.B * w.Hq * t["splits"] * (w.D + 2) * 4),
+        "roofline": t["roofline"],
         "e2e": {"value": world * nb["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": t["h2d"], "d2h_bytes_per_step": t["d2h"], "us_per_step": e2e_ms * 1e3},
+                "h2d_bytes_per_step": t["h2d"], "d2h_bytes_per_step": t["d2h"], "us_per_step": e2e_ms * 1e3,
+                "us_host_and_copies_beyond_device_step": (e2e_ms - step_ms) * 1e3},
         "gpu_launches": args.steps,
         "clocks": t["clocks"],
     }
-    line["config"]["partial_bytes_per_step"] = 2 * w.B * w.Hq * t["splits"] * (w.D + 2) * 4
+    if not args.no_configs and not args.batch:
+        configs = {}
+        for name in CONFIG_WORKLOADS:
+            if name == w.name:
+                continue
+            wc = synth.WORKLOADS[name]
+            tc = measure_workload(wc, args, world, rank, dev, peak, peak_kind)
+            configs[name] = {"format": FMT_NAME[wc.fmt], "B": wc.B, "Hkv": wc.Hkv, "Hq": wc.Hq, "D": wc.D,
+                             "context": wc.N, "splits": tc["splits"], "l2": tc["l2"],
+                             "bytes_per_step": tc["bytes"]["step"], "us_per_step": tc["step_ms"] * 1e3,
+                             "us_per_step_median": tc["step_ms_median"] * 1e3,
+                             "value": world * tc["bytes"]["step"] / (tc["step_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                             "roofline": tc["roofline"], "clocks": tc["clocks"]}
+        line["configs"] = configs
     if not args.no_append:
-        line["append"] = time_append(w, dev, args.flush_mb)
+        line["append"] = dict(time_append(synth.WORKLOADS[args.append_workload], dev, args.flush_mb),
+                              workload=args.append_workload)
     if args.project:
         line["project"] = time_project(w, dev, args.flush_mb, B=args.project_b)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

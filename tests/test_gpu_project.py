@@ -11,7 +11,7 @@ import torch
 import oracle
 from sub_byte_quantized_kvq_gb300 import kvq, synth
 
-from _kvq_pairs import Pair, make_kv
+from _kvq_pairs import ORACLE_FMT, Pair, make_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -249,3 +249,47 @@ def test_project_capacity_overflow_is_flagged():
     torch.cuda.synchronize()
     assert pair.gpu.status_word() & kvq.KVQ_STATUS_CAPACITY          # 40 tokens > 32 slots for sequence 0
     assert pair.gpu.seq_lens.cpu().tolist() == [20, 32]
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_project_end_to_end_against_the_oracles_own_projection(fmt):
+    """End to end from x and the weights: the oracle projects with its own fp64
+    product (rounded once to fp32, the quantizer's input precision) and
+    quantizes that, while the fused GPU path projects on the tensor cores
+    (fp32 accumulation) and quantizes in the same kernel.  The two quantizer
+    inputs differ only within the fp32 accumulation bound, so a decision can
+    differ only where those inputs straddle it.  Such a straddle moves an
+    element by a quantization step; everything else moves by no more than the
+    inputs do (a staged tail row, an FP8 page's scale): the elements that move
+    by more than 1e-5 of their size are counted and bounded (0.2% of the
+    elements), and the GPU's
+    attention over its cache must lie within 2e-3, plus the straddles' own
+    effect on the exact attention, of the oracle's attention over the
+    oracle's cache."""
+    B, Hkv, D, P, hidden, T = 2, 2, 128, 24, 256, 200
+    tps = [200, 143]
+    pair = Pair(fmt, B, Hkv, D, P, seed=21, tiers=tiers_for(fmt, B, P))
+    x, wk, wv = synth.projection_inputs(21, B, T, hidden, Hkv, D)
+    kg, vg = pair.project(x, wk, wv, tps)           # GPU cache, and the oracle fed the GPU's own K / V
+    pair.assert_cache_equal()
+    k64, v64 = oracle.project_kv(x.float().numpy(), wk.float().numpy(), wv.float().numpy(), Hkv, D)
+    own = oracle.OracleCache(ORACLE_FMT[fmt], B, Hkv, D, P, pair.ref.cfg.num_pages, pair.ref.cfg.num_tier_pages,
+                             page_table=pair.pt, static_channels=pair.ref.static_ch.copy())
+    own.append(k64.astype(np.float32), v64.astype(np.float32), np.array(tps, np.int32))
+    n_diff = n_all = 0
+    for b in range(B):
+        for h in range(Hkv):
+            for role in range(2):
+                a = own.dequantize(b, h, role, 0, tps[b])
+                g = pair.ref.dequantize(b, h, role, 0, tps[b])
+                n_diff += int((np.abs(a - g) > 1e-5 * np.maximum(np.abs(a), np.abs(g)) + 1e-6).sum())
+                n_all += a.size
+    assert n_diff <= 0.002 * n_all, f"{n_diff} of {n_all} dequantized elements differ"
+    q = synth.queries_bf16(21, B, 4 * Hkv, D, device="cuda")
+    out = kvq.kvq_decode_attention(pair.gpu, q, D ** -0.5, T, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    qb = q.cpu().view(torch.int16).numpy().view(np.uint16)
+    exp_own = own.decode(qb, D ** -0.5)
+    exp_gpu_inputs = pair.ref.decode(qb, D ** -0.5)
+    err = np.abs(out.cpu().numpy() - exp_own)
+    assert (err <= 2e-3 + np.abs(exp_own - exp_gpu_inputs)).all(), f"max err {err.max():.3e}"

@@ -57,8 +57,8 @@ def _ref_block(ref, entry, role):
     return pool[off:off + stride]
 
 
-@pytest.mark.parametrize("name", ["cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k", "static_4k", "a3_4k",
-                                  "group_4k"])
+@pytest.mark.parametrize("name", ["tiny_int4", "cb2_4k", "fp4_32k", "tiered_32k", "longctx_128k", "static_4k",
+                                  "a3_4k", "group_4k"])
 def test_full_size_workload_sampled(name):
     w = synth.WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -74,7 +74,7 @@ def test_full_size_workload_sampled(name):
         np.testing.assert_array_equal(built.cache.static_mask.cpu().numpy(), _static_mask(built, dev))
     qbits = q.cpu().view(torch.int16).numpy().view(np.uint16)
     rng = np.random.default_rng(1)
-    units = [(0, 0), (w.B - 1, w.Hkv - 1)]
+    units = sorted({(0, 0), (w.B - 1, w.Hkv - 1)})
     for b, h in units:
         ref, pt = _oracle_unit(built, b, h, dev)
         pages = sorted({0, w.pages - 1, w.pages // 2, *rng.integers(0, w.pages, 6).tolist()})
