@@ -2,9 +2,9 @@
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its cpu_baseline
 and reference legs) may import this package.  It shares no code with the CUDA
-path.  The arithmetic lives in ``kvq_oracle.c`` (plain C: attention in fp64,
-quantizer decisions in binary32 as the kernels take them, compiled with
-``-ffp-contract=off``); this module compiles it with gcc, loads it with ctypes
+path.  The arithmetic lives in ``kvq_oracle.c`` (plain C, everything in fp64:
+the quantizer's statistics, fits and decisions and the attention, compiled
+with ``-ffp-contract=off``); this module compiles it with gcc, loads it with ctypes
 and keeps a numpy model of the paged cache (pools, page table, staging tail,
 sequence lengths) that mirrors the layout the library documents.
 """
@@ -104,7 +104,7 @@ def block_stride(blk_fmt: int, D: int) -> int: return int(lib().or_block_stride(
 
 
 def outlier_mask(x, sigma: float = 3.0, cap: int | None = None):
-    """binary32 outlier rule over x (taken as float32)."""
+    """fp64 outlier rule over x (taken as float32, the values a cache receives)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     m = np.zeros(x.size, dtype=np.uint8)
     n = lib().or_outlier_mask(_p(x), x.size, sigma, kmax(x.size) if cap is None else cap, _p(m))
@@ -112,10 +112,10 @@ def outlier_mask(x, sigma: float = 3.0, cap: int | None = None):
 
 
 def lloyd4(v, iters: int = 16):
-    """binary32 Lloyd-Max fit of v (taken as float32).
-    Returns (centroids before fp16 rounding, fp16 bits, codes, passes)."""
+    """fp64 Lloyd-Max fit of v (taken as float32, the values a cache receives).
+    Returns (fp64 centroids before fp16 rounding, fp16 bits, codes, passes)."""
     v = np.ascontiguousarray(v, dtype=np.float32)
-    c = np.zeros(4, np.float32)
+    c = np.zeros(4, np.float64)
     c16 = np.zeros(4, np.uint16)
     codes = np.zeros(max(v.size, 1), np.uint8)
     passes = lib().or_lloyd4(_p(v), v.size, iters, _p(c), _p(c16), _p(codes))

@@ -17,11 +17,13 @@
  *        Quantization", section "2. FP4/INT4 KV-Cache Quantization"
  *        (block-wise asymmetric quantization, E2M1, the scale formula).
  *
- * Attention is fp64.  The quantizer takes its decisions (outlier tests,
- * Lloyd-Max assignments, INT4 codes) in IEEE binary32, the precision the CUDA
- * kernels use -- the pages fix none -- with ascending-index reductions; compile
- * with -ffp-contract=off so no multiply-add is fused.  Where the pages leave a
- * step open, the reading taken is stated next to the code.
+ * Everything is fp64 (IEEE binary64): the quantizer's statistics and decisions
+ * (outlier tests, the Lloyd-Max fit and its assignments, INT4 / 3-bit scales
+ * and codes, E2M1 and FP8 scales and codes) and the attention.  Inputs are the
+ * binary32 values the cache receives, converted exactly; results are rounded
+ * once, to the stored format.  Reductions run in ascending index order;
+ * compile with -ffp-contract=off so no multiply-add is fused.  Where the pages
+ * leave a step open, the reading taken is stated next to the code.
  *
  * Every function here is pinned by tests/test_oracle_*.py against something
  * other than itself (library routines, closed forms, brute force, invariants).
@@ -148,16 +150,17 @@ EXPORT double or_bf16_decode(uint16_t h)
     return (double)f;
 }
 
-/* IEEE binary32 division, correctly rounded: the fp64 quotient of two binary32
- * values rounded to binary32 (53 >= 2*24+2 bits, so the double rounding is
- * innocuous and equals a single correct rounding). */
-static float f32_div(float a, float b) { return (float)((double)a / (double)b); }
+/* The binary32 value nearest to the fp64 quotient a / b (one rounding to
+ * binary32 of the fp64 quotient; 53 >= 2*24 + 2 bits, so for binary32 inputs
+ * this double rounding equals a single correct rounding of the exact
+ * quotient). */
+static float f32_of_quotient(float a, float b) { return (float)((double)a / (double)b); }
 
 /* ------------------------------------------------------------------------- */
 /* Outlier isolation ([P1] "1. Dynamic Outlier Isolation" and the             */
 /* compress_kv_head listing; [P3] outlier channels; [P4] "Channel-Outlier     */
 /* Isolation").  For one vector x[0..n) (a token's head vector, or one        */
-/* 32-value group for INT4), in binary32:                                     */
+/* 32-value group for INT4), in fp64:                                         */
 /*   mu  = (sum x) / n                    ascending index                     */
 /*   s   = sqrt( sum (x - mu)^2 / (n-1) ) unbiased, as torch's .std()         */
 /*   x_i is an outlier  iff  |x_i - mu| > sigma * s   (strict, as the listing)*/
@@ -176,19 +179,19 @@ EXPORT int or_kmax(int n) /* capacity at sigma = 3 */
 
 EXPORT int or_outlier_mask(const float* x, int n, double sigma, int kmax, uint8_t* mask)
 {
-    float sum = 0.0f;
-    for (int i = 0; i < n; ++i) sum += x[i];
-    float mu = sum / (float)n;
-    float ss = 0.0f;
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) sum += (double)x[i];
+    double mu = sum / (double)n;
+    double ss = 0.0;
     for (int i = 0; i < n; ++i) {
-        float d = x[i] - mu;
+        double d = (double)x[i] - mu;
         ss += d * d;
     }
-    float s = sqrtf(ss / (float)(n - 1));
-    float thr = (float)sigma * s;
+    double s = sqrt(ss / (double)(n - 1));
+    double thr = sigma * s;
     int k = 0;
     for (int i = 0; i < n; ++i) {
-        int out = fabsf(x[i] - mu) > thr;
+        int out = fabs((double)x[i] - mu) > thr;
         if (out && k >= kmax) out = 0;
         mask[i] = (uint8_t)out;
         k += out;
@@ -200,71 +203,71 @@ EXPORT int or_outlier_mask(const float* x, int n, double sigma, int kmax, uint8_
 /* 2-bit non-uniform codebook ([P1] "2. Centroid Vector Quantization for      */
 /* Residuals": a 4-centroid codebook fitted by k-means; the listing starts    */
 /* the centroids at linspace(min, max, 4) and assigns by argmin distance).    */
-/* In one dimension k-means is the Lloyd-Max iteration (binary32):            */
+/* In one dimension k-means is the Lloyd-Max iteration (fp64):                */
 /*   c = (mn, mn+h, mn+2h, mx) with h = (mx-mn)/3                             */
 /*   repeat up to `iters` times:                                              */
 /*     a = nearest-centroid assignment (ties -> lower index, argmin's rule)   */
 /*     stop if a equals the previous assignment                               */
 /*     c_j = mean of the values assigned to j (ascending order); an empty    */
 /*           cell keeps its centroid                                          */
-/*   centroids are stored as fp16 (round to nearest even);                    */
-/*   final code = nearest fp16 centroid, ties -> lower index.                 */
+/*   centroids are stored as fp16 (one round-to-nearest-even of the fp64      */
+/*   value); final code = nearest fp16 centroid, ties -> lower index.         */
 /* n == 0 (every value of the channel is an outlier) gives four zero          */
 /* centroids.  Returns the number of assignment passes made.                  */
 /* ------------------------------------------------------------------------- */
 
-static int nearest4(float v, const float* c)
+static int nearest4(double v, const double* c)
 {
     int best = 0;
-    float bd = fabsf(v - c[0]);
+    double bd = fabs(v - c[0]);
     for (int j = 1; j < 4; ++j) {
-        float d = fabsf(v - c[j]);
+        double d = fabs(v - c[j]);
         if (d < bd) { bd = d; best = j; }
     }
     return best;
 }
 
-EXPORT int or_lloyd4(const float* v, int n, int iters, float* c_out, uint16_t* c16_out, uint8_t* codes_out)
+EXPORT int or_lloyd4(const float* v, int n, int iters, double* c_out, uint16_t* c16_out, uint8_t* codes_out)
 {
-    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    double c[4] = {0.0, 0.0, 0.0, 0.0};
     int passes = 0;
     if (n > 0) {
-        float mn = v[0], mx = v[0];
+        double mn = v[0], mx = v[0];
         for (int i = 1; i < n; ++i) {
             if (v[i] < mn) mn = v[i];
             if (v[i] > mx) mx = v[i];
         }
-        float h = (mx - mn) / 3.0f;
+        double h = (mx - mn) / 3.0;
         c[0] = mn;
         c[1] = mn + h;
-        c[2] = mn + 2.0f * h;
+        c[2] = mn + 2.0 * h;
         c[3] = mx;
         uint8_t prev[64], a[64];
         int have_prev = 0;
         for (int it = 0; it < iters; ++it) {
-            for (int i = 0; i < n; ++i) a[i] = (uint8_t)nearest4(v[i], c);
+            for (int i = 0; i < n; ++i) a[i] = (uint8_t)nearest4((double)v[i], c);
             ++passes;
             if (have_prev && memcmp(a, prev, (size_t)n) == 0) break;
             for (int j = 0; j < 4; ++j) {
-                float sum = 0.0f;
+                double sum = 0.0;
                 int cnt = 0;
                 for (int i = 0; i < n; ++i)
-                    if (a[i] == j) { sum += v[i]; ++cnt; }
-                if (cnt > 0) c[j] = sum / (float)cnt;
+                    if (a[i] == j) { sum += (double)v[i]; ++cnt; }
+                if (cnt > 0) c[j] = sum / (double)cnt;
             }
             memcpy(prev, a, (size_t)n);
             have_prev = 1;
         }
     }
-    float c16[4];
+    double c16[4];
     for (int j = 0; j < 4; ++j) {
-        uint16_t h = or_fp16_encode((double)c[j]);
+        uint16_t h = or_fp16_encode(c[j]);
         if (c16_out) c16_out[j] = h;
-        c16[j] = (float)or_fp16_decode(h);
+        c16[j] = or_fp16_decode(h);
         if (c_out) c_out[j] = c[j];
     }
     if (codes_out)
-        for (int i = 0; i < n; ++i) codes_out[i] = (uint8_t)nearest4(v[i], c16);
+        for (int i = 0; i < n; ++i) codes_out[i] = (uint8_t)nearest4((double)v[i], c16);
     return passes;
 }
 
@@ -504,10 +507,11 @@ static int fp8_byte(int D, int role, int t, int c)
 /*   mn, mx over the group's non-outliers; S = fp16((mx - mn) / 15),          */
 /*   m = fp16(mn) (the zero point stored as the group minimum: x = q*S + m is */
 /*   the same affine map as (q - Z)*S with Z = -mn/S);                        */
-/*   q = clamp(rint((x - m) / S), 0, 15) in binary32 from the stored S, m;    */
+/*   q = clamp(rint((x - m) / S), 0, 15) in fp64 from the stored S, m;        */
 /*   S == 0 gives q = 0; outlier slots hold q = 0 and the value as fp16.      */
 /* E2M1 reading (one e4m3 scale per 16 values, no outliers):                  */
-/*   s = e4m3(f32(amax / 6)); q = e2m1(f32(x / s)), s == 0 gives q = 0.       */
+/*   s = e4m3(amax / 6); q = e2m1(x / s) (quotients in fp64, rounded once to  */
+/*   the format); s == 0 gives q = 0.                                         */
 /* ------------------------------------------------------------------------- */
 
 static void quantize_token_int4(const float* x, int D, double sigma, int role, int t, uint8_t* blk)
@@ -530,8 +534,8 @@ static void quantize_token_int4(const float* x, int D, double sigma, int role, i
             have = 1;
         }
         uint16_t S16 = 0, m16 = 0;
-        if (have) { S16 = or_fp16_encode((double)((mx - mn) / 15.0f)); m16 = or_fp16_encode((double)mn); }
-        float S = (float)or_fp16_decode(S16), m = (float)or_fp16_decode(m16);
+        if (have) { S16 = or_fp16_encode(((double)mx - (double)mn) / 15.0); m16 = or_fp16_encode((double)mn); }
+        double S = or_fp16_decode(S16), m = or_fp16_decode(m16);
         for (int i = 0; i < 32; ++i) {
             int c = 32 * g + i;
             uint8_t q = 0;
@@ -539,10 +543,10 @@ static void quantize_token_int4(const float* x, int D, double sigma, int role, i
                 chans[t * cap + cnt] = (uint8_t)c;
                 put_u16(vals + 2 * (t * cap + cnt), or_fp16_encode((double)v[i]));
                 ++cnt;
-            } else if (S != 0.0f) {
-                float r = rintf((v[i] - m) / S);
-                if (r < 0.0f) r = 0.0f;
-                if (r > 15.0f) r = 15.0f;
+            } else if (S != 0.0) {
+                double r = rint(((double)v[i] - m) / S);
+                if (r < 0.0) r = 0.0;
+                if (r > 15.0) r = 15.0;
                 q = (uint8_t)r;
             }
             nib_set(blk, D, role, t, c, q);
@@ -562,11 +566,11 @@ static void quantize_token_e2m1(const float* x, int D, int role, int t, uint8_t*
             float a = fabsf(x[16 * s + i]);
             if (a > amax) amax = a;
         }
-        uint8_t s8 = or_e4m3_encode((double)f32_div(amax, 6.0f));
-        float sc = (float)or_e4m3_decode(s8);
+        uint8_t s8 = or_e4m3_encode((double)amax / 6.0);
+        double sc = or_e4m3_decode(s8);
         for (int i = 0; i < 16; ++i) {
             uint8_t q = 0;
-            if (sc != 0.0f) q = or_e2m1_encode((double)f32_div(x[16 * s + i], sc));
+            if (sc != 0.0) q = or_e2m1_encode((double)x[16 * s + i] / sc);
             nib_set(blk, D, role, t, 16 * s + i, q);
         }
         blk[8 * D + 16 * s + t] = s8;
@@ -581,7 +585,8 @@ static void quantize_token_e2m1(const float* x, int D, int role, int t, uint8_t*
 /* slots are 0; the side-list keeps (channel, e4m3(x)) sorted by (token,      */
 /* channel) with a per-token count.                                           */
 /* FP8 tier ([P2] "Tier 1 (High-Precision FP8)"): one fp32 scale per block,   */
-/* s = f32(amax / 448); q = e4m3(f32(x / s)); s == 0 gives q = 0.             */
+/* s = f32(amax / 448) (the fp64 quotient rounded to binary32, the stored     */
+/* scale); q = e4m3(x / s) with the quotient in fp64; s == 0 gives q = 0.     */
 /* ------------------------------------------------------------------------- */
 
 static void write_side_list(const float* x, int D, uint8_t mask[16][128], uint8_t* hdr);
@@ -637,7 +642,7 @@ static void write_side_list(const float* x, int D, uint8_t mask[16][128], uint8_
 /* ASYM3 ([P3] "Sub-Byte KV-Cache Quantization": asymmetric 3-bit packing with
  * dynamic outlier preservation).  Outliers as CB2 (sigma rule per token over
  * the head vector, e4m3 side-list).  Per channel, over its non-outliers in
- * binary32 (the INT4 recipe with 8 levels): S = fp16((max - min) / 7),
+ * fp64 (the INT4 recipe with 8 levels): S = fp16((max - min) / 7),
  * m = fp16(min), q = clamp(rint((x - m) / S), 0, 7) (q = 0 when S == 0 or the
  * channel has no non-outlier); outlier slots hold q = 0.  The value a code
  * stands for is fp16(q * S + m), one rounding of the exact value. */
@@ -658,16 +663,16 @@ static void quantize_page_a3(const float* x, int D, double sigma, int role, uint
             have = 1;
         }
         uint16_t S16 = 0, m16 = 0;
-        if (have) { S16 = or_fp16_encode((double)((mx - mn) / 7.0f)); m16 = or_fp16_encode((double)mn); }
-        float S = (float)or_fp16_decode(S16), m = (float)or_fp16_decode(m16);
+        if (have) { S16 = or_fp16_encode(((double)mx - (double)mn) / 7.0); m16 = or_fp16_encode((double)mn); }
+        double S = or_fp16_decode(S16), m = or_fp16_decode(m16);
         put_u16(blk + 6 * D + 2 * a3_rho(role, c), S16);
         put_u16(blk + 8 * D + 2 * a3_rho(role, c), m16);
         for (int t = 0; t < 16; ++t) {
             uint8_t q = 0;
-            if (!mask[t][c] && S != 0.0f) {
-                float r = rintf((x[t * D + c] - m) / S);
-                if (r < 0.0f) r = 0.0f;
-                if (r > 7.0f) r = 7.0f;
+            if (!mask[t][c] && S != 0.0) {
+                double r = rint(((double)x[t * D + c] - m) / S);
+                if (r < 0.0) r = 0.0;
+                if (r > 7.0) r = 7.0;
                 q = (uint8_t)r;
             }
             a3_code_set(blk, D, role, t, c, q);
@@ -738,11 +743,11 @@ static void quantize_page_fp8(const float* x, int D, int role, uint8_t* blk)
         float a = fabsf(x[i]);
         if (a > amax) amax = a;
     }
-    float s = f32_div(amax, 448.0f);
+    float s = f32_of_quotient(amax, 448.0f);
     for (int t = 0; t < 16; ++t)
         for (int c = 0; c < D; ++c) {
             uint8_t q = 0;
-            if (s != 0.0f) q = or_e4m3_encode((double)f32_div(x[t * D + c], s));
+            if (s != 0.0f) q = or_e4m3_encode((double)x[t * D + c] / (double)s);
             blk[fp8_byte(D, role, t, c)] = q;
         }
     put_f32(blk + 16 * D, s);

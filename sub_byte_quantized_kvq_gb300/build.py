@@ -17,8 +17,9 @@ LIB = os.path.join(BUILD, "libkvq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
-# The quantizer takes its binary32 decisions exactly as written (no fused
-# multiply-add), so that they match the CPU oracle bit for bit.
+# The quantizer's arithmetic runs exactly as written (no fused multiply-add):
+# its binary32 error bounds and its fp64 recomputations assume one rounding
+# per operation, as the definition has.
 PER_TU = {"kvq_quantize.cu": ["--fmad=false"]}
 TUS = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu", "kvq_decode_int4.cu", "kvq_decode_e2m1.cu",
        "kvq_decode_cb2.cu", "kvq_decode_tiered.cu", "kvq_decode_cb2s.cu",

@@ -1,7 +1,13 @@
-// kvq_quantize.cu -- quantize-on-append into the paged cache.  The quantizer's
-// decisions (outlier tests, Lloyd-Max, INT4 codes) are taken in binary32 in a
-// fixed order; the file is compiled with --fmad=false so no multiply-add is
-// fused and codes are bit-identical to the CPU reference.
+// kvq_quantize.cu -- quantize-on-append into the paged cache.  The quantizer
+// is defined in fp64 (statistics, Lloyd-Max fit, scales and codes, each result
+// rounded once to its stored format).  Every decision is first taken in
+// binary32 together with a bound on how far that arithmetic can be from the
+// fp64 one; where the bound does not separate the two sides of the decision
+// (a value within rounding of a threshold, a Lloyd cell boundary or a
+// rounding midpoint) the unit is recomputed in fp64 in the definition's own
+// order, so codes are bit-identical to the fp64 definition while fp64 runs
+// only on those rare units.  Compiled with --fmad=false: no multiply-add is
+// fused in either precision.
 //
 // "The Sub-10ms Barrier: Fusing Sparse MoE Routing with FP4 KV-Cache
 // Quantization", section 2 ("Outlier Isolation and Block-wise Quantization"):
@@ -131,28 +137,190 @@ __device__ __forceinline__ uint8_t f32_to_e2m1(float x) {
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Outlier statistics of one vector (binary32, ascending order): mean mu and
-// threshold sigma * s, s the unbiased standard deviation.
-__device__ __forceinline__ void outlier_stats(const float* x, int n, int stride, float sigma, float& mu, float& thr) {
-  float sum = 0.f;
-  for (int i = 0; i < n; ++i) sum += x[i * stride];
-  mu = __fdiv_rn(sum, (float)n);
+// ----------------------------------------------------------------------------- certified decisions
+// Unit roundoff of binary32, and the relative nudge used to test a rounding
+// decision: a binary32 result r within relative error 3u of the exact value
+// rounds to the same code as the exact value (and as the fp64 value, which is
+// far closer) whenever r * (1 - kNudge) and r * (1 + kNudge) round to the same
+// code, rounding being monotone (the nudged products are themselves rounded,
+// by at most u, so they still enclose r (1 +- 5u)).
+constexpr float kU = 5.9604645e-08f;      // 2^-24
+constexpr float kNudge = 4.76837158e-07f; // 2^-21
+
+// Round |a| (finite, >= 0) to the grid of a binary format with `mbits`
+// mantissa bits and smallest normal exponent emin, ties to even, in fp64:
+// quantum 2^(max(e, emin) - mbits) for a in [2^e, 2^(e+1)).  The result is a
+// grid point, exact in binary32 for the formats used here (fp16, e4m3, e2m1),
+// so a conversion of it from binary32 is exact (or saturates / overflows as
+// the format does).
+__device__ __noinline__ double grid_round64(double a, int mbits, int emin) {
+  if (a == 0.0) return 0.0;
+  int e = ilogb(a);
+  if (e < emin) e = emin;
+  const double q = ldexp(1.0, e - mbits);
+  return rint(a / q) * q;
+}
+__device__ __noinline__ uint16_t f16_from_f64(double v) {
+  const float r = (float)grid_round64(fabs(v), 10, -14);
+  return (uint16_t)(f32_to_f16_bits(r) | (signbit(v) ? 0x8000u : 0u));
+}
+__device__ __noinline__ uint8_t e4m3_from_f64(double v) {
+  const float r = (float)grid_round64(fabs(v), 3, -6);
+  return (uint8_t)(f32_to_e4m3(r) | (signbit(v) ? 0x80u : 0u));
+}
+__device__ __noinline__ uint8_t e2m1_from_f64(double v) {
+  const float r = (float)grid_round64(fabs(v), 1, 0);
+  return (uint8_t)(f32_to_e2m1(r) | (signbit(v) ? 0x8u : 0u));
+}
+
+// The fp64 side of each certified rounding below (called only when the
+// binary32 result cannot be certified; kept out of line so the common path
+// holds no fp64 state).
+__device__ __noinline__ uint16_t f16_of_quotient64(float a, float b) { return f16_from_f64((double)a / (double)b); }
+__device__ __noinline__ uint16_t f16_of_range64(float mx, float mn, float div) {
+  return f16_from_f64(((double)mx - (double)mn) / (double)div);
+}
+__device__ __noinline__ uint8_t e4m3_of_quotient64(float a, float b) { return e4m3_from_f64((double)a / (double)b); }
+__device__ __noinline__ uint8_t e2m1_of_quotient64(float a, float b) { return e2m1_from_f64((double)a / (double)b); }
+__device__ __noinline__ uint32_t affine_code64(float x, float m, float S, float qmax) {
+  const double r = rint(((double)x - (double)m) / (double)S);
+  return (uint32_t)fmin(fmax(r, 0.0), (double)qmax);
+}
+
+// Whether the binary32 quotient r = fl(a / b) is exact: then it is the fp64
+// quotient too, and any rounding of it (ties included) agrees with the
+// definition.  The residual a - r b is exact in one fused multiply-add.
+__device__ __forceinline__ bool quotient_exact(float r, float a, float b) { return __fmaf_rn(-r, b, a) == 0.f; }
+// Whether the binary32 difference d = fl(x - m) is exact (TwoSum error term).
+__device__ __forceinline__ bool difference_exact(float d, float x, float m) {
+  const float bb = d - x;
+  return (x - (d - bb)) + (-m - bb) == 0.f;
+}
+
+// fp16 bits of q = a / b, q's fp64 value rounded once (a, b binary32): the
+// binary32 quotient when it is exact or the nudge cannot change its rounding,
+// else fp64.
+__device__ __forceinline__ uint16_t f16_of_quotient(float a, float b) {
+  const float r = __fdiv_rn(a, b);
+  const uint16_t h = f32_to_f16_bits(r);
+  if (f32_to_f16_bits(r * (1.f - kNudge)) == h && f32_to_f16_bits(r * (1.f + kNudge)) == h) return h;
+  if (quotient_exact(r, a, b)) return h;
+  return f16_of_quotient64(a, b);
+}
+// fp16 bits of (mx - mn) / div (the affine formats' scale S), the same way;
+// the binary32 value carries two roundings (the difference, the quotient).
+__device__ __forceinline__ uint16_t f16_of_range(float mx, float mn, float div) {
+  const float d = mx - mn, r = __fdiv_rn(d, div);
+  const uint16_t h = f32_to_f16_bits(r);
+  if (f32_to_f16_bits(r * (1.f - kNudge)) == h && f32_to_f16_bits(r * (1.f + kNudge)) == h) return h;
+  if (difference_exact(d, mx, mn) && quotient_exact(r, d, div)) return h;
+  return f16_of_range64(mx, mn, div);
+}
+// e4m3 / e2m1 code of a / b, the same way.
+__device__ __forceinline__ uint8_t e4m3_of_quotient(float a, float b) {
+  const float r = __fdiv_rn(a, b);
+  const uint8_t c = f32_to_e4m3(r);
+  if (f32_to_e4m3(r * (1.f - kNudge)) == c && f32_to_e4m3(r * (1.f + kNudge)) == c) return c;
+  if (quotient_exact(r, a, b)) return c;
+  return e4m3_of_quotient64(a, b);
+}
+__device__ __forceinline__ uint8_t e2m1_of_quotient(float a, float b) {
+  const float r = __fdiv_rn(a, b);
+  const uint8_t c = f32_to_e2m1(r);
+  if (f32_to_e2m1(r * (1.f - kNudge)) == c && f32_to_e2m1(r * (1.f + kNudge)) == c) return c;
+  if (quotient_exact(r, a, b)) return c;
+  return e2m1_of_quotient64(a, b);
+}
+// Affine code clamp(rint((x - m) / S), 0, qmax) (S, m fp16 values, S != 0)
+// with the quotient in fp64: (x - m) and the division are each rounded once in
+// binary32 (relative error <= 2u + u^2, no cancellation term since x and m are
+// exact inputs), so the nudge test certifies the binary32 code; so does an
+// exact difference and quotient (a tie then resolves to even in both).
+__device__ __forceinline__ uint32_t affine_code(float x, float m, float S, float qmax) {
+  const float d = x - m, r = __fdiv_rn(d, S);
+  const float c = fminf(fmaxf(rintf(r), 0.f), qmax);
+  const float lo = fminf(fmaxf(rintf(r * (1.f - kNudge)), 0.f), qmax);
+  const float hi = fminf(fmaxf(rintf(r * (1.f + kNudge)), 0.f), qmax);
+  if (lo == c && hi == c) return (uint32_t)c;
+  if (difference_exact(d, x, m) && quotient_exact(r, d, S)) return (uint32_t)c;
+  return affine_code64(x, m, S, qmax);
+}
+
+// The outlier decisions of outlier_decide below, in fp64 in the definition's
+// order (ascending sums, strict comparison).
+__device__ __noinline__ void outlier_decide64(const float* x, int n, int stride, double sigma, int kmax,
+                                              uint32_t* bits) {
+  double sum64 = 0.0;
+  for (int i = 0; i < n; ++i) sum64 += (double)x[i * stride];
+  const double mu64 = sum64 / (double)n;
+  double ss64 = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const double d = (double)x[i * stride] - mu64;
+    ss64 += d * d;
+  }
+  const double thr64 = sigma * sqrt(ss64 / (double)(n - 1));
+  int k = 0;
+  for (int w = 0; w < (n + 31) / 32; ++w) {
+    uint32_t m = 0;
+    for (int j = 0; j < 32 && 32 * w + j < n; ++j) {
+      int out = fabs((double)x[(32 * w + j) * stride] - mu64) > thr64;
+      if (out && k >= kmax) out = 0;
+      m |= (uint32_t)out << j;
+      k += out;
+    }
+    bits[w] = m;
+  }
+}
+
+// Outlier decisions of one vector x[i * stride], i < n <= 128, as bits
+// (bit i % 32 of bits[i / 32]): x_i is an outlier iff |x_i - mu| > sigma * s,
+// mu the mean and s the unbiased standard deviation, at most kmax kept (the
+// lowest indices).  Defined in fp64 with ascending-index sums.  The binary32
+// pass (sequential sums) stays within E = 2 n (2 + sigma) u max|x| of the
+// exact |x_i - mu| - sigma s for every i (mean: (n + 1) u max|x|; s: the
+// deviation errors plus n u s from the sum of squares, s <= 2 max|x|), and
+// the fp64 pass within 1e-12 of that; when some |x_i - mu| - sigma s is not
+// farther than E from 0 the vector is decided again in fp64.
+__device__ __noinline__ void outlier_decide(const float* x, int n, int stride, double sigma, int kmax, uint32_t* bits) {
+  const float sg = (float)sigma;
+  float sum = 0.f, amax = 0.f;
+  for (int i = 0; i < n; ++i) {
+    const float v = x[i * stride];
+    sum += v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+  const float mu = __fdiv_rn(sum, (float)n);
   float ss = 0.f;
   for (int i = 0; i < n; ++i) {
     const float d = x[i * stride] - mu;
     ss += d * d;
   }
-  thr = sigma * __fsqrt_rn(__fdiv_rn(ss, (float)(n - 1)));
+  const float thr = sg * __fsqrt_rn(__fdiv_rn(ss, (float)(n - 1)));
+  const float E = 2.f * (float)n * (2.f + sg) * kU * amax;
+  bool sure = true;
+  int k = 0;
+  for (int w = 0; w < (n + 31) / 32; ++w) {
+    uint32_t m = 0;
+    for (int j = 0; j < 32 && 32 * w + j < n; ++j) {
+      const float f = fabsf(x[(32 * w + j) * stride] - mu);
+      sure = sure && fabsf(f - thr) > E;   // false for a NaN anywhere: decided in fp64
+      int out = f > thr;
+      if (out && k >= kmax) out = 0;
+      m |= (uint32_t)out << j;
+      k += out;
+    }
+    bits[w] = m;
+  }
+  if (!sure) outlier_decide64(x, n, stride, sigma, kmax, bits);
 }
 
-// Outlier mask of one vector: |x - mu| > sigma * s; at most kmax kept (lowest indices).
-__device__ int outlier_mask(const float* x, int n, int stride, float sigma, int kmax, uint8_t* mask, int mstride) {
-  float mu, thr;
-  outlier_stats(x, n, stride, sigma, mu, thr);
+// Outlier mask of one vector as bytes mask[i * mstride] (see outlier_decide).
+__device__ int outlier_mask(const float* x, int n, int stride, double sigma, int kmax, uint8_t* mask, int mstride) {
+  uint32_t bits[4];
+  outlier_decide(x, n, stride, sigma, kmax, bits);
   int k = 0;
   for (int i = 0; i < n; ++i) {
-    int out = fabsf(x[i * stride] - mu) > thr;
-    if (out && k >= kmax) out = 0;
+    const int out = (bits[i >> 5] >> (i & 31)) & 1u;
     mask[i * mstride] = (uint8_t)out;
     k += out;
   }
@@ -162,20 +330,8 @@ __device__ int outlier_mask(const float* x, int n, int stride, float sigma, int 
 // The same decisions for one row of D values as bits: bit c % 32 of
 // bits[c / 32] is set for an outlier channel c.
 template <int D>
-__device__ void outlier_bits(const float* x, float sigma, int kmax, uint32_t* bits) {
-  float mu, thr;
-  outlier_stats(x, D, 1, sigma, mu, thr);
-  int k = 0;
-  for (int w = 0; w < D / 32; ++w) {
-    uint32_t m = 0;
-    for (int j = 0; j < 32; ++j) {
-      int out = fabsf(x[32 * w + j] - mu) > thr;
-      if (out && k >= kmax) out = 0;
-      m |= (uint32_t)out << j;
-      k += out;
-    }
-    bits[w] = m;
-  }
+__device__ void outlier_bits(const float* x, double sigma, int kmax, uint32_t* bits) {
+  outlier_decide(x, D, 1, sigma, kmax, bits);
 }
 
 __device__ __forceinline__ int nearest4(float v, const float* c) {
@@ -187,35 +343,236 @@ __device__ __forceinline__ int nearest4(float v, const float* c) {
   }
   return best;
 }
+// Nearest of four centroids (lowest index on ties) and whether the choice is
+// certain: the runner-up is farther by more than E.
+__device__ __forceinline__ int nearest4_sure(float v, const float* c, float E, bool& sure) {
+  int best = 0;
+  float bd = fabsf(v - c[0]), sd = INFINITY;
+  for (int j = 1; j < 4; ++j) {
+    const float d = fabsf(v - c[j]);
+    if (d < bd) { sd = bd; bd = d; best = j; }
+    else sd = fminf(sd, d);
+  }
+  sure = sure && sd - bd > E;
+  return best;
+}
 
-// Lloyd-Max 4-centroid fit, in binary32, of the values x[r * xs] of the rows
-// r < NROWS set in `keep`, taken in row order: linspace(min, max, 4) start,
-// nearest centroid (lowest index on ties), at most `iters` assignment passes,
-// stop when an assignment repeats, centroid = mean of its values.  Returns the
-// fp16 centroids and, 2 bits per row, the code of each kept row (0 elsewhere).
-// Values are read from shared memory on every pass; assignments are packed 16
-// to a word, so the fit holds few registers.
+// Lloyd-Max 4-centroid fit of the values x[r * xs] of the rows r < NROWS set
+// in `keep`, taken in row order, exactly as defined (fp64): linspace(min, max,
+// 4) start, nearest centroid (lowest index on ties), at most `iters`
+// assignment passes, stop when an assignment repeats, centroid = mean of its
+// values (an empty cell keeps its centroid), centroids rounded once to fp16,
+// codes = the nearest fp16 centroid.
 template <int NROWS>
-__device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
-                            uint32_t (&code)[(NROWS + 15) / 16]) {
+__device__ __noinline__ void lloyd4_rows64(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
+                                           uint32_t (&code)[(NROWS + 15) / 16]) {
   constexpr int NW = (NROWS + 15) / 16;
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+  double c[4] = {0.0, 0.0, 0.0, 0.0};
   for (int w = 0; w < NW; ++w) code[w] = 0u;
+  auto near64 = [](double v, const double* cc) {
+    int best = 0;
+    double bd = fabs(v - cc[0]);
+    for (int j = 1; j < 4; ++j) {
+      const double d = fabs(v - cc[j]);
+      if (d < bd) { bd = d; best = j; }
+    }
+    return best;
+  };
   if (keep) {
     bool have = false;
-    float mn = 0.f, mx = 0.f;
+    double mn = 0.0, mx = 0.0;
+    for (int r = 0; r < NROWS; ++r) {
+      if (!(keep >> r & 1u)) continue;
+      const double v = x[r * xs];
+      if (!have) { mn = v; mx = v; have = true; }
+      mn = v < mn ? v : mn;
+      mx = v > mx ? v : mx;
+    }
+    const double h = (mx - mn) / 3.0;
+    c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0 * h; c[3] = mx;
+    uint32_t prev[NW], a[NW];
+    bool have_prev = false;
+    for (int it = 0; it < iters; ++it) {
+      for (int w = 0; w < NW; ++w) a[w] = 0u;
+      for (int r = 0; r < NROWS; ++r)
+        if (keep >> r & 1u) a[r >> 4] |= (uint32_t)near64((double)x[r * xs], c) << (2 * (r & 15));
+      bool same = have_prev;
+      for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
+      if (same) break;
+      for (int jj = 0; jj < 4; ++jj) {
+        double sum = 0.0;
+        int cnt = 0;
+        for (int r = 0; r < NROWS; ++r)
+          if ((keep >> r & 1u) && ((a[r >> 4] >> (2 * (r & 15))) & 3u) == (uint32_t)jj) {
+            sum += (double)x[r * xs];
+            ++cnt;
+          }
+        if (cnt > 0) c[jj] = sum / (double)cnt;
+      }
+      for (int w = 0; w < NW; ++w) prev[w] = a[w];
+      have_prev = true;
+    }
+  }
+  double cf[4];
+  for (int jj = 0; jj < 4; ++jj) {
+    c16[jj] = f16_from_f64(c[jj]);
+    cf[jj] = (double)f16_bits_to_f32(c16[jj]);
+  }
+  for (int r = 0; r < NROWS; ++r)
+    if (keep >> r & 1u) code[r >> 4] |= (uint32_t)near64((double)x[r * xs], cf) << (2 * (r & 15));
+}
+
+// Exponent of the lowest set bit of binary32 v != 0 (v is a multiple of 2^e).
+__device__ __forceinline__ int low_bit_exp(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const int ef = (int)((u >> 23) & 0xFFu);
+  const uint32_t m = (u & 0x7FFFFFu) | (ef ? 0x800000u : 0u);
+  return (ef ? ef : 1) - 150 + (__ffs((int)m) - 1);
+}
+
+// Whether v's four distances |v - c_j| decide alike in binary32 and fp64: each
+// c_j is its exact value (a binary32 mean that is the exact mean, or an input
+// value) and each subtraction is exact, so both precisions compare the same
+// exact numbers, ties included.
+__device__ __forceinline__ bool distances_exact(float v, const float* c, const bool* cx) {
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ok = ok && cx[j] && difference_exact(v - c[j], v, c[j]);
+  return ok;
+}
+
+// The fp64 mean of the rows of `keep` whose code in `asg` is j, summed in row
+// order (the definition's order).
+template <int NROWS>
+__device__ __noinline__ double cell_mean64(const float* x, int xs, uint64_t keep, const uint32_t* asg, int j) {
+  double sum = 0.0;
+  int cnt = 0;
+  for (int r = 0; r < NROWS; ++r)
+    if ((keep >> r & 1u) && ((asg[r >> 4] >> (2 * (r & 15))) & 3u) == (uint32_t)j) {
+      sum += (double)x[r * xs];
+      ++cnt;
+    }
+  return sum / (double)cnt;
+}
+// The nearest of four fp16 centroids to v by fp64 distances (lowest index on ties).
+__device__ __noinline__ int nearest4_64(float v, const float* cf) {
+  int best = 0;
+  double bd = fabs((double)v - (double)cf[0]);
+  for (int j = 1; j < 4; ++j) {
+    const double d = fabs((double)v - (double)cf[j]);
+    if (d < bd) { bd = d; best = j; }
+  }
+  return best;
+}
+
+// Centroid j's fp64 value as the definition computes it, given its source: a
+// linspace point (from the min mn and max mx), or the mean of a cell whose
+// sum `sum` of `cnt` values is exact in binary32 (so the fp64 sum, in any
+// order, is the same number).
+__device__ __noinline__ double centroid64(int j, float mn, float mx, bool lin, float sum, int cnt) {
+  if (lin) {
+    const double h = ((double)mx - (double)mn) / 3.0;
+    return j == 0 ? (double)mn : j == 1 ? (double)mn + h : j == 2 ? (double)mn + 2.0 * h : (double)mx;
+  }
+  return (double)sum / (double)cnt;
+}
+// The fp64 nearest centroid of v (lowest index on ties) among those whose
+// binary32 distance is within 2E of the binary32 best -- the others are
+// farther in fp64 as well (each distance is within E / 2 of its fp64 value).
+__device__ __noinline__ int nearest4_by64(float v, const float* c, float E, float mn, float mx, const bool* lin,
+                                          const float* sumc, const int* cntc) {
+  float bd = INFINITY;
+  for (int j = 0; j < 4; ++j) bd = fminf(bd, fabsf(v - c[j]));
+  int best = -1;
+  double b64 = 0.0;
+  for (int j = 0; j < 4; ++j) {
+    if (fabsf(v - c[j]) > bd + 2.f * E) continue;
+    const double d = fabs((double)v - centroid64(j, mn, mx, lin[j], sumc[j], cntc[j]));
+    if (best < 0 || d < b64) { b64 = d; best = j; }
+  }
+  return best;
+}
+// The mean of the rows of `keep` whose code in `asg` is j, from a compensated
+// (TwoSum) binary32 sum: within 4 u |mean| + 4 n^2 u^2 max|value| of the
+// exact mean, and so of its fp64 value.  Returns the mean and its bound.
+template <int NROWS>
+__device__ __noinline__ float2 cell_mean_tight(const float* x, int xs, uint64_t keep, const uint32_t* asg, int j) {
+  float hi = 0.f, lo = 0.f, m = 0.f;
+  int n = 0;
+  for (int r = 0; r < NROWS; ++r)
+    if ((keep >> r & 1u) && ((asg[r >> 4] >> (2 * (r & 15))) & 3u) == (uint32_t)j) {
+      const float v = x[r * xs];
+      const float sm = hi + v, bb = sm - hi;
+      lo += (hi - (sm - bb)) + (v - bb);
+      hi = sm;
+      m = fmaxf(m, fabsf(v));
+      ++n;
+    }
+  const float fn = (float)n;
+  const float q1 = __fdiv_rn(hi, fn);
+  const float r1 = __fmaf_rn(-q1, fn, hi);   // exact
+  const float mean = q1 + __fdiv_rn(r1 + lo, fn);
+  return make_float2(mean, 4.f * kU * fabsf(mean) + 4.f * fn * fn * kU * kU * m);
+}
+
+// The same fit, run in binary32 with a bound: while the assignments agree, a
+// centroid is the mean of the same values in either precision, and a binary32
+// mean of cnt values lies within cnt u max|value| of the fp64 one (a sum of
+// cnt terms, then one division); the linspace points lie within 4 u max|x|.
+// So every assignment whose runner-up is farther by more than E = 2 (NROWS +
+// 4) u max|x| is the fp64 one; so is one whose four distances are exact
+// (exact centroids -- exact sums, by the span of the values' bits, and exact
+// quotients -- and exact subtractions).  Any other assignment is taken again
+// in fp64 from the centroids' fp64 values (their sums are exact when the
+// values' bits span at most 24 bits; otherwise the channel is refitted by
+// lloyd4_rows64).  The fp16 rounding of each final centroid is checked over
+// +-2 (cnt + 2) u max|member| around it, then from a compensated mean, then
+// done in fp64.  Each final code is checked by its own margin, 4 u (|x| +
+// max|centroid|) (one rounded subtraction per distance), else by exact
+// distances, else taken with fp64 distances.  Values are read from shared
+// memory on every pass; assignments are packed 16 to a word, so the fit holds
+// few registers.
+template <int NROWS>
+__device__ __noinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
+                                         uint32_t (&code)[(NROWS + 15) / 16]) {
+  constexpr int NW = (NROWS + 15) / 16;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  bool cx[4] = {true, true, true, true};       // centroid j is exactly its fp64 value
+  bool lin[4] = {false, false, false, false};  // centroid j is still its linspace point
+  float sumc[4] = {0.f, 0.f, 0.f, 0.f};        // the sum and count centroid j was last formed from
+  int cntc[4] = {1, 1, 1, 1};
+#pragma unroll
+  for (int w = 0; w < NW; ++w) code[w] = 0u;
+  bool sure = true, flat = false, sums_exact = false;
+  float E = 0.f, mn = 0.f, mx = 0.f;
+  uint32_t prev[NW];
+  bool have_prev = false;
+  if (keep) {
+    bool have = false;
+    int elo = 1000;
     for (int r = 0; r < NROWS; ++r) {
       if (!(keep >> r & 1u)) continue;
       const float v = x[r * xs];
       if (!have) { mn = v; mx = v; have = true; }
       mn = v < mn ? v : mn;
       mx = v > mx ? v : mx;
+      if (v != 0.f) elo = min(elo, low_bit_exp(v));
     }
+    const float amax = fmaxf(fabsf(mn), fabsf(mx));
+    // every partial sum of at most NROWS of these values is a multiple of
+    // 2^elo below NROWS * amax: exact in binary32 (and fp64) if that spans
+    // at most 24 bits
+    int eh = 0;
+    frexpf(amax * (float)NROWS, &eh);
+    sums_exact = amax == 0.f || eh - elo <= 24;
+    // one value repeated: all centroids equal it in either precision and
+    // every assignment is centroid 0; no margin to check
+    flat = mn == mx;
+    E = flat ? -1.f : 2.f * (float)(NROWS + 4) * kU * amax;
     const float h = __fdiv_rn(mx - mn, 3.0f);
     c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0f * h; c[3] = mx;
-    uint32_t prev[NW];
-    bool have_prev = false;
+    cx[1] = cx[2] = flat;   // linspace interior points: exact only when h = 0
+    lin[0] = lin[1] = lin[2] = lin[3] = true;
     for (int it = 0; it < iters; ++it) {
       // one pass assigns every value and sums each centroid's members in row
       // order (four independent sums: adding +0.0 to the others changes none
@@ -228,7 +585,12 @@ __device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, ui
       for (int r = 0; r < NROWS; ++r) {
         if (!(keep >> r & 1u)) continue;
         const float v = x[r * xs];
-        const uint32_t j = (uint32_t)nearest4(v, c);
+        bool ok = true;
+        uint32_t j = (uint32_t)nearest4_sure(v, c, E, ok);
+        if (!ok && !distances_exact(v, c, cx)) {
+          if (sums_exact) j = (uint32_t)nearest4_by64(v, c, E, mn, mx, lin, sumc, cntc);
+          else sure = false;
+        }
         a[r >> 4] |= j << (2 * (r & 15));
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -243,16 +605,79 @@ __device__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, ui
       // centroid j = the mean of its values
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
-        if (cnt[jj] > 0) c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
+        if (cnt[jj] > 0) {
+          c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
+          cx[jj] = sums_exact && quotient_exact(c[jj], sum[jj], (float)cnt[jj]);
+          lin[jj] = false;
+          sumc[jj] = sum[jj];
+          cntc[jj] = cnt[jj];
+        }
 #pragma unroll
       for (int w = 0; w < NW; ++w) prev[w] = a[w];
       have_prev = true;
     }
   }
-  float cf[4];
-  for (int jj = 0; jj < 4; ++jj) { c16[jj] = f32_to_f16_bits(c[jj]); cf[jj] = f16_bits_to_f32(c16[jj]); }
+  if (!sure) {   // an assignment neither bound nor exact sums settle: the whole fit in fp64
+    lloyd4_rows64<NROWS>(x, xs, keep, iters, c16, code);
+    return;
+  }
+  // each centroid's own bound: its cell in the last update (prev), else the
+  // channel's bound (a linspace point, or a mean of an earlier cell)
+  float ec[4] = {E, E, E, E};
+  int ncell[4] = {0, 0, 0, 0};
+  if (have_prev && !flat) {
+    float mcell[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < NROWS; ++r) {
+      if (!(keep >> r & 1u)) continue;
+      const uint32_t j = (prev[r >> 4] >> (2 * (r & 15))) & 3u;
+      const float av = fabsf(x[r * xs]);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        mcell[jj] = j == (uint32_t)jj ? fmaxf(mcell[jj], av) : mcell[jj];
+        ncell[jj] += j == (uint32_t)jj;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      if (ncell[jj] > 0) ec[jj] = 2.f * (float)(ncell[jj] + 2) * kU * mcell[jj];
+  }
+  float cf[4], cmax = 0.f;
+  for (int jj = 0; jj < 4; ++jj) {
+    c16[jj] = f32_to_f16_bits(c[jj]);
+    const float e = fmaxf(ec[jj], fabsf(c[jj]) * kNudge);
+    bool ok = cx[jj] || (f32_to_f16_bits(c[jj] - e) == c16[jj] && f32_to_f16_bits(c[jj] + e) == c16[jj]);
+    if (!ok && !lin[jj] && !sums_exact && ncell[jj] > 0) {   // a compensated mean of its cell
+      const float2 mb = cell_mean_tight<NROWS>(x, xs, keep, prev, jj);
+      const uint16_t hm = f32_to_f16_bits(mb.x);
+      if (f32_to_f16_bits(mb.x - mb.y) == hm && f32_to_f16_bits(mb.x + mb.y) == hm) {
+        c16[jj] = hm;
+        ok = true;
+      }
+    }
+    if (!ok) {
+      if (lin[jj] || sums_exact) {
+        c16[jj] = f16_from_f64(centroid64(jj, mn, mx, lin[jj], sumc[jj], cntc[jj]));
+      } else if (ncell[jj] > 0) {
+        c16[jj] = f16_from_f64(cell_mean64<NROWS>(x, xs, keep, prev, jj));
+      } else {   // not a mean of the last cells and its sum not kept exactly: refit in fp64
+        lloyd4_rows64<NROWS>(x, xs, keep, iters, c16, code);
+        return;
+      }
+    }
+    cf[jj] = f16_bits_to_f32(c16[jj]);
+    cmax = fmaxf(cmax, fabsf(cf[jj]));
+  }
+  // final codes: each |x - c16_j| is one rounded binary32 subtraction
+  const bool cfx[4] = {true, true, true, true};
   for (int r = 0; r < NROWS; ++r)
-    if (keep >> r & 1u) code[r >> 4] |= (uint32_t)nearest4(x[r * xs], cf) << (2 * (r & 15));
+    if (keep >> r & 1u) {
+      const float v = x[r * xs];
+      const float ef = flat ? -1.f : 4.f * kU * (fabsf(v) + cmax);
+      bool ok = true;
+      uint32_t q = (uint32_t)nearest4_sure(v, cf, ef, ok);
+      if (!ok && !distances_exact(v, cf, cfx)) q = (uint32_t)nearest4_64(v, cf);
+      code[r >> 4] |= q << (2 * (r & 15));
+    }
 }
 
 // Element (t, c) held by fragment (lane, step, slot) -- the inverse of frag_pos.
@@ -324,7 +749,7 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int 
   const bool act = t >= lo && t < hi;
   const float* xg = xs[act ? t : lo] + (32 + GP) * g;
   uint8_t mask[32];
-  outlier_mask(xg, 32, 1, (float)sigma, kmax_outliers(32), mask, 1);
+  outlier_mask(xg, 32, 1, sigma, kmax_outliers(32), mask, 1);
   bool have = false;
   float mn = 0.f, mx = 0.f;
   for (int i = 0; i < 32; ++i) {
@@ -334,7 +759,7 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int 
     if (!have || v > mx) mx = v;
     have = true;
   }
-  const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 15.0f)) : 0;
+  const uint16_t S16 = have ? f16_of_range(mx, mn, 15.0f) : 0;
   const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
   const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
   int cnt = 0;
@@ -345,9 +770,7 @@ __device__ void quantize_tokens_int4(const float (*xs)[XS], int t0, int lo, int 
     if (mask[i]) {
       ++cnt;
     } else if (S != 0.f) {
-      float r = rintf(__fdiv_rn(xg[i] - m, S));
-      r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
-      q = (uint32_t)r;
+      q = affine_code(xg[i], m, S, 15.f);
     }
     nb[i >> 3] |= q << (4 * (i & 7));
   }
@@ -393,12 +816,12 @@ __device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int lo, int 
   const float* x = xs[act ? t : lo] + 16 * g + GP * (g >> 1);
   float amax = 0.f;
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const uint8_t s8 = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+  const uint8_t s8 = e4m3_of_quotient(amax, 6.0f);
   const float sc = e4m3_to_f32(s8);
   uint32_t nb[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    nb[i >> 3] |= (uint32_t)(sc != 0.f ? f32_to_e2m1(__fdiv_rn(x[i], sc)) : 0) << (4 * (i & 7));
+    nb[i >> 3] |= (uint32_t)(sc != 0.f ? e2m1_of_quotient(x[i], sc) : 0) << (4 * (i & 7));
   store_codes<16>(blk, role, NS, t, 16 * g, lo, hi, nb, NS);
   if (act) blk[e2m1_sc_off(D) + 16 * g + t] = s8;
 }
@@ -680,7 +1103,7 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
     for (int i = tid; i < 16 * D; i += g.n) {
       const int t = i / D, c = i - t * D;
       const FragPos p = frag_pos(role, t, c);
-      blk[8 * NS * p.lane + 8 * p.step + p.slot] = s != 0.f ? f32_to_e4m3(__fdiv_rn(xs[t][c], s)) : 0;
+      blk[8 * NS * p.lane + 8 * p.step + p.slot] = s != 0.f ? e4m3_of_quotient(xs[t][c], s) : 0;
     }
     if (tid == 0) *reinterpret_cast<float*>(blk + fp8_sc_off(D)) = s;
   } else if (stat) {
@@ -723,7 +1146,7 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
       for (int i = tid; i < 16 * D; i += g.n)
         mask[i / D][i % D] = (uint8_t)((rbits[(i / D) * (D / 32) + (i % D) / 32] >> (i % 32)) & 1u);
     } else if (tid < 16) {
-      outlier_mask(&xs[tid][0], D, 1, (float)a.sigma, kmax_outliers(D), &mask[tid][0], 1);
+      outlier_mask(&xs[tid][0], D, 1, a.sigma, kmax_outliers(D), &mask[tid][0], 1);
     }
     g.sync();
     if (tid < D && a3) {
@@ -737,16 +1160,12 @@ __device__ void page_quantize(const AppendArgs& a, int h, int role, uint32_t u, 
         if (!have || v > mx) mx = v;
         have = true;
       }
-      const uint16_t S16 = have ? f32_to_f16_bits(__fdiv_rn(mx - mn, 7.0f)) : 0;
+      const uint16_t S16 = have ? f16_of_range(mx, mn, 7.0f) : 0;
       const uint16_t m16 = have ? f32_to_f16_bits(mn) : 0;
       const float S = f16_bits_to_f32(S16), m = f16_bits_to_f32(m16);
       for (int t = 0; t < 16; ++t) {
         uint8_t q = 0;
-        if (!mask[t][c] && S != 0.f) {
-          float r = rintf(__fdiv_rn(xs[t][c] - m, S));
-          r = fminf(fmaxf(r, 0.f), 7.f);
-          q = (uint8_t)r;
-        }
+        if (!mask[t][c] && S != 0.f) q = (uint8_t)affine_code(xs[t][c], m, S, 7.f);
         codes[t][c] = q;
       }
       const int r = a3_rho(role, c);
@@ -905,7 +1324,7 @@ __device__ void group_quantize(const AppendArgs& a, int h, int role, const int32
     reinterpret_cast<uint4*>(blk)[i] = make_uint4(0, 0, 0, 0);
   g.sync();   // also orders the caller's writes of xs before the reads below
   if (!have_bits) {
-    if (tid < GT) outlier_bits<D>(&xs[tid][0], (float)a.sigma, kmax_outliers(D), ws.rbits + tid * NWD);
+    if (tid < GT) outlier_bits<D>(&xs[tid][0], a.sigma, kmax_outliers(D), ws.rbits + tid * NWD);
     g.sync();
   }
   if (tid < D) {
@@ -1315,7 +1734,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
       // per-token outlier decisions of every row at once (one thread per row)
       const bool pre_bits = KIND >= kProjPage && a.fmt != KVQ_FMT_CB2_STATIC;
       if (pre_bits) {
-        for (int r = tid; r < kPM; r += kPThreads) outlier_bits<D>(xs[r], (float)a.sigma, kmax_outliers(D), rbits + r * (D / 32));
+        for (int r = tid; r < kPM; r += kPThreads) outlier_bits<D>(xs[r], a.sigma, kmax_outliers(D), rbits + r * (D / 32));
         __syncthreads();
       }
       for (int s = grp; s < SPT; s += NB) {
