@@ -93,7 +93,7 @@ typedef enum {
     /* [P3] "Sub-Byte KV-Cache Quantization": asymmetric 3-bit codes with
      * dynamic outlier preservation.  Per (page, channel) over its
      * non-outliers: S = fp16((max - min)/7), m = fp16(min), q =
-     * clamp(rint((x - m)/S), 0, 7) (binary32); a code stands for
+     * clamp(rint((x - m)/S), 0, 7) (fp64); a code stands for
      * fp16(q*S + m).  Outliers as KVQ_FMT_CB2_OUTLIER (sigma rule per token,
      * e4m3 side-list).  Quantized when a page fills; the partial last page
      * waits in fp32 staging. */
@@ -180,10 +180,14 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* ti
  * Tokens land at positions seq_lens[b] .. ; per-token formats quantize each
  * token in place; page formats write fp32 staging and quantize each page that
  * fills (FP8 when its page-table entry carries the tier bit).  seq_lens is
- * advanced on the device.  Quantization is deterministic and bit-identical to
- * the CPU reference (fp64 statistics, fixed reduction order, no fused
- * multiply-add).  Sequences that would overflow their page table or name a bad
- * page are skipped and flagged in the status word. */
+ * advanced on the device.  The quantizer is defined in fp64 (outlier
+ * statistics, the Lloyd-Max fit, scales and codes; ascending-index sums; each
+ * result rounded once to its stored format) and the cache is bit-identical to
+ * that definition: decisions are taken in binary32 with a certified error
+ * bound, and a unit whose decision the bound does not settle (a value within
+ * rounding of a threshold or a midpoint) is recomputed in fp64.  Sequences
+ * that would overflow their page table or name a bad page are skipped and
+ * flagged in the status word. */
 kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, const void* k_new,
                                const void* v_new, kvq_dtype in_dtype, int32_t t_new,
                                const int32_t* t_per_seq, void* stream);
@@ -229,7 +233,9 @@ kvq_status kvq_decode_num_splits(const kvq_config* cfg, int32_t num_q_heads, int
  * cache; [P3] "Sub-Byte Dequantization on the Fly" in tensor-core fragment
  * registers).  One query token per sequence, grouped-query attention:
  *   q       device bf16 [num_seqs][num_q_heads][D]; query head h reads kv head
- *           h / (num_q_heads / Hkv).
+ *           h / (num_q_heads / Hkv).  Any finite bf16 value: each head is
+ *           scaled by a power of two into fp16 range for the tensor cores and
+ *           the scale is undone in its scores.
  *   out     device [num_seqs][num_q_heads][D] in out_dtype (bf16 or f32):
  *           softmax(softmax_scale * q K^T) V over the seq_lens[b] cached tokens
  *           (0 for an empty sequence).
@@ -284,10 +290,12 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
  *     make that first call before any stream capture.
  *   - Every call on a device shares the one scratch, which keeps the last
  *     call's contents; calls that may overlap on the GPU (different streams)
- *     race on it -- serialise them.  The scratch starts zeroed, and its
- *     arrival counters return to zero after every call (a call that sets
- *     KVQ_STATUS_TIMEOUT may leave them set; this entry point offers no way
- *     to clear them, so treat that status as fatal for it). */
+ *     race on it -- serialise them.  Each call first clears its own arrival
+ *     counters with a memset on `stream` (their place in the scratch depends
+ *     on the call's shape), then launches the decode; the partials need no
+ *     initialisation.
+ *   - The looked-up address is kept per device ordinal for the life of the
+ *     process: do not use this call on a device after cudaDeviceReset. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q,
                                         int32_t num_q_heads, float softmax_scale, int32_t max_seq_len,

@@ -568,6 +568,7 @@ __device__ __forceinline__ void mask_v_tokens(uint32_t (&a)[4], int ntok, int q4
 
 template <int D, int NT>
 struct WarpState {
+  float scl[NT][2];         // score scale of heads nt*8+2q, +1: softmax scale * log2(e) * 2^k_h
   float o[NT][D / 16][4];   // O^T accumulators: rows channel 16s+g (+8), cols head nt*8+2q (+1)
   float m[NT][2];           // running max (log2 units) of heads nt*8+2q, +1
   float l[NT][2];           // per-lane partial softmax sums
@@ -610,9 +611,12 @@ __device__ __forceinline__ void load_codes(uint32_t blk_s, int lane, uint32_t (&
   }
 }
 
+// Scores (in the scaled query's units) -> probabilities: each head's score
+// scale st.scl undoes its query scale 2^-k_h and applies softmax_scale *
+// log2(e); then the online softmax and the P^T fragments.
 template <int D, int NT, int PPI>
 __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)[PPI][NT][4], const int (&ntok)[PPI],
-                                              float scale, const WarpSmem& sm, int lane, bool corr,
+                                              float /*scale: in st.scl*/, const WarpSmem& sm, int lane, bool corr,
                                               uint32_t (&phi)[PPI][NT][2], uint32_t (&plo)[PPI][NT][2]) {
   const int g = lane >> 2, q4 = lane & 3;
 #pragma unroll
@@ -620,7 +624,7 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[p][nt][r] *= scale;
+      for (int r = 0; r < 4; ++r) acc[p][nt][r] *= st.scl[nt][r & 1];
   float alpha[NT][2];
   const bool rescale = online_softmax<PPI, NT>(acc, ntok, g, st.m, st.l, alpha);
   if (rescale) {
@@ -1177,12 +1181,41 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   const int win_spec = spec_page < min(p0 + a.pps, a.ppsm) ? pt[spec_page] : 0;
 
   // query of the CTA's G heads: fp32 in shared memory as [D][GS] (outlier
-  // corrections gather its columns), fp16 B fragments in registers
+  // corrections gather its columns), fp16 B fragments in registers.  Each
+  // head is scaled by a power of two 2^-k_h that puts its largest component
+  // in [2^14, 2^15), so every bf16 value in range reaches the fp16 tensor-core
+  // operand without overflow and, down to 2^-28 of the head's largest, without
+  // loss; 2^k_h goes into that head's score scale (a power-of-two scaling
+  // commutes exactly with the products and fp32 sums).
+  // the per-head scales live in warp 0's probability scratch, which the
+  // page loop first writes after the barrier that follows their last read
+  float* const qscale = sm.psm - w * (align16(warp_smem_bytes<FMT, D>(GS)) / 4);
   const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
   for (int i = threadIdx.x; i < GS * D; i += W * 32) {
     const int h = i / D, c = i % D;   // D is a power of two
     qsm[c * GS + h] = h < G ? __bfloat162float(qg[i]) : 0.f;
   }
+  __syncthreads();
+  for (int h = w; h < GS; h += W) {
+    float mx = 0.f;
+    for (int c = lane; c < D; c += 32) mx = fmaxf(mx, fabsf(qsm[c * GS + h]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int e = 0;
+    frexpf(mx, &e);                             // mx in [2^(e-1), 2^e)
+    const int k = mx > 0.f ? min(max(e - 15, -100), 100) : 0;
+    if (lane == 0) qscale[h] = ldexpf(1.f, -k);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < GS * D; i += W * 32) qsm[i] *= qscale[i % GS];
+  float scl[NT][2];   // score scale of heads nt*8+2q, +1 (read now: the scales' area is reused)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = nt * 8 + 2 * q4 + j;
+      scl[nt][j] = h < G ? __fdiv_rn(a.scale_log2, qscale[h]) : a.scale_log2;   // exact: a power of two
+    }
   for (int i = threadIdx.x; i < zero_block_bytes<FMT, D>() / 16; i += W * 32)
     reinterpret_cast<uint4*>(zb)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (has_ds<FMT>())
@@ -1318,25 +1351,27 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
 #pragma unroll 1
   for (int it = 0; it < NV; ++it) issue_v(it);
 
+  __syncthreads();   // the scaled query
   uint32_t qf[NT][NS][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h = nt * 8 + g;
-    const __nv_bfloat16* qh = qg + (size_t)h * D + 2 * q4;
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
       const bool on = h < G;
-      const float x0 = on ? __bfloat162float(qh[16 * s]) : 0.f, x1 = on ? __bfloat162float(qh[16 * s + 1]) : 0.f;
-      const float x8 = on ? __bfloat162float(qh[16 * s + 8]) : 0.f, x9 = on ? __bfloat162float(qh[16 * s + 9]) : 0.f;
+      const int c = 16 * s + 2 * q4;
+      const float x0 = on ? qsm[c * GS + h] : 0.f, x1 = on ? qsm[(c + 1) * GS + h] : 0.f;
+      const float x8 = on ? qsm[(c + 8) * GS + h] : 0.f, x9 = on ? qsm[(c + 9) * GS + h] : 0.f;
       qf[nt][s][0] = h2_as_u32(__floats2half2_rn(x0, x1));
       qf[nt][s][1] = h2_as_u32(__floats2half2_rn(x8, x9));
     }
   }
-  __syncthreads();
 
   WarpState<D, NT> st;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    st.scl[nt][0] = scl[nt][0];
+    st.scl[nt][1] = scl[nt][1];
 #pragma unroll
     for (int s = 0; s < NS; ++s) st.o[nt][s][0] = st.o[nt][s][1] = st.o[nt][s][2] = st.o[nt][s][3] = 0.f;
     st.m[nt][0] = st.m[nt][1] = -INFINITY;
@@ -1352,9 +1387,8 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     for (int nt = 0; nt < NT; ++nt) {
       const int h = nt * 8 + g;
       const bool on = h < G;
-      const float qa = (on && ia < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia] & (D - 1))]) : 0.f;
-      const float qb =
-          (on && ia + 1 < a.n_static) ? __bfloat162float(qg[(size_t)h * D + (mk[ia + 1] & (D - 1))]) : 0.f;
+      const float qa = (on && ia < a.n_static) ? qsm[(mk[ia] & (D - 1)) * GS + h] : 0.f;
+      const float qb = (on && ia + 1 < a.n_static) ? qsm[(mk[ia + 1] & (D - 1)) * GS + h] : 0.f;
       st.qs[nt] = h2_as_u32(__floats2half2_rn(qa, qb));
     }
     vch = g < a.n_static ? (mk[a.n_static + g] & (D - 1)) : 0;

@@ -257,3 +257,33 @@ def test_workspace_and_argument_errors():
     with pytest.raises(kvq.KVQError) as e:   # 3 query heads do not divide over 2 kv heads
         kvq.kvq_decode_attention(pair.gpu, torch.zeros((1, 3, 128), dtype=torch.bfloat16, device="cuda"), 0.1, 32)
     assert e.value.status == kvq.KVQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt,D", [(CB2, 128), (TIERED, 128), (E2M1, 128), (INT4, 64), (CB2S, 128), (A3, 64),
+                                   (CB2G, 128)])
+def test_decode_query_of_extreme_magnitude(fmt, D):
+    """Query heads far outside fp16's comfortable range: components near 1e5
+    (above fp16's 65504), heads whose largest component is 1e-6 (below fp16's
+    normal range), and a head mixing both scales.  Each head's query is
+    brought into fp16 range by a power of two folded into its score scale,
+    so the result stays within the attention tolerance of the fp64 oracle."""
+    B, Hkv, G, P = 2, 2, 8, 10
+    pair = Pair(fmt, B, Hkv, D, P, seed=31, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(31, B, 150, Hkv, D, *_dist(fmt))
+    pair.append(k, v, t_per_seq=[150, 97])
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((B, Hkv * G, D))
+    q[:, 0] *= 1e5 / 4            # components up to ~1e5
+    q[:, 1] *= 1e-6               # tiny head
+    q[:, 2, :4] = [3e4, -5e4, 2e-7, 1.0]
+    q[:, 3] *= 3e-5 / 4
+    q[:, 9] = 0.0                 # an all-zero head: uniform attention
+    qt = torch.from_numpy(q).float().to(torch.bfloat16)
+    qbits = qt.view(torch.int16).numpy().view(np.uint16)
+    for od in (torch.float32, torch.bfloat16):
+        out = kvq.kvq_decode_attention(pair.gpu, qt.cuda(), D ** -0.5, 150, 3, out_dtype=od)
+        torch.cuda.synchronize()
+        exp = pair.ref.decode(qbits, D ** -0.5)
+        got = out.float().cpu().numpy()
+        assert np.isfinite(got).all()
+        assert_attention_close(got, exp, od)
