@@ -492,11 +492,18 @@ __device__ __noinline__ int nearest4_by64(float v, const float* c, float E, floa
   }
   return best;
 }
-// The mean of the rows of `keep` whose code in `asg` is j, from a compensated
-// (TwoSum) binary32 sum: within 4 u |mean| + 4 n^2 u^2 max|value| of the
-// exact mean, and so of its fp64 value.  Returns the mean and its bound.
+// fp16 bits of the mean of the rows of `keep` whose code in `asg` is j, when
+// a compensated (TwoSum) binary32 evaluation settles its rounding; 0xFFFF
+// (a NaN pattern no mean produces here) when it does not.  The sum is kept
+// as hi + lo (within n^2 u^2 max|value| of the exact sum), the mean as q1 +
+// d with q1 = hi / n and d = (hi - q1 n + lo) / n (the first residual exact),
+// so q1 + d is within 4 u |d| + 4 n u^2 max|value| of the exact mean, which
+// is far closer to it than to any fp16 rounding boundary except in an exact
+// tie; the side of the boundary is the sign of (q1 - b) + d, whose first
+// difference is exact (q1 and b are close).  The fp64 mean lies as close.
 template <int NROWS>
-__device__ __noinline__ float2 cell_mean_tight(const float* x, int xs, uint64_t keep, const uint32_t* asg, int j) {
+__device__ __noinline__ uint16_t cell_mean_f16_tight(const float* x, int xs, uint64_t keep, const uint32_t* asg,
+                                                     int j) {
   float hi = 0.f, lo = 0.f, m = 0.f;
   int n = 0;
   for (int r = 0; r < NROWS; ++r)
@@ -510,87 +517,187 @@ __device__ __noinline__ float2 cell_mean_tight(const float* x, int xs, uint64_t 
     }
   const float fn = (float)n;
   const float q1 = __fdiv_rn(hi, fn);
-  const float r1 = __fmaf_rn(-q1, fn, hi);   // exact
-  const float mean = q1 + __fdiv_rn(r1 + lo, fn);
-  return make_float2(mean, 4.f * kU * fabsf(mean) + 4.f * fn * fn * kU * kU * m);
+  const float d = __fdiv_rn(__fmaf_rn(-q1, fn, hi) + lo, fn);
+  const float mean = q1 + d;
+  const float tol = 4.f * kU * fabsf(d) + 4.f * fn * kU * kU * m;
+  const float e = kU * fabsf(mean) + tol;
+  const uint16_t h = f32_to_f16_bits(mean);
+  const uint16_t lo16 = f32_to_f16_bits(mean - e), hi16 = f32_to_f16_bits(mean + e);
+  if (lo16 == h && hi16 == h) return h;
+  const float vl = f16_bits_to_f32(lo16), vh = f16_bits_to_f32(hi16);
+  if (!isfinite(vl) || !isfinite(vh)) return 0xFFFFu;
+  // one fp16 boundary b inside [mean - e, mean + e]: which side is the mean on?
+  const float b = (vl + vh) * 0.5f;
+  if (f32_to_f16_bits(b) != lo16 && f32_to_f16_bits(b) != hi16) return 0xFFFFu;   // not adjacent
+  const float t = (q1 - b) + d;
+  if (t > tol) return hi16;
+  if (t < -tol) return lo16;
+  return 0xFFFFu;
+}
+
+// Final codes of the rows of `rows` that the midpoint count did not settle:
+// nearest fp16 centroid by a distance margin, exact distances, else fp64.
+// (Rare; out of line so that it takes no registers from the fit's loop.)
+template <int NROWS>
+__device__ __noinline__ void lloyd_fix_codes(const float* x, int xs, uint64_t rows, const float* cf, bool flat,
+                                             float cmax, uint32_t* code) {
+  const bool cfx[4] = {true, true, true, true};
+  for (int r = 0; r < NROWS; ++r) {
+    if (!(rows >> r & 1u)) continue;
+    const float v = x[r * xs];
+    const float ef = flat ? -1.f : 4.f * kU * (fabsf(v) + cmax);
+    bool ok = true;
+    uint32_t q = (uint32_t)nearest4_sure(v, cf, ef, ok);
+    if (!ok && !distances_exact(v, cf, cfx)) q = (uint32_t)nearest4_64(v, cf);
+    code[r >> 4] = (code[r >> 4] & ~(3u << (2 * (r & 15)))) | (q << (2 * (r & 15)));
+  }
+}
+
+// State of one channel's binary32 fit that the rare paths need: the values'
+// range, the bound E, and per centroid its source (a linspace point, or the
+// binary32 sum and count of the cell it was last the mean of).
+struct LloydState {
+  float c[4];
+  float sumc[4];
+  int cntc[4];
+  bool lin[4];
+  float mn, mx, amax, E;
+  int sums_exact;   // -1: not yet known; else whether every partial sum of the values is exact
+};
+
+// Whether every partial sum of at most NROWS of the kept values is exact in
+// binary32 (and so in fp64): they are multiples of 2^elo (the lowest set bit
+// of any value) below NROWS * max|x|, so exact if that spans at most 24 bits.
+template <int NROWS>
+__device__ __noinline__ bool sums_exact_of(const float* x, int xs, uint64_t keep, float amax) {
+  if (amax == 0.f) return true;
+  int elo = 1000;
+  for (int r = 0; r < NROWS; ++r)
+    if (keep >> r & 1u) {
+      const float v = x[r * xs];
+      if (v != 0.f) elo = min(elo, low_bit_exp(v));
+    }
+  int eh = 0;
+  frexpf(amax * (float)NROWS, &eh);
+  return eh - elo <= 24;
+}
+// Whether centroid j is exactly its fp64 value.
+template <int NROWS>
+__device__ __forceinline__ bool centroid_exact(LloydState& S, const float* x, int xs, uint64_t keep, int j) {
+  if (S.lin[j]) return j == 0 || j == 3 || S.mn == S.mx;
+  if (S.sums_exact < 0) S.sums_exact = sums_exact_of<NROWS>(x, xs, keep, S.amax);
+  return S.sums_exact && quotient_exact(S.c[j], S.sumc[j], (float)S.cntc[j]);
+}
+
+// The rows of `rows` whose binary32 assignment was not certified by the
+// midpoint margin (all kept rows when the centroids are not strictly
+// sorted), assigned again: by distances with a margin, by exact distances,
+// else in fp64 from the centroids' fp64 values (needs exact sums; otherwise
+// the fit is marked unsure).  Rebuilds the assignment words and the four
+// sums and counts in row order.  Returns false when a row is left unsure.
+// (Rare; out of line like lloyd_fix_codes.)
+template <int NROWS>
+__device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int xs, uint64_t keep, uint64_t rows,
+                                            uint32_t* a, float* sum, int* cnt) {
+  constexpr int NW = (NROWS + 15) / 16;
+  bool cx[4];
+  for (int j = 0; j < 4; ++j) cx[j] = centroid_exact<NROWS>(S, x, xs, keep, j);
+  bool sure = true;
+  for (int r = 0; r < NROWS; ++r) {
+    if (!(rows >> r & 1u)) continue;
+    const float v = x[r * xs];
+    bool ok = true;
+    uint32_t j = (uint32_t)nearest4_sure(v, S.c, S.E, ok);
+    if (!ok && !distances_exact(v, S.c, cx)) {
+      if (S.sums_exact < 0) S.sums_exact = sums_exact_of<NROWS>(x, xs, keep, S.amax);
+      if (S.sums_exact) j = (uint32_t)nearest4_by64(v, S.c, S.E, S.mn, S.mx, S.lin, S.sumc, S.cntc);
+      else sure = false;
+    }
+    a[r >> 4] = (a[r >> 4] & ~(3u << (2 * (r & 15)))) | (j << (2 * (r & 15)));
+  }
+  for (int jj = 0; jj < 4; ++jj) { sum[jj] = 0.f; cnt[jj] = 0; }
+  for (int r = 0; r < NROWS; ++r)
+    if (keep >> r & 1u) {
+      const uint32_t j = (a[r >> 4] >> (2 * (r & 15))) & 3u;
+      sum[j] += x[r * xs];
+      ++cnt[j];
+    }
+  (void)NW;
+  return sure;
 }
 
 // The same fit, run in binary32 with a bound: while the assignments agree, a
 // centroid is the mean of the same values in either precision, and a binary32
-// mean of cnt values lies within cnt u max|value| of the fp64 one (a sum of
-// cnt terms, then one division); the linspace points lie within 4 u max|x|.
-// So every assignment whose runner-up is farther by more than E = 2 (NROWS +
-// 4) u max|x| is the fp64 one; so is one whose four distances are exact
-// (exact centroids -- exact sums, by the span of the values' bits, and exact
-// quotients -- and exact subtractions).  Any other assignment is taken again
-// in fp64 from the centroids' fp64 values (their sums are exact when the
-// values' bits span at most 24 bits; otherwise the channel is refitted by
-// lloyd4_rows64).  The fp16 rounding of each final centroid is checked over
-// +-2 (cnt + 2) u max|member| around it, then from a compensated mean, then
-// done in fp64.  Each final code is checked by its own margin, 4 u (|x| +
-// max|centroid|) (one rounded subtraction per distance), else by exact
-// distances, else taken with fp64 distances.  Values are read from shared
-// memory on every pass; assignments are packed 16 to a word, so the fit holds
-// few registers.
+// mean of cnt values lies within cnt u max|x| of the fp64 one (a sum of cnt
+// terms, then one division); the linspace points lie within 4 u max|x|.
+// Centroids stay sorted (the linspace start is, and the means of cells cut at
+// midpoints keep the order; an empty cell's centroid lies between its
+// neighbours' cells).  With strictly sorted centroids the nearest one (lowest
+// index on ties) is the number of midpoints (c_j + c_j+1) / 2 a value
+// exceeds, and a value farther than E = 2 (NROWS + 4) u max|x| from every
+// binary32 midpoint is assigned as fp64 would.  The other rows (all rows if
+// the centroids are not strictly sorted) are assigned again out of line
+// (lloyd_fix_rows); a row that neither a margin, exact distances nor fp64
+// centroids settle sends the channel to lloyd4_rows64.  The fp16 rounding of
+// each final centroid is checked over +-2 (cnt + 2) u max|x| around it, then
+// from a compensated mean of its cell, then done in fp64.  Each final code
+// counts the exact midpoints of the sorted fp16 centroids it exceeds (one
+// fp64 comparison where it lies within 2^-45 of one), or, unsorted, is taken
+// like an assignment.  Values are read from shared memory on every pass;
+// assignments are packed 16 to a word, so the fit holds few registers.
 template <int NROWS>
-__device__ __noinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
-                                         uint32_t (&code)[(NROWS + 15) / 16]) {
+__device__ __forceinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, int iters, uint16_t* c16,
+                                            uint32_t (&code)[(NROWS + 15) / 16]) {
   constexpr int NW = (NROWS + 15) / 16;
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
-  bool cx[4] = {true, true, true, true};       // centroid j is exactly its fp64 value
-  bool lin[4] = {false, false, false, false};  // centroid j is still its linspace point
-  float sumc[4] = {0.f, 0.f, 0.f, 0.f};        // the sum and count centroid j was last formed from
-  int cntc[4] = {1, 1, 1, 1};
+  LloydState S;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { S.c[j] = 0.f; S.sumc[j] = 0.f; S.cntc[j] = 1; S.lin[j] = false; }
+  S.mn = S.mx = S.amax = S.E = 0.f;
+  S.sums_exact = -1;
+  bool last[4] = {false, false, false, false};   // centroid j was formed in the last update
 #pragma unroll
   for (int w = 0; w < NW; ++w) code[w] = 0u;
-  bool sure = true, flat = false, sums_exact = false;
-  float E = 0.f, mn = 0.f, mx = 0.f;
+  bool sure = true, flat = false;
   uint32_t prev[NW];
   bool have_prev = false;
   if (keep) {
     bool have = false;
-    int elo = 1000;
+    float mn = 0.f, mx = 0.f;
     for (int r = 0; r < NROWS; ++r) {
       if (!(keep >> r & 1u)) continue;
       const float v = x[r * xs];
       if (!have) { mn = v; mx = v; have = true; }
       mn = v < mn ? v : mn;
       mx = v > mx ? v : mx;
-      if (v != 0.f) elo = min(elo, low_bit_exp(v));
     }
-    const float amax = fmaxf(fabsf(mn), fabsf(mx));
-    // every partial sum of at most NROWS of these values is a multiple of
-    // 2^elo below NROWS * amax: exact in binary32 (and fp64) if that spans
-    // at most 24 bits
-    int eh = 0;
-    frexpf(amax * (float)NROWS, &eh);
-    sums_exact = amax == 0.f || eh - elo <= 24;
+    S.mn = mn;
+    S.mx = mx;
+    S.amax = fmaxf(fabsf(mn), fabsf(mx));
     // one value repeated: all centroids equal it in either precision and
     // every assignment is centroid 0; no margin to check
     flat = mn == mx;
-    E = flat ? -1.f : 2.f * (float)(NROWS + 4) * kU * amax;
+    S.E = flat ? -1.f : 2.f * (float)(NROWS + 4) * kU * S.amax;
     const float h = __fdiv_rn(mx - mn, 3.0f);
-    c[0] = mn; c[1] = mn + h; c[2] = mn + 2.0f * h; c[3] = mx;
-    cx[1] = cx[2] = flat;   // linspace interior points: exact only when h = 0
-    lin[0] = lin[1] = lin[2] = lin[3] = true;
+    S.c[0] = mn; S.c[1] = mn + h; S.c[2] = mn + 2.0f * h; S.c[3] = mx;
+    S.lin[0] = S.lin[1] = S.lin[2] = S.lin[3] = true;
     for (int it = 0; it < iters; ++it) {
       // one pass assigns every value and sums each centroid's members in row
       // order (four independent sums: adding +0.0 to the others changes none
       // of them, a sum that starts at +0.0 never being -0.0)
+      const bool srt = S.c[0] < S.c[1] && S.c[1] < S.c[2] && S.c[2] < S.c[3];
+      const float m0 = (S.c[0] + S.c[1]) * 0.5f, m1 = (S.c[1] + S.c[2]) * 0.5f, m2 = (S.c[2] + S.c[3]) * 0.5f;
       uint32_t a[NW];
 #pragma unroll
       for (int w = 0; w < NW; ++w) a[w] = 0u;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
       int cnt[4] = {0, 0, 0, 0};
+      uint64_t unc = 0;
       for (int r = 0; r < NROWS; ++r) {
         if (!(keep >> r & 1u)) continue;
         const float v = x[r * xs];
-        bool ok = true;
-        uint32_t j = (uint32_t)nearest4_sure(v, c, E, ok);
-        if (!ok && !distances_exact(v, c, cx)) {
-          if (sums_exact) j = (uint32_t)nearest4_by64(v, c, E, mn, mx, lin, sumc, cntc);
-          else sure = false;
-        }
+        const uint32_t j = (uint32_t)(v > m0) + (uint32_t)(v > m1) + (uint32_t)(v > m2);
+        const float mg = fminf(fminf(fabsf(v - m0), fabsf(v - m1)), fabsf(v - m2));
+        unc |= (uint64_t)(!(mg > S.E)) << r;
         a[r >> 4] |= j << (2 * (r & 15));
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -598,20 +705,23 @@ __device__ __noinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, 
           cnt[jj] += j == (uint32_t)jj;
         }
       }
+      if (!srt) unc = keep;
+      if (unc) sure = lloyd_fix_rows<NROWS>(S, x, xs, keep, unc, a, sum, cnt) && sure;
       bool same = have_prev;
 #pragma unroll
       for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];
       if (same) break;
       // centroid j = the mean of its values
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
+      for (int jj = 0; jj < 4; ++jj) {
+        last[jj] = cnt[jj] > 0;
         if (cnt[jj] > 0) {
-          c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
-          cx[jj] = sums_exact && quotient_exact(c[jj], sum[jj], (float)cnt[jj]);
-          lin[jj] = false;
-          sumc[jj] = sum[jj];
-          cntc[jj] = cnt[jj];
+          S.c[jj] = __fdiv_rn(sum[jj], (float)cnt[jj]);
+          S.lin[jj] = false;
+          S.sumc[jj] = sum[jj];
+          S.cntc[jj] = cnt[jj];
         }
+      }
 #pragma unroll
       for (int w = 0; w < NW; ++w) prev[w] = a[w];
       have_prev = true;
@@ -621,43 +731,25 @@ __device__ __noinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, 
     lloyd4_rows64<NROWS>(x, xs, keep, iters, c16, code);
     return;
   }
-  // each centroid's own bound: its cell in the last update (prev), else the
-  // channel's bound (a linspace point, or a mean of an earlier cell)
-  float ec[4] = {E, E, E, E};
-  int ncell[4] = {0, 0, 0, 0};
-  if (have_prev && !flat) {
-    float mcell[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < NROWS; ++r) {
-      if (!(keep >> r & 1u)) continue;
-      const uint32_t j = (prev[r >> 4] >> (2 * (r & 15))) & 3u;
-      const float av = fabsf(x[r * xs]);
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        mcell[jj] = j == (uint32_t)jj ? fmaxf(mcell[jj], av) : mcell[jj];
-        ncell[jj] += j == (uint32_t)jj;
-      }
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-      if (ncell[jj] > 0) ec[jj] = 2.f * (float)(ncell[jj] + 2) * kU * mcell[jj];
-  }
-  float cf[4], cmax = 0.f;
+  float cf[4];
   for (int jj = 0; jj < 4; ++jj) {
-    c16[jj] = f32_to_f16_bits(c[jj]);
-    const float e = fmaxf(ec[jj], fabsf(c[jj]) * kNudge);
-    bool ok = cx[jj] || (f32_to_f16_bits(c[jj] - e) == c16[jj] && f32_to_f16_bits(c[jj] + e) == c16[jj]);
-    if (!ok && !lin[jj] && !sums_exact && ncell[jj] > 0) {   // a compensated mean of its cell
-      const float2 mb = cell_mean_tight<NROWS>(x, xs, keep, prev, jj);
-      const uint16_t hm = f32_to_f16_bits(mb.x);
-      if (f32_to_f16_bits(mb.x - mb.y) == hm && f32_to_f16_bits(mb.x + mb.y) == hm) {
+    c16[jj] = f32_to_f16_bits(S.c[jj]);
+    // a mean of cnt values: within cnt u max|x| (linspace points: 4 u max|x|)
+    const float ec = flat ? 0.f : 2.f * (float)((S.lin[jj] ? 2 : S.cntc[jj]) + 2) * kU * S.amax;
+    const float e = fmaxf(ec, fabsf(S.c[jj]) * kNudge);
+    bool ok = f32_to_f16_bits(S.c[jj] - e) == c16[jj] && f32_to_f16_bits(S.c[jj] + e) == c16[jj];
+    if (!ok) ok = centroid_exact<NROWS>(S, x, xs, keep, jj);
+    if (!ok && !S.lin[jj] && !S.sums_exact && last[jj]) {   // a compensated mean of its cell
+      const uint16_t hm = cell_mean_f16_tight<NROWS>(x, xs, keep, prev, jj);
+      if (hm != 0xFFFFu) {
         c16[jj] = hm;
         ok = true;
       }
     }
     if (!ok) {
-      if (lin[jj] || sums_exact) {
-        c16[jj] = f16_from_f64(centroid64(jj, mn, mx, lin[jj], sumc[jj], cntc[jj]));
-      } else if (ncell[jj] > 0) {
+      if (S.lin[jj] || S.sums_exact) {
+        c16[jj] = f16_from_f64(centroid64(jj, S.mn, S.mx, S.lin[jj], S.sumc[jj], S.cntc[jj]));
+      } else if (last[jj]) {
         c16[jj] = f16_from_f64(cell_mean64<NROWS>(x, xs, keep, prev, jj));
       } else {   // not a mean of the last cells and its sum not kept exactly: refit in fp64
         lloyd4_rows64<NROWS>(x, xs, keep, iters, c16, code);
@@ -665,19 +757,27 @@ __device__ __noinline__ void lloyd4_rows(const float* x, int xs, uint64_t keep, 
       }
     }
     cf[jj] = f16_bits_to_f32(c16[jj]);
-    cmax = fmaxf(cmax, fabsf(cf[jj]));
   }
-  // final codes: each |x - c16_j| is one rounded binary32 subtraction
-  const bool cfx[4] = {true, true, true, true};
+  // final codes: the midpoints of strictly sorted fp16 centroids are exact in
+  // binary32 when their sums are (checked); fp64 compares |x - c_j| exactly
+  // unless x lies within its rounding (2^-45 of |x| + max|c|) of a midpoint
+  const bool fsrt = cf[0] < cf[1] && cf[1] < cf[2] && cf[2] < cf[3];
+  const float s0 = cf[0] + cf[1], s1 = cf[1] + cf[2], s2 = cf[2] + cf[3];
+  const bool bex = fsrt && difference_exact(s0, cf[0], -cf[1]) && difference_exact(s1, cf[1], -cf[2]) &&
+                   difference_exact(s2, cf[2], -cf[3]);
+  const float b0 = s0 * 0.5f, b1 = s1 * 0.5f, b2 = s2 * 0.5f;
+  const float cmax = fmaxf(fmaxf(fabsf(cf[0]), fabsf(cf[1])), fmaxf(fabsf(cf[2]), fabsf(cf[3])));
+  uint64_t unc = 0;
   for (int r = 0; r < NROWS; ++r)
     if (keep >> r & 1u) {
       const float v = x[r * xs];
-      const float ef = flat ? -1.f : 4.f * kU * (fabsf(v) + cmax);
-      bool ok = true;
-      uint32_t q = (uint32_t)nearest4_sure(v, cf, ef, ok);
-      if (!ok && !distances_exact(v, cf, cfx)) q = (uint32_t)nearest4_64(v, cf);
+      const uint32_t q = (uint32_t)(v > b0) + (uint32_t)(v > b1) + (uint32_t)(v > b2);
+      const float mg = fminf(fminf(fabsf(v - b0), fabsf(v - b1)), fabsf(v - b2));
+      unc |= (uint64_t)(!(mg > 2.8421709e-14f * (fabsf(v) + cmax))) << r;   // 2^-45
       code[r >> 4] |= q << (2 * (r & 15));
     }
+  if (!bex) unc = keep;
+  if (unc) lloyd_fix_codes<NROWS>(x, xs, unc, cf, flat, cmax, code);
 }
 
 // Element (t, c) held by fragment (lane, step, slot) -- the inverse of frag_pos.
@@ -2059,8 +2159,11 @@ inline int cluster_for(int hidden) {
 
 // Launches with clusters of cs CTAs; with one_wave, only when every cluster
 // can be resident at once (else cudaErrorLaunchOutOfResources, nothing launched).
+// `enqueued` tells whether the projection kernel itself went onto the stream:
+// an error after that point must reach the caller, not start another launch.
 template <int KIND, int D, int R>
-cudaError_t launch_r(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
+cudaError_t launch_r(ProjArgs& p, int cs, bool one_wave, cudaStream_t st, bool& enqueued) {
+  enqueued = false;
   const int slice = p.hidden / cs;
   const size_t smem = (size_t)Plan<KIND, D, R>::smem(slice);
   auto kern = project_one_kernel<KIND, D, R>;
@@ -2086,6 +2189,7 @@ cudaError_t launch_r(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
     return cudaErrorLaunchOutOfResources;
   e = cudaLaunchKernelEx(&cfg, kern, p, slice);
   if (e != cudaSuccess) return e;
+  enqueued = true;
   append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
   return cudaGetLastError();
 }
@@ -2093,8 +2197,9 @@ cudaError_t launch_r(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
 // 16 sequences per cluster, or 32 (the weights streamed half as often) when
 // there are more than 16.
 template <int KIND, int D>
-cudaError_t launch(ProjArgs& p, int cs, bool one_wave, cudaStream_t st) {
-  return p.a.B > 16 ? launch_r<KIND, D, 32>(p, cs, one_wave, st) : launch_r<KIND, D, 16>(p, cs, one_wave, st);
+cudaError_t launch(ProjArgs& p, int cs, bool one_wave, cudaStream_t st, bool& enqueued) {
+  return p.a.B > 16 ? launch_r<KIND, D, 32>(p, cs, one_wave, st, enqueued)
+                    : launch_r<KIND, D, 16>(p, cs, one_wave, st, enqueued);
 }
 }  // namespace small
 
@@ -2135,8 +2240,9 @@ static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
     for (int pass = 0; pass < 2; ++pass)
       for (int cs = small::cluster_for(p.hidden); cs >= 1; cs >>= 1) {
         if (p.hidden % (32 * cs) || p.hidden / cs > small::kMaxSlice) break;
-        const cudaError_t e = small::launch<KIND, D>(p, cs, pass == 0, st);
-        if (e == cudaSuccess) return e;
+        bool enqueued = false;
+        const cudaError_t e = small::launch<KIND, D>(p, cs, pass == 0, st, enqueued);
+        if (e == cudaSuccess || enqueued) return e;   // once enqueued, never launch the projection again
         (void)cudaGetLastError();   // refused: a narrower cluster, else the tile kernel
       }
   }
