@@ -47,6 +47,8 @@ from sub_byte_quantized_kvq_gb300 import kvq, synth, workloads  # noqa: E402
 METRIC = "quantized-KV decode attention: achieved HBM GB/s vs peak; us per decode step"
 FMT_NAME = {0: "INT4_G32", 1: "FP4_E2M1_S16", 2: "CB2_OUTLIER", 3: "TIERED", 4: "CB2_STATIC", 5: "ASYM3_OUTLIER",
             6: "CB2_GROUP4"}
+DECODE_MATH = {"auto": kvq.KVQ_DECODE_AUTO, "tensor_cores": kvq.KVQ_DECODE_TENSOR_CORES,
+               "cuda_cores": kvq.KVQ_DECODE_CUDA_CORES}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 KERNEL_SOURCES = ["kvq_common.cuh", "kvq_decode.cuh", "kvq_internal.cuh"]
 
@@ -59,6 +61,9 @@ def parse_args():
     p.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     p.add_argument("--workload", default="tiered_32k", choices=sorted(synth.WORKLOADS))
     p.add_argument("--batch", type=int, default=0, help="override the workload's sequence count (profiling)")
+    p.add_argument("--q-heads", type=int, default=0, help="override the workload's query heads (GQA group size)")
+    p.add_argument("--decode-math", default="auto", choices=sorted(DECODE_MATH),
+                   help="tensor or CUDA cores for the dense products of the codebook pages")
     p.add_argument("--no-configs", action="store_true",
                    help="time only --workload (skip the other workloads carried under \"configs\")")
     p.add_argument("--seed", type=int, default=0)
@@ -469,10 +474,11 @@ def time_project(w: synth.Workload, dev, flush_mb: int, reps: int = 10, warmup: 
 CONFIG_WORKLOADS = ("cb2_4k", "fp4_32k", "longctx_128k")   # carried beside the headline workload
 
 
-def traffic_record(workload: str, batch: int):
+def traffic_record(workload: str, other_launch):
     """DRAM bytes per launch of decode_split_kernel for `workload` from the
     committed ncu record, or None when the record is for other kernel sources
-    (the kernel changed since the counters were taken) or another shape."""
+    (the kernel changed since the counters were taken) or the timed launch is
+    not the recorded one (`other_launch`: another shape or decode math)."""
     try:
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
@@ -481,7 +487,7 @@ def traffic_record(workload: str, batch: int):
     if tr.get("kernel_src_sha") != kernel_source_sha():
         return None
     rec = tr.get("workloads", {}).get(workload)
-    if rec is None or batch:
+    if rec is None or other_launch:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -490,6 +496,7 @@ def measure_workload(w: synth.Workload, args, world: int, rank: int, dev, peak: 
     """Build the workload's cache on the device, time its decode step, and
     return the timing with its roofline (the split kernel is the whole step)."""
     built = workloads.build(w, seed=args.seed + rank, device=dev)
+    built.cache.cfg.decode_math = DECODE_MATH[args.decode_math]
     torch.cuda.synchronize()
     t = time_gpu(built, args, world, dev)
     del built
@@ -501,7 +508,7 @@ def measure_workload(w: synth.Workload, args, world: int, rank: int, dev, peak: 
     achieved = nb["step"] / (t["step_ms"] * 1e-3) / 1e9
     t["roofline"] = {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic_record(w.name, args.batch),
+                     "traffic": traffic_record(w.name, args.batch or args.q_heads or args.decode_math != "auto"),
                      "algorithmic_bytes_per_launch": nb["step"], "us_per_launch": t["step_ms"] * 1e3,
                      "frac_of_nominal_8000_gbs": achieved / 8000.0}
     t["l2"] = ("flushed before every step (write 256 MB + read 256 MB)" if t["flushed"]
@@ -515,8 +522,12 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
+    if args.q_heads:
+        w = dataclasses.replace(w, Hq=args.q_heads)
     config = {"workload": w.name, "format": FMT_NAME[w.fmt], "B": w.B, "Hkv": w.Hkv, "Hq": w.Hq, "D": w.D,
               "context": w.N, "page_tokens": 16}
+    if args.decode_math != "auto":
+        config["decode_math"] = args.decode_math
 
     if args.impl == "reference":
         if rank != 0:
@@ -560,7 +571,7 @@ def main():
         "gpu_launches": args.steps,
         "clocks": t["clocks"],
     }
-    if not args.no_configs and not args.batch:
+    if not args.no_configs and not args.batch and not args.q_heads:
         configs = {}
         for name in CONFIG_WORKLOADS:
             if name == w.name:

@@ -110,6 +110,16 @@ typedef enum {
 
 typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
 
+/* Where decode runs the dense QK^T and PV products of the codebook pages.
+ * KVQ_DECODE_TENSOR_CORES: mma.sync tiles (the query heads of a kv head are
+ * the tile's N = 8 columns; G <= 4 leaves half of them empty).
+ * KVQ_DECODE_CUDA_CORES: fp32 FMAs on the dequantized values, only for
+ * KVQ_FMT_CB2_OUTLIER at G <= 4 (other formats and larger groups take the
+ * tensor cores whatever is asked).  KVQ_DECODE_AUTO picks the one measured
+ * faster for the format and group size.  Both give the same quantity within
+ * the decode tolerance (different rounding, not the same bits). */
+typedef enum { KVQ_DECODE_AUTO = 0, KVQ_DECODE_TENSOR_CORES = 1, KVQ_DECODE_CUDA_CORES = 2 } kvq_decode_math;
+
 #define KVQ_PAGE_TOKENS 16
 #define KVQ_TIER_BIT 0x80000000u
 
@@ -131,6 +141,7 @@ typedef struct {
     double sigma;               /* outlier threshold in standard deviations, >= 3 (3.0) */
     int32_t static_channels;    /* CB2_STATIC: fp16 channels per (kv head, K|V), 1..8
                                    (ceil(D / 100) for the pages' 1%); ignored otherwise */
+    int32_t decode_math;        /* kvq_decode_math (KVQ_DECODE_AUTO = 0) */
 } kvq_config;
 
 /* The cache.  All pointers are device memory owned by the caller.

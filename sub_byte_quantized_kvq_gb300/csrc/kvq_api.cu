@@ -181,6 +181,7 @@ static bool cfg_ok(const kvq_config* c) {
   if (c->num_tier_pages < 0 || (c->format != KVQ_FMT_TIERED && c->num_tier_pages != 0)) return false;
   if (!(c->sigma >= 3.0) || !std::isfinite(c->sigma)) return false;
   if (c->lloyd_iters < 1 || c->lloyd_iters > 64) return false;
+  if (c->decode_math < KVQ_DECODE_AUTO || c->decode_math > KVQ_DECODE_CUDA_CORES) return false;
   if (c->num_seqs > 65535 || c->num_kv_heads > 32767) return false;  // grid dimensions
   return true;
 }
@@ -216,10 +217,17 @@ static size_t arrivals_offset(const kvq_config* c, int num_q_heads, int S) {
   return (rows * c->head_dim * sizeof(float) + rows * sizeof(float2) + 15) / 16 * 16;
 }
 
+// The decode math a call runs: CUDA cores only where that path exists
+// (CB2, G <= 4); AUTO takes the tensor cores.
+static int decode_math(const kvq_config* c, int G) {
+  const bool cc_ok = c->format == KVQ_FMT_CB2_OUTLIER && G <= 4;
+  return cc_ok && c->decode_math == KVQ_DECODE_CUDA_CORES ? KVQ_DECODE_CUDA_CORES : KVQ_DECODE_TENSOR_CORES;
+}
+
 static int auto_splits(const kvq_config* c, int G, int max_seq_len) {
   const long long pages = (max_seq_len + kPage - 1) / kPage;
   const long long units = (long long)c->num_seqs * c->num_kv_heads;
-  const int per_sm = decode_ctas_per_sm(c->format, c->head_dim, G);
+  const int per_sm = decode_ctas_per_sm(c->format, c->head_dim, G, decode_math(c, G));
   const long long slots = (long long)num_sms() * (per_sm > 0 ? per_sm : 1);
   long long smax = pages / (2 * kWarpsPerCta);
   if (smax < 1) smax = 1;
@@ -397,6 +405,7 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.arrivals = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + arrivals_offset(cfg, num_q_heads, S));
   a.static_mask = cache->static_mask;
   a.n_static = cfg->format == KVQ_FMT_CB2_STATIC ? cfg->static_channels : 0;
+  a.math = decode_math(cfg, G);
   return KVQ_OK;
 }
 }  // namespace kvq

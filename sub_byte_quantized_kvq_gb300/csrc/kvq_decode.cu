@@ -17,11 +17,11 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __rest
 }
 
 // ----------------------------------------------------------------------------- host side
-static KernelInfo pick_kernel(int fmt, int D, int G) {
+static KernelInfo pick_kernel(int fmt, int D, int G, int math) {
   switch (fmt) {
     case KVQ_FMT_INT4_G32: return decode_kernel_int4(D, G);
     case KVQ_FMT_FP4_E2M1_S16: return decode_kernel_e2m1(D, G);
-    case KVQ_FMT_CB2_OUTLIER: return decode_kernel_cb2(D, G);
+    case KVQ_FMT_CB2_OUTLIER: return decode_kernel_cb2(D, G, math == KVQ_DECODE_CUDA_CORES);
     case KVQ_FMT_CB2_STATIC: return decode_kernel_cb2s(D, G);
     case KVQ_FMT_ASYM3_OUTLIER: return decode_kernel_a3(D, G);
     case KVQ_FMT_CB2_GROUP4: return decode_kernel_cb2g(D, G);
@@ -83,13 +83,13 @@ const Prepared* prepare(const KernelInfo& k) {
 }  // namespace
 
 // CTAs of the split kernel that fit on one SM (0 if the kernel cannot run).
-int decode_ctas_per_sm(int fmt, int D, int G) {
-  const Prepared* p = prepare(pick_kernel(fmt, D, G));
+int decode_ctas_per_sm(int fmt, int D, int G, int math) {
+  const Prepared* p = prepare(pick_kernel(fmt, D, G, math));
   return p ? p->ctas_per_sm : 0;
 }
 
 cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_t st) {
-  const KernelInfo k = pick_kernel(fmt, D, a.G);
+  const KernelInfo k = pick_kernel(fmt, D, a.G, a.math);
   if (!prepare(k)) {
     const cudaError_t e = cudaGetLastError();
     return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;

@@ -169,11 +169,19 @@ __device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
 
 // CB2, K role: channels x = 16s + 2q, y = x + 1 (and +8); tokens g, g + 8.
 // kcb = block + 4D + 16q (the lane's codebook column).
-__device__ __forceinline__ void cb2_k_frag(uint32_t kcb, uint32_t w16, int s, uint32_t (&a)[4]) {
+// The codebook columns of step s (cb2_k_cols) and the expansion of the codes
+// against them (cb2_k_expand) are separate so that pages sharing a codebook
+// (the group format) load the columns once per step.
+struct KCols {
+  uint4 a, b;
+};
+__device__ __forceinline__ KCols cb2_k_cols(uint32_t kcb, int s) {
+  return {lds128(kcb + 128 * s), lds128(kcb + 128 * s + 64)};
+}
+__device__ __forceinline__ void cb2_k_expand(const KCols& c, uint32_t w16, uint32_t (&a)[4]) {
   const uint32_t sel1 = (w16 & 0x3333u) | 0x4040u;
   const uint32_t sel2 = ((w16 >> 2) & 0x3333u) | 0x4040u;
-  const uint4 ca = lds128(kcb + 128 * s);
-  const uint4 cb = lds128(kcb + 128 * s + 64);
+  const uint4 ca = c.a, cb = c.b;
   uint32_t lo = prmt(ca.x, ca.z, sel1), hi = prmt(ca.y, ca.w, sel1);
   a[0] = prmt(lo, hi, 0x5140u);
   a[1] = prmt(lo, hi, 0x7362u);
@@ -182,13 +190,16 @@ __device__ __forceinline__ void cb2_k_frag(uint32_t kcb, uint32_t w16, int s, ui
   a[2] = prmt(lo, hi, 0x5140u);
   a[3] = prmt(lo, hi, 0x7362u);
 }
+__device__ __forceinline__ void cb2_k_frag(uint32_t kcb, uint32_t w16, int s, uint32_t (&a)[4]) {
+  cb2_k_expand(cb2_k_cols(kcb, s), w16, a);
+}
 
 // CB2, V role: channels cA = 16s + g, cB = cA + 8; tokens 2q, 2q+1 (and +8).
 // vcb = block + 4D + 16g.
-__device__ __forceinline__ void cb2_v_frag(uint32_t vcb, uint32_t w16, int s, uint32_t (&a)[4]) {
+__device__ __forceinline__ uint4 cb2_v_cols(uint32_t vcb, int s) { return lds128(vcb + 128 * s); }
+__device__ __forceinline__ void cb2_v_expand(const uint4& c, uint32_t w16, uint32_t (&a)[4]) {
   const uint32_t sel1 = (w16 & 0x3333u) | 0x4400u;
   const uint32_t sel2 = ((w16 >> 2) & 0x3333u) | 0x4400u;
-  const uint4 c = lds128(vcb + 128 * s);
   uint32_t lo = prmt(c.x, c.z, sel1), hi = prmt(c.y, c.w, sel1);
   a[0] = prmt(lo, hi, 0x5140u);
   a[1] = prmt(lo, hi, 0x7362u);
@@ -196,6 +207,9 @@ __device__ __forceinline__ void cb2_v_frag(uint32_t vcb, uint32_t w16, int s, ui
   hi = prmt(c.y, c.w, sel2);
   a[2] = prmt(lo, hi, 0x5140u);
   a[3] = prmt(lo, hi, 0x7362u);
+}
+__device__ __forceinline__ void cb2_v_frag(uint32_t vcb, uint32_t w16, int s, uint32_t (&a)[4]) {
+  cb2_v_expand(cb2_v_cols(vcb, s), w16, a);
 }
 
 // FP8 e4m3 codes, either role: slot k = byte k of the lane's 8 bytes for step s.
@@ -428,14 +442,15 @@ __device__ __forceinline__ void cb2_bounce(const uint8_t* side, int base, int nc
 
 // ----------------------------------------------------------------------------- online softmax
 // acc[p][nt][r]: scores in log2 units of page p for token g (r < 2) / g + 8
-// (r >= 2) and head nt*8 + 2q + (r & 1).  Replaces them with p = 2^(s - m) (0
-// for tokens >= ntok[p]), raises the running max m only when a score exceeds
-// it by more than kRescaleTh (so most pages skip the rescale), and updates the
-// per-lane partial sums l.  Returns whether any lane changed its max (alpha
-// holds the factors).
+// (r >= 2) and head nt*8 + 2q + (r & 1), -inf for tokens that do not exist
+// (the caller masks partial and absent pages).  Replaces them with p = 2^(s -
+// m), raises the running max m only when a score exceeds it by more than
+// kRescaleTh (so most pages skip the rescale), and updates the per-lane
+// partial sums l.  Returns whether any lane changed its max (alpha holds the
+// factors).
 template <int PPI, int NT>
-__device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const int (&ntok)[PPI], int g,
-                                               float (&m)[NT][2], float (&l)[NT][2], float (&alpha)[NT][2]) {
+__device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], float (&m)[NT][2], float (&l)[NT][2],
+                                               float (&alpha)[NT][2]) {
   bool any = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -443,10 +458,7 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
     for (int j = 0; j < 2; ++j) {
       float mx = -INFINITY;
 #pragma unroll
-      for (int p = 0; p < PPI; ++p) {
-        mx = fmaxf(mx, (g < ntok[p]) ? acc[p][nt][j] : -INFINITY);
-        mx = fmaxf(mx, (g + 8 < ntok[p]) ? acc[p][nt][2 + j] : -INFINITY);
-      }
+      for (int p = 0; p < PPI; ++p) mx = fmaxf(mx, fmaxf(acc[p][nt][j], acc[p][nt][2 + j]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -455,11 +467,12 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
       alpha[nt][j] = need ? ex2(m[nt][j] - mn) : 1.f;
       m[nt][j] = mn;
       any |= need;
+      const float mb = mn == -INFINITY ? 0.f : mn;   // no score yet: every p is 2^-inf = 0
       float sum = 0.f;
 #pragma unroll
       for (int p = 0; p < PPI; ++p) {
-        const float p0 = (g < ntok[p]) ? ex2(acc[p][nt][j] - mn) : 0.f;
-        const float p1 = (g + 8 < ntok[p]) ? ex2(acc[p][nt][2 + j] - mn) : 0.f;
+        const float p0 = ex2(acc[p][nt][j] - mb);
+        const float p1 = ex2(acc[p][nt][2 + j] - mb);
         acc[p][nt][j] = p0;
         acc[p][nt][2 + j] = p1;
         sum += p0 + p1;
@@ -472,15 +485,17 @@ __device__ __forceinline__ bool online_softmax(float (&acc)[PPI][NT][4], const i
 
 // Rescale the output accumulators (and the shared-memory outlier correction
 // corr[c][h]) by alpha after a max change.
-template <int D, int NT, bool kCorr>
+template <int D, int NT, bool kCorr, bool kO = true>
 __device__ __forceinline__ void rescale_state(float (&o)[NT][D / 16][4], const float (&alpha)[NT][2],
                                               uint32_t corr_s, int G, int GS, int lane) {
+  if (kO) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int s = 0; s < D / 16; ++s)
+      for (int s = 0; s < D / 16; ++s)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) o[nt][s][r] *= alpha[nt][r & 1];
+        for (int r = 0; r < 4; ++r) o[nt][s][r] *= alpha[nt][r & 1];
+  }
   if (kCorr) {
     __syncwarp();
 #pragma unroll
@@ -614,10 +629,17 @@ __device__ __forceinline__ void load_codes(uint32_t blk_s, int lane, uint32_t (&
 // Scores (in the scaled query's units) -> probabilities: each head's score
 // scale st.scl undoes its query scale 2^-k_h and applies softmax_scale *
 // log2(e); then the online softmax and the P^T fragments.
-template <int D, int NT, int PPI>
+struct NoRescale {
+  template <class A>
+  __device__ __forceinline__ void operator()(const A&) const {}
+};
+// kO = false: the caller keeps the output in its own accumulators and
+// rescales them in extra(alpha) (st.o is left alone).
+template <int D, int NT, int PPI, bool kO = true, class Extra = NoRescale>
 __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)[PPI][NT][4], const int (&ntok)[PPI],
                                               float /*scale: in st.scl*/, const WarpSmem& sm, int lane, bool corr,
-                                              uint32_t (&phi)[PPI][NT][2], uint32_t (&plo)[PPI][NT][2]) {
+                                              uint32_t (&phi)[PPI][NT][2], uint32_t (&plo)[PPI][NT][2],
+                                              Extra&& extra = Extra()) {
   const int g = lane >> 2, q4 = lane & 3;
 #pragma unroll
   for (int p = 0; p < PPI; ++p)
@@ -625,15 +647,30 @@ __device__ __forceinline__ void softmax_frags(WarpState<D, NT>& st, float (&acc)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[p][nt][r] *= st.scl[nt][r & 1];
+  // tokens past a partial or absent page's end: -inf (a warp-uniform branch,
+  // taken only for those pages)
+  bool partial = false;
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) partial |= ntok[p] < kPage;
+  if (partial) {
+#pragma unroll
+    for (int p = 0; p < PPI; ++p)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (g + 8 * (r >> 1) >= ntok[p]) acc[p][nt][r] = -INFINITY;
+  }
   float alpha[NT][2];
-  const bool rescale = online_softmax<PPI, NT>(acc, ntok, g, st.m, st.l, alpha);
+  const bool rescale = online_softmax<PPI, NT>(acc, st.m, st.l, alpha);
   if (rescale) {
-    if (corr) rescale_state<D, NT, true>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
-    else rescale_state<D, NT, false>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
+    if (corr) rescale_state<D, NT, true, kO>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
+    else rescale_state<D, NT, false, kO>(st.o, alpha, sm.corr_s, sm.G, sm.GS, lane);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) st.sv[nt][r] *= alpha[nt][r & 1];
+    extra(alpha);   // accumulators the caller keeps in another layout
   }
 #pragma unroll
   for (int p = 0; p < PPI; ++p) p_frags<NT>(acc[p], g, q4, phi[p], plo[p]);
@@ -704,16 +741,21 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     else load_codes<D>(kb_s[p] + CODES, lane, kc[p]);
   }
 #pragma unroll
-  for (int s = 0; s < NS; ++s)
+  for (int s = 0; s < NS; ++s) {
+    KCols gcols;   // the group's codebook columns of step s, shared by its pages
+    if constexpr (GRP) gcols = cb2_k_cols(kb_s[0] + 16 * q4, s);
 #pragma unroll
     for (int p = 0; p < PPI; ++p) {
       uint32_t ak[4];
+      const uint32_t w16 = (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1];
       if (T && tier[p]) fp8_frag(lds64(kb_s[p] + 8 * NS * lane + 8 * s), ak);
       else if constexpr (A3) a3_k_frag<D>(kb_s[p], kc[p], ky[p], s, q4, ak);
-      else cb2_k_frag(kcb(p) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
+      else if constexpr (GRP) cb2_k_expand(gcols, w16, ak);
+      else cb2_k_frag(kcb(p) + 16 * q4, w16, s, ak);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
     }
+  }
   if constexpr (T) {
 #pragma unroll
     for (int p = 0; p < PPI; ++p) {
@@ -728,20 +770,21 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
     for (int p = 0; p < PPI; ++p) cb2s_k_correct<D, NT>(kb_s[p], a.n_static, st.qs, lane, acc[p]);
   }
-  // outlier corrections (the chunk loop is rolled; the pages are unrolled)
+  // outlier corrections: the first chunk (the records that arrived with the
+  // block) runs without a branch -- on empty slots for a page with none, an
+  // FP8 tier page or an absent one -- so it schedules with the code around
+  // it; further chunks (rare) go through the rolled loop
 #pragma unroll
   for (int p = 0; p < PPI; ++p) {
     if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
     const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(kb_s[p] + SIDE), D);
+    cb2_k_correct<D, NT, Fmt<FMT>::kMain>(kb_s[p] + SIDE + 4, min(kChunk, n_ch), GRP ? kb_s[0] : kb_s[p], sm.qsm_s,
+                                          sm.G, sm.GS, lane, acc[p]);
 #pragma unroll 1
-    for (int base = 0; base < n_ch; base += kChunk) {
-      uint32_t recs = kb_s[p] + SIDE + 4;
-      if (base > 0) {
-        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
-        recs = sm.bounce_s;
-      }
-      cb2_k_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), GRP ? kb_s[0] : kb_s[p], sm.qsm_s, sm.G,
-                                            sm.GS, lane, acc[p]);
+    for (int base = kChunk; base < n_ch; base += kChunk) {
+      cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
+      cb2_k_correct<D, NT, Fmt<FMT>::kMain>(sm.bounce_s, min(kChunk, n_ch - base), GRP ? kb_s[0] : kb_s[p], sm.qsm_s,
+                                            sm.G, sm.GS, lane, acc[p]);
       __syncwarp();
     }
   }
@@ -760,7 +803,9 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
     sv[p] = (T && tier[p]) ? ldsf(vb_s[p] + fp8_sc_off(D)) : 1.f;
   }
 #pragma unroll
-  for (int s = 0; s < NS; ++s)
+  for (int s = 0; s < NS; ++s) {
+    uint4 gvcols;   // as gcols, V role
+    if constexpr (GRP) gvcols = cb2_v_cols(vb_s[0] + 16 * g, s);
 #pragma unroll
     for (int p = 0; p < PPI; ++p) {
       uint32_t av[4];
@@ -775,8 +820,10 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
           for (int r = 0; r < 4; ++r) st.o[nt][s][r] = fmaf(sv[p], t4[r], st.o[nt][s][r]);
         }
       } else {
+        const uint32_t w16 = (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1];
         if constexpr (A3) a3_v_frag<D>(vb_s[p], vc[p], vy[p], s, g, av);
-        else cb2_v_frag(vcb(p) + 16 * g, (s & 1) ? (vc[p][s >> 1] >> 16) : vc[p][s >> 1], s, av);
+        else if constexpr (GRP) cb2_v_expand(gvcols, w16, av);
+        else cb2_v_frag(vcb(p) + 16 * g, w16, s, av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma16816(st.o[nt][s], av[0], av[1], av[2], av[3], phi[p][nt][0], phi[p][nt][1]);
@@ -784,6 +831,7 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         }
       }
     }
+  }
   if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
 #pragma unroll
     for (int p = 0; p < PPI; ++p) cb2s_v_accum<D, NT>(vb_s[p], a.n_static, phi[p], plo[p], lane, st.sv);
@@ -792,6 +840,154 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
   for (int p = 0; p < PPI; ++p) {
     if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
     const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + SIDE), D);
+    if (n_ch > 0) {
+      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(vb_s[p] + SIDE + 4, min(kChunk, n_ch), GRP ? vb_s[0] : vb_s[p], phi[p],
+                                            plo[p], sm.corr_s, sm.G, sm.GS, lane);
+      __syncwarp();
+    }
+#pragma unroll 1
+    for (int base = kChunk; base < n_ch; base += kChunk) {
+      cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
+      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(sm.bounce_s, min(kChunk, n_ch - base), GRP ? vb_s[0] : vb_s[p], phi[p],
+                                            plo[p], sm.corr_s, sm.G, sm.GS, lane);
+      __syncwarp();
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- CUDA-core QK / PV (G <= 4)
+// The same codebook pages with QK^T and PV on the FMA pipe instead of the
+// tensor cores (kvq_config.decode_math = KVQ_DECODE_CUDA_CORES), for the
+// small GQA groups whose heads fill only half of an m16n8 tile.  The code
+// expansion is the same (cb2_k_frag / cb2_v_frag); each lane then
+// multiplies its 8 values of a step in fp32:
+//   QK: lane (g, q) holds K[t = g, g + 8][c = 16 s + 2q, +1, +8, +9]; partial
+//       scores of its two tokens for the G heads (query rows read from the
+//       fp32 query in shared memory), summed over the 4 lanes of a token;
+//   PV: lane (g, q) holds V^T[c = 16 s + g, +8][t = 2q, 2q + 1, +8, +9];
+//       partial outputs of its two channels for the G heads over its four
+//       tokens (occ), summed over the 4 lanes once, after the page loop.
+// The outlier corrections stay the exact-input mma tiles of iter_cb2.
+template <int FMT, int D, int PPI, class KDone, class VWait>
+__device__ __forceinline__ void iter_cb2_cc(WarpState<D, 1>& st, float (&occ)[D / 16][8], const uint32_t (&kb_s)[PPI],
+                                            const uint32_t (&vb_s)[PPI], const int32_t (&ent)[PPI],
+                                            const int (&ntok)[PPI], const DecodeArgs& a, int kvh, const WarpSmem& sm,
+                                            int lane, KDone&& k_done, VWait&& v_wait) {
+  constexpr int NS = D / 16;
+  constexpr int SIDE = side_off<D, kBlkCb2>();
+  const int g = lane >> 2, q4 = lane & 3;
+  float sc[PPI][2][4];   // [page][token g, g + 8][head]
+  uint32_t kc[PPI][NS / 2];
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) sc[p][i][h] = 0.f;
+    load_codes<D>(kb_s[p], lane, kc[p]);
+  }
+#pragma unroll
+  for (int s = 0; s < NS; ++s) {
+    // query rows of this lane's four channels (qsm is [D][4]: one row per channel)
+    const int c0 = 16 * s + 2 * q4;
+    const float4 q0 = *reinterpret_cast<const float4*>(sm.qsm + 4 * c0);
+    const float4 q1 = *reinterpret_cast<const float4*>(sm.qsm + 4 * (c0 + 1));
+    const float4 q8 = *reinterpret_cast<const float4*>(sm.qsm + 4 * (c0 + 8));
+    const float4 q9 = *reinterpret_cast<const float4*>(sm.qsm + 4 * (c0 + 9));
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) {
+      uint32_t ak[4];
+      cb2_k_frag(kb_s[p] + cb2_cb_off(D) + 16 * q4, (s & 1) ? (kc[p][s >> 1] >> 16) : kc[p][s >> 1], s, ak);
+      const float2 k0 = __half22float2(u32_as_h2(ak[0]));   // token g, channels c0, c0 + 1
+      const float2 k1 = __half22float2(u32_as_h2(ak[1]));   // token g + 8
+      const float2 k2 = __half22float2(u32_as_h2(ak[2]));   // token g, channels c0 + 8, c0 + 9
+      const float2 k3 = __half22float2(u32_as_h2(ak[3]));   // token g + 8
+      const float qq[4][4] = {{q0.x, q0.y, q0.z, q0.w}, {q1.x, q1.y, q1.z, q1.w},
+                              {q8.x, q8.y, q8.z, q8.w}, {q9.x, q9.y, q9.z, q9.w}};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        sc[p][0][h] = fmaf(k0.x, qq[0][h], fmaf(k0.y, qq[1][h], fmaf(k2.x, qq[2][h], fmaf(k2.y, qq[3][h], sc[p][0][h]))));
+        sc[p][1][h] = fmaf(k1.x, qq[0][h], fmaf(k1.y, qq[1][h], fmaf(k3.x, qq[2][h], fmaf(k3.y, qq[3][h], sc[p][1][h]))));
+      }
+    }
+  }
+  // sum over the four lanes of a token, then the score layout of the mma path
+  // (lane (g, q) holds heads 2q, 2q + 1; q >= 2 are padding heads)
+  float acc[PPI][1][4];
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        sc[p][i][h] += __shfl_xor_sync(0xffffffffu, sc[p][i][h], 1);
+        sc[p][i][h] += __shfl_xor_sync(0xffffffffu, sc[p][i][h], 2);
+      }
+    const bool lo = q4 == 0, on = q4 < 2;
+    acc[p][0][0] = on ? (lo ? sc[p][0][0] : sc[p][0][2]) : 0.f;
+    acc[p][0][1] = on ? (lo ? sc[p][0][1] : sc[p][0][3]) : 0.f;
+    acc[p][0][2] = on ? (lo ? sc[p][1][0] : sc[p][1][2]) : 0.f;
+    acc[p][0][3] = on ? (lo ? sc[p][1][1] : sc[p][1][3]) : 0.f;
+  }
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    const int n_ch = min((int)lds8(kb_s[p] + SIDE), D);
+#pragma unroll 1
+    for (int base = 0; base < n_ch; base += kChunk) {
+      uint32_t recs = kb_s[p] + SIDE + 4;
+      if (base > 0) {
+        cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 0) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
+        recs = sm.bounce_s;
+      }
+      cb2_k_correct<D, 1, kBlkCb2>(recs, min(kChunk, n_ch - base), kb_s[p], sm.qsm_s, sm.G, sm.GS, lane, acc[p]);
+      __syncwarp();
+    }
+  }
+  k_done();
+  uint32_t phi[PPI][1][2], plo[PPI][1][2];
+  softmax_frags<D, 1, PPI, false>(st, acc, ntok, a.scale_log2, sm, lane, true, phi, plo, [&](const float (&alpha)[1][2]) {
+    // occ holds all four heads: head h's factor sits in lane (0, h / 2), register h % 2
+    float ah[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) ah[h] = __shfl_sync(0xffffffffu, alpha[0][h & 1], h >> 1);
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) occ[s][i] *= ah[i & 3];
+  });
+  v_wait();
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    // probabilities of this lane's V tokens t = 2q, 2q + 1, 2q + 8, 2q + 9 for
+    // every head: P[t][h] is register 2 (t >= 8) + h % 2 of lane (t % 8, h / 2)
+    float pv[4][4];   // [token 2q, 2q+1, 2q+8, 2q+9][head]
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = 2 * q4 + (i & 1) + 8 * (i >> 1);
+        pv[i][h] = __shfl_sync(0xffffffffu, acc[p][0][2 * (i >> 1) + (h & 1)], 4 * (t & 7) + (h >> 1));
+      }
+    uint32_t vc[NS / 2];
+    load_codes<D>(vb_s[p], lane, vc);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      uint32_t av[4];
+      cb2_v_frag(vb_s[p] + cb2_cb_off(D) + 16 * g, (s & 1) ? (vc[s >> 1] >> 16) : vc[s >> 1], s, av);
+      const float2 v0 = __half22float2(u32_as_h2(av[0]));   // channel c, tokens 2q, 2q + 1
+      const float2 v1 = __half22float2(u32_as_h2(av[1]));   // channel c + 8
+      const float2 v2 = __half22float2(u32_as_h2(av[2]));   // channel c, tokens 2q + 8, 2q + 9
+      const float2 v3 = __half22float2(u32_as_h2(av[3]));   // channel c + 8
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        occ[s][h] = fmaf(pv[0][h], v0.x, fmaf(pv[1][h], v0.y, fmaf(pv[2][h], v2.x, fmaf(pv[3][h], v2.y, occ[s][h]))));
+        occ[s][4 + h] = fmaf(pv[0][h], v1.x, fmaf(pv[1][h], v1.y, fmaf(pv[2][h], v3.x, fmaf(pv[3][h], v3.y, occ[s][4 + h]))));
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < PPI; ++p) {
+    const int n_ch = min((int)lds8(vb_s[p] + SIDE), D);
 #pragma unroll 1
     for (int base = 0; base < n_ch; base += kChunk) {
       uint32_t recs = vb_s[p] + SIDE + 4;
@@ -799,10 +995,31 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
         cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);
         recs = sm.bounce_s;
       }
-      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(recs, min(kChunk, n_ch - base), GRP ? vb_s[0] : vb_s[p], phi[p], plo[p],
-                                            sm.corr_s, sm.G, sm.GS, lane);
+      cb2_v_correct<D, 1, kBlkCb2>(recs, min(kChunk, n_ch - base), vb_s[p], phi[p], plo[p], sm.corr_s, sm.G, sm.GS,
+                                   lane);
       __syncwarp();
     }
+  }
+}
+
+// occ (lane (g, q): channels 16 s + g, +8 of every head, over its four tokens)
+// summed over the 4 lanes of a channel pair and added into the output
+// accumulators' layout (lane (g, q): heads 2q, 2q + 1).
+template <int D>
+__device__ __forceinline__ void fold_occ(WarpState<D, 1>& st, float (&occ)[D / 16][8], int lane) {
+  const int q4 = lane & 3;
+  const bool lo = q4 == 0, on = q4 < 2;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      occ[s][i] += __shfl_xor_sync(0xffffffffu, occ[s][i], 1);
+      occ[s][i] += __shfl_xor_sync(0xffffffffu, occ[s][i], 2);
+    }
+    st.o[0][s][0] += on ? (lo ? occ[s][0] : occ[s][2]) : 0.f;
+    st.o[0][s][1] += on ? (lo ? occ[s][1] : occ[s][3]) : 0.f;
+    st.o[0][s][2] += on ? (lo ? occ[s][4] : occ[s][6]) : 0.f;
+    st.o[0][s][3] += on ? (lo ? occ[s][5] : occ[s][7]) : 0.f;
   }
 }
 
@@ -1129,13 +1346,14 @@ __device__ __forceinline__ void merge_group(const float* __restrict__ part_o, co
 // ----------------------------------------------------------------------------- split kernel
 // Resident CTAs per SM the register budget is cut for (shared memory allows
 // as many for G <= 8).
-template <int FMT, int D, int NT>
+template <int FMT, int D, int NT, bool CC = false>
 __host__ __device__ constexpr int min_ctas_per_sm() {
-  return NT == 2 ? 2 : Fmt<FMT>::kMain == kBlkInt4 ? 3 : 4;
+  return CC ? (D == 128 ? 3 : 4) : NT == 2 ? 2 : Fmt<FMT>::kMain == kBlkInt4 ? 3 : 4;
 }
 
-template <int FMT, int D, int NT, int W>
-__global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_split_kernel(const DecodeArgs a) {
+// CC: QK^T and PV of the codebook pages on CUDA cores (iter_cb2_cc; CB2 at G <= 4).
+template <int FMT, int D, int NT, int W, bool CC = false>
+__global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT, CC>()) decode_split_kernel(const DecodeArgs a) {
   using F = Fmt<FMT>;
   constexpr int NS = D / 16, PPI = F::kPPI, NK = Ring<FMT>::kK, NV = Ring<FMT>::kV;
   constexpr int HS = half_slot_bytes<FMT, D>();
@@ -1275,39 +1493,40 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
         ent[j] = __shfl_sync(0xffffffffu, win, li - win_base);
       }
     }
-    if (lane == 0) {
-      uint32_t bytes[PPI], total = 0;
+    // lane j < PPI validates page j and issues its copy; lane 0 arms the
+    // barrier with the total first (every lane fences its own copy against
+    // the warp's earlier generic reads of the stage)
+    int32_t e = kNoPage;
 #pragma unroll
-      for (int j = 0; j < PPI; ++j) {
-        bytes[j] = 0;
-        int32_t m = kNoPage;
-        if (ent[j] != kNoPage) {
-          const uint32_t u = (uint32_t)ent[j], phys = u & 0x7FFFFFFFu;
-          const bool tier = (u >> 31) != 0;
-          const bool ok =
-              tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
-          if (ok) {
-            m = ent[j];
-            bytes[j] = tier ? fetch_bytes<D>(kBlkFp8) : F::kGroup ? (j == 0 ? 8 * D + GPB : GPB) : main_fetch;
-          } else {
-            m = kBadEntry;
-            atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-          }
+    for (int j = 0; j < PPI; ++j) e = lane == j ? ent[j] : e;
+    uint32_t bytes = 0;
+    if (lane < PPI) {
+      int32_t m = kNoPage;
+      if (e != kNoPage) {
+        const uint32_t u = (uint32_t)e, phys = u & 0x7FFFFFFFu;
+        const bool tier = (u >> 31) != 0;
+        const bool ok =
+            tier ? (FMT == KVQ_FMT_TIERED && phys < (uint32_t)a.num_tier_pages) : phys < (uint32_t)a.num_pages;
+        if (ok) {
+          m = e;
+          bytes = tier ? fetch_bytes<D>(kBlkFp8) : F::kGroup ? (lane == 0 ? 8 * D + GPB : GPB) : main_fetch;
+        } else {
+          m = kBadEntry;
+          atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
         }
-        meta[slot * PPI + j] = m;
-        total += bytes[j];
       }
+      meta[slot * PPI + lane] = m;
+    }
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+    if (lane == 0) {
+      if (total == 0) mbar_arrive(&kbar[slot]);
+      else mbar_arrive_expect_tx(&kbar[slot], total);
+    }
+    __syncwarp();
+    if (bytes) {
       fence_proxy_async();
-      if (total == 0) {
-        mbar_arrive(&kbar[slot]);
-      } else {
-        mbar_arrive_expect_tx(&kbar[slot], total);
-#pragma unroll
-        for (int j = 0; j < PPI; ++j)
-          if (bytes[j])
-            bulk_g2s(kslots + slot * STG + copy_dst<FMT, D>(j), block_src<FMT, D>(a, kvh, ent[j], 0) + copy_src<FMT, D>(j),
-                     bytes[j], &kbar[slot]);
-      }
+      bulk_g2s(kslots + slot * STG + copy_dst<FMT, D>(lane), block_src<FMT, D>(a, kvh, e, 0) + copy_src<FMT, D>(lane),
+               bytes, &kbar[slot]);
     }
     __syncwarp();
     ++k_issued;
@@ -1317,29 +1536,22 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
   auto issue_v = [&](int it) {
     if (it >= n_iter) return;
     const int slot = it % NV, kslot = it % NK;
+    // as issue_k: lane j < PPI copies page j
+    const int32_t e = lane < PPI ? meta[kslot * PPI + lane] : kNoPage;
+    const uint32_t bytes = (e == kNoPage || e == kBadEntry)       ? 0u
+                           : (FMT == KVQ_FMT_TIERED && e < 0)     ? (uint32_t)fetch_bytes<D>(kBlkFp8)
+                           : F::kGroup                            ? (uint32_t)(lane == 0 ? 8 * D + GPB : GPB)
+                                                                  : (uint32_t)main_fetch;
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
     if (lane == 0) {
-      uint32_t bytes[PPI], total = 0;
-      int32_t ent[PPI];
-#pragma unroll
-      for (int j = 0; j < PPI; ++j) {
-        ent[j] = meta[kslot * PPI + j];
-        bytes[j] = (ent[j] == kNoPage || ent[j] == kBadEntry) ? 0u
-                   : (FMT == KVQ_FMT_TIERED && ent[j] < 0) ? (uint32_t)fetch_bytes<D>(kBlkFp8)
-                   : F::kGroup                             ? (uint32_t)(j == 0 ? 8 * D + GPB : GPB)
-                                                           : (uint32_t)main_fetch;
-        total += bytes[j];
-      }
+      if (total == 0) mbar_arrive(&vbar[slot]);
+      else mbar_arrive_expect_tx(&vbar[slot], total);
+    }
+    __syncwarp();
+    if (bytes) {
       fence_proxy_async();
-      if (total == 0) {
-        mbar_arrive(&vbar[slot]);
-      } else {
-        mbar_arrive_expect_tx(&vbar[slot], total);
-#pragma unroll
-        for (int j = 0; j < PPI; ++j)
-          if (bytes[j])
-            bulk_g2s(vslots + slot * STG + copy_dst<FMT, D>(j), block_src<FMT, D>(a, kvh, ent[j], 1) + copy_src<FMT, D>(j),
-                     bytes[j], &vbar[slot]);
-      }
+      bulk_g2s(vslots + slot * STG + copy_dst<FMT, D>(lane), block_src<FMT, D>(a, kvh, e, 1) + copy_src<FMT, D>(lane),
+               bytes, &vbar[slot]);
     }
     __syncwarp();
     ++v_issued;
@@ -1394,6 +1606,13 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     vch = g < a.n_static ? (mk[a.n_static + g] & (D - 1)) : 0;
   }
 
+  static_assert(!CC || (FMT == KVQ_FMT_CB2_OUTLIER && NT == 1), "CUDA-core path: CB2 pages, G <= 4");
+  float occ[CC ? NS : 1][8];   // CC: per-lane partial outputs (see iter_cb2_cc)
+#pragma unroll
+  for (int s = 0; s < (CC ? NS : 1); ++s)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) occ[s][i] = 0.f;
+
   bool timed_out = false;
 #pragma unroll 1
   for (int it = 0; it < n_iter; ++it) {
@@ -1435,7 +1654,9 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
       v_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[vs], (it / NV) & 1, kWaitLimitNs));
       v_waited += v_ok;
     };
-    if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s || F::kMain == kBlkA3 || F::kGroup) {
+    if constexpr (CC) {
+      iter_cb2_cc<FMT, D, PPI>(st, occ, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
+    } else if constexpr (F::kMain == kBlkCb2 || F::kMain == kBlkCb2s || F::kMain == kBlkA3 || F::kGroup) {
       iter_cb2<FMT, D, NT, PPI>(st, qf, kb_s, vb_s, ent, ntok, a, kvh, sm, lane, k_done, v_wait);
     } else if constexpr (F::kMain == kBlkE2m1) {
       iter_e2m1<D, NT, PPI>(st, qf, kb_s, vb_s, ntok, a.scale_log2, sm, lane, k_done, v_wait);
@@ -1450,6 +1671,7 @@ __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<FMT, D, NT>()) decode_
     __syncwarp();
     issue_v(it + NV);
   }
+  if constexpr (CC) fold_occ<D>(st, occ, lane);
   if (timed_out) {
     if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
     // let copies still in flight land (bounded) before the CTA can exit
@@ -1592,13 +1814,13 @@ struct KernelInfo {
   int threads;
 };
 
-template <int FMT, int D, int NT>
+template <int FMT, int D, int NT, bool CC = false>
 static KernelInfo kernel_info(int G) {
   const int GS = (G + 3) & ~3;
   const size_t plan = cta_smem_bytes<FMT, D, kWarps>(GS);
   const size_t merge = mbar_bytes<FMT, kWarps>() + align16(D * GS * 4) + (size_t)kWarps * GS * D * 4 +
                        2 * (size_t)kWarps * GS * 4 + 2 * (size_t)GS * 4 + 16;
-  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps>), plan > merge ? plan : merge,
+  return {reinterpret_cast<void*>(decode_split_kernel<FMT, D, NT, kWarps, CC>), plan > merge ? plan : merge,
           kWarps * 32};
 }
 
@@ -1611,7 +1833,7 @@ static KernelInfo kernel_info_fmt(int D, int G) {
 // One translation unit per format instantiates its kernels.
 KernelInfo decode_kernel_int4(int D, int G);
 KernelInfo decode_kernel_e2m1(int D, int G);
-KernelInfo decode_kernel_cb2(int D, int G);
+KernelInfo decode_kernel_cb2(int D, int G, bool cuda_cores);
 KernelInfo decode_kernel_tiered(int D, int G);
 KernelInfo decode_kernel_cb2s(int D, int G);
 KernelInfo decode_kernel_a3(int D, int G);

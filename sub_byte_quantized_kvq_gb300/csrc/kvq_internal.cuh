@@ -31,6 +31,7 @@ struct DecodeArgs {
   uint32_t* arrivals;  // [B][Hkv] arrival counters, zero between calls
   const uint8_t* static_mask;  // CB2_STATIC: [Hkv][2][n_static] channels
   int n_static;
+  int math;         // KVQ_DECODE_TENSOR_CORES or KVQ_DECODE_CUDA_CORES (resolved, never AUTO)
 };
 
 struct AppendArgs {
@@ -55,7 +56,7 @@ cudaError_t decode_split_launch(const DecodeArgs& a, int fmt, int D, cudaStream_
 cudaError_t decode_combine_launch(const float* part_o, const float2* part_ml, int B, int Hkv, int Hq, int S, int D, void* out,
                                   int out_dtype, cudaStream_t st);
 // Resident CTAs per SM of the split kernel for (format, head_dim, G); 0 on error.
-int decode_ctas_per_sm(int fmt, int D, int G);
+int decode_ctas_per_sm(int fmt, int D, int G, int math);
 // Warps per CTA of the split decode kernel.
 constexpr int kWarpsPerCta = 4;
 // Quantize-on-append launches (see kvq_quantize.cu).

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 KVQ_FMT_INT4_G32, KVQ_FMT_FP4_E2M1_S16, KVQ_FMT_CB2_OUTLIER, KVQ_FMT_TIERED, KVQ_FMT_CB2_STATIC = 0, 1, 2, 3, 4
 KVQ_FMT_ASYM3_OUTLIER, KVQ_FMT_CB2_GROUP4 = 5, 6
 KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
+KVQ_DECODE_AUTO, KVQ_DECODE_TENSOR_CORES, KVQ_DECODE_CUDA_CORES = 0, 1, 2
 KVQ_TIER_BIT = 1 << 31
 KVQ_STATUS_BAD_PAGE, KVQ_STATUS_CAPACITY, KVQ_STATUS_SEQ_TOO_LONG, KVQ_STATUS_TIMEOUT = 1, 2, 4, 8
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY, KVQ_ERR_CUDA = range(6)
@@ -36,7 +37,8 @@ class kvq_config(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("pages_per_seq_max", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("num_tier_pages", ctypes.c_int32), ("format", ctypes.c_int32), ("lloyd_iters", ctypes.c_int32),
-                ("sigma", ctypes.c_double), ("static_channels", ctypes.c_int32)]
+                ("sigma", ctypes.c_double), ("static_channels", ctypes.c_int32),
+                ("decode_math", ctypes.c_int32)]
 
 
 class kvq_cache(ctypes.Structure):
@@ -115,12 +117,14 @@ class QuantizedKVCache:
 
     def __init__(self, fmt: int, num_seqs: int, num_kv_heads: int, head_dim: int, pages_per_seq_max: int,
                  num_pages: int, num_tier_pages: int = 0, sigma: float = 3.0, lloyd_iters: int = 16,
-                 page_table: torch.Tensor | None = None, device="cuda", static_channels: int = 0):
+                 page_table: torch.Tensor | None = None, device="cuda", static_channels: int = 0,
+                 decode_math: int = KVQ_DECODE_AUTO):
         """static_channels (KVQ_FMT_CB2_STATIC): fp16 channels per (kv head, K|V);
         fill `static_mask` ([Hkv, 2, n]) before the first append, e.g. with
-        kvq_select_static_channels."""
+        kvq_select_static_channels.  decode_math: KVQ_DECODE_* (cfg.decode_math
+        may be changed between calls)."""
         self.cfg = kvq_config(num_seqs, num_kv_heads, head_dim, pages_per_seq_max, num_pages, num_tier_pages, fmt,
-                              lloyd_iters, sigma, static_channels)
+                              lloyd_iters, sigma, static_channels, decode_math)
         pb, tb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
         _check(lib().kvq_cache_bytes(ctypes.byref(self.cfg), ctypes.byref(pb), ctypes.byref(tb), ctypes.byref(sb)),
                "kvq_cache_bytes")

@@ -76,6 +76,11 @@ def test_invalid_arguments_rejected_before_launch(kvq):
     assert L.kvq_block_bytes(ctypes.byref(_cfg(kvq, 2, 96)), 0, ctypes.byref(n)) == kvq.KVQ_ERR_UNSUPPORTED
     assert L.kvq_block_bytes(ctypes.byref(_cfg(kvq, 2, sigma=2.0)), 0, ctypes.byref(n)) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_block_bytes(ctypes.byref(_cfg(kvq, 2, num_tier_pages=3)), 0, ctypes.byref(n)) == kvq.KVQ_ERR_INVALID_ARG
+    for bad in (-1, 3):
+        assert L.kvq_block_bytes(ctypes.byref(_cfg(kvq, 2, decode_math=bad)), 0, ctypes.byref(n)) == \
+            kvq.KVQ_ERR_INVALID_ARG
+    for ok in (kvq.KVQ_DECODE_AUTO, kvq.KVQ_DECODE_TENSOR_CORES, kvq.KVQ_DECODE_CUDA_CORES):
+        assert L.kvq_block_bytes(ctypes.byref(_cfg(kvq, 0, decode_math=ok)), 0, ctypes.byref(n)) == kvq.KVQ_OK
     cache = kvq.kvq_cache()   # all-null cache
     c = _cfg(kvq)
     assert L.kvq_quantize_append(ctypes.byref(c), ctypes.byref(cache), None, None, 0, 1, None, None) == \

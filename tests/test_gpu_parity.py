@@ -117,6 +117,46 @@ def test_decode_attention_parity(fmt, D, G):
     assert pair.gpu.status_word() == 0
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 4])
+@pytest.mark.parametrize("dist", ["normal", "student_t4"])
+def test_decode_cuda_cores_parity(D, G, dist):
+    """KVQ_DECODE_CUDA_CORES: the CB2 pages' QK^T and PV as fp32 FMAs (G <= 4),
+    against the oracle with the same bar as the tensor-core path; heavy tails
+    give side-lists longer than the prefetched records."""
+    B, Hkv, P = 3, 2, 14
+    lens = [209, 77, 1]
+    pair = Pair(CB2, B, Hkv, D, P, seed=21)
+    k, v = make_kv(22, B, max(lens), Hkv, D, *((dist, 4, 8.0) if dist == "normal" else (dist, 0, 1.0)))
+    pair.append(k, v, t_per_seq=lens)
+    pair.gpu.cfg.decode_math = kvq.KVQ_DECODE_CUDA_CORES
+    for splits in (0, 1, 5):
+        for od in (torch.float32, torch.bfloat16):
+            got, exp = pair.decode(Hkv * G, seed=splits, num_splits=splits, out_dtype=od)
+            assert_attention_close(got, exp, od)
+    assert pair.gpu.status_word() == 0
+
+
+def test_decode_cuda_cores_token_by_token_and_fallback():
+    """The CUDA-core path after single-token appends (partial pages from
+    staging, page boundaries); a group size it does not cover (G = 8) runs the
+    tensor-core kernel, bit for bit."""
+    B, Hkv, D, P = 2, 2, 128, 4
+    pair = Pair(CB2, B, Hkv, D, P, seed=23)
+    k, v = make_kv(24, B, 40, Hkv, D)
+    pair.gpu.cfg.decode_math = kvq.KVQ_DECODE_CUDA_CORES
+    for t in range(40):
+        pair.append(k[:, t:t + 1], v[:, t:t + 1])
+        if t in (0, 15, 16, 31, 32, 39):
+            got, exp = pair.decode(Hkv * 4, seed=t)
+            assert_attention_close(got, exp)
+    cc, _ = pair.decode(Hkv * 8, seed=5)
+    pair.gpu.cfg.decode_math = kvq.KVQ_DECODE_TENSOR_CORES
+    tc, exp = pair.decode(Hkv * 8, seed=5)
+    np.testing.assert_array_equal(cc, tc)
+    assert_attention_close(tc, exp)
+
+
 @pytest.mark.parametrize("fmt", [INT4, E2M1, CB2, TIERED, CB2S, A3, CB2G])
 def test_fused_merge_matches_split_then_combine(fmt):
     """kvq_decode_attention merges the splits inside its one launch (the last
@@ -221,6 +261,30 @@ def test_bad_page_entry_is_flagged_and_skipped():
     assert pair.gpu.seq_lens.cpu().tolist() == [0, 40]          # sequence 0 skipped, 1 appended
     pair.gpu.page_table.copy_(pt)
     pair.gpu.status.zero_()
+
+
+@pytest.mark.parametrize("fmt", [CB2, TIERED, E2M1])
+def test_decode_bad_page_entry_is_flagged_and_skipped(fmt):
+    """A page-table entry outside its pool at decode time: the page is skipped
+    (its tokens do not take part), KVQ_STATUS_BAD_PAGE is set, and the other
+    pages still give a finite softmax over the rest of the sequence."""
+    B, Hkv, D, P = 2, 2, 128, 6
+    pair = Pair(fmt, B, Hkv, D, P, seed=12, tiers=_tiers(fmt, B, P))
+    k, v = make_kv(12, B, 96, Hkv, D, *_dist(fmt))
+    pair.append(k, v)
+    pt = pair.gpu.page_table.clone()
+    pair.gpu.page_table[1, 2] = pair.gpu.cfg.num_pages + 3
+    q = torch.ones((B, 4 * Hkv, D), dtype=torch.bfloat16, device="cuda")
+    out = kvq.kvq_decode_attention(pair.gpu, q, D ** -0.5, 96, 2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() & kvq.KVQ_STATUS_BAD_PAGE
+    assert torch.isfinite(out).all()
+    pair.gpu.page_table.copy_(pt)
+    pair.gpu.status.zero_()
+    good = kvq.kvq_decode_attention(pair.gpu, q, D ** -0.5, 96, 2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert pair.gpu.status_word() == 0
+    assert torch.equal(out[0], good[0])          # the other sequence is untouched
 
 
 def test_capacity_overflow_matches_oracle():
