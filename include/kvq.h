@@ -222,7 +222,8 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
  *             16-byte aligned: receives the projected K (index 0) and V of the
  *             tokens appended; other rows are not written.
  * Errors: KVQ_ERR_INVALID_ARG for a null or misaligned pointer or a bad size,
- * KVQ_ERR_UNSUPPORTED for head_dim other than 64 / 128 or num_seqs * t_new >= 2^31,
+ * KVQ_ERR_UNSUPPORTED for head_dim other than 64 / 128, num_seqs * t_new >= 2^31 or
+ * t_new > 8,387,456 (65535 tiles of 128 positions),
  * KVQ_ERR_CAPACITY as for kvq_quantize_append, KVQ_ERR_CUDA when the driver
  * offers no tensor-map encoder or a launch fails.  A tensor-core wait that gives up sets
  * KVQ_STATUS_TIMEOUT and leaves that tile's blocks unwritten. */

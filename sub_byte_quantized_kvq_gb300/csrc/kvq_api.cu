@@ -323,6 +323,7 @@ kvq_status kvq_project_append(const kvq_config* cfg, const kvq_cache* cache, con
   if (t_new == 0) return KVQ_OK;
   if ((long long)t_new > (long long)cfg->pages_per_seq_max * kPage) return KVQ_ERR_CAPACITY;
   if ((long long)cfg->num_seqs * t_new >= (1ll << 31)) return KVQ_ERR_UNSUPPORTED;   // TMA row coordinates are int32
+  if (t_new > 65535 * 128 - 1024) return KVQ_ERR_UNSUPPORTED;   // 128-row tiles in the grid's y dimension
   ProjArgs p;
   fill_append_args(cfg, cache, t_new, t_per_seq, p.a);
   p.x = static_cast<const __nv_bfloat16*>(x);

@@ -840,11 +840,10 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
   for (int p = 0; p < PPI; ++p) {
     if constexpr (FMT == KVQ_FMT_CB2_STATIC) break;
     const int n_ch = (T && tier[p]) ? 0 : min((int)lds8(vb_s[p] + SIDE), D);
-    if (n_ch > 0) {
-      cb2_v_correct<D, NT, Fmt<FMT>::kMain>(vb_s[p] + SIDE + 4, min(kChunk, n_ch), GRP ? vb_s[0] : vb_s[p], phi[p],
-                                            plo[p], sm.corr_s, sm.G, sm.GS, lane);
-      __syncwarp();
-    }
+    // as for K: the first chunk without a branch (empty slots write nothing)
+    cb2_v_correct<D, NT, Fmt<FMT>::kMain>(vb_s[p] + SIDE + 4, min(kChunk, n_ch), GRP ? vb_s[0] : vb_s[p], phi[p],
+                                          plo[p], sm.corr_s, sm.G, sm.GS, lane);
+    __syncwarp();
 #pragma unroll 1
     for (int base = kChunk; base < n_ch; base += kChunk) {
       cb2_bounce(block_src<FMT, D>(a, kvh, ent[p], 1) + SIDE, base, min(kChunk, n_ch - base), sm.bounce_s, lane);

@@ -1597,8 +1597,11 @@ cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st) {
 // Autonomous Workflows, item 1: the attention projection and the KV-cache
 // write in one kernel).
 //
-// One CTA (512 threads) per (tile of 128 sequence positions, kv head,
-// sequence) computes K and V together (N = 2 D accumulator columns).  Tile
+// One CTA (512 threads) per (kv head, tile of 128 sequence positions,
+// sequence) computes K and V together (N = 2 D accumulator columns).  The kv
+// heads are the grid's fastest dimension, so the CTAs that read the same x
+// rows run at about the same time and all but the first find them in L2
+// (measured 2-5% faster than tiles first).  Tile
 // rows are whole pages (4-page groups for the CB2 group format), so each block
 // is written by one CTA.  Warp 0 streams the operands with TMA (one 2-D box
 // per unit of x rows, one per weight matrix; 128-byte swizzle, 64 hidden
@@ -1704,7 +1707,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __gr
   constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS, S = P::S;
   extern __shared__ __align__(1024) uint8_t psm_raw[];
   const AppendArgs& a = p.a;
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, tile = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
@@ -2254,7 +2257,7 @@ static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
       cudaFuncSetAttribute(project_append_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
   if (e != cudaSuccess) return e;
   const int units_max = (p.a.t_new + 2 * P::U - 2) / P::U;   // units a span of t_new positions can touch
-  const dim3 grid((units_max + P::SPT - 1) / P::SPT, p.a.Hkv, p.a.B);
+  const dim3 grid(p.a.Hkv, (units_max + P::SPT - 1) / P::SPT, p.a.B);
   project_append_kernel<KIND, D><<<grid, kPThreads, P::SMEM, st>>>(p);
   append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
   return cudaGetLastError();
