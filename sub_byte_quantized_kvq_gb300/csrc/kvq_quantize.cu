@@ -581,6 +581,32 @@ __device__ __noinline__ bool sums_exact_of(const float* x, int xs, uint64_t keep
   frexpf(amax * (float)NROWS, &eh);
   return eh - elo <= 24;
 }
+// fp16 bits of sum / cnt rounded once (ties to even), for a sum that is
+// exact in binary32: the binary32 quotient is within one rounding of the
+// mean, so the answer is its fp16 rounding or a neighbour, and which side of
+// a neighbouring midpoint b the mean lies on is the sign of sum - b cnt, which
+// one fused multiply-add gives exactly (b cnt is exact; the result is rounded
+// once, keeping its sign, and is zero only on a tie).  The fp64 mean is never
+// closer to b than a binary32 ulp of the sum unless it equals b, so rounding
+// it to fp64 first (the definition) picks the same fp16 value.  0xFFFF for
+// the largest fp16 values (left to fp64).
+__device__ __forceinline__ uint16_t f16_of_exact_mean(float sum, int cnt) {
+  const float fc = (float)cnt, as = fabsf(sum);
+  uint16_t h = f32_to_f16_bits(__fdiv_rn(as, fc));
+  if (h >= 0x7BFFu) return 0xFFFFu;
+  const float vh = f16_bits_to_f32(h);
+  const float bh = (vh + f16_bits_to_f32((uint16_t)(h + 1))) * 0.5f;
+  const float rh = __fmaf_rn(-bh, fc, as);
+  if (rh > 0.f || (rh == 0.f && (h & 1u))) {
+    h = (uint16_t)(h + 1);
+  } else if (h > 0) {
+    const float bl = (f16_bits_to_f32((uint16_t)(h - 1)) + vh) * 0.5f;
+    const float rl = __fmaf_rn(-bl, fc, as);
+    if (rl < 0.f || (rl == 0.f && (h & 1u))) h = (uint16_t)(h - 1);
+  }
+  return (uint16_t)(h | (sum < 0.f ? 0x8000u : 0u));
+}
+
 // Whether centroid j is exactly its fp64 value.
 template <int NROWS>
 __device__ __forceinline__ bool centroid_exact(LloydState& S, const float* x, int xs, uint64_t keep, int j) {
@@ -739,6 +765,13 @@ __device__ __forceinline__ void lloyd4_rows(const float* x, int xs, uint64_t kee
     const float e = fmaxf(ec, fabsf(S.c[jj]) * kNudge);
     bool ok = f32_to_f16_bits(S.c[jj] - e) == c16[jj] && f32_to_f16_bits(S.c[jj] + e) == c16[jj];
     if (!ok) ok = centroid_exact<NROWS>(S, x, xs, keep, jj);
+    if (!ok && !S.lin[jj] && S.sums_exact == 1) {   // an exact sum: its mean rounded exactly
+      const uint16_t hm = f16_of_exact_mean(S.sumc[jj], S.cntc[jj]);
+      if (hm != 0xFFFFu) {
+        c16[jj] = hm;
+        ok = true;
+      }
+    }
     if (!ok && !S.lin[jj] && !S.sums_exact && last[jj]) {   // a compensated mean of its cell
       const uint16_t hm = cell_mean_f16_tight<NROWS>(x, xs, keep, prev, jj);
       if (hm != 0xFFFFu) {
@@ -918,10 +951,27 @@ __device__ void quantize_tokens_e2m1(const float (*xs)[XS], int t0, int lo, int 
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint8_t s8 = e4m3_of_quotient(amax, 6.0f);
   const float sc = e4m3_to_f32(s8);
-  uint32_t nb[2] = {0u, 0u};
+  // binary32 codes, certified or flagged; the flagged ones (rare) are taken
+  // again in fp64 after the loop, so the unrolled loop holds no call
+  uint32_t nb[2] = {0u, 0u}, unsure = 0u;
+  if (sc != 0.f) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    nb[i >> 3] |= (uint32_t)(sc != 0.f ? e2m1_of_quotient(x[i], sc) : 0) << (4 * (i & 7));
+    for (int i = 0; i < 16; ++i) {
+      const float r = __fdiv_rn(x[i], sc);
+      const uint8_t c = f32_to_e2m1(r);
+      const bool sure = (f32_to_e2m1(r * (1.f - kNudge)) == c && f32_to_e2m1(r * (1.f + kNudge)) == c) ||
+                        quotient_exact(r, x[i], sc);
+      unsure |= (uint32_t)!sure << i;
+      nb[i >> 3] |= (uint32_t)c << (4 * (i & 7));
+    }
+  }
+  while (unsure) {
+    const int i = __ffs(unsure) - 1;
+    unsure &= unsure - 1u;
+    const uint32_t c = e2m1_of_quotient64(x[i], sc), sh = 4 * (i & 7);
+    if (i < 8) nb[0] = (nb[0] & ~(0xFu << sh)) | (c << sh);
+    else nb[1] = (nb[1] & ~(0xFu << sh)) | (c << sh);
+  }
   store_codes<16>(blk, role, NS, t, 16 * g, lo, hi, nb, NS);
   if (act) blk[e2m1_sc_off(D) + 16 * g + t] = s8;
 }
@@ -1701,8 +1751,11 @@ KVQ_PLAN_FITS(kProjGroup, 64);
 KVQ_PLAN_FITS(kProjGroup, 128);
 #undef KVQ_PLAN_FITS
 
+// Two CTAs per SM (64 registers a thread, a few spilled): one CTA's
+// quantization epilogue then runs beside the other's MMAs; one CTA per SM
+// measured 1.1-1.7x slower on every format.
 template <int KIND, int D>
-__global__ void __launch_bounds__(kPThreads, 1) project_append_kernel(const __grid_constant__ ProjArgs p) {
+__global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __grid_constant__ ProjArgs p) {
   using P = ProjPlan<KIND, D>;
   constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS, S = P::S;
   extern __shared__ __align__(1024) uint8_t psm_raw[];
