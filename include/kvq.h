@@ -256,12 +256,14 @@ kvq_status kvq_decode_num_splits(const kvq_config* cfg, int32_t num_q_heads, int
  *   num_splits   context splits per (sequence, kv head), at most 256
  *           (KVQ_ERR_CAPACITY beyond); 0 = library choice.
  *   workspace    device, >= kvq_decode_workspace_bytes(), 16-byte aligned:
- *           fp32 split partials, then 4 * num_seqs * Hkv bytes of arrival
- *           counters.  The counters must be zero before a workspace's first
- *           use (zero the whole workspace once); every call leaves them zero
- *           again, except one that sets KVQ_STATUS_TIMEOUT, after which the
- *           workspace must be zeroed before its next use.  The partials need
- *           no initialisation.
+ *           4 * num_seqs * Hkv bytes of arrival counters (padded to 256
+ *           bytes), then the fp32 split partials.  The counters must be zero
+ *           before a workspace's first use (zero the whole workspace once);
+ *           every call leaves them zero again, so one workspace serves calls
+ *           of any shape (splits, query heads, length) on the same cache.  Zero
+ *           it again after a call that set KVQ_STATUS_TIMEOUT, and before using
+ *           it for a cache with more (sequence, kv head) pairs.  The partials
+ *           need no initialisation.
  * One kernel launch: split CTAs stream each page's packed blocks into shared
  * memory with bulk asynchronous copies, expand codes straight into
  * tensor-core fragments, correct outliers, run an online softmax and write

@@ -210,11 +210,17 @@ static int num_sms() {
 // 90% of its last wave of resident CTA slots (so no nearly empty final wave),
 // keeping at least 2 pages per warp in each split; otherwise the count with the
 // best last-wave fill.
-// Workspace layout: part_o fp32 [B][Hq][S][D], part_ml float2 [B][Hq][S],
-// then (16-byte aligned) the fused combine's arrival counters u32 [B][Hkv].
-static size_t arrivals_offset(const kvq_config* c, int num_q_heads, int S) {
+// Workspace layout: the fused merge's arrival counters u32 [B][Hkv] first
+// (padded to 256 bytes), then part_o fp32 [B][Hq][S][D] and part_ml float2
+// [B][Hq][S].  The counters' place depends only on the cache's (sequence, kv
+// head) count, so calls of any shape (splits, query heads, length) can share
+// a workspace: each call's last CTAs leave the counters at zero.
+static size_t partials_offset(const kvq_config* c) {
+  return ((size_t)c->num_seqs * c->num_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
+}
+static size_t partials_bytes(const kvq_config* c, int num_q_heads, int S) {
   const size_t rows = (size_t)c->num_seqs * num_q_heads * S;
-  return (rows * c->head_dim * sizeof(float) + rows * sizeof(float2) + 15) / 16 * 16;
+  return rows * c->head_dim * sizeof(float) + rows * sizeof(float2);
 }
 
 // The decode math a call runs: CUDA cores only where that path exists
@@ -351,7 +357,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t num_q_heads
   if (!dim_supported(cfg) || num_q_heads / cfg->num_kv_heads > 16) return KVQ_ERR_UNSUPPORTED;
   int S = num_splits;
   if (S == 0) S = auto_splits(cfg, num_q_heads / cfg->num_kv_heads, max_seq_len);
-  *bytes = arrivals_offset(cfg, num_q_heads, S) + (size_t)cfg->num_seqs * cfg->num_kv_heads * sizeof(uint32_t);
+  *bytes = partials_offset(cfg) + partials_bytes(cfg, num_q_heads, S);
   return KVQ_OK;
 }
 
@@ -385,9 +391,8 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.seq_lens = cache->seq_lens;
   a.staging = cache->staging;
   a.q = static_cast<const __nv_bfloat16*>(q);
-  a.part_o = static_cast<float*>(workspace);
-  a.part_ml = reinterpret_cast<float2*>(static_cast<float*>(workspace) +
-                                        (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
+  a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + partials_offset(cfg));
+  a.part_ml = reinterpret_cast<float2*>(a.part_o + (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
   a.status = cache->status;
   a.B = cfg->num_seqs;
   a.Hkv = cfg->num_kv_heads;
@@ -403,7 +408,7 @@ static kvq_status decode_prepare(const kvq_config* cfg, const kvq_cache* cache, 
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = nullptr;
   a.out_dtype = KVQ_F32;
-  a.arrivals = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + arrivals_offset(cfg, num_q_heads, S));
+  a.arrivals = static_cast<uint32_t*>(workspace);
   a.static_mask = cache->static_mask;
   a.n_static = cfg->format == KVQ_FMT_CB2_STATIC ? cfg->static_channels : 0;
   a.math = decode_math(cfg, G);
@@ -439,7 +444,7 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
   if (st != KVQ_OK) return st;
   if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
   const int S = num_splits ? num_splits : auto_splits(cfg, num_q_heads / cfg->num_kv_heads, max_seq_len);
-  const float* part_o = static_cast<const float*>(workspace);
+  const float* part_o = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + partials_offset(cfg));
   const float2* part_ml = reinterpret_cast<const float2*>(part_o + (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
   if (S > kMaxSplits) return KVQ_ERR_CAPACITY;
   if (decode_combine_launch(part_o, part_ml, cfg->num_seqs, cfg->num_kv_heads, num_q_heads, S, cfg->head_dim, out,

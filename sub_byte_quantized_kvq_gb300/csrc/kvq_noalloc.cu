@@ -52,10 +52,11 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // before anything is enqueued
   void* scratch = scratch_on_current_device();
   if (!scratch) return KVQ_ERR_CUDA;
-  // The arrival counters sit where the call's shape (sequences, query heads,
-  // splits, head_dim) puts them, so after a call of another shape they would
-  // lie on that call's partials: this call clears its own counters on the
-  // stream before the launch (a memset, which allocates nothing).
+  // The scratch is shared by every cache in the process: the arrival counters
+  // sit at its start, B * Hkv of them, so a call on a cache with more
+  // (sequence, kv head) pairs than the last one's would find that call's
+  // partials there.  This call clears its own counters on the stream before
+  // the launch (a memset, which allocates nothing).
   return kvq::decode_attention_zeroing_counters(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, out,
                                                 out_dtype, scratch, (size_t)KVQ_NOALLOC_SCRATCH_BYTES,
                                                 static_cast<cudaStream_t>(stream));

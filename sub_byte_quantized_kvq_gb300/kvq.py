@@ -236,7 +236,7 @@ def kvq_select_static_channels(cache: QuantizedKVCache, k: torch.Tensor, v: torc
 
 def alloc_workspace(cache: QuantizedKVCache, num_q_heads: int, max_seq_len: int, num_splits: int = 0) -> torch.Tensor:
     nbytes = kvq_decode_workspace_bytes(cache, num_q_heads, max_seq_len, num_splits)
-    # zeroed once: its tail holds the fused split merge's arrival counters
+    # zeroed once: its head holds the fused split merge's arrival counters
     return torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.float32, device=cache.device)
 
 

@@ -92,7 +92,7 @@ def test_invalid_arguments_rejected_before_launch(kvq):
     assert L.kvq_dequantize(ctypes.byref(c), ctypes.byref(cache), 0, 0, 0, 0, 1, None, None) == kvq.KVQ_ERR_INVALID_ARG
     # workspace size with an explicit split count is pure host arithmetic
     assert L.kvq_decode_workspace_bytes(ctypes.byref(c), 32, 4096, 8, ctypes.byref(n)) == 0
-    assert n.value == 4 * 32 * 8 * (128 * 4 + 8) + 4 * 4 * 8   # partials, then one arrival counter per (seq, kv head)
+    assert n.value == 256 + 4 * 32 * 8 * (128 * 4 + 8)   # one arrival counter per (seq, kv head), padded; partials
     assert L.kvq_decode_workspace_bytes(ctypes.byref(c), 30, 4096, 8, ctypes.byref(n)) == kvq.KVQ_ERR_INVALID_ARG
 
 

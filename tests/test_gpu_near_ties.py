@@ -110,3 +110,25 @@ def test_e2m1_bit_exact_on_decision_boundaries(D):
         kv[idx] = np.concatenate([nt.e2m1_tie_block(rng, scale_tie=(idx[2] + s) % 2 == 0) for s in range(D // 16)])
     pair.append(torch.from_numpy(kv[0]), torch.from_numpy(kv[1]))
     pair.assert_cache_equal()
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_CB2_OUTLIER, kvq.KVQ_FMT_CB2_GROUP4, kvq.KVQ_FMT_CB2_STATIC])
+@pytest.mark.parametrize("step", [0.25, 0.125])
+def test_lloyd_on_a_coarse_value_grid_bit_exact(fmt, step):
+    """Values on a coarse grid (multiples of `step` in [-2, 2], plus a few
+    large ones): a value often sits exactly on the midpoint of two cell means
+    or at the same distance from both, and cell sums are exact.  The binary32
+    margin cannot settle such rows; they take the fp64 distances of the
+    definition, and the cache must match the oracle bit for bit."""
+    rng = np.random.default_rng(int(400 + 1000 * step) + fmt)
+    B, Hkv, D = 2, 2, 128
+    npages = 8
+    pair = Pair(fmt, B, Hkv, D, npages, seed=11)
+    T = 16 * npages
+    levels = np.arange(-2.0, 2.0 + step, step, dtype=F32)
+    kv = rng.choice(levels, size=(2, B, T, Hkv, D)).astype(F32)
+    kv[:, :, :, :, 5] *= 8.0   # an outlier channel
+    k, v = torch.from_numpy(kv[0]), torch.from_numpy(kv[1])   # exact in bf16
+    pair.append(k[:, :37].contiguous(), v[:, :37].contiguous(), dtype=torch.bfloat16)
+    pair.append(k[:, 37:].contiguous(), v[:, 37:].contiguous(), dtype=torch.bfloat16)
+    pair.assert_cache_equal()

@@ -181,8 +181,33 @@ def test_fused_merge_matches_split_then_combine(fmt):
             one = kvq.kvq_decode_attention(cache, q, D ** -0.5, L, S, out_dtype=torch.float32, workspace=ws)
             torch.cuda.synchronize()
             assert torch.equal(one, two), f"S={S}"
-        off = kvq.kvq_decode_workspace_bytes(cache, Hq, L, S) - 4 * B * Hkv   # the arrival counters
-        assert (ws.view(torch.int32)[off // 4:off // 4 + B * Hkv] == 0).all()
+        assert (ws.view(torch.int32)[:B * Hkv] == 0).all()   # the arrival counters, at the start
+    assert cache.status_word() == 0
+
+
+def test_one_workspace_across_call_shapes():
+    """The arrival counters sit at the workspace's start whatever the call's
+    shape, so one workspace (sized for the largest call) serves calls with
+    other split counts, query heads and lengths; each gives the result of a
+    fresh workspace, bit for bit."""
+    B, Hkv, D, P = 3, 2, 128, 14
+    lens = [209, 77, 130]
+    pair = Pair(CB2, B, Hkv, D, P, seed=31)
+    k, v = make_kv(32, B, max(lens), Hkv, D)
+    pair.append(k, v, t_per_seq=lens)
+    cache = pair.gpu
+    from sub_byte_quantized_kvq_gb300 import synth
+    calls = ((4, 5, 224), (4, 1, 224), (8, 14, 224), (4, 5, 213), (8, 0, 224), (4, 14, 213))
+    big = max(kvq.kvq_decode_workspace_bytes(cache, Hkv * G, L, S) for G, S, L in calls)
+    ws = torch.zeros((big + 15) // 16 * 4, dtype=torch.float32, device="cuda")
+    for G, S, L in calls:
+        q = synth.queries_bf16(G + S, B, Hkv * G, D, device="cuda")
+        shared = kvq.kvq_decode_attention(cache, q, D ** -0.5, L, S, out_dtype=torch.float32, workspace=ws)
+        fresh = kvq.kvq_decode_attention(cache, q, D ** -0.5, L, S, out_dtype=torch.float32,
+                                         workspace=kvq.alloc_workspace(cache, Hkv * G, L, S))
+        torch.cuda.synchronize()
+        assert torch.equal(shared, fresh), (G, S, L)
+        assert (ws.view(torch.int32)[:B * Hkv] == 0).all()
     assert cache.status_word() == 0
 
 

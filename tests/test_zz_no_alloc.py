@@ -71,10 +71,11 @@ def test_noalloc_rejects_partials_larger_than_its_scratch():
 
 
 def test_noalloc_shape_changes_between_calls():
-    """The arrival counters sit where each call's shape puts them.  Run
-    splits 5, then 1 (whose counters fall on the first call's partials), then
-    a cache with other sequence and head counts, then the first again: every
-    call must still merge its splits and match the workspace entry point."""
+    """The scratch is shared by every cache: its arrival counters sit at the
+    start, one per (sequence, kv head) of the calling cache.  Run splits 5,
+    then 1, then a cache with more (sequence, kv head) pairs, then the first
+    again: every call must still merge its splits and match the workspace
+    entry point."""
     a, qa, La = _cache(kvq.KVQ_FMT_CB2_OUTLIER)
     b, qb, Lb = _cache(kvq.KVQ_FMT_CB2_OUTLIER, B=5, Hkv=3, G=2, lens=(33, 160, 16, 95, 200), P=16)
     scale = qa.shape[-1] ** -0.5
