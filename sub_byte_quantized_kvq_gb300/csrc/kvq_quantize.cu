@@ -618,13 +618,40 @@ __device__ __forceinline__ bool centroid_exact(LloydState& S, const float* x, in
 // The rows of `rows` whose binary32 assignment was not certified by the
 // midpoint margin (all kept rows when the centroids are not strictly
 // sorted), assigned again: by distances with a margin, by exact distances,
-// else in fp64 from the centroids' fp64 values (needs exact sums; otherwise
-// the fit is marked unsure).  Rebuilds the assignment words and the four
+// else in fp64 from the centroids' fp64 values (from exact binary32 sums, or
+// recomputed from the cells the previous pass formed; a centroid formed in an
+// earlier pass leaves the fit unsure).  Rebuilds the assignment words and the four
 // sums and counts in row order.  Returns false when a row is left unsure.
 // (Rare; out of line like lloyd_fix_codes.)
+// The fp64 nearest centroid of v (lowest index on ties) among those within
+// 2E of the binary32 best, each candidate's fp64 value recomputed as the
+// definition forms it: a linspace point from the range, or the fp64 mean, in
+// row order, of the values the previous pass assigned to it (`prev`; that
+// pass matched the definition).  -1 when a candidate was last formed in an
+// earlier pass (its cell is no longer at hand).
+template <int NROWS>
+__device__ __noinline__ int nearest4_by_cells64(float v, const LloydState& S, const float* x, int xs, uint64_t keep,
+                                                const uint32_t* prev, const bool* lastf) {
+  float bd = INFINITY;
+  for (int j = 0; j < 4; ++j) bd = fminf(bd, fabsf(v - S.c[j]));
+  int best = -1;
+  double b64 = 0.0;
+  for (int j = 0; j < 4; ++j) {
+    if (fabsf(v - S.c[j]) > bd + 2.f * S.E) continue;
+    double c;
+    if (S.lin[j]) c = centroid64(j, S.mn, S.mx, true, 0.f, 1);
+    else if (lastf[j]) c = cell_mean64<NROWS>(x, xs, keep, prev, j);
+    else return -1;
+    const double d = fabs((double)v - c);
+    if (best < 0 || d < b64) { b64 = d; best = j; }
+  }
+  return best;
+}
+
 template <int NROWS>
 __device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int xs, uint64_t keep, uint64_t rows,
-                                            uint32_t* a, float* sum, int* cnt) {
+                                            uint32_t* a, float* sum, int* cnt, const uint32_t* prev,
+                                            const bool* lastf) {
   constexpr int NW = (NROWS + 15) / 16;
   bool cx[4];
   for (int j = 0; j < 4; ++j) cx[j] = centroid_exact<NROWS>(S, x, xs, keep, j);
@@ -636,8 +663,13 @@ __device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int x
     uint32_t j = (uint32_t)nearest4_sure(v, S.c, S.E, ok);
     if (!ok && !distances_exact(v, S.c, cx)) {
       if (S.sums_exact < 0) S.sums_exact = sums_exact_of<NROWS>(x, xs, keep, S.amax);
-      if (S.sums_exact) j = (uint32_t)nearest4_by64(v, S.c, S.E, S.mn, S.mx, S.lin, S.sumc, S.cntc);
-      else sure = false;
+      if (S.sums_exact) {
+        j = (uint32_t)nearest4_by64(v, S.c, S.E, S.mn, S.mx, S.lin, S.sumc, S.cntc);
+      } else {   // inexact sums: the candidates' fp64 means from their cells
+        const int jc = nearest4_by_cells64<NROWS>(v, S, x, xs, keep, prev, lastf);
+        if (jc >= 0) j = (uint32_t)jc;
+        else sure = false;
+      }
     }
     a[r >> 4] = (a[r >> 4] & ~(3u << (2 * (r & 15)))) | (j << (2 * (r & 15)));
   }
@@ -732,7 +764,7 @@ __device__ __forceinline__ void lloyd4_rows(const float* x, int xs, uint64_t kee
         }
       }
       if (!srt) unc = keep;
-      if (unc) sure = lloyd_fix_rows<NROWS>(S, x, xs, keep, unc, a, sum, cnt) && sure;
+      if (unc) sure = lloyd_fix_rows<NROWS>(S, x, xs, keep, unc, a, sum, cnt, prev, last) && sure;
       bool same = have_prev;
 #pragma unroll
       for (int w = 0; w < NW; ++w) same = same && a[w] == prev[w];

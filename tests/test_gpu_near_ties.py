@@ -112,23 +112,36 @@ def test_e2m1_bit_exact_on_decision_boundaries(D):
     pair.assert_cache_equal()
 
 
+def coarse_grid_kv(rng, B, T, Hkv, D, step, tiny):
+    """K, V float32 [2, B, T, Hkv, D] on multiples of `step` in [-2, 2] with one
+    outlier channel; `tiny` puts a value of 2^-30 in row 3 of every page, so
+    the values span more than 24 bits and no cell sum is exact in binary32."""
+    levels = np.arange(-2.0, 2.0 + step, step, dtype=F32)
+    kv = rng.choice(levels, size=(2, B, T, Hkv, D)).astype(F32)
+    kv[:, :, :, :, 5] *= 8.0   # an outlier channel
+    if tiny:
+        kv[:, :, 3::16] = F32(2.0 ** -30)
+    return kv
+
+
 @pytest.mark.parametrize("fmt", [kvq.KVQ_FMT_CB2_OUTLIER, kvq.KVQ_FMT_CB2_GROUP4, kvq.KVQ_FMT_CB2_STATIC])
 @pytest.mark.parametrize("step", [0.25, 0.125])
-def test_lloyd_on_a_coarse_value_grid_bit_exact(fmt, step):
+@pytest.mark.parametrize("tiny", [False, True])
+def test_lloyd_on_a_coarse_value_grid_bit_exact(fmt, step, tiny):
     """Values on a coarse grid (multiples of `step` in [-2, 2], plus a few
     large ones): a value often sits exactly on the midpoint of two cell means
-    or at the same distance from both, and cell sums are exact.  The binary32
-    margin cannot settle such rows; they take the fp64 distances of the
-    definition, and the cache must match the oracle bit for bit."""
-    rng = np.random.default_rng(int(400 + 1000 * step) + fmt)
+    or at the same distance from both.  The binary32 margin cannot settle
+    such rows; they take the fp64 distances of the definition, from exact
+    binary32 sums or (tiny: the sums are inexact) from fp64 means of the
+    cells, and the cache must match the oracle bit for bit."""
+    rng = np.random.default_rng(int(400 + 1000 * step) + fmt + 7 * tiny)
     B, Hkv, D = 2, 2, 128
     npages = 8
     pair = Pair(fmt, B, Hkv, D, npages, seed=11)
     T = 16 * npages
-    levels = np.arange(-2.0, 2.0 + step, step, dtype=F32)
-    kv = rng.choice(levels, size=(2, B, T, Hkv, D)).astype(F32)
-    kv[:, :, :, :, 5] *= 8.0   # an outlier channel
-    k, v = torch.from_numpy(kv[0]), torch.from_numpy(kv[1])   # exact in bf16
-    pair.append(k[:, :37].contiguous(), v[:, :37].contiguous(), dtype=torch.bfloat16)
-    pair.append(k[:, 37:].contiguous(), v[:, 37:].contiguous(), dtype=torch.bfloat16)
+    kv = coarse_grid_kv(rng, B, T, Hkv, D, step, tiny)
+    k, v = torch.from_numpy(kv[0]), torch.from_numpy(kv[1])
+    dt = torch.bfloat16 if not tiny else torch.float32   # the grid is exact in bf16; 2^-30 rows need fp32
+    pair.append(k[:, :37].contiguous(), v[:, :37].contiguous(), dtype=dt)
+    pair.append(k[:, 37:].contiguous(), v[:, 37:].contiguous(), dtype=dt)
     pair.assert_cache_equal()
