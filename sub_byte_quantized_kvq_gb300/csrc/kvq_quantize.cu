@@ -721,16 +721,25 @@ __device__ __forceinline__ void lloyd4_rows(const float* x, int xs, uint64_t kee
   if (keep) {
     bool have = false;
     float mn = 0.f, mx = 0.f;
+    int elo = 1000;   // lowest set bit of any nonzero value
     for (int r = 0; r < NROWS; ++r) {
       if (!(keep >> r & 1u)) continue;
       const float v = x[r * xs];
       if (!have) { mn = v; mx = v; have = true; }
       mn = v < mn ? v : mn;
       mx = v > mx ? v : mx;
+      if (v != 0.f) elo = min(elo, low_bit_exp(v));
     }
     S.mn = mn;
     S.mx = mx;
     S.amax = fmaxf(fabsf(mn), fabsf(mx));
+    {   // whether every partial sum of the values is exact (as sums_exact_of;
+        // taken here for every fit: the rare paths that need it would
+        // otherwise stall their warp on a separate pass over the rows)
+      int eh = 0;
+      frexpf(S.amax * (float)NROWS, &eh);
+      S.sums_exact = S.amax == 0.f || eh - elo <= 24;
+    }
     // one value repeated: all centroids equal it in either precision and
     // every assignment is centroid 0; no margin to check
     flat = mn == mx;
