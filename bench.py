@@ -373,8 +373,9 @@ def time_oracle(w: synth.Workload, seed: int, target_s: float, reps: int | None 
 # ----------------------------------------------------------------------------- append timing (optional)
 def time_append(w: synth.Workload, dev, flush_mb: int) -> dict:
     """kvq_quantize_append for every sequence of the workload: one token into
-    staging, one token that completes a page (page quantizer), and a 4096-token
-    prefill chunk (bf16 inputs, N(0,1)).  L2 flushed before every timed call;
+    staging, one token that completes a page (its 15 earlier tokens appended
+    beforehand; page quantizer), and a 4096-token prefill chunk (bf16 inputs,
+    N(0,1)).  L2 flushed before every timed call;
     CUDA events on the current stream; mean of 5 calls after 3 warm-up calls."""
     flush = L2Flush(flush_mb, dev)
     res = {"l2": "flushed before every timed call"}
@@ -386,6 +387,9 @@ def time_append(w: synth.Workload, dev, flush_mb: int) -> dict:
         vv = torch.randn_like(kk)
         if w.fmt == synth.FMT_CB2S:
             kvq.kvq_select_static_channels(c, kk[0].contiguous(), vv[0].contiguous())
+        if start:   # the page's earlier tokens, appended beforehand (untimed): the serving case
+            k0 = torch.randn((w.B, start, w.Hkv, w.D), device=dev).to(torch.bfloat16)
+            kvq.kvq_quantize_append(c, k0, torch.randn_like(k0))
         ts = []
         for r in range(8):
             c.seq_lens.fill_(start)

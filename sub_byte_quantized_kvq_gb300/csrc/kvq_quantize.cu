@@ -284,10 +284,17 @@ __device__ __noinline__ void outlier_decide64(const float* x, int n, int stride,
 __device__ __noinline__ void outlier_decide(const float* x, int n, int stride, double sigma, int kmax, uint32_t* bits) {
   const float sg = (float)sigma;
   float sum = 0.f, amax = 0.f;
+  const float v0 = x[0];
+  bool cst = true;   // every value equal (no NaN)
   for (int i = 0; i < n; ++i) {
     const float v = x[i * stride];
     sum += v;
     amax = fmaxf(amax, fabsf(v));
+    cst = cst && v == v0;
+  }
+  if (cst) {   // a constant vector: its mean is the value itself in either precision, so no outliers
+    for (int w = 0; w < (n + 31) / 32; ++w) bits[w] = 0u;
+    return;
   }
   const float mu = __fdiv_rn(sum, (float)n);
   float ss = 0.f;
@@ -655,7 +662,7 @@ __device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int x
   constexpr int NW = (NROWS + 15) / 16;
   bool cx[4];
   for (int j = 0; j < 4; ++j) cx[j] = centroid_exact<NROWS>(S, x, xs, keep, j);
-  bool sure = true;
+  bool sure = true, changed = false;
   for (int r = 0; r < NROWS; ++r) {
     if (!(rows >> r & 1u)) continue;
     const float v = x[r * xs];
@@ -671,8 +678,10 @@ __device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int x
         else sure = false;
       }
     }
+    changed |= ((a[r >> 4] >> (2 * (r & 15))) & 3u) != j;
     a[r >> 4] = (a[r >> 4] & ~(3u << (2 * (r & 15)))) | (j << (2 * (r & 15)));
   }
+  if (!changed) return sure;   // the pass's own sums and counts stand
   for (int jj = 0; jj < 4; ++jj) { sum[jj] = 0.f; cnt[jj] = 0; }
   for (int r = 0; r < NROWS; ++r)
     if (keep >> r & 1u) {
