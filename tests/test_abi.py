@@ -96,6 +96,23 @@ def test_invalid_arguments_rejected_before_launch(kvq):
     assert L.kvq_decode_workspace_bytes(ctypes.byref(c), 30, 4096, 8, ctypes.byref(n)) == kvq.KVQ_ERR_INVALID_ARG
 
 
+def test_projection_size_limits_before_launch(kvq):
+    """kvq_project_append refuses sizes its launch cannot express before it
+    touches any buffer (the pointers here are never dereferenced)."""
+    L = kvq.lib()
+    fake = ctypes.c_void_p(1 << 20)   # 16-byte aligned, never read
+    c = _cfg(kvq, 0, 128, num_seqs=1, pages_per_seq_max=600000, num_pages=600000)
+    cache = kvq.kvq_cache(fake, None, fake, fake, None, fake, None)   # INT4: no staging
+    args = lambda t: (ctypes.byref(c), ctypes.byref(cache), fake, 4096, fake, fake, t, None, None, None)
+    assert L.kvq_project_append(*args(65535 * 128 - 1023)) == kvq.KVQ_ERR_UNSUPPORTED   # grid rows
+    assert L.kvq_project_append(*args(600000 * 16 + 1)) == kvq.KVQ_ERR_CAPACITY
+    c.num_seqs = 300
+    assert L.kvq_project_append(*args(7200000)) == kvq.KVQ_ERR_UNSUPPORTED   # 2^31 TMA rows
+    assert L.kvq_project_append(*args(0)) == kvq.KVQ_OK                      # nothing to do
+    assert L.kvq_project_append(ctypes.byref(c), ctypes.byref(cache), fake, 4010, fake, fake, 16, None, None,
+                                None) == kvq.KVQ_ERR_INVALID_ARG              # hidden not a multiple of 32
+
+
 def test_status_strings_and_version(kvq):
     for s in range(7):
         assert kvq.kvq_status_string(s)
