@@ -150,6 +150,17 @@ def test_decode_cuda_cores_token_by_token_and_fallback():
         if t in (0, 15, 16, 31, 32, 39):
             got, exp = pair.decode(Hkv * 4, seed=t)
             assert_attention_close(got, exp)
+    # the two-stage calls run the same CUDA-core kernel
+    from sub_byte_quantized_kvq_gb300 import synth
+    cache, Hq, L = pair.gpu, Hkv * 4, 40
+    q = synth.queries_bf16(6, B, Hq, D, device="cuda")
+    ws = kvq.alloc_workspace(cache, Hq, L, 3)
+    one = kvq.kvq_decode_attention(cache, q, D ** -0.5, L, 3, out_dtype=torch.float32, workspace=ws)
+    two = torch.empty_like(one)
+    kvq.kvq_decode_split(cache, q, D ** -0.5, L, ws, 3)
+    kvq.kvq_decode_combine(cache, Hq, L, ws, two, 3)
+    torch.cuda.synchronize()
+    assert torch.equal(one, two)
     cc, _ = pair.decode(Hkv * 8, seed=5)
     pair.gpu.cfg.decode_math = kvq.KVQ_DECODE_TENSOR_CORES
     tc, exp = pair.decode(Hkv * 8, seed=5)
