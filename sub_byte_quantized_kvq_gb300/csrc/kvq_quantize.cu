@@ -483,22 +483,6 @@ __device__ __noinline__ double centroid64(int j, float mn, float mx, bool lin, f
   }
   return (double)sum / (double)cnt;
 }
-// The fp64 nearest centroid of v (lowest index on ties) among those whose
-// binary32 distance is within 2E of the binary32 best -- the others are
-// farther in fp64 as well (each distance is within E / 2 of its fp64 value).
-__device__ __noinline__ int nearest4_by64(float v, const float* c, float E, float mn, float mx, const bool* lin,
-                                          const float* sumc, const int* cntc) {
-  float bd = INFINITY;
-  for (int j = 0; j < 4; ++j) bd = fminf(bd, fabsf(v - c[j]));
-  int best = -1;
-  double b64 = 0.0;
-  for (int j = 0; j < 4; ++j) {
-    if (fabsf(v - c[j]) > bd + 2.f * E) continue;
-    const double d = fabs((double)v - centroid64(j, mn, mx, lin[j], sumc[j], cntc[j]));
-    if (best < 0 || d < b64) { b64 = d; best = j; }
-  }
-  return best;
-}
 // fp16 bits of the mean of the rows of `keep` whose code in `asg` is j, when
 // a compensated (TwoSum) binary32 evaluation settles its rounding; 0xFFFF
 // (a NaN pattern no mean produces here) when it does not.  The sum is kept
@@ -660,18 +644,43 @@ __device__ __noinline__ bool lloyd_fix_rows(LloydState& S, const float* x, int x
                                             uint32_t* a, float* sum, int* cnt, const uint32_t* prev,
                                             const bool* lastf) {
   constexpr int NW = (NROWS + 15) / 16;
-  bool cx[4];
-  for (int j = 0; j < 4; ++j) cx[j] = centroid_exact<NROWS>(S, x, xs, keep, j);
+  bool cx[4] = {false, false, false, false}, have_cx = false, have64 = false;
+  double c64[4] = {0.0, 0.0, 0.0, 0.0};
   bool sure = true, changed = false;
-  for (int r = 0; r < NROWS; ++r) {
-    if (!(rows >> r & 1u)) continue;
+  for (uint64_t m = rows; m; m &= m - 1) {
+    const int r = __ffsll((long long)m) - 1;
     const float v = x[r * xs];
     bool ok = true;
     uint32_t j = (uint32_t)nearest4_sure(v, S.c, S.E, ok);
+    if (!ok && !have_cx) {
+      for (int jj = 0; jj < 4; ++jj) cx[jj] = centroid_exact<NROWS>(S, x, xs, keep, jj);
+      have_cx = true;
+    }
     if (!ok && !distances_exact(v, S.c, cx)) {
       if (S.sums_exact < 0) S.sums_exact = sums_exact_of<NROWS>(x, xs, keep, S.amax);
       if (S.sums_exact) {
-        j = (uint32_t)nearest4_by64(v, S.c, S.E, S.mn, S.mx, S.lin, S.sumc, S.cntc);
+        if (!have64) {   // the four fp64 centroids as centroid64 forms them, at once (independent divisions)
+          const double h = ((double)S.mx - (double)S.mn) / 3.0;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            c64[jj] = S.lin[jj] ? (jj == 0 ? (double)S.mn : jj == 1 ? (double)S.mn + h : jj == 2 ? (double)S.mn + 2.0 * h
+                                                                                         : (double)S.mx)
+                                : (double)S.sumc[jj] / (double)S.cntc[jj];
+          have64 = true;
+        }
+        // the fp64 nearest (lowest index on ties) among the centroids whose
+        // binary32 distance is within 2E of the binary32 best: the others are
+        // farther in fp64 as well (each distance is within E / 2 of its fp64 value)
+        float bd = INFINITY;
+        for (int jj = 0; jj < 4; ++jj) bd = fminf(bd, fabsf(v - S.c[jj]));
+        int best = -1;
+        double b64 = 0.0;
+        for (int jj = 0; jj < 4; ++jj) {
+          if (fabsf(v - S.c[jj]) > bd + 2.f * S.E) continue;
+          const double d = fabs((double)v - c64[jj]);
+          if (best < 0 || d < b64) { b64 = d; best = jj; }
+        }
+        j = (uint32_t)best;
       } else {   // inexact sums: the candidates' fp64 means from their cells
         const int jc = nearest4_by_cells64<NROWS>(v, S, x, xs, keep, prev, lastf);
         if (jc >= 0) j = (uint32_t)jc;
