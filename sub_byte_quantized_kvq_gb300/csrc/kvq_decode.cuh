@@ -22,15 +22,17 @@
 //    mbarrier), one copy per block: for the page formats one K stage (refilled
 //    as soon as the iteration's scores are done) and one V stage (a V block is
 //    read only after the K phase and the softmax of its iteration); E2M1 two
-//    and two, INT4 three and two single pages; no register staging, no TMA
-//    multicast.
+//    and two (three pages per iteration), INT4 three and two single pages; no
+//    register staging, no TMA multicast.
 //  * QK^T: A = K (16 tokens x 16 channels, built in registers from the codes),
 //    B = Q^T (16 channels x 8 heads, fp16, loaded once).  PV: A = V^T (16
 //    channels x 16 tokens, built in registers), B = P^T (fp16 hi + lo split of
 //    the fp32 probabilities, so P carries ~22 bits).  mma.sync m16n8k16 with
 //    fp32 accumulation; the layouts in include/kvq.h make every A register one
 //    or two byte-permutes of shared-memory words.  The PPI pages of an
-//    iteration are independent mma chains the scheduler interleaves.
+//    iteration are independent mma chains the scheduler interleaves.  For
+//    CB2 at G <= 4 the same products can run as fp32 FMAs instead
+//    (iter_cb2_cc, kvq_config.decode_math; measured slower).
 //  * CB2 outliers: a code slot holding an outlier stores code 0 (value c0).
 //    The side-list's channel records go six at a time into one mma tile; the
 //    correction x - c0 is applied as two mma with exact fp16 operands (+ the
