@@ -333,6 +333,16 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t
 /* Static, NUL-terminated description of a status code. */
 const char* kvq_status_string(kvq_status status);
 
+/* The CUDA runtime error code (a cudaError_t value) behind the most recent
+ * KVQ_ERR_CUDA returned on the calling thread, or 0 if this thread has seen
+ * none.  A later successful call does not clear it.  Host only, no GPU needed. */
+int32_t kvq_last_cuda_error(void);
+
+/* Static, NUL-terminated name of a CUDA runtime error code (as returned by
+ * kvq_last_cuda_error), e.g. "cudaErrorInvalidValue"; the runtime's
+ * "unrecognized error code" for values it does not know. */
+const char* kvq_cuda_error_name(int32_t error);
+
 /* Library version, "MAJOR.MINOR.PATCH". */
 const char* kvq_version(void);
 

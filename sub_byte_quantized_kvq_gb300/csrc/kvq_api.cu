@@ -5,6 +5,13 @@
 #include "kvq_project.cuh"
 
 namespace kvq {
+// The CUDA runtime's error behind the last KVQ_ERR_CUDA this thread saw.
+thread_local int g_last_cuda_error = 0;
+kvq_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KVQ_OK;
+  g_last_cuda_error = (int)e;
+  return KVQ_ERR_CUDA;
+}
 
 // ----------------------------------------------------------------------------- debug dequantization
 // One thread per (token, channel) of the requested range; values are exactly
@@ -313,8 +320,7 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
   a.kv[0] = k_new;
   a.kv[1] = v_new;
   a.in_dtype = in_dtype;
-  if (append_launch(a, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(append_launch(a, cfg->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -337,8 +343,7 @@ kvq_status kvq_project_append(const kvq_config* cfg, const kvq_cache* cache, con
   p.w[1] = static_cast<const __nv_bfloat16*>(w_v);
   p.hidden = hidden;
   p.kv_out = kv_out;
-  if (project_append_launch(p, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(project_append_launch(p, cfg->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_decode_num_splits(const kvq_config* cfg, int32_t num_q_heads, int32_t max_seq_len,
@@ -425,9 +430,7 @@ kvq_status kvq_decode_split(const kvq_config* cfg, const kvq_cache* cache, const
   kvq_status st = decode_prepare(cfg, cache, q, num_q_heads, softmax_scale, max_seq_len, num_splits, workspace,
                                  workspace_bytes, a);
   if (st != KVQ_OK) return st;
-  if (decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_t max_seq_len, int32_t num_splits,
@@ -447,10 +450,8 @@ kvq_status kvq_decode_combine(const kvq_config* cfg, int32_t num_q_heads, int32_
   const float* part_o = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + partials_offset(cfg));
   const float2* part_ml = reinterpret_cast<const float2*>(part_o + (size_t)cfg->num_seqs * num_q_heads * S * cfg->head_dim);
   if (S > kMaxSplits) return KVQ_ERR_CAPACITY;
-  if (decode_combine_launch(part_o, part_ml, cfg->num_seqs, cfg->num_kv_heads, num_q_heads, S, cfg->head_dim, out,
-                            out_dtype, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(decode_combine_launch(part_o, part_ml, cfg->num_seqs, cfg->num_kv_heads, num_q_heads, S,
+                                           cfg->head_dim, out, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t num_q_heads,
@@ -463,9 +464,7 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
   if (st != KVQ_OK) return st;
   a.out = out;   // one launch: the split kernel's last CTA per (sequence, kv head) merges the splits
   a.out_dtype = out_dtype;
-  if (decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(decode_split_launch(a, cfg->format, cfg->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -482,9 +481,9 @@ kvq_status decode_attention_zeroing_counters(const kvq_config* cfg, const kvq_ca
   if (s != KVQ_OK) return s;
   a.out = out;
   a.out_dtype = out_dtype;
-  if (cudaMemsetAsync(a.arrivals, 0, (size_t)a.B * a.Hkv * sizeof(uint32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
-  if (decode_split_launch(a, cfg->format, cfg->head_dim, st) != cudaSuccess) return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  const kvq_status zs = cuda_status(cudaMemsetAsync(a.arrivals, 0, (size_t)a.B * a.Hkv * sizeof(uint32_t), st));
+  if (zs != KVQ_OK) return zs;
+  return cuda_status(decode_split_launch(a, cfg->format, cfg->head_dim, st));
 }
 }  // namespace kvq
 
@@ -495,10 +494,8 @@ kvq_status kvq_select_static_channels(const kvq_config* cfg, const void* k, cons
   if (!cfg_ok(cfg) || cfg->format != KVQ_FMT_CB2_STATIC || !k || !v || !mask || t < 1) return KVQ_ERR_INVALID_ARG;
   if (in_dtype != KVQ_BF16 && in_dtype != KVQ_F16 && in_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
   if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
-  if (select_static_launch(k, v, in_dtype, t, cfg->num_kv_heads, cfg->head_dim, cfg->static_channels, mask,
-                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(select_static_launch(k, v, in_dtype, t, cfg->num_kv_heads, cfg->head_dim, cfg->static_channels,
+                                          mask, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t seq, int32_t kv_head, int32_t which,
@@ -509,11 +506,13 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t
   if (tok_begin < 0 || tok_end < tok_begin || (long long)tok_end > (long long)cfg->pages_per_seq_max * kPage)
     return KVQ_ERR_INVALID_ARG;
   if (!dim_supported(cfg)) return KVQ_ERR_UNSUPPORTED;
-  if (dequantize_launch(*cfg, *cache, seq, kv_head, which, tok_begin, tok_end, out,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return cuda_status(dequantize_launch(*cfg, *cache, seq, kv_head, which, tok_begin, tok_end, out,
+                                       static_cast<cudaStream_t>(stream)));
 }
+
+int32_t kvq_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* kvq_cuda_error_name(int32_t error) { return cudaGetErrorName(static_cast<cudaError_t>(error)); }
 
 const char* kvq_status_string(kvq_status s) {
   switch (s) {

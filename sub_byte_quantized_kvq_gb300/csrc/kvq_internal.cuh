@@ -64,6 +64,9 @@ cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st);
 
 cudaError_t select_static_launch(const void* k, const void* v, int in_dtype, int t, int Hkv, int D, int n_s,
                                  uint8_t* mask, cudaStream_t st);
+// KVQ_OK for cudaSuccess; otherwise records e for kvq_last_cuda_error and
+// returns KVQ_ERR_CUDA.
+kvq_status cuda_status(cudaError_t e);
 // kvq_decode_attention after clearing the call's arrival counters with a
 // memset on `st` (validation first: an argument error enqueues nothing).
 kvq_status decode_attention_zeroing_counters(const kvq_config* cfg, const kvq_cache* cache, const void* q,

@@ -27,15 +27,26 @@ void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch,
 
 // Device address of the scratch on the current device, looked up once per
 // device ordinal (with that device current) and cached for the life of the
-// process; nullptr if the lookup fails.  The cache is keyed by ordinal, so the
-// entry point must not be used on a device after cudaDeviceReset on it.
-void* scratch_on_current_device() {
+// process; nullptr if the lookup fails (the runtime's error in *err).  The
+// cache is keyed by ordinal, so the entry point must not be used on a device
+// after cudaDeviceReset on it.
+void* scratch_on_current_device(cudaError_t* err) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    if (p == nullptr) {
+      *err = cudaErrorInvalidSymbol;
+      return nullptr;
+    }
     g_scratch_addr[dev] = p;
   }
   return g_scratch_addr[dev];
@@ -50,8 +61,9 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const kvq_status st = kvq_decode_workspace_bytes(cfg, num_q_heads, max_seq_len, num_splits, &need);
   if (st != KVQ_OK) return st;
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // before anything is enqueued
-  void* scratch = scratch_on_current_device();
-  if (!scratch) return KVQ_ERR_CUDA;
+  cudaError_t err = cudaSuccess;
+  void* scratch = scratch_on_current_device(&err);
+  if (!scratch) return kvq::cuda_status(err);
   // The scratch is shared by every cache in the process: the arrival counters
   // sit at its start, B * Hkv of them, so a call on a cache with more
   // (sequence, kv head) pairs than the last one's would find that call's

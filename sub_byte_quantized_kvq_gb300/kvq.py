@@ -30,6 +30,8 @@ class KVQError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
         msg = kvq_status_string(status) if _lib is not None else str(status)
+        if status == KVQ_ERR_CUDA and _lib is not None:   # the runtime's own error name
+            msg += f" {_lib.kvq_cuda_error_name(_lib.kvq_last_cuda_error()).decode()}"
         super().__init__(f"{what}: {msg} (status {status})" if what else msg)
 
 
@@ -53,7 +55,7 @@ EXPORTS = ("kvq_block_bytes", "kvq_cache_bytes", "kvq_quantize_append", "kvq_pro
            "kvq_decode_workspace_bytes",
            "kvq_decode_num_splits", "kvq_decode_split", "kvq_decode_combine", "kvq_decode_attention",
            "kvq_decode_attention_noalloc", "kvq_select_static_channels", "kvq_dequantize", "kvq_status_string",
-           "kvq_version")
+           "kvq_last_cuda_error", "kvq_cuda_error_name", "kvq_version")
 
 
 def lib() -> ctypes.CDLL:
@@ -80,6 +82,8 @@ def lib() -> ctypes.CDLL:
                 "kvq_select_static_channels": (I, [pcfg, P, P, I, I, P, P]),
                 "kvq_dequantize": (I, [pcfg, pcache, I, I, I, I, I, P, P]),
                 "kvq_status_string": (ctypes.c_char_p, [I]),
+                "kvq_last_cuda_error": (I, []),
+                "kvq_cuda_error_name": (ctypes.c_char_p, [I]),
                 "kvq_version": (ctypes.c_char_p, []),
             }
             for name, (res, args) in sig.items():

@@ -118,3 +118,19 @@ def test_status_strings_and_version(kvq):
         assert kvq.kvq_status_string(s)
     assert kvq.kvq_status_string(99) == "unknown status"
     assert re.fullmatch(r"\d+\.\d+\.\d+", kvq.kvq_version())
+
+
+def test_cuda_error_accessors(kvq):
+    """kvq_last_cuda_error is per thread (0 on a thread that has seen no
+    KVQ_ERR_CUDA) and kvq_cuda_error_name maps runtime codes to their names;
+    neither needs a GPU."""
+    import threading
+    L = kvq.lib()
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(L.kvq_last_cuda_error()))
+    t.start()
+    t.join()
+    assert seen == [0]
+    assert L.kvq_cuda_error_name(0).decode() == "cudaSuccess"
+    assert L.kvq_cuda_error_name(1).decode() == "cudaErrorInvalidValue"
+    assert L.kvq_cuda_error_name(2).decode() == "cudaErrorMemoryAllocation"
