@@ -1707,18 +1707,24 @@ cudaError_t append_launch(const AppendArgs& a, int D, cudaStream_t st) {
 // write in one kernel).
 //
 // One CTA (512 threads) per (kv head, tile of 128 sequence positions,
-// sequence) computes K and V together (N = 2 D accumulator columns).  The kv
-// heads are the grid's fastest dimension, so the CTAs that read the same x
-// rows run at about the same time and all but the first find them in L2
-// (measured 2-5% faster than tiles first).  Tile
+// sequence) computes K and V together (N = 2 D accumulator columns).  Two
+// CTAs holding neighbouring tiles of the same kv head form a cluster and share
+// each MMA (tcgen05.mma.cta_group::2, M = 256): each stages its own x rows but
+// only one of the two weight matrices, so a stage is 32 KB instead of 48 and
+// three fit where two did (the pair's mainloop measured 1.2x the single CTA's
+// rate).  The kv heads are the grid's fastest dimension, so the CTAs that read
+// the same x rows run at about the same time and all but the first find them
+// in L2 (measured 2-5% faster than tiles first).  Tile
 // rows are whole pages (4-page groups for the CB2 group format), so each block
 // is written by one CTA.  Warp 0 streams the operands with TMA (one 2-D box
 // per unit of x rows, one per weight matrix; 128-byte swizzle, 64 hidden
-// columns per stage) into a ring of shared-memory stages; warp 1 issues the
-// MMAs of each stage and commits it back to the producer; the other warps
-// sleep on the accumulator's mbarrier.  The epilogue reads the accumulators
-// with tcgen05.ld into an fp32 tile in shared memory and runs the same
-// per-token / per-page / per-group quantizers as kvq_quantize_append.
+// columns per stage) into a ring of shared-memory stages; warp 1 (of the
+// pair's even CTA) issues the MMAs of each stage and commits it back to both
+// producers; the other warps sleep on the accumulator's mbarrier.  The
+// epilogue reads each CTA's own accumulators with tcgen05.ld into an fp32 tile
+// in shared memory and runs the same per-token / per-page / per-group
+// quantizers as kvq_quantize_append.  Where a cluster launch is refused, one
+// CTA per tile does the same work alone (M = 128, both weight matrices).
 namespace tc {
 // Shared-memory matrix descriptor, K-major with 128-byte swizzle: rows of
 // 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), leading byte
@@ -1738,6 +1744,37 @@ __device__ __forceinline__ void mma(uint32_t tmem, uint64_t ad, uint64_t bd, uin
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+// CTA pairs (cta_group::2): an M = 256 MMA issued by the pair's even CTA reads
+// A rows 0..127 and B rows 0..N/2-1 from its own shared memory and A rows
+// 128..255, B rows N/2..N-1 from the odd CTA's, at the same offsets; D rows
+// 0..127 land in the even CTA's tensor memory, 128..255 in the odd CTA's.
+__device__ __forceinline__ void mma_pair(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accumulate) {
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem),
+               "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate));
+}
+// Arrives on the mbarrier at `bar`'s offset in both CTAs of the pair once the
+// issuing thread's earlier MMAs are complete.
+__device__ __forceinline__ void commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((unsigned short)3)
+      : "memory");
+}
+// Shared-memory address of the same location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -1765,16 +1802,27 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// The same into this CTA's shared memory, completing on the mbarrier at
+// cluster address `bar` (the pair's even CTA's).
+__device__ __forceinline__ void tma2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 }  // namespace tc
 
 // Fused projection plan: a tile is kPM rows (sequence positions, whole units
 // of U rows: pages, or 4-page groups for the CB2 group format) x N = 2 D
 // columns (K then V of one kv head) in TMEM; the hidden dimension streams
-// through S stages of kPK columns (A: kPM rows, B: N rows, 128 bytes each).
+// through S stages of kPK columns (A: kPM rows, B: N / CG rows, 128 bytes
+// each).  CG = 2: two CTAs of a cluster share each MMA (M = 256, the two
+// tiles' rows), and each stages one of the two weight matrices.
 enum { kProjInt4 = 0, kProjE2m1 = 1, kProjPage = 2, kProjGroup = 3 };
 constexpr int kPM = 128, kPK = 64, kPThreads = 512;
 
-template <int KIND, int D>
+template <int KIND, int D, int CG = 1>
 struct ProjPlan {
   static constexpr int U = KIND == kProjGroup ? kPage * kGroupPages : kPage;  // rows of one unit
   static constexpr int SPT = kPM / U;                                         // units per tile
@@ -1782,8 +1830,8 @@ struct ProjPlan {
   static constexpr int GS = kPThreads / NB;                                   // threads per unit group
   static constexpr int N = 2 * D;                                             // TMEM columns: K | V
   static constexpr int XS = D + 4;  // row stride of the fp32 tile: rows start 4 banks apart
-  static constexpr int S = D == 128 ? 2 : 3;                                  // operand stages
-  static constexpr int A_BYTES = kPM * kPK * 2, B_BYTES = N * kPK * 2, STAGE = A_BYTES + B_BYTES;
+  static constexpr int S = CG == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 2 : 3);   // operand stages
+  static constexpr int A_BYTES = kPM * kPK * 2, B_BYTES = N / CG * kPK * 2, STAGE = A_BYTES + B_BYTES;
   // a unit group's scratch: the block (per-token formats); the block, mask and
   // codes, and per-warp partials (pages); the 4 blocks and 2-bit codes (groups)
   static constexpr int WS = KIND == kProjInt4   ? block_stride(kBlkInt4, D)
@@ -1798,7 +1846,8 @@ struct ProjPlan {
 
 #define KVQ_PLAN_FITS(K, D_)                                                                          \
   static_assert(ProjPlan<K, D_>::SMEM <= 227 * 1024 && ProjPlan<K, D_>::N <= 256 &&                     \
-                    ProjPlan<K, D_>::STAGE % 1024 == 0 && ProjPlan<K, D_>::A_BYTES % 1024 == 0,        \
+                    ProjPlan<K, D_>::STAGE % 1024 == 0 && ProjPlan<K, D_>::A_BYTES % 1024 == 0 &&      \
+                    ProjPlan<K, D_, 2>::SMEM <= 113 * 1024 && ProjPlan<K, D_, 2>::STAGE % 1024 == 0,   \
                 "fused projection plan does not fit")
 KVQ_PLAN_FITS(kProjInt4, 64);
 KVQ_PLAN_FITS(kProjInt4, 128);
@@ -1813,28 +1862,38 @@ KVQ_PLAN_FITS(kProjGroup, 128);
 // Two CTAs per SM (64 registers a thread, a few spilled): one CTA's
 // quantization epilogue then runs beside the other's MMAs; one CTA per SM
 // measured 1.1-1.7x slower on every format.
-template <int KIND, int D>
+template <int KIND, int D, int CG>
 __global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __grid_constant__ ProjArgs p) {
-  using P = ProjPlan<KIND, D>;
+  using P = ProjPlan<KIND, D, CG>;
   constexpr int U = P::U, SPT = P::SPT, NB = P::NB, GS = P::GS, N = P::N, XS = P::XS, S = P::S;
   extern __shared__ __align__(1024) uint8_t psm_raw[];
   const AppendArgs& a = p.a;
-  const int h = blockIdx.x, tile = blockIdx.y, b = blockIdx.z;
+  // grid (Hkv, tiles, B); pairs: (2 Hkv, tile pairs, B) in clusters of two
+  // along x, the cluster's CTAs holding tiles 2y and 2y + 1 of kv head x / 2
+  const int h = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tile = CG == 2 ? 2 * (int)blockIdx.y + (int)(blockIdx.x & 1) : (int)blockIdx.y;
+  const int b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int start, n;
   if (seq_append_state(a, b, start, n) != kSeqOk) return;
   const int end = start + n, first = start / U, last = (end - 1) / U, nu = last - first + 1;
   const int32_t* pt = a.page_table + (size_t)b * a.ppsm;
-  // Unit in slot s of this tile, or -1.  Tile 0 holds both the first unit
+  // Unit in slot s of tile t, or -1.  Tile 0 holds both the first unit
   // (which reads the staged rows) and the last (which writes them), so no
   // other CTA touches this sequence's staging.
-  auto unit_of = [&](int s) -> int {
-    if (nu <= SPT) return tile == 0 && s < nu ? first + s : -1;
-    if (tile == 0) return s < SPT - 1 ? first + s : last;
-    const int u = first + (SPT - 1) + SPT * (tile - 1) + s;
+  auto unit_at = [&](int t, int s) -> int {
+    if (nu <= SPT) return t == 0 && s < nu ? first + s : -1;
+    if (t == 0) return s < SPT - 1 ? first + s : last;
+    const int u = first + (SPT - 1) + SPT * (t - 1) + s;
     return u < last ? u : -1;
   };
-  if (unit_of(0) < 0) return;
+  auto unit_of = [&](int s) { return unit_at(tile, s); };
+  // CTA pairs: cluster rank = tile & 1; a CTA without units still stages its
+  // weight half for its partner
+  const uint32_t rank = CG == 2 ? tc::cluster_rank() : 0u;
+  const int peer_tile = tile ^ 1;
+  const bool active = unit_of(0) >= 0;
+  if (!active && (CG == 1 || unit_at(peer_tile, 0) < 0)) return;   // both CTAs of a pair leave together
 
   // 1024-byte aligned base: the swizzled stages need it
   uint8_t* psm = psm_raw + (((smem_u32(psm_raw) + 1023u) & ~1023u) - smem_u32(psm_raw));
@@ -1860,12 +1919,19 @@ __global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __gr
     fence_mbar_init();
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(N)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 2) {   // one warp of each CTA of the pair, together
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(N)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(N)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc::fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) tc::cluster_sync();   // the partner's barriers are initialised before any copy
+  else __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const int nk = (p.hidden + kPK - 1) / kPK;
@@ -1875,23 +1941,53 @@ __global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __gr
     // producer: stage kc = the x rows of every unit of the tile (one box per
     // unit; rows of other sequences or past the end are never used) and the
     // K | V weight rows of head h, hidden columns [kPK kc, kPK kc + kPK)
-    int nvalid = 0;
-    for (int s = 0; s < SPT; ++s) nvalid += unit_of(s) >= 0;
-    const uint32_t bytes = (uint32_t)(nvalid * U * kPK * 2 + P::B_BYTES);
+    int nvalid = 0, nvalid_peer = 0;
+    for (int s = 0; s < SPT; ++s) {
+      nvalid += unit_of(s) >= 0;
+      nvalid_peer += CG == 2 && unit_at(peer_tile, s) >= 0;
+    }
+    // pairs: the even CTA's barrier counts the bytes of both CTAs' copies
+    const uint32_t bytes = CG == 2 ? (uint32_t)((nvalid + nvalid_peer) * U * kPK * 2 + 2 * P::B_BYTES)
+                                   : (uint32_t)(nvalid * U * kPK * 2 + P::B_BYTES);
     for (int kc = 0; kc < nk && ok; ++kc) {
       const int s = kc % S;
       if (kc >= S && !mbar_wait_bounded(&empty[s], (kc / S - 1) & 1, kWaitLimitNs)) ok = false;
       if (!ok) break;
       uint8_t* st = psm + s * P::STAGE;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      for (int sl = 0; sl < SPT; ++sl) {
-        const int u = unit_of(sl);
-        if (u >= 0) tc::tma2d(st + sl * U * kPK * 2, &p.tm_x, kPK * kc, b * a.t_new + (u * U - start), &full[s]);
+      if constexpr (CG == 2) {
+        const uint32_t fb = tc::map_rank(&full[s], 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
+        for (int sl = 0; sl < SPT; ++sl) {
+          const int u = unit_of(sl);
+          if (u >= 0) tc::tma2d_pair(st + sl * U * kPK * 2, &p.tm_x, kPK * kc, b * a.t_new + (u * U - start), fb);
+        }
+        tc::tma2d_pair(st + P::A_BYTES, &p.tm_w[rank], kPK * kc, h * D, fb);
+      } else {
+        mbar_arrive_expect_tx(&full[s], bytes);
+        for (int sl = 0; sl < SPT; ++sl) {
+          const int u = unit_of(sl);
+          if (u >= 0) tc::tma2d(st + sl * U * kPK * 2, &p.tm_x, kPK * kc, b * a.t_new + (u * U - start), &full[s]);
+        }
+        tc::tma2d(st + P::A_BYTES, &p.tm_w[0], kPK * kc, h * D, &full[s]);
+        tc::tma2d(st + P::A_BYTES + D * kPK * 2, &p.tm_w[1], kPK * kc, h * D, &full[s]);
       }
-      tc::tma2d(st + P::A_BYTES, &p.tm_w[0], kPK * kc, h * D, &full[s]);
-      tc::tma2d(st + P::A_BYTES + D * kPK * 2, &p.tm_w[1], kPK * kc, h * D, &full[s]);
     }
-  } else if (tid == 32) {
+  } else if (tid == 32 && CG == 2 && rank == 0) {
+    // MMA issuer of the pair: M = 256 over both CTAs' stages, each stage
+    // handed back to both producers on completion
+    const uint32_t idesc = tc::idesc_bf16(2 * kPM, N);
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      const int s = kc % S;
+      if (!mbar_wait_bounded(&full[s], (kc / S) & 1, kWaitLimitNs)) { ok = false; break; }
+      tc::fence_after();
+      const uint32_t sa = smem_u32(psm + s * P::STAGE), sb = sa + P::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < kPK / 16; ++kk)
+        tc::mma_pair(tmem, tc::desc_sw128(sa + 32 * kk), tc::desc_sw128(sb + 32 * kk), idesc, (kc | kk) != 0);
+      tc::commit_pair(&empty[s]);
+    }
+    tc::commit_pair(done);
+  } else if (tid == 32 && CG == 1) {
     // MMA issuer: kPK / 16 MMAs per stage, the stage handed back on completion
     const uint32_t idesc = tc::idesc_bf16(kPM, N);
     for (int kc = 0; kc < nk && ok; ++kc) {
@@ -1916,7 +2012,7 @@ __global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __gr
   }
   const bool all_ok = __syncthreads_and(ok) != 0;
   tc::fence_after();
-  if (all_ok) {
+  if (all_ok && active) {
     const int grp = warp / (GS / 32);
     const Grp g{tid % GS, GS, 1 + grp};
     uint8_t* gws = ws + grp * P::WSR;
@@ -1983,12 +2079,17 @@ __global__ void __launch_bounds__(kPThreads, 2) project_append_kernel(const __gr
       }
       __syncthreads();
     }
-  } else if (tid == 0) {
+  } else if (tid == 0 && !all_ok) {
     atomicOr(a.status, KVQ_STATUS_TIMEOUT);
   }
   tc::fence_before();
-  __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
+  if constexpr (CG == 2) {   // both CTAs are done with their tensor memory and the partner's stages
+    tc::cluster_sync();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
+  } else {
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
+  }
   if (tid == 0 && all_ok) {   // after a timeout a late arrival may still be pending: leave them
     for (int s = 0; s < S; ++s) {
       mbar_inval(&full[s]);
@@ -2365,12 +2466,43 @@ static cudaError_t project_launch_k(ProjArgs& p, cudaStream_t st) {
       !encode_rows(&p.tm_w[0], p.w[0], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D) ||
       !encode_rows(&p.tm_w[1], p.w[1], (uint64_t)p.a.Hkv * D, (uint64_t)p.hidden, (uint32_t)D))
     return cudaErrorInvalidValue;
-  const cudaError_t e =
-      cudaFuncSetAttribute(project_append_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
-  if (e != cudaSuccess) return e;
   const int units_max = (p.a.t_new + 2 * P::U - 2) / P::U;   // units a span of t_new positions can touch
-  const dim3 grid(p.a.Hkv, (units_max + P::SPT - 1) / P::SPT, p.a.B);
-  project_append_kernel<KIND, D><<<grid, kPThreads, P::SMEM, st>>>(p);
+  const int tiles = (units_max + P::SPT - 1) / P::SPT;
+  // CTA pairs first (clusters of two CTAs, one tile each, sharing each MMA);
+  // if the pair kernel cannot launch, the one-CTA kernel
+  {
+    using P2 = ProjPlan<KIND, D, 2>;
+    auto kern = project_append_kernel<KIND, D, 2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P2::SMEM);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2u * (unsigned)p.a.Hkv, (unsigned)((tiles + 1) / 2), (unsigned)p.a.B);
+      cfg.blockDim = dim3(kPThreads);
+      cfg.dynamicSmemBytes = P2::SMEM;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int nclusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
+      if (e == cudaSuccess && nclusters >= 1) {
+        e = cudaLaunchKernelEx(&cfg, kern, p);
+        if (e != cudaSuccess) return e;
+        append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
+        return cudaGetLastError();
+      }
+    }
+    (void)cudaGetLastError();
+  }
+  const cudaError_t e =
+      cudaFuncSetAttribute(project_append_kernel<KIND, D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.a.Hkv, tiles, p.a.B);
+  project_append_kernel<KIND, D, 1><<<grid, kPThreads, P::SMEM, st>>>(p);
   append_finish_kernel<<<p.a.B, 128, 0, st>>>(p.a);
   return cudaGetLastError();
 }
