@@ -759,6 +759,11 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
         }
+        const float sk = ldsf(kb_s[p] + fp8_sc_off(D));   // the tier page's scale
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
       } else {
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
@@ -785,16 +790,6 @@ __device__ __forceinline__ void iter_cb2(WarpState<D, NT>& st, const uint32_t (&
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(acc[p][nt], ak[0], ak[1], ak[2], ak[3], qf[nt][s][0], qf[nt][s][1]);
       }
-    }
-  }
-  if constexpr (T) {
-#pragma unroll
-    for (int p = 0; p < PPI; ++p) {
-      const float sk = tier[p] ? ldsf(kb_s[p] + fp8_sc_off(D)) : 1.f;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[p][nt][r] *= sk;
     }
   }
   if constexpr (FMT == KVQ_FMT_CB2_STATIC) {
