@@ -28,6 +28,7 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -179,10 +180,22 @@ def algorithmic_bytes(built: workloads.Built) -> dict:
     return step_bytes(w.fmt, w.D, w.Hkv, w.Hq, w.B, w.N, built.page_table, meta, w.static_channels)
 
 
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(text: str) -> str:
+    """C++ source with comments removed and white space collapsed (string
+    literals, such as inline PTX, kept)."""
+    code = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(code.split())
+
+
 def kernel_source_sha() -> str:
+    """Hash of the decode kernel's code: a comment or layout edit leaves the
+    stored traffic record valid, any code change invalidates it."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "sub_byte_quantized_kvq_gb300", "csrc", f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, "sub_byte_quantized_kvq_gb300", "csrc", f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -30,7 +30,9 @@
 //    the fp32 probabilities, so P carries ~22 bits).  mma.sync m16n8k16 with
 //    fp32 accumulation; the layouts in include/kvq.h make every A register one
 //    or two byte-permutes of shared-memory words.  The PPI pages of an
-//    iteration are independent mma chains the scheduler interleaves.  For
+//    iteration are independent mma chains the scheduler interleaves; the
+//    tiered format instead branches on each page's tier once, around all of
+//    its steps, so that every page's steps still schedule as one block.  For
 //    CB2 at G <= 4 the same products can run as fp32 FMAs instead
 //    (iter_cb2_cc, kvq_config.decode_math; measured slower).
 //  * CB2 outliers: a code slot holding an outlier stores code 0 (value c0).

@@ -12,6 +12,8 @@
    ties to the lower page index ("Hierarchical Token Gating and Tiered
    KV-Cache Paging", 2. Entropy-Guided Tiered KV-Cache Quantization: the pages
    carrying the largest cumulative attention weight go to the FP8 tier).
+3. The source hash that keys the stored DRAM traffic record ignores comments
+   and layout but not code (a stale record reads as traffic null).
 """
 import math
 
@@ -143,3 +145,11 @@ def test_tier_pages_ties_go_to_the_lower_page():
     # s = 0: every position weighs 1, so all full pages tie and the last (partial) page is lightest
     got = synth.tier_pages(0, 1, 16 * 20 + 3, 0.10, 0.0)
     assert np.nonzero(got[0])[0].tolist() == [0, 1, 2]
+
+
+
+def test_source_hash_ignores_comments_not_code():
+    base = 'asm("mov.u32 %0, %%globaltimer; // kept");\nconstexpr float kTh = 8.0f;\n'
+    assert bench.code_only(base) == bench.code_only("// a note\n" + base.replace(";\n", ";   /* x\n y */\n\n"))
+    assert "// kept" in bench.code_only(base)                      # string literals are code
+    assert bench.code_only(base) != bench.code_only(base.replace("8.0f", "7.0f"))
